@@ -1,0 +1,54 @@
+/*
+ * sarbp_oracle.h - plain FP64 CPU time-domain SAR backprojector.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load or call this code; the product path
+ * (libsarbp) never does, and shares no code, header or constant with it.
+ *
+ * Source of the method (SARBP-GPU = the page "基于GPU的SAR后向投影成像优化与CUDA加速实践"):
+ *   SARBP-GPU §1.1  every pixel sums, over all pulses, the echo found at its
+ *                    range history after phase compensation;
+ *   SARBP-GPU §1.2  the loop is O(Na * Nx * Ny);
+ *   SARBP-GPU §2.2  steps: pixel coordinates, slant range per pulse, linear
+ *                    interpolation of the range-compressed echo, phase
+ *                    compensation, accumulation;
+ *   SARBP-GPU §3.3  kernel pseudo-code: uniform range axis (first sample and
+ *                    spacing), floor/fraction interpolation, phase 4*pi*R/lambda
+ *                    applied as exp(+j*phase), planar real/imaginary output,
+ *                    monostatic geometry.
+ */
+#ifndef SARBP_ORACLE_H
+#define SARBP_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int64_t nx, ny;        /* image width (x) and height (y), pixels              */
+    int64_t na, nr;        /* pulses, range bins                                  */
+    double x0, y0, z0;     /* position of pixel (0, 0)                            */
+    double dx, dy;         /* pixel spacing; pixel (ix, iy) = (x0+ix*dx, y0+iy*dy, z0) */
+    double r0, dr;         /* range of bin k = r0 + k * dr                        */
+    double wavelength;     /* carrier wavelength                                  */
+} oracle_geometry;
+
+/*
+ * Backproject the pixels listed in `pixels` (linear index iy * nx + ix).
+ *   echo        complex64 as interleaved float pairs, [na][nr][2], pulse-major
+ *   antenna_pos float64 [na][3], antenna phase centre of each pulse (x, y, z)
+ *   out         float64 [npix][2], complex128 result per listed pixel
+ *   nthreads    worker threads; <= 0 means all online CPUs
+ * Returns the number of threads used, or -1 on a bad argument.
+ */
+int oracle_backproject(const oracle_geometry* g, const float* echo,
+                       const double* antenna_pos, const int64_t* pixels,
+                       int64_t npix, double* out, int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SARBP_ORACLE_H */
