@@ -1,0 +1,346 @@
+"""Benchmark: giga pixel-pulse backprojections per second on GB300.
+
+One step is one full backprojection of the page-sized airborne spotlight
+scene (Na = 4096 pulses, Nr = 4096 range bins, 1024 x 1024 image at 0.15 m;
+SARBP-GPU §1.2 and §3.3 of the page "基于GPU的SAR后向投影成像优化与CUDA加速实践"):
+the echo table build, the main backprojection kernel and the partial-sum
+reduction, all through the C-ABI call sarbp_backproject.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) each rank backprojects its
+own, independently seeded frame on its own GPU; there is no data exchange.
+The reported value is all ranks' updates divided by the slowest rank's time.
+``--impl reference`` times the FP64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "giga pixel-pulse backprojections/sec on 1 GB300; % of SFU/FP32 roofline"
+UNIT = "Gupd/s"
+WORKLOAD = ("page-sized airborne spotlight: Na=4096 pulses, Nr=4096 complex64 bins, "
+            "1024x1024 image at 0.15 m, 64 point targets + clutter sigma=0.1")
+# SARBP-GPU §3.3: about 0.8 s per frame on an RTX 3080 for Na = 4096 and a
+# 1024 x 1024 image (4096 * 1024 * 1024 updates, §1.2) -> 5.37 Gupd/s.
+PAGE_GUPD = 4096 * 1024 * 1024 / 0.8 / 1e9
+MUFU_PER_SM_CLK = 16          # sine/cosine lanes per SM per clock
+MUFU_PER_UPDATE = 2           # sin and cos of the phase; the range needs no sqrt here
+PAGE_SFU_PER_UPDATE = 3       # the page's loop: sqrt, sin, cos
+SM_MAX_MHZ_FALLBACK = 2070.0
+L2_FLUSH_BYTES = 256 << 20
+# dram read+write bytes of one bp_kernel launch, from ncu (None until captured
+# for the current kernel)
+MAIN_KERNEL_TRAFFIC = None
+
+
+# ------------------------------------------------------------------ ranks
+def rank_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(updates_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput in Gupd/s: every rank's updates over the slowest rank's time."""
+    return updates_per_step * steps * world / max_seconds / 1e9
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, stamped in wall time."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm = float(parts[1])
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            active = [n for n, v in zip(self.NAMES, parts[4:]) if v.lower() == "active"]
+            self.samples.append((ts, sm, smax, active))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not inside:
+            inside = self.samples
+            window = "whole run (timed region shorter than the sampling interval)"
+        reasons = sorted({r for s in inside for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_rate(scene, seconds: float = 8.0, threads: int = 0, seed: int = 0):
+    """Oracle Gupd/s on a random pixel sample sized for about ``seconds`` of wall time."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    npx = scene.params["nx"] * scene.params["ny"]
+    probe = rng.choice(npx, size=64, replace=False)
+    _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, probe,
+                                       threads=threads, return_info=True)
+    per_pixel = max(secs, 1e-6) / probe.size
+    count = int(min(npx, max(256, seconds / per_pixel)))
+    pix = rng.choice(npx, size=count, replace=False)
+    _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, pix,
+                                       threads=threads, return_info=True)
+    updates = count * scene.params["na"]
+    return dict(value=updates / secs / 1e9, unit=UNIT, cores=int(used), kind="oracle",
+                sample=f"{count} random pixels x all {scene.params['na']} pulses "
+                       f"({updates:.3e} updates) of the same scene, {secs:.2f} s wall")
+
+
+def run_reference(args, scene):
+    """The oracle as it stands, timed on the host cores, one bounded sample per step."""
+    import oracle
+    rng = np.random.default_rng(7)
+    npx = scene.params["nx"] * scene.params["ny"]
+    calib = oracle_rate(scene, seconds=1.0)
+    per_step_pixels = int(max(64, min(npx, calib["value"] * 1e9 * args.ref_step_seconds
+                                      / scene.params["na"])))
+    pix = rng.choice(npx, size=per_step_pixels, replace=False)
+    for _ in range(args.warmup):
+        oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, pix[:64])
+    total, used = 0.0, 0
+    for _ in range(args.steps):
+        _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, pix,
+                                           return_info=True)
+        total += secs
+    updates = per_step_pixels * scene.params["na"]
+    value = updates * args.steps / total / 1e9
+    sample = (f"{per_step_pixels} random pixels x all {scene.params['na']} pulses per step "
+              f"({updates:.3e} updates)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": value / PAGE_GUPD,
+        "dtype": "f64", "data": "synthetic", "config": config_block(scene, "n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(used), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_block(scene, l2):
+    p = scene.params
+    return {"workload": WORKLOAD, "na": p["na"], "nr": p["nr"], "nx": p["nx"], "ny": p["ny"],
+            "pixel_m": p["dx"], "updates_per_step": p["na"] * p["nx"] * p["ny"], "l2": l2,
+            "seed": scene.cfg.seed}
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_ours(args, scene, rank, world, local, dist):
+    import torch
+
+    from domain_backprojection_sarbp_gb300 import Plan
+    from domain_backprojection_sarbp_gb300 import build as native_build
+
+    native_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = scene.params
+    updates = p["na"] * p["nx"] * p["ny"]
+    echoes = torch.from_numpy(scene.echoes).to(dev)
+    pos = torch.from_numpy(scene.antenna_pos).to(dev)
+    image = torch.empty((p["ny"], p["nx"]), dtype=torch.complex64, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = Plan(p)
+    info = plan.describe()
+    plan.set_timing(True)
+
+    for _ in range(args.warmup):
+        plan.backproject(image, echoes, pos)
+    torch.cuda.synchronize(dev)
+    plan.kernel_times()                                  # drop warm-up launches
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(float(i))                            # evict L2 between steps (untimed)
+        starts[i].record(stream)
+        plan.backproject(image, echoes, pos)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    t1 = time.time()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    main_ms, launches = plan.kernel_times()
+    total_s = sum(step_ms) / 1e3
+    max_s = max_over_ranks(dist, total_s, device=dev)
+    value = aggregate_value(updates, args.steps, world, max_s)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # end to end through the host-buffer entry point: pinned inputs in, image out
+    h_echo = torch.from_numpy(scene.echoes).pin_memory()
+    h_pos = torch.from_numpy(scene.antenna_pos).pin_memory()
+    h_img = torch.empty((p["ny"], p["nx"]), dtype=torch.complex64).pin_memory()
+    for _ in range(max(1, min(args.warmup, 3))):
+        plan.backproject_host(h_img, h_echo, h_pos, stream=stream)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier(dist)
+    te0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        plan.backproject_host(h_img, h_echo, h_pos, stream=stream)
+    te = time.perf_counter() - te0
+    e2e_max = max_over_ranks(dist, te, device=dev)
+    plan.close()
+
+    sms = info["sms"]
+    clock_mhz = SM_MAX_MHZ_FALLBACK
+    if clocks and clocks.get("sm_max_mhz"):
+        clock_mhz = clocks["sm_max_mhz"]
+    peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / MUFU_PER_UPDATE / 1e9
+    page_peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / PAGE_SFU_PER_UPDATE / 1e9
+    achieved = updates / (main_ms / max(launches, 1) / 1e3) / 1e9 if launches else None
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": value / PAGE_GUPD,
+        "dtype": "f32", "data": "synthetic",
+        "config": config_block(scene, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)"),
+        "roofline": {
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
+            "frac": (achieved / peak) if achieved else None, "traffic": MAIN_KERNEL_TRAFFIC,
+            "kernel": "bp_kernel",
+            "peak_basis": f"{sms} SMs x {clock_mhz:.0f} MHz x {MUFU_PER_SM_CLK} MUFU/clk / "
+                          f"{MUFU_PER_UPDATE} MUFU per update",
+            "frac_of_page_loop_roof": (achieved / page_peak) if achieved else None,
+        },
+        "e2e": {"value": aggregate_value(updates, e2e_steps, world, e2e_max), "unit": UNIT,
+                "h2d_bytes_per_step": int(scene.echoes.nbytes + scene.antenna_pos.nbytes),
+                "d2h_bytes_per_step": int(p["nx"] * p["ny"] * 8),
+                "api": "sarbp_backproject_host (pinned host buffers)"},
+        "gpu_launches": args.steps * info["kernels_per_call"],
+        "clocks": clocks,
+        "plan": info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_rate(scene, seconds=args.cpu_seconds)
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="page_spotlight")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from synth import scenes
+    rank, world, local = rank_env()
+    cfg = scenes.config_by_name(args.config)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        oracle.build()
+        scene = scenes.make_scene(cfg)
+        print(json.dumps(run_reference(args, scene)), flush=True)
+        return 0
+
+    import torch
+    dist = init_dist(world, "nccl" if torch.cuda.is_available() else "gloo")
+    # each rank backprojects its own frame: same geometry, its own seed
+    scene = scenes.make_scene(cfg, seed=cfg.seed + 1000 * rank)
+    if rank == 0:
+        import oracle
+        oracle.build()
+    out = run_ours(args, scene, rank, world, local, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,491 @@
+// sarbp_api.cu - host side of libsarbp: argument checks, plans, launches.
+//
+// SARBP-GPU = the page "基于GPU的SAR后向投影成像优化与CUDA加速实践"; the operation
+// and its parameters follow §2.2 and the kernel pseudo-code of §3.3 (range
+// axis given by its first sample and spacing, carrier wavelength, pixel grid
+// origin and spacing, antenna phase centre per pulse). The page has no
+// library interface; this one fixes the sizes in a plan so that every call
+// only enqueues kernels and never allocates.
+#include "../../include/sarbp.h"
+#include "sarbp_internal.h"
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+using namespace sarbp;
+
+struct sarbp_plan_s {
+    sarbp_params p{};
+    int device = -1;
+    int sms = 0, ctas_per_sm = 0;
+    int tiles_x = 0, tiles_y = 0, tiles = 0;
+    int W = 0, full_window = 0;
+    float4* table_alloc = nullptr;   // (na * W + 2 * TABLE_PAD) entries
+    int* klo = nullptr;              // na
+    float4* partial = nullptr;       // 2 * max_ctas * TILE_PIX / 2
+    int max_ctas = 0;
+    size_t scratch_bytes = 0;
+    // host-buffer entry point staging (allocated on first use)
+    void* d_image = nullptr;
+    void* d_echo = nullptr;
+    double* d_pos = nullptr;
+    // kernel timing
+    bool timing = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> events;
+    size_t events_used = 0;
+    std::string last_error;
+};
+
+namespace {
+
+constexpr double PI = 3.14159265358979323846;
+
+bool isfin(double v) { return std::isfinite(v); }
+
+sarbp_status cuda_fail(sarbp_plan_s* plan, cudaError_t e, const char* what)
+{
+    if (plan) {
+        plan->last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    }
+    return e == cudaErrorMemoryAllocation ? SARBP_ERR_OOM : SARBP_ERR_CUDA;
+}
+
+sarbp_status check_sizes(const sarbp_params* p)
+{
+    if (!p)
+        return SARBP_ERR_INVALID_ARG;
+    if (p->nx < 0 || p->ny < 0 || p->na < 0 || p->nr < 0)
+        return SARBP_ERR_INVALID_ARG;
+    if ((int64_t)p->nx * (int64_t)p->ny > (int64_t(1) << 30))
+        return SARBP_ERR_INVALID_ARG;
+    if (!(isfin(p->dx) && p->dx > 0 && isfin(p->dy) && p->dy > 0))
+        return SARBP_ERR_INVALID_ARG;
+    if (!(isfin(p->dr) && p->dr > 0))
+        return SARBP_ERR_INVALID_ARG;
+    return SARBP_OK;
+}
+
+sarbp_status check_geometry(const sarbp_params* p)
+{
+    if (!(isfin(p->x0) && isfin(p->y0) && isfin(p->z0) && isfin(p->r0)))
+        return SARBP_ERR_INVALID_ARG;
+    if (!(isfin(p->wavelength) && p->wavelength > 0))
+        return SARBP_ERR_INVALID_ARG;
+    if (p->flags & ~SARBP_ACCUMULATE)
+        return SARBP_ERR_INVALID_ARG;
+    return SARBP_OK;
+}
+
+bool aligned8(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 7u) == 0; }
+
+double tile_qmax(double dx, double dy)
+{
+    const double hx = 0.5 * (TILE_X - 1) * dx, hy = 0.5 * (TILE_Y - 1) * dy;
+    return std::sqrt(hx * hx + hy * hy);
+}
+
+unsigned long long frac_fixed64(double v)
+{
+    double f = v - std::floor(v);
+    if (!(f >= 0.0 && f < 1.0))
+        f = 0.0;
+    const double scaled = std::ldexp(f, 64);
+    if (scaled >= 18446744073709551615.0)
+        return ~0ull;
+    return (unsigned long long)scaled;
+}
+
+int ctas_for(const sarbp_plan_s* plan)
+{
+    const long long units = (long long)plan->tiles * plan->p.na;
+    long long want = (units + MIN_PULSES_PER_CTA - 1) / MIN_PULSES_PER_CTA;
+    if (want < 1)
+        want = 1;
+    return (int)std::min<long long>(plan->max_ctas, want);
+}
+
+BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
+{
+    BpConst k{};
+    k.nx = p->nx;
+    k.ny = p->ny;
+    k.na = p->na;
+    k.nr = p->nr;
+    k.W = plan->W;
+    k.tiles_x = plan->tiles_x;
+    k.tiles = plan->tiles;
+    k.full_window = plan->full_window;
+    k.ctas = ctas_for(plan);
+    k.flags = p->flags;
+    k.units = (long long)plan->tiles * p->na;
+    k.x0 = p->x0;
+    k.y0 = p->y0;
+    k.z0 = p->z0;
+    k.dx = p->dx;
+    k.dy = p->dy;
+    k.r0 = p->r0;
+    k.dr = p->dr;
+    k.inv_dr = 1.0 / p->dr;
+    k.rect_x0 = p->x0;
+    k.rect_x1 = p->x0 + ((double)plan->tiles_x * TILE_X - 1.0) * p->dx;
+    k.rect_y0 = p->y0;
+    k.rect_y1 = p->y0 + ((double)plan->tiles_y * TILE_Y - 1.0) * p->dy;
+    k.qmax = tile_qmax(p->dx, p->dy);
+    // Taylor remainder allowed on the fast path: 5e-5 rad of phase
+    k.fast_tol_bins = 5e-5 * p->wavelength / (4.0 * PI * p->dr);
+    const double alpha = 2.0 * p->dr / p->wavelength;   // turns per bin
+    const double beta = 2.0 * p->r0 / p->wavelength;    // turns at bin 0
+    k.alpha_fx = frac_fixed64(alpha);
+    k.beta_fx = frac_fixed64(beta);
+    k.c_phase = (float)(2.0 * PI * alpha);
+    k.inv_c = (float)(1.0 / (2.0 * PI * alpha));
+    k.dx_f = (float)p->dx;
+    k.dy_f = (float)p->dy;
+    k.inv_dr_f = (float)(1.0 / p->dr);
+    return k;
+}
+
+void free_plan(sarbp_plan_s* plan)
+{
+    if (!plan)
+        return;
+    cudaFree(plan->table_alloc);
+    cudaFree(plan->klo);
+    cudaFree(plan->partial);
+    cudaFree(plan->d_image);
+    cudaFree(plan->d_echo);
+    cudaFree(plan->d_pos);
+    for (auto& ev : plan->events) {
+        cudaEventDestroy(ev.first);
+        cudaEventDestroy(ev.second);
+    }
+    delete plan;
+}
+
+// Tiles whose units are split between CTAs need the reduce kernel.
+bool any_split_tile(const BpConst& k)
+{
+    if (k.ctas <= 1)
+        return false;
+    for (long long b = 1; b < k.ctas; ++b) {
+        const long long s = b * k.units / k.ctas;
+        if (s % k.na != 0 && s < k.units)
+            return true;                    // a CTA boundary inside a tile
+    }
+    return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sarbp_status_string(sarbp_status status)
+{
+    switch (status) {
+    case SARBP_OK: return "ok";
+    case SARBP_ERR_INVALID_ARG: return "invalid argument";
+    case SARBP_ERR_PLAN_MISMATCH: return "parameters do not match the plan";
+    case SARBP_ERR_CUDA: return "CUDA error";
+    case SARBP_ERR_OOM: return "out of memory";
+    case SARBP_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    }
+    return "unknown status";
+}
+
+const char* sarbp_last_error(sarbp_plan_t plan)
+{
+    return plan ? plan->last_error.c_str() : "";
+}
+
+sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
+{
+    if (!out)
+        return SARBP_ERR_INVALID_ARG;
+    *out = nullptr;
+    sarbp_status st = check_sizes(p);
+    if (st != SARBP_OK)
+        return st;
+    if (p->flags & ~SARBP_ACCUMULATE)
+        return SARBP_ERR_INVALID_ARG;
+    if (!(isfin(p->wavelength) && p->wavelength > 0))
+        return SARBP_ERR_INVALID_ARG;
+
+    auto* plan = new (std::nothrow) sarbp_plan_s();
+    if (!plan)
+        return SARBP_ERR_OOM;
+    plan->p = *p;
+
+    cudaError_t e = cudaGetDevice(&plan->device);
+    if (e != cudaSuccess) {
+        st = cuda_fail(plan, e, "cudaGetDevice");
+        free_plan(plan);
+        return st;
+    }
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, plan->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, plan->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&plan->sms, cudaDevAttrMultiProcessorCount, plan->device);
+    if (e != cudaSuccess) {
+        st = cuda_fail(plan, e, "cudaDeviceGetAttribute");
+        free_plan(plan);
+        return st;
+    }
+    if (major != 10 || minor != 3) {
+        free_plan(plan);
+        return SARBP_ERR_UNSUPPORTED_DEVICE;
+    }
+    e = backproject_occupancy(&plan->ctas_per_sm);
+    if (e != cudaSuccess || plan->ctas_per_sm < 1) {
+        st = cuda_fail(plan, e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "occupancy");
+        free_plan(plan);
+        return st;
+    }
+    plan->max_ctas = plan->sms * plan->ctas_per_sm;
+
+    plan->tiles_x = (p->nx + TILE_X - 1) / TILE_X;
+    plan->tiles_y = (p->ny + TILE_Y - 1) / TILE_Y;
+    plan->tiles = plan->tiles_x * plan->tiles_y;
+
+    // Table rows: the range extent of the tile-padded image plus a tile's reach
+    const double ext_x = ((double)plan->tiles_x * TILE_X - 1.0) * p->dx;
+    const double ext_y = ((double)plan->tiles_y * TILE_Y - 1.0) * p->dy;
+    const double diag = std::sqrt(ext_x * ext_x + ext_y * ext_y);
+    const double w_geom = std::ceil((diag + 2.0 * tile_qmax(p->dx, p->dy)) / p->dr) + 2 * MARGIN + 6;
+    const long long w_full = (long long)p->nr + 2 * MARGIN + 8;
+    if (w_geom < (double)w_full) {
+        plan->W = (int)w_geom;
+        plan->full_window = 0;
+    } else {
+        plan->W = (int)w_full;
+        plan->full_window = 1;
+    }
+    plan->W = (plan->W + 3) & ~3;
+
+    if (plan->tiles > 0 && p->na > 0) {
+        const size_t table_entries = (size_t)p->na * plan->W + 2 * TABLE_PAD;
+        const size_t sizes[3] = {table_entries * sizeof(float4), (size_t)p->na * sizeof(int),
+                                 (size_t)plan->max_ctas * TILE_PIX * sizeof(float4)};
+        void** ptrs[3] = {reinterpret_cast<void**>(&plan->table_alloc),
+                          reinterpret_cast<void**>(&plan->klo),
+                          reinterpret_cast<void**>(&plan->partial)};
+        for (int i = 0; i < 3; ++i) {
+            e = cudaMalloc(ptrs[i], sizes[i]);
+            if (e != cudaSuccess) {
+                st = cuda_fail(plan, e, "cudaMalloc");
+                free_plan(plan);
+                return st;
+            }
+            plan->scratch_bytes += sizes[i];
+        }
+        // the pads stay zero so that no read near the table's ends sees garbage
+        e = cudaMemset(plan->table_alloc, 0, table_entries * sizeof(float4));
+        if (e != cudaSuccess) {
+            st = cuda_fail(plan, e, "cudaMemset");
+            free_plan(plan);
+            return st;
+        }
+    }
+    *out = plan;
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_destroy(sarbp_plan_t plan)
+{
+    free_plan(plan);
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out)
+{
+    if (!plan || !out)
+        return SARBP_ERR_INVALID_ARG;
+    out->tile_x = TILE_X;
+    out->tile_y = TILE_Y;
+    out->tiles = plan->tiles;
+    out->ctas = ctas_for(plan);
+    out->ctas_per_sm = plan->ctas_per_sm;
+    out->sms = plan->sms;
+    out->window = plan->W;
+    out->full_window = plan->full_window;
+    out->kernels_per_call = 0;
+    if (plan->tiles > 0 && plan->p.na > 0 && plan->p.nr >= 2)
+        out->kernels_per_call = any_split_tile(make_const(plan, &plan->p)) ? 3 : 2;
+    else if (plan->tiles > 0)
+        out->kernels_per_call = 0;   // a memset at most
+    out->scratch_bytes = plan->scratch_bytes;
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_set_timing(sarbp_plan_t plan, int enable)
+{
+    if (!plan)
+        return SARBP_ERR_INVALID_ARG;
+    plan->timing = enable != 0;
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* launches)
+{
+    if (!plan || !main_ms || !launches)
+        return SARBP_ERR_INVALID_ARG;
+    double total = 0.0;
+    for (size_t i = 0; i < plan->events_used; ++i) {
+        cudaError_t e = cudaEventSynchronize(plan->events[i].second);
+        float ms = 0.f;
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&ms, plan->events[i].first, plan->events[i].second);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "kernel timing");
+        total += ms;
+    }
+    *main_ms = total;
+    *launches = (int32_t)plan->events_used;
+    plan->events_used = 0;
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoes,
+                               const double* antenna_pos, const sarbp_params* params,
+                               void* stream)
+{
+    if (!plan || !params)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr)
+        return SARBP_ERR_PLAN_MISMATCH;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels > 0 && (!image || !aligned8(image)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && (!antenna_pos || !aligned8(antenna_pos)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && params->nr > 0 && (!echoes || !aligned8(echoes)))
+        return SARBP_ERR_INVALID_ARG;
+    plan->last_error.clear();
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pixels == 0)
+        return SARBP_OK;
+    if (params->na == 0 || params->nr < 2) {
+        // no pulse can contribute: the image is the zero sum
+        if (!(params->flags & SARBP_ACCUMULATE)) {
+            e = cudaMemsetAsync(image, 0, (size_t)pixels * 8, s);
+            if (e != cudaSuccess)
+                return cuda_fail(plan, e, "cudaMemsetAsync");
+        }
+        return SARBP_OK;
+    }
+
+    const BpConst k = make_const(plan, params);
+    float4* table = plan->table_alloc + TABLE_PAD;
+    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "table kernel launch");
+
+    std::pair<cudaEvent_t, cudaEvent_t>* ev = nullptr;
+    if (plan->timing) {
+        if (plan->events_used == plan->events.size()) {
+            cudaEvent_t a, b;
+            e = cudaEventCreate(&a);
+            if (e == cudaSuccess) {
+                e = cudaEventCreate(&b);
+                if (e != cudaSuccess)
+                    cudaEventDestroy(a);
+            }
+            if (e != cudaSuccess)
+                return cuda_fail(plan, e, "cudaEventCreate");
+            plan->events.emplace_back(a, b);
+        }
+        ev = &plan->events[plan->events_used++];
+        cudaEventRecord(ev->first, s);
+    }
+    e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
+                           plan->partial, s);
+    if (ev)
+        cudaEventRecord(ev->second, s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "backprojection kernel launch");
+    if (any_split_tile(k)) {
+        e = launch_reduce(k, plan->partial, static_cast<float2*>(image), s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "reduce kernel launch");
+    }
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
+                                    const double* antenna_pos, const sarbp_params* params,
+                                    void* stream)
+{
+    if (!plan || !params)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    const long long pixels = (long long)params->nx * params->ny;
+    const size_t img_bytes = (size_t)pixels * 8;
+    const size_t echo_bytes = (size_t)params->na * params->nr * 8;
+    const size_t pos_bytes = (size_t)params->na * 3 * sizeof(double);
+    if (pixels > 0 && !image)
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && !antenna_pos)
+        return SARBP_ERR_INVALID_ARG;
+    if (echo_bytes > 0 && !echoes)
+        return SARBP_ERR_INVALID_ARG;
+    if (params->nx != plan->p.nx || params->ny != plan->p.ny || params->na != plan->p.na ||
+        params->nr != plan->p.nr)
+        return SARBP_ERR_PLAN_MISMATCH;
+
+    cudaError_t e = cudaSuccess;
+    if (img_bytes && !plan->d_image)
+        e = cudaMalloc(&plan->d_image, img_bytes);
+    if (e == cudaSuccess && echo_bytes && !plan->d_echo)
+        e = cudaMalloc(&plan->d_echo, echo_bytes);
+    if (e == cudaSuccess && pos_bytes && !plan->d_pos)
+        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), pos_bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMalloc (host staging)");
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (echo_bytes)
+        e = cudaMemcpyAsync(plan->d_echo, echoes, echo_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && pos_bytes)
+        e = cudaMemcpyAsync(plan->d_pos, antenna_pos, pos_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && img_bytes && (params->flags & SARBP_ACCUMULATE))
+        e = cudaMemcpyAsync(plan->d_image, image, img_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMemcpyAsync (to device)");
+    st = sarbp_backproject(plan, plan->d_image, plan->d_echo, plan->d_pos, params, stream);
+    if (st != SARBP_OK)
+        return st;
+    if (img_bytes)
+        e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMemcpyAsync (to host)");
+    return SARBP_OK;
+}
+
+}  // extern "C"

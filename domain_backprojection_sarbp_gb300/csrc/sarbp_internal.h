@@ -1,0 +1,55 @@
+// sarbp_internal.h - constants and launch helpers shared by the libsarbp host
+// code and its kernels. Not part of the public C-ABI (include/sarbp.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sarbp {
+
+// Work tile: one thread owns TILE_X consecutive pixels of one image row; the
+// 32 lanes of a warp own 32 consecutive rows; WARPS warps stack vertically.
+constexpr int TILE_X = 32;
+constexpr int WARPS = 4;
+constexpr int THREADS = 32 * WARPS;
+constexpr int TILE_Y = 32 * WARPS;
+constexpr int TILE_PIX = TILE_X * TILE_Y;
+constexpr int CHUNK = THREADS;             // pulses whose records are built together
+constexpr int MARGIN = 4;                  // spare table entries at each end of a row
+constexpr int TABLE_PAD = 64;              // spare entries before/after the whole table
+constexpr int MIN_PULSES_PER_CTA = 32;     // keeps tiny problems from over-splitting
+constexpr int KLO_INVALID = INT32_MIN;     // pulse with a non-finite antenna position
+
+enum RecordKind : int { REC_SKIP = 0, REC_FAST = 1, REC_EXACT = 2 };
+
+// Launch constants, computed on the host in float64 for every call.
+struct BpConst {
+    int nx, ny, na, nr;
+    int W;                       // table entries per pulse (row pitch, float4 units)
+    int tiles_x, tiles;
+    int full_window;             // every row spans bins [-MARGIN-4, nr+...)
+    int ctas;                    // persistent CTAs of the main kernel
+    unsigned flags;
+    long long units;             // tiles * na (tile-pulse work units)
+
+    double x0, y0, z0, dx, dy, r0, dr, inv_dr;
+    double rect_x0, rect_x1, rect_y0, rect_y1;  // tile-padded image rectangle
+    double qmax;                 // largest distance from a tile centre to its pixels
+    double fast_tol_bins;        // Taylor remainder allowed on the fast path, in bins
+
+    unsigned long long alpha_fx; // frac(2 dr / lambda) * 2^64
+    unsigned long long beta_fx;  // frac(2 r0 / lambda) * 2^64
+    float c_phase;               // 2 pi * 2 dr / lambda: phase per bin, radians
+    float inv_c;                 // 1 / c_phase
+    float dx_f, dy_f, inv_dr_f;
+};
+
+cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos,
+                         float4* table, int* klo, cudaStream_t s);
+cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
+                               const int* klo, float2* image, float4* partial, cudaStream_t s);
+cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
+                          cudaStream_t s);
+cudaError_t backproject_occupancy(int* ctas_per_sm);
+
+}  // namespace sarbp

@@ -1,0 +1,439 @@
+// sarbp_kernels.cu - the device side of libsarbp (sm_103a).
+//
+// SARBP-GPU = the page "基于GPU的SAR后向投影成像优化与CUDA加速实践". The page's
+// loop (§2.2 steps, §3.3 pseudo-code) spends, per pixel and pulse, a square
+// root for the slant range, a floor and two complex gathers for the linear
+// interpolation, and a sine and a cosine for exp(+j 4 pi R / lambda). Its
+// design (one thread per pixel, §2.1; shared-memory echo tiles, §2.3; double
+// precision phase or Kahan sums, §2.2 and §4.3) targets an sm_86 card. This file
+// computes the same sum with less work per update:
+//
+// 1. Echo table (table_kernel). Writing u = (R - r0)/dr = k + f, the phase
+//    4 pi R / lambda splits into 2 pi (2 r_k / lambda) + c f with
+//    c = 2 pi (2 dr / lambda). So
+//        w(f) exp(j 4 pi R / lambda) = exp(j c f) [A_k + f D_k],
+//        A_k = e_k psi_k,  D_k = (e_{k+1} - e_k) psi_k,  psi_k = exp(j 2 pi 2 r_k / lambda).
+//    One 16-byte row entry (A_k, D_k / c) then serves one update: one gather
+//    instead of two, and a phase that depends on the in-bin fraction f only,
+//    so it needs no reduction of a thousand-turn argument. psi_k comes from an
+//    exact 64-bit fixed-point phase accumulator. Each row keeps only the bins
+//    the image can reach (its window starts at klo[n]), zero outside the
+//    recorded range 0 <= k <= nr - 2, so the window rule costs nothing per update.
+//
+// 2. Range without a square root (bp_kernel). For each (tile, pulse) the slant
+//    range to the tile centre is computed in float64 and the range of every
+//    pixel of the tile is a Taylor polynomial of |p - a_n| about it (complete
+//    to third order, with the fourth-order terms in the row offset), in bins. A thread owns 32 pixels of one row, so per pulse it reduces the
+//    polynomial to a quadratic in its column offset (a split float for the
+//    large linear term keeps 2^-22-bin accuracy), and each update costs two
+//    FMAs for u. Pulses where the remainder bound exceeds 5e-5 rad of phase
+//    (near field, huge tiles) take an exact float32 path instead.
+//
+// 3. Work split (stream-K). The (tile, pulse) units are cut into one equal,
+//    contiguous range per resident CTA. A tile covered by one CTA is written
+//    directly; the pieces of a shared tile go to partial buffers that
+//    reduce_kernel sums in CTA order, so the result is deterministic.
+#include "sarbp_internal.h"
+
+#include <cmath>
+#include <cstdint>
+
+namespace sarbp {
+namespace {
+
+constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/round(x) in the mantissa
+constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
+
+struct __align__(16) Record {
+    float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
+    float4 b;  // c03, c04, c10, c11
+    float4 c;  // c12, c13, c20, c21
+    float4 d;  // c22, unused, kbase (int bits), kind (int bits)
+    float4 e;  // exact path: 2 vx, 2 vy, R_t, R_t^2
+};
+
+// ---------------------------------------------------------------------------
+// Echo table: one block per pulse.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __restrict__ echo,
+                                                    const double* __restrict__ pos,
+                                                    float4* __restrict__ table,
+                                                    int* __restrict__ klo)
+{
+    const int n = blockIdx.x;
+    __shared__ int s_lo;
+    if (threadIdx.x == 0) {
+        const double ax = pos[3 * (size_t)n + 0];
+        const double ay = pos[3 * (size_t)n + 1];
+        const double az = pos[3 * (size_t)n + 2];
+        int lo;
+        if (!(isfinite(ax) && isfinite(ay) && isfinite(az))) {
+            lo = KLO_INVALID;
+        } else if (k.full_window) {
+            lo = -(MARGIN + 4);
+        } else {
+            // nearest point of the tile-padded image rectangle to the antenna
+            const double cx = fmin(fmax(ax, k.rect_x0), k.rect_x1);
+            const double cy = fmin(fmax(ay, k.rect_y0), k.rect_y1);
+            const double ddx = cx - ax, ddy = cy - ay, ddz = k.z0 - az;
+            const double rmin = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
+            double u = (rmin - k.qmax - k.r0) * k.inv_dr;
+            u = fmin(fmax(u, -1.0e9), 1.0e9);
+            lo = (int)floor(u) - MARGIN;
+        }
+        s_lo = lo;
+        klo[n] = lo;
+    }
+    __syncthreads();
+    const int lo = s_lo;
+    float4* row = table + (size_t)n * k.W;
+    const float2* erow = echo + (size_t)n * k.nr;
+    for (int w = threadIdx.x; w < k.W; w += blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long kk = (long long)lo + w;
+        if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 2) {
+            const float2 e0 = erow[kk];
+            const float2 e1 = erow[kk + 1];
+            // frac(2 r_k / lambda) in 64-bit fixed point, exact up to the
+            // rounding of the two constants
+            const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
+            const float turns = (float)(ph >> 40) * 0x1p-24f;
+            float s, c;
+            sincospif(2.0f * turns, &s, &c);
+            const float dre = e1.x - e0.x;
+            const float dim = e1.y - e0.y;
+            v.x = e0.x * c - e0.y * s;
+            v.y = e0.x * s + e0.y * c;
+            v.z = (dre * c - dim * s) * k.inv_c;
+            v.w = (dre * s + dim * c) * k.inv_c;
+        }
+        row[w] = v;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-(tile, pulse) record, float64.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float f32(double v) { return __double2float_rn(v); }
+
+__device__ void make_record(const BpConst& k, const double* __restrict__ pos,
+                            const int* __restrict__ klo, int n, double xc, double yc,
+                            Record& out)
+{
+    const double ax = pos[3 * (size_t)n + 0];
+    const double ay = pos[3 * (size_t)n + 1];
+    const double az = pos[3 * (size_t)n + 2];
+    const int lo = klo[n];
+    const double vx = xc - ax, vy = yc - ay, vz = k.z0 - az;
+    const double r2 = vx * vx + vy * vy + vz * vz;
+    const double r = sqrt(r2);
+    int kind = REC_SKIP;
+    Record rec;
+    rec.a = rec.b = rec.c = rec.d = rec.e = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lo != KLO_INVALID && isfinite(r)) {
+        const double u = (r - k.r0) * k.inv_dr;
+        const double umin = (r - k.qmax - k.r0) * k.inv_dr - 1e-6;
+        const double umax = (r + k.qmax - k.r0) * k.inv_dr + 1e-6;
+        // every pixel of the tile has k <= -1 or k >= nr - 1: no recorded echo
+        if (!(umax < 0.0 || umin >= (double)k.nr - 1.0)) {
+            const double kt = floor(fmin(fmax(u, -1.0e9), 1.0e9));
+            const double kb = fmin(fmax(kt - lo, -1.0e9), 1.0e9);
+            const double kmin_rel = floor(umin) - lo;
+            const double kmax_rel = floor(umax) - lo;
+            const bool in_row = kmin_rel >= MARGIN && kmax_rel <= (double)(k.W - 1 - MARGIN);
+
+            // Taylor coefficients of |p - a_n| about the tile centre, in bins
+            // per power of the pixel offsets (i, j). With g = v / R, M = I - g g^T,
+            // a = (g.q)/R and b = |q|^2/R^2, |v + q| = R sqrt(1 + 2a + b) gives
+            //   order 2:  (q^T M q) / (2R)
+            //   order 3:  -(g.q)(q^T M q) / (2R^2)
+            //   order 4:  (-|q|^4/8 + 3 (g.q)^2 |q|^2 / 4 - 5 (g.q)^4 / 8) / R^3
+            // Order-4 terms with j^2 or more are kept (they fold into the
+            // per-thread coefficients for free); the others are bounded below.
+            const double ir = 1.0 / r;
+            const double ir3 = ir * ir * ir;
+            const double gx = vx * ir, gy = vy * ir;
+            const double mxx = 1.0 - gx * gx, mxy = -gx * gy, myy = 1.0 - gy * gy;
+            const double dx = k.dx, dy = k.dy, idr = k.inv_dr;
+            const double h2 = 0.5 * ir, h3 = -0.5 * ir * ir;
+            const double c10 = gx * dx * idr;
+            const double c01 = gy * dy * idr;
+            const double c20 = mxx * h2 * dx * dx * idr;
+            const double c11 = 2.0 * mxy * h2 * dx * dy * idr;
+            const double c02 = myy * h2 * dy * dy * idr;
+            const double c30 = h3 * gx * mxx * dx * dx * dx * idr;
+            const double c21 = h3 * (2.0 * gx * mxy + gy * mxx) * dx * dx * dy * idr;
+            const double c12 = h3 * (gx * myy + 2.0 * gy * mxy) * dx * dy * dy * idr;
+            const double c03 = h3 * gy * myy * dy * dy * dy * idr;
+            const double gx2 = gx * gx, gy2 = gy * gy;
+            const double k40 = -0.125 + 0.75 * gx2 - 0.625 * gx2 * gx2;
+            const double k31 = 1.5 * gx * gy - 2.5 * gx2 * gx * gy;
+            const double k22 = -0.25 + 0.75 * (gx2 + gy2) - 3.75 * gx2 * gy2;
+            const double k13 = 1.5 * gx * gy - 2.5 * gx * gy2 * gy;
+            const double k04 = -0.125 + 0.75 * gy2 - 0.625 * gy2 * gy2;
+            const double c22 = k22 * ir3 * dx * dx * dy * dy * idr;
+            const double c13 = k13 * ir3 * dx * dy * dy * dy * idr;
+            const double c04 = k04 * ir3 * dy * dy * dy * dy * idr;
+
+            // dropped: c30 i^3, c31 i^3 j, c40 i^4 (metres), plus the order-5
+            // remainder, at most |q|^5 / R^4 while |q| <= R / 8
+            const double hx = 0.5 * (TILE_X - 1) * dx, hy = 0.5 * (TILE_Y - 1) * dy;
+            const double hx3 = hx * hx * hx;
+            const double q5 = k.qmax * k.qmax * k.qmax * k.qmax * k.qmax;
+            const double dropped = fabs(gx * mxx) * 0.5 * ir * ir * hx3
+                                 + (fabs(k31) * hx3 * hy + fabs(k40) * hx3 * hx) * ir3
+                                 + q5 * ir3 * ir;
+            const bool fast = in_row && r > 8.0 * k.qmax && dropped * idr <= k.fast_tol_bins;
+            kind = fast ? REC_FAST : REC_EXACT;
+
+            const float c01h = f32(c01);
+            rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), f32(c02));
+            rec.b = make_float4(f32(c03), f32(c04), f32(c10), f32(c11));
+            rec.c = make_float4(f32(c12), f32(c13), f32(c20), f32(c21));
+            rec.d = make_float4(f32(c22), 0.f, __int_as_float((int)kb), 0.f);
+            rec.e = make_float4(f32(2.0 * vx), f32(2.0 * vy), f32(r), f32(r2));
+        }
+    }
+    rec.d.w = __int_as_float(kind);
+    out = rec;
+}
+
+// ---------------------------------------------------------------------------
+// Updates of one pulse for the 32 pixels a thread owns.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fast_pulse(const BpConst& k, const Record& rec, const float4* row,
+                                           float jf, float jf2, float jf3, float jf4,
+                                           float (&acc_re)[TILE_X], float (&acc_im)[TILE_X])
+{
+    // u(i) = E0 + i E1 + i^2 E2 for this thread's row j; the large c01 j term
+    // is split into an integer (folded into the row pointer) and a fraction
+    const float hi = rec.a.y * jf;
+    float lo = fmaf(rec.a.y, jf, -hi);
+    lo = fmaf(rec.a.z, jf, lo);
+    const float small = fmaf(rec.b.y, jf4, fmaf(rec.b.x, jf3, fmaf(rec.a.w, jf2, rec.a.x + lo)));
+    const float t = hi + MAGIC;
+    const float hir = t - MAGIC;
+    const float e0 = (hi - hir) + small;
+    const int shift = __float_as_int(t) - MAGIC_BITS;
+    const float e1 = fmaf(rec.c.y, jf3, fmaf(rec.c.x, jf2, fmaf(rec.b.w, jf, rec.b.z)));
+    const float e2 = fmaf(rec.d.x, jf2, fmaf(rec.c.w, jf, rec.c.z));
+    const int kbase = __float_as_int(rec.d.z);
+    const unsigned long long base =
+        reinterpret_cast<unsigned long long>(row + kbase + shift) - (unsigned long long)MAGIC_BITS * 16ull;
+    const float c_phase = k.c_phase;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float i = (float)m - 0.5f * (TILE_X - 1);
+        const float ub = fmaf(i, fmaf(i, e2, e1), e0);
+        const float tt = __fadd_rd(ub, MAGIC);
+        const float f = ub - (tt - MAGIC);
+        const float x = f * c_phase;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(
+            base + (unsigned long long)(unsigned)__float_as_int(tt) * 16ull));
+        const float wr = fmaf(x, v.z, v.x);
+        const float wi = fmaf(x, v.w, v.y);
+        float s, c;
+        __sincosf(x, &s, &c);
+        acc_re[m] = fmaf(wr, c, fmaf(-wi, s, acc_re[m]));
+        acc_im[m] = fmaf(wr, s, fmaf(wi, c, acc_im[m]));
+    }
+}
+
+__device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec, const float4* row,
+                                         float jf, float (&acc_re)[TILE_X], float (&acc_im)[TILE_X])
+{
+    // |p - a|^2 = R_t^2 + s with s = 2 v.q + |q|^2, and R - R_t = s / (R_t + R)
+    const float two_vx = rec.e.x, two_vy = rec.e.y, rt = rec.e.z, rt2 = rec.e.w;
+    const float qy = jf * k.dy_f;
+    const float sy = qy * (two_vy + qy);
+    const int kbase = __float_as_int(rec.d.z);
+    const float c_phase = k.c_phase;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
+        const float s = fmaf(qx, two_vx + qx, sy);
+        const float rp = sqrtf(fmaxf(rt2 + s, 0.0f));
+        const float den = rt + rp;
+        const float dr_m = den > 0.0f ? s / den : 0.0f;
+        const float ub = fmaf(dr_m, k.inv_dr_f, rec.a.x);
+        if (!(ub > -1.0e6f && ub < 1.0e6f))
+            continue;
+        const float kf = floorf(ub);
+        const int kr = kbase + (int)kf;
+        if (kr < 0 || kr > k.W - 1)
+            continue;                       // outside the row: no recorded echo there
+        const float x = (ub - kf) * c_phase;
+        const float4 v = __ldg(row + kr);
+        const float wr = fmaf(x, v.z, v.x);
+        const float wi = fmaf(x, v.w, v.y);
+        float sn, cs;
+        __sincosf(x, &sn, &cs);
+        acc_re[m] = fmaf(wr, cs, fmaf(-wi, sn, acc_re[m]));
+        acc_im[m] = fmaf(wr, sn, fmaf(wi, cs, acc_im[m]));
+    }
+}
+
+__device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
+{
+    return b * k.units / k.ctas;
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel: persistent, one contiguous range of (tile, pulse) units per CTA.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double* __restrict__ pos,
+                                                        const float4* __restrict__ table,
+                                                        const int* __restrict__ klo,
+                                                        float2* __restrict__ image,
+                                                        float4* __restrict__ partial)
+{
+    __shared__ Record s_rec[CHUNK];
+    const int tid = threadIdx.x;
+    const int jr = tid;                                   // warp w, lane l -> row 32 w + l
+    const float jf = (float)jr - 0.5f * (TILE_Y - 1);
+    const float jf2 = jf * jf;
+    const float jf3 = jf2 * jf;
+    const float jf4 = jf2 * jf2;
+    const long long b = blockIdx.x;
+    const long long u0 = cta_start(k, b);
+    const long long u1 = cta_start(k, b + 1);
+    if (u0 >= u1)
+        return;
+    const long long t_first = u0 / k.na;
+    const long long t_last = (u1 - 1) / k.na;
+
+    for (long long t = t_first; t <= t_last; ++t) {
+        const int n0 = (int)(max(u0, t * k.na) - t * k.na);
+        const int n1 = (int)(min(u1, (t + 1) * k.na) - t * k.na);
+        const int col0 = (int)(t % k.tiles_x) * TILE_X;
+        const int row0 = (int)(t / k.tiles_x) * TILE_Y;
+        const double xc = k.x0 + ((double)col0 + 0.5 * (TILE_X - 1)) * k.dx;
+        const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
+
+        float acc_re[TILE_X], acc_im[TILE_X];
+#pragma unroll
+        for (int m = 0; m < TILE_X; ++m) {
+            acc_re[m] = 0.f;
+            acc_im[m] = 0.f;
+        }
+
+        for (int c0 = n0; c0 < n1; c0 += CHUNK) {
+            const int cnt = min(CHUNK, n1 - c0);
+            __syncthreads();
+            if (tid < cnt)
+                make_record(k, pos, klo, c0 + tid, xc, yc, s_rec[tid]);
+            __syncthreads();
+#pragma unroll 1
+            for (int p = 0; p < cnt; ++p) {
+                const Record rec = s_rec[p];
+                const int kind = __float_as_int(rec.d.w);
+                const float4* row = table + (size_t)(c0 + p) * k.W;
+                if (kind == REC_FAST)
+                    fast_pulse(k, rec, row, jf, jf2, jf3, jf4, acc_re, acc_im);
+                else if (kind == REC_EXACT)
+                    exact_pulse(k, rec, row, jf, acc_re, acc_im);
+            }
+        }
+
+        const int rowi = row0 + jr;
+        if (n0 == 0 && n1 == k.na) {
+            if (rowi < k.ny) {
+                float2* dst = image + (size_t)rowi * k.nx;
+                const bool acc = (k.flags & 1u) != 0;
+#pragma unroll
+                for (int m = 0; m < TILE_X; ++m) {
+                    const int col = col0 + m;
+                    if (col < k.nx) {
+                        float2 v = make_float2(acc_re[m], acc_im[m]);
+                        if (acc) {
+                            const float2 o = dst[col];
+                            v.x += o.x;
+                            v.y += o.y;
+                        }
+                        dst[col] = v;
+                    }
+                }
+            }
+        } else {
+            const int slot = (t == t_first) ? 0 : 1;
+            float4* dst = partial + ((size_t)(b * 2 + slot) * TILE_PIX + (size_t)jr * TILE_X) / 2;
+#pragma unroll
+            for (int m = 0; m < TILE_X; m += 2)
+                dst[m / 2] = make_float4(acc_re[m], acc_im[m], acc_re[m + 1], acc_im[m + 1]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Sum the partial pieces of shared tiles in CTA order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ long long cta_of_unit(const BpConst& k, long long u)
+{
+    return ((u + 1) * k.ctas - 1) / k.units;   // largest b with cta_start(b) <= u
+}
+
+__global__ void __launch_bounds__(THREADS) reduce_kernel(BpConst k, const float4* __restrict__ partial,
+                                                         float2* __restrict__ image)
+{
+    const long long t = blockIdx.x;
+    const long long bf = cta_of_unit(k, t * k.na);
+    const long long bl = cta_of_unit(k, (t + 1) * k.na - 1);
+    if (bf == bl)
+        return;                                    // written directly by one CTA
+    const int col0 = (int)(t % k.tiles_x) * TILE_X;
+    const int row0 = (int)(t / k.tiles_x) * TILE_Y;
+    const float2* part = reinterpret_cast<const float2*>(partial);
+    const bool acc = (k.flags & 1u) != 0;
+    for (int p = threadIdx.x; p < TILE_PIX; p += blockDim.x) {
+        float2 sum = make_float2(0.f, 0.f);
+        for (long long b = bf; b <= bl; ++b) {
+            const long long s0 = cta_start(k, b);
+            if (s0 >= cta_start(k, b + 1))
+                continue;                          // CTA with no work
+            const int slot = (s0 / k.na == t) ? 0 : 1;
+            const float2 v = part[(size_t)(b * 2 + slot) * TILE_PIX + p];
+            sum.x += v.x;
+            sum.y += v.y;
+        }
+        const int rowi = row0 + p / TILE_X;
+        const int col = col0 + p % TILE_X;
+        if (rowi < k.ny && col < k.nx) {
+            float2* dst = image + (size_t)rowi * k.nx + col;
+            if (acc) {
+                const float2 o = *dst;
+                sum.x += o.x;
+                sum.y += o.y;
+            }
+            *dst = sum;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
+                         int* klo, cudaStream_t s)
+{
+    table_kernel<<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
+                               const int* klo, float2* image, float4* partial, cudaStream_t s)
+{
+    bp_kernel<<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image, cudaStream_t s)
+{
+    reduce_kernel<<<k.tiles, THREADS, 0, s>>>(k, partial, image);
+    return cudaGetLastError();
+}
+
+cudaError_t backproject_occupancy(int* ctas_per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, bp_kernel, THREADS, 0);
+}
+
+}  // namespace sarbp

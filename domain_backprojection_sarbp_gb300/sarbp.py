@@ -1,0 +1,167 @@
+"""Python binding of libsarbp: argument marshalling over the C-ABI.
+
+Every step of the backprojection runs in the library's CUDA kernels; this
+module only checks tensor dtypes, shapes and devices and passes pointers.
+PyTorch provides device memory and streams. There is no CPU fallback: when
+the library is missing, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _native
+from ._native import Params, PlanInfo, SARBP_ACCUMULATE
+
+
+class SarbpError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        text = _native.lib().sarbp_status_string(status).decode()
+        super().__init__(f"{where}: {text}" + (f" ({detail})" if detail else ""))
+
+
+def _params(p, flags=None) -> Params:
+    if isinstance(p, Params):
+        out = Params.from_buffer_copy(p)
+    else:
+        out = Params.from_dict(p)
+    if flags is not None:
+        out.flags = int(flags)
+    return out
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_device_tensor(t, name, dtype, shape):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else None)
+
+
+class Plan:
+    """A libsarbp plan: fixed sizes, device scratch, repeated backprojections."""
+
+    def __init__(self, params):
+        self._lib = _native.lib()
+        self.params = _params(params)
+        handle = ctypes.c_void_p()
+        st = self._lib.sarbp_plan(ctypes.byref(handle), ctypes.byref(self.params))
+        if st != _native.SARBP_OK:
+            raise SarbpError(st, "sarbp_plan")
+        self._h = handle
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.sarbp_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _raise(self, st, where):
+        detail = self._lib.sarbp_last_error(self._h).decode(errors="replace")
+        raise SarbpError(st, where, detail)
+
+    def backproject(self, image, echoes, antenna_pos, params=None, accumulate=False, stream=None):
+        """Enqueue I(p) = sum_n w_n exp(+j 4 pi R_n / lambda) on ``stream`` (device tensors).
+
+        image complex64 [ny, nx]; echoes complex64 [na, nr]; antenna_pos float64 [na, 3].
+        """
+        import torch
+        p = _params(params if params is not None else self.params,
+                    SARBP_ACCUMULATE if accumulate else None)
+        img = _check_device_tensor(image, "image", torch.complex64, (p.ny, p.nx))
+        ech = _check_device_tensor(echoes, "echoes", torch.complex64, (p.na, p.nr))
+        pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))
+        st = self._lib.sarbp_backproject(self._h, img, ech, pos, ctypes.byref(p),
+                                         _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject")
+        return image
+
+    def backproject_host(self, image, echoes, antenna_pos, params=None, accumulate=False,
+                         stream=None):
+        """Same operation on host arrays (numpy or CPU tensors); returns when the image is on the host."""
+        p = _params(params if params is not None else self.params,
+                    SARBP_ACCUMULATE if accumulate else None)
+
+        def host_ptr(a, name, shape, np_dtype):
+            if hasattr(a, "is_cuda"):
+                if a.is_cuda or not a.is_contiguous():
+                    raise ValueError(f"{name} must be a contiguous CPU tensor")
+                if tuple(a.shape) != shape:
+                    raise ValueError(f"{name} must have shape {shape}")
+                return ctypes.c_void_p(a.data_ptr() if a.numel() else None)
+            if not (isinstance(a, np.ndarray) and a.dtype == np_dtype and a.flags.c_contiguous
+                    and a.shape == shape):
+                raise ValueError(f"{name} must be a C-contiguous {np_dtype} array of shape {shape}")
+            return ctypes.c_void_p(a.ctypes.data if a.size else None)
+
+        img = host_ptr(image, "image", (p.ny, p.nx), np.complex64)
+        ech = host_ptr(echoes, "echoes", (p.na, p.nr), np.complex64)
+        pos = host_ptr(antenna_pos, "antenna_pos", (p.na, 3), np.float64)
+        stream_h = ctypes.c_void_p(None) if stream is None else _stream_handle(stream)
+        st = self._lib.sarbp_backproject_host(self._h, img, ech, pos, ctypes.byref(p), stream_h)
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject_host")
+        return image
+
+    def describe(self) -> dict:
+        info = PlanInfo()
+        st = self._lib.sarbp_plan_describe(self._h, ctypes.byref(info))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_plan_describe")
+        return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+
+    def set_timing(self, enable: bool = True):
+        self._lib.sarbp_set_timing(self._h, 1 if enable else 0)
+
+    def kernel_times(self):
+        """(summed milliseconds, launches) of the main kernel since the last query."""
+        ms = ctypes.c_double()
+        n = ctypes.c_int32()
+        st = self._lib.sarbp_kernel_times(self._h, ctypes.byref(ms), ctypes.byref(n))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_kernel_times")
+        return ms.value, n.value
+
+
+def backproject(image, echoes, antenna_pos, params, accumulate=False, stream=None):
+    """One-shot convenience: plan, backproject, destroy (the plan is freed after a stream sync)."""
+    import torch
+    with Plan(params) as plan:
+        plan.backproject(image, echoes, antenna_pos, accumulate=accumulate, stream=stream)
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return image

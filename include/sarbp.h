@@ -1,0 +1,174 @@
+/*
+ * sarbp.h - libsarbp: time-domain SAR backprojection on one GB300 GPU (sm_103a).
+ *
+ * SARBP-GPU = the page "基于GPU的SAR后向投影成像优化与CUDA加速实践" (a GPU
+ * back-projection SAR imaging retrospective). The operation every entry point
+ * computes is the one that page defines:
+ *
+ *   SARBP-GPU §1.1  for every image pixel, visit every pulse, take the echo at
+ *                   that pixel's range history, compensate its phase and add
+ *                   it coherently into the pixel;
+ *   SARBP-GPU §2.2  the per-pulse steps: slant range from the antenna phase
+ *                   centre, linear interpolation of the range-compressed echo,
+ *                   multiplication by the phase term, accumulation;
+ *   SARBP-GPU §3.3  the kernel pseudo-code: uniform range axis (first sample
+ *                   and spacing), fraction = index - floor(index), phase
+ *                   4*pi*R/lambda applied as exp(+j*phase), monostatic range.
+ *
+ * In formulas, for pixel p = (x0 + ix*dx, y0 + iy*dy, z0) and antenna
+ * positions a_n (n = 0 .. na-1):
+ *
+ *   R_n  = |p - a_n|,  u = (R_n - r0) / dr,  k = floor(u),  f = u - k
+ *   w_n  = (1 - f) e[n][k] + f e[n][k+1]     if 0 <= k and k + 1 <= nr - 1, else 0
+ *   I(p) = sum_n w_n * exp(+j 4 pi R_n / lambda)
+ *
+ * The zero outside the recorded range window is this library's reading of
+ * the page's index clamp (the page treats an index outside the echo as a bug).
+ *
+ * Data layout. All arrays are dense and row-major:
+ *   image        complex64 (interleaved float re, im), [ny][nx], x fastest
+ *   echoes       complex64, [na][nr], pulse-major, range fastest
+ *   antenna_pos  float64, [na][3] = (x, y, z) in metres
+ *
+ * Threading. A plan may be used from one host thread and one stream at a
+ * time. Different plans are independent.
+ *
+ * Errors. No call throws or aborts. Every call returns a status; argument
+ * checks happen before any GPU work is queued, and a call that returns an
+ * error other than SARBP_ERR_CUDA has queued nothing. Errors raised by the
+ * GPU after a call returned surface on a later call or on stream
+ * synchronisation, as usual for asynchronous CUDA work.
+ */
+#ifndef SARBP_H
+#define SARBP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SARBP_VERSION_MAJOR 0
+#define SARBP_VERSION_MINOR 1
+
+typedef enum sarbp_status {
+    SARBP_OK = 0,
+    SARBP_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size or geometry   */
+    SARBP_ERR_PLAN_MISMATCH = 2,      /* params disagree with the plan's fixed fields     */
+    SARBP_ERR_CUDA = 3,               /* a CUDA call failed; see sarbp_last_error         */
+    SARBP_ERR_OOM = 4,                /* device or host allocation failed                 */
+    SARBP_ERR_UNSUPPORTED_DEVICE = 5  /* current device is not compute capability 10.3    */
+} sarbp_status;
+
+/* params.flags */
+#define SARBP_ACCUMULATE 1u  /* add into the image instead of overwriting it: lets a
+                                caller backproject pulses in batches (SARBP-GPU §3.3
+                                stream overlap of echo loading and computation)       */
+
+typedef struct sarbp_params {
+    int32_t nx, ny;       /* image width (x) and height (y), pixels, >= 0             */
+    int32_t na, nr;       /* pulses and range bins, >= 0                              */
+    double x0, y0, z0;    /* position of pixel (0, 0), metres                         */
+    double dx, dy;        /* pixel spacing, metres, > 0                               */
+    double r0, dr;        /* range of bin k is r0 + k*dr, metres; dr > 0              */
+    double wavelength;    /* carrier wavelength lambda = c / fc, metres, > 0
+                             (SARBP-GPU §4.2: the carrier, not the bandwidth one)     */
+    uint32_t flags;       /* SARBP_ACCUMULATE or 0                                    */
+} sarbp_params;
+
+typedef struct sarbp_plan_s* sarbp_plan_t;
+
+/*
+ * sarbp_plan - fix the problem sizes and allocate the plan's device scratch.
+ *
+ * out    receives the new plan (set to NULL on error).
+ * p      host pointer. Fixed for the plan's lifetime: nx, ny, na, nr, dx, dy,
+ *        dr. The other fields may change from call to call.
+ *
+ * Uses the CUDA device current on the calling thread; later calls must run
+ * with that device current. Scratch owned by the plan: the pre-multiplied
+ * echo table (na x W x 16 bytes, W <= nr + 24, where W covers the image's
+ * range extent), one int per pulse, and the partial-sum buffers of the work
+ * split (about 40 MB). Returns SARBP_ERR_INVALID_ARG for negative sizes,
+ * non-finite or non-positive dx, dy, dr, wavelength, unknown flags, or image
+ * sizes above 2^30 pixels; SARBP_ERR_UNSUPPORTED_DEVICE off compute
+ * capability 10.3; SARBP_ERR_OOM if an allocation fails.
+ */
+sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p);
+
+/*
+ * sarbp_backproject - enqueue one backprojection on `stream` and return.
+ *
+ * image        device pointer, complex64 [ny][nx], caller-owned, 8-byte aligned.
+ *              Overwritten, or added into when params->flags has SARBP_ACCUMULATE.
+ * echoes       device pointer, complex64 [na][nr], caller-owned, 8-byte aligned.
+ * antenna_pos  device pointer, float64 [na][3], caller-owned, 8-byte aligned.
+ * params       host pointer; nx, ny, na, nr, dx, dy, dr must equal the plan's
+ *              (else SARBP_ERR_PLAN_MISMATCH).
+ * stream       a cudaStream_t of the plan's device (NULL = legacy default stream).
+ *
+ * The inputs must stay valid and unmodified until the work on `stream` has
+ * finished. A pulse whose antenna position is not finite contributes nothing.
+ * Two calls with identical inputs give bitwise identical images (the pulse
+ * sum has a fixed order). Null pointers are accepted only where the matching
+ * array is empty.
+ */
+sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoes,
+                               const double* antenna_pos, const sarbp_params* params,
+                               void* stream);
+
+/*
+ * sarbp_backproject_host - the same operation on HOST buffers.
+ *
+ * image, echoes, antenna_pos are host pointers with the layouts above (pinned
+ * memory gives the fastest copies; pageable memory works). The call copies
+ * the inputs to plan-owned device buffers (allocated on first use and kept
+ * until sarbp_destroy), backprojects on `stream`, copies the image back and
+ * waits for the stream: when it returns SARBP_OK the image is on the host.
+ * With SARBP_ACCUMULATE the host image is copied in first and added into.
+ */
+sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
+                                    const double* antenna_pos, const sarbp_params* params,
+                                    void* stream);
+
+/* sarbp_destroy - free the plan and its scratch. NULL is accepted. The caller
+   must make sure no work that uses the plan is still running. */
+sarbp_status sarbp_destroy(sarbp_plan_t plan);
+
+/* Static, never-NULL description of a status code. */
+const char* sarbp_status_string(sarbp_status status);
+
+/* The message of the most recent CUDA failure seen by this plan ("" if none).
+   The pointer stays valid until the plan's next call. */
+const char* sarbp_last_error(sarbp_plan_t plan);
+
+/* Plan facts, for tests and benchmarks. */
+typedef struct sarbp_plan_info {
+    int32_t tile_x, tile_y;       /* pixels per work tile                              */
+    int32_t tiles;                /* work tiles covering the image                     */
+    int32_t ctas;                 /* persistent CTAs of the main kernel                */
+    int32_t ctas_per_sm, sms;     /* occupancy used to size the grid                   */
+    int32_t window;               /* W: table entries per pulse                        */
+    int32_t full_window;          /* 1 if every table row spans the whole range axis   */
+    int32_t kernels_per_call;     /* kernel launches one sarbp_backproject enqueues    */
+    size_t scratch_bytes;         /* device memory held by the plan                    */
+} sarbp_plan_info;
+
+sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out);
+
+/*
+ * Kernel timing. When enabled, each sarbp_backproject records CUDA events
+ * around its main backprojection kernel on the call's stream.
+ * sarbp_kernel_times waits for the recorded events, returns the summed
+ * milliseconds and the number of timed launches since the previous query,
+ * and resets both. Timing adds two event records per call and no sync.
+ */
+sarbp_status sarbp_set_timing(sarbp_plan_t plan, int enable);
+sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SARBP_H */

@@ -1,0 +1,265 @@
+"""libsarbp (CUDA, sm_103a) against the FP64 oracle, through the C-ABI.
+
+Acceptance (tests/parity.py): relative L2 <= 1e-3, max |error| <= 1e-3 of the
+oracle's peak, identical per-target argmax. SARBP-GPU §4.2 (the page
+"基于GPU的SAR后向投影成像优化与CUDA加速实践") asks for the same check: run the
+same backprojection on CPU and GPU over simulated point targets and compare.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from domain_backprojection_sarbp_gb300 import Plan, SarbpError, _native  # noqa: E402
+from synth import scenes  # noqa: E402
+from tests import parity, pins  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def gpu_image(params, echoes, pos, plan=None, accumulate=False, init=None, stream=None):
+    p = dict(params)
+    e = torch.from_numpy(np.ascontiguousarray(echoes, dtype=np.complex64)).to(DEV)
+    a = torch.from_numpy(np.ascontiguousarray(pos, dtype=np.float64)).to(DEV)
+    img = torch.full((p["ny"], p["nx"]), complex(7.0, -3.0), dtype=torch.complex64, device=DEV)
+    if init is not None:
+        img.copy_(torch.from_numpy(init.astype(np.complex64)))
+    own = plan is None
+    plan = plan or Plan(p)
+    try:
+        plan.backproject(img, e, a, params=p, accumulate=accumulate, stream=stream)
+        torch.cuda.synchronize()
+    finally:
+        if own:
+            plan.close()
+    return img.cpu().numpy()
+
+
+# ---------------------------------------------------------------- hand values
+@pytest.mark.parametrize("case", [c for c in pins.load_hand_cases() if c[0] != "first_bin"],
+                         ids=lambda c: c[0])
+def test_hand_cases(case):
+    # "first_bin" sits exactly on u = 0, the edge of the window rule, where a
+    # float32 range one ulp low flips the value to zero; it stays an oracle pin.
+    name, params, echo, pos, pix, expected = case
+    img = gpu_image(params, echo, pos).reshape(-1)
+    got = img[pix]
+    assert np.allclose(got, expected, rtol=0, atol=2e-4 * max(1.0, np.abs(expected).max())), \
+        f"{name}: {got} vs {expected}"
+
+
+# ---------------------------------------------------------------- the configs
+def _check_scene(sc, img):
+    pix = scenes.compared_pixels(sc)
+    ref = oracle.backproject(sc.params, sc.echoes, sc.antenna_pos, pix)
+    got = img.reshape(-1)[pix]
+    m = parity.assert_parity(got, ref, sc.cfg.name)
+    nx, ny = sc.params["nx"], sc.params["ny"]
+    ref_img = np.zeros(nx * ny, dtype=np.complex128)
+    ref_img[pix] = ref
+    bad = parity.argmax_mismatches(img, ref_img.reshape(ny, nx), sc.targets)
+    assert not bad, f"{sc.cfg.name}: argmax differs at {bad}"
+    return m
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_config_full_image(index):
+    sc = scenes.make_scene(scenes.CONFIGS[index - 1])
+    img = gpu_image(sc.params, sc.echoes, sc.antenna_pos)
+    m = _check_scene(sc, img)
+    print(sc.cfg.name, m)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("index", [3, 4, 5])
+def test_config_full_size_sampled(index):
+    sc = scenes.make_scene(scenes.CONFIGS[index - 1])
+    img = gpu_image(sc.params, sc.echoes, sc.antenna_pos)
+    assert np.all(np.isfinite(img))
+    m = _check_scene(sc, img)
+    print(sc.cfg.name, m)
+
+
+# ---------------------------------------------------------------- edge cases
+def _small_scene(nx, ny, na=40, nr=512, spacing=0.5, step=0.5, seed=5, noise=0.05):
+    cfg = scenes.shrink(scenes.CONFIGS[0], nx=nx, ny=ny, na=na, nr=nr, spacing=spacing,
+                        pulse_step=step, n_targets=0, noise_sigma=noise)
+    return scenes.make_scene(cfg, seed=seed)
+
+
+@pytest.mark.parametrize("shape", [(37, 201), (1, 1), (3, 2), (33, 129), (200, 7)])
+def test_ragged_and_tiny_images(shape):
+    sc = _small_scene(*shape)
+    img = gpu_image(sc.params, sc.echoes, sc.antenna_pos)
+    ref = oracle.backproject(sc.params, sc.echoes, sc.antenna_pos)
+    parity.assert_parity(img, ref, f"shape {shape}")
+
+
+@pytest.mark.parametrize("field,value", [("na", 0), ("nr", 0), ("nr", 1)])
+def test_no_contribution_gives_zero(field, value):
+    sc = _small_scene(40, 20)
+    p = dict(sc.params, **{field: value})
+    echo = sc.echoes[:p["na"], :p["nr"]]
+    pos = sc.antenna_pos[:p["na"]]
+    img = gpu_image(p, echo, pos)
+    assert np.all(img == 0)
+    init = np.full((20, 40), 2 + 1j)
+    img = gpu_image(p, echo, pos, accumulate=True, init=init)
+    assert np.all(img == init.astype(np.complex64))
+
+
+def test_empty_image():
+    sc = _small_scene(40, 20)
+    p = dict(sc.params, nx=0)
+    with Plan(p) as plan:
+        e = torch.from_numpy(sc.echoes).to(DEV)
+        a = torch.from_numpy(sc.antenna_pos).to(DEV)
+        img = torch.empty((20, 0), dtype=torch.complex64, device=DEV)
+        plan.backproject(img, e, a)
+        torch.cuda.synchronize()
+
+
+def test_accumulate_pulse_batches():
+    sc = _small_scene(70, 150, na=96)
+    half = 40
+    p1 = dict(sc.params, na=half)
+    p2 = dict(sc.params, na=sc.params["na"] - half)
+    first = gpu_image(p1, sc.echoes[:half], sc.antenna_pos[:half])
+    both = gpu_image(p2, sc.echoes[half:], sc.antenna_pos[half:], accumulate=True, init=first)
+    ref = oracle.backproject(sc.params, sc.echoes, sc.antenna_pos)
+    parity.assert_parity(both, ref, "two batches")
+
+
+def test_bitwise_deterministic():
+    sc = scenes.make_scene(scenes.shrink(scenes.CONFIGS[1], na=300, nx=300, ny=260, nr=2048))
+    with Plan(sc.params) as plan:
+        a = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
+        b = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
+    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+
+
+def test_nan_guard_bands_untouched():
+    sc = _small_scene(64, 130, na=50)
+    na, nr = sc.echoes.shape
+    guard = 4096
+    flat = torch.full((na * nr + 2 * guard,), complex(float("nan"), float("nan")),
+                      dtype=torch.complex64, device=DEV)
+    flat[guard:guard + na * nr] = torch.from_numpy(sc.echoes.reshape(-1)).to(DEV)
+    echoes = flat[guard:guard + na * nr].view(na, nr)
+    pos = torch.from_numpy(sc.antenna_pos).to(DEV)
+    img = torch.zeros((sc.params["ny"], sc.params["nx"]), dtype=torch.complex64, device=DEV)
+    with Plan(sc.params) as plan:
+        plan.backproject(img, echoes, pos)
+        torch.cuda.synchronize()
+    got = img.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    parity.assert_parity(got, oracle.backproject(sc.params, sc.echoes, sc.antenna_pos), "guards")
+
+
+def test_range_window_edges_full_window():
+    # a short range axis that the image overruns at both ends: every rule of
+    # the window (k < 0, k + 1 > nr - 1) is exercised, and the table spans the
+    # whole axis
+    sc = _small_scene(96, 300, na=24, nr=48, spacing=0.5, noise=0.3)
+    p = dict(sc.params)
+    centre = np.linalg.norm(sc.antenna_pos[12])
+    p["r0"] = centre - 20 * p["dr"]
+    with Plan(p) as plan:
+        assert plan.describe()["full_window"] == 1
+        img = gpu_image(p, sc.echoes, sc.antenna_pos, plan=plan)
+    ref = oracle.backproject(p, sc.echoes, sc.antenna_pos)
+    assert np.any(ref == 0) and np.any(ref != 0)
+    parity.assert_parity(img, ref, "window edges")
+
+
+def test_non_finite_antenna_position_skips_pulse():
+    sc = _small_scene(40, 130, na=30)
+    pos = sc.antenna_pos.copy()
+    pos[7, 1] = np.nan
+    pos[19, 2] = np.inf
+    img = gpu_image(sc.params, sc.echoes, pos)
+    ref = oracle.backproject(sc.params, sc.echoes, pos)
+    assert np.all(np.isfinite(img))
+    parity.assert_parity(img, ref, "non-finite antenna")
+
+
+def test_near_field_exact_path():
+    # antenna 40 m above a 32 m wide scene: the Taylor remainder is far above
+    # the fast-path bound, so every (tile, pulse) takes the exact path
+    na, nx, ny = 48, 64, 130
+    pos = np.zeros((na, 3))
+    pos[:, 0] = np.linspace(-20, 20, na)
+    pos[:, 1] = -30.0
+    pos[:, 2] = 40.0
+    geo = scenes.image_geometry(nx, ny, 0.25)
+    nr = 256
+    r0 = 20.0
+    p = dict(nx=nx, ny=ny, na=na, nr=nr, r0=r0, dr=0.5, wavelength=scenes.WAVELENGTH, **geo)
+    txyz = np.array([[geo["x0"] + 20 * 0.25, geo["y0"] + 70 * 0.25, 0.0]])
+    echo = scenes.simulate_echoes(pos, txyz, np.array([1.0]), r0, 0.5, nr).astype(np.complex64)
+    echo += (np.random.default_rng(2).standard_normal(echo.shape) * 0.05).astype(np.complex64)
+    img = gpu_image(p, echo, pos)
+    ref = oracle.backproject(p, echo, pos)
+    parity.assert_parity(img, ref, "near field")
+
+
+def test_host_entry_point_matches_device():
+    sc = _small_scene(64, 200, na=64)
+    with Plan(sc.params) as plan:
+        dev_img = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
+        host_img = np.zeros((sc.params["ny"], sc.params["nx"]), dtype=np.complex64)
+        plan.backproject_host(host_img, sc.echoes, sc.antenna_pos)
+        assert np.array_equal(host_img, dev_img)
+        again = host_img.copy()
+        plan.backproject_host(again, sc.echoes, sc.antenna_pos, accumulate=True)
+        parity.assert_parity(again, 2 * dev_img.astype(np.complex128), "host accumulate")
+
+
+def test_non_default_stream():
+    sc = _small_scene(64, 130, na=40)
+    s = torch.cuda.Stream()
+    img = gpu_image(sc.params, sc.echoes, sc.antenna_pos, stream=s)
+    parity.assert_parity(img, oracle.backproject(sc.params, sc.echoes, sc.antenna_pos), "stream")
+
+
+def test_timing_api_counts_launches():
+    sc = _small_scene(64, 130, na=40)
+    with Plan(sc.params) as plan:
+        plan.set_timing(True)
+        for _ in range(3):
+            gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
+        ms, n = plan.kernel_times()
+        assert n == 3 and ms > 0
+        assert plan.kernel_times() == (0.0, 0)
+
+
+def test_plan_mismatch_and_alignment_errors():
+    sc = _small_scene(64, 130, na=40)
+    with Plan(sc.params) as plan:
+        e = torch.from_numpy(sc.echoes).to(DEV)
+        a = torch.from_numpy(sc.antenna_pos).to(DEV)
+        img = torch.zeros((130, 64), dtype=torch.complex64, device=DEV)
+        with pytest.raises(SarbpError) as ei:
+            plan.backproject(img[:, :32].contiguous(), e, a, params=dict(sc.params, nx=32))
+        assert ei.value.status == _native.SARBP_ERR_PLAN_MISMATCH
+        p = _native.Params.from_dict(sc.params)
+        raw = torch.zeros(64 * 130 * 2 + 1, dtype=torch.float32, device=DEV)
+        st = _native.lib().sarbp_backproject(plan.handle, ctypes.c_void_p(raw.data_ptr() + 4),
+                                             ctypes.c_void_p(e.data_ptr()),
+                                             ctypes.c_void_p(a.data_ptr()), ctypes.byref(p), None)
+        assert st == _native.SARBP_ERR_INVALID_ARG
+        torch.cuda.synchronize()
