@@ -13,12 +13,13 @@ SARBP_ERR_PLAN_MISMATCH = 2
 SARBP_ERR_CUDA = 3
 SARBP_ERR_OOM = 4
 SARBP_ERR_UNSUPPORTED_DEVICE = 5
+SARBP_ERR_SCRATCH_TOO_SMALL = 6
 SARBP_ACCUMULATE = 1
 
 EXPORTS = (
     "sarbp_plan", "sarbp_backproject", "sarbp_backproject_host", "sarbp_destroy",
     "sarbp_status_string", "sarbp_last_error", "sarbp_plan_describe",
-    "sarbp_set_timing", "sarbp_kernel_times",
+    "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
 )
 
 
@@ -60,6 +61,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_backproject.restype = st
     lib.sarbp_backproject_host.argtypes = [vp, vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject_host.restype = st
+    lib.sarbp_backproject_noalloc.argtypes = [vp, vp, vp, P(Params), vp]
+    lib.sarbp_backproject_noalloc.restype = st
     lib.sarbp_destroy.argtypes = [vp]
     lib.sarbp_destroy.restype = st
     lib.sarbp_status_string.argtypes = [st]

@@ -194,6 +194,8 @@ const char* sarbp_status_string(sarbp_status status)
     case SARBP_ERR_CUDA: return "CUDA error";
     case SARBP_ERR_OOM: return "out of memory";
     case SARBP_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case SARBP_ERR_SCRATCH_TOO_SMALL:
+        return "problem exceeds the 16 MiB fixed scratch of sarbp_backproject_noalloc";
     }
     return "unknown status";
 }
@@ -485,6 +487,111 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMemcpyAsync (to host)");
+    return SARBP_OK;
+}
+
+// No-allocation variant: the table and window starts of one chunk of pulses
+// live in a fixed device array; every CTA owns whole tiles, so no partial-sum
+// buffer is needed.
+sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
+                                       const double* antenna_pos, const sarbp_params* params,
+                                       void* stream)
+{
+    if (!params)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels > 0 && (!image || !aligned8(image)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && (!antenna_pos || !aligned8(antenna_pos)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && params->nr > 0 && (!echoes || !aligned8(echoes)))
+        return SARBP_ERR_INVALID_ARG;
+
+    // the geometry a plan would fix, computed locally (nothing is stored)
+    sarbp_plan_s geo;
+    geo.p = *params;
+    geo.tiles_x = (params->nx + TILE_X - 1) / TILE_X;
+    geo.tiles_y = (params->ny + TILE_Y - 1) / TILE_Y;
+    geo.tiles = geo.tiles_x * geo.tiles_y;
+    const double ext_x = ((double)geo.tiles_x * TILE_X - 1.0) * params->dx;
+    const double ext_y = ((double)geo.tiles_y * TILE_Y - 1.0) * params->dy;
+    const double diag = std::sqrt(ext_x * ext_x + ext_y * ext_y);
+    const double w_geom =
+        std::ceil((diag + 2.0 * tile_qmax(params->dx, params->dy)) / params->dr) + 2 * MARGIN + 6;
+    const long long w_full = (long long)params->nr + 2 * MARGIN + 8;
+    geo.full_window = w_geom < (double)w_full ? 0 : 1;
+    const double w_any = geo.full_window ? (double)w_full : w_geom;
+    // rows are (W x 16 B); the window starts take 4 B per pulse
+    const double pad_bytes = 2.0 * TABLE_PAD * sizeof(float4) + 256.0;
+    const double row_bytes = (std::ceil(w_any / 4.0) * 4.0) * sizeof(float4) + sizeof(int);
+    if (pixels > 0 && params->na > 0 && params->nr >= 2 &&
+        row_bytes + pad_bytes > (double)NOALLOC_SCRATCH_BYTES)
+        return SARBP_ERR_SCRATCH_TOO_SMALL;
+    geo.W = ((int)w_any + 3) & ~3;
+
+    int dev = -1, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess)
+        return SARBP_ERR_CUDA;
+    if (major != 10 || minor != 3)
+        return SARBP_ERR_UNSUPPORTED_DEVICE;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pixels == 0)
+        return SARBP_OK;
+    if (params->na == 0 || params->nr < 2) {
+        if (!(params->flags & SARBP_ACCUMULATE) &&
+            cudaMemsetAsync(image, 0, (size_t)pixels * 8, s) != cudaSuccess)
+            return SARBP_ERR_CUDA;
+        return SARBP_OK;
+    }
+
+    void* scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess)
+        return SARBP_ERR_CUDA;
+    const size_t entry_bytes = (size_t)geo.W * sizeof(float4) + sizeof(int);
+    const size_t usable = NOALLOC_SCRATCH_BYTES - (size_t)pad_bytes;
+    const int chunk = (int)std::min<size_t>((size_t)params->na, usable / entry_bytes);
+    // layout: [window starts, 256-B aligned][pad][chunk rows][pad]
+    const size_t klo_bytes = (((size_t)chunk * sizeof(int)) + 255) & ~size_t(255);
+    int* klo = static_cast<int*>(scratch);
+    float4* table_alloc = reinterpret_cast<float4*>(static_cast<unsigned char*>(scratch) + klo_bytes);
+    float4* table = table_alloc + TABLE_PAD;
+    // the pads are never written by the kernels and must read as zero
+    if (cudaMemsetAsync(table_alloc, 0, TABLE_PAD * sizeof(float4), s) != cudaSuccess ||
+        cudaMemsetAsync(table + (size_t)chunk * geo.W, 0, TABLE_PAD * sizeof(float4), s) !=
+            cudaSuccess)
+        return SARBP_ERR_CUDA;
+
+    const float2* ech = static_cast<const float2*>(echoes);
+    for (int c0 = 0; c0 < params->na; c0 += chunk) {
+        const int cn = std::min(chunk, params->na - c0);
+        sarbp_params pc = *params;
+        pc.na = cn;
+        if (c0 > 0)
+            pc.flags |= SARBP_ACCUMULATE;
+        geo.p = pc;
+        BpConst k = make_const(&geo, &pc);
+        k.ctas = geo.tiles;                     // one whole tile per CTA: direct writes only
+        k.units = (long long)geo.tiles * cn;
+        e = launch_table(k, ech + (size_t)c0 * params->nr, antenna_pos + 3 * (size_t)c0, table,
+                         klo, s);
+        if (e == cudaSuccess)
+            e = launch_backproject(k, antenna_pos + 3 * (size_t)c0, table, klo,
+                                   static_cast<float2*>(image), nullptr, s);
+        if (e != cudaSuccess)
+            return SARBP_ERR_CUDA;
+    }
     return SARBP_OK;
 }
 

@@ -52,4 +52,9 @@ cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);
 
+// Device address of the fixed scratch array used by sarbp_backproject_noalloc
+// (looked up once per device, with that device current).
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(16) << 20;
+cudaError_t noalloc_scratch(void** ptr);
+
 }  // namespace sarbp

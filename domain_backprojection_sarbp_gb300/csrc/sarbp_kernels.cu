@@ -37,6 +37,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 namespace sarbp {
 namespace {
@@ -409,7 +410,37 @@ __global__ void __launch_bounds__(THREADS) reduce_kernel(BpConst k, const float4
     }
 }
 
+// Scratch of sarbp_backproject_noalloc: window starts and echo-table rows of
+// one chunk of pulses. Every GPU that loads the library holds it until exit.
+static __device__ __align__(256) unsigned char noalloc_scratch_array[NOALLOC_SCRATCH_BYTES];
+
 }  // namespace
+
+cudaError_t noalloc_scratch(void** ptr)
+{
+    // The symbol's name is only a host-side stand-in; kernels need the device
+    // address, looked up once per device and cached.
+    constexpr int MAX_CACHED_DEVICES = 64;
+    static std::mutex mu;
+    static void* cached[MAX_CACHED_DEVICES] = {};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < MAX_CACHED_DEVICES && cached[dev]) {
+        *ptr = cached[dev];
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, noalloc_scratch_array);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < MAX_CACHED_DEVICES)
+        cached[dev] = p;
+    *ptr = p;
+    return cudaSuccess;
+}
 
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
                          int* klo, cudaStream_t s)

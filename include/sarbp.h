@@ -58,7 +58,9 @@ typedef enum sarbp_status {
     SARBP_ERR_PLAN_MISMATCH = 2,      /* params disagree with the plan's fixed fields     */
     SARBP_ERR_CUDA = 3,               /* a CUDA call failed; see sarbp_last_error         */
     SARBP_ERR_OOM = 4,                /* device or host allocation failed                 */
-    SARBP_ERR_UNSUPPORTED_DEVICE = 5  /* current device is not compute capability 10.3    */
+    SARBP_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3    */
+    SARBP_ERR_SCRATCH_TOO_SMALL = 6   /* one pulse's table row exceeds the fixed scratch
+                                         of sarbp_backproject_noalloc                    */
 } sarbp_status;
 
 /* params.flags */
@@ -166,6 +168,41 @@ sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out);
  */
 sarbp_status sarbp_set_timing(sarbp_plan_t plan, int enable);
 sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* launches);
+
+/*
+ * sarbp_backproject_noalloc - the same backprojection without any device
+ * memory allocation. The page has no counterpart: this is an interface for
+ * callers that cannot allocate GPU memory themselves, for example a plug-in
+ * that is only handed buffers by its host application, a framework whose
+ * memory pool owns the whole device, or a real-time radar loop that forbids
+ * cudaMalloc (it synchronises the device and has unbounded latency) once
+ * processing has started. Such callers cannot create a plan either.
+ *
+ * image, echoes, antenna_pos, params, stream: as for sarbp_backproject. All
+ * sizes come from params; no plan is involved.
+ *
+ * Scratch: a fixed, file-scope device array of SARBP_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU loading the library holds until the process exits.
+ * Pulses are processed in chunks whose echo-table rows fit in it, so the
+ * pulse sum is grouped differently from sarbp_backproject and results agree
+ * to float32 rounding, not bitwise. Problems where a single pulse's table row
+ * (about (image range extent / dr) x 16 bytes) does not fit are rejected with
+ * SARBP_ERR_SCRATCH_TOO_SMALL before any work is queued.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * All calls share the one array and it keeps the last call's contents; the
+ * parts that must start at zero are cleared by each call. Calls whose work
+ * overlaps on the GPU (for example on two streams, or from two threads) race
+ * on the array: serialise them.
+ */
+#define SARBP_NOALLOC_SCRATCH_BYTES (16u << 20)
+sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
+                                       const double* antenna_pos, const sarbp_params* params,
+                                       void* stream);
 
 #ifdef __cplusplus
 }
