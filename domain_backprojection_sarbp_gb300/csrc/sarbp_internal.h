@@ -9,8 +9,18 @@ namespace sarbp {
 
 // Work tile: one thread owns TILE_X consecutive pixels of one image row; the
 // 32 lanes of a warp own 32 consecutive rows; WARPS warps stack vertically.
-constexpr int TILE_X = 32;
-constexpr int WARPS = 4;
+#ifndef SARBP_TILE_X
+#define SARBP_TILE_X 32
+#endif
+#ifndef SARBP_WARPS
+#define SARBP_WARPS 8
+#endif
+#ifndef SARBP_MIN_BLOCKS
+#define SARBP_MIN_BLOCKS 2
+#endif
+constexpr int TILE_X = SARBP_TILE_X;
+constexpr int WARPS = SARBP_WARPS;
+constexpr int MIN_BLOCKS = SARBP_MIN_BLOCKS;   // resident CTAs per SM the register budget targets
 constexpr int THREADS = 32 * WARPS;
 constexpr int TILE_Y = 32 * WARPS;
 constexpr int TILE_PIX = TILE_X * TILE_Y;
@@ -42,6 +52,7 @@ struct BpConst {
     float c_phase;               // 2 pi * 2 dr / lambda: phase per bin, radians
     float inv_c;                 // 1 / c_phase
     float dx_f, dy_f, inv_dr_f;
+    float rot_re, rot_im;        // exp(-j c_phase): phase step from one bin to the next
 };
 
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos,

@@ -27,7 +27,8 @@
 //    polynomial to a quadratic in its column offset (a split float for the
 //    large linear term keeps 2^-22-bin accuracy), and each update costs two
 //    FMAs for u. Pulses where the remainder bound exceeds 5e-5 rad of phase
-//    (near field, huge tiles) take an exact float32 path instead.
+//    (near field, very fine bins) take an exact path instead (float64 range
+//    per row, float32 difference across the row).
 //
 // 3. Work split (stream-K). The (tile, pulse) units are cut into one equal,
 //    contiguous range per resident CTA. A tile covered by one CTA is written
@@ -49,8 +50,7 @@ struct __align__(16) Record {
     float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
     float4 b;  // c03, c04, c10, c11
     float4 c;  // c12, c13, c20, c21
-    float4 d;  // c22, unused, kbase (int bits), kind (int bits)
-    float4 e;  // exact path: 2 vx, 2 vy, R_t, R_t^2
+    float4 d;  // c22, row index of bin 0 (int bits), kbase (int bits), kind (int bits)
 };
 
 // ---------------------------------------------------------------------------
@@ -130,7 +130,8 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
     const double r = sqrt(r2);
     int kind = REC_SKIP;
     Record rec;
-    rec.a = rec.b = rec.c = rec.d = rec.e = make_float4(0.f, 0.f, 0.f, 0.f);
+    rec.a = rec.b = rec.c = rec.d = make_float4(0.f, 0.f, 0.f, 0.f);
+    rec.d.y = __int_as_float(-lo);
     if (lo != KLO_INVALID && isfinite(r)) {
         const double u = (r - k.r0) * k.inv_dr;
         const double umin = (r - k.qmax - k.r0) * k.inv_dr - 1e-6;
@@ -162,7 +163,6 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             const double c20 = mxx * h2 * dx * dx * idr;
             const double c11 = 2.0 * mxy * h2 * dx * dy * idr;
             const double c02 = myy * h2 * dy * dy * idr;
-            const double c30 = h3 * gx * mxx * dx * dx * dx * idr;
             const double c21 = h3 * (2.0 * gx * mxy + gy * mxx) * dx * dx * dy * idr;
             const double c12 = h3 * (gx * myy + 2.0 * gy * mxy) * dx * dy * dy * idr;
             const double c03 = h3 * gy * myy * dy * dy * dy * idr;
@@ -191,8 +191,7 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), f32(c02));
             rec.b = make_float4(f32(c03), f32(c04), f32(c10), f32(c11));
             rec.c = make_float4(f32(c12), f32(c13), f32(c20), f32(c21));
-            rec.d = make_float4(f32(c22), 0.f, __int_as_float((int)kb), 0.f);
-            rec.e = make_float4(f32(2.0 * vx), f32(2.0 * vy), f32(r), f32(r2));
+            rec.d = make_float4(f32(c22), __int_as_float(-lo), __int_as_float((int)kb), 0.f);
         }
     }
     rec.d.w = __int_as_float(kind);
@@ -200,63 +199,177 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
 }
 
 // ---------------------------------------------------------------------------
-// Updates of one pulse for the 32 pixels a thread owns.
+// Updates of one pulse for the TILE_X pixels a thread owns.
+//
+// Pixels are handled in pairs (q, q + NP), NP = TILE_X / 2, as float2 values so
+// that the range polynomial, the floor, the fraction, the phase scaling and
+// the complex multiply-accumulate issue as packed f32x2 instructions.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void fast_pulse(const BpConst& k, const Record& rec, const float4* row,
-                                           float jf, float jf2, float jf3, float jf4,
-                                           float (&acc_re)[TILE_X], float (&acc_im)[TILE_X])
+constexpr int NP = TILE_X / 2;
+
+// What one pulse needs, built one pulse ahead of its use.
+enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3 };
+
+struct FastState {
+    float e0, e1, e2;             // u(i) = e0 + i e1 + i^2 e2, bins, relative to the row index kb
+    float v0;                     // e0 - k0: u(0) relative to the thread's first bin k0 (hinge)
+    unsigned long long base;      // row pointer + (kb - magic bias) entries, in bytes (gather)
+    float4 t0, t1;                // table entries k0 and k0 + 1 (hinge)
+    int mode;
+};
+
+__device__ __forceinline__ FastState fast_setup(const BpConst& k, const Record& rec, const float4* row,
+                                                float jf, float jf2, float jf3, float jf4)
 {
     // u(i) = E0 + i E1 + i^2 E2 for this thread's row j; the large c01 j term
-    // is split into an integer (folded into the row pointer) and a fraction
-    const float hi = rec.a.y * jf;
-    float lo = fmaf(rec.a.y, jf, -hi);
-    lo = fmaf(rec.a.z, jf, lo);
-    const float small = fmaf(rec.b.y, jf4, fmaf(rec.b.x, jf3, fmaf(rec.a.w, jf2, rec.a.x + lo)));
+    // is split into an integer (folded into the row index) and a fraction
+    const float4 ra = rec.a, rb = rec.b, rc = rec.c, rd = rec.d;
+    const float hi = ra.y * jf;
+    float lo = fmaf(ra.y, jf, -hi);
+    lo = fmaf(ra.z, jf, lo);
+    const float small = fmaf(rb.y, jf4, fmaf(rb.x, jf3, fmaf(ra.w, jf2, ra.x + lo)));
     const float t = hi + MAGIC;
     const float hir = t - MAGIC;
-    const float e0 = (hi - hir) + small;
-    const int shift = __float_as_int(t) - MAGIC_BITS;
-    const float e1 = fmaf(rec.c.y, jf3, fmaf(rec.c.x, jf2, fmaf(rec.b.w, jf, rec.b.z)));
-    const float e2 = fmaf(rec.d.x, jf2, fmaf(rec.c.w, jf, rec.c.z));
-    const int kbase = __float_as_int(rec.d.z);
-    const unsigned long long base =
-        reinterpret_cast<unsigned long long>(row + kbase + shift) - (unsigned long long)MAGIC_BITS * 16ull;
-    const float c_phase = k.c_phase;
+    FastState st;
+    st.e0 = (hi - hir) + small;
+    st.e1 = fmaf(rc.y, jf3, fmaf(rc.x, jf2, fmaf(rb.w, jf, rb.z)));
+    st.e2 = fmaf(rd.x, jf2, fmaf(rc.w, jf, rc.z));
+    const int kb = __float_as_int(rd.z) + (__float_as_int(t) - MAGIC_BITS);
+    st.base = reinterpret_cast<unsigned long long>(row) +
+              (unsigned long long)(long long)(kb - MAGIC_BITS) * 16ull;
+    const int kind = __float_as_int(rd.w);
+
+    // Bounds of u over the thread's pixels; when they span less than one bin,
+    // every pixel lies in bin k0 or k0 + 1 and two table entries serve all.
+    constexpr float half = 0.5f * (TILE_X - 1);
+    const float lo_u = st.e0 - half * fabsf(st.e1) - half * half * fmaxf(-st.e2, 0.0f);
+    const float hi_u = st.e0 + half * fabsf(st.e1) + half * half * fmaxf(st.e2, 0.0f);
+    const float tk = __fadd_rd(lo_u, MAGIC);
+    const float k0 = tk - MAGIC;
+    const int idx0 = kb + (__float_as_int(tk) - MAGIC_BITS);
+    const int bin0 = __float_as_int(rd.y);               // row index of absolute bin 0
+    // both bins must hold recorded samples: the identity behind the hinge
+    // form does not hold across the zero entries outside 0 <= k <= nr - 2
+    const bool hinge = kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
+                       idx0 + 1 <= bin0 + k.nr - 2;
+    st.v0 = st.e0 - k0;
+    st.t0 = st.t1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (hinge) {
+        st.t0 = __ldg(row + idx0);
+        st.t1 = __ldg(row + idx0 + 1);
+    }
+    st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
+                               : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
+    return st;
+}
+
+// All pixels in bins k0, k0 + 1. With v = u - k0 in [0, 2), x = c v and
+// h = max(x - c, 0), the interpolated, phase-compensated sample is
+//   exp(j x) [A + x D + h G],  A = t0.A,  D = t0.D,  G = exp(-j c) t1.D - t0.D
+// (the linear interpolant over the two bins written as one line plus a hinge).
+__device__ __forceinline__ void hinge_pulse(const BpConst& k, const FastState& st,
+                                            float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float c = k.c_phase;
+    const float gre = k.rot_re * st.t1.z - k.rot_im * st.t1.w - st.t0.z;
+    const float gim = k.rot_re * st.t1.w + k.rot_im * st.t1.z - st.t0.w;
+    const float2 pc0 = make_float2(c * st.v0, c * st.v0);
+    const float2 pc1 = make_float2(c * st.e1, c * st.e1);
+    const float2 pc2 = make_float2(c * st.e2, c * st.e2);
+    const float2 are = make_float2(st.t0.x, st.t0.x), aim = make_float2(st.t0.y, st.t0.y);
+    const float2 dre = make_float2(st.t0.z, st.t0.z), dim = make_float2(st.t0.w, st.t0.w);
+    const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
+    const float2 negc = make_float2(-c, -c);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float i0 = -0.5f * (TILE_X - 1);
 #pragma unroll
-    for (int m = 0; m < TILE_X; ++m) {
-        const float i = (float)m - 0.5f * (TILE_X - 1);
-        const float ub = fmaf(i, fmaf(i, e2, e1), e0);
-        const float tt = __fadd_rd(ub, MAGIC);
-        const float f = ub - (tt - MAGIC);
-        const float x = f * c_phase;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(
-            base + (unsigned long long)(unsigned)__float_as_int(tt) * 16ull));
-        const float wr = fmaf(x, v.z, v.x);
-        const float wi = fmaf(x, v.w, v.y);
-        float s, c;
-        __sincosf(x, &s, &c);
-        acc_re[m] = fmaf(wr, c, fmaf(-wi, s, acc_re[m]));
-        acc_im[m] = fmaf(wr, s, fmaf(wi, c, acc_im[m]));
+    for (int q = 0; q < NP; ++q) {
+        const float2 id = make_float2(i0 + q, i0 + q + NP);
+        const float2 x = __ffma2_rn(id, __ffma2_rn(id, pc2, pc1), pc0);
+        float2 h = __fadd2_rn(x, negc);
+        h.x = fmaxf(h.x, 0.0f);
+        h.y = fmaxf(h.y, 0.0f);
+        const float2 wr = __ffma2_rn(h, g_re, __ffma2_rn(x, dre, are));
+        const float2 wi = __ffma2_rn(h, g_im, __ffma2_rn(x, dim, aim));
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, cs, accre[q]);
+        accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, cs, accim[q]));
+        accre[q] = __ffma2_rn(__fmul2_rn(wi, sn), neg1, accre[q]);
     }
 }
 
-__device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec, const float4* row,
-                                         float jf, float (&acc_re)[TILE_X], float (&acc_im)[TILE_X])
+__device__ __forceinline__ float4 gather(unsigned long long base, float biased_index)
 {
-    // |p - a|^2 = R_t^2 + s with s = 2 v.q + |q|^2, and R - R_t = s / (R_t + R)
-    const float two_vx = rec.e.x, two_vy = rec.e.y, rt = rec.e.z, rt2 = rec.e.w;
-    const float qy = jf * k.dy_f;
-    const float sy = qy * (two_vy + qy);
-    const int kbase = __float_as_int(rec.d.z);
+    return __ldg(reinterpret_cast<const float4*>(
+        base + (unsigned long long)(unsigned)__float_as_int(biased_index) * 16ull));
+}
+
+// General case: one gather per pixel.
+__device__ __forceinline__ void gather_pulse(const FastState& st, float c_phase,
+                                             float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float2 mm = make_float2(MAGIC, MAGIC);
+    const float2 nmm = make_float2(-MAGIC, -MAGIC);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float2 cc = make_float2(c_phase, c_phase);
+    const float2 p0 = make_float2(st.e0, st.e0);
+    const float2 p1 = make_float2(st.e1, st.e1);
+    const float2 p2 = make_float2(st.e2, st.e2);
+    const float i0 = -0.5f * (TILE_X - 1);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float2 id = make_float2(i0 + q, i0 + q + NP);
+        const float2 u = __ffma2_rn(id, __ffma2_rn(id, p2, p1), p0);
+        const float2 tt = __fadd2_rd(u, mm);        // floor(u) + MAGIC: the index in the mantissa
+        const float2 fl = __fadd2_rn(tt, nmm);      // floor(u), exact
+        const float2 f = __ffma2_rn(fl, neg1, u);   // u - floor(u), exact
+        const float2 x = __fmul2_rn(f, cc);         // phase inside the bin, radians
+        const float4 va = gather(st.base, tt.x);
+        const float4 vb = gather(st.base, tt.y);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 wr = make_float2(fmaf(x.x, va.z, va.x), fmaf(x.y, vb.z, vb.x));
+        const float2 wi = make_float2(fmaf(x.x, va.w, va.y), fmaf(x.y, vb.w, vb.y));
+        const float2 c = make_float2(ca, cb);
+        const float2 s = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, c, accre[q]);
+        accim[q] = __ffma2_rn(wr, s, __ffma2_rn(wi, c, accim[q]));
+        accre[q] = __ffma2_rn(__fmul2_rn(wi, s), neg1, accre[q]);
+    }
+}
+
+// Fallback when the tile polynomial is not accurate enough (near field, very
+// fine range bins): a float64 range to the centre of the thread's own row,
+// then R - R_row = s / (R_row + R), s = 2 v.q + |q|^2, in float32 over the
+// row's +-15.5 pixels, with explicit bounds on every table index.
+__device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec, const float4* row,
+                                            const double* __restrict__ a, double xc, double yrow,
+                                            float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const double vx = xc - a[0], vy = yrow - a[1], vz = k.z0 - a[2];
+    const double r2 = vx * vx + vy * vy + vz * vz;
+    const double r = sqrt(r2);
+    const double u = (r - k.r0) * k.inv_dr;
+    if (!(fabs(u) < 1.0e9))
+        return;
+    const double ku = floor(u);
+    const int kbase = (int)ku + __float_as_int(rec.d.y);  // row index of the bin below u(0)
+    const float frac0 = (float)(u - ku);
+    const float two_vx = (float)(2.0 * vx), rf = (float)r, r2f = (float)r2;
     const float c_phase = k.c_phase;
 #pragma unroll
     for (int m = 0; m < TILE_X; ++m) {
         const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
-        const float s = fmaf(qx, two_vx + qx, sy);
-        const float rp = sqrtf(fmaxf(rt2 + s, 0.0f));
-        const float den = rt + rp;
+        const float s = qx * (two_vx + qx);
+        const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
+        const float den = rf + rp;
         const float dr_m = den > 0.0f ? s / den : 0.0f;
-        const float ub = fmaf(dr_m, k.inv_dr_f, rec.a.x);
+        const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
         if (!(ub > -1.0e6f && ub < 1.0e6f))
             continue;
         const float kf = floorf(ub);
@@ -269,8 +382,10 @@ __device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec,
         const float wi = fmaf(x, v.w, v.y);
         float sn, cs;
         __sincosf(x, &sn, &cs);
-        acc_re[m] = fmaf(wr, cs, fmaf(-wi, sn, acc_re[m]));
-        acc_im[m] = fmaf(wr, sn, fmaf(wi, cs, acc_im[m]));
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        re = fmaf(wr, cs, fmaf(-wi, sn, re));
+        im = fmaf(wr, sn, fmaf(wi, cs, im));
     }
 }
 
@@ -282,7 +397,7 @@ __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
 // ---------------------------------------------------------------------------
 // Main kernel: persistent, one contiguous range of (tile, pulse) units per CTA.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double* __restrict__ pos,
+__global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, const double* __restrict__ pos,
                                                         const float4* __restrict__ table,
                                                         const int* __restrict__ klo,
                                                         float2* __restrict__ image,
@@ -311,11 +426,12 @@ __global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double*
         const double xc = k.x0 + ((double)col0 + 0.5 * (TILE_X - 1)) * k.dx;
         const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
 
-        float acc_re[TILE_X], acc_im[TILE_X];
+        const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
+        float2 accre[NP], accim[NP];
 #pragma unroll
-        for (int m = 0; m < TILE_X; ++m) {
-            acc_re[m] = 0.f;
-            acc_im[m] = 0.f;
+        for (int q = 0; q < NP; ++q) {
+            accre[q] = make_float2(0.f, 0.f);
+            accim[q] = make_float2(0.f, 0.f);
         }
 
         for (int c0 = n0; c0 < n1; c0 += CHUNK) {
@@ -324,15 +440,23 @@ __global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double*
             if (tid < cnt)
                 make_record(k, pos, klo, c0 + tid, xc, yc, s_rec[tid]);
             __syncthreads();
+            const float4* rows = table + (size_t)c0 * k.W;
+            FastState cur = fast_setup(k, s_rec[0], rows, jf, jf2, jf3, jf4);
 #pragma unroll 1
             for (int p = 0; p < cnt; ++p) {
-                const Record rec = s_rec[p];
-                const int kind = __float_as_int(rec.d.w);
-                const float4* row = table + (size_t)(c0 + p) * k.W;
-                if (kind == REC_FAST)
-                    fast_pulse(k, rec, row, jf, jf2, jf3, jf4, acc_re, acc_im);
-                else if (kind == REC_EXACT)
-                    exact_pulse(k, rec, row, jf, acc_re, acc_im);
+                // the next pulse's state is built here so that its latency
+                // overlaps this pulse's updates
+                const int pn = min(p + 1, cnt - 1);
+                const FastState nxt =
+                    fast_setup(k, s_rec[pn], rows + (size_t)pn * k.W, jf, jf2, jf3, jf4);
+                if (cur.mode == MODE_HINGE)
+                    hinge_pulse(k, cur, accre, accim);
+                else if (cur.mode == MODE_GATHER)
+                    gather_pulse(cur, k.c_phase, accre, accim);
+                else if (cur.mode == MODE_EXACT)
+                    exact_pulse(k, s_rec[p], rows + (size_t)p * k.W, pos + 3 * (size_t)(c0 + p), xc,
+                                yrow, accre, accim);
+                cur = nxt;
             }
         }
 
@@ -345,7 +469,9 @@ __global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double*
                 for (int m = 0; m < TILE_X; ++m) {
                     const int col = col0 + m;
                     if (col < k.nx) {
-                        float2 v = make_float2(acc_re[m], acc_im[m]);
+                        const int q = m % NP;
+                        float2 v = (m < NP) ? make_float2(accre[q].x, accim[q].x)
+                                            : make_float2(accre[q].y, accim[q].y);
                         if (acc) {
                             const float2 o = dst[col];
                             v.x += o.x;
@@ -359,8 +485,14 @@ __global__ void __launch_bounds__(THREADS, 4) bp_kernel(BpConst k, const double*
             const int slot = (t == t_first) ? 0 : 1;
             float4* dst = partial + ((size_t)(b * 2 + slot) * TILE_PIX + (size_t)jr * TILE_X) / 2;
 #pragma unroll
-            for (int m = 0; m < TILE_X; m += 2)
-                dst[m / 2] = make_float4(acc_re[m], acc_im[m], acc_re[m + 1], acc_im[m + 1]);
+            for (int m = 0; m < TILE_X; m += 2) {
+                const int q0 = m % NP, q1 = (m + 1) % NP;
+                const float2 v0 = (m < NP) ? make_float2(accre[q0].x, accim[q0].x)
+                                           : make_float2(accre[q0].y, accim[q0].y);
+                const float2 v1 = (m + 1 < NP) ? make_float2(accre[q1].x, accim[q1].x)
+                                               : make_float2(accre[q1].y, accim[q1].y);
+                dst[m / 2] = make_float4(v0.x, v0.y, v1.x, v1.y);
+            }
         }
     }
 }
