@@ -148,6 +148,7 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     const double turns = alpha - std::floor(alpha);      // exp(-j c) = exp(-j 2 pi frac(alpha))
     k.rot_re = (float)std::cos(2.0 * PI * turns);
     k.rot_im = (float)-std::sin(2.0 * PI * turns);
+    k.i0 = -0.5f * (float)(TILE_X - 1);
     k.dx_f = (float)p->dx;
     k.dy_f = (float)p->dy;
     k.inv_dr_f = (float)(1.0 / p->dr);

@@ -53,6 +53,7 @@ struct BpConst {
     float inv_c;                 // 1 / c_phase
     float dx_f, dy_f, inv_dr_f;
     float rot_re, rot_im;        // exp(-j c_phase): phase step from one bin to the next
+    float i0;                    // column offset of a thread's first pixel from the tile centre
 };
 
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos,

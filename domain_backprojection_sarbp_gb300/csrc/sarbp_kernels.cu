@@ -207,19 +207,21 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
 // ---------------------------------------------------------------------------
 constexpr int NP = TILE_X / 2;
 
-// What one pulse needs, built one pulse ahead of its use.
+// What one pulse needs, built one pulse ahead of its use. Nothing here waits
+// on the two table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3 };
 
-struct FastState {
-    float e0, e1, e2;             // u(i) = e0 + i e1 + i^2 e2, bins, relative to the row index kb
-    float v0;                     // e0 - k0: u(0) relative to the thread's first bin k0 (hinge)
-    unsigned long long base;      // row pointer + (kb - magic bias) entries, in bytes (gather)
-    float4 t0, t1;                // table entries k0 and k0 + 1 (hinge)
+struct PulseState {
+    float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; gather: e0, e1, e2 (both halves)
+    float4 t0;                    // hinge: table entry k0
+    float2 t1d;                   // hinge: D part of entry k0 + 1
+    unsigned long long base;      // gather: row pointer + (kb - magic bias) entries, in bytes
     int mode;
 };
 
-__device__ __forceinline__ FastState fast_setup(const BpConst& k, const Record& rec, const float4* row,
-                                                float jf, float jf2, float jf3, float jf4)
+__device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record& rec,
+                                                  const float4* row, float jf, float jf2,
+                                                  float jf3, float jf4)
 {
     // u(i) = E0 + i E1 + i^2 E2 for this thread's row j; the large c01 j term
     // is split into an integer (folded into the row index) and a fraction
@@ -230,20 +232,17 @@ __device__ __forceinline__ FastState fast_setup(const BpConst& k, const Record& 
     const float small = fmaf(rb.y, jf4, fmaf(rb.x, jf3, fmaf(ra.w, jf2, ra.x + lo)));
     const float t = hi + MAGIC;
     const float hir = t - MAGIC;
-    FastState st;
-    st.e0 = (hi - hir) + small;
-    st.e1 = fmaf(rc.y, jf3, fmaf(rc.x, jf2, fmaf(rb.w, jf, rb.z)));
-    st.e2 = fmaf(rd.x, jf2, fmaf(rc.w, jf, rc.z));
+    const float e0 = (hi - hir) + small;
+    const float e1 = fmaf(rc.y, jf3, fmaf(rc.x, jf2, fmaf(rb.w, jf, rb.z)));
+    const float e2 = fmaf(rd.x, jf2, fmaf(rc.w, jf, rc.z));
     const int kb = __float_as_int(rd.z) + (__float_as_int(t) - MAGIC_BITS);
-    st.base = reinterpret_cast<unsigned long long>(row) +
-              (unsigned long long)(long long)(kb - MAGIC_BITS) * 16ull;
     const int kind = __float_as_int(rd.w);
 
     // Bounds of u over the thread's pixels; when they span less than one bin,
     // every pixel lies in bin k0 or k0 + 1 and two table entries serve all.
     constexpr float half = 0.5f * (TILE_X - 1);
-    const float lo_u = st.e0 - half * fabsf(st.e1) - half * half * fmaxf(-st.e2, 0.0f);
-    const float hi_u = st.e0 + half * fabsf(st.e1) + half * half * fmaxf(st.e2, 0.0f);
+    const float lo_u = e0 - half * fabsf(e1) - half * half * fmaxf(-e2, 0.0f);
+    const float hi_u = e0 + half * fabsf(e1) + half * half * fmaxf(e2, 0.0f);
     const float tk = __fadd_rd(lo_u, MAGIC);
     const float k0 = tk - MAGIC;
     const int idx0 = kb + (__float_as_int(tk) - MAGIC_BITS);
@@ -252,14 +251,27 @@ __device__ __forceinline__ FastState fast_setup(const BpConst& k, const Record& 
     // form does not hold across the zero entries outside 0 <= k <= nr - 2
     const bool hinge = kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
                        idx0 + 1 <= bin0 + k.nr - 2;
-    st.v0 = st.e0 - k0;
-    st.t0 = st.t1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (hinge) {
-        st.t0 = __ldg(row + idx0);
-        st.t1 = __ldg(row + idx0 + 1);
-    }
+    PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
+    st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    st.t1d = make_float2(0.f, 0.f);
+    if (hinge) {
+        st.t0 = __ldg(row + idx0);
+        const float4 t1 = __ldg(row + idx0 + 1);
+        st.t1d = make_float2(t1.z, t1.w);
+        const float c = k.c_phase;
+        const float v0 = c * (e0 - k0), w1 = c * e1, w2 = c * e2;
+        st.q0 = make_float2(v0, v0);
+        st.q1 = make_float2(w1, w1);
+        st.q2 = make_float2(w2, w2);
+    } else {
+        st.q0 = make_float2(e0, e0);
+        st.q1 = make_float2(e1, e1);
+        st.q2 = make_float2(e2, e2);
+    }
+    st.base = reinterpret_cast<unsigned long long>(row) +
+              (unsigned long long)(long long)(kb - MAGIC_BITS) * 16ull;
     return st;
 }
 
@@ -267,25 +279,22 @@ __device__ __forceinline__ FastState fast_setup(const BpConst& k, const Record& 
 // h = max(x - c, 0), the interpolated, phase-compensated sample is
 //   exp(j x) [A + x D + h G],  A = t0.A,  D = t0.D,  G = exp(-j c) t1.D - t0.D
 // (the linear interpolant over the two bins written as one line plus a hinge).
-__device__ __forceinline__ void hinge_pulse(const BpConst& k, const FastState& st,
+__device__ __forceinline__ void hinge_pulse(const BpConst& k, const PulseState& st,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const float c = k.c_phase;
-    const float gre = k.rot_re * st.t1.z - k.rot_im * st.t1.w - st.t0.z;
-    const float gim = k.rot_re * st.t1.w + k.rot_im * st.t1.z - st.t0.w;
-    const float2 pc0 = make_float2(c * st.v0, c * st.v0);
-    const float2 pc1 = make_float2(c * st.e1, c * st.e1);
-    const float2 pc2 = make_float2(c * st.e2, c * st.e2);
+    const float gre = k.rot_re * st.t1d.x - k.rot_im * st.t1d.y - st.t0.z;
+    const float gim = k.rot_re * st.t1d.y + k.rot_im * st.t1d.x - st.t0.w;
     const float2 are = make_float2(st.t0.x, st.t0.x), aim = make_float2(st.t0.y, st.t0.y);
     const float2 dre = make_float2(st.t0.z, st.t0.z), dim = make_float2(st.t0.w, st.t0.w);
     const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
-    const float2 negc = make_float2(-c, -c);
+    const float2 negc = make_float2(-k.c_phase, -k.c_phase);
     const float2 neg1 = make_float2(-1.0f, -1.0f);
-    const float i0 = -0.5f * (TILE_X - 1);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);    // pixel offsets of pair 0 (runtime: no constant pairs)
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 id = make_float2(i0 + q, i0 + q + NP);
-        const float2 x = __ffma2_rn(id, __ffma2_rn(id, pc2, pc1), pc0);
+        const float2 x = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        id = __fadd2_rn(id, one);
         float2 h = __fadd2_rn(x, negc);
         h.x = fmaxf(h.x, 0.0f);
         h.y = fmaxf(h.y, 0.0f);
@@ -309,21 +318,19 @@ __device__ __forceinline__ float4 gather(unsigned long long base, float biased_i
 }
 
 // General case: one gather per pixel.
-__device__ __forceinline__ void gather_pulse(const FastState& st, float c_phase,
+__device__ __forceinline__ void gather_pulse(const BpConst& k, const PulseState& st,
                                              float2 (&accre)[NP], float2 (&accim)[NP])
 {
     const float2 mm = make_float2(MAGIC, MAGIC);
     const float2 nmm = make_float2(-MAGIC, -MAGIC);
     const float2 neg1 = make_float2(-1.0f, -1.0f);
-    const float2 cc = make_float2(c_phase, c_phase);
-    const float2 p0 = make_float2(st.e0, st.e0);
-    const float2 p1 = make_float2(st.e1, st.e1);
-    const float2 p2 = make_float2(st.e2, st.e2);
-    const float i0 = -0.5f * (TILE_X - 1);
+    const float2 cc = make_float2(k.c_phase, k.c_phase);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 id = make_float2(i0 + q, i0 + q + NP);
-        const float2 u = __ffma2_rn(id, __ffma2_rn(id, p2, p1), p0);
+        const float2 u = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        id = __fadd2_rn(id, one);
         const float2 tt = __fadd2_rd(u, mm);        // floor(u) + MAGIC: the index in the mantissa
         const float2 fl = __fadd2_rn(tt, nmm);      // floor(u), exact
         const float2 f = __ffma2_rn(fl, neg1, u);   // u - floor(u), exact
@@ -389,6 +396,18 @@ __device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec,
     }
 }
 
+__device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
+                                            const float4* row, const double* a, double xc,
+                                            double yrow, float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    if (st.mode == MODE_HINGE)
+        hinge_pulse(k, st, accre, accim);
+    else if (st.mode == MODE_GATHER)
+        gather_pulse(k, st, accre, accim);
+    else if (st.mode == MODE_EXACT)
+        exact_pulse(k, rec, row, a, xc, yrow, accre, accim);
+}
+
 __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
 {
     return b * k.units / k.ctas;
@@ -441,22 +460,22 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 make_record(k, pos, klo, c0 + tid, xc, yc, s_rec[tid]);
             __syncthreads();
             const float4* rows = table + (size_t)c0 * k.W;
-            FastState cur = fast_setup(k, s_rec[0], rows, jf, jf2, jf3, jf4);
+            // Two pulse states in ping-pong: the state of pulse p + 1 is built
+            // while pulse p is applied, with no copy between them.
+            PulseState sa = pulse_setup(k, s_rec[0], rows, jf, jf2, jf3, jf4);
 #pragma unroll 1
-            for (int p = 0; p < cnt; ++p) {
-                // the next pulse's state is built here so that its latency
-                // overlaps this pulse's updates
-                const int pn = min(p + 1, cnt - 1);
-                const FastState nxt =
-                    fast_setup(k, s_rec[pn], rows + (size_t)pn * k.W, jf, jf2, jf3, jf4);
-                if (cur.mode == MODE_HINGE)
-                    hinge_pulse(k, cur, accre, accim);
-                else if (cur.mode == MODE_GATHER)
-                    gather_pulse(cur, k.c_phase, accre, accim);
-                else if (cur.mode == MODE_EXACT)
-                    exact_pulse(k, s_rec[p], rows + (size_t)p * k.W, pos + 3 * (size_t)(c0 + p), xc,
-                                yrow, accre, accim);
-                cur = nxt;
+            for (int p = 0; p < cnt; p += 2) {
+                const int p1 = min(p + 1, cnt - 1);
+                const PulseState sb =
+                    pulse_setup(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse(k, sa, s_rec[p], rows + (size_t)p * k.W, pos + 3 * (size_t)(c0 + p),
+                            xc, yrow, accre, accim);
+                if (p + 1 >= cnt)
+                    break;
+                const int p2 = min(p + 2, cnt - 1);
+                sa = pulse_setup(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
+                            pos + 3 * (size_t)(c0 + p + 1), xc, yrow, accre, accim);
             }
         }
 
