@@ -13,10 +13,10 @@ namespace sarbp {
 #define SARBP_TILE_X 32
 #endif
 #ifndef SARBP_WARPS
-#define SARBP_WARPS 8
+#define SARBP_WARPS 16
 #endif
 #ifndef SARBP_MIN_BLOCKS
-#define SARBP_MIN_BLOCKS 2
+#define SARBP_MIN_BLOCKS 1
 #endif
 constexpr int TILE_X = SARBP_TILE_X;
 constexpr int WARPS = SARBP_WARPS;

@@ -524,39 +524,68 @@ __device__ __forceinline__ long long cta_of_unit(const BpConst& k, long long u)
     return ((u + 1) * k.ctas - 1) / k.units;   // largest b with cta_start(b) <= u
 }
 
-__global__ void __launch_bounds__(THREADS) reduce_kernel(BpConst k, const float4* __restrict__ partial,
-                                                         float2* __restrict__ image)
+constexpr int REDUCE_THREADS = 256;
+constexpr int REDUCE_VEC = 8;                                  // float4 (2 pixels) per thread
+constexpr int REDUCE_PIX = REDUCE_THREADS * REDUCE_VEC * 2;    // pixels per block
+constexpr int REDUCE_PARTS = (TILE_PIX + REDUCE_PIX - 1) / REDUCE_PIX;
+
+// One block per (tile, part of the tile). The CTAs that share the tile are
+// visited in ascending order, so the sum is the same on every run.
+__global__ void __launch_bounds__(REDUCE_THREADS) reduce_kernel(BpConst k, const float4* __restrict__ partial,
+                                                                float2* __restrict__ image)
 {
-    const long long t = blockIdx.x;
+    const long long t = blockIdx.x / REDUCE_PARTS;
+    const int part = blockIdx.x % REDUCE_PARTS;
     const long long bf = cta_of_unit(k, t * k.na);
     const long long bl = cta_of_unit(k, (t + 1) * k.na - 1);
     if (bf == bl)
         return;                                    // written directly by one CTA
     const int col0 = (int)(t % k.tiles_x) * TILE_X;
     const int row0 = (int)(t / k.tiles_x) * TILE_Y;
-    const float2* part = reinterpret_cast<const float2*>(partial);
-    const bool acc = (k.flags & 1u) != 0;
-    for (int p = threadIdx.x; p < TILE_PIX; p += blockDim.x) {
-        float2 sum = make_float2(0.f, 0.f);
-        for (long long b = bf; b <= bl; ++b) {
-            const long long s0 = cta_start(k, b);
-            if (s0 >= cta_start(k, b + 1))
-                continue;                          // CTA with no work
-            const int slot = (s0 / k.na == t) ? 0 : 1;
-            const float2 v = part[(size_t)(b * 2 + slot) * TILE_PIX + p];
-            sum.x += v.x;
-            sum.y += v.y;
-        }
-        const int rowi = row0 + p / TILE_X;
-        const int col = col0 + p % TILE_X;
-        if (rowi < k.ny && col < k.nx) {
-            float2* dst = image + (size_t)rowi * k.nx + col;
-            if (acc) {
-                const float2 o = *dst;
-                sum.x += o.x;
-                sum.y += o.y;
+    float4 sum[REDUCE_VEC];
+#pragma unroll
+    for (int r = 0; r < REDUCE_VEC; ++r)
+        sum[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int f0 = part * (REDUCE_PIX / 2) + threadIdx.x;   // float4 index within the tile
+    for (long long b = bf; b <= bl; ++b) {
+        const long long s0 = cta_start(k, b);
+        if (s0 >= cta_start(k, b + 1))
+            continue;                              // CTA with no work
+        const int slot = (s0 / k.na == t) ? 0 : 1;
+        const float4* src = partial + (size_t)(b * 2 + slot) * (TILE_PIX / 2);
+#pragma unroll
+        for (int r = 0; r < REDUCE_VEC; ++r) {
+            const int f = f0 + r * REDUCE_THREADS;
+            if (f < TILE_PIX / 2) {
+                const float4 v = src[f];
+                sum[r].x += v.x;
+                sum[r].y += v.y;
+                sum[r].z += v.z;
+                sum[r].w += v.w;
             }
-            *dst = sum;
+        }
+    }
+    const bool acc = (k.flags & 1u) != 0;
+#pragma unroll
+    for (int r = 0; r < REDUCE_VEC; ++r) {
+        const int f = f0 + r * REDUCE_THREADS;
+        if (f >= TILE_PIX / 2)
+            continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = 2 * f + h;
+            const int rowi = row0 + p / TILE_X;
+            const int col = col0 + p % TILE_X;
+            if (rowi < k.ny && col < k.nx) {
+                float2 v = h ? make_float2(sum[r].z, sum[r].w) : make_float2(sum[r].x, sum[r].y);
+                float2* dst = image + (size_t)rowi * k.nx + col;
+                if (acc) {
+                    const float2 o = *dst;
+                    v.x += o.x;
+                    v.y += o.y;
+                }
+                *dst = v;
+            }
         }
     }
 }
@@ -609,7 +638,7 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
 
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image, cudaStream_t s)
 {
-    reduce_kernel<<<k.tiles, THREADS, 0, s>>>(k, partial, image);
+    reduce_kernel<<<(unsigned)k.tiles * REDUCE_PARTS, REDUCE_THREADS, 0, s>>>(k, partial, image);
     return cudaGetLastError();
 }
 
