@@ -46,7 +46,7 @@ SM_MAX_MHZ_FALLBACK = 2070.0
 L2_FLUSH_BYTES = 256 << 20
 # dram read+write bytes of one bp_kernel launch, from ncu (None until captured
 # for the current kernel)
-MAIN_KERNEL_TRAFFIC = None
+MAIN_KERNEL_TRAFFIC = 10_684_672   # ncu, current bp_kernel, page-sized scene
 
 
 # ------------------------------------------------------------------ ranks
