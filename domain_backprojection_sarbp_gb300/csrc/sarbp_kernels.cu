@@ -279,27 +279,30 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
 // h = max(x - c, 0), the interpolated, phase-compensated sample is
 //   exp(j x) [A + x D + h G],  A = t0.A,  D = t0.D,  G = exp(-j c) t1.D - t0.D
 // (the linear interpolant over the two bins written as one line plus a hinge).
+// With max(y, 0) = (y + |y|) / 2 this is A' + x D' + |x - c| G' where
+// A' = A - c G / 2, D' = D + G / 2, G' = G / 2.
 __device__ __forceinline__ void hinge_pulse(const BpConst& k, const PulseState& st,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const float gre = k.rot_re * st.t1d.x - k.rot_im * st.t1d.y - st.t0.z;
-    const float gim = k.rot_re * st.t1d.y + k.rot_im * st.t1d.x - st.t0.w;
-    const float2 are = make_float2(st.t0.x, st.t0.x), aim = make_float2(st.t0.y, st.t0.y);
-    const float2 dre = make_float2(st.t0.z, st.t0.z), dim = make_float2(st.t0.w, st.t0.w);
+    const float c = k.c_phase;
+    const float gre = 0.5f * (k.rot_re * st.t1d.x - k.rot_im * st.t1d.y - st.t0.z);
+    const float gim = 0.5f * (k.rot_re * st.t1d.y + k.rot_im * st.t1d.x - st.t0.w);
+    const float a_re = fmaf(-c, gre, st.t0.x), a_im = fmaf(-c, gim, st.t0.y);
+    const float d_re = st.t0.z + gre, d_im = st.t0.w + gim;
+    const float2 are = make_float2(a_re, a_re), aim = make_float2(a_im, a_im);
+    const float2 dre = make_float2(d_re, d_re), dim = make_float2(d_im, d_im);
     const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
-    const float2 negc = make_float2(-k.c_phase, -k.c_phase);
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float2 negc = make_float2(-c, -c);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);    // pixel offsets of pair 0 (runtime: no constant pairs)
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
         const float2 x = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
         id = __fadd2_rn(id, one);
-        float2 h = __fadd2_rn(x, negc);
-        h.x = fmaxf(h.x, 0.0f);
-        h.y = fmaxf(h.y, 0.0f);
-        const float2 wr = __ffma2_rn(h, g_re, __ffma2_rn(x, dre, are));
-        const float2 wi = __ffma2_rn(h, g_im, __ffma2_rn(x, dim, aim));
+        const float2 y = __fadd2_rn(x, negc);
+        const float2 ay = make_float2(fabsf(y.x), fabsf(y.y));
+        const float2 wr = __ffma2_rn(ay, g_re, __ffma2_rn(x, dre, are));
+        const float2 wi = __ffma2_rn(ay, g_im, __ffma2_rn(x, dim, aim));
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
         __sincosf(x.y, &sb, &cb);
@@ -307,7 +310,7 @@ __device__ __forceinline__ void hinge_pulse(const BpConst& k, const PulseState& 
         const float2 sn = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, cs, accre[q]);
         accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, cs, accim[q]));
-        accre[q] = __ffma2_rn(__fmul2_rn(wi, sn), neg1, accre[q]);
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), sn, accre[q]);
     }
 }
 
