@@ -264,6 +264,7 @@ def run_ours(args, scene, rank, world, local, dist):
         plan.backproject_host(h_img, h_echo, h_pos, stream=stream)
     te = time.perf_counter() - te0
     e2e_max = max_over_ranks(dist, te, device=dev)
+    h2d_bytes, d2h_bytes = plan.host_transfer_bytes()
     plan.close()
 
     sms = info["sms"]
@@ -288,9 +289,9 @@ def run_ours(args, scene, rank, world, local, dist):
             "frac_of_page_loop_roof": (achieved / page_peak) if achieved else None,
         },
         "e2e": {"value": aggregate_value(updates, e2e_steps, world, e2e_max), "unit": UNIT,
-                "h2d_bytes_per_step": int(scene.echoes.nbytes + scene.antenna_pos.nbytes),
-                "d2h_bytes_per_step": int(p["nx"] * p["ny"] * 8),
-                "api": "sarbp_backproject_host (pinned host buffers)"},
+                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
+                "api": "sarbp_backproject_host (pinned host buffers; copies the band of range "
+                       "bins the image reaches)"},
         "gpu_launches": args.steps * info["kernels_per_call"],
         "clocks": clocks,
         "plan": info,

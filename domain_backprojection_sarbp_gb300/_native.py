@@ -20,6 +20,7 @@ EXPORTS = (
     "sarbp_plan", "sarbp_backproject", "sarbp_backproject_host", "sarbp_destroy",
     "sarbp_status_string", "sarbp_last_error", "sarbp_plan_describe",
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
+    "sarbp_host_transfer_bytes",
 )
 
 
@@ -63,6 +64,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_backproject_host.restype = st
     lib.sarbp_backproject_noalloc.argtypes = [vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject_noalloc.restype = st
+    lib.sarbp_host_transfer_bytes.argtypes = [vp, P(ctypes.c_uint64), P(ctypes.c_uint64)]
+    lib.sarbp_host_transfer_bytes.restype = st
     lib.sarbp_destroy.argtypes = [vp]
     lib.sarbp_destroy.restype = st
     lib.sarbp_status_string.argtypes = [st]

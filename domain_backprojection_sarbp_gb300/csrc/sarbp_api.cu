@@ -35,6 +35,7 @@ struct sarbp_plan_s {
     void* d_image = nullptr;
     void* d_echo = nullptr;
     double* d_pos = nullptr;
+    size_t last_h2d = 0, last_d2h = 0;   // bytes moved by the last host-buffer call
     // kernel timing
     bool timing = false;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> events;
@@ -184,6 +185,69 @@ bool any_split_tile(const BpConst& k)
     }
     return false;
 }
+
+}  // namespace
+
+namespace {
+
+// Queue the three kernels of one backprojection. Arguments are already
+// checked; params may describe a band of the plan's range axis (fewer bins,
+// shifted r0), which the plan's table rows always cover.
+sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void* echoes,
+                                    const double* antenna_pos, const sarbp_params* params,
+                                    cudaStream_t s)
+{
+    cudaError_t e = cudaSuccess;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels == 0)
+        return SARBP_OK;
+    if (params->na == 0 || params->nr < 2) {
+        // no pulse can contribute: the image is the zero sum
+        if (!(params->flags & SARBP_ACCUMULATE)) {
+            e = cudaMemsetAsync(image, 0, (size_t)pixels * 8, s);
+            if (e != cudaSuccess)
+                return cuda_fail(plan, e, "cudaMemsetAsync");
+        }
+        return SARBP_OK;
+    }
+
+    const BpConst k = make_const(plan, params);
+    float4* table = plan->table_alloc + TABLE_PAD;
+    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "table kernel launch");
+
+    std::pair<cudaEvent_t, cudaEvent_t>* ev = nullptr;
+    if (plan->timing) {
+        if (plan->events_used == plan->events.size()) {
+            cudaEvent_t a, b;
+            e = cudaEventCreate(&a);
+            if (e == cudaSuccess) {
+                e = cudaEventCreate(&b);
+                if (e != cudaSuccess)
+                    cudaEventDestroy(a);
+            }
+            if (e != cudaSuccess)
+                return cuda_fail(plan, e, "cudaEventCreate");
+            plan->events.emplace_back(a, b);
+        }
+        ev = &plan->events[plan->events_used++];
+        cudaEventRecord(ev->first, s);
+    }
+    e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
+                           plan->partial, s);
+    if (ev)
+        cudaEventRecord(ev->second, s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "backprojection kernel launch");
+    if (any_split_tile(k)) {
+        e = launch_reduce(k, plan->partial, static_cast<float2*>(image), s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "reduce kernel launch");
+    }
+    return SARBP_OK;
+}
+
 
 }  // namespace
 
@@ -390,54 +454,8 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
     if (dev != plan->device)
         return SARBP_ERR_INVALID_ARG;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pixels == 0)
-        return SARBP_OK;
-    if (params->na == 0 || params->nr < 2) {
-        // no pulse can contribute: the image is the zero sum
-        if (!(params->flags & SARBP_ACCUMULATE)) {
-            e = cudaMemsetAsync(image, 0, (size_t)pixels * 8, s);
-            if (e != cudaSuccess)
-                return cuda_fail(plan, e, "cudaMemsetAsync");
-        }
-        return SARBP_OK;
-    }
-
-    const BpConst k = make_const(plan, params);
-    float4* table = plan->table_alloc + TABLE_PAD;
-    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
-    if (e != cudaSuccess)
-        return cuda_fail(plan, e, "table kernel launch");
-
-    std::pair<cudaEvent_t, cudaEvent_t>* ev = nullptr;
-    if (plan->timing) {
-        if (plan->events_used == plan->events.size()) {
-            cudaEvent_t a, b;
-            e = cudaEventCreate(&a);
-            if (e == cudaSuccess) {
-                e = cudaEventCreate(&b);
-                if (e != cudaSuccess)
-                    cudaEventDestroy(a);
-            }
-            if (e != cudaSuccess)
-                return cuda_fail(plan, e, "cudaEventCreate");
-            plan->events.emplace_back(a, b);
-        }
-        ev = &plan->events[plan->events_used++];
-        cudaEventRecord(ev->first, s);
-    }
-    e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
-                           plan->partial, s);
-    if (ev)
-        cudaEventRecord(ev->second, s);
-    if (e != cudaSuccess)
-        return cuda_fail(plan, e, "backprojection kernel launch");
-    if (any_split_tile(k)) {
-        e = launch_reduce(k, plan->partial, static_cast<float2*>(image), s);
-        if (e != cudaSuccess)
-            return cuda_fail(plan, e, "reduce kernel launch");
-    }
-    return SARBP_OK;
+    return enqueue_backprojection(plan, image, echoes, antenna_pos, params,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
@@ -449,48 +467,109 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
     sarbp_status st = check_sizes(params);
     if (st != SARBP_OK)
         return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr)
+        return SARBP_ERR_PLAN_MISMATCH;
     const long long pixels = (long long)params->nx * params->ny;
     const size_t img_bytes = (size_t)pixels * 8;
-    const size_t echo_bytes = (size_t)params->na * params->nr * 8;
-    const size_t pos_bytes = (size_t)params->na * 3 * sizeof(double);
     if (pixels > 0 && !image)
         return SARBP_ERR_INVALID_ARG;
     if (params->na > 0 && !antenna_pos)
         return SARBP_ERR_INVALID_ARG;
-    if (echo_bytes > 0 && !echoes)
+    if ((size_t)params->na * params->nr > 0 && !echoes)
         return SARBP_ERR_INVALID_ARG;
-    if (params->nx != plan->p.nx || params->ny != plan->p.ny || params->na != plan->p.na ||
-        params->nr != plan->p.nr)
-        return SARBP_ERR_PLAN_MISMATCH;
+    plan->last_error.clear();
+    plan->last_h2d = plan->last_d2h = 0;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+    if (pixels == 0)
+        return SARBP_OK;
 
-    cudaError_t e = cudaSuccess;
+    // The band of range bins the image can reach, from the host copy of the
+    // antenna positions: for every pulse the nearest and farthest point of the
+    // image rectangle, plus margins; pulses with a non-finite position
+    // contribute nothing and are left out. Only this band is copied.
+    long long band_lo = params->nr, band_hi = -1;
+    const double xa = params->x0, xb = params->x0 + (params->nx - 1) * params->dx;
+    const double ya = params->y0, yb = params->y0 + (params->ny - 1) * params->dy;
+    for (int n = 0; n < params->na && params->nr >= 2; ++n) {
+        const double ax = antenna_pos[3 * (size_t)n], ay = antenna_pos[3 * (size_t)n + 1],
+                     az = antenna_pos[3 * (size_t)n + 2];
+        if (!(isfin(ax) && isfin(ay) && isfin(az)))
+            continue;
+        const double dz = params->z0 - az;
+        const double nx_ = std::min(std::max(ax, xa), xb) - ax;
+        const double ny_ = std::min(std::max(ay, ya), yb) - ay;
+        const double fx = std::max(std::fabs(xa - ax), std::fabs(xb - ax));
+        const double fy = std::max(std::fabs(ya - ay), std::fabs(yb - ay));
+        const double rmin = std::sqrt(nx_ * nx_ + ny_ * ny_ + dz * dz);
+        const double rmax = std::sqrt(fx * fx + fy * fy + dz * dz);
+        const double ulo = std::floor((rmin - params->r0) / params->dr) - 2.0;
+        const double uhi = std::floor((rmax - params->r0) / params->dr) + 3.0;
+        band_lo = std::min<long long>(band_lo, (long long)std::max(ulo, 0.0));
+        band_hi = std::max<long long>(band_hi, (long long)std::min(uhi, (double)params->nr - 1.0));
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (img_bytes && !plan->d_image)
         e = cudaMalloc(&plan->d_image, img_bytes);
-    if (e == cudaSuccess && echo_bytes && !plan->d_echo)
-        e = cudaMalloc(&plan->d_echo, echo_bytes);
-    if (e == cudaSuccess && pos_bytes && !plan->d_pos)
-        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), pos_bytes);
+    if (e == cudaSuccess && params->na > 0 && !plan->d_pos)
+        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
+    if (e == cudaSuccess && band_hi >= band_lo && !plan->d_echo)
+        e = cudaMalloc(&plan->d_echo, (size_t)params->na * params->nr * 8);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMalloc (host staging)");
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (echo_bytes)
-        e = cudaMemcpyAsync(plan->d_echo, echoes, echo_bytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && pos_bytes)
-        e = cudaMemcpyAsync(plan->d_pos, antenna_pos, pos_bytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && img_bytes && (params->flags & SARBP_ACCUMULATE))
+    sarbp_params band = *params;
+    if (band_hi >= band_lo) {
+        const size_t width = (size_t)(band_hi - band_lo + 1);
+        band.nr = (int32_t)width;
+        band.r0 = params->r0 + (double)band_lo * params->dr;
+        e = cudaMemcpy2DAsync(plan->d_echo, width * 8,
+                              static_cast<const char*>(echoes) + (size_t)band_lo * 8,
+                              (size_t)params->nr * 8, width * 8, (size_t)params->na,
+                              cudaMemcpyHostToDevice, s);
+        plan->last_h2d += width * 8 * (size_t)params->na;
+    } else {
+        band.nr = 0;                         // no pulse reaches the range axis
+    }
+    if (e == cudaSuccess && params->na > 0) {
+        e = cudaMemcpyAsync(plan->d_pos, antenna_pos, (size_t)params->na * 3 * sizeof(double),
+                            cudaMemcpyHostToDevice, s);
+        plan->last_h2d += (size_t)params->na * 3 * sizeof(double);
+    }
+    if (e == cudaSuccess && (params->flags & SARBP_ACCUMULATE)) {
         e = cudaMemcpyAsync(plan->d_image, image, img_bytes, cudaMemcpyHostToDevice, s);
+        plan->last_h2d += img_bytes;
+    }
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMemcpyAsync (to device)");
-    st = sarbp_backproject(plan, plan->d_image, plan->d_echo, plan->d_pos, params, stream);
+    st = enqueue_backprojection(plan, plan->d_image, plan->d_echo, plan->d_pos, &band, s);
     if (st != SARBP_OK)
         return st;
-    if (img_bytes)
-        e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
+    e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
+    plan->last_d2h = img_bytes;
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMemcpyAsync (to host)");
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_host_transfer_bytes(sarbp_plan_t plan, uint64_t* h2d, uint64_t* d2h)
+{
+    if (!plan || !h2d || !d2h)
+        return SARBP_ERR_INVALID_ARG;
+    *h2d = plan->last_h2d;
+    *d2h = plan->last_d2h;
     return SARBP_OK;
 }
 

@@ -138,6 +138,15 @@ class Plan:
             self._raise(st, "sarbp_backproject_host")
         return image
 
+    def host_transfer_bytes(self):
+        """(host-to-device, device-to-host) bytes of the last backproject_host call."""
+        h2d = ctypes.c_uint64()
+        d2h = ctypes.c_uint64()
+        st = self._lib.sarbp_host_transfer_bytes(self._h, ctypes.byref(h2d), ctypes.byref(d2h))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_host_transfer_bytes")
+        return h2d.value, d2h.value
+
     def describe(self) -> dict:
         info = PlanInfo()
         st = self._lib.sarbp_plan_describe(self._h, ctypes.byref(info))

@@ -124,15 +124,24 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
  * sarbp_backproject_host - the same operation on HOST buffers.
  *
  * image, echoes, antenna_pos are host pointers with the layouts above (pinned
- * memory gives the fastest copies; pageable memory works). The call copies
- * the inputs to plan-owned device buffers (allocated on first use and kept
- * until sarbp_destroy), backprojects on `stream`, copies the image back and
- * waits for the stream: when it returns SARBP_OK the image is on the host.
- * With SARBP_ACCUMULATE the host image is copied in first and added into.
+ * memory gives the fastest copies; pageable memory works). From the antenna
+ * positions the call finds, in float64 on the host, the band of range bins
+ * that any pixel can reach (nearest and farthest point of the image for every
+ * pulse, plus two bins of margin each side) and copies only that band of every
+ * pulse, then backprojects it on `stream` against the same range axis, copies
+ * the image back and waits for the stream: when it returns SARBP_OK the image
+ * is on the host. The result equals sarbp_backproject's to float32 rounding.
+ * Device buffers are owned by the plan (allocated on first use, kept until
+ * sarbp_destroy). With SARBP_ACCUMULATE the host image is copied in first and
+ * added into.
  */
 sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
                                     void* stream);
+
+/* Bytes copied host-to-device and device-to-host by the plan's last
+   sarbp_backproject_host call. */
+sarbp_status sarbp_host_transfer_bytes(sarbp_plan_t plan, uint64_t* h2d, uint64_t* d2h);
 
 /* sarbp_destroy - free the plan and its scratch. NULL is accepted. The caller
    must make sure no work that uses the plan is still running. */

@@ -223,10 +223,35 @@ def test_host_entry_point_matches_device():
         dev_img = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
         host_img = np.zeros((sc.params["ny"], sc.params["nx"]), dtype=np.complex64)
         plan.backproject_host(host_img, sc.echoes, sc.antenna_pos)
-        assert np.array_equal(host_img, dev_img)
+        parity.assert_parity(host_img, dev_img, "host entry point")
+        parity.assert_parity(host_img, oracle.backproject(sc.params, sc.echoes, sc.antenna_pos),
+                             "host entry point vs oracle")
+        h2d, d2h = plan.host_transfer_bytes()
+        # only the band of bins the image reaches is copied, not all 512 per pulse
+        assert h2d < sc.echoes.nbytes // 2 and d2h == host_img.nbytes
         again = host_img.copy()
         plan.backproject_host(again, sc.echoes, sc.antenna_pos, accumulate=True)
-        parity.assert_parity(again, 2 * dev_img.astype(np.complex128), "host accumulate")
+        parity.assert_parity(again, 2 * host_img.astype(np.complex128), "host accumulate")
+
+
+def test_host_entry_point_at_range_axis_edges():
+    sc = _small_scene(96, 300, na=24, nr=48, spacing=0.5, noise=0.3)
+    p = dict(sc.params)
+    p["r0"] = np.linalg.norm(sc.antenna_pos[12]) - 20 * p["dr"]
+    with Plan(p) as plan:
+        img = np.zeros((p["ny"], p["nx"]), dtype=np.complex64)
+        plan.backproject_host(img, sc.echoes, sc.antenna_pos, params=p)
+    parity.assert_parity(img, oracle.backproject(p, sc.echoes, sc.antenna_pos), "host, axis edges")
+
+
+def test_host_entry_point_no_reachable_bin():
+    sc = _small_scene(40, 20, na=8)
+    p = dict(sc.params, r0=sc.params["r0"] + 1.0e5)      # every range is below the axis
+    with Plan(p) as plan:
+        img = np.full((20, 40), 3 + 3j, dtype=np.complex64)
+        plan.backproject_host(img, sc.echoes, sc.antenna_pos, params=p)
+        assert np.all(img == 0)
+        assert plan.host_transfer_bytes()[0] == sc.antenna_pos.nbytes
 
 
 def test_non_default_stream():
