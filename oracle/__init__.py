@@ -5,10 +5,15 @@ benchmark's CPU-baseline leg are the only callers. The product path (the CUDA
 library and its binding) never imports this package.
 
 Pinned functions (each pinned by tests that do not re-type its formula):
-``backproject`` - pinned by hand-computed single-pulse values, the closed form
-at an isolated noiseless target, linearity, focusing, symmetry and the range
-window rule (tests/test_oracle_pins.py), and by planted-mistake checks that
-each such pin rejects a broken copy of the oracle (tests/test_oracle_mutations.py).
+``backproject`` (linear) - pinned by hand-computed single-pulse values, the
+closed form at an isolated noiseless target, linearity, focusing, symmetry and
+the range window rule (tests/test_oracle_pins.py), and by planted-mistake
+checks that each such pin rejects a broken copy of the oracle
+(tests/test_oracle_mutations.py).
+``backproject(interp="sinc8")`` - pinned by on-sample and half-sample values
+of the windowed-sinc kernel, reconstruction of a band-limited signal, the
+stencil window rule, linearity, pulse-order invariance and focusing
+(tests/test_oracle_sinc_pins.py), with its own planted mistakes.
 """
 
 from __future__ import annotations
@@ -60,11 +65,15 @@ def build(force: bool = False) -> str:
 
 def load_library(path: str) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
-    lib.oracle_backproject.restype = ctypes.c_int
-    lib.oracle_backproject.argtypes = [
-        ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p,
-        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
-    ]
+    for name in ("oracle_backproject", "oracle_backproject_sinc8"):
+        fn = getattr(lib, name, None)
+        if fn is None:
+            continue
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+        ]
     return lib
 
 
@@ -85,13 +94,17 @@ def geometry(params: dict) -> OracleGeometry:
 
 def backproject(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
                 pixels: np.ndarray | None = None, threads: int = 0,
-                library: ctypes.CDLL | None = None, return_info: bool = False):
+                library: ctypes.CDLL | None = None, return_info: bool = False,
+                interp: str = "linear"):
     """FP64 image at ``pixels`` (linear iy*nx+ix); the full [ny, nx] image if None.
 
     ``echoes`` complex64 [na, nr]; ``antenna_pos`` float64 [na, 3].
+    ``interp`` is "linear" (the page's kernel) or "sinc8" (8-tap windowed sinc).
     With ``return_info`` also returns (seconds, threads used).
     """
     library = library or lib()
+    fn = {"linear": library.oracle_backproject,
+          "sinc8": library.oracle_backproject_sinc8}[interp]
     nx, ny, na, nr = (int(params[k]) for k in ("nx", "ny", "na", "nr"))
     echoes = np.ascontiguousarray(echoes, dtype=np.complex64).reshape(na, nr)
     pos = np.ascontiguousarray(antenna_pos, dtype=np.float64).reshape(na, 3)
@@ -101,7 +114,7 @@ def backproject(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
     out = np.zeros((pix.size, 2), dtype=np.float64)
     g = geometry(params)
     t0 = time.perf_counter()
-    used = library.oracle_backproject(
+    used = fn(
         ctypes.byref(g), echoes.ctypes.data if echoes.size else None,
         pos.ctypes.data if pos.size else None, pix.ctypes.data if pix.size else None,
         pix.size, out.ctypes.data if out.size else None, int(threads))

@@ -68,6 +68,59 @@ static void backproject_pixel(const oracle_geometry* g, const float* echo,
     out[1] = acc_im;
 }
 
+/* Windowed-sinc kernel: sinc(t) * Hann window of half-width 4 samples. */
+static double sinc8_kernel(double t)
+{
+    const double window = 0.5 + 0.5 * cos(2.0 * ORACLE_PI * t / 8.0);
+    if (t == 0.0)
+        return window;
+    return sin(ORACLE_PI * t) / (ORACLE_PI * t) * window;
+}
+
+/* One pixel, all pulses, 8-tap windowed-sinc interpolation. */
+static void backproject_pixel_sinc8(const oracle_geometry* g, const float* echo,
+                                    const double* antenna_pos, int64_t pixel, double* out)
+{
+    const int64_t ix = pixel % g->nx;
+    const int64_t iy = pixel / g->nx;
+    const double x = g->x0 + (double)ix * g->dx;
+    const double y = g->y0 + (double)iy * g->dy;
+    const double z = g->z0;
+    double acc_re = 0.0;
+    double acc_im = 0.0;
+
+    for (int64_t n = 0; n < g->na; ++n) {
+        const double* a = antenna_pos + 3 * n;
+        const double ddx = x - a[0];
+        const double ddy = y - a[1];
+        const double ddz = z - a[2];
+        const double range = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
+
+        const double u = (range - g->r0) / g->dr;
+        const double k = floor(u);
+        if (!(k - 3.0 >= 0.0 && k + 4.0 <= (double)(g->nr - 1)))
+            continue;                      /* stencil outside the recorded range window */
+        const int64_t kk = (int64_t)k;
+
+        double w_re = 0.0;
+        double w_im = 0.0;
+        for (int64_t m = kk - 3; m <= kk + 4; ++m) {
+            const double h = sinc8_kernel(u - (double)m);
+            const float* e = echo + 2 * (n * g->nr + m);
+            w_re += h * (double)e[0];
+            w_im += h * (double)e[1];
+        }
+
+        const double phase = 4.0 * ORACLE_PI * range / g->wavelength;
+        const double c = cos(phase);
+        const double s = sin(phase);
+        acc_re += w_re * c - w_im * s;
+        acc_im += w_re * s + w_im * c;
+    }
+    out[0] = acc_re;
+    out[1] = acc_im;
+}
+
 typedef struct {
     const oracle_geometry* g;
     const float* echo;
@@ -75,19 +128,22 @@ typedef struct {
     const int64_t* pixels;
     double* out;
     int64_t begin, end;
+    void (*pixel_fn)(const oracle_geometry*, const float*, const double*, int64_t, double*);
 } oracle_job;
 
 static void* oracle_worker(void* arg)
 {
     const oracle_job* job = (const oracle_job*)arg;
     for (int64_t i = job->begin; i < job->end; ++i)
-        backproject_pixel(job->g, job->echo, job->antenna_pos, job->pixels[i], job->out + 2 * i);
+        job->pixel_fn(job->g, job->echo, job->antenna_pos, job->pixels[i], job->out + 2 * i);
     return NULL;
 }
 
-int oracle_backproject(const oracle_geometry* g, const float* echo,
-                       const double* antenna_pos, const int64_t* pixels,
-                       int64_t npix, double* out, int nthreads)
+static int run_pixels(const oracle_geometry* g, const float* echo,
+                      const double* antenna_pos, const int64_t* pixels,
+                      int64_t npix, double* out, int nthreads,
+                      void (*pixel_fn)(const oracle_geometry*, const float*, const double*,
+                                       int64_t, double*))
 {
     if (!g || npix < 0 || g->nx <= 0 || g->ny <= 0 || g->na < 0 || g->nr < 0)
         return -1;
@@ -123,6 +179,7 @@ int oracle_backproject(const oracle_geometry* g, const float* echo,
         jobs[t].out = out;
         jobs[t].begin = npix * t / nthreads;
         jobs[t].end = npix * (t + 1) / nthreads;
+        jobs[t].pixel_fn = pixel_fn;
         if (t == 0)
             continue;
         if (pthread_create(&threads[t], NULL, oracle_worker, &jobs[t]) == 0)
@@ -138,4 +195,19 @@ int oracle_backproject(const oracle_geometry* g, const float* echo,
     free(threads);
     free(joinable);
     return nthreads;
+}
+
+int oracle_backproject(const oracle_geometry* g, const float* echo,
+                       const double* antenna_pos, const int64_t* pixels,
+                       int64_t npix, double* out, int nthreads)
+{
+    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads, backproject_pixel);
+}
+
+int oracle_backproject_sinc8(const oracle_geometry* g, const float* echo,
+                             const double* antenna_pos, const int64_t* pixels,
+                             int64_t npix, double* out, int nthreads)
+{
+    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads,
+                      backproject_pixel_sinc8);
 }

@@ -47,6 +47,17 @@ int oracle_backproject(const oracle_geometry* g, const float* echo,
                        const double* antenna_pos, const int64_t* pixels,
                        int64_t npix, double* out, int nthreads);
 
+/*
+ * Same sum with truncated-sinc interpolation instead of linear (SARBP-GPU
+ * §2.2 names sinc interpolation as the more accurate, costlier choice):
+ *   w_n = sum_{m = k-3}^{k+4} e[n][m] * h(u - m),
+ *   h(t) = sinc(t) * (1/2 + 1/2 cos(2 pi t / 8)),  sinc(t) = sin(pi t) / (pi t),
+ * and w_n = 0 unless the whole stencil k-3 .. k+4 lies in 0 .. nr-1.
+ */
+int oracle_backproject_sinc8(const oracle_geometry* g, const float* echo,
+                             const double* antenna_pos, const int64_t* pixels,
+                             int64_t npix, double* out, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
