@@ -265,6 +265,30 @@ def run_ours(args, scene, rank, world, local, dist):
     te = time.perf_counter() - te0
     e2e_max = max_over_ranks(dist, te, device=dev)
     h2d_bytes, d2h_bytes = plan.host_transfer_bytes()
+
+    # the windowed-sinc variant on the same scene (device-resident, L2 flushed)
+    variants = {}
+    if not args.no_variants:
+        sinc_steps = max(3, min(args.steps, 20))
+        for _ in range(3):
+            plan.backproject(image, echoes, pos, interp="sinc8")
+        torch.cuda.synchronize(dev)
+        plan.kernel_times()
+        s_ms = 0.0
+        for i in range(sinc_steps):
+            flush.fill_(float(i))
+            starts[0].record(stream)
+            plan.backproject(image, echoes, pos, interp="sinc8")
+            ends[0].record(stream)
+            ends[0].synchronize()
+            s_ms += starts[0].elapsed_time(ends[0])
+        sinc_main_ms, sinc_launches = plan.kernel_times()
+        variants["sinc8"] = {
+            "interp": "8-tap windowed sinc (SARBP_SINC8)", "steps": sinc_steps,
+            "value": updates * sinc_steps / (s_ms / 1e3) / 1e9, "unit": UNIT,
+            "ms_per_step": s_ms / sinc_steps,
+            "main_kernel_gupd": updates / (sinc_main_ms / max(sinc_launches, 1) / 1e3) / 1e9,
+        }
     plan.close()
 
     sms = info["sms"]
@@ -295,6 +319,7 @@ def run_ours(args, scene, rank, world, local, dist):
         "gpu_launches": args.steps * info["kernels_per_call"],
         "clocks": clocks,
         "plan": info,
+        "variants": variants,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_rate(scene, seconds=args.cpu_seconds)
@@ -311,6 +336,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the windowed-sinc variant measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -15,6 +15,7 @@ SARBP_ERR_OOM = 4
 SARBP_ERR_UNSUPPORTED_DEVICE = 5
 SARBP_ERR_SCRATCH_TOO_SMALL = 6
 SARBP_ACCUMULATE = 1
+SARBP_SINC8 = 2
 
 EXPORTS = (
     "sarbp_plan", "sarbp_backproject", "sarbp_backproject_host", "sarbp_destroy",

@@ -28,6 +28,7 @@ struct sarbp_plan_s {
     int W = 0, full_window = 0;
     float4* table_alloc = nullptr;   // (na * W + 2 * TABLE_PAD) entries
     int* klo = nullptr;              // na
+    float2* psi = nullptr;           // nr: per-bin phasors (windowed-sinc interpolation)
     float4* partial = nullptr;       // 2 * max_ctas * TILE_PIX / 2
     int max_ctas = 0;
     size_t scratch_bytes = 0;
@@ -78,7 +79,7 @@ sarbp_status check_geometry(const sarbp_params* p)
         return SARBP_ERR_INVALID_ARG;
     if (!(isfin(p->wavelength) && p->wavelength > 0))
         return SARBP_ERR_INVALID_ARG;
-    if (p->flags & ~SARBP_ACCUMULATE)
+    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8))
         return SARBP_ERR_INVALID_ARG;
     return SARBP_OK;
 }
@@ -162,6 +163,7 @@ void free_plan(sarbp_plan_s* plan)
         return;
     cudaFree(plan->table_alloc);
     cudaFree(plan->klo);
+    cudaFree(plan->psi);
     cudaFree(plan->partial);
     cudaFree(plan->d_image);
     cudaFree(plan->d_echo);
@@ -216,6 +218,11 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
     e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "table kernel launch");
+    if (k.flags & SARBP_SINC8) {
+        e = launch_psi(k, plan->psi, s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "phasor kernel launch");
+    }
 
     std::pair<cudaEvent_t, cudaEvent_t>* ev = nullptr;
     if (plan->timing) {
@@ -235,7 +242,7 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         cudaEventRecord(ev->first, s);
     }
     e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
-                           plan->partial, s);
+                           plan->partial, plan->psi, s);
     if (ev)
         cudaEventRecord(ev->second, s);
     if (e != cudaSuccess)
@@ -281,7 +288,7 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
     sarbp_status st = check_sizes(p);
     if (st != SARBP_OK)
         return st;
-    if (p->flags & ~SARBP_ACCUMULATE)
+    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8))
         return SARBP_ERR_INVALID_ARG;
     if (!(isfin(p->wavelength) && p->wavelength > 0))
         return SARBP_ERR_INVALID_ARG;
@@ -341,12 +348,14 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
 
     if (plan->tiles > 0 && p->na > 0) {
         const size_t table_entries = (size_t)p->na * plan->W + 2 * TABLE_PAD;
-        const size_t sizes[3] = {table_entries * sizeof(float4), (size_t)p->na * sizeof(int),
-                                 (size_t)plan->max_ctas * TILE_PIX * sizeof(float4)};
-        void** ptrs[3] = {reinterpret_cast<void**>(&plan->table_alloc),
+        const size_t sizes[4] = {table_entries * sizeof(float4), (size_t)p->na * sizeof(int),
+                                 (size_t)plan->max_ctas * TILE_PIX * sizeof(float4),
+                                 ((size_t)p->nr + 1) * sizeof(float2)};
+        void** ptrs[4] = {reinterpret_cast<void**>(&plan->table_alloc),
                           reinterpret_cast<void**>(&plan->klo),
-                          reinterpret_cast<void**>(&plan->partial)};
-        for (int i = 0; i < 3; ++i) {
+                          reinterpret_cast<void**>(&plan->partial),
+                          reinterpret_cast<void**>(&plan->psi)};
+        for (int i = 0; i < 4; ++i) {
             e = cudaMalloc(ptrs[i], sizes[i]);
             if (e != cudaSuccess) {
                 st = cuda_fail(plan, e, "cudaMalloc");
@@ -512,8 +521,8 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
         const double fy = std::max(std::fabs(ya - ay), std::fabs(yb - ay));
         const double rmin = std::sqrt(nx_ * nx_ + ny_ * ny_ + dz * dz);
         const double rmax = std::sqrt(fx * fx + fy * fy + dz * dz);
-        const double ulo = std::floor((rmin - params->r0) / params->dr) - 2.0;
-        const double uhi = std::floor((rmax - params->r0) / params->dr) + 3.0;
+        const double ulo = std::floor((rmin - params->r0) / params->dr) - 6.0;
+        const double uhi = std::floor((rmax - params->r0) / params->dr) + 7.0;
         band_lo = std::min<long long>(band_lo, (long long)std::max(ulo, 0.0));
         band_hi = std::max<long long>(band_hi, (long long)std::min(uhi, (double)params->nr - 1.0));
     }
@@ -588,6 +597,8 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
     st = check_geometry(params);
     if (st != SARBP_OK)
         return st;
+    if (params->flags & SARBP_SINC8)
+        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
     const long long pixels = (long long)params->nx * params->ny;
     if (pixels > 0 && (!image || !aligned8(image)))
         return SARBP_ERR_INVALID_ARG;
@@ -671,7 +682,7 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
                          klo, s);
         if (e == cudaSuccess)
             e = launch_backproject(k, antenna_pos + 3 * (size_t)c0, table, klo,
-                                   static_cast<float2*>(image), nullptr, s);
+                                   static_cast<float2*>(image), nullptr, nullptr, s);
         if (e != cudaSuccess)
             return SARBP_ERR_CUDA;
     }

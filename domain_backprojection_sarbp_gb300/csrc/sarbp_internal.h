@@ -31,6 +31,8 @@ constexpr int MIN_PULSES_PER_CTA = 32;     // keeps tiny problems from over-spli
 constexpr int KLO_INVALID = INT32_MIN;     // pulse with a non-finite antenna position
 
 enum RecordKind : int { REC_SKIP = 0, REC_FAST = 1, REC_EXACT = 2 };
+constexpr unsigned FLAG_ACCUMULATE = 1u;   // same values as SARBP_ACCUMULATE / SARBP_SINC8
+constexpr unsigned FLAG_SINC8 = 2u;
 
 // Launch constants, computed on the host in float64 for every call.
 struct BpConst {
@@ -58,8 +60,10 @@ struct BpConst {
 
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos,
                          float4* table, int* klo, cudaStream_t s);
+cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s);
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
-                               const int* klo, float2* image, float4* partial, cudaStream_t s);
+                               const int* klo, float2* image, float4* partial,
+                               const float2* psi, cudaStream_t s);
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);

@@ -38,6 +38,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 namespace sarbp {
@@ -56,6 +57,10 @@ struct __align__(16) Record {
 // ---------------------------------------------------------------------------
 // Echo table: one block per pulse.
 // ---------------------------------------------------------------------------
+// Linear interpolation: entries (A_k, D_k / c) as above. Windowed-sinc
+// interpolation: entries are plain sample pairs (e_k, e_{k+1}), zero where a
+// sample lies outside 0 .. nr - 1, and the phase comes from psi_k (psi_kernel).
+template <bool SINC>
 __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __restrict__ echo,
                                                     const double* __restrict__ pos,
                                                     float4* __restrict__ table,
@@ -92,7 +97,18 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
     for (int w = threadIdx.x; w < k.W; w += blockDim.x) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         const long long kk = (long long)lo + w;
-        if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 2) {
+        if (SINC) {
+            if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 1) {
+                const float2 e0 = erow[kk];
+                v.x = e0.x;
+                v.y = e0.y;
+            }
+            if (lo != KLO_INVALID && kk + 1 >= 0 && kk + 1 <= (long long)k.nr - 1) {
+                const float2 e1 = erow[kk + 1];
+                v.z = e1.x;
+                v.w = e1.y;
+            }
+        } else if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 2) {
             const float2 e0 = erow[kk];
             const float2 e1 = erow[kk + 1];
             // frac(2 r_k / lambda) in 64-bit fixed point, exact up to the
@@ -110,6 +126,19 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
         }
         row[w] = v;
     }
+}
+
+// psi_k = exp(j 2 pi frac(2 r_k / lambda)) for every bin of the range axis.
+__global__ void __launch_bounds__(256) psi_kernel(BpConst k, float2* __restrict__ psi)
+{
+    const long long kk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (kk >= k.nr)
+        return;
+    const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
+    const float turns = (float)(ph >> 40) * 0x1p-24f;
+    float s, c;
+    sincospif(2.0f * turns, &s, &c);
+    psi[kk] = make_float2(c, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -216,9 +245,12 @@ struct PulseState {
     float4 t0;                    // hinge: table entry k0
     float2 t1d;                   // hinge: D part of entry k0 + 1
     unsigned long long base;      // gather: row pointer + (kb - magic bias) entries, in bytes
+    int kb;                       // row index the polynomial u is relative to
+    int bin0;                     // row index of absolute bin 0
     int mode;
 };
 
+template <bool SINC>
 __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record& rec,
                                                   const float4* row, float jf, float jf2,
                                                   float jf3, float jf4)
@@ -249,7 +281,7 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const int bin0 = __float_as_int(rd.y);               // row index of absolute bin 0
     // both bins must hold recorded samples: the identity behind the hinge
     // form does not hold across the zero entries outside 0 <= k <= nr - 2
-    const bool hinge = kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
+    const bool hinge = !SINC && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
                        idx0 + 1 <= bin0 + k.nr - 2;
     PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
@@ -272,6 +304,8 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     }
     st.base = reinterpret_cast<unsigned long long>(row) +
               (unsigned long long)(long long)(kb - MAGIC_BITS) * 16ull;
+    st.kb = kb;
+    st.bin0 = bin0;
     return st;
 }
 
@@ -399,10 +433,146 @@ __device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Windowed-sinc interpolation (8 taps, k-3 .. k+4).
+//
+// The echo at range u = k + f is psi(u) sum_m e_m h(u - m) with
+// psi(u) = psi_k exp(j c f). For tap m = k - 3 + t the argument is
+// f + d, d = 3 - t, and
+//   h(f + d) = (-1)^d sin(pi f) / (pi (f + d)) * (1 + cos(pi (f + d) / 4)) / 2,
+// so one sine, one sine/cosine pair (angle addition for the window) and one
+// reciprocal (batch inversion of the eight f + d) serve all eight weights.
+// ---------------------------------------------------------------------------
+// One pixel at row position ub (relative to row index kb). CHECK_ROW adds
+// bounds on the table row for the exact path.
+template <bool CHECK_ROW>
+__device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, int bin0,
+                                           const float4* row, const float2* __restrict__ psi,
+                                           float& re, float& im)
+{
+    if (CHECK_ROW && !(ub > -1.0e6f && ub < 1.0e6f))
+        return;
+    const float tt = __fadd_rd(ub, MAGIC);
+    const float f = ub - (tt - MAGIC);
+    const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
+    const int kabs = kr - bin0;
+    if (kabs < 3 || kabs > k.nr - 5)
+        return;                                 // stencil reaches outside the recorded range
+    if (CHECK_ROW && (kr < 3 || kr + 3 > k.W - 1))
+        return;
+    const float4* p = row + (kr - 3);
+    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
+    const float2 ps = __ldg(psi + kabs);
+
+    // f + d for d = 3 .. -4. f in [1e-7, 1 - 1e-7] keeps every f + d off 0 (the
+    // fraction can round to exactly 1 for tiny negative u); the weights are
+    // continuous in f, so the clamp changes them by less than 1e-6.
+    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
+    const float x0 = fc + 3.0f, x1 = fc + 2.0f, x2 = fc + 1.0f, x3 = fc;
+    const float x4 = fc - 1.0f, x5 = fc - 2.0f, x6 = fc - 3.0f, x7 = fc - 4.0f;
+    const float a1 = x0 * x1, a2 = a1 * x2, a3 = a2 * x3, a4 = a3 * x4, a5 = a4 * x5,
+                a6 = a5 * x6, a7 = a6 * x7;
+    float r = __fdividef(1.0f, a7);
+    const float i7 = r * a6; r *= x7;
+    const float i6 = r * a5; r *= x6;
+    const float i5 = r * a4; r *= x5;
+    const float i4 = r * a3; r *= x4;
+    const float i3 = r * a2; r *= x3;
+    const float i2 = r * a1; r *= x2;
+    const float i1 = r * x0;
+    const float i0 = r * x1;
+    // sin(pi f) / pi with relative accuracy: the centre weight divides it by f
+    const float sf = sinpif(fc) * 0.318309886f;
+    float s4, c4;
+    __sincosf(0.785398163f * fc, &s4, &c4);                     // pi f / 4
+    // (1 + cos(pi (f + d) / 4)) / 2 with cos(pi d/4), sin(pi d/4) for d = 3 .. -4
+    constexpr float H = 0.353553391f;                            // sqrt(2) / 4
+    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));           // d = 3
+    const float w1 = fmaf(-s4, 0.5f, 0.5f);                      // d = 2
+    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));            // d = 1
+    const float w3 = fmaf(c4, 0.5f, 0.5f);                       // d = 0
+    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));             // d = -1
+    const float w5 = fmaf(s4, 0.5f, 0.5f);                       // d = -2
+    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));            // d = -3
+    const float w7 = fmaf(c4, -0.5f, 0.5f);                      // d = -4
+    // (-1)^d: d = 3, 1, -1, -3 are odd
+    const float h0 = -sf * i0 * w0, h1 = sf * i1 * w1, h2 = -sf * i2 * w2, h3 = sf * i3 * w3;
+    const float h4 = -sf * i4 * w4, h5 = sf * i5 * w5, h6 = -sf * i6 * w6, h7 = sf * i7 * w7;
+
+    float sre = h0 * s0.x, sim = h0 * s0.y;
+    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
+    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
+    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
+    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
+    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
+    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
+    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
+    float sn, cs;
+    __sincosf(f * k.c_phase, &sn, &cs);
+    const float zr = ps.x * cs - ps.y * sn;
+    const float zi = ps.x * sn + ps.y * cs;
+    re = fmaf(sre, zr, fmaf(-sim, zi, re));
+    im = fmaf(sre, zi, fmaf(sim, zr, im));
+}
+
+__device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& st, const float4* row,
+                                           const float2* __restrict__ psi,
+                                           float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float i = k.i0 + (float)m;
+        const float ub = fmaf(i, fmaf(i, e2, e1), e0);
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        sinc_pixel<false>(k, ub, st.kb, st.bin0, row, psi, re, im);
+    }
+}
+
+__device__ __forceinline__ void sinc_exact_pulse(const BpConst& k, const Record& rec, const float4* row,
+                                                 const double* __restrict__ a, double xc,
+                                                 double yrow, const float2* __restrict__ psi,
+                                                 float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const double vx = xc - a[0], vy = yrow - a[1], vz = k.z0 - a[2];
+    const double r2 = vx * vx + vy * vy + vz * vz;
+    const double r = sqrt(r2);
+    const double u = (r - k.r0) * k.inv_dr;
+    if (!(fabs(u) < 1.0e9))
+        return;
+    const double ku = floor(u);
+    const int bin0 = __float_as_int(rec.d.y);
+    const int kbase = (int)ku + bin0;
+    const float frac0 = (float)(u - ku);
+    const float two_vx = (float)(2.0 * vx), rf = (float)r, r2f = (float)r2;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
+        const float s = qx * (two_vx + qx);
+        const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
+        const float den = rf + rp;
+        const float dr_m = den > 0.0f ? s / den : 0.0f;
+        const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        sinc_pixel<true>(k, ub, kbase, bin0, row, psi, re, im);
+    }
+}
+
+template <bool SINC>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, float2 (&accre)[NP], float2 (&accim)[NP])
+                                            double yrow, const float2* __restrict__ psi,
+                                            float2 (&accre)[NP], float2 (&accim)[NP])
 {
+    if (SINC) {
+        if (st.mode == MODE_GATHER)
+            sinc_pulse(k, st, row, psi, accre, accim);
+        else if (st.mode == MODE_EXACT)
+            sinc_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
+        return;
+    }
     if (st.mode == MODE_HINGE)
         hinge_pulse(k, st, accre, accim);
     else if (st.mode == MODE_GATHER)
@@ -419,11 +589,13 @@ __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
 // ---------------------------------------------------------------------------
 // Main kernel: persistent, one contiguous range of (tile, pulse) units per CTA.
 // ---------------------------------------------------------------------------
+template <bool SINC>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, const double* __restrict__ pos,
                                                         const float4* __restrict__ table,
                                                         const int* __restrict__ klo,
                                                         float2* __restrict__ image,
-                                                        float4* __restrict__ partial)
+                                                        float4* __restrict__ partial,
+                                                        const float2* __restrict__ psi)
 {
     __shared__ Record s_rec[CHUNK];
     const int tid = threadIdx.x;
@@ -465,20 +637,20 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const float4* rows = table + (size_t)c0 * k.W;
             // Two pulse states in ping-pong: the state of pulse p + 1 is built
             // while pulse p is applied, with no copy between them.
-            PulseState sa = pulse_setup(k, s_rec[0], rows, jf, jf2, jf3, jf4);
+            PulseState sa = pulse_setup<SINC>(k, s_rec[0], rows, jf, jf2, jf3, jf4);
 #pragma unroll 1
             for (int p = 0; p < cnt; p += 2) {
                 const int p1 = min(p + 1, cnt - 1);
                 const PulseState sb =
-                    pulse_setup(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
-                apply_pulse(k, sa, s_rec[p], rows + (size_t)p * k.W, pos + 3 * (size_t)(c0 + p),
-                            xc, yrow, accre, accim);
+                    pulse_setup<SINC>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse<SINC>(k, sa, s_rec[p], rows + (size_t)p * k.W,
+                                  pos + 3 * (size_t)(c0 + p), xc, yrow, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
-                sa = pulse_setup(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
-                apply_pulse(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
-                            pos + 3 * (size_t)(c0 + p + 1), xc, yrow, accre, accim);
+                sa = pulse_setup<SINC>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse<SINC>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
+                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, psi, accre, accim);
             }
         }
 
@@ -486,7 +658,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         if (n0 == 0 && n1 == k.na) {
             if (rowi < k.ny) {
                 float2* dst = image + (size_t)rowi * k.nx;
-                const bool acc = (k.flags & 1u) != 0;
+                const bool acc = (k.flags & FLAG_ACCUMULATE) != 0;
 #pragma unroll
                 for (int m = 0; m < TILE_X; ++m) {
                     const int col = col0 + m;
@@ -568,7 +740,7 @@ __global__ void __launch_bounds__(REDUCE_THREADS) reduce_kernel(BpConst k, const
             }
         }
     }
-    const bool acc = (k.flags & 1u) != 0;
+    const bool acc = (k.flags & FLAG_ACCUMULATE) != 0;
 #pragma unroll
     for (int r = 0; r < REDUCE_VEC; ++r) {
         const int f = f0 + r * REDUCE_THREADS;
@@ -628,14 +800,27 @@ cudaError_t noalloc_scratch(void** ptr)
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
                          int* klo, cudaStream_t s)
 {
-    table_kernel<<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+    if (k.flags & FLAG_SINC8)
+        table_kernel<true><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+    else
+        table_kernel<false><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
+{
+    psi_kernel<<<(unsigned)((k.nr + 255) / 256), 256, 0, s>>>(k, psi);
     return cudaGetLastError();
 }
 
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
-                               const int* klo, float2* image, float4* partial, cudaStream_t s)
+                               const int* klo, float2* image, float4* partial,
+                               const float2* psi, cudaStream_t s)
 {
-    bp_kernel<<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial);
+    if (k.flags & FLAG_SINC8)
+        bp_kernel<true><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+    else
+        bp_kernel<false><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
     return cudaGetLastError();
 }
 
@@ -647,7 +832,12 @@ cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image
 
 cudaError_t backproject_occupancy(int* ctas_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, bp_kernel, THREADS, 0);
+    int a = 0, b = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, bp_kernel<false>, THREADS, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, bp_kernel<true>, THREADS, 0);
+    *ctas_per_sm = std::min(a, b);
+    return e;
 }
 
 }  // namespace sarbp

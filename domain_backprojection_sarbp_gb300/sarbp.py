@@ -13,7 +13,7 @@ import ctypes
 import numpy as np
 
 from . import _native
-from ._native import Params, PlanInfo, SARBP_ACCUMULATE
+from ._native import Params, PlanInfo, SARBP_ACCUMULATE, SARBP_SINC8
 
 
 class SarbpError(RuntimeError):
@@ -23,13 +23,17 @@ class SarbpError(RuntimeError):
         super().__init__(f"{where}: {text}" + (f" ({detail})" if detail else ""))
 
 
-def _params(p, flags=None) -> Params:
+def _params(p, accumulate=False, interp="linear") -> Params:
     if isinstance(p, Params):
         out = Params.from_buffer_copy(p)
     else:
         out = Params.from_dict(p)
-    if flags is not None:
-        out.flags = int(flags)
+    if accumulate:
+        out.flags |= SARBP_ACCUMULATE
+    if interp == "sinc8":
+        out.flags |= SARBP_SINC8
+    elif interp != "linear":
+        raise ValueError(f"interp must be 'linear' or 'sinc8', got {interp!r}")
     return out
 
 
@@ -94,14 +98,15 @@ class Plan:
         detail = self._lib.sarbp_last_error(self._h).decode(errors="replace")
         raise SarbpError(st, where, detail)
 
-    def backproject(self, image, echoes, antenna_pos, params=None, accumulate=False, stream=None):
+    def backproject(self, image, echoes, antenna_pos, params=None, accumulate=False, stream=None,
+                    interp="linear"):
         """Enqueue I(p) = sum_n w_n exp(+j 4 pi R_n / lambda) on ``stream`` (device tensors).
 
         image complex64 [ny, nx]; echoes complex64 [na, nr]; antenna_pos float64 [na, 3].
+        ``interp``: "linear" or "sinc8" (8-tap windowed sinc).
         """
         import torch
-        p = _params(params if params is not None else self.params,
-                    SARBP_ACCUMULATE if accumulate else None)
+        p = _params(params if params is not None else self.params, accumulate, interp)
         img = _check_device_tensor(image, "image", torch.complex64, (p.ny, p.nx))
         ech = _check_device_tensor(echoes, "echoes", torch.complex64, (p.na, p.nr))
         pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))
@@ -112,10 +117,9 @@ class Plan:
         return image
 
     def backproject_host(self, image, echoes, antenna_pos, params=None, accumulate=False,
-                         stream=None):
+                         stream=None, interp="linear"):
         """Same operation on host arrays (numpy or CPU tensors); returns when the image is on the host."""
-        p = _params(params if params is not None else self.params,
-                    SARBP_ACCUMULATE if accumulate else None)
+        p = _params(params if params is not None else self.params, accumulate, interp)
 
         def host_ptr(a, name, shape, np_dtype):
             if hasattr(a, "is_cuda"):

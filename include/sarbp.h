@@ -68,6 +68,12 @@ typedef enum sarbp_status {
                                 caller backproject pulses in batches (SARBP-GPU §3.3
                                 stream overlap of echo loading and computation)       */
 
+#define SARBP_SINC8 2u       /* interpolate with an 8-tap windowed sinc instead of linearly
+                                (SARBP-GPU §2.2: sinc interpolation, more accurate and
+                                costlier): w = sum_{m=k-3}^{k+4} e[m] h(u - m),
+                                h(t) = sinc(t) (1/2 + 1/2 cos(2 pi t / 8)), zero unless
+                                the whole stencil lies in 0 .. nr-1                    */
+
 typedef struct sarbp_params {
     int32_t nx, ny;       /* image width (x) and height (y), pixels, >= 0             */
     int32_t na, nr;       /* pulses and range bins, >= 0                              */
@@ -76,7 +82,7 @@ typedef struct sarbp_params {
     double r0, dr;        /* range of bin k is r0 + k*dr, metres; dr > 0              */
     double wavelength;    /* carrier wavelength lambda = c / fc, metres, > 0
                              (SARBP-GPU §4.2: the carrier, not the bandwidth one)     */
-    uint32_t flags;       /* SARBP_ACCUMULATE or 0                                    */
+    uint32_t flags;       /* SARBP_ACCUMULATE, SARBP_SINC8, or 0                      */
 } sarbp_params;
 
 typedef struct sarbp_plan_s* sarbp_plan_t;
@@ -91,8 +97,8 @@ typedef struct sarbp_plan_s* sarbp_plan_t;
  * Uses the CUDA device current on the calling thread; later calls must run
  * with that device current. Scratch owned by the plan: the pre-multiplied
  * echo table (na x W x 16 bytes, W <= nr + 24, where W covers the image's
- * range extent), one int per pulse, and the partial-sum buffers of the work
- * split (about 40 MB). Returns SARBP_ERR_INVALID_ARG for negative sizes,
+ * range extent), one int per pulse, one complex64 per range bin, and the
+ * partial-sum buffers of the work split (about 40 MB). Returns SARBP_ERR_INVALID_ARG for negative sizes,
  * non-finite or non-positive dx, dy, dr, wavelength, unknown flags, or image
  * sizes above 2^30 pixels; SARBP_ERR_UNSUPPORTED_DEVICE off compute
  * capability 10.3; SARBP_ERR_OOM if an allocation fails.
@@ -104,6 +110,7 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p);
  *
  * image        device pointer, complex64 [ny][nx], caller-owned, 8-byte aligned.
  *              Overwritten, or added into when params->flags has SARBP_ACCUMULATE.
+ *              With SARBP_SINC8 the echo is interpolated with the windowed sinc.
  * echoes       device pointer, complex64 [na][nr], caller-owned, 8-byte aligned.
  * antenna_pos  device pointer, float64 [na][3], caller-owned, 8-byte aligned.
  * params       host pointer; nx, ny, na, nr, dx, dy, dr must equal the plan's
@@ -127,7 +134,7 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
  * memory gives the fastest copies; pageable memory works). From the antenna
  * positions the call finds, in float64 on the host, the band of range bins
  * that any pixel can reach (nearest and farthest point of the image for every
- * pulse, plus two bins of margin each side) and copies only that band of every
+ * pulse, plus six bins of margin each side) and copies only that band of every
  * pulse, then backprojects it on `stream` against the same range axis, copies
  * the image back and waits for the stream: when it returns SARBP_OK the image
  * is on the host. The result equals sarbp_backproject's to float32 rounding.
@@ -188,7 +195,8 @@ sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* lau
  * processing has started. Such callers cannot create a plan either.
  *
  * image, echoes, antenna_pos, params, stream: as for sarbp_backproject. All
- * sizes come from params; no plan is involved.
+ * sizes come from params; no plan is involved. Linear interpolation only:
+ * SARBP_SINC8 is rejected with SARBP_ERR_INVALID_ARG.
  *
  * Scratch: a fixed, file-scope device array of SARBP_NOALLOC_SCRATCH_BYTES
  * (16 MiB) that every GPU loading the library holds until the process exits.
