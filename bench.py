@@ -43,6 +43,7 @@ MUFU_PER_SM_CLK = 16          # sine/cosine lanes per SM per clock
 MUFU_PER_UPDATE = 2           # sin and cos of the phase; the range needs no sqrt here
 PAGE_SFU_PER_UPDATE = 3       # the page's loop: sqrt, sin, cos
 SM_MAX_MHZ_FALLBACK = 2070.0
+HBM_GBS = 6796.9            # measured copy bandwidth of the GB300s (MEASURED_PEAKS.json)
 L2_FLUSH_BYTES = 256 << 20
 # dram read+write bytes of one bp_kernel launch, from ncu (None until captured
 # for the current kernel)
@@ -283,6 +284,36 @@ def run_ours(args, scene, rank, world, local, dist):
             ends[0].synchronize()
             s_ms += starts[0].elapsed_time(ends[0])
         sinc_main_ms, sinc_launches = plan.kernel_times()
+        # range compression of this scene's shape (SARBP-GPU §3.1): raw chirps -> echoes
+        from domain_backprojection_sarbp_gb300 import RangeCompressor
+        from synth import chirp as chirp_mod
+        ref = torch.from_numpy(chirp_mod.chirp().astype(np.complex64)).to(dev)
+        raw = torch.empty_like(echoes).normal_()
+        rc_out = torch.empty_like(echoes)
+        band = chirp_mod.BANDWIDTH / (chirp_mod.C_LIGHT / (2 * chirp_mod.DR))
+        rc_steps = max(3, min(args.steps, 20))
+        with RangeCompressor(ref, p["na"], p["nr"], "hamming", band) as rcomp:
+            for _ in range(3):
+                rcomp(rc_out, raw)
+            torch.cuda.synchronize(dev)
+            r_ms = 0.0
+            for i in range(rc_steps):
+                flush.fill_(float(i))
+                starts[0].record(stream)
+                rcomp(rc_out, raw)
+                ends[0].record(stream)
+                ends[0].synchronize()
+                r_ms += starts[0].elapsed_time(ends[0])
+        rc_bytes = 2 * p["na"] * p["nr"] * 8
+        rc_gbs = rc_bytes * rc_steps / (r_ms / 1e3) / 1e9
+        variants["range_compression"] = {
+            "what": f"matched filter, {p['na']} pulses x {p['nr']} samples, 359-sample chirp, "
+                    "Hamming, FFT size 8192", "steps": rc_steps, "ms_per_step": r_ms / rc_steps,
+            "achieved_gbs": rc_gbs, "roofline": {"bound": "hbm", "peak": HBM_GBS, "unit": "GB/s",
+                                                 "frac": rc_gbs / HBM_GBS,
+                                                 "algorithmic_bytes": rc_bytes},
+        }
+        del raw, rc_out
         variants["sinc8"] = {
             "interp": "8-tap windowed sinc (SARBP_SINC8)", "steps": sinc_steps,
             "value": updates * sinc_steps / (s_ms / 1e3) / 1e9, "unit": UNIT,

@@ -21,8 +21,11 @@ EXPORTS = (
     "sarbp_plan", "sarbp_backproject", "sarbp_backproject_host", "sarbp_destroy",
     "sarbp_status_string", "sarbp_last_error", "sarbp_plan_describe",
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
-    "sarbp_host_transfer_bytes",
+    "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
 )
+
+SARBP_WINDOW_NONE = 0
+SARBP_WINDOW_HAMMING = 1
 
 
 class Params(ctypes.Structure):
@@ -42,6 +45,13 @@ class Params(ctypes.Structure):
                    float(d["x0"]), float(d["y0"]), float(d["z0"]),
                    float(d["dx"]), float(d["dy"]), float(d["r0"]), float(d["dr"]),
                    float(d["wavelength"]), int(d.get("flags", flags)))
+
+
+class RcParams(ctypes.Structure):
+    _fields_ = [
+        ("na", ctypes.c_int32), ("ns", ctypes.c_int32), ("nref", ctypes.c_int32),
+        ("window", ctypes.c_uint32), ("band_fraction", ctypes.c_double),
+    ]
 
 
 class PlanInfo(ctypes.Structure):
@@ -67,6 +77,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_backproject_noalloc.restype = st
     lib.sarbp_host_transfer_bytes.argtypes = [vp, P(ctypes.c_uint64), P(ctypes.c_uint64)]
     lib.sarbp_host_transfer_bytes.restype = st
+    lib.sarbp_rc_plan.argtypes = [P(vp), P(RcParams), vp, vp]
+    lib.sarbp_rc_plan.restype = st
+    lib.sarbp_range_compress.argtypes = [vp, vp, vp, vp]
+    lib.sarbp_range_compress.restype = st
+    lib.sarbp_rc_destroy.argtypes = [vp]
+    lib.sarbp_rc_destroy.restype = st
     lib.sarbp_destroy.argtypes = [vp]
     lib.sarbp_destroy.restype = st
     lib.sarbp_status_string.argtypes = [st]

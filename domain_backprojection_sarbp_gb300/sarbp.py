@@ -178,3 +178,49 @@ def backproject(image, echoes, antenna_pos, params, accumulate=False, stream=Non
         plan.backproject(image, echoes, antenna_pos, accumulate=accumulate, stream=stream)
         torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
     return image
+
+
+class RangeCompressor:
+    """Matched filtering of raw pulses (libsarbp's sarbp_range_compress)."""
+
+    def __init__(self, reference, na, ns, window="none", band_fraction=1.0, stream=None):
+        import torch
+        self._lib = _native.lib()
+        ref = _check_device_tensor(reference, "reference", torch.complex64, (reference.shape[0],))
+        win = {"none": _native.SARBP_WINDOW_NONE, "hamming": _native.SARBP_WINDOW_HAMMING}[window]
+        self.params = _native.RcParams(int(na), int(ns), int(reference.shape[0]), win,
+                                       float(band_fraction))
+        handle = ctypes.c_void_p()
+        st = self._lib.sarbp_rc_plan(ctypes.byref(handle), ctypes.byref(self.params), ref,
+                                     _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            raise SarbpError(st, "sarbp_rc_plan")
+        self._h = handle
+
+    def __call__(self, out, raw, stream=None):
+        """Enqueue rc[n][k] = sum_l raw[n][k + l] conj(ref[l]) (device tensors [na, ns])."""
+        import torch
+        shape = (self.params.na, self.params.ns)
+        o = _check_device_tensor(out, "out", torch.complex64, shape)
+        r = _check_device_tensor(raw, "raw", torch.complex64, shape)
+        st = self._lib.sarbp_range_compress(self._h, o, r, _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            raise SarbpError(st, "sarbp_range_compress")
+        return out
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.sarbp_rc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

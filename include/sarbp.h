@@ -186,6 +186,48 @@ sarbp_status sarbp_set_timing(sarbp_plan_t plan, int enable);
 sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* launches);
 
 /*
+ * Range compression (matched filtering), the step that produces the echoes
+ * backprojection consumes (SARBP-GPU §3.1: FFT every pulse along range,
+ * multiply by the matched filter's frequency response, optionally weighted by
+ * a Hamming window to lower the sidelobes, inverse FFT, all pulses as one
+ * batch). For every pulse n and 0 <= k < ns:
+ *
+ *   rc[n][k] = sum_{l=0}^{nref-1} raw[n][k + l] * conj(ref[l])   (raw = 0 beyond ns)
+ *
+ * computed through FFTs of size N, the smallest power of two >= ns + nref - 1
+ * (no circular wrap), N <= 16384. With SARBP_WINDOW_HAMMING the filter
+ * spectrum is weighted by 0.54 + 0.46 cos(2 pi f / b) for |f| <= b/2 and 0
+ * outside (f = signed frequency in cycles per sample, b = band_fraction, the
+ * chirp bandwidth over the sampling rate); SARBP_WINDOW_NONE is the plain
+ * matched filter.
+ */
+#define SARBP_WINDOW_NONE 0u
+#define SARBP_WINDOW_HAMMING 1u
+
+typedef struct sarbp_rc_params {
+    int32_t na;            /* pulses                                               */
+    int32_t ns;            /* samples per pulse, input and output                  */
+    int32_t nref;          /* samples of the reference (transmitted) pulse         */
+    uint32_t window;       /* SARBP_WINDOW_NONE or SARBP_WINDOW_HAMMING            */
+    double band_fraction;  /* b in (0, 1] for the Hamming window                   */
+} sarbp_rc_params;
+
+typedef struct sarbp_rc_plan_s* sarbp_rc_plan_t;
+
+/* Build the filter spectrum from `ref` (device, complex64 [nref], read only
+   during this call's work on `stream`) and allocate twiddles (N x 12 bytes).
+   INVALID_ARG for bad sizes, N > 16384, an unknown window or b outside (0, 1]. */
+sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const void* ref,
+                           void* stream);
+
+/* Enqueue the compression of raw (device, complex64 [na][ns]) into out
+   (device, complex64 [na][ns]); the two must not overlap. One CTA per pulse. */
+sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* raw, void* stream);
+
+/* Free the plan. NULL is accepted. */
+sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan);
+
+/*
  * sarbp_backproject_noalloc - the same backprojection without any device
  * memory allocation. The page has no counterpart: this is an interface for
  * callers that cannot allocate GPU memory themselves, for example a plug-in
