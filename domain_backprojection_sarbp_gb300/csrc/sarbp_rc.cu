@@ -13,11 +13,11 @@
 // |f| <= b/2 (f in cycles per sample), zero outside it.
 //
 // One CTA per pulse holds its zero-padded row in shared memory. The forward
-// transform is an in-place radix-2 decimation in frequency (natural order in,
-// bit-reversed out); the filter spectrum H is stored in bit-reversed order, so
-// the product needs no reordering; the inverse is an in-place decimation in
-// time (bit-reversed in, natural out). The plan builds H with the same
-// forward kernel on the zero-padded reference.
+// transform is an in-place radix-4 decimation in frequency (natural order in,
+// digit-reversed out); the filter spectrum H is stored in that same order, so
+// the product needs no reordering; the inverse mirrors the forward passes
+// (digit-reversed in, natural out). The plan builds H with the same forward
+// transform on the zero-padded reference.
 #include "../../include/sarbp.h"
 #include "sarbp_internal.h"
 
@@ -36,43 +36,97 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b)
     return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
 }
 
-// Forward DIF, in place: x natural -> X bit-reversed. tw[m] = exp(-j 2 pi m / N), m < N/2.
+// Forward transform, in place: radix-4 decimation-in-frequency passes over
+// spans N, N/4, ..., then one radix-2 pass of span 2 when log2 N is odd. The
+// result at position p is X[sigma(p)], sigma the mixed digit reversal below.
+// tw[t] = exp(-j 2 pi t / N), t < N.
 __device__ void dif_forward(float2* x, int n, int log2n, const float2* __restrict__ tw)
 {
-    for (int s = 0; s < log2n; ++s) {
-        const int h = n >> (s + 1);                 // butterfly span
-        const int tstep = 1 << s;                   // twiddle stride: N / (2h)
+    const int n4 = log2n / 2;
+    for (int lvl = 0; lvl < n4; ++lvl) {
+        const int lq = log2n - 2 * lvl - 2;          // q = span / 4 = 2^lq
+        const int q = 1 << lq;
+        const int tstep = 1 << (2 * lvl);            // N / span
+        for (int b = threadIdx.x; b < n / 4; b += blockDim.x) {
+            const int j = b & (q - 1);
+            const int base = ((b >> lq) << (lq + 2)) + j;
+            const float2 x0 = x[base], x1 = x[base + q], x2 = x[base + 2 * q], x3 = x[base + 3 * q];
+            const float2 a0 = make_float2(x0.x + x2.x, x0.y + x2.y);
+            const float2 a1 = make_float2(x0.x - x2.x, x0.y - x2.y);
+            const float2 a2 = make_float2(x1.x + x3.x, x1.y + x3.y);
+            const float2 a3 = make_float2(x1.y - x3.y, x3.x - x1.x);      // -j (x1 - x3)
+            x[base] = make_float2(a0.x + a2.x, a0.y + a2.y);
+            const int t = j * tstep;
+            x[base + q] = cmul(make_float2(a1.x + a3.x, a1.y + a3.y), __ldg(tw + t));
+            x[base + 2 * q] = cmul(make_float2(a0.x - a2.x, a0.y - a2.y), __ldg(tw + 2 * t));
+            x[base + 3 * q] = cmul(make_float2(a1.x - a3.x, a1.y - a3.y), __ldg(tw + 3 * t));
+        }
+        __syncthreads();
+    }
+    if (log2n & 1) {                                 // span 2: no twiddle
         for (int b = threadIdx.x; b < n / 2; b += blockDim.x) {
-            const int j = b & (h - 1);
-            const int i = ((b >> (log2n - 1 - s)) << (log2n - s)) + j;
-            const float2 a = x[i], c = x[i + h];
-            x[i] = make_float2(a.x + c.x, a.y + c.y);
-            x[i + h] = cmul(make_float2(a.x - c.x, a.y - c.y), __ldg(tw + j * tstep));
+            const float2 a = x[2 * b], c = x[2 * b + 1];
+            x[2 * b] = make_float2(a.x + c.x, a.y + c.y);
+            x[2 * b + 1] = make_float2(a.x - c.x, a.y - c.y);
         }
         __syncthreads();
     }
 }
 
-// Inverse DIT, in place: X bit-reversed -> x natural (unscaled), conj twiddles.
+// Inverse of dif_forward up to the factor N: the same passes mirrored
+// (conjugate twiddles first, then the inverse 4-point transform).
 __device__ void dit_inverse(float2* x, int n, int log2n, const float2* __restrict__ tw)
 {
-    for (int s = log2n - 1; s >= 0; --s) {
-        const int h = n >> (s + 1);
-        const int tstep = 1 << s;
+    const int n4 = log2n / 2;
+    if (log2n & 1) {
         for (int b = threadIdx.x; b < n / 2; b += blockDim.x) {
-            const int j = b & (h - 1);
-            const int i = ((b >> (log2n - 1 - s)) << (log2n - s)) + j;
-            const float2 w = __ldg(tw + j * tstep);
-            const float2 c = cmul(x[i + h], make_float2(w.x, -w.y));
-            const float2 a = x[i];
-            x[i] = make_float2(a.x + c.x, a.y + c.y);
-            x[i + h] = make_float2(a.x - c.x, a.y - c.y);
+            const float2 a = x[2 * b], c = x[2 * b + 1];
+            x[2 * b] = make_float2(a.x + c.x, a.y + c.y);
+            x[2 * b + 1] = make_float2(a.x - c.x, a.y - c.y);
+        }
+        __syncthreads();
+    }
+    for (int lvl = n4 - 1; lvl >= 0; --lvl) {
+        const int lq = log2n - 2 * lvl - 2;
+        const int q = 1 << lq;
+        const int tstep = 1 << (2 * lvl);
+        for (int b = threadIdx.x; b < n / 4; b += blockDim.x) {
+            const int j = b & (q - 1);
+            const int base = ((b >> lq) << (lq + 2)) + j;
+            const int t = j * tstep;
+            const float2 w1 = __ldg(tw + t), w2 = __ldg(tw + 2 * t), w3 = __ldg(tw + 3 * t);
+            const float2 z0 = x[base];
+            const float2 z1 = cmul(x[base + q], make_float2(w1.x, -w1.y));
+            const float2 z2 = cmul(x[base + 2 * q], make_float2(w2.x, -w2.y));
+            const float2 z3 = cmul(x[base + 3 * q], make_float2(w3.x, -w3.y));
+            const float2 b0 = make_float2(z0.x + z2.x, z0.y + z2.y);
+            const float2 b1 = make_float2(z0.x - z2.x, z0.y - z2.y);
+            const float2 b2 = make_float2(z1.x + z3.x, z1.y + z3.y);
+            const float2 b3 = make_float2(z3.y - z1.y, z1.x - z3.x);     // +j (z1 - z3)
+            x[base] = make_float2(b0.x + b2.x, b0.y + b2.y);
+            x[base + q] = make_float2(b1.x + b3.x, b1.y + b3.y);
+            x[base + 2 * q] = make_float2(b0.x - b2.x, b0.y - b2.y);
+            x[base + 3 * q] = make_float2(b1.x - b3.x, b1.y - b3.y);
         }
         __syncthreads();
     }
 }
 
-// The filter: H[p] = conj(FFT(ref)[k]) * W(k) at bit-reversed position p, k = bitrev(p).
+// Natural frequency index held at position p after dif_forward: the base-4
+// digits of p (most significant first) become the least significant digits
+// of the index, and the final base-2 digit, if any, the most significant.
+__device__ __forceinline__ int natural_index(int p, int log2n)
+{
+    const int n4 = log2n / 2;
+    int k = 0;
+    for (int lvl = 0; lvl < n4; ++lvl)
+        k |= ((p >> (log2n - 2 * lvl - 2)) & 3) << (2 * lvl);
+    if (log2n & 1)
+        k |= (p & 1) << (2 * n4);
+    return k;
+}
+
+// The filter: H[p] = conj(FFT(ref)[k]) * W(k) at position p, k = natural_index(p).
 __global__ void __launch_bounds__(RC_THREADS) rc_filter_kernel(const float2* __restrict__ ref, int nref,
                                                                int n, int log2n,
                                                                const float2* __restrict__ tw,
@@ -85,7 +139,7 @@ __global__ void __launch_bounds__(RC_THREADS) rc_filter_kernel(const float2* __r
     __syncthreads();
     dif_forward(row, n, log2n, tw);
     for (int p = threadIdx.x; p < n; p += blockDim.x) {
-        const int k = (int)(__brev((unsigned)p) >> (32 - log2n));
+        const int k = natural_index(p, log2n);
         float w = 1.0f;
         if (window == SARBP_WINDOW_HAMMING) {
             const float f = (float)(k < n / 2 ? k : k - n) / (float)n;
@@ -124,8 +178,8 @@ struct sarbp_rc_plan_s {
     sarbp_rc_params p{};
     int n = 0, log2n = 0;
     int device = -1;
-    float2* tw = nullptr;      // N/2 twiddles
-    float2* h = nullptr;       // N filter coefficients, bit-reversed order
+    float2* tw = nullptr;      // N twiddles
+    float2* h = nullptr;       // N filter coefficients, in the forward transform's order
 };
 
 extern "C" {
@@ -174,14 +228,14 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
         e = cudaFuncSetAttribute(rc_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
     if (e == cudaSuccess)
-        e = cudaMalloc(&plan->tw, (size_t)plan->n / 2 * sizeof(float2));
+        e = cudaMalloc(&plan->tw, (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess)
         e = cudaMalloc(&plan->h, (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess) {
         // twiddles in float64, rounded once
-        std::vector<float2> tw((size_t)plan->n / 2);
+        std::vector<float2> tw((size_t)plan->n);
         const double pi = 3.14159265358979323846;
-        for (int m = 0; m < plan->n / 2; ++m) {
+        for (int m = 0; m < plan->n; ++m) {
             const double a = -2.0 * pi * (double)m / (double)plan->n;
             tw[m] = make_float2((float)std::cos(a), (float)std::sin(a));
         }
