@@ -14,6 +14,9 @@ checks that each such pin rejects a broken copy of the oracle
 of the windowed-sinc kernel, reconstruction of a band-limited signal, the
 stencil window rule, linearity, pulse-order invariance and focusing
 (tests/test_oracle_sinc_pins.py), with its own planted mistakes.
+``backproject(interp="nearest")`` - pinned by on-sample values, the rounding
+boundary at half a bin, the window rule and the generic invariants
+(tests/test_oracle_nearest_pins.py), with its own planted mistakes.
 """
 
 from __future__ import annotations
@@ -65,7 +68,7 @@ def build(force: bool = False) -> str:
 
 def load_library(path: str) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
-    for name in ("oracle_backproject", "oracle_backproject_sinc8"):
+    for name in ("oracle_backproject", "oracle_backproject_sinc8", "oracle_backproject_nearest"):
         fn = getattr(lib, name, None)
         if fn is None:
             continue
@@ -99,12 +102,14 @@ def backproject(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
     """FP64 image at ``pixels`` (linear iy*nx+ix); the full [ny, nx] image if None.
 
     ``echoes`` complex64 [na, nr]; ``antenna_pos`` float64 [na, 3].
-    ``interp`` is "linear" (the page's kernel) or "sinc8" (8-tap windowed sinc).
+    ``interp`` is "linear" (the page's kernel), "sinc8" (8-tap windowed sinc) or
+    "nearest" (nearest sample).
     With ``return_info`` also returns (seconds, threads used).
     """
     library = library or lib()
     fn = {"linear": library.oracle_backproject,
-          "sinc8": library.oracle_backproject_sinc8}[interp]
+          "sinc8": library.oracle_backproject_sinc8,
+          "nearest": library.oracle_backproject_nearest}[interp]
     nx, ny, na, nr = (int(params[k]) for k in ("nx", "ny", "na", "nr"))
     echoes = np.ascontiguousarray(echoes, dtype=np.complex64).reshape(na, nr)
     pos = np.ascontiguousarray(antenna_pos, dtype=np.float64).reshape(na, 3)

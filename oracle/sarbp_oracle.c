@@ -121,6 +121,41 @@ static void backproject_pixel_sinc8(const oracle_geometry* g, const float* echo,
     out[1] = acc_im;
 }
 
+/* One pixel, all pulses, nearest-neighbour interpolation. */
+static void backproject_pixel_nearest(const oracle_geometry* g, const float* echo,
+                                      const double* antenna_pos, int64_t pixel, double* out)
+{
+    const int64_t ix = pixel % g->nx;
+    const int64_t iy = pixel / g->nx;
+    const double x = g->x0 + (double)ix * g->dx;
+    const double y = g->y0 + (double)iy * g->dy;
+    const double z = g->z0;
+    double acc_re = 0.0;
+    double acc_im = 0.0;
+
+    for (int64_t n = 0; n < g->na; ++n) {
+        const double* a = antenna_pos + 3 * n;
+        const double ddx = x - a[0];
+        const double ddy = y - a[1];
+        const double ddz = z - a[2];
+        const double range = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
+
+        const double u = (range - g->r0) / g->dr;
+        const double k = floor(u + 0.5);
+        if (!(k >= 0.0 && k <= (double)(g->nr - 1)))
+            continue;                      /* nearest sample not recorded */
+        const float* e = echo + 2 * (n * g->nr + (int64_t)k);
+
+        const double phase = 4.0 * ORACLE_PI * range / g->wavelength;
+        const double c = cos(phase);
+        const double s = sin(phase);
+        acc_re += (double)e[0] * c - (double)e[1] * s;
+        acc_im += (double)e[0] * s + (double)e[1] * c;
+    }
+    out[0] = acc_re;
+    out[1] = acc_im;
+}
+
 typedef struct {
     const oracle_geometry* g;
     const float* echo;
@@ -210,4 +245,12 @@ int oracle_backproject_sinc8(const oracle_geometry* g, const float* echo,
 {
     return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads,
                       backproject_pixel_sinc8);
+}
+
+int oracle_backproject_nearest(const oracle_geometry* g, const float* echo,
+                               const double* antenna_pos, const int64_t* pixels,
+                               int64_t npix, double* out, int nthreads)
+{
+    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads,
+                      backproject_pixel_nearest);
 }

@@ -58,6 +58,15 @@ int oracle_backproject_sinc8(const oracle_geometry* g, const float* echo,
                              const double* antenna_pos, const int64_t* pixels,
                              int64_t npix, double* out, int nthreads);
 
+/*
+ * Same sum with nearest-neighbour interpolation (SARBP-GPU §2.2: the fastest,
+ * least accurate of the three choices): k = floor(u + 1/2), w_n = e[n][k],
+ * and w_n = 0 unless 0 <= k <= nr - 1.
+ */
+int oracle_backproject_nearest(const oracle_geometry* g, const float* echo,
+                               const double* antenna_pos, const int64_t* pixels,
+                               int64_t npix, double* out, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

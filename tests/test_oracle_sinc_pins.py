@@ -33,8 +33,8 @@ MUTATIONS = {
     "sinc_unnormalised": [("sin(ORACLE_PI * t) / (ORACLE_PI * t)", "sin(t) / t")],
     "window_rule_loose": [("k - 3.0 >= 0.0 && k + 4.0 <= (double)(g->nr - 1)",
                            "k - 2.0 >= 0.0 && k + 4.0 <= (double)(g->nr - 1)")],
-    "sinc_phase_sign": [("acc_im += w_re * s + w_im * c;\n    }\n    out[0] = acc_re;\n    out[1] = acc_im;\n}\n\ntypedef",
-                         "acc_im += -w_re * s + w_im * c;\n    }\n    out[0] = acc_re;\n    out[1] = acc_im;\n}\n\ntypedef")],
+    "sinc_phase_sign": [("acc_im += w_re * s + w_im * c;\n    }\n    out[0] = acc_re;\n    out[1] = acc_im;\n}\n\n/* One pixel, all pulses, nearest",
+                         "acc_im += -w_re * s + w_im * c;\n    }\n    out[0] = acc_re;\n    out[1] = acc_im;\n}\n\n/* One pixel, all pulses, nearest")],
 }
 
 
