@@ -270,20 +270,30 @@ def run_ours(args, scene, rank, world, local, dist):
     # the windowed-sinc variant on the same scene (device-resident, L2 flushed)
     variants = {}
     if not args.no_variants:
-        sinc_steps = max(3, min(args.steps, 20))
-        for _ in range(3):
-            plan.backproject(image, echoes, pos, interp="sinc8")
-        torch.cuda.synchronize(dev)
-        plan.kernel_times()
-        s_ms = 0.0
-        for i in range(sinc_steps):
-            flush.fill_(float(i))
-            starts[0].record(stream)
-            plan.backproject(image, echoes, pos, interp="sinc8")
-            ends[0].record(stream)
-            ends[0].synchronize()
-            s_ms += starts[0].elapsed_time(ends[0])
-        sinc_main_ms, sinc_launches = plan.kernel_times()
+        def time_interp(interp, label):
+            steps_v = max(3, min(args.steps, 20))
+            for _ in range(3):
+                plan.backproject(image, echoes, pos, interp=interp)
+            torch.cuda.synchronize(dev)
+            plan.kernel_times()
+            total = 0.0
+            for i in range(steps_v):
+                flush.fill_(float(i))
+                starts[0].record(stream)
+                plan.backproject(image, echoes, pos, interp=interp)
+                ends[0].record(stream)
+                ends[0].synchronize()
+                total += starts[0].elapsed_time(ends[0])
+            main_ms_v, launches_v = plan.kernel_times()
+            variants[interp] = {
+                "interp": label, "steps": steps_v,
+                "value": updates * steps_v / (total / 1e3) / 1e9, "unit": UNIT,
+                "ms_per_step": total / steps_v,
+                "main_kernel_gupd": updates / (main_ms_v / max(launches_v, 1) / 1e3) / 1e9,
+            }
+
+        time_interp("sinc8", "8-tap windowed sinc (SARBP_SINC8)")
+        time_interp("nearest", "nearest neighbour (SARBP_NEAREST)")
         # range compression of this scene's shape (SARBP-GPU §3.1): raw chirps -> echoes
         from domain_backprojection_sarbp_gb300 import RangeCompressor
         from synth import chirp as chirp_mod
@@ -314,12 +324,6 @@ def run_ours(args, scene, rank, world, local, dist):
                                                  "algorithmic_bytes": rc_bytes},
         }
         del raw, rc_out
-        variants["sinc8"] = {
-            "interp": "8-tap windowed sinc (SARBP_SINC8)", "steps": sinc_steps,
-            "value": updates * sinc_steps / (s_ms / 1e3) / 1e9, "unit": UNIT,
-            "ms_per_step": s_ms / sinc_steps,
-            "main_kernel_gupd": updates / (sinc_main_ms / max(sinc_launches, 1) / 1e3) / 1e9,
-        }
     plan.close()
 
     sms = info["sms"]

@@ -16,6 +16,7 @@ SARBP_ERR_UNSUPPORTED_DEVICE = 5
 SARBP_ERR_SCRATCH_TOO_SMALL = 6
 SARBP_ACCUMULATE = 1
 SARBP_SINC8 = 2
+SARBP_NEAREST = 4
 
 EXPORTS = (
     "sarbp_plan", "sarbp_backproject", "sarbp_backproject_host", "sarbp_destroy",

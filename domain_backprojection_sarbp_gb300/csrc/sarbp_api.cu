@@ -79,7 +79,9 @@ sarbp_status check_geometry(const sarbp_params* p)
         return SARBP_ERR_INVALID_ARG;
     if (!(isfin(p->wavelength) && p->wavelength > 0))
         return SARBP_ERR_INVALID_ARG;
-    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8))
+    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8 | SARBP_NEAREST))
+        return SARBP_ERR_INVALID_ARG;
+    if ((p->flags & SARBP_SINC8) && (p->flags & SARBP_NEAREST))
         return SARBP_ERR_INVALID_ARG;
     return SARBP_OK;
 }
@@ -218,7 +220,7 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
     e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "table kernel launch");
-    if (k.flags & SARBP_SINC8) {
+    if (k.flags & (SARBP_SINC8 | SARBP_NEAREST)) {
         e = launch_psi(k, plan->psi, s);
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "phasor kernel launch");
@@ -288,7 +290,9 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
     sarbp_status st = check_sizes(p);
     if (st != SARBP_OK)
         return st;
-    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8))
+    if (p->flags & ~(SARBP_ACCUMULATE | SARBP_SINC8 | SARBP_NEAREST))
+        return SARBP_ERR_INVALID_ARG;
+    if ((p->flags & SARBP_SINC8) && (p->flags & SARBP_NEAREST))
         return SARBP_ERR_INVALID_ARG;
     if (!(isfin(p->wavelength) && p->wavelength > 0))
         return SARBP_ERR_INVALID_ARG;
@@ -597,7 +601,7 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
     st = check_geometry(params);
     if (st != SARBP_OK)
         return st;
-    if (params->flags & SARBP_SINC8)
+    if (params->flags & (SARBP_SINC8 | SARBP_NEAREST))
         return SARBP_ERR_INVALID_ARG;          // linear interpolation only
     const long long pixels = (long long)params->nx * params->ny;
     if (pixels > 0 && (!image || !aligned8(image)))

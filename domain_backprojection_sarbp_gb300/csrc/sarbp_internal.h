@@ -31,8 +31,9 @@ constexpr int MIN_PULSES_PER_CTA = 32;     // keeps tiny problems from over-spli
 constexpr int KLO_INVALID = INT32_MIN;     // pulse with a non-finite antenna position
 
 enum RecordKind : int { REC_SKIP = 0, REC_FAST = 1, REC_EXACT = 2 };
-constexpr unsigned FLAG_ACCUMULATE = 1u;   // same values as SARBP_ACCUMULATE / SARBP_SINC8
+constexpr unsigned FLAG_ACCUMULATE = 1u;   // same values as SARBP_ACCUMULATE / _SINC8 / _NEAREST
 constexpr unsigned FLAG_SINC8 = 2u;
+constexpr unsigned FLAG_NEAREST = 4u;
 
 // Launch constants, computed on the host in float64 for every call.
 struct BpConst {

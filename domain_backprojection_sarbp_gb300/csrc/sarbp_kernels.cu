@@ -47,6 +47,8 @@ namespace {
 constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/round(x) in the mantissa
 constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 
+enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2 };
+
 struct __align__(16) Record {
     float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
     float4 b;  // c03, c04, c10, c11
@@ -57,9 +59,10 @@ struct __align__(16) Record {
 // ---------------------------------------------------------------------------
 // Echo table: one block per pulse.
 // ---------------------------------------------------------------------------
-// Linear interpolation: entries (A_k, D_k / c) as above. Windowed-sinc
-// interpolation: entries are plain sample pairs (e_k, e_{k+1}), zero where a
-// sample lies outside 0 .. nr - 1, and the phase comes from psi_k (psi_kernel).
+// Linear interpolation: entries (A_k, D_k / c) as above. Windowed-sinc and
+// nearest-neighbour interpolation: entries are plain sample pairs
+// (e_k, e_{k+1}), zero where a sample lies outside 0 .. nr - 1, and the phase
+// comes from psi_k (psi_kernel).
 template <bool SINC>
 __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __restrict__ echo,
                                                     const double* __restrict__ pos,
@@ -250,7 +253,7 @@ struct PulseState {
     int mode;
 };
 
-template <bool SINC>
+template <int INTERP>
 __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record& rec,
                                                   const float4* row, float jf, float jf2,
                                                   float jf3, float jf4)
@@ -281,7 +284,7 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const int bin0 = __float_as_int(rd.y);               // row index of absolute bin 0
     // both bins must hold recorded samples: the identity behind the hinge
     // form does not hold across the zero entries outside 0 <= k <= nr - 2
-    const bool hinge = !SINC && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
+    const bool hinge = INTERP == INTERP_LINEAR && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
                        idx0 + 1 <= bin0 + k.nr - 2;
     PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
@@ -560,13 +563,95 @@ __device__ __forceinline__ void sinc_exact_pulse(const BpConst& k, const Record&
     }
 }
 
-template <bool SINC>
+// ---------------------------------------------------------------------------
+// Nearest-neighbour interpolation: k = floor(u + 1/2), value e_k psi(u) with
+// psi(u) = psi_k exp(j c (u - k)), u - k in [-1/2, 1/2).
+// ---------------------------------------------------------------------------
+template <bool CHECK_ROW>
+__device__ __forceinline__ void nearest_pixel(const BpConst& k, float ub, int kb, int bin0,
+                                              const float4* row, const float2* __restrict__ psi,
+                                              float& re, float& im)
+{
+    if (CHECK_ROW && !(ub > -1.0e6f && ub < 1.0e6f))
+        return;
+    const float tt = __fadd_rd(ub + 0.5f, MAGIC);
+    const float d = ub - (tt - MAGIC);                  // u - k in [-1/2, 1/2)
+    const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
+    const int kabs = kr - bin0;
+    if (kabs < 0 || kabs > k.nr - 1)
+        return;                                         // nearest sample not recorded
+    if (CHECK_ROW && (kr < 0 || kr > k.W - 1))
+        return;
+    const float2 e = __ldg(reinterpret_cast<const float2*>(row) + 2 * (size_t)kr);
+    const float2 ps = __ldg(psi + kabs);
+    float sn, cs;
+    __sincosf(d * k.c_phase, &sn, &cs);
+    const float zr = ps.x * cs - ps.y * sn;
+    const float zi = ps.x * sn + ps.y * cs;
+    re = fmaf(e.x, zr, fmaf(-e.y, zi, re));
+    im = fmaf(e.x, zi, fmaf(e.y, zr, im));
+}
+
+__device__ __forceinline__ void nearest_pulse(const BpConst& k, const PulseState& st, const float4* row,
+                                              const float2* __restrict__ psi,
+                                              float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float i = k.i0 + (float)m;
+        const float ub = fmaf(i, fmaf(i, e2, e1), e0);
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        nearest_pixel<false>(k, ub, st.kb, st.bin0, row, psi, re, im);
+    }
+}
+
+__device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Record& rec,
+                                                    const float4* row, const double* __restrict__ a,
+                                                    double xc, double yrow,
+                                                    const float2* __restrict__ psi,
+                                                    float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const double vx = xc - a[0], vy = yrow - a[1], vz = k.z0 - a[2];
+    const double r2 = vx * vx + vy * vy + vz * vz;
+    const double r = sqrt(r2);
+    const double u = (r - k.r0) * k.inv_dr;
+    if (!(fabs(u) < 1.0e9))
+        return;
+    const double ku = floor(u);
+    const int bin0 = __float_as_int(rec.d.y);
+    const int kbase = (int)ku + bin0;
+    const float frac0 = (float)(u - ku);
+    const float two_vx = (float)(2.0 * vx), rf = (float)r, r2f = (float)r2;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
+        const float s = qx * (two_vx + qx);
+        const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
+        const float den = rf + rp;
+        const float dr_m = den > 0.0f ? s / den : 0.0f;
+        const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        nearest_pixel<true>(k, ub, kbase, bin0, row, psi, re, im);
+    }
+}
+
+template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
                                             double yrow, const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    if (SINC) {
+    if (INTERP == INTERP_NEAREST) {
+        if (st.mode == MODE_GATHER)
+            nearest_pulse(k, st, row, psi, accre, accim);
+        else if (st.mode == MODE_EXACT)
+            nearest_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
+        return;
+    }
+    if (INTERP == INTERP_SINC8) {
         if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
@@ -589,7 +674,7 @@ __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
 // ---------------------------------------------------------------------------
 // Main kernel: persistent, one contiguous range of (tile, pulse) units per CTA.
 // ---------------------------------------------------------------------------
-template <bool SINC>
+template <int INTERP>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, const double* __restrict__ pos,
                                                         const float4* __restrict__ table,
                                                         const int* __restrict__ klo,
@@ -637,19 +722,19 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const float4* rows = table + (size_t)c0 * k.W;
             // Two pulse states in ping-pong: the state of pulse p + 1 is built
             // while pulse p is applied, with no copy between them.
-            PulseState sa = pulse_setup<SINC>(k, s_rec[0], rows, jf, jf2, jf3, jf4);
+            PulseState sa = pulse_setup<INTERP>(k, s_rec[0], rows, jf, jf2, jf3, jf4);
 #pragma unroll 1
             for (int p = 0; p < cnt; p += 2) {
                 const int p1 = min(p + 1, cnt - 1);
                 const PulseState sb =
-                    pulse_setup<SINC>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
-                apply_pulse<SINC>(k, sa, s_rec[p], rows + (size_t)p * k.W,
+                    pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
-                sa = pulse_setup<SINC>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
-                apply_pulse<SINC>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
+                sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
+                apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, psi, accre, accim);
             }
         }
@@ -800,7 +885,7 @@ cudaError_t noalloc_scratch(void** ptr)
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
                          int* klo, cudaStream_t s)
 {
-    if (k.flags & FLAG_SINC8)
+    if (k.flags & (FLAG_SINC8 | FLAG_NEAREST))
         table_kernel<true><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
     else
         table_kernel<false><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
@@ -818,9 +903,11 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
                                const float2* psi, cudaStream_t s)
 {
     if (k.flags & FLAG_SINC8)
-        bp_kernel<true><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+        bp_kernel<INTERP_SINC8><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+    else if (k.flags & FLAG_NEAREST)
+        bp_kernel<INTERP_NEAREST><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
     else
-        bp_kernel<false><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+        bp_kernel<INTERP_LINEAR><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
     return cudaGetLastError();
 }
 
@@ -832,11 +919,14 @@ cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image
 
 cudaError_t backproject_occupancy(int* ctas_per_sm)
 {
-    int a = 0, b = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, bp_kernel<false>, THREADS, 0);
+    int a = 0, b = 0, c = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, bp_kernel<INTERP_LINEAR>,
+                                                                  THREADS, 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, bp_kernel<true>, THREADS, 0);
-    *ctas_per_sm = std::min(a, b);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, bp_kernel<INTERP_SINC8>, THREADS, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, bp_kernel<INTERP_NEAREST>, THREADS, 0);
+    *ctas_per_sm = std::min(a, std::min(b, c));
     return e;
 }
 

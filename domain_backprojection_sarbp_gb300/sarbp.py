@@ -13,7 +13,7 @@ import ctypes
 import numpy as np
 
 from . import _native
-from ._native import Params, PlanInfo, SARBP_ACCUMULATE, SARBP_SINC8
+from ._native import Params, PlanInfo, SARBP_ACCUMULATE, SARBP_NEAREST, SARBP_SINC8
 
 
 class SarbpError(RuntimeError):
@@ -32,8 +32,10 @@ def _params(p, accumulate=False, interp="linear") -> Params:
         out.flags |= SARBP_ACCUMULATE
     if interp == "sinc8":
         out.flags |= SARBP_SINC8
+    elif interp == "nearest":
+        out.flags |= SARBP_NEAREST
     elif interp != "linear":
-        raise ValueError(f"interp must be 'linear' or 'sinc8', got {interp!r}")
+        raise ValueError(f"interp must be 'linear', 'sinc8' or 'nearest', got {interp!r}")
     return out
 
 
@@ -103,7 +105,7 @@ class Plan:
         """Enqueue I(p) = sum_n w_n exp(+j 4 pi R_n / lambda) on ``stream`` (device tensors).
 
         image complex64 [ny, nx]; echoes complex64 [na, nr]; antenna_pos float64 [na, 3].
-        ``interp``: "linear" or "sinc8" (8-tap windowed sinc).
+        ``interp``: "linear", "sinc8" (8-tap windowed sinc) or "nearest".
         """
         import torch
         p = _params(params if params is not None else self.params, accumulate, interp)

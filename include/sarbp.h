@@ -74,6 +74,10 @@ typedef enum sarbp_status {
                                 h(t) = sinc(t) (1/2 + 1/2 cos(2 pi t / 8)), zero unless
                                 the whole stencil lies in 0 .. nr-1                    */
 
+#define SARBP_NEAREST 4u     /* nearest-neighbour interpolation (SARBP-GPU §2.2: fastest,
+                                least accurate): w = e[k], k = floor(u + 1/2), zero
+                                unless 0 <= k <= nr-1. Not combinable with SINC8.  */
+
 typedef struct sarbp_params {
     int32_t nx, ny;       /* image width (x) and height (y), pixels, >= 0             */
     int32_t na, nr;       /* pulses and range bins, >= 0                              */
@@ -82,7 +86,8 @@ typedef struct sarbp_params {
     double r0, dr;        /* range of bin k is r0 + k*dr, metres; dr > 0              */
     double wavelength;    /* carrier wavelength lambda = c / fc, metres, > 0
                              (SARBP-GPU §4.2: the carrier, not the bandwidth one)     */
-    uint32_t flags;       /* SARBP_ACCUMULATE, SARBP_SINC8, or 0                      */
+    uint32_t flags;       /* SARBP_ACCUMULATE with at most one of SARBP_SINC8,
+                             SARBP_NEAREST (default: linear interpolation)          */
 } sarbp_params;
 
 typedef struct sarbp_plan_s* sarbp_plan_t;
@@ -110,7 +115,8 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p);
  *
  * image        device pointer, complex64 [ny][nx], caller-owned, 8-byte aligned.
  *              Overwritten, or added into when params->flags has SARBP_ACCUMULATE.
- *              With SARBP_SINC8 the echo is interpolated with the windowed sinc.
+ *              With SARBP_SINC8 or SARBP_NEAREST the echo is interpolated with
+ *              the windowed sinc or the nearest sample instead of linearly.
  * echoes       device pointer, complex64 [na][nr], caller-owned, 8-byte aligned.
  * antenna_pos  device pointer, float64 [na][3], caller-owned, 8-byte aligned.
  * params       host pointer; nx, ny, na, nr, dx, dy, dr must equal the plan's
@@ -238,7 +244,7 @@ sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan);
  *
  * image, echoes, antenna_pos, params, stream: as for sarbp_backproject. All
  * sizes come from params; no plan is involved. Linear interpolation only:
- * SARBP_SINC8 is rejected with SARBP_ERR_INVALID_ARG.
+ * SARBP_SINC8 and SARBP_NEAREST are rejected with SARBP_ERR_INVALID_ARG.
  *
  * Scratch: a fixed, file-scope device array of SARBP_NOALLOC_SCRATCH_BYTES
  * (16 MiB) that every GPU loading the library holds until the process exits.

@@ -53,7 +53,7 @@ def _params(**kw):
 @pytest.mark.parametrize("bad", [
     dict(nx=-1), dict(ny=-3), dict(na=-1), dict(nr=-2), dict(dx=0.0), dict(dy=-0.5),
     dict(dr=0.0), dict(dr=float("nan")), dict(dx=float("inf")), dict(wavelength=0.0),
-    dict(wavelength=float("nan")), dict(flags=4), dict(nx=1 << 16, ny=1 << 16),
+    dict(wavelength=float("nan")), dict(flags=8), dict(flags=6), dict(nx=1 << 16, ny=1 << 16),
 ])
 def test_plan_rejects_bad_params(lib, bad):
     h = ctypes.c_void_p(123)
