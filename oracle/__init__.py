@@ -14,6 +14,9 @@ checks that each such pin rejects a broken copy of the oracle
 of the windowed-sinc kernel, reconstruction of a band-limited signal, the
 stencil window rule, linearity, pulse-order invariance and focusing
 (tests/test_oracle_sinc_pins.py), with its own planted mistakes.
+``backproject_heights`` - pinned by reduction to ``backproject`` (zero and
+constant heights), a hand-derived value on a raised pixel, and focusing of
+targets on a rough surface (tests/test_oracle_heights_pins.py).
 ``backproject(interp="nearest")`` - pinned by on-sample values, the rounding
 boundary at half a bin, the window rule and the generic invariants
 (tests/test_oracle_nearest_pins.py), with its own planted mistakes.
@@ -77,6 +80,13 @@ def load_library(path: str) -> ctypes.CDLL:
             ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
         ]
+    fn = getattr(lib, "oracle_backproject_heights", None)
+    if fn is not None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+        ]
     return lib
 
 
@@ -130,3 +140,29 @@ def backproject(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
     if full:
         img = img.reshape(ny, nx)
     return (img, secs, used) if return_info else img
+
+
+def backproject_heights(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
+                        heights: np.ndarray, pixels: np.ndarray | None = None, threads: int = 0,
+                        library: ctypes.CDLL | None = None):
+    """FP64 linear-interpolation image over pixels raised to z0 + heights[iy, ix]
+    (``heights`` float32 [ny, nx])."""
+    library = library or lib()
+    nx, ny, na, nr = (int(params[k]) for k in ("nx", "ny", "na", "nr"))
+    echoes = np.ascontiguousarray(echoes, dtype=np.complex64).reshape(na, nr)
+    pos = np.ascontiguousarray(antenna_pos, dtype=np.float64).reshape(na, 3)
+    hts = np.ascontiguousarray(heights, dtype=np.float32).reshape(ny, nx)
+    full = pixels is None
+    pix = (np.arange(nx * ny, dtype=np.int64) if full
+           else np.ascontiguousarray(pixels, dtype=np.int64).reshape(-1))
+    out = np.zeros((pix.size, 2), dtype=np.float64)
+    g = geometry(params)
+    used = library.oracle_backproject_heights(
+        ctypes.byref(g), echoes.ctypes.data if echoes.size else None,
+        pos.ctypes.data if pos.size else None, hts.ctypes.data,
+        pix.ctypes.data if pix.size else None, pix.size, out.ctypes.data if out.size else None,
+        int(threads))
+    if used < 0:
+        raise ValueError("oracle_backproject_heights rejected its arguments")
+    img = out[:, 0] + 1j * out[:, 1]
+    return img.reshape(ny, nx) if full else img

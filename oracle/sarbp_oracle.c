@@ -29,8 +29,9 @@ static const double ORACLE_PI = 3.14159265358979323846;
 
 /* One pixel, all pulses. */
 static void backproject_pixel(const oracle_geometry* g, const float* echo,
-                              const double* antenna_pos, int64_t pixel, double* out)
+                              const double* antenna_pos, const float* heights, int64_t pixel, double* out)
 {
+    (void)heights;
     const int64_t ix = pixel % g->nx;
     const int64_t iy = pixel / g->nx;
     const double x = g->x0 + (double)ix * g->dx;
@@ -79,8 +80,9 @@ static double sinc8_kernel(double t)
 
 /* One pixel, all pulses, 8-tap windowed-sinc interpolation. */
 static void backproject_pixel_sinc8(const oracle_geometry* g, const float* echo,
-                                    const double* antenna_pos, int64_t pixel, double* out)
+                                    const double* antenna_pos, const float* heights, int64_t pixel, double* out)
 {
+    (void)heights;
     const int64_t ix = pixel % g->nx;
     const int64_t iy = pixel / g->nx;
     const double x = g->x0 + (double)ix * g->dx;
@@ -123,8 +125,9 @@ static void backproject_pixel_sinc8(const oracle_geometry* g, const float* echo,
 
 /* One pixel, all pulses, nearest-neighbour interpolation. */
 static void backproject_pixel_nearest(const oracle_geometry* g, const float* echo,
-                                      const double* antenna_pos, int64_t pixel, double* out)
+                                      const double* antenna_pos, const float* heights, int64_t pixel, double* out)
 {
+    (void)heights;
     const int64_t ix = pixel % g->nx;
     const int64_t iy = pixel / g->nx;
     const double x = g->x0 + (double)ix * g->dx;
@@ -156,29 +159,43 @@ static void backproject_pixel_nearest(const oracle_geometry* g, const float* ech
     out[1] = acc_im;
 }
 
+/* One pixel of a non-planar grid: the linear-interpolation steps above with
+   the pixel raised to z0 + heights[pixel]. */
+static void backproject_pixel_heights(const oracle_geometry* g, const float* echo,
+                                      const double* antenna_pos, const float* heights,
+                                      int64_t pixel, double* out)
+{
+    oracle_geometry raised = *g;
+    raised.z0 = g->z0 + (double)heights[pixel];
+    backproject_pixel(&raised, echo, antenna_pos, NULL, pixel, out);
+}
+
 typedef struct {
     const oracle_geometry* g;
     const float* echo;
     const double* antenna_pos;
     const int64_t* pixels;
+    const float* heights;
     double* out;
     int64_t begin, end;
-    void (*pixel_fn)(const oracle_geometry*, const float*, const double*, int64_t, double*);
+    void (*pixel_fn)(const oracle_geometry*, const float*, const double*, const float*, int64_t,
+                     double*);
 } oracle_job;
 
 static void* oracle_worker(void* arg)
 {
     const oracle_job* job = (const oracle_job*)arg;
     for (int64_t i = job->begin; i < job->end; ++i)
-        job->pixel_fn(job->g, job->echo, job->antenna_pos, job->pixels[i], job->out + 2 * i);
+        job->pixel_fn(job->g, job->echo, job->antenna_pos, job->heights, job->pixels[i],
+                      job->out + 2 * i);
     return NULL;
 }
 
 static int run_pixels(const oracle_geometry* g, const float* echo,
-                      const double* antenna_pos, const int64_t* pixels,
+                      const double* antenna_pos, const float* heights, const int64_t* pixels,
                       int64_t npix, double* out, int nthreads,
                       void (*pixel_fn)(const oracle_geometry*, const float*, const double*,
-                                       int64_t, double*))
+                                       const float*, int64_t, double*))
 {
     if (!g || npix < 0 || g->nx <= 0 || g->ny <= 0 || g->na < 0 || g->nr < 0)
         return -1;
@@ -215,6 +232,7 @@ static int run_pixels(const oracle_geometry* g, const float* echo,
         jobs[t].begin = npix * t / nthreads;
         jobs[t].end = npix * (t + 1) / nthreads;
         jobs[t].pixel_fn = pixel_fn;
+        jobs[t].heights = heights;
         if (t == 0)
             continue;
         if (pthread_create(&threads[t], NULL, oracle_worker, &jobs[t]) == 0)
@@ -236,14 +254,14 @@ int oracle_backproject(const oracle_geometry* g, const float* echo,
                        const double* antenna_pos, const int64_t* pixels,
                        int64_t npix, double* out, int nthreads)
 {
-    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads, backproject_pixel);
+    return run_pixels(g, echo, antenna_pos, NULL, pixels, npix, out, nthreads, backproject_pixel);
 }
 
 int oracle_backproject_sinc8(const oracle_geometry* g, const float* echo,
                              const double* antenna_pos, const int64_t* pixels,
                              int64_t npix, double* out, int nthreads)
 {
-    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads,
+    return run_pixels(g, echo, antenna_pos, NULL, pixels, npix, out, nthreads,
                       backproject_pixel_sinc8);
 }
 
@@ -251,6 +269,16 @@ int oracle_backproject_nearest(const oracle_geometry* g, const float* echo,
                                const double* antenna_pos, const int64_t* pixels,
                                int64_t npix, double* out, int nthreads)
 {
-    return run_pixels(g, echo, antenna_pos, pixels, npix, out, nthreads,
+    return run_pixels(g, echo, antenna_pos, NULL, pixels, npix, out, nthreads,
                       backproject_pixel_nearest);
+}
+
+int oracle_backproject_heights(const oracle_geometry* g, const float* echo,
+                               const double* antenna_pos, const float* heights,
+                               const int64_t* pixels, int64_t npix, double* out, int nthreads)
+{
+    if (g && g->nx > 0 && g->ny > 0 && !heights)
+        return -1;
+    return run_pixels(g, echo, antenna_pos, heights, pixels, npix, out, nthreads,
+                      backproject_pixel_heights);
 }

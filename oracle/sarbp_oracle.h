@@ -67,6 +67,15 @@ int oracle_backproject_nearest(const oracle_geometry* g, const float* echo,
                                const double* antenna_pos, const int64_t* pixels,
                                int64_t npix, double* out, int nthreads);
 
+/*
+ * Linear interpolation over a non-planar grid (SARBP-GPU §3.3: the range
+ * history may need terrain elevation): pixel (ix, iy) sits at
+ * (x0 + ix*dx, y0 + iy*dy, z0 + heights[iy*nx + ix]), heights float32 [ny][nx].
+ */
+int oracle_backproject_heights(const oracle_geometry* g, const float* echo,
+                               const double* antenna_pos, const float* heights,
+                               const int64_t* pixels, int64_t npix, double* out, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
