@@ -294,6 +294,32 @@ def run_ours(args, scene, rank, world, local, dist):
 
         time_interp("sinc8", "8-tap windowed sinc (SARBP_SINC8)")
         time_interp("nearest", "nearest neighbour (SARBP_NEAREST)")
+        # the same pulses onto pixels raised by 40 m of seeded terrain
+        from synth import scenes as scenes_mod
+        hmap = scenes_mod.terrain(p["nx"], p["ny"], p["dx"], 20337, relief=40.0)
+        heights = torch.from_numpy(hmap).to(dev)
+        with Plan(p, height_range=(float(hmap.min()), float(hmap.max()))) as hplan:
+            hplan.set_timing(True)
+            for _ in range(3):
+                hplan.backproject_heights(image, echoes, pos, heights)
+            torch.cuda.synchronize(dev)
+            hplan.kernel_times()
+            steps_v = max(3, min(args.steps, 20))
+            total = 0.0
+            for i in range(steps_v):
+                flush.fill_(float(i))
+                starts[0].record(stream)
+                hplan.backproject_heights(image, echoes, pos, heights)
+                ends[0].record(stream)
+                ends[0].synchronize()
+                total += starts[0].elapsed_time(ends[0])
+            main_ms_v, launches_v = hplan.kernel_times()
+        variants["heights"] = {
+            "interp": "linear, pixels on a 40 m terrain height map (sarbp_backproject_heights)",
+            "steps": steps_v, "value": updates * steps_v / (total / 1e3) / 1e9, "unit": UNIT,
+            "ms_per_step": total / steps_v,
+            "main_kernel_gupd": updates / (main_ms_v / max(launches_v, 1) / 1e3) / 1e9,
+        }
         # range compression of this scene's shape (SARBP-GPU §3.1): raw chirps -> echoes
         from domain_backprojection_sarbp_gb300 import RangeCompressor
         from synth import chirp as chirp_mod

@@ -23,6 +23,7 @@ EXPORTS = (
     "sarbp_status_string", "sarbp_last_error", "sarbp_plan_describe",
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
     "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
+    "sarbp_plan_heights", "sarbp_backproject_heights",
 )
 
 SARBP_WINDOW_NONE = 0
@@ -72,6 +73,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_plan.restype = st
     lib.sarbp_backproject.argtypes = [vp, vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject.restype = st
+    lib.sarbp_plan_heights.argtypes = [P(vp), P(Params), ctypes.c_double, ctypes.c_double]
+    lib.sarbp_plan_heights.restype = st
+    lib.sarbp_backproject_heights.argtypes = [vp, vp, vp, vp, vp, P(Params), vp]
+    lib.sarbp_backproject_heights.restype = st
     lib.sarbp_backproject_host.argtypes = [vp, vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject_host.restype = st
     lib.sarbp_backproject_noalloc.argtypes = [vp, vp, vp, P(Params), vp]

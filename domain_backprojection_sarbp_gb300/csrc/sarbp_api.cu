@@ -26,6 +26,8 @@ struct sarbp_plan_s {
     int sms = 0, ctas_per_sm = 0;
     int tiles_x = 0, tiles_y = 0, tiles = 0;
     int W = 0, full_window = 0;
+    int heights_mode = 0;            // plan made by sarbp_plan_heights
+    double h_min = 0.0, h_max = 0.0; // its height bounds
     float4* table_alloc = nullptr;   // (na * W + 2 * TABLE_PAD) entries
     int* klo = nullptr;              // na
     float2* psi = nullptr;           // nr: per-bin phasors (windowed-sinc interpolation)
@@ -94,6 +96,14 @@ double tile_qmax(double dx, double dy)
     return std::sqrt(hx * hx + hy * hy);
 }
 
+// Reach of a tile of a height-map plan: from the tile centre at the mid height
+// to any pixel whose height lies in [h_min, h_max].
+double tile_qmax3(double dx, double dy, double h_span)
+{
+    const double q = tile_qmax(dx, dy), hz = 0.5 * h_span;
+    return std::sqrt(q * q + hz * hz);
+}
+
 unsigned long long frac_fixed64(double v)
 {
     double f = v - std::floor(v);
@@ -156,6 +166,13 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     k.dx_f = (float)p->dx;
     k.dy_f = (float)p->dy;
     k.inv_dr_f = (float)(1.0 / p->dr);
+    k.heights_mode = plan->heights_mode;
+    k.z_lo = p->z0 + plan->h_min;
+    k.z_hi = p->z0 + plan->h_max;
+    k.z_mid = p->z0 + 0.5 * (plan->h_min + plan->h_max);
+    k.qmax3 = tile_qmax3(p->dx, p->dy, plan->h_max - plan->h_min);
+    k.h_lo_f = (float)plan->h_min;
+    k.h_hi_f = (float)plan->h_max;
     return k;
 }
 
@@ -199,7 +216,7 @@ namespace {
 // shifted r0), which the plan's table rows always cover.
 sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
-                                    cudaStream_t s)
+                                    cudaStream_t s, const float* heights = nullptr)
 {
     cudaError_t e = cudaSuccess;
     const long long pixels = (long long)params->nx * params->ny;
@@ -244,7 +261,7 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         cudaEventRecord(ev->first, s);
     }
     e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
-                           plan->partial, plan->psi, s);
+                           plan->partial, plan->psi, heights, s);
     if (ev)
         cudaEventRecord(ev->second, s);
     if (e != cudaSuccess)
@@ -282,7 +299,12 @@ const char* sarbp_last_error(sarbp_plan_t plan)
     return plan ? plan->last_error.c_str() : "";
 }
 
-sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
+}  // extern "C"
+
+namespace {
+
+sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_mode,
+                         double h_min, double h_max)
 {
     if (!out)
         return SARBP_ERR_INVALID_ARG;
@@ -301,6 +323,9 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
     if (!plan)
         return SARBP_ERR_OOM;
     plan->p = *p;
+    plan->heights_mode = heights_mode;
+    plan->h_min = h_min;
+    plan->h_max = h_max;
 
     cudaError_t e = cudaGetDevice(&plan->device);
     if (e != cudaSuccess) {
@@ -324,6 +349,8 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
         return SARBP_ERR_UNSUPPORTED_DEVICE;
     }
     e = backproject_occupancy(&plan->ctas_per_sm);
+    if (e == cudaSuccess && heights_mode)
+        e = prepare_heights_kernel();
     if (e != cudaSuccess || plan->ctas_per_sm < 1) {
         st = cuda_fail(plan, e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "occupancy");
         free_plan(plan);
@@ -338,8 +365,11 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
     // Table rows: the range extent of the tile-padded image plus a tile's reach
     const double ext_x = ((double)plan->tiles_x * TILE_X - 1.0) * p->dx;
     const double ext_y = ((double)plan->tiles_y * TILE_Y - 1.0) * p->dy;
-    const double diag = std::sqrt(ext_x * ext_x + ext_y * ext_y);
-    const double w_geom = std::ceil((diag + 2.0 * tile_qmax(p->dx, p->dy)) / p->dr) + 2 * MARGIN + 6;
+    // (a height-map plan: the slab z0 + [h_min, h_max] over the padded image)
+    const double h_span = h_max - h_min;
+    const double diag = std::sqrt(ext_x * ext_x + ext_y * ext_y + h_span * h_span);
+    const double w_geom =
+        std::ceil((diag + 2.0 * tile_qmax3(p->dx, p->dy, h_span)) / p->dr) + 2 * MARGIN + 6;
     const long long w_full = (long long)p->nr + 2 * MARGIN + 8;
     if (w_geom < (double)w_full) {
         plan->W = (int)w_geom;
@@ -378,6 +408,28 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
     }
     *out = plan;
     return SARBP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p)
+{
+    return plan_create(out, p, 0, 0.0, 0.0);
+}
+
+sarbp_status sarbp_plan_heights(sarbp_plan_t* out, const sarbp_params* p, double h_min,
+                                double h_max)
+{
+    if (!out)
+        return SARBP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!p || (p->flags & (SARBP_SINC8 | SARBP_NEAREST)))
+        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
+    if (!(isfin(h_min) && isfin(h_max) && h_min <= h_max))
+        return SARBP_ERR_INVALID_ARG;
+    return plan_create(out, p, 1, h_min, h_max);
 }
 
 sarbp_status sarbp_destroy(sarbp_plan_t plan)
@@ -449,7 +501,7 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
         return st;
     const sarbp_params& q = plan->p;
     if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
-        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr)
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || plan->heights_mode)
         return SARBP_ERR_PLAN_MISMATCH;
     const long long pixels = (long long)params->nx * params->ny;
     if (pixels > 0 && (!image || !aligned8(image)))
@@ -471,6 +523,46 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
                                   static_cast<cudaStream_t>(stream));
 }
 
+sarbp_status sarbp_backproject_heights(sarbp_plan_t plan, void* image, const void* echoes,
+                                       const double* antenna_pos, const float* heights,
+                                       const sarbp_params* params, void* stream)
+{
+    if (!plan || !params)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    if (params->flags & (SARBP_SINC8 | SARBP_NEAREST))
+        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || !plan->heights_mode)
+        return SARBP_ERR_PLAN_MISMATCH;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels > 0 && (!image || !aligned8(image)))
+        return SARBP_ERR_INVALID_ARG;
+    if (pixels > 0 && (!heights || (reinterpret_cast<uintptr_t>(heights) & 3u) != 0))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && (!antenna_pos || !aligned8(antenna_pos)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && params->nr > 0 && (!echoes || !aligned8(echoes)))
+        return SARBP_ERR_INVALID_ARG;
+    plan->last_error.clear();
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+
+    return enqueue_backprojection(plan, image, echoes, antenna_pos, params,
+                                  static_cast<cudaStream_t>(stream), heights);
+}
+
 sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
                                     void* stream)
@@ -485,7 +577,7 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
         return st;
     const sarbp_params& q = plan->p;
     if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
-        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr)
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || plan->heights_mode)
         return SARBP_ERR_PLAN_MISMATCH;
     const long long pixels = (long long)params->nx * params->ny;
     const size_t img_bytes = (size_t)pixels * 8;
@@ -686,7 +778,7 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
                          klo, s);
         if (e == cudaSuccess)
             e = launch_backproject(k, antenna_pos + 3 * (size_t)c0, table, klo,
-                                   static_cast<float2*>(image), nullptr, nullptr, s);
+                                   static_cast<float2*>(image), nullptr, nullptr, nullptr, s);
         if (e != cudaSuccess)
             return SARBP_ERR_CUDA;
     }

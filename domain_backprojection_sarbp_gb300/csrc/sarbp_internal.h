@@ -55,6 +55,11 @@ struct BpConst {
     float c_phase;               // 2 pi * 2 dr / lambda: phase per bin, radians
     float inv_c;                 // 1 / c_phase
     float dx_f, dy_f, inv_dr_f;
+    int heights_mode;            // pixels raised by a height map (exact path only)
+    double z_lo, z_hi;           // z0 + height bounds given at plan time
+    double qmax3;                // tile reach including height offsets from the mid height
+    double z_mid;                // z0 + mid height: records are built on this plane
+    float h_lo_f, h_hi_f;        // height bounds; the kernel clamps heights into them
     float rot_re, rot_im;        // exp(-j c_phase): phase step from one bin to the next
     float i0;                    // column offset of a thread's first pixel from the tile centre
 };
@@ -64,7 +69,8 @@ cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos
 cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s);
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
                                const int* klo, float2* image, float4* partial,
-                               const float2* psi, cudaStream_t s);
+                               const float2* psi, const float* heights, cudaStream_t s);
+cudaError_t prepare_heights_kernel();
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);

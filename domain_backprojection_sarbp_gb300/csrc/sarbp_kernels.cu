@@ -47,7 +47,8 @@ namespace {
 constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/round(x) in the mantissa
 constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 
-enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2 };
+enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3 };
+constexpr int HROW = TILE_X + 1;           // shared-memory row stride of a tile's heights
 
 struct __align__(16) Record {
     float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
@@ -81,12 +82,14 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
         } else if (k.full_window) {
             lo = -(MARGIN + 4);
         } else {
-            // nearest point of the tile-padded image rectangle to the antenna
+            // nearest point of the tile-padded image box (a rectangle at z0, or
+            // the slab z0 + [h_min, h_max] for a height map) to the antenna
             const double cx = fmin(fmax(ax, k.rect_x0), k.rect_x1);
             const double cy = fmin(fmax(ay, k.rect_y0), k.rect_y1);
-            const double ddx = cx - ax, ddy = cy - ay, ddz = k.z0 - az;
+            const double cz = k.heights_mode ? fmin(fmax(az, k.z_lo), k.z_hi) : k.z0;
+            const double ddx = cx - ax, ddy = cy - ay, ddz = cz - az;
             const double rmin = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
-            double u = (rmin - k.qmax - k.r0) * k.inv_dr;
+            double u = (rmin - (k.heights_mode ? k.qmax3 : k.qmax) - k.r0) * k.inv_dr;
             u = fmin(fmax(u, -1.0e9), 1.0e9);
             lo = (int)floor(u) - MARGIN;
         }
@@ -157,17 +160,18 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
     const double ay = pos[3 * (size_t)n + 1];
     const double az = pos[3 * (size_t)n + 2];
     const int lo = klo[n];
-    const double vx = xc - ax, vy = yc - ay, vz = k.z0 - az;
+    const double vx = xc - ax, vy = yc - ay, vz = (k.heights_mode ? k.z_mid : k.z0) - az;
     const double r2 = vx * vx + vy * vy + vz * vz;
     const double r = sqrt(r2);
+    const double reach = k.heights_mode ? k.qmax3 : k.qmax;
     int kind = REC_SKIP;
     Record rec;
     rec.a = rec.b = rec.c = rec.d = make_float4(0.f, 0.f, 0.f, 0.f);
     rec.d.y = __int_as_float(-lo);
     if (lo != KLO_INVALID && isfinite(r)) {
         const double u = (r - k.r0) * k.inv_dr;
-        const double umin = (r - k.qmax - k.r0) * k.inv_dr - 1e-6;
-        const double umax = (r + k.qmax - k.r0) * k.inv_dr + 1e-6;
+        const double umin = (r - reach - k.r0) * k.inv_dr - 1e-6;
+        const double umax = (r + reach - k.r0) * k.inv_dr + 1e-6;
         // every pixel of the tile has k <= -1 or k >= nr - 1: no recorded echo
         if (!(umax < 0.0 || umin >= (double)k.nr - 1.0)) {
             const double kt = floor(fmin(fmax(u, -1.0e9), 1.0e9));
@@ -287,8 +291,11 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const bool hinge = INTERP == INTERP_LINEAR && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
                        idx0 + 1 <= bin0 + k.nr - 2;
     PulseState st;
-    st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
-                               : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
+    if (INTERP == INTERP_HEIGHTS)
+        st.mode = kind == REC_SKIP ? MODE_SKIP : MODE_EXACT;
+    else
+        st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
+                                   : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
     st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
     if (hinge) {
@@ -638,12 +645,68 @@ __device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Reco
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pixels on a height map: float64 range to the centre of the thread's row at
+// the row's mean height z_row, then R - R_row = s / (R_row + R) with
+// s = 2 v.q + |q|^2, q = (qx, 0, h - h_row), in float32, bounds on every index.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void heights_pulse(const BpConst& k, const Record& rec, const float4* row,
+                                              const double* __restrict__ a, double xc, double yrow,
+                                              double zrow, float hrow, const float* s_h,
+                                              float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const double vx = xc - a[0], vy = yrow - a[1], vz = zrow - a[2];
+    const double r2 = vx * vx + vy * vy + vz * vz;
+    const double r = sqrt(r2);
+    const double u = (r - k.r0) * k.inv_dr;
+    if (!(fabs(u) < 1.0e9))
+        return;
+    const double ku = floor(u);
+    const int kbase = (int)ku + __float_as_int(rec.d.y);
+    const float frac0 = (float)(u - ku);
+    const float two_vx = (float)(2.0 * vx), two_vz = (float)(2.0 * vz);
+    const float rf = (float)r, r2f = (float)r2;
+    const float c_phase = k.c_phase;
+#pragma unroll
+    for (int m = 0; m < TILE_X; ++m) {
+        const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
+        const float dz = s_h[m] - hrow;
+        const float s = fmaf(qx, two_vx + qx, dz * (two_vz + dz));
+        const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
+        const float den = rf + rp;
+        const float dr_m = den > 0.0f ? s / den : 0.0f;
+        const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
+        if (!(ub > -1.0e6f && ub < 1.0e6f))
+            continue;
+        const float kf = floorf(ub);
+        const int kr = kbase + (int)kf;
+        if (kr < 0 || kr > k.W - 1)
+            continue;                       // outside the row: no recorded echo there
+        const float x = (ub - kf) * c_phase;
+        const float4 v = __ldg(row + kr);
+        const float wr = fmaf(x, v.z, v.x);
+        const float wi = fmaf(x, v.w, v.y);
+        float sn, cs;
+        __sincosf(x, &sn, &cs);
+        float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+        float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+        re = fmaf(wr, cs, fmaf(-wi, sn, re));
+        im = fmaf(wr, sn, fmaf(wi, cs, im));
+    }
+}
+
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, const float2* __restrict__ psi,
+                                            double yrow, double zrow, float hrow, const float* s_h,
+                                            const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
+    if (INTERP == INTERP_HEIGHTS) {
+        if (st.mode == MODE_EXACT)
+            heights_pulse(k, rec, row, a, xc, yrow, zrow, hrow, s_h, accre, accim);
+        return;
+    }
     if (INTERP == INTERP_NEAREST) {
         if (st.mode == MODE_GATHER)
             nearest_pulse(k, st, row, psi, accre, accim);
@@ -680,9 +743,11 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                                                         const int* __restrict__ klo,
                                                         float2* __restrict__ image,
                                                         float4* __restrict__ partial,
-                                                        const float2* __restrict__ psi)
+                                                        const float2* __restrict__ psi,
+                                                        const float* __restrict__ heights)
 {
     __shared__ Record s_rec[CHUNK];
+    extern __shared__ float s_heights[];            // heights mode: TILE_Y x HROW
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
     const float jf = (float)jr - 0.5f * (TILE_Y - 1);
@@ -706,6 +771,24 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
 
         const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
+        float hrow = 0.0f;
+        double zrow = k.z0;
+        if (INTERP == INTERP_HEIGHTS) {
+            // the thread's own row of the tile, heights clamped to the plan's
+            // bounds; pixels outside the image repeat the last row or column
+            // (their results are never stored)
+            const int rowi_h = min(row0 + jr, k.ny - 1);
+            float sum = 0.0f;
+#pragma unroll 4
+            for (int m = 0; m < TILE_X; ++m) {
+                const int col = min(col0 + m, k.nx - 1);
+                const float hv = fminf(fmaxf(heights[(size_t)rowi_h * k.nx + col], k.h_lo_f), k.h_hi_f);
+                s_heights[jr * HROW + m] = hv;
+                sum += hv;
+            }
+            hrow = sum * (1.0f / TILE_X);
+            zrow = k.z0 + (double)hrow;
+        }
         float2 accre[NP], accim[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -729,13 +812,15 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 const PulseState sb =
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
-                                  pos + 3 * (size_t)(c0 + p), xc, yrow, psi, accre, accim);
+                                  pos + 3 * (size_t)(c0 + p), xc, yrow, zrow, hrow,
+                                  s_heights + jr * HROW, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
-                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, psi, accre, accim);
+                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, zrow, hrow,
+                                  s_heights + jr * HROW, psi, accre, accim);
             }
         }
 
@@ -898,16 +983,30 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
     return cudaGetLastError();
 }
 
+constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW * sizeof(float);
+
+cudaError_t prepare_heights_kernel()
+{
+    return cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)HEIGHTS_SMEM);
+}
+
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
                                const int* klo, float2* image, float4* partial,
-                               const float2* psi, cudaStream_t s)
+                               const float2* psi, const float* heights, cudaStream_t s)
 {
-    if (k.flags & FLAG_SINC8)
-        bp_kernel<INTERP_SINC8><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+    if (k.heights_mode)
+        bp_kernel<INTERP_HEIGHTS><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(k, pos, table, klo, image,
+                                                                       partial, psi, heights);
+    else if (k.flags & FLAG_SINC8)
+        bp_kernel<INTERP_SINC8><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi,
+                                                           nullptr);
     else if (k.flags & FLAG_NEAREST)
-        bp_kernel<INTERP_NEAREST><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+        bp_kernel<INTERP_NEAREST><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial,
+                                                             psi, nullptr);
     else
-        bp_kernel<INTERP_LINEAR><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi);
+        bp_kernel<INTERP_LINEAR><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial,
+                                                            psi, nullptr);
     return cudaGetLastError();
 }
 

@@ -66,13 +66,22 @@ def _check_device_tensor(t, name, dtype, shape):
 class Plan:
     """A libsarbp plan: fixed sizes, device scratch, repeated backprojections."""
 
-    def __init__(self, params):
+    def __init__(self, params, height_range=None):
+        """``height_range`` = (h_min, h_max) makes a height-map plan (sarbp_plan_heights),
+        used with :meth:`backproject_heights` only."""
         self._lib = _native.lib()
         self.params = _params(params)
+        self.height_range = None if height_range is None else tuple(map(float, height_range))
         handle = ctypes.c_void_p()
-        st = self._lib.sarbp_plan(ctypes.byref(handle), ctypes.byref(self.params))
+        if self.height_range is None:
+            st = self._lib.sarbp_plan(ctypes.byref(handle), ctypes.byref(self.params))
+            where = "sarbp_plan"
+        else:
+            st = self._lib.sarbp_plan_heights(ctypes.byref(handle), ctypes.byref(self.params),
+                                              *self.height_range)
+            where = "sarbp_plan_heights"
         if st != _native.SARBP_OK:
-            raise SarbpError(st, "sarbp_plan")
+            raise SarbpError(st, where)
         self._h = handle
 
     @property
@@ -116,6 +125,24 @@ class Plan:
                                          _stream_handle(stream))
         if st != _native.SARBP_OK:
             self._raise(st, "sarbp_backproject")
+        return image
+
+    def backproject_heights(self, image, echoes, antenna_pos, heights, params=None,
+                            accumulate=False, stream=None):
+        """Linear-interpolation backprojection of pixels raised to z0 + heights[iy, ix].
+
+        heights float32 [ny, nx] on the device, clamped to the plan's height range.
+        """
+        import torch
+        p = _params(params if params is not None else self.params, accumulate)
+        img = _check_device_tensor(image, "image", torch.complex64, (p.ny, p.nx))
+        ech = _check_device_tensor(echoes, "echoes", torch.complex64, (p.na, p.nr))
+        pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))
+        hts = _check_device_tensor(heights, "heights", torch.float32, (p.ny, p.nx))
+        st = self._lib.sarbp_backproject_heights(self._h, img, ech, pos, hts, ctypes.byref(p),
+                                                 _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject_heights")
         return image
 
     def backproject_host(self, image, echoes, antenna_pos, params=None, accumulate=False,

@@ -152,6 +152,42 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
                                     const double* antenna_pos, const sarbp_params* params,
                                     void* stream);
 
+/*
+ * Pixels on a height map (SARBP-GPU §3.3 remarks that the range history may
+ * have to take terrain elevation into account; the page gives no formula, so
+ * this is the plain reading): pixel (ix, iy) sits at
+ *   (x0 + ix*dx, y0 + iy*dy, z0 + heights[iy*nx + ix])
+ * and the sum is otherwise that of sarbp_backproject with linear interpolation.
+ *
+ * sarbp_plan_heights - as sarbp_plan, for heights within [h_min, h_max]
+ * (metres, added to z0). The table rows cover the slab z0 + [h_min, h_max]
+ * over the image, so W grows with h_max - h_min. SARBP_ERR_INVALID_ARG as for
+ * sarbp_plan, and also for SARBP_SINC8 / SARBP_NEAREST in p->flags and for
+ * non-finite bounds or h_min > h_max.
+ */
+sarbp_status sarbp_plan_heights(sarbp_plan_t* out, const sarbp_params* p, double h_min,
+                                double h_max);
+
+/*
+ * sarbp_backproject_heights - enqueue one backprojection over a height map.
+ *
+ * heights  device pointer, float32 [ny][nx], caller-owned, 4-byte aligned,
+ *          read during the work on `stream`. Each value is clamped to the
+ *          plan's [h_min, h_max] (a NaN height is taken as h_min).
+ * image, echoes, antenna_pos, params, stream: as for sarbp_backproject
+ * (SARBP_ACCUMULATE allowed; SARBP_SINC8 / SARBP_NEAREST rejected with
+ * SARBP_ERR_INVALID_ARG). The plan must come from sarbp_plan_heights, and
+ * plans from sarbp_plan_heights are refused by sarbp_backproject and
+ * sarbp_backproject_host (SARBP_ERR_PLAN_MISMATCH either way).
+ *
+ * Every pixel takes the float64 range to its row's centre at the row's mean
+ * height and a float32 difference to the pixel, so this path runs slower than
+ * the planar one; results are deterministic like sarbp_backproject's.
+ */
+sarbp_status sarbp_backproject_heights(sarbp_plan_t plan, void* image, const void* echoes,
+                                       const double* antenna_pos, const float* heights,
+                                       const sarbp_params* params, void* stream);
+
 /* Bytes copied host-to-device and device-to-host by the plan's last
    sarbp_backproject_host call. */
 sarbp_status sarbp_host_transfer_bytes(sarbp_plan_t plan, uint64_t* h2d, uint64_t* d2h);

@@ -18,4 +18,5 @@ from .scenes import (  # noqa: F401
     simulate_echoes,
     straight_track,
     compared_pixels,
+    terrain,
 )

@@ -93,6 +93,7 @@ class Scene:
     antenna_pos: np.ndarray      # float64 [na, 3]
     targets: np.ndarray          # int64 [T, 2] as (ix, iy), on pixel centres
     amps: np.ndarray             # float64 [T]
+    heights: np.ndarray | None = None   # float32 [ny, nx] terrain above z0, or None (flat)
 
 
 def straight_track(na: int, step: float, altitude: float = ALTITUDE,
@@ -170,9 +171,37 @@ def simulate_echoes(antenna_pos: np.ndarray, target_xyz: np.ndarray, amps: np.nd
     return out
 
 
+def terrain(nx: int, ny: int, spacing: float, seed: int, relief: float = 40.0,
+            mean: float = 20.0) -> np.ndarray:
+    """Seeded smooth terrain, float32 [ny, nx] metres above z0.
+
+    Four 2-D sinusoids (wavelengths 60 to 600 m, random directions, phases and
+    amplitudes), shifted and scaled so that the heights span exactly
+    ``relief`` metres peak to peak around ``mean``. The steepest slope is of
+    order pi * relief / 60 m.
+    """
+    rng = np.random.default_rng(seed)
+    yy, xx = np.mgrid[0:ny, 0:nx].astype(np.float64) * spacing
+    h = np.zeros((ny, nx), dtype=np.float64)
+    for _ in range(4):
+        lam = rng.uniform(60.0, 600.0)
+        ang = rng.uniform(0.0, np.pi)
+        ph = rng.uniform(0.0, 2.0 * np.pi)
+        amp = rng.uniform(0.5, 1.0)
+        h += amp * np.sin(2.0 * np.pi * (xx * np.cos(ang) + yy * np.sin(ang)) / lam + ph)
+    span = float(h.max() - h.min()) if h.size else 0.0
+    if span > 0:
+        h = (h - 0.5 * (h.max() + h.min())) * (relief / span)
+    return (mean + h).astype(np.float32)
+
+
 def make_scene(cfg: SceneConfig, noise: bool = True, seed: int | None = None,
-               n_targets: int | None = None) -> Scene:
-    """Build one seeded scene. The result is a pure function of (cfg, seed, noise, n_targets)."""
+               n_targets: int | None = None, heights: np.ndarray | None = None) -> Scene:
+    """Build one seeded scene. The result is a pure function of (cfg, seed, noise, n_targets).
+
+    With ``heights`` (float32 [ny, nx]) every target sits on that surface,
+    at z0 + heights[iy, ix] above its pixel.
+    """
     seed = cfg.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     count = cfg.n_targets if n_targets is None else n_targets
@@ -196,6 +225,8 @@ def make_scene(cfg: SceneConfig, noise: bool = True, seed: int | None = None,
     txyz[:, 0] = geo["x0"] + targets[:, 0] * geo["dx"]
     txyz[:, 1] = geo["y0"] + targets[:, 1] * geo["dy"]
     txyz[:, 2] = geo["z0"]
+    if heights is not None:
+        txyz[:, 2] += heights[targets[:, 1], targets[:, 0]].astype(np.float64)
 
     echoes = np.empty((cfg.na, cfg.nr), dtype=np.complex64)
     scale = cfg.noise_sigma / np.sqrt(2.0)
@@ -207,7 +238,7 @@ def make_scene(cfg: SceneConfig, noise: bool = True, seed: int | None = None,
             block += scale * (g[..., 0] + 1j * g[..., 1])
         echoes[n0:n1] = block.astype(np.complex64)
     return Scene(cfg=cfg, params=params, echoes=echoes, antenna_pos=pos,
-                 targets=targets, amps=amps)
+                 targets=targets, amps=amps, heights=heights)
 
 
 def compared_pixels(scene: Scene, n_random: int = 4096, full_limit: int = 512 * 512,

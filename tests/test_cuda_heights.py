@@ -1,0 +1,207 @@
+"""Backprojection over a height map (sarbp_backproject_heights) against the FP64 oracle.
+
+SARBP-GPU §3.3 (the page "基于GPU的SAR后向投影成像优化与CUDA加速实践") notes
+that the range history may need the terrain elevation; pixel (ix, iy) sits
+at (x0 + ix dx, y0 + iy dy, z0 + h[iy, ix]). Acceptance as for the planar
+path (tests/parity.py): relative L2 <= 1e-3, max |error| <= 1e-3 of the
+peak, the same argmax at every target.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from domain_backprojection_sarbp_gb300 import Plan, SarbpError, _native  # noqa: E402
+from synth import scenes  # noqa: E402
+from tests import parity  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _dev(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=dtype)).to(DEV)
+
+
+def heights_image(params, echoes, pos, heights, h_range, init=None, accumulate=False, plan=None):
+    img = torch.full((params["ny"], params["nx"]), complex(7.0, -3.0), dtype=torch.complex64,
+                     device=DEV)
+    if init is not None:
+        img.copy_(torch.from_numpy(init.astype(np.complex64)))
+    own = plan is None
+    plan = plan or Plan(params, height_range=h_range)
+    try:
+        plan.backproject_heights(img, _dev(echoes, np.complex64), _dev(pos, np.float64),
+                                 _dev(heights, np.float32), params=params, accumulate=accumulate)
+        torch.cuda.synchronize()
+    finally:
+        if own:
+            plan.close()
+    return img.cpu().numpy()
+
+
+def terrain_scene(cfg, relief, mean=20.0, noise=True):
+    h = scenes.terrain(cfg.nx, cfg.ny, cfg.spacing, cfg.seed + 77, relief=relief, mean=mean)
+    return scenes.make_scene(cfg, noise=noise, heights=h), h
+
+
+# ------------------------------------------------ several tiles, ragged tails
+@pytest.mark.parametrize("relief", [10.0, 40.0])
+def test_terrain_several_tiles(relief):
+    # 100 x 600 pixels: four 32-wide tiles (the last 4 wide) by two 512-high
+    # tiles (the last 88 high)
+    cfg = scenes.shrink(scenes.CONFIGS[1], na=512, nx=100, ny=600, n_targets=6)
+    sc, h = terrain_scene(cfg, relief)
+    h_range = (float(h.min()), float(h.max()))
+    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, h_range)
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
+    parity.assert_parity(got, ref, f"terrain relief {relief}")
+    assert not parity.argmax_mismatches(got, ref, sc.targets)
+
+
+def test_focusing_pin_on_the_gpu():
+    """The oracle's focusing pin (targets on a rough surface focus on their
+    pixels with the right heights and not on a flat grid), run on this path."""
+    from tests.test_oracle_heights_pins import pin_focusing_on_rough_surface
+
+    def gpu_bp(params, echo, pos, h):
+        return heights_image(params, echo, pos, h, (float(h.min()), float(h.max())))
+    ok, detail = pin_focusing_on_rough_surface(gpu_bp)
+    assert ok, detail
+
+
+def test_constant_height_is_the_raised_plane():
+    sc = scenes.make_scene(scenes.CONFIGS[0])
+    p = sc.params
+    h = np.full((p["ny"], p["nx"]), 7.25, dtype=np.float32)
+    got = heights_image(p, sc.echoes, sc.antenna_pos, h, (0.0, 10.0))
+    ref = oracle.backproject(dict(p, z0=p["z0"] + 7.25), sc.echoes, sc.antenna_pos)
+    parity.assert_parity(got, ref, "constant height")
+
+
+def test_wide_height_range():
+    """A 500 m height range widens every table row; pixels at both extremes
+    still receive every pulse's echo."""
+    cfg = scenes.shrink(scenes.CONFIGS[1], na=256, nx=96, ny=96, n_targets=4)
+    base = scenes.terrain(cfg.nx, cfg.ny, cfg.spacing, cfg.seed + 5, relief=4.0, mean=0.0)
+    h = base.copy()
+    h[:48] += -100.0
+    h[48:] += 400.0
+    sc = scenes.make_scene(cfg, heights=h)
+    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (-110.0, 410.0))
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
+    parity.assert_parity(got, ref, "wide height range")
+
+
+def test_heights_are_clamped_to_the_plan_range():
+    cfg = scenes.shrink(scenes.CONFIGS[1], na=128, nx=64, ny=80, n_targets=2)
+    sc, h = terrain_scene(cfg, 30.0)
+    wild = h.copy()
+    wild[3, 5] = 1.0e6
+    wild[7, 9] = -1.0e6
+    wild[11, 13] = np.nan
+    wild[2, 40] = np.inf
+    lo, hi = 10.0, 25.0
+    tame = np.clip(wild, lo, hi)
+    tame[11, 13] = lo                     # a NaN height is taken as the lower bound
+    with Plan(sc.params, height_range=(lo, hi)) as plan:
+        a = heights_image(sc.params, sc.echoes, sc.antenna_pos, wild, None, plan=plan)
+        b = heights_image(sc.params, sc.echoes, sc.antenna_pos, tame, None, plan=plan)
+    assert np.all(np.isfinite(a))
+    assert np.array_equal(a, b)
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, tame)
+    parity.assert_parity(a, ref, "clamped heights")
+
+
+def test_accumulate_and_determinism():
+    cfg = scenes.shrink(scenes.CONFIGS[1], na=256, nx=70, ny=530, n_targets=3)
+    sc, h = terrain_scene(cfg, 20.0)
+    rng = np.random.default_rng(3)
+    init = (rng.standard_normal((cfg.ny, cfg.nx)) + 1j * rng.standard_normal((cfg.ny, cfg.nx)))
+    init = init.astype(np.complex64)
+    rng_h = (float(h.min()), float(h.max()))
+    with Plan(sc.params, height_range=rng_h) as plan:
+        one = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan)
+        two = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan)
+        acc = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, init=init,
+                            accumulate=True, plan=plan)
+    assert np.array_equal(one, two)
+    scale = np.abs(one).max()
+    assert np.abs(acc - (init + one)).max() <= 1e-5 * scale
+
+
+# ------------------------------------------- full size, sampled pixels
+@pytest.mark.slow
+def test_page_spotlight_on_terrain_sampled():
+    """4096 pulses onto 1024 x 1024 pixels on 40 m of relief, in the launch
+    configuration the planar benchmark uses; compared on sampled pixels."""
+    cfg = scenes.CONFIGS[2]
+    sc, h = terrain_scene(cfg, 40.0)
+    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (float(h.min()), float(h.max())))
+    pix = scenes.compared_pixels(sc)
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h, pixels=pix)
+    parity.assert_parity(got.reshape(-1)[pix], ref, "page_spotlight on terrain")
+    full = np.zeros(cfg.nx * cfg.ny, dtype=np.complex128)
+    full[pix] = ref
+    assert not parity.argmax_mismatches(got, full.reshape(cfg.ny, cfg.nx), sc.targets)
+
+
+# ------------------------------------------------------------ the interface
+def test_plans_do_not_mix():
+    sc = scenes.make_scene(scenes.CONFIGS[0])
+    p = sc.params
+    h = np.zeros((p["ny"], p["nx"]), dtype=np.float32)
+    img = torch.zeros((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+    e, a, hd = _dev(sc.echoes, np.complex64), _dev(sc.antenna_pos, np.float64), _dev(h, np.float32)
+    with Plan(p, height_range=(0.0, 1.0)) as hp, Plan(p) as fp:
+        with pytest.raises(SarbpError) as ex:
+            hp.backproject(img, e, a)
+        assert ex.value.status == _native.SARBP_ERR_PLAN_MISMATCH
+        with pytest.raises(SarbpError) as ex:
+            hp.backproject_host(np.zeros((p["ny"], p["nx"]), np.complex64), sc.echoes,
+                                sc.antenna_pos)
+        assert ex.value.status == _native.SARBP_ERR_PLAN_MISMATCH
+        with pytest.raises(SarbpError) as ex:
+            fp.backproject_heights(img, e, a, hd)
+        assert ex.value.status == _native.SARBP_ERR_PLAN_MISMATCH
+
+
+def test_bad_height_arguments():
+    sc = scenes.make_scene(scenes.CONFIGS[0])
+    p = sc.params
+    lib = _native.lib()
+    prm = _native.Params.from_dict(p)
+    h = ctypes.c_void_p()
+    for lo, hi in ((1.0, 0.0), (float("nan"), 1.0), (0.0, float("inf"))):
+        assert lib.sarbp_plan_heights(ctypes.byref(h), ctypes.byref(prm), lo, hi) == \
+            _native.SARBP_ERR_INVALID_ARG
+        assert not h.value
+    sinc = _native.Params.from_dict(p, flags=_native.SARBP_SINC8)
+    assert lib.sarbp_plan_heights(ctypes.byref(h), ctypes.byref(sinc), 0.0, 1.0) == \
+        _native.SARBP_ERR_INVALID_ARG
+    img = torch.zeros((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+    e, a = _dev(sc.echoes, np.complex64), _dev(sc.antenna_pos, np.float64)
+    hd = torch.zeros(p["ny"] * p["nx"] + 1, dtype=torch.float32, device=DEV)
+    with Plan(p, height_range=(0.0, 1.0)) as plan:
+        # heights that are not 4-byte aligned, and missing heights
+        odd = ctypes.c_void_p(hd.data_ptr() + 2)
+        for ptr in (odd, ctypes.c_void_p(None)):
+            st = lib.sarbp_backproject_heights(
+                plan.handle, ctypes.c_void_p(img.data_ptr()), ctypes.c_void_p(e.data_ptr()),
+                ctypes.c_void_p(a.data_ptr()), ptr, ctypes.byref(prm), None)
+            assert st == _native.SARBP_ERR_INVALID_ARG
+        with pytest.raises(SarbpError):
+            plan.backproject_heights(img, e, a, hd[:-1].reshape(p["ny"], p["nx"]),
+                                     params=dict(p, flags=_native.SARBP_NEAREST))
