@@ -23,7 +23,7 @@ EXPORTS = (
     "sarbp_status_string", "sarbp_last_error", "sarbp_plan_describe",
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
     "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
-    "sarbp_plan_heights", "sarbp_backproject_heights",
+    "sarbp_plan_heights", "sarbp_backproject_heights", "sarbp_backproject_streamed",
 )
 
 SARBP_WINDOW_NONE = 0
@@ -79,6 +79,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_backproject_heights.restype = st
     lib.sarbp_backproject_host.argtypes = [vp, vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject_host.restype = st
+    lib.sarbp_backproject_streamed.argtypes = [vp, vp, vp, vp, P(Params), ctypes.c_int32, vp]
+    lib.sarbp_backproject_streamed.restype = st
     lib.sarbp_backproject_noalloc.argtypes = [vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject_noalloc.restype = st
     lib.sarbp_host_transfer_bytes.argtypes = [vp, P(ctypes.c_uint64), P(ctypes.c_uint64)]

@@ -39,6 +39,12 @@ struct sarbp_plan_s {
     void* d_echo = nullptr;
     double* d_pos = nullptr;
     size_t last_h2d = 0, last_d2h = 0;   // bytes moved by the last host-buffer call
+    // streamed entry point: two staging buffers, a copy stream, their events
+    void* d_stage[2] = {nullptr, nullptr};
+    size_t stage_bytes = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copied[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr};
+    cudaEvent_t call_start = nullptr;
     // kernel timing
     bool timing = false;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> events;
@@ -187,6 +193,17 @@ void free_plan(sarbp_plan_s* plan)
     cudaFree(plan->d_image);
     cudaFree(plan->d_echo);
     cudaFree(plan->d_pos);
+    for (int b = 0; b < 2; ++b) {
+        cudaFree(plan->d_stage[b]);
+        if (plan->copied[b])
+            cudaEventDestroy(plan->copied[b]);
+        if (plan->consumed[b])
+            cudaEventDestroy(plan->consumed[b]);
+    }
+    if (plan->call_start)
+        cudaEventDestroy(plan->call_start);
+    if (plan->copy_stream)
+        cudaStreamDestroy(plan->copy_stream);
     for (auto& ev : plan->events) {
         cudaEventDestroy(ev.first);
         cudaEventDestroy(ev.second);
@@ -210,6 +227,39 @@ bool any_split_tile(const BpConst& k)
 }  // namespace
 
 namespace {
+
+// The band of range bins that pulses n0 .. n1-1 can reach from the image,
+// found in float64 on the host from the antenna positions: for every pulse
+// the nearest and farthest point of the image rectangle, plus margins (six
+// bins below, seven above). Pulses with a non-finite position contribute
+// nothing and are left out. Returns false when no pulse reaches the axis.
+bool host_band(const sarbp_params* params, const double* antenna_pos, int n0, int n1,
+               long long* lo, long long* hi)
+{
+    long long band_lo = params->nr, band_hi = -1;
+    const double xa = params->x0, xb = params->x0 + (params->nx - 1) * params->dx;
+    const double ya = params->y0, yb = params->y0 + (params->ny - 1) * params->dy;
+    for (int n = n0; n < n1 && params->nr >= 2; ++n) {
+        const double ax = antenna_pos[3 * (size_t)n], ay = antenna_pos[3 * (size_t)n + 1],
+                     az = antenna_pos[3 * (size_t)n + 2];
+        if (!(isfin(ax) && isfin(ay) && isfin(az)))
+            continue;
+        const double dz = params->z0 - az;
+        const double nx_ = std::min(std::max(ax, xa), xb) - ax;
+        const double ny_ = std::min(std::max(ay, ya), yb) - ay;
+        const double fx = std::max(std::fabs(xa - ax), std::fabs(xb - ax));
+        const double fy = std::max(std::fabs(ya - ay), std::fabs(yb - ay));
+        const double rmin = std::sqrt(nx_ * nx_ + ny_ * ny_ + dz * dz);
+        const double rmax = std::sqrt(fx * fx + fy * fy + dz * dz);
+        const double ulo = std::floor((rmin - params->r0) / params->dr) - 6.0;
+        const double uhi = std::floor((rmax - params->r0) / params->dr) + 7.0;
+        band_lo = std::min<long long>(band_lo, (long long)std::max(ulo, 0.0));
+        band_hi = std::max<long long>(band_hi, (long long)std::min(uhi, (double)params->nr - 1.0));
+    }
+    *lo = band_lo;
+    *hi = band_hi;
+    return band_hi >= band_lo;
+}
 
 // Queue the three kernels of one backprojection. Arguments are already
 // checked; params may describe a band of the plan's range axis (fewer bins,
@@ -598,30 +648,9 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
     if (pixels == 0)
         return SARBP_OK;
 
-    // The band of range bins the image can reach, from the host copy of the
-    // antenna positions: for every pulse the nearest and farthest point of the
-    // image rectangle, plus margins; pulses with a non-finite position
-    // contribute nothing and are left out. Only this band is copied.
-    long long band_lo = params->nr, band_hi = -1;
-    const double xa = params->x0, xb = params->x0 + (params->nx - 1) * params->dx;
-    const double ya = params->y0, yb = params->y0 + (params->ny - 1) * params->dy;
-    for (int n = 0; n < params->na && params->nr >= 2; ++n) {
-        const double ax = antenna_pos[3 * (size_t)n], ay = antenna_pos[3 * (size_t)n + 1],
-                     az = antenna_pos[3 * (size_t)n + 2];
-        if (!(isfin(ax) && isfin(ay) && isfin(az)))
-            continue;
-        const double dz = params->z0 - az;
-        const double nx_ = std::min(std::max(ax, xa), xb) - ax;
-        const double ny_ = std::min(std::max(ay, ya), yb) - ay;
-        const double fx = std::max(std::fabs(xa - ax), std::fabs(xb - ax));
-        const double fy = std::max(std::fabs(ya - ay), std::fabs(yb - ay));
-        const double rmin = std::sqrt(nx_ * nx_ + ny_ * ny_ + dz * dz);
-        const double rmax = std::sqrt(fx * fx + fy * fy + dz * dz);
-        const double ulo = std::floor((rmin - params->r0) / params->dr) - 6.0;
-        const double uhi = std::floor((rmax - params->r0) / params->dr) + 7.0;
-        band_lo = std::min<long long>(band_lo, (long long)std::max(ulo, 0.0));
-        band_hi = std::max<long long>(band_hi, (long long)std::min(uhi, (double)params->nr - 1.0));
-    }
+    // Only the band of range bins the image can reach is copied.
+    long long band_lo = 0, band_hi = -1;
+    host_band(params, antenna_pos, 0, params->na, &band_lo, &band_hi);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (img_bytes && !plan->d_image)
@@ -660,6 +689,143 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
     st = enqueue_backprojection(plan, plan->d_image, plan->d_echo, plan->d_pos, &band, s);
     if (st != SARBP_OK)
         return st;
+    e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
+    plan->last_d2h = img_bytes;
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMemcpyAsync (to host)");
+    return SARBP_OK;
+}
+
+sarbp_status sarbp_backproject_streamed(sarbp_plan_t plan, void* image, const void* echoes,
+                                        const double* antenna_pos, const sarbp_params* params,
+                                        int32_t chunk_pulses, void* stream)
+{
+    if (!plan || !params || chunk_pulses < 1)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || plan->heights_mode)
+        return SARBP_ERR_PLAN_MISMATCH;
+    const long long pixels = (long long)params->nx * params->ny;
+    const size_t img_bytes = (size_t)pixels * 8;
+    if (pixels > 0 && !image)
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && !antenna_pos)
+        return SARBP_ERR_INVALID_ARG;
+    if ((size_t)params->na * params->nr > 0 && !echoes)
+        return SARBP_ERR_INVALID_ARG;
+    plan->last_error.clear();
+    plan->last_h2d = plan->last_d2h = 0;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+    if (pixels == 0)
+        return SARBP_OK;
+
+    const int chunk = std::max(1, std::min(chunk_pulses, std::max(params->na, 1)));
+    const size_t stage_need = (size_t)chunk * (size_t)params->nr * 8;
+    if (img_bytes && !plan->d_image)
+        e = cudaMalloc(&plan->d_image, img_bytes);
+    if (e == cudaSuccess && params->na > 0 && !plan->d_pos)
+        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
+    if (e == cudaSuccess && stage_need > plan->stage_bytes) {
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            cudaFree(plan->d_stage[b]);
+            plan->d_stage[b] = nullptr;
+            e = cudaMalloc(&plan->d_stage[b], stage_need);
+        }
+        plan->stage_bytes = e == cudaSuccess ? stage_need : 0;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMalloc (streaming buffers)");
+    if (!plan->copy_stream) {
+        e = cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = cudaEventCreateWithFlags(&plan->copied[b], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&plan->consumed[b], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&plan->call_start, cudaEventDisableTiming);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "stream/event creation");
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = plan->copy_stream;
+    // the copy stream starts after all earlier work on `stream` (which may
+    // still read the staging buffers of a previous call)
+    e = cudaEventRecord(plan->call_start, s);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(cs, plan->call_start, 0);
+    if (e == cudaSuccess && params->na > 0) {
+        e = cudaMemcpyAsync(plan->d_pos, antenna_pos, (size_t)params->na * 3 * sizeof(double),
+                            cudaMemcpyHostToDevice, cs);
+        plan->last_h2d += (size_t)params->na * 3 * sizeof(double);
+    }
+    if (e == cudaSuccess && (params->flags & SARBP_ACCUMULATE)) {
+        e = cudaMemcpyAsync(plan->d_image, image, img_bytes, cudaMemcpyHostToDevice, s);
+        plan->last_h2d += img_bytes;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaMemcpyAsync (to device)");
+
+    if (params->na == 0 || params->nr < 2) {
+        sarbp_params none = *params;
+        st = enqueue_backprojection(plan, plan->d_image, nullptr, plan->d_pos, &none, s);
+        if (st != SARBP_OK)
+            return st;
+    }
+    for (int c0 = 0, i = 0; c0 < params->na && params->nr >= 2; c0 += chunk, ++i) {
+        const int b = i & 1;
+        const int cn = std::min(chunk, params->na - c0);
+        long long lo = 0, hi = -1;
+        const bool any = host_band(params, antenna_pos, c0, c0 + cn, &lo, &hi);
+        sarbp_params sub = *params;
+        sub.na = cn;
+        if (c0 > 0)
+            sub.flags |= SARBP_ACCUMULATE;
+        // staging buffer b was last read by chunk i - 2
+        if (i >= 2)
+            e = cudaStreamWaitEvent(cs, plan->consumed[b], 0);
+        if (e == cudaSuccess && any) {
+            const size_t width = (size_t)(hi - lo + 1);
+            sub.nr = (int32_t)width;
+            sub.r0 = params->r0 + (double)lo * params->dr;
+            e = cudaMemcpy2DAsync(plan->d_stage[b], width * 8,
+                                  static_cast<const char*>(echoes) +
+                                      ((size_t)c0 * params->nr + (size_t)lo) * 8,
+                                  (size_t)params->nr * 8, width * 8, (size_t)cn,
+                                  cudaMemcpyHostToDevice, cs);
+            plan->last_h2d += width * 8 * (size_t)cn;
+        } else {
+            sub.nr = 0;                      // no pulse of the chunk reaches the axis
+        }
+        if (e == cudaSuccess)
+            e = cudaEventRecord(plan->copied[b], cs);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(s, plan->copied[b], 0);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "chunk copy");
+        st = enqueue_backprojection(plan, plan->d_image, plan->d_stage[b], plan->d_pos + 3 * (size_t)c0,
+                                    &sub, s);
+        if (st != SARBP_OK)
+            return st;
+        e = cudaEventRecord(plan->consumed[b], s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "cudaEventRecord");
+    }
     e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
     plan->last_d2h = img_bytes;
     if (e == cudaSuccess)

@@ -63,6 +63,25 @@ def _check_device_tensor(t, name, dtype, shape):
     return ctypes.c_void_p(t.data_ptr() if t.numel() else None)
 
 
+def _host_ptr(a, name, shape, np_dtype):
+    if hasattr(a, "is_cuda"):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+        if tuple(a.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+        return ctypes.c_void_p(a.data_ptr() if a.numel() else None)
+    if not (isinstance(a, np.ndarray) and a.dtype == np_dtype and a.flags.c_contiguous
+            and a.shape == shape):
+        raise ValueError(f"{name} must be a C-contiguous {np_dtype} array of shape {shape}")
+    return ctypes.c_void_p(a.ctypes.data if a.size else None)
+
+
+def _host_args(p, image, echoes, antenna_pos):
+    return (_host_ptr(image, "image", (p.ny, p.nx), np.complex64),
+            _host_ptr(echoes, "echoes", (p.na, p.nr), np.complex64),
+            _host_ptr(antenna_pos, "antenna_pos", (p.na, 3), np.float64))
+
+
 class Plan:
     """A libsarbp plan: fixed sizes, device scratch, repeated backprojections."""
 
@@ -149,26 +168,24 @@ class Plan:
                          stream=None, interp="linear"):
         """Same operation on host arrays (numpy or CPU tensors); returns when the image is on the host."""
         p = _params(params if params is not None else self.params, accumulate, interp)
-
-        def host_ptr(a, name, shape, np_dtype):
-            if hasattr(a, "is_cuda"):
-                if a.is_cuda or not a.is_contiguous():
-                    raise ValueError(f"{name} must be a contiguous CPU tensor")
-                if tuple(a.shape) != shape:
-                    raise ValueError(f"{name} must have shape {shape}")
-                return ctypes.c_void_p(a.data_ptr() if a.numel() else None)
-            if not (isinstance(a, np.ndarray) and a.dtype == np_dtype and a.flags.c_contiguous
-                    and a.shape == shape):
-                raise ValueError(f"{name} must be a C-contiguous {np_dtype} array of shape {shape}")
-            return ctypes.c_void_p(a.ctypes.data if a.size else None)
-
-        img = host_ptr(image, "image", (p.ny, p.nx), np.complex64)
-        ech = host_ptr(echoes, "echoes", (p.na, p.nr), np.complex64)
-        pos = host_ptr(antenna_pos, "antenna_pos", (p.na, 3), np.float64)
+        img, ech, pos = _host_args(p, image, echoes, antenna_pos)
         stream_h = ctypes.c_void_p(None) if stream is None else _stream_handle(stream)
         st = self._lib.sarbp_backproject_host(self._h, img, ech, pos, ctypes.byref(p), stream_h)
         if st != _native.SARBP_OK:
             self._raise(st, "sarbp_backproject_host")
+        return image
+
+    def backproject_streamed(self, image, echoes, antenna_pos, chunk_pulses=1024, params=None,
+                             accumulate=False, stream=None):
+        """Host arrays, pulses in chunks of ``chunk_pulses`` whose copies overlap the compute
+        (linear interpolation); returns when the image is on the host."""
+        p = _params(params if params is not None else self.params, accumulate)
+        img, ech, pos = _host_args(p, image, echoes, antenna_pos)
+        stream_h = ctypes.c_void_p(None) if stream is None else _stream_handle(stream)
+        st = self._lib.sarbp_backproject_streamed(self._h, img, ech, pos, ctypes.byref(p),
+                                                  int(chunk_pulses), stream_h)
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject_streamed")
         return image
 
     def host_transfer_bytes(self):

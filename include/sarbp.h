@@ -153,6 +153,34 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
                                     void* stream);
 
 /*
+ * sarbp_backproject_streamed - sarbp_backproject_host with the pulses taken
+ * in chunks and the copies overlapped with the computation (SARBP-GPU §3.3:
+ * pulses processed in batches, with transfers to the GPU overlapped with its
+ * work on streams).
+ *
+ * image, echoes, antenna_pos: HOST pointers as for sarbp_backproject_host.
+ * chunk_pulses: pulses per chunk, >= 1 (values above na mean one chunk).
+ *
+ * For chunk c (pulses c*chunk_pulses ...) the call finds on the host the band
+ * of range bins those pulses can reach from the image, copies that band into
+ * one of two device staging buffers on the plan's own copy stream, and
+ * backprojects it on `stream` into a device image, adding into the sum of the
+ * chunks before it; the copy of chunk c+1 runs while chunk c is computed.
+ * Pinned host memory is needed for the copies to overlap. The call returns
+ * when the image is on the host. With one chunk the result is bitwise that of
+ * sarbp_backproject_host; with several, the pulse sum is grouped by chunk and
+ * agrees to float32 rounding.
+ *
+ * Device memory owned by the plan, allocated on first use and kept until
+ * sarbp_destroy: the image, the antenna positions and two staging buffers of
+ * chunk_pulses x nr x 8 bytes. SARBP_ERR_INVALID_ARG for chunk_pulses < 1;
+ * SARBP_ERR_PLAN_MISMATCH as for sarbp_backproject_host.
+ */
+sarbp_status sarbp_backproject_streamed(sarbp_plan_t plan, void* image, const void* echoes,
+                                        const double* antenna_pos, const sarbp_params* params,
+                                        int32_t chunk_pulses, void* stream);
+
+/*
  * Pixels on a height map (SARBP-GPU §3.3 remarks that the range history may
  * have to take terrain elevation into account; the page gives no formula, so
  * this is the plain reading): pixel (ix, iy) sits at
