@@ -91,6 +91,16 @@ def test_nearest_config_full_image(index):
     print(check(sc.params, sc.echoes, sc.antenna_pos, img, targets=sc.targets))
 
 
+@pytest.mark.slow
+def test_nearest_page_scene_full_size():
+    """4096 pulses onto 1024 x 1024 pixels, the bench's launch configuration;
+    compared on the sampled pixel set."""
+    sc = scenes.make_scene(scenes.CONFIGS[2])
+    img = nearest_image(sc.params, sc.echoes, sc.antenna_pos)
+    print(check(sc.params, sc.echoes, sc.antenna_pos, img, pix=scenes.compared_pixels(sc),
+                targets=sc.targets))
+
+
 def _small(nx, ny, na=40, nr=512, noise=0.05):
     cfg = scenes.shrink(scenes.CONFIGS[0], nx=nx, ny=ny, na=na, nr=nr, spacing=0.5,
                         pulse_step=0.5, n_targets=0, noise_sigma=noise)
