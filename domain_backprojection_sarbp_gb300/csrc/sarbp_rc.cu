@@ -12,12 +12,18 @@
 // optional Hamming weighting 0.54 + 0.46 cos(2 pi f / b) over the centred band
 // |f| <= b/2 (f in cycles per sample), zero outside it.
 //
-// One CTA per pulse holds its zero-padded row in shared memory. The forward
-// transform is an in-place radix-4 decimation in frequency (natural order in,
-// digit-reversed out); the filter spectrum H is stored in that same order, so
-// the product needs no reordering; the inverse mirrors the forward passes
-// (digit-reversed in, natural out). The plan builds H with the same forward
-// transform on the zero-padded reference.
+// One CTA per pulse. The transforms are self-sorting (Stockham) passes of
+// radix 16 held in registers (16 complex values per thread), plus one pass of
+// radix 2, 4 or 8 when log2 N is not a multiple of 4; shared memory only
+// carries the data between passes, as separate real and imaginary planes
+// padded by one word every 32 (conflict-free for the strides used). The
+// forward transform takes the raw row straight from global memory (zero
+// beyond ns) and its last pass leaves each thread holding the spectrum at
+// indices j + t N/16, which are exactly the inputs of the inverse transform's
+// first pass: the filter multiply happens there in registers, with no trip
+// through shared memory. The inverse's last pass writes natural-order samples
+// straight to global memory. The filter spectrum H (conj FFT of the reference
+// times the window, divided by N) is built once by the plan, in natural order.
 #include "../../include/sarbp.h"
 #include "sarbp_internal.h"
 
@@ -28,148 +34,328 @@
 
 namespace {
 
-constexpr int RC_THREADS = 512;
-constexpr int RC_MAX_LOG2 = 14;            // N <= 16384: 128 KB of shared memory per row
+constexpr int RC_MAX_LOG2 = 14;            // N <= 16384: 135 KB of shared memory per row
+constexpr int EPT = 16;                    // complex values a thread holds
 
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
 __device__ __forceinline__ float2 cmul(float2 a, float2 b)
 {
-    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+    return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+__device__ __forceinline__ float2 conj_if(float2 a, bool c) { return c ? make_float2(a.x, -a.y) : a; }
+// a times S i, S = -1 (forward) or +1 (inverse)
+template <int S>
+__device__ __forceinline__ float2 mul_si(float2 a)
+{
+    return S < 0 ? make_float2(a.y, -a.x) : make_float2(-a.y, a.x);
 }
 
-// Forward transform, in place: radix-4 decimation-in-frequency passes over
-// spans N, N/4, ..., then one radix-2 pass of span 2 when log2 N is odd. The
-// result at position p is X[sigma(p)], sigma the mixed digit reversal below.
-// tw[t] = exp(-j 2 pi t / N), t < N.
-__device__ void dif_forward(float2* x, int n, int log2n, const float2* __restrict__ tw)
+// In-register DFTs, natural order in and out: X[k] = sum_m x[m] exp(S 2 pi i m k / R).
+template <int S>
+__device__ __forceinline__ void dft4(float2& a, float2& b, float2& c, float2& d)
 {
-    const int n4 = log2n / 2;
-    for (int lvl = 0; lvl < n4; ++lvl) {
-        const int lq = log2n - 2 * lvl - 2;          // q = span / 4 = 2^lq
-        const int q = 1 << lq;
-        const int tstep = 1 << (2 * lvl);            // N / span
-        for (int b = threadIdx.x; b < n / 4; b += blockDim.x) {
-            const int j = b & (q - 1);
-            const int base = ((b >> lq) << (lq + 2)) + j;
-            const float2 x0 = x[base], x1 = x[base + q], x2 = x[base + 2 * q], x3 = x[base + 3 * q];
-            const float2 a0 = make_float2(x0.x + x2.x, x0.y + x2.y);
-            const float2 a1 = make_float2(x0.x - x2.x, x0.y - x2.y);
-            const float2 a2 = make_float2(x1.x + x3.x, x1.y + x3.y);
-            const float2 a3 = make_float2(x1.y - x3.y, x3.x - x1.x);      // -j (x1 - x3)
-            x[base] = make_float2(a0.x + a2.x, a0.y + a2.y);
-            const int t = j * tstep;
-            x[base + q] = cmul(make_float2(a1.x + a3.x, a1.y + a3.y), __ldg(tw + t));
-            x[base + 2 * q] = cmul(make_float2(a0.x - a2.x, a0.y - a2.y), __ldg(tw + 2 * t));
-            x[base + 3 * q] = cmul(make_float2(a1.x - a3.x, a1.y - a3.y), __ldg(tw + 3 * t));
-        }
-        __syncthreads();
-    }
-    if (log2n & 1) {                                 // span 2: no twiddle
-        for (int b = threadIdx.x; b < n / 2; b += blockDim.x) {
-            const float2 a = x[2 * b], c = x[2 * b + 1];
-            x[2 * b] = make_float2(a.x + c.x, a.y + c.y);
-            x[2 * b + 1] = make_float2(a.x - c.x, a.y - c.y);
-        }
-        __syncthreads();
-    }
+    const float2 s0 = cadd(a, c), s1 = csub(a, c), s2 = cadd(b, d), s3 = mul_si<S>(csub(b, d));
+    a = cadd(s0, s2);
+    c = csub(s0, s2);
+    b = cadd(s1, s3);
+    d = csub(s1, s3);
 }
 
-// Inverse of dif_forward up to the factor N: the same passes mirrored
-// (conjugate twiddles first, then the inverse 4-point transform).
-__device__ void dit_inverse(float2* x, int n, int log2n, const float2* __restrict__ tw)
+template <int R, int S>
+__device__ __forceinline__ void dft(float2* v)
 {
-    const int n4 = log2n / 2;
-    if (log2n & 1) {
-        for (int b = threadIdx.x; b < n / 2; b += blockDim.x) {
-            const float2 a = x[2 * b], c = x[2 * b + 1];
-            x[2 * b] = make_float2(a.x + c.x, a.y + c.y);
-            x[2 * b + 1] = make_float2(a.x - c.x, a.y - c.y);
+    constexpr float H = 0.707106781186547524f;     // cos(pi/4)
+    constexpr float C1 = 0.923879532511286756f;    // cos(pi/8)
+    constexpr float S1 = 0.382683432365089772f;    // sin(pi/8)
+    if (R == 2) {
+        const float2 a = v[0], b = v[1];
+        v[0] = cadd(a, b);
+        v[1] = csub(a, b);
+    } else if (R == 4) {
+        dft4<S>(v[0], v[1], v[2], v[3]);
+    } else if (R == 8) {
+        float2 e0 = v[0], e1 = v[2], e2 = v[4], e3 = v[6];
+        float2 o0 = v[1], o1 = v[3], o2 = v[5], o3 = v[7];
+        dft4<S>(e0, e1, e2, e3);
+        dft4<S>(o0, o1, o2, o3);
+        o1 = cmul(o1, make_float2(H, S * H));           // W8^1
+        o2 = mul_si<S>(o2);                             // W8^2
+        o3 = cmul(o3, make_float2(-H, S * H));          // W8^3
+        v[0] = cadd(e0, o0); v[4] = csub(e0, o0);
+        v[1] = cadd(e1, o1); v[5] = csub(e1, o1);
+        v[2] = cadd(e2, o2); v[6] = csub(e2, o2);
+        v[3] = cadd(e3, o3); v[7] = csub(e3, o3);
+    } else {
+        // 16 = 4 x 4: m = 4 m1 + m2, k = k1 + 4 k2
+        float2 y[16];
+#pragma unroll
+        for (int m2 = 0; m2 < 4; ++m2) {
+            float2 a = v[m2], b = v[m2 + 4], c = v[m2 + 8], d = v[m2 + 12];
+            dft4<S>(a, b, c, d);
+            y[m2] = a; y[m2 + 4] = b; y[m2 + 8] = c; y[m2 + 12] = d;   // y[m2 + 4 k1]
         }
-        __syncthreads();
-    }
-    for (int lvl = n4 - 1; lvl >= 0; --lvl) {
-        const int lq = log2n - 2 * lvl - 2;
-        const int q = 1 << lq;
-        const int tstep = 1 << (2 * lvl);
-        for (int b = threadIdx.x; b < n / 4; b += blockDim.x) {
-            const int j = b & (q - 1);
-            const int base = ((b >> lq) << (lq + 2)) + j;
-            const int t = j * tstep;
-            const float2 w1 = __ldg(tw + t), w2 = __ldg(tw + 2 * t), w3 = __ldg(tw + 3 * t);
-            const float2 z0 = x[base];
-            const float2 z1 = cmul(x[base + q], make_float2(w1.x, -w1.y));
-            const float2 z2 = cmul(x[base + 2 * q], make_float2(w2.x, -w2.y));
-            const float2 z3 = cmul(x[base + 3 * q], make_float2(w3.x, -w3.y));
-            const float2 b0 = make_float2(z0.x + z2.x, z0.y + z2.y);
-            const float2 b1 = make_float2(z0.x - z2.x, z0.y - z2.y);
-            const float2 b2 = make_float2(z1.x + z3.x, z1.y + z3.y);
-            const float2 b3 = make_float2(z3.y - z1.y, z1.x - z3.x);     // +j (z1 - z3)
-            x[base] = make_float2(b0.x + b2.x, b0.y + b2.y);
-            x[base + q] = make_float2(b1.x + b3.x, b1.y + b3.y);
-            x[base + 2 * q] = make_float2(b0.x - b2.x, b0.y - b2.y);
-            x[base + 3 * q] = make_float2(b1.x - b3.x, b1.y - b3.y);
+        // twiddles W16^(m2 k1)
+        y[5] = cmul(y[5], make_float2(C1, S * S1));      // m2 1, k1 1
+        y[9] = cmul(y[9], make_float2(H, S * H));        // 1, 2
+        y[13] = cmul(y[13], make_float2(S1, S * C1));    // 1, 3
+        y[6] = cmul(y[6], make_float2(H, S * H));        // 2, 1
+        y[10] = mul_si<S>(y[10]);                        // 2, 2
+        y[14] = cmul(y[14], make_float2(-H, S * H));     // 2, 3
+        y[7] = cmul(y[7], make_float2(S1, S * C1));      // 3, 1
+        y[11] = cmul(y[11], make_float2(-H, S * H));     // 3, 2
+        y[15] = cmul(y[15], make_float2(-C1, -S * S1));  // 3, 3: W16^9
+#pragma unroll
+        for (int k1 = 0; k1 < 4; ++k1) {
+            float2 a = y[4 * k1], b = y[4 * k1 + 1], c = y[4 * k1 + 2], d = y[4 * k1 + 3];
+            dft4<S>(a, b, c, d);
+            v[k1] = a; v[k1 + 4] = b; v[k1 + 8] = c; v[k1 + 12] = d;     // X[k1 + 4 k2]
         }
-        __syncthreads();
     }
 }
 
-// Natural frequency index held at position p after dif_forward: the base-4
-// digits of p (most significant first) become the least significant digits
-// of the index, and the final base-2 digit, if any, the most significant.
-__device__ __forceinline__ int natural_index(int p, int log2n)
+// v[t] *= w^t, w = tw[k * stride] (conjugated for the inverse), t = 1 .. R-1.
+// Powers from at most four table entries, each product at most three
+// roundings deep.
+template <int R, int S>
+__device__ __forceinline__ void twiddle_inputs(float2* v, int k, int stride,
+                                               const float2* __restrict__ tw)
 {
-    const int n4 = log2n / 2;
-    int k = 0;
-    for (int lvl = 0; lvl < n4; ++lvl)
-        k |= ((p >> (log2n - 2 * lvl - 2)) & 3) << (2 * lvl);
-    if (log2n & 1)
-        k |= (p & 1) << (2 * n4);
-    return k;
+    const bool c = S > 0;
+    const int m = k * stride;
+    const float2 w1 = conj_if(__ldg(tw + m), c);
+    v[1] = cmul(v[1], w1);
+    if (R >= 4) {
+        const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1);
+        v[2] = cmul(v[2], w2);
+        v[3] = cmul(v[3], w3);
+        if (R >= 8) {
+            const float2 w4 = conj_if(__ldg(tw + 4 * m), c);
+            v[4] = cmul(v[4], w4);
+            v[5] = cmul(v[5], cmul(w4, w1));
+            v[6] = cmul(v[6], cmul(w4, w2));
+            v[7] = cmul(v[7], cmul(w4, w3));
+            if (R == 16) {
+                const float2 w8 = conj_if(__ldg(tw + 8 * m), c);
+                const float2 w12 = conj_if(__ldg(tw + 12 * m), c);
+                v[8] = cmul(v[8], w8);
+                v[9] = cmul(v[9], cmul(w8, w1));
+                v[10] = cmul(v[10], cmul(w8, w2));
+                v[11] = cmul(v[11], cmul(w8, w3));
+                v[12] = cmul(v[12], w12);
+                v[13] = cmul(v[13], cmul(w12, w1));
+                v[14] = cmul(v[14], cmul(w12, w2));
+                v[15] = cmul(v[15], cmul(w12, w3));
+            }
+        }
+    }
 }
 
-// The filter: H[p] = conj(FFT(ref)[k]) * W(k) at position p, k = natural_index(p).
-__global__ void __launch_bounds__(RC_THREADS) rc_filter_kernel(const float2* __restrict__ ref, int nref,
-                                                               int n, int log2n,
-                                                               const float2* __restrict__ tw,
-                                                               unsigned window, float band,
-                                                               float2* __restrict__ h)
+__device__ __forceinline__ int pad(int i) { return i + (i >> 5); }
+
+// Shared row: real plane then imaginary plane, each pad(n - 1) + 1 words.
+struct Row {
+    float* re;
+    float* im;
+    __device__ __forceinline__ float2 ld(int i) const { return make_float2(re[pad(i)], im[pad(i)]); }
+    __device__ __forceinline__ void st(int i, float2 v) const
+    {
+        re[pad(i)] = v.x;
+        im[pad(i)] = v.y;
+    }
+};
+
+// One radix-16 Stockham pass from shared memory to registers: thread j
+// (j < n / 16) reads x[j + t n/16], applies the twiddles of span ns and the
+// DFT. Its outputs belong at (j / ns) ns 16 + j % ns + t ns.
+template <int S>
+__device__ __forceinline__ void pass16_load(const Row& r, float2* v, int j, int n, int ns,
+                                            const float2* __restrict__ tw)
 {
-    extern __shared__ float2 row[];
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-        row[i] = i < nref ? ref[i] : make_float2(0.f, 0.f);
+    const int q = n >> 4;
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+        v[t] = r.ld(j + t * q);
+    if (ns > 1)
+        twiddle_inputs<16, S>(v, j & (ns - 1), n / (ns * 16), tw);
+    dft<16, S>(v);
+}
+
+// Forward transform of one zero-padded row (x = src[0 .. len-1], 0 beyond)
+// up to its last pass, which is left in registers: on return thread `tid`
+// holds X[j + t n/RL] in v[b RL + t] for its butterflies j = tid + b T,
+// RL = 16 when passes > 1, else R0. Ends with a barrier.
+template <int R0>
+__device__ __forceinline__ void forward_to_registers(const float2* __restrict__ src, int len, int n,
+                                                     int passes, const float2* __restrict__ tw,
+                                                     const Row& r, float2 (&v)[EPT])
+{
+    const int T = blockDim.x, tid = threadIdx.x;
+    constexpr int B0 = EPT / R0;
+    const int nb0 = n / R0;
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = tid + b * T;
+#pragma unroll
+        for (int t = 0; t < R0; ++t) {
+            const int i = j + t * nb0;
+            v[b * R0 + t] = (j < nb0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
+        }
+        dft<R0, -1>(v + b * R0);
+    }
+    if (passes == 1)
+        return;
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = tid + b * T;
+        if (j < nb0) {
+#pragma unroll
+            for (int t = 0; t < R0; ++t)
+                r.st(j * R0 + t, v[b * R0 + t]);
+        }
+    }
     __syncthreads();
-    dif_forward(row, n, log2n, tw);
-    for (int p = threadIdx.x; p < n; p += blockDim.x) {
-        const int k = natural_index(p, log2n);
-        float w = 1.0f;
-        if (window == SARBP_WINDOW_HAMMING) {
-            const float f = (float)(k < n / 2 ? k : k - n) / (float)n;
-            w = fabsf(f) <= 0.5f * band ? 0.54f + 0.46f * cospif(2.0f * f / band) : 0.0f;
+    const bool act = tid < (n >> 4);
+    int ns = R0;
+    for (int p = 1; p < passes; ++p) {
+        if (act)
+            pass16_load<-1>(r, v, tid, n, ns, tw);
+        __syncthreads();
+        if (p < passes - 1) {
+            if (act) {
+                const int k = tid & (ns - 1);
+                const int base = (tid - k) * 16 + k;
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    r.st(base + t * ns, v[t]);
+            }
+            __syncthreads();
         }
-        const float2 v = row[p];
-        h[p] = make_float2(v.x * w, -v.y * w);
+        ns *= 16;
     }
 }
 
-__global__ void __launch_bounds__(RC_THREADS) rc_kernel(const float2* __restrict__ raw, int ns, int n,
-                                                        int log2n, const float2* __restrict__ tw,
-                                                        const float2* __restrict__ h,
-                                                        float2* __restrict__ out)
+template <int R0>
+__global__ void __launch_bounds__(1024) rc_filter_kernel(const float2* __restrict__ ref, int nref,
+                                                         int n, int passes,
+                                                         const float2* __restrict__ tw,
+                                                         unsigned window, float band,
+                                                         float2* __restrict__ h)
 {
-    extern __shared__ float2 row[];
-    const size_t base = (size_t)blockIdx.x * ns;
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-        row[i] = i < ns ? raw[base + i] : make_float2(0.f, 0.f);
-    __syncthreads();
-    dif_forward(row, n, log2n, tw);
-    for (int p = threadIdx.x; p < n; p += blockDim.x)
-        row[p] = cmul(row[p], __ldg(h + p));
-    __syncthreads();
-    dit_inverse(row, n, log2n, tw);
-    const float scale = 1.0f / (float)n;
-    for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-        const float2 v = row[i];
-        out[base + i] = make_float2(v.x * scale, v.y * scale);
+    extern __shared__ float smem[];
+    const int plane = pad(n - 1) + 1;
+    const Row r{smem, smem + plane};
+    float2 v[EPT];
+    forward_to_registers<R0>(ref, nref, n, passes, tw, r, v);
+    const int RL = passes > 1 ? 16 : R0;
+    const int BL = EPT / RL, nbl = n / RL;
+    const float inv_n = 1.0f / (float)n;
+    for (int b = 0; b < BL; ++b) {
+        const int j = threadIdx.x + b * blockDim.x;
+        if (j >= nbl)
+            continue;
+        for (int t = 0; t < RL; ++t) {
+            const int m = j + t * nbl;                  // natural frequency index
+            float w = 1.0f;
+            if (window == SARBP_WINDOW_HAMMING) {
+                const float f = (float)(m < n / 2 ? m : m - n) / (float)n;
+                w = fabsf(f) <= 0.5f * band ? 0.54f + 0.46f * cospif(2.0f * f / band) : 0.0f;
+            }
+            const float2 x = v[b * RL + t];
+            h[m] = make_float2(x.x * w * inv_n, -x.y * w * inv_n);
+        }
     }
+}
+
+template <int R0>
+__global__ void __launch_bounds__(1024) rc_kernel(const float2* __restrict__ raw, int ns_in, int n,
+                                                  int passes, const float2* __restrict__ tw,
+                                                  const float2* __restrict__ h,
+                                                  float2* __restrict__ out)
+{
+    extern __shared__ float smem[];
+    const int plane = pad(n - 1) + 1;
+    const Row r{smem, smem + plane};
+    const int T = blockDim.x, tid = threadIdx.x;
+    const size_t row0 = (size_t)blockIdx.x * ns_in;
+    float2 v[EPT];
+    forward_to_registers<R0>(raw + row0, ns_in, n, passes, tw, r, v);
+
+    if (passes == 1) {
+        // n = R0 <= 16: thread 0 holds the whole spectrum
+        if (tid == 0) {
+#pragma unroll
+            for (int t = 0; t < R0; ++t)
+                v[t] = cmul(v[t], __ldg(h + t));
+            dft<R0, 1>(v);
+#pragma unroll
+            for (int t = 0; t < R0; ++t)
+                if (t < ns_in)
+                    out[row0 + t] = v[t];
+        }
+        return;
+    }
+
+    // filter, then the inverse's first pass (radix 16, span 1) on the held values
+    const int q = n >> 4;
+    const bool act = tid < q;
+    if (act) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            v[t] = cmul(v[t], __ldg(h + tid + t * q));
+        dft<16, 1>(v);
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            r.st(tid * 16 + t, v[t]);
+    }
+    __syncthreads();
+    int ns = 16;
+    for (int p = 1; p < passes - 1; ++p) {
+        if (act)
+            pass16_load<1>(r, v, tid, n, ns, tw);
+        __syncthreads();
+        if (act) {
+            const int k = tid & (ns - 1);
+            const int base = (tid - k) * 16 + k;
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                r.st(base + t * ns, v[t]);
+        }
+        __syncthreads();
+        ns *= 16;
+    }
+    // last pass: radix R0, span ns = n / R0; outputs go to j + t n/R0
+    constexpr int B0 = EPT / R0;
+    const int nb0 = n / R0;
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = tid + b * T;
+        if (j >= nb0)
+            continue;
+        float2* w = v + b * R0;
+#pragma unroll
+        for (int t = 0; t < R0; ++t)
+            w[t] = r.ld(j + t * nb0);
+        twiddle_inputs<R0, 1>(w, j, 1, tw);
+        dft<R0, 1>(w);
+#pragma unroll
+        for (int t = 0; t < R0; ++t) {
+            const int i = j + t * nb0;
+            if (i < ns_in)
+                out[row0 + i] = w[t];
+        }
+    }
+}
+
+template <int R0>
+cudaError_t set_smem(size_t bytes)
+{
+    cudaError_t e = cudaFuncSetAttribute(rc_kernel<R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_filter_kernel<R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes);
+    return e;
 }
 
 }  // namespace
@@ -177,10 +363,43 @@ __global__ void __launch_bounds__(RC_THREADS) rc_kernel(const float2* __restrict
 struct sarbp_rc_plan_s {
     sarbp_rc_params p{};
     int n = 0, log2n = 0;
+    int r0 = 2, passes = 1;    // first forward pass radix (2, 4, 8, 16), then radix-16 passes
+    int threads = 32;
+    size_t smem = 0;
     int device = -1;
-    float2* tw = nullptr;      // N twiddles
-    float2* h = nullptr;       // N filter coefficients, in the forward transform's order
+    float2* tw = nullptr;      // N twiddles exp(-2 pi i m / N)
+    float2* h = nullptr;       // N filter coefficients / N, natural order
 };
+
+namespace {
+
+cudaError_t launch_filter(const sarbp_rc_plan_s* plan, const float2* ref, cudaStream_t s)
+{
+    const int n = plan->n, ps = plan->passes, nref = plan->p.nref;
+    const unsigned win = plan->p.window;
+    const float band = (float)plan->p.band_fraction;
+    switch (plan->r0) {
+    case 2: rc_filter_kernel<2><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
+    case 4: rc_filter_kernel<4><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
+    case 8: rc_filter_kernel<8><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
+    default: rc_filter_kernel<16><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rc(const sarbp_rc_plan_s* plan, const float2* raw, float2* out, cudaStream_t s)
+{
+    const int na = plan->p.na, ns = plan->p.ns, n = plan->n, ps = plan->passes;
+    switch (plan->r0) {
+    case 2: rc_kernel<2><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
+    case 4: rc_kernel<4><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
+    case 8: rc_kernel<8><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
+    default: rc_kernel<16><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -211,6 +430,18 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     plan->p = *p;
     plan->log2n = log2n;
     plan->n = 1 << log2n;
+    if (log2n < 4) {
+        plan->r0 = plan->n;
+        plan->passes = 1;
+    } else {
+        plan->r0 = (log2n % 4) ? (1 << (log2n % 4)) : 16;
+        plan->passes = 1;
+        for (int l = log2n - (log2n % 4 ? log2n % 4 : 4); l > 0; l -= 4)
+            ++plan->passes;
+    }
+    plan->threads = plan->n / 16 > 32 ? plan->n / 16 : 32;
+    const int plane = (plan->n - 1) + ((plan->n - 1) >> 5) + 1;
+    plan->smem = 2 * (size_t)plane * sizeof(float);
     cudaError_t e = cudaGetDevice(&plan->device);
     int major = 0, minor = 0;
     if (e == cudaSuccess)
@@ -221,12 +452,14 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
         delete plan;
         return SARBP_ERR_UNSUPPORTED_DEVICE;
     }
-    const size_t smem = (size_t)plan->n * sizeof(float2);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(rc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(rc_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    if (e == cudaSuccess) {
+        switch (plan->r0) {
+        case 2: e = set_smem<2>(plan->smem); break;
+        case 4: e = set_smem<4>(plan->smem); break;
+        case 8: e = set_smem<8>(plan->smem); break;
+        default: e = set_smem<16>(plan->smem); break;
+        }
+    }
     if (e == cudaSuccess)
         e = cudaMalloc(&plan->tw, (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess)
@@ -242,12 +475,8 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
         e = cudaMemcpy(plan->tw, tw.data(), tw.size() * sizeof(float2), cudaMemcpyHostToDevice);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (e == cudaSuccess) {
-        rc_filter_kernel<<<1, RC_THREADS, smem, s>>>(static_cast<const float2*>(ref), p->nref,
-                                                     plan->n, plan->log2n, plan->tw, p->window,
-                                                     (float)p->band_fraction, plan->h);
-        e = cudaGetLastError();
-    }
+    if (e == cudaSuccess)
+        e = launch_filter(plan, static_cast<const float2*>(ref), s);
     if (e != cudaSuccess) {
         cudaFree(plan->tw);
         cudaFree(plan->h);
@@ -271,10 +500,10 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
         return SARBP_ERR_INVALID_ARG;
-    rc_kernel<<<p.na, RC_THREADS, (size_t)plan->n * sizeof(float2), static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const float2*>(raw), p.ns, plan->n, plan->log2n, plan->tw, plan->h,
-        static_cast<float2*>(out));
-    return cudaGetLastError() == cudaSuccess ? SARBP_OK : SARBP_ERR_CUDA;
+    return launch_rc(plan, static_cast<const float2*>(raw), static_cast<float2*>(out),
+                     static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SARBP_OK
+               : SARBP_ERR_CUDA;
 }
 
 sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan)

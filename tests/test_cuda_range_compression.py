@@ -39,7 +39,10 @@ def gpu_compress(raw, ref, window="none", band=1.0):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("ns,nref", [(100, 7), (1000, 25), (4096, 359), (16384 - 358, 359)])
+# FFT sizes 2 .. 16384: every first-pass radix (2, 4, 8, 16) and one to four passes
+@pytest.mark.parametrize("ns,nref", [(1, 1), (3, 2), (5, 3), (10, 5), (20, 9), (50, 10), (100, 7),
+                                     (200, 40), (400, 100), (1000, 25), (1500, 300), (3000, 500),
+                                     (4096, 359), (16384 - 358, 359)])
 def test_random_rows(ns, nref):
     rng = np.random.default_rng(ns)
     raw = (rng.standard_normal((5, ns)) + 1j * rng.standard_normal((5, ns))).astype(np.complex64)
