@@ -151,114 +151,146 @@ __device__ __forceinline__ void twiddle_inputs(float2* v, int k, int stride,
     }
 }
 
-__device__ __forceinline__ int pad(int i) { return i + (i >> 5); }
+__host__ __device__ constexpr int pad(int i) { return i + (i >> 5); }
 
-// Shared row: real plane then imaginary plane, each pad(n - 1) + 1 words.
+// Pass structure of an N = 2^L transform: a first pass of radix R0 (2, 4, 8
+// or 16, so that the rest are radix 16), PASSES passes in all, T threads.
+template <int L>
+struct Fft {
+    static constexpr int N = 1 << L;
+    static constexpr int R0 = L < 4 ? N : ((L % 4) ? (1 << (L % 4)) : 16);
+    static constexpr int PASSES = L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4;
+    static constexpr int T = N / 16 > 32 ? N / 16 : 32;
+    static constexpr int PLANE = pad(N - 1) + 1;       // words per padded plane
+    static constexpr int Q = N / 16 > 0 ? N / 16 : 1;  // radix-16 butterflies
+};
+
+// Shared row: real plane then imaginary plane. Every access pattern used
+// below is base + t S with (base mod 32) + (t S mod 32) < 32, for which
+// pad(base + t S) = pad(base) + pad(t S): one padded base per butterfly and
+// compile-time offsets.
 struct Row {
     float* re;
     float* im;
-    __device__ __forceinline__ float2 ld(int i) const { return make_float2(re[pad(i)], im[pad(i)]); }
-    __device__ __forceinline__ void st(int i, float2 v) const
+    __device__ __forceinline__ float2 ld(int pi) const { return make_float2(re[pi], im[pi]); }
+    __device__ __forceinline__ void st(int pi, float2 v) const
     {
-        re[pad(i)] = v.x;
-        im[pad(i)] = v.y;
+        re[pi] = v.x;
+        im[pi] = v.y;
     }
 };
 
-// One radix-16 Stockham pass from shared memory to registers: thread j
-// (j < n / 16) reads x[j + t n/16], applies the twiddles of span ns and the
-// DFT. Its outputs belong at (j / ns) ns 16 + j % ns + t ns.
-template <int S>
-__device__ __forceinline__ void pass16_load(const Row& r, float2* v, int j, int n, int ns,
-                                            const float2* __restrict__ tw)
+// Radix-R Stockham pass body from shared memory: inputs x[j + t N/R], twiddles
+// of span NS, the DFT. Outputs belong at pad(base) + pad(t NS), base =
+// (j / NS) NS R + j % NS.
+template <int R, int S, int N, int NS>
+__device__ __forceinline__ void pass_load(const Row& r, float2* v, int j,
+                                          const float2* __restrict__ tw)
 {
-    const int q = n >> 4;
+    constexpr int STRIDE = N / R;
+    const int pb = pad(j);
 #pragma unroll
-    for (int t = 0; t < 16; ++t)
-        v[t] = r.ld(j + t * q);
-    if (ns > 1)
-        twiddle_inputs<16, S>(v, j & (ns - 1), n / (ns * 16), tw);
-    dft<16, S>(v);
+    for (int t = 0; t < R; ++t)
+        v[t] = r.ld(pb + pad(t * STRIDE));
+    if (NS > 1)
+        twiddle_inputs<R, S>(v, j & (NS - 1), N / (NS * R), tw);
+    dft<R, S>(v);
 }
 
-// Forward transform of one zero-padded row (x = src[0 .. len-1], 0 beyond)
-// up to its last pass, which is left in registers: on return thread `tid`
-// holds X[j + t n/RL] in v[b RL + t] for its butterflies j = tid + b T,
-// RL = 16 when passes > 1, else R0. Ends with a barrier.
-template <int R0>
-__device__ __forceinline__ void forward_to_registers(const float2* __restrict__ src, int len, int n,
-                                                     int passes, const float2* __restrict__ tw,
-                                                     const Row& r, float2 (&v)[EPT])
+template <int R, int NS>
+__device__ __forceinline__ void pass_store(const Row& r, const float2* v, int j)
 {
-    const int T = blockDim.x, tid = threadIdx.x;
-    constexpr int B0 = EPT / R0;
-    const int nb0 = n / R0;
+    const int k = j & (NS - 1);
+    const int pb = pad((j - k) * R + k);
+#pragma unroll
+    for (int t = 0; t < R; ++t)
+        r.st(pb + pad(t * NS), v[t]);
+}
+
+// Radix-16 passes p = P0 .. P1-1 of one direction (span NS at pass P0),
+// shared memory to shared memory, ending with a barrier. Unrolled at compile
+// time so that every span and offset is a constant.
+template <int L, int S, int P, int P1, int NS>
+struct Middle {
+    static __device__ __forceinline__ void run(const Row& r, float2* v, int tid,
+                                               const float2* __restrict__ tw)
+    {
+        if constexpr (P < P1) {
+            const bool act = tid < Fft<L>::Q;
+            if (act)
+                pass_load<16, S, Fft<L>::N, NS>(r, v, tid, tw);
+            __syncthreads();
+            if (act)
+                pass_store<16, NS>(r, v, tid);
+            __syncthreads();
+            Middle<L, S, P + 1, P1, NS * 16>::run(r, v, tid, tw);
+        }
+    }
+};
+
+// Forward transform of one zero-padded row (src[0 .. len-1], 0 beyond) up
+// to its last pass, which stays in registers: thread tid holds X[j + t N/RL]
+// in v[b RL + t], j = tid + b T, RL = 16 when PASSES > 1, else R0. Ends after
+// a barrier, so the shared row may be rewritten.
+template <int L>
+__device__ __forceinline__ void forward_to_registers(const float2* __restrict__ src, int len,
+                                                     const float2* __restrict__ tw, const Row& r,
+                                                     float2 (&v)[EPT])
+{
+    using F = Fft<L>;
+    constexpr int R0 = F::R0, B0 = EPT / R0, NB0 = F::N / R0;
+    const int tid = threadIdx.x;
 #pragma unroll
     for (int b = 0; b < B0; ++b) {
-        const int j = tid + b * T;
+        const int j = tid + b * F::T;
 #pragma unroll
         for (int t = 0; t < R0; ++t) {
-            const int i = j + t * nb0;
-            v[b * R0 + t] = (j < nb0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
+            const int i = j + t * NB0;
+            v[b * R0 + t] = (j < NB0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
         }
         dft<R0, -1>(v + b * R0);
     }
-    if (passes == 1)
-        return;
+    if constexpr (F::PASSES > 1) {
 #pragma unroll
-    for (int b = 0; b < B0; ++b) {
-        const int j = tid + b * T;
-        if (j < nb0) {
-#pragma unroll
-            for (int t = 0; t < R0; ++t)
-                r.st(j * R0 + t, v[b * R0 + t]);
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+            if (j < NB0)
+                pass_store<R0, 1>(r, v + b * R0, j);
         }
-    }
-    __syncthreads();
-    const bool act = tid < (n >> 4);
-    int ns = R0;
-    for (int p = 1; p < passes; ++p) {
-        if (act)
-            pass16_load<-1>(r, v, tid, n, ns, tw);
         __syncthreads();
-        if (p < passes - 1) {
-            if (act) {
-                const int k = tid & (ns - 1);
-                const int base = (tid - k) * 16 + k;
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    r.st(base + t * ns, v[t]);
-            }
-            __syncthreads();
-        }
-        ns *= 16;
+        Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid, tw);
+        constexpr int NSL = F::N / 16;                 // span of the last pass
+        if (tid < F::Q)
+            pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
+        __syncthreads();
     }
 }
 
-template <int R0>
-__global__ void __launch_bounds__(1024) rc_filter_kernel(const float2* __restrict__ ref, int nref,
-                                                         int n, int passes,
-                                                         const float2* __restrict__ tw,
-                                                         unsigned window, float band,
-                                                         float2* __restrict__ h)
+template <int L>
+__global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __restrict__ ref, int nref,
+                                                              const float2* __restrict__ tw,
+                                                              unsigned window, float band,
+                                                              float2* __restrict__ h)
 {
+    using F = Fft<L>;
     extern __shared__ float smem[];
-    const int plane = pad(n - 1) + 1;
-    const Row r{smem, smem + plane};
+    const Row r{smem, smem + F::PLANE};
     float2 v[EPT];
-    forward_to_registers<R0>(ref, nref, n, passes, tw, r, v);
-    const int RL = passes > 1 ? 16 : R0;
-    const int BL = EPT / RL, nbl = n / RL;
-    const float inv_n = 1.0f / (float)n;
+    forward_to_registers<L>(ref, nref, tw, r, v);
+    constexpr int RL = F::PASSES > 1 ? 16 : F::R0;
+    constexpr int BL = EPT / RL, NBL = F::N / RL;
+    const float inv_n = 1.0f / (float)F::N;
+#pragma unroll
     for (int b = 0; b < BL; ++b) {
-        const int j = threadIdx.x + b * blockDim.x;
-        if (j >= nbl)
+        const int j = threadIdx.x + b * F::T;
+        if (j >= NBL)
             continue;
+#pragma unroll
         for (int t = 0; t < RL; ++t) {
-            const int m = j + t * nbl;                  // natural frequency index
+            const int m = j + t * NBL;                  // natural frequency index
             float w = 1.0f;
             if (window == SARBP_WINDOW_HAMMING) {
-                const float f = (float)(m < n / 2 ? m : m - n) / (float)n;
+                const float f = (float)(m < F::N / 2 ? m : m - F::N) / (float)F::N;
                 w = fabsf(f) <= 0.5f * band ? 0.54f + 0.46f * cospif(2.0f * f / band) : 0.0f;
             }
             const float2 x = v[b * RL + t];
@@ -267,22 +299,23 @@ __global__ void __launch_bounds__(1024) rc_filter_kernel(const float2* __restric
     }
 }
 
-template <int R0>
-__global__ void __launch_bounds__(1024) rc_kernel(const float2* __restrict__ raw, int ns_in, int n,
-                                                  int passes, const float2* __restrict__ tw,
-                                                  const float2* __restrict__ h,
-                                                  float2* __restrict__ out)
+template <int L>
+__global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict__ raw, int ns_in,
+                                                       const float2* __restrict__ tw,
+                                                       const float2* __restrict__ h,
+                                                       float2* __restrict__ out)
 {
+    using F = Fft<L>;
+    constexpr int N = F::N, R0 = F::R0;
     extern __shared__ float smem[];
-    const int plane = pad(n - 1) + 1;
-    const Row r{smem, smem + plane};
-    const int T = blockDim.x, tid = threadIdx.x;
+    const Row r{smem, smem + F::PLANE};
+    const int tid = threadIdx.x;
     const size_t row0 = (size_t)blockIdx.x * ns_in;
     float2 v[EPT];
-    forward_to_registers<R0>(raw + row0, ns_in, n, passes, tw, r, v);
+    forward_to_registers<L>(raw + row0, ns_in, tw, r, v);
 
-    if (passes == 1) {
-        // n = R0 <= 16: thread 0 holds the whole spectrum
+    if constexpr (F::PASSES == 1) {
+        // N = R0 <= 16: thread 0 holds the whole spectrum
         if (tid == 0) {
 #pragma unroll
             for (int t = 0; t < R0; ++t)
@@ -293,69 +326,101 @@ __global__ void __launch_bounds__(1024) rc_kernel(const float2* __restrict__ raw
                 if (t < ns_in)
                     out[row0 + t] = v[t];
         }
-        return;
-    }
-
-    // filter, then the inverse's first pass (radix 16, span 1) on the held values
-    const int q = n >> 4;
-    const bool act = tid < q;
-    if (act) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            v[t] = cmul(v[t], __ldg(h + tid + t * q));
-        dft<16, 1>(v);
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            r.st(tid * 16 + t, v[t]);
-    }
-    __syncthreads();
-    int ns = 16;
-    for (int p = 1; p < passes - 1; ++p) {
-        if (act)
-            pass16_load<1>(r, v, tid, n, ns, tw);
-        __syncthreads();
-        if (act) {
-            const int k = tid & (ns - 1);
-            const int base = (tid - k) * 16 + k;
+    } else {
+        // filter, then the inverse's first pass (radix 16, span 1) on the held values
+        constexpr int Q = F::Q;
+        if (tid < Q) {
 #pragma unroll
             for (int t = 0; t < 16; ++t)
-                r.st(base + t * ns, v[t]);
+                v[t] = cmul(v[t], __ldg(h + tid + t * Q));
+            dft<16, 1>(v);
+            pass_store<16, 1>(r, v, tid);
         }
         __syncthreads();
-        ns *= 16;
-    }
-    // last pass: radix R0, span ns = n / R0; outputs go to j + t n/R0
-    constexpr int B0 = EPT / R0;
-    const int nb0 = n / R0;
+        Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid, tw);
+        // last pass: radix R0, span N / R0; outputs go to j + t N/R0
+        constexpr int B0 = EPT / R0, NB0 = N / R0;
 #pragma unroll
-    for (int b = 0; b < B0; ++b) {
-        const int j = tid + b * T;
-        if (j >= nb0)
-            continue;
-        float2* w = v + b * R0;
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+            if (j >= NB0)
+                continue;
+            float2* w = v + b * R0;
+            pass_load<R0, 1, N, NB0>(r, w, j, tw);
 #pragma unroll
-        for (int t = 0; t < R0; ++t)
-            w[t] = r.ld(j + t * nb0);
-        twiddle_inputs<R0, 1>(w, j, 1, tw);
-        dft<R0, 1>(w);
-#pragma unroll
-        for (int t = 0; t < R0; ++t) {
-            const int i = j + t * nb0;
-            if (i < ns_in)
-                out[row0 + i] = w[t];
+            for (int t = 0; t < R0; ++t) {
+                const int i = j + t * NB0;
+                if (i < ns_in)
+                    out[row0 + i] = w[t];
+            }
         }
     }
 }
 
-template <int R0>
-cudaError_t set_smem(size_t bytes)
+template <int L>
+cudaError_t set_smem_l()
 {
-    cudaError_t e = cudaFuncSetAttribute(rc_kernel<R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bytes);
+    const int bytes = 2 * Fft<L>::PLANE * (int)sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(rc_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(rc_filter_kernel<R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes);
+        e = cudaFuncSetAttribute(rc_filter_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return e;
+}
+
+template <int L>
+cudaError_t launch_l(bool filter, int na, const float2* in, int len, const float2* tw,
+                     const float2* h_in, unsigned window, float band, float2* out, cudaStream_t s)
+{
+    const size_t bytes = 2 * (size_t)Fft<L>::PLANE * sizeof(float);
+    if (filter)
+        rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, tw, window, band, out);
+    else
+        rc_kernel<L><<<na, Fft<L>::T, bytes, s>>>(in, len, tw, h_in, out);
+    return cudaGetLastError();
+}
+
+// log2 N -> the instantiation for it
+cudaError_t set_smem(int log2n)
+{
+    switch (log2n) {
+    case 1: return set_smem_l<1>();
+    case 2: return set_smem_l<2>();
+    case 3: return set_smem_l<3>();
+    case 4: return set_smem_l<4>();
+    case 5: return set_smem_l<5>();
+    case 6: return set_smem_l<6>();
+    case 7: return set_smem_l<7>();
+    case 8: return set_smem_l<8>();
+    case 9: return set_smem_l<9>();
+    case 10: return set_smem_l<10>();
+    case 11: return set_smem_l<11>();
+    case 12: return set_smem_l<12>();
+    case 13: return set_smem_l<13>();
+    case 14: return set_smem_l<14>();
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch(int log2n, bool filter, int na, const float2* in, int len, const float2* tw,
+                   const float2* h_in, unsigned window, float band, float2* out, cudaStream_t s)
+{
+    switch (log2n) {
+    case 1: return launch_l<1>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 2: return launch_l<2>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 3: return launch_l<3>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 4: return launch_l<4>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 5: return launch_l<5>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 6: return launch_l<6>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 7: return launch_l<7>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 8: return launch_l<8>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 9: return launch_l<9>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 10: return launch_l<10>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 11: return launch_l<11>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 12: return launch_l<12>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 13: return launch_l<13>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 14: return launch_l<14>(filter, na, in, len, tw, h_in, window, band, out, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -363,43 +428,10 @@ cudaError_t set_smem(size_t bytes)
 struct sarbp_rc_plan_s {
     sarbp_rc_params p{};
     int n = 0, log2n = 0;
-    int r0 = 2, passes = 1;    // first forward pass radix (2, 4, 8, 16), then radix-16 passes
-    int threads = 32;
-    size_t smem = 0;
     int device = -1;
     float2* tw = nullptr;      // N twiddles exp(-2 pi i m / N)
     float2* h = nullptr;       // N filter coefficients / N, natural order
 };
-
-namespace {
-
-cudaError_t launch_filter(const sarbp_rc_plan_s* plan, const float2* ref, cudaStream_t s)
-{
-    const int n = plan->n, ps = plan->passes, nref = plan->p.nref;
-    const unsigned win = plan->p.window;
-    const float band = (float)plan->p.band_fraction;
-    switch (plan->r0) {
-    case 2: rc_filter_kernel<2><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
-    case 4: rc_filter_kernel<4><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
-    case 8: rc_filter_kernel<8><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
-    default: rc_filter_kernel<16><<<1, plan->threads, plan->smem, s>>>(ref, nref, n, ps, plan->tw, win, band, plan->h); break;
-    }
-    return cudaGetLastError();
-}
-
-cudaError_t launch_rc(const sarbp_rc_plan_s* plan, const float2* raw, float2* out, cudaStream_t s)
-{
-    const int na = plan->p.na, ns = plan->p.ns, n = plan->n, ps = plan->passes;
-    switch (plan->r0) {
-    case 2: rc_kernel<2><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
-    case 4: rc_kernel<4><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
-    case 8: rc_kernel<8><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
-    default: rc_kernel<16><<<na, plan->threads, plan->smem, s>>>(raw, ns, n, ps, plan->tw, plan->h, out); break;
-    }
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 extern "C" {
 
@@ -430,18 +462,6 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     plan->p = *p;
     plan->log2n = log2n;
     plan->n = 1 << log2n;
-    if (log2n < 4) {
-        plan->r0 = plan->n;
-        plan->passes = 1;
-    } else {
-        plan->r0 = (log2n % 4) ? (1 << (log2n % 4)) : 16;
-        plan->passes = 1;
-        for (int l = log2n - (log2n % 4 ? log2n % 4 : 4); l > 0; l -= 4)
-            ++plan->passes;
-    }
-    plan->threads = plan->n / 16 > 32 ? plan->n / 16 : 32;
-    const int plane = (plan->n - 1) + ((plan->n - 1) >> 5) + 1;
-    plan->smem = 2 * (size_t)plane * sizeof(float);
     cudaError_t e = cudaGetDevice(&plan->device);
     int major = 0, minor = 0;
     if (e == cudaSuccess)
@@ -452,14 +472,8 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
         delete plan;
         return SARBP_ERR_UNSUPPORTED_DEVICE;
     }
-    if (e == cudaSuccess) {
-        switch (plan->r0) {
-        case 2: e = set_smem<2>(plan->smem); break;
-        case 4: e = set_smem<4>(plan->smem); break;
-        case 8: e = set_smem<8>(plan->smem); break;
-        default: e = set_smem<16>(plan->smem); break;
-        }
-    }
+    if (e == cudaSuccess)
+        e = set_smem(log2n);
     if (e == cudaSuccess)
         e = cudaMalloc(&plan->tw, (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess)
@@ -476,7 +490,8 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (e == cudaSuccess)
-        e = launch_filter(plan, static_cast<const float2*>(ref), s);
+        e = launch(log2n, true, 1, static_cast<const float2*>(ref), p->nref, plan->tw, nullptr,
+                   p->window, (float)p->band_fraction, plan->h, s);
     if (e != cudaSuccess) {
         cudaFree(plan->tw);
         cudaFree(plan->h);
@@ -500,8 +515,9 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
         return SARBP_ERR_INVALID_ARG;
-    return launch_rc(plan, static_cast<const float2*>(raw), static_cast<float2*>(out),
-                     static_cast<cudaStream_t>(stream)) == cudaSuccess
+    return launch(plan->log2n, false, p.na, static_cast<const float2*>(raw), p.ns, plan->tw, plan->h,
+                  p.window, 0.0f, static_cast<float2*>(out), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
                ? SARBP_OK
                : SARBP_ERR_CUDA;
 }
