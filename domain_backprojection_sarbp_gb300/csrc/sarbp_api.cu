@@ -179,6 +179,11 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     k.qmax3 = tile_qmax3(p->dx, p->dy, plan->h_max - plan->h_min);
     k.h_lo_f = (float)plan->h_min;
     k.h_hi_f = (float)plan->h_max;
+    k.dy_lo = (float)(p->dy - (double)k.dy_f);
+    k.r0_hi = (float)p->r0;
+    k.r0_lo = (float)(p->r0 - (double)k.r0_hi);
+    k.idr_hi = (float)(1.0 / p->dr);
+    k.idr_lo = (float)(1.0 / p->dr - (double)k.idr_hi);
     return k;
 }
 

@@ -48,7 +48,7 @@ constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/rou
 constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 
 enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3 };
-constexpr int HROW = TILE_X + 1;           // shared-memory row stride of a tile's heights
+constexpr int HROW2 = TILE_X / 2 + 1;      // float2 pairs per row of a tile's heights (padded)
 
 struct __align__(16) Record {
     float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
@@ -228,6 +228,18 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             rec.b = make_float4(f32(c03), f32(c04), f32(c10), f32(c11));
             rec.c = make_float4(f32(c12), f32(c13), f32(c20), f32(c21));
             rec.d = make_float4(f32(c22), __int_as_float(-lo), __int_as_float((int)kb), 0.f);
+            if (k.heights_mode) {
+                // height map: the antenna-to-tile-centre vector as float pairs,
+                // with its z part taken from z0 (each row adds its own height)
+                const double vz0 = k.z0 - az;
+                const float vxh = f32(vx), vyh = f32(vy), vzh = f32(vz0);
+                rec.a = make_float4(vxh, f32(vx - (double)vxh), vyh, f32(vy - (double)vyh));
+                rec.b = make_float4(vzh, f32(vz0 - (double)vzh), 0.f, 0.f);
+                rec.c = make_float4(0.f, 0.f, 0.f, 0.f);
+                rec.d.x = 0.f;
+                rec.d.z = 0.f;
+                kind = REC_EXACT;
+            }
         }
     }
     rec.d.w = __int_as_float(kind);
@@ -262,6 +274,11 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
                                                   const float4* row, float jf, float jf2,
                                                   float jf3, float jf4)
 {
+    if (INTERP == INTERP_HEIGHTS) {
+        PulseState st;
+        st.mode = __float_as_int(rec.d.w) == REC_SKIP ? MODE_SKIP : MODE_EXACT;
+        return st;
+    }
     // u(i) = E0 + i E1 + i^2 E2 for this thread's row j; the large c01 j term
     // is split into an integer (folded into the row index) and a fraction
     const float4 ra = rec.a, rb = rec.b, rc = rec.c, rd = rec.d;
@@ -291,11 +308,8 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const bool hinge = INTERP == INTERP_LINEAR && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
                        idx0 + 1 <= bin0 + k.nr - 2;
     PulseState st;
-    if (INTERP == INTERP_HEIGHTS)
-        st.mode = kind == REC_SKIP ? MODE_SKIP : MODE_EXACT;
-    else
-        st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
-                                   : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
+    st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
+                               : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
     st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
     if (hinge) {
@@ -646,16 +660,158 @@ __device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Reco
 }
 
 // ---------------------------------------------------------------------------
-// Pixels on a height map: float64 range to the centre of the thread's row at
-// the row's mean height z_row, then R - R_row = s / (R_row + R) with
-// s = 2 v.q + |q|^2, q = (qx, 0, h - h_row), in float32, bounds on every index.
+// Pixels on a height map.
+//
+// Each thread's row has a reference point: the tile-centre column of its row
+// at the row's mean height h_row. Its range R_row is found in float-pair
+// arithmetic (about 44 bits: error-free sums and products, Knuth and
+// Dekker), so u_row = (R_row - r0) / dr is exact to ~1e-9 bins. A pixel is
+// offset from it by q = (q_x, 0, h - h_row); with s = 2 v.q + |q|^2 and
+// t = s / R_row^2,
+//   R - R_row = (s / (2 R_row)) (1 - t/4 + t^2/8 - 5 t^3/64 + ...),
+// which is used when |t| <= 0.01 for every pixel of the row (the next term
+// is then below 6e-10 of the offset). Otherwise the row falls back to the
+// float64 reference and an exact float32 difference per pixel.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void heights_pulse(const BpConst& k, const Record& rec, const float4* row,
-                                              const double* __restrict__ a, double xc, double yrow,
-                                              double zrow, float hrow, const float* s_h,
-                                              float2 (&accre)[NP], float2 (&accim)[NP])
+struct HRow {
+    float hrow;    // the row's reference height (mean of its pixels)
+    float qm;      // largest |q| over the row's pixels
+    float jy;      // row offset from the tile centre, in pixels
+    double zrow;   // z0 + hrow
+};
+
+struct F2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ F2 two_sum(float a, float b)
 {
-    const double vx = xc - a[0], vy = yrow - a[1], vz = zrow - a[2];
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+__device__ __forceinline__ F2 fast_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ F2 two_prod(float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    return {p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b)
+{
+    F2 s = two_sum(a.hi, b.hi);
+    const F2 t = two_sum(a.lo, b.lo);
+    s.lo = __fadd_rn(s.lo, t.hi);
+    s = fast_two_sum(s.hi, s.lo);
+    s.lo = __fadd_rn(s.lo, t.lo);
+    return fast_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b)
+{
+    F2 p = two_prod(a.hi, b.hi);
+    p.lo = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, p.lo));
+    return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ F2 f2_sqr(F2 a)
+{
+    F2 p = two_prod(a.hi, a.hi);
+    p.lo = fmaf(2.0f * a.hi, a.lo, p.lo);
+    return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ F2 f2_sqrt(F2 a)
+{
+    const float x = __fsqrt_rn(a.hi);
+    const F2 p = two_prod(x, x);
+    const float d = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo);
+    return fast_two_sum(x, __fmul_rn(d, __fdiv_rn(0.5f, x)));
+}
+
+// Returns false (and leaves the sums untouched) when the series does not apply.
+__device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Record& rec,
+                                                     const float4* row, const HRow& hr,
+                                                     const float2* s_h2,
+                                                     float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    // reference vector: tile centre -> row centre -> row height
+    const F2 vx = {rec.a.x, rec.a.y};
+    const F2 yo = f2_add(two_prod(hr.jy, k.dy_f), two_prod(hr.jy, k.dy_lo));
+    const F2 vy = f2_add({rec.a.z, rec.a.w}, yo);
+    const F2 vz = f2_add({rec.b.x, rec.b.y}, {hr.hrow, 0.0f});
+    const F2 r2 = f2_add(f2_add(f2_sqr(vx), f2_sqr(vy)), f2_sqr(vz));
+    const F2 r = f2_sqrt(r2);
+    const F2 u = f2_mul(f2_add(r, {-k.r0_hi, -k.r0_lo}), {k.idr_hi, k.idr_lo});
+    if (!(fabsf(u.hi) < 1.0e7f))
+        return true;                              // far outside any window: nothing to add
+    float ku = floorf(u.hi);
+    float frac = __fadd_rn(__fsub_rn(u.hi, ku), u.lo);
+    const float kf = floorf(frac);                // -1, 0 or 1 after the lo part
+    ku += kf;
+    frac -= kf;
+    const float R = r.hi;
+    const float t_bound = hr.qm * (2.0f * R + hr.qm) / (R * R);
+    if (!(t_bound <= 0.01f))
+        return false;
+    const int kbase = (int)ku + __float_as_int(rec.d.y);
+    const float inv_r = __fdiv_rn(1.0f, R);
+    const float g = inv_r * inv_r;                // 1 / R^2
+    const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
+
+    const float2 two_vx = make_float2(2.0f * vx.hi, 2.0f * vx.hi);
+    const float2 two_vz = make_float2(2.0f * vz.hi, 2.0f * vz.hi);
+    const float2 hrw = make_float2(-hr.hrow, -hr.hrow);
+    const float2 g2 = make_float2(g, g), hb2 = make_float2(hb, hb);
+    const float2 c3 = make_float2(-5.0f / 64.0f, -5.0f / 64.0f);
+    const float2 c2 = make_float2(0.125f, 0.125f), c1 = make_float2(-0.25f, -0.25f);
+    const float2 one = make_float2(1.0f, 1.0f), neg1 = make_float2(-1.0f, -1.0f);
+    const float2 f0 = make_float2(frac, frac);
+    const float2 mm = make_float2(MAGIC, MAGIC), nmm = make_float2(-MAGIC, -MAGIC);
+    const float2 cc = make_float2(k.c_phase, k.c_phase);
+    const float2 dx2 = make_float2(k.dx_f, k.dx_f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+    const int wmax = k.W - 1;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float2 qx = __fmul2_rn(id, dx2);
+        id = __fadd2_rn(id, one);
+        const float2 dz = __fadd2_rn(s_h2[q], hrw);
+        const float2 s = __ffma2_rn(dz, __fadd2_rn(dz, two_vz), __fmul2_rn(qx, __fadd2_rn(qx, two_vx)));
+        const float2 t = __fmul2_rn(s, g2);
+        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(t, c3, c2), t, c1), t, one);
+        const float2 ub = __ffma2_rn(__fmul2_rn(s, hb2), poly, f0);
+        const float2 tt = __fadd2_rd(ub, mm);
+        const float2 f = __ffma2_rn(__fadd2_rn(tt, nmm), neg1, ub);
+        const float2 x = __fmul2_rn(f, cc);
+        const int ka = min(max(kbase + (__float_as_int(tt.x) - MAGIC_BITS), 0), wmax);
+        const int kb = min(max(kbase + (__float_as_int(tt.y) - MAGIC_BITS), 0), wmax);
+        const float4 va = __ldg(row + ka);
+        const float4 vb = __ldg(row + kb);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 wr = make_float2(fmaf(x.x, va.z, va.x), fmaf(x.y, vb.z, vb.x));
+        const float2 wi = make_float2(fmaf(x.x, va.w, va.y), fmaf(x.y, vb.w, vb.y));
+        const float2 c = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, c, accre[q]);
+        accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, c, accim[q]));
+        accre[q] = __ffma2_rn(__fmul2_rn(wi, sn), neg1, accre[q]);
+    }
+    return true;
+}
+
+// The fallback: float64 range to the row's reference point, then
+// R - R_row = s / (R_row + R) in float32, bounds on every table index.
+__device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Record& rec,
+                                                    const float4* row, const double* __restrict__ a,
+                                                    double xc, double yrow, const HRow& hr,
+                                                    const float2* s_h2, float2 (&accre)[NP],
+                                                    float2 (&accim)[NP])
+{
+    const double vx = xc - a[0], vy = yrow - a[1], vz = hr.zrow - a[2];
     const double r2 = vx * vx + vy * vy + vz * vz;
     const double r = sqrt(r2);
     const double u = (r - k.r0) * k.inv_dr;
@@ -670,7 +826,8 @@ __device__ __forceinline__ void heights_pulse(const BpConst& k, const Record& re
 #pragma unroll
     for (int m = 0; m < TILE_X; ++m) {
         const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
-        const float dz = s_h[m] - hrow;
+        const float hm = (m < NP) ? s_h2[m % NP].x : s_h2[m % NP].y;
+        const float dz = hm - hr.hrow;
         const float s = fmaf(qx, two_vx + qx, dz * (two_vz + dz));
         const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
         const float den = rf + rp;
@@ -698,13 +855,13 @@ __device__ __forceinline__ void heights_pulse(const BpConst& k, const Record& re
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, double zrow, float hrow, const float* s_h,
+                                            double yrow, const HRow& hr, const float2* s_h2,
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
     if (INTERP == INTERP_HEIGHTS) {
-        if (st.mode == MODE_EXACT)
-            heights_pulse(k, rec, row, a, xc, yrow, zrow, hrow, s_h, accre, accim);
+        if (st.mode == MODE_EXACT && !heights_series_pulse(k, rec, row, hr, s_h2, accre, accim))
+            heights_exact_pulse(k, rec, row, a, xc, yrow, hr, s_h2, accre, accim);
         return;
     }
     if (INTERP == INTERP_NEAREST) {
@@ -747,7 +904,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                                                         const float* __restrict__ heights)
 {
     __shared__ Record s_rec[CHUNK];
-    extern __shared__ float s_heights[];            // heights mode: TILE_Y x HROW
+    extern __shared__ float2 s_heights[];           // heights mode: TILE_Y x HROW2 pairs (h[q], h[q + 16])
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
     const float jf = (float)jr - 0.5f * (TILE_Y - 1);
@@ -771,23 +928,31 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
 
         const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
-        float hrow = 0.0f;
-        double zrow = k.z0;
+        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0};
         if (INTERP == INTERP_HEIGHTS) {
             // the thread's own row of the tile, heights clamped to the plan's
             // bounds; pixels outside the image repeat the last row or column
             // (their results are never stored)
             const int rowi_h = min(row0 + jr, k.ny - 1);
+            const float* hsrc = heights + (size_t)rowi_h * k.nx;
             float sum = 0.0f;
 #pragma unroll 4
-            for (int m = 0; m < TILE_X; ++m) {
-                const int col = min(col0 + m, k.nx - 1);
-                const float hv = fminf(fmaxf(heights[(size_t)rowi_h * k.nx + col], k.h_lo_f), k.h_hi_f);
-                s_heights[jr * HROW + m] = hv;
-                sum += hv;
+            for (int q = 0; q < NP; ++q) {
+                const float a = fminf(fmaxf(hsrc[min(col0 + q, k.nx - 1)], k.h_lo_f), k.h_hi_f);
+                const float b = fminf(fmaxf(hsrc[min(col0 + q + NP, k.nx - 1)], k.h_lo_f), k.h_hi_f);
+                s_heights[jr * HROW2 + q] = make_float2(a, b);
+                sum += a + b;
             }
-            hrow = sum * (1.0f / TILE_X);
-            zrow = k.z0 + (double)hrow;
+            hr.hrow = sum * (1.0f / TILE_X);
+            float dzm = 0.0f;
+#pragma unroll 4
+            for (int q = 0; q < NP; ++q) {
+                const float2 h2 = s_heights[jr * HROW2 + q];
+                dzm = fmaxf(dzm, fmaxf(fabsf(h2.x - hr.hrow), fabsf(h2.y - hr.hrow)));
+            }
+            const float hx = 0.5f * (TILE_X - 1) * k.dx_f;
+            hr.qm = 1.0001f * sqrtf(hx * hx + dzm * dzm);
+            hr.zrow = k.z0 + (double)hr.hrow;
         }
         float2 accre[NP], accim[NP];
 #pragma unroll
@@ -812,15 +977,15 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 const PulseState sb =
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
-                                  pos + 3 * (size_t)(c0 + p), xc, yrow, zrow, hrow,
-                                  s_heights + jr * HROW, psi, accre, accim);
+                                  pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
+                                  s_heights + jr * HROW2, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
-                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, zrow, hrow,
-                                  s_heights + jr * HROW, psi, accre, accim);
+                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
+                                  s_heights + jr * HROW2, psi, accre, accim);
             }
         }
 
@@ -983,7 +1148,7 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
     return cudaGetLastError();
 }
 
-constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW * sizeof(float);
+constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW2 * sizeof(float2);
 
 cudaError_t prepare_heights_kernel()
 {

@@ -67,7 +67,7 @@ def test_terrain_several_tiles(relief):
     h_range = (float(h.min()), float(h.max()))
     got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, h_range)
     ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
-    parity.assert_parity(got, ref, f"terrain relief {relief}")
+    print(parity.assert_parity(got, ref, f"terrain relief {relief}"))
     assert not parity.argmax_mismatches(got, ref, sc.targets)
 
 
@@ -102,7 +102,25 @@ def test_wide_height_range():
     sc = scenes.make_scene(cfg, heights=h)
     got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (-110.0, 410.0))
     ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
-    parity.assert_parity(got, ref, "wide height range")
+    print(parity.assert_parity(got, ref, "wide height range"))
+
+
+def test_near_field_uses_the_exact_rows():
+    """Antenna 40-60 m from the pixels: the range series does not apply
+    (|t| > 0.01) and every row takes the float64 reference with an exact
+    float32 difference per pixel."""
+    na, nx, ny = 48, 70, 530
+    pos = np.zeros((na, 3))
+    pos[:, 0] = np.linspace(-20, 20, na)
+    pos[:, 1] = -30.0
+    pos[:, 2] = 40.0
+    geo = scenes.image_geometry(nx, ny, 0.1)
+    p = dict(nx=nx, ny=ny, na=na, nr=512, r0=10.0, dr=0.25, wavelength=scenes.WAVELENGTH, **geo)
+    echo = (np.random.default_rng(8).standard_normal((na, 512)) * (1 + 1j)).astype(np.complex64)
+    h = scenes.terrain(nx, ny, 0.1, 99, relief=3.0, mean=1.0)
+    got = heights_image(p, echo, pos, h, (float(h.min()), float(h.max())))
+    ref = oracle.backproject_heights(p, echo, pos, h)
+    print(parity.assert_parity(got, ref, "near field on terrain"))
 
 
 def test_heights_are_clamped_to_the_plan_range():
@@ -152,7 +170,7 @@ def test_page_spotlight_on_terrain_sampled():
     got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (float(h.min()), float(h.max())))
     pix = scenes.compared_pixels(sc)
     ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h, pixels=pix)
-    parity.assert_parity(got.reshape(-1)[pix], ref, "page_spotlight on terrain")
+    print(parity.assert_parity(got.reshape(-1)[pix], ref, "page_spotlight on terrain"))
     full = np.zeros(cfg.nx * cfg.ny, dtype=np.complex128)
     full[pix] = ref
     assert not parity.argmax_mismatches(got, full.reshape(cfg.ny, cfg.nx), sc.targets)
