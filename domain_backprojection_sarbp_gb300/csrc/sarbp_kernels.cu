@@ -48,6 +48,7 @@ constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/rou
 constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 
 enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3 };
+constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr int HROW2 = TILE_X / 2 + 1;      // float2 pairs per row of a tile's heights (padded)
 
 struct __align__(16) Record {
@@ -257,7 +258,7 @@ constexpr int NP = TILE_X / 2;
 
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the two table loads; their values are consumed by the next pulse step.
-enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3 };
+enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; gather: e0, e1, e2 (both halves)
@@ -310,7 +311,18 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
-    st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (INTERP == INTERP_SINC8 && kind == REC_FAST) {
+        // windowed sinc: when the thread's pixels span at most a quarter bin and
+        // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
+        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN)
+        const int kabs0 = idx0 - bin0;
+        if (hi_u - lo_u <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1) {
+            st.mode = MODE_POLY;
+            st.t0 = make_float4(lo_u, hi_u, k0, __int_as_float(kabs0));
+        }
+    }
+    if (st.mode != MODE_POLY)
+        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
     if (hinge) {
         st.t0 = __ldg(row + idx0);
@@ -537,6 +549,123 @@ __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, i
     const float zi = ps.x * sn + ps.y * cs;
     re = fmaf(sre, zr, fmaf(-sim, zi, re));
     im = fmaf(sre, zi, fmaf(sim, zr, im));
+}
+
+// Windowed-sinc interpolant G(u) = sum_m e_m h(u - m) at one position ub
+// (row units, relative to kb), no phase. The whole stencil must lie inside
+// the row and the recorded range.
+__device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row)
+{
+    const float tt = __fadd_rd(ub, MAGIC);
+    const float f = ub - (tt - MAGIC);
+    const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
+    const float4* p = row + (kr - 3);
+    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
+    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
+    const float x0 = fc + 3.0f, x1 = fc + 2.0f, x2 = fc + 1.0f, x3 = fc;
+    const float x4 = fc - 1.0f, x5 = fc - 2.0f, x6 = fc - 3.0f, x7 = fc - 4.0f;
+    const float a1 = x0 * x1, a2 = a1 * x2, a3 = a2 * x3, a4 = a3 * x4, a5 = a4 * x5,
+                a6 = a5 * x6, a7 = a6 * x7;
+    float r = __fdividef(1.0f, a7);
+    const float i7 = r * a6; r *= x7;
+    const float i6 = r * a5; r *= x6;
+    const float i5 = r * a4; r *= x5;
+    const float i4 = r * a3; r *= x4;
+    const float i3 = r * a2; r *= x3;
+    const float i2 = r * a1; r *= x2;
+    const float i1 = r * x0;
+    const float i0 = r * x1;
+    const float sf = sinpif(fc) * 0.318309886f;
+    float s4, c4;
+    __sincosf(0.785398163f * fc, &s4, &c4);
+    constexpr float H = 0.353553391f;
+    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));
+    const float w1 = fmaf(-s4, 0.5f, 0.5f);
+    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));
+    const float w3 = fmaf(c4, 0.5f, 0.5f);
+    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));
+    const float w5 = fmaf(s4, 0.5f, 0.5f);
+    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));
+    const float w7 = fmaf(c4, -0.5f, 0.5f);
+    const float h0 = -sf * i0 * w0, h1 = sf * i1 * w1, h2 = -sf * i2 * w2, h3 = sf * i3 * w3;
+    const float h4 = -sf * i4 * w4, h5 = sf * i5 * w5, h6 = -sf * i6 * w6, h7 = sf * i7 * w7;
+    float sre = h0 * s0.x, sim = h0 * s0.y;
+    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
+    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
+    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
+    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
+    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
+    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
+    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
+    return make_float2(sre, sim);
+}
+
+// All of the thread's pixels within SINC_SPAN bins, every stencil inside the
+// recorded range. G(u) is smooth (a sum of eight windowed sincs), so over the
+// interval [lo_u, hi_u] it is interpolated at the five Chebyshev nodes
+// mid + half cos((2i+1) pi / 10) by a degree-4 polynomial in
+// t = (u - mid) / half. The interpolation error is at most
+// max|G^(5)| (half)^5 / (2^4 5!) <= pi^5 |e| 8 (1/8)^5 / 1920 ~ 4e-5 |e| for
+// half <= 1/8. The echo phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0))
+// is applied per pixel; psi_k0 is folded into the coefficients.
+__device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseState& st,
+                                                const float4* row, const float2* __restrict__ psi,
+                                                float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float lo_u = st.t0.x, hi_u = st.t0.y, k0 = st.t0.z;
+    const int kabs0 = __float_as_int(st.t0.w);
+    const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
+    constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
+    const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
+    const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
+    const float2 g2 = sinc_value(mid, st.kb, row);
+    const float2 g3 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
+    const float2 g4 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
+    // monomial coefficients of the interpolant (inverse Vandermonde of the nodes)
+    const float2 s04 = make_float2(g0.x + g4.x, g0.y + g4.y), d04 = make_float2(g0.x - g4.x, g0.y - g4.y);
+    const float2 s13 = make_float2(g1.x + g3.x, g1.y + g3.y), d13 = make_float2(g1.x - g3.x, g1.y - g3.y);
+    float2 p[5];
+    p[0] = g2;
+    p[1] = make_float2(fmaf(1.376381920f, d13.x, -0.324919696f * d04.x),
+                       fmaf(1.376381920f, d13.y, -0.324919696f * d04.y));
+    p[2] = make_float2(fmaf(-0.341640786f, s04.x, fmaf(2.341640786f, s13.x, -4.0f * g2.x)),
+                       fmaf(-0.341640786f, s04.y, fmaf(2.341640786f, s13.y, -4.0f * g2.y)));
+    p[3] = make_float2(fmaf(0.940456404f, d04.x, -1.521690426f * d13.x),
+                       fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
+    p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
+                       fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
+    const float2 ps = __ldg(psi + kabs0);
+    float2 pr[5], pi[5];
+#pragma unroll
+    for (int n = 0; n < 5; ++n) {
+        const float re = p[n].x * ps.x - p[n].y * ps.y;
+        const float im = p[n].x * ps.y + p[n].y * ps.x;
+        pr[n] = make_float2(re, re);
+        pi[n] = make_float2(im, im);
+    }
+    const float ih = half > 1.0e-7f ? 1.0f / half : 0.0f;
+    const float2 ih2 = make_float2(ih, ih), nm2 = make_float2(-mid * ih, -mid * ih);
+    const float c = k.c_phase;
+    const float2 c2 = make_float2(c, c), nk0c = make_float2(-k0 * c, -k0 * c);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float2 u = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        id = __fadd2_rn(id, one);
+        const float2 t = __ffma2_rn(u, ih2, nm2);
+        const float2 gr = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pr[4], t, pr[3]), t, pr[2]), t, pr[1]), t, pr[0]);
+        const float2 gi = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pi[4], t, pi[3]), t, pi[2]), t, pi[1]), t, pi[0]);
+        const float2 x = __ffma2_rn(u, c2, nk0c);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(gr, cs, accre[q]);
+        accim[q] = __ffma2_rn(gr, sn, __ffma2_rn(gi, cs, accim[q]));
+        accre[q] = __ffma2_rn(make_float2(-gi.x, -gi.y), sn, accre[q]);
+    }
 }
 
 __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& st, const float4* row,
@@ -872,7 +1001,9 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
         return;
     }
     if (INTERP == INTERP_SINC8) {
-        if (st.mode == MODE_GATHER)
+        if (st.mode == MODE_POLY)
+            sinc_poly_pulse(k, st, row, psi, accre, accim);
+        else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
             sinc_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
