@@ -258,7 +258,8 @@ constexpr int NP = TILE_X / 2;
 
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the two table loads; their values are consumed by the next pulse step.
-enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4 };
+enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
+                       MODE_PAIR = 5 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; gather: e0, e1, e2 (both halves)
@@ -324,6 +325,19 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     if (st.mode != MODE_POLY)
         st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
+    if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
+        // nearest sample: when every pixel rounds to bin kn or kn + 1, one table
+        // entry (e_kn, e_kn+1) serves the thread; psi_kn must exist
+        const float tkn = __fadd_rd(lo_u + 0.5f, MAGIC);
+        const float kn = tkn - MAGIC;
+        const int idxn = kb + (__float_as_int(tkn) - MAGIC_BITS);
+        const int kabsn = idxn - bin0;
+        if (hi_u + 0.5f - kn < 2.0f && kabsn >= 0 && kabsn <= k.nr - 1) {
+            st.mode = MODE_PAIR;
+            st.t0 = __ldg(row + idxn);
+            st.t1d = make_float2(kn, __int_as_float(kabsn));
+        }
+    }
     if (hinge) {
         st.t0 = __ldg(row + idx0);
         const float4 t1 = __ldg(row + idx0 + 1);
@@ -742,6 +756,44 @@ __device__ __forceinline__ void nearest_pixel(const BpConst& k, float ub, int kb
     im = fmaf(e.x, zi, fmaf(e.y, zr, im));
 }
 
+// Every pixel rounds to bin kn or kn + 1: the two samples come from one
+// table entry, pre-multiplied by psi_kn, since the echo phase
+// psi_k exp(j c (u - k)) equals psi_kn exp(j c (u - kn)) for either k. Per
+// pixel: the choice of sample (u + 1/2 >= kn + 1), the phase, the sum.
+__device__ __forceinline__ void nearest_pair_pulse(const BpConst& k, const PulseState& st,
+                                                   const float2* __restrict__ psi,
+                                                   float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float kn = st.t1d.x;
+    const float2 ps = __ldg(psi + __float_as_int(st.t1d.y));
+    const float4 e = st.t0;
+    const float w0r = e.x * ps.x - e.y * ps.y, w0i = e.x * ps.y + e.y * ps.x;
+    const float w1r = e.z * ps.x - e.w * ps.y, w1i = e.z * ps.y + e.w * ps.x;
+    const float up = kn + 1.0f;
+    const float c = k.c_phase;
+    const float2 c2 = make_float2(c, c), nknc = make_float2(-kn * c, -kn * c);
+    const float2 one = make_float2(1.0f, 1.0f), hf = make_float2(0.5f, 0.5f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float2 u = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        id = __fadd2_rn(id, one);
+        const float2 v = __fadd2_rn(u, hf);
+        const bool ba = v.x >= up, bb = v.y >= up;
+        const float2 wr = make_float2(ba ? w1r : w0r, bb ? w1r : w0r);
+        const float2 wi = make_float2(ba ? w1i : w0i, bb ? w1i : w0i);
+        const float2 x = __ffma2_rn(u, c2, nknc);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, cs, accre[q]);
+        accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, cs, accim[q]));
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), sn, accre[q]);
+    }
+}
+
 __device__ __forceinline__ void nearest_pulse(const BpConst& k, const PulseState& st, const float4* row,
                                               const float2* __restrict__ psi,
                                               float2 (&accre)[NP], float2 (&accim)[NP])
@@ -994,7 +1046,9 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
         return;
     }
     if (INTERP == INTERP_NEAREST) {
-        if (st.mode == MODE_GATHER)
+        if (st.mode == MODE_PAIR)
+            nearest_pair_pulse(k, st, psi, accre, accim);
+        else if (st.mode == MODE_GATHER)
             nearest_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
             nearest_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
