@@ -383,6 +383,11 @@ def run_ours(args, scene, rank, world, local, dist):
     peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / MUFU_PER_UPDATE / 1e9
     page_peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / PAGE_SFU_PER_UPDATE / 1e9
     achieved = updates / (main_ms / max(launches, 1) / 1e3) / 1e9 if launches else None
+    # every interpolation variant issues one sine and one cosine per update on its
+    # common path, so it shares the main kernel's MUFU roof
+    for var in variants.values():
+        if "main_kernel_gupd" in var:
+            var["mufu_roof_frac"] = var["main_kernel_gupd"] / peak
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
