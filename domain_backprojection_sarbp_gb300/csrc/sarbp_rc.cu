@@ -114,30 +114,31 @@ __device__ __forceinline__ void dft(float2* v)
     }
 }
 
-// v[t] *= w^t, w = tw[k * stride] (conjugated for the inverse), t = 1 .. R-1.
-// Powers from at most four table entries, each product at most three
-// roundings deep.
-template <int R, int S>
-__device__ __forceinline__ void twiddle_inputs(float2* v, int k, int stride,
-                                               const float2* __restrict__ tw)
+// v[t] *= w^t for t = 1 .. R-1, where w is the input twiddle of span NS at
+// position k. The table region of span NS (tw + 4 (NS - 1)) holds, for
+// t in {1, 4, 8, 12}, the four rows w^t over k = 0 .. NS-1 (forward sign;
+// conjugated for the inverse), so the 32 lanes of a warp read consecutive
+// entries. The other powers are products at most three roundings deep.
+template <int R, int S, int NS>
+__device__ __forceinline__ void twiddle_inputs(float2* v, int k, const float2* __restrict__ tw)
 {
     const bool c = S > 0;
-    const int m = k * stride;
-    const float2 w1 = conj_if(__ldg(tw + m), c);
+    const float2* t = tw + 4 * (NS - 1) + k;
+    const float2 w1 = conj_if(__ldg(t), c);
     v[1] = cmul(v[1], w1);
     if (R >= 4) {
         const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1);
         v[2] = cmul(v[2], w2);
         v[3] = cmul(v[3], w3);
         if (R >= 8) {
-            const float2 w4 = conj_if(__ldg(tw + 4 * m), c);
+            const float2 w4 = conj_if(__ldg(t + NS), c);
             v[4] = cmul(v[4], w4);
             v[5] = cmul(v[5], cmul(w4, w1));
             v[6] = cmul(v[6], cmul(w4, w2));
             v[7] = cmul(v[7], cmul(w4, w3));
             if (R == 16) {
-                const float2 w8 = conj_if(__ldg(tw + 8 * m), c);
-                const float2 w12 = conj_if(__ldg(tw + 12 * m), c);
+                const float2 w8 = conj_if(__ldg(t + 2 * NS), c);
+                const float2 w12 = conj_if(__ldg(t + 3 * NS), c);
                 v[8] = cmul(v[8], w8);
                 v[9] = cmul(v[9], cmul(w8, w1));
                 v[10] = cmul(v[10], cmul(w8, w2));
@@ -193,7 +194,7 @@ __device__ __forceinline__ void pass_load(const Row& r, float2* v, int j,
     for (int t = 0; t < R; ++t)
         v[t] = r.ld(pb + pad(t * STRIDE));
     if (NS > 1)
-        twiddle_inputs<R, S>(v, j & (NS - 1), N / (NS * R), tw);
+        twiddle_inputs<R, S, NS>(v, j & (NS - 1), tw);
     dft<R, S>(v);
 }
 
@@ -429,7 +430,7 @@ struct sarbp_rc_plan_s {
     sarbp_rc_params p{};
     int n = 0, log2n = 0;
     int device = -1;
-    float2* tw = nullptr;      // N twiddles exp(-2 pi i m / N)
+    float2* tw = nullptr;      // per-span twiddle rows, 4 N entries
     float2* h = nullptr;       // N filter coefficients / N, natural order
 };
 
@@ -474,17 +475,26 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     }
     if (e == cudaSuccess)
         e = set_smem(log2n);
+    // per-span twiddle rows: span ns (a power of two) at offset 4 (ns - 1),
+    // rows t = 1, 4, 8, 12 of exp(-2 pi i t k / (ns r)), r = min(16, N / ns),
+    // computed in float64 and rounded once
+    const size_t tw_entries = 4 * (size_t)plan->n;
     if (e == cudaSuccess)
-        e = cudaMalloc(&plan->tw, (size_t)plan->n * sizeof(float2));
+        e = cudaMalloc(&plan->tw, tw_entries * sizeof(float2));
     if (e == cudaSuccess)
         e = cudaMalloc(&plan->h, (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess) {
-        // twiddles in float64, rounded once
-        std::vector<float2> tw((size_t)plan->n);
+        std::vector<float2> tw(tw_entries, make_float2(0.f, 0.f));
         const double pi = 3.14159265358979323846;
-        for (int m = 0; m < plan->n; ++m) {
-            const double a = -2.0 * pi * (double)m / (double)plan->n;
-            tw[m] = make_float2((float)std::cos(a), (float)std::sin(a));
+        const int powers[4] = {1, 4, 8, 12};
+        for (int ns = 1; ns < plan->n; ns *= 2) {
+            const int r = plan->n / ns < 16 ? plan->n / ns : 16;
+            for (int row = 0; row < 4; ++row)
+                for (int k = 0; k < ns; ++k) {
+                    const double a = -2.0 * pi * (double)powers[row] * (double)k / ((double)ns * r);
+                    tw[4 * (size_t)(ns - 1) + (size_t)row * ns + k] =
+                        make_float2((float)std::cos(a), (float)std::sin(a));
+                }
         }
         e = cudaMemcpy(plan->tw, tw.data(), tw.size() * sizeof(float2), cudaMemcpyHostToDevice);
     }
