@@ -163,7 +163,6 @@ struct Fft {
     static constexpr int PASSES = L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4;
     static constexpr int T = N / 16 > 32 ? N / 16 : 32;
     static constexpr int PLANE = pad(N - 1) + 1;       // words per padded plane
-    static constexpr int Q = N / 16 > 0 ? N / 16 : 1;  // radix-16 butterflies
 };
 
 // Shared row: real plane then imaginary plane. Every access pattern used
@@ -217,7 +216,7 @@ struct Middle {
                                                const float2* __restrict__ tw)
     {
         if constexpr (P < P1) {
-            const bool act = tid < Fft<L>::Q;
+            const bool act = tid < (Fft<L>::N / 16);
             if (act)
                 pass_load<16, S, Fft<L>::N, NS>(r, v, tid, tw);
             __syncthreads();
@@ -261,7 +260,7 @@ __device__ __forceinline__ void forward_to_registers(const float2* __restrict__ 
         __syncthreads();
         Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid, tw);
         constexpr int NSL = F::N / 16;                 // span of the last pass
-        if (tid < F::Q)
+        if (tid < (F::N / 16))
             pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
         __syncthreads();
     }
@@ -329,7 +328,7 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
         }
     } else {
         // filter, then the inverse's first pass (radix 16, span 1) on the held values
-        constexpr int Q = F::Q;
+        constexpr int Q = (F::N / 16);
         if (tid < Q) {
 #pragma unroll
             for (int t = 0; t < 16; ++t)
