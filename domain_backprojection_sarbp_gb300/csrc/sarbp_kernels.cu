@@ -189,46 +189,53 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             //   order 4:  (-|q|^4/8 + 3 (g.q)^2 |q|^2 / 4 - 5 (g.q)^4 / 8) / R^3
             // Order-4 terms with j^2 or more are kept (they fold into the
             // per-thread coefficients for free); the others are bounded below.
-            const double ir = 1.0 / r;
-            const double ir3 = ir * ir * ir;
-            const double gx = vx * ir, gy = vy * ir;
-            const double mxx = 1.0 - gx * gx, mxy = -gx * gy, myy = 1.0 - gy * gy;
-            const double dx = k.dx, dy = k.dy, idr = k.inv_dr;
-            const double h2 = 0.5 * ir, h3 = -0.5 * ir * ir;
-            const double c10 = gx * dx * idr;
-            const double c01 = gy * dy * idr;
-            const double c20 = mxx * h2 * dx * dx * idr;
-            const double c11 = 2.0 * mxy * h2 * dx * dy * idr;
-            const double c02 = myy * h2 * dy * dy * idr;
-            const double c21 = h3 * (2.0 * gx * mxy + gy * mxx) * dx * dx * dy * idr;
-            const double c12 = h3 * (gx * myy + 2.0 * gy * mxy) * dx * dy * dy * idr;
-            const double c03 = h3 * gy * myy * dy * dy * dy * idr;
-            const double gx2 = gx * gx, gy2 = gy * gy;
-            const double k40 = -0.125 + 0.75 * gx2 - 0.625 * gx2 * gx2;
-            const double k31 = 1.5 * gx * gy - 2.5 * gx2 * gx * gy;
-            const double k22 = -0.25 + 0.75 * (gx2 + gy2) - 3.75 * gx2 * gy2;
-            const double k13 = 1.5 * gx * gy - 2.5 * gx * gy2 * gy;
-            const double k04 = -0.125 + 0.75 * gy2 - 0.625 * gy2 * gy2;
-            const double c22 = k22 * ir3 * dx * dx * dy * dy * idr;
-            const double c13 = k13 * ir3 * dx * dy * dy * dy * idr;
-            const double c04 = k04 * ir3 * dy * dy * dy * dy * idr;
+            // float64 only where float32 would not hold: the reciprocal range (one
+            // Newton step on a float seed), gy and c01 (c01 j reaches tens of
+            // bins and is split below), c10 (rounded once); every other
+            // coefficient multiplies offsets small enough for float32
+            double ir = (double)(1.0f / (float)r);
+            ir = ir * fma(-r, ir, 2.0);
+            const double gy = vy * ir;
+            const double c01 = gy * k.dy * k.inv_dr;
+            const float irf = (float)ir, gx = (float)(vx * ir), gyf = (float)gy;
+            const float mxx = 1.0f - gx * gx, mxy = -gx * gyf, myy = 1.0f - gyf * gyf;
+            const float dx = k.dx_f, dy = k.dy_f, idr = k.inv_dr_f;
+            const float ir3 = irf * irf * irf;
+            const float h2 = 0.5f * irf, h3 = -0.5f * irf * irf;
+            const float c10 = f32(vx * ir * k.dx * k.inv_dr);   // times i: keep one rounding
+            const float c20 = mxx * h2 * dx * dx * idr;
+            const float c11 = 2.0f * mxy * h2 * dx * dy * idr;
+            const float c02 = myy * h2 * dy * dy * idr;
+            const float c21 = h3 * (2.0f * gx * mxy + gyf * mxx) * dx * dx * dy * idr;
+            const float c12 = h3 * (gx * myy + 2.0f * gyf * mxy) * dx * dy * dy * idr;
+            const float c03 = h3 * gyf * myy * dy * dy * dy * idr;
+            const float gx2 = gx * gx, gy2 = gyf * gyf;
+            const float k40 = -0.125f + 0.75f * gx2 - 0.625f * gx2 * gx2;
+            const float k31 = 1.5f * gx * gyf - 2.5f * gx2 * gx * gyf;
+            const float k22 = -0.25f + 0.75f * (gx2 + gy2) - 3.75f * gx2 * gy2;
+            const float k13 = 1.5f * gx * gyf - 2.5f * gx * gy2 * gyf;
+            const float k04 = -0.125f + 0.75f * gy2 - 0.625f * gy2 * gy2;
+            const float c22 = k22 * ir3 * dx * dx * dy * dy * idr;
+            const float c13 = k13 * ir3 * dx * dy * dy * dy * idr;
+            const float c04 = k04 * ir3 * dy * dy * dy * dy * idr;
 
             // dropped: c30 i^3, c31 i^3 j, c40 i^4 (metres), plus the order-5
             // remainder, at most |q|^5 / R^4 while |q| <= R / 8
-            const double hx = 0.5 * (TILE_X - 1) * dx, hy = 0.5 * (TILE_Y - 1) * dy;
-            const double hx3 = hx * hx * hx;
-            const double q5 = k.qmax * k.qmax * k.qmax * k.qmax * k.qmax;
-            const double dropped = fabs(gx * mxx) * 0.5 * ir * ir * hx3
-                                 + (fabs(k31) * hx3 * hy + fabs(k40) * hx3 * hx) * ir3
-                                 + q5 * ir3 * ir;
-            const bool fast = in_row && r > 8.0 * k.qmax && dropped * idr <= k.fast_tol_bins;
+            const float hx = 0.5f * (TILE_X - 1) * dx, hy = 0.5f * (TILE_Y - 1) * dy;
+            const float hx3 = hx * hx * hx;
+            const float qm = (float)k.qmax;
+            const float q5 = qm * qm * qm * qm * qm;
+            const float dropped = fabsf(gx * mxx) * 0.5f * irf * irf * hx3
+                                + (fabsf(k31) * hx3 * hy + fabsf(k40) * hx3 * hx) * ir3
+                                + q5 * ir3 * irf;
+            const bool fast = in_row && r > 8.0 * k.qmax && dropped * idr <= (float)k.fast_tol_bins;
             kind = fast ? REC_FAST : REC_EXACT;
 
             const float c01h = f32(c01);
-            rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), f32(c02));
-            rec.b = make_float4(f32(c03), f32(c04), f32(c10), f32(c11));
-            rec.c = make_float4(f32(c12), f32(c13), f32(c20), f32(c21));
-            rec.d = make_float4(f32(c22), __int_as_float(-lo), __int_as_float((int)kb), 0.f);
+            rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), c02);
+            rec.b = make_float4(c03, c04, c10, c11);
+            rec.c = make_float4(c12, c13, c20, c21);
+            rec.d = make_float4(c22, __int_as_float(-lo), __int_as_float((int)kb), 0.f);
             if (k.heights_mode) {
                 // height map: the antenna-to-tile-centre vector as float pairs,
                 // with its z part taken from z0 (each row adds its own height)
