@@ -15,8 +15,8 @@
 // One CTA per pulse. The transforms are self-sorting (Stockham) passes of
 // radix 16 held in registers (16 complex values per thread), plus one pass of
 // radix 2, 4 or 8 when log2 N is not a multiple of 4; shared memory only
-// carries the data between passes, as separate real and imaginary planes
-// padded by one word every 32 (conflict-free for the strides used). The
+// carries the data between passes, as float2 values padded by one slot
+// every 16 (conflict-free for the strides used). The
 // forward transform takes the raw row straight from global memory (zero
 // beyond ns) and its last pass leaves each thread holding the spectrum at
 // indices j + t N/16, which are exactly the inputs of the inverse transform's
@@ -152,7 +152,7 @@ __device__ __forceinline__ void twiddle_inputs(float2* v, int k, const float2* _
     }
 }
 
-__host__ __device__ constexpr int pad(int i) { return i + (i >> 5); }
+__host__ __device__ constexpr int pad(int i) { return i + (i >> 4); }
 
 // Pass structure of an N = 2^L transform: a first pass of radix R0 (2, 4, 8
 // or 16, so that the rest are radix 16), PASSES passes in all, T threads.
@@ -162,22 +162,19 @@ struct Fft {
     static constexpr int R0 = L < 4 ? N : ((L % 4) ? (1 << (L % 4)) : 16);
     static constexpr int PASSES = L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4;
     static constexpr int T = N / 16 > 32 ? N / 16 : 32;
-    static constexpr int PLANE = pad(N - 1) + 1;       // words per padded plane
+    static constexpr int SLOTS = pad(N - 1) + 1;       // float2 slots of the padded row
 };
 
-// Shared row: real plane then imaginary plane. Every access pattern used
-// below is base + t S with (base mod 32) + (t S mod 32) < 32, for which
+// Shared row: complex values as float2, one spare slot after every 16 (a
+// warp's 8-byte accesses are served 16 lanes at a time; with this padding
+// the strides used hit 16 distinct bank pairs). Every access pattern below is
+// base + t S with (base mod 16) + (t S mod 16) < 16, for which
 // pad(base + t S) = pad(base) + pad(t S): one padded base per butterfly and
 // compile-time offsets.
 struct Row {
-    float* re;
-    float* im;
-    __device__ __forceinline__ float2 ld(int pi) const { return make_float2(re[pi], im[pi]); }
-    __device__ __forceinline__ void st(int pi, float2 v) const
-    {
-        re[pi] = v.x;
-        im[pi] = v.y;
-    }
+    float2* d;
+    __device__ __forceinline__ float2 ld(int pi) const { return d[pi]; }
+    __device__ __forceinline__ void st(int pi, float2 v) const { d[pi] = v; }
 };
 
 // Radix-R Stockham pass body from shared memory: inputs x[j + t N/R], twiddles
@@ -273,8 +270,8 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __re
                                                               float2* __restrict__ h)
 {
     using F = Fft<L>;
-    extern __shared__ float smem[];
-    const Row r{smem, smem + F::PLANE};
+    extern __shared__ float2 smem[];
+    const Row r{smem};
     float2 v[EPT];
     forward_to_registers<L>(ref, nref, tw, r, v);
     constexpr int RL = F::PASSES > 1 ? 16 : F::R0;
@@ -307,8 +304,8 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
 {
     using F = Fft<L>;
     constexpr int N = F::N, R0 = F::R0;
-    extern __shared__ float smem[];
-    const Row r{smem, smem + F::PLANE};
+    extern __shared__ float2 smem[];
+    const Row r{smem};
     const int tid = threadIdx.x;
     const size_t row0 = (size_t)blockIdx.x * ns_in;
     float2 v[EPT];
@@ -360,7 +357,7 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
 template <int L>
 cudaError_t set_smem_l()
 {
-    const int bytes = 2 * Fft<L>::PLANE * (int)sizeof(float);
+    const int bytes = Fft<L>::SLOTS * (int)sizeof(float2);
     cudaError_t e = cudaFuncSetAttribute(rc_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_filter_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -371,7 +368,7 @@ template <int L>
 cudaError_t launch_l(bool filter, int na, const float2* in, int len, const float2* tw,
                      const float2* h_in, unsigned window, float band, float2* out, cudaStream_t s)
 {
-    const size_t bytes = 2 * (size_t)Fft<L>::PLANE * sizeof(float);
+    const size_t bytes = (size_t)Fft<L>::SLOTS * sizeof(float2);
     if (filter)
         rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, tw, window, band, out);
     else
