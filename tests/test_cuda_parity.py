@@ -109,6 +109,37 @@ def test_ragged_and_tiny_images(shape):
     parity.assert_parity(img, ref, f"shape {shape}")
 
 
+@pytest.mark.slow
+def test_maximum_image_size():
+    """The largest image a plan accepts, 2^30 pixels (32768 x 32768, 8 GiB on the
+    device), 16 pulses of clutter; sampled pixels against the oracle. One pixel
+    more is refused."""
+    nx = ny = 32768
+    na, nr = 16, 4096
+    spacing = 0.05
+    rng = np.random.default_rng(30)
+    pos = scenes.straight_track(na, 1.0)
+    geo = scenes.image_geometry(nx, ny, spacing)
+    corner = np.array([geo["x0"], geo["y0"] + ny * spacing, 0.0])
+    rmin = float(np.min(np.linalg.norm(pos - np.array([0.0, geo["y0"], 0.0]), axis=1))) - 50.0
+    p = dict(nx=nx, ny=ny, na=na, nr=nr, r0=rmin, dr=scenes.DR, wavelength=scenes.WAVELENGTH, **geo)
+    assert float(np.max(np.linalg.norm(pos - corner, axis=1))) < rmin + (nr - 2) * scenes.DR
+    echo = (rng.standard_normal((na, nr)) + 1j * rng.standard_normal((na, nr))).astype(np.complex64)
+    img = torch.empty((ny, nx), dtype=torch.complex64, device=DEV)
+    with Plan(p) as plan:
+        plan.backproject(img, torch.from_numpy(echo).to(DEV), torch.from_numpy(pos).to(DEV))
+        torch.cuda.synchronize()
+    pix = np.unique(np.concatenate([rng.choice(nx * ny, 4000, replace=False),
+                                    [0, nx - 1, nx * ny - nx, nx * ny - 1]])).astype(np.int64)
+    got = img.reshape(-1)[torch.from_numpy(pix).to(DEV)].cpu().numpy()
+    del img
+    ref = oracle.backproject(p, echo, pos, pix)
+    parity.assert_parity(got, ref, "2^30 pixels")
+    with pytest.raises(SarbpError) as ex:
+        Plan(dict(p, ny=ny + 1))
+    assert ex.value.status == _native.SARBP_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("field,value", [("na", 0), ("nr", 0), ("nr", 1)])
 def test_no_contribution_gives_zero(field, value):
     sc = _small_scene(40, 20)
