@@ -17,6 +17,9 @@ stencil window rule, linearity, pulse-order invariance and focusing
 ``backproject_heights`` - pinned by reduction to ``backproject`` (zero and
 constant heights), a hand-derived value on a raised pixel, and focusing of
 targets on a rough surface (tests/test_oracle_heights_pins.py).
+``backproject_volume`` - a stack of ``backproject`` planes at z0 + iz dz; pinned by
+three-dimensional focusing of targets seen from a multi-pass aperture
+(tests/test_oracle_volume_pins.py).
 ``backproject(interp="nearest")`` - pinned by on-sample values, the rounding
 boundary at half a bin, the window rule and the generic invariants
 (tests/test_oracle_nearest_pins.py), with its own planted mistakes.
@@ -140,6 +143,17 @@ def backproject(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
     if full:
         img = img.reshape(ny, nx)
     return (img, secs, used) if return_info else img
+
+
+def backproject_volume(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray, nz: int,
+                       dz: float, threads: int = 0, library: ctypes.CDLL | None = None,
+                       interp: str = "linear") -> np.ndarray:
+    """FP64 voxel grid [nz, ny, nx]: plane iz is the image at height z0 + iz * dz."""
+    planes = [backproject(dict(params, z0=float(params["z0"]) + iz * float(dz)), echoes,
+                          antenna_pos, threads=threads, library=library, interp=interp)
+              for iz in range(int(nz))]
+    nx, ny = int(params["nx"]), int(params["ny"])
+    return np.stack(planes) if planes else np.zeros((0, ny, nx), dtype=np.complex128)
 
 
 def backproject_heights(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,

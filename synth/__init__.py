@@ -19,4 +19,5 @@ from .scenes import (  # noqa: F401
     straight_track,
     compared_pixels,
     terrain,
+    multipass_track,
 )

@@ -107,6 +107,18 @@ def straight_track(na: int, step: float, altitude: float = ALTITUDE,
     return pos
 
 
+def multipass_track(na_per_pass: int, passes: int, step: float, baseline: float,
+                    altitude: float = ALTITUDE, ground_offset: float = GROUND_OFFSET) -> np.ndarray:
+    """Several parallel straight passes stacked vertically, ``baseline`` metres
+    apart and centred on ``altitude`` (a two-dimensional aperture, as used for
+    three-dimensional imaging). Pulses of pass 0 first, float64 [passes * na_per_pass, 3]."""
+    tracks = []
+    for p in range(passes):
+        alt = altitude + (p - (passes - 1) / 2.0) * baseline
+        tracks.append(straight_track(na_per_pass, step, altitude=alt, ground_offset=ground_offset))
+    return np.concatenate(tracks, axis=0)
+
+
 def _motion(rng: np.random.Generator, na: int) -> np.ndarray:
     """Per-axis sum of three seeded sinusoids, |delta| <= 0.5 m."""
     n = np.arange(na, dtype=np.float64)
