@@ -309,6 +309,30 @@ def run_ours(args, scene, rank, world, local, dist):
         }
         time_interp("sinc8", "8-tap windowed sinc (SARBP_SINC8)")
         time_interp("nearest", "nearest neighbour (SARBP_NEAREST)")
+        # the same pulses onto a voxel grid of 8 planes 0.5 m apart
+        nzv = 8
+        vol = torch.empty((nzv, p["ny"], p["nx"]), dtype=torch.complex64, device=dev)
+        for _ in range(2):
+            plan.backproject_volume(vol, echoes, pos, 0.5)
+        torch.cuda.synchronize(dev)
+        plan.kernel_times()
+        steps_v = max(3, min(args.steps, 10))
+        total = 0.0
+        for i in range(steps_v):
+            flush.fill_(float(i))
+            starts[0].record(stream)
+            plan.backproject_volume(vol, echoes, pos, 0.5)
+            ends[0].record(stream)
+            ends[0].synchronize()
+            total += starts[0].elapsed_time(ends[0])
+        main_ms_v, launches_v = plan.kernel_times()
+        variants["volume"] = {
+            "interp": f"linear, voxel grid of {nzv} planes (sarbp_backproject_volume)",
+            "steps": steps_v, "value": nzv * updates * steps_v / (total / 1e3) / 1e9, "unit": UNIT,
+            "ms_per_step": total / steps_v,
+            "main_kernel_gupd": updates / (main_ms_v / max(launches_v, 1) / 1e3) / 1e9,
+        }
+        del vol
         # the same pulses onto pixels raised by 40 m of seeded terrain
         from synth import scenes as scenes_mod
         hmap = scenes_mod.terrain(p["nx"], p["ny"], p["dx"], 20337, relief=40.0)

@@ -24,6 +24,7 @@ EXPORTS = (
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
     "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
     "sarbp_plan_heights", "sarbp_backproject_heights", "sarbp_backproject_streamed",
+    "sarbp_backproject_volume",
 )
 
 SARBP_WINDOW_NONE = 0
@@ -73,6 +74,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_plan.restype = st
     lib.sarbp_backproject.argtypes = [vp, vp, vp, vp, P(Params), vp]
     lib.sarbp_backproject.restype = st
+    lib.sarbp_backproject_volume.argtypes = [vp, vp, vp, vp, P(Params), ctypes.c_int32,
+                                             ctypes.c_double, vp]
+    lib.sarbp_backproject_volume.restype = st
     lib.sarbp_plan_heights.argtypes = [P(vp), P(Params), ctypes.c_double, ctypes.c_double]
     lib.sarbp_plan_heights.restype = st
     lib.sarbp_backproject_heights.argtypes = [vp, vp, vp, vp, vp, P(Params), vp]

@@ -578,6 +578,53 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
                                   static_cast<cudaStream_t>(stream));
 }
 
+sarbp_status sarbp_backproject_volume(sarbp_plan_t plan, void* volume, const void* echoes,
+                                      const double* antenna_pos, const sarbp_params* params,
+                                      int32_t nz, double dz, void* stream)
+{
+    if (!plan || !params || nz < 0 || !isfin(dz))
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || plan->heights_mode)
+        return SARBP_ERR_PLAN_MISMATCH;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels > 0 && nz > 0 && (!volume || !aligned8(volume)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && (!antenna_pos || !aligned8(antenna_pos)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && params->nr > 0 && (!echoes || !aligned8(echoes)))
+        return SARBP_ERR_INVALID_ARG;
+    for (int iz = 0; iz < nz; ++iz)
+        if (!isfin(params->z0 + (double)iz * dz))
+            return SARBP_ERR_INVALID_ARG;
+    plan->last_error.clear();
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+
+    for (int iz = 0; iz < nz; ++iz) {
+        sarbp_params pz = *params;
+        pz.z0 = params->z0 + (double)iz * dz;
+        void* plane = static_cast<char*>(volume) + (size_t)iz * (size_t)pixels * 8;
+        st = enqueue_backprojection(plan, plane, echoes, antenna_pos, &pz,
+                                    static_cast<cudaStream_t>(stream));
+        if (st != SARBP_OK)
+            return st;
+    }
+    return SARBP_OK;
+}
+
 sarbp_status sarbp_backproject_heights(sarbp_plan_t plan, void* image, const void* echoes,
                                        const double* antenna_pos, const float* heights,
                                        const sarbp_params* params, void* stream)

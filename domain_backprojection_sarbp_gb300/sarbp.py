@@ -146,6 +146,23 @@ class Plan:
             self._raise(st, "sarbp_backproject")
         return image
 
+    def backproject_volume(self, volume, echoes, antenna_pos, dz, params=None, accumulate=False,
+                           stream=None, interp="linear"):
+        """Voxel grid: volume complex64 [nz, ny, nx] on the device, plane iz at z0 + iz * dz."""
+        import torch
+        p = _params(params if params is not None else self.params, accumulate, interp)
+        if not isinstance(volume, torch.Tensor) or volume.dim() != 3:
+            raise ValueError("volume must be a 3-D tensor [nz, ny, nx]")
+        nz = int(volume.shape[0])
+        vol = _check_device_tensor(volume, "volume", torch.complex64, (nz, p.ny, p.nx))
+        ech = _check_device_tensor(echoes, "echoes", torch.complex64, (p.na, p.nr))
+        pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))
+        st = self._lib.sarbp_backproject_volume(self._h, vol, ech, pos, ctypes.byref(p), nz,
+                                                float(dz), _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject_volume")
+        return volume
+
     def backproject_heights(self, image, echoes, antenna_pos, heights, params=None,
                             accumulate=False, stream=None):
         """Linear-interpolation backprojection of pixels raised to z0 + heights[iy, ix].

@@ -181,6 +181,26 @@ sarbp_status sarbp_backproject_streamed(sarbp_plan_t plan, void* image, const vo
                                         int32_t chunk_pulses, void* stream);
 
 /*
+ * sarbp_backproject_volume - backprojection onto a voxel grid: nz planes at
+ * heights z0 + iz * dz (iz = 0 .. nz-1), plane iz being the image
+ * sarbp_backproject makes with params->z0 replaced by that height (SARBP-GPU
+ * §3.3: the pixel grid may leave the ground plane; with a two-dimensional
+ * aperture, e.g. several passes at different heights given as one pulse list,
+ * the voxels resolve height).
+ *
+ * volume  device pointer, complex64 [nz][ny][nx], caller-owned, 8-byte aligned.
+ *         Overwritten, or added into with SARBP_ACCUMULATE.
+ * nz, dz  number of planes (>= 0) and their spacing in metres (finite).
+ * echoes, antenna_pos, params, stream, the plan and the interpolation flags:
+ *         as for sarbp_backproject. The planes are enqueued one after another
+ *         on `stream`; each equals the corresponding sarbp_backproject call
+ *         bit for bit.
+ */
+sarbp_status sarbp_backproject_volume(sarbp_plan_t plan, void* volume, const void* echoes,
+                                      const double* antenna_pos, const sarbp_params* params,
+                                      int32_t nz, double dz, void* stream);
+
+/*
  * Pixels on a height map (SARBP-GPU §3.3 remarks that the range history may
  * have to take terrain elevation into account; the page gives no formula, so
  * this is the plain reading): pixel (ix, iy) sits at
