@@ -23,7 +23,8 @@
 // 2. Range without a square root (bp_kernel). For each (tile, pulse) the slant
 //    range to the tile centre is computed in float64 and the range of every
 //    pixel of the tile is a Taylor polynomial of |p - a_n| about it (complete
-//    to third order, with the fourth-order terms in the row offset), in bins. A thread owns 32 pixels of one row, so per pulse it reduces the
+//    to third order, with the fourth-order terms in the row offset), in bins.
+//    A thread owns 32 pixels of one row, so per pulse it reduces the
 //    polynomial to a quadratic in its column offset (a split float for the
 //    large linear term keeps 2^-22-bin accuracy), and each update costs two
 //    FMAs for u. Pulses where the remainder bound exceeds 5e-5 rad of phase
@@ -34,6 +35,12 @@
 //    contiguous range per resident CTA. A tile covered by one CTA is written
 //    directly; the pieces of a shared tile go to partial buffers that
 //    reduce_kernel sums in CTA order, so the result is deterministic.
+//
+// 4. Variants of the same kernel (template INTERP): the 8-tap windowed sinc
+//    (a degree-4 polynomial per thread and pulse when the thread's pixels span
+//    at most a quarter bin), the nearest sample (one table entry per thread
+//    and pulse when its pixels round to two bins), and pixels on a height map
+//    (a float-pair row reference and a range series per pixel).
 #include "sarbp_internal.h"
 
 #include <cmath>
@@ -264,14 +271,15 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
 constexpr int NP = TILE_X / 2;
 
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
-// on the two table loads; their values are consumed by the next pulse step.
+// on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
                        MODE_PAIR = 5 };
 
 struct PulseState {
-    float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; gather: e0, e1, e2 (both halves)
-    float4 t0;                    // hinge: table entry k0
-    float2 t1d;                   // hinge: D part of entry k0 + 1
+    float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; otherwise e0, e1, e2 (both halves)
+    float4 t0;                    // hinge: table entry k0; sinc polynomial: lo_u, hi_u, k0, bin k0;
+                                  // nearest pair: table entry (e_kn, e_kn+1)
+    float2 t1d;                   // hinge: D part of entry k0 + 1; nearest pair: kn, bin kn
     unsigned long long base;      // gather: row pointer + (kb - magic bias) entries, in bytes
     int kb;                       // row index the polynomial u is relative to
     int bin0;                     // row index of absolute bin 0
