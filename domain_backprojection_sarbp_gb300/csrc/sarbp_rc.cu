@@ -14,7 +14,9 @@
 //
 // One CTA per pulse. The transforms are self-sorting (Stockham) passes of
 // radix 16 held in registers (16 complex values per thread), plus one pass of
-// radix 2, 4 or 8 when log2 N is not a multiple of 4; shared memory only
+// radix 2, 4 or 8 when log2 N is not a multiple of 4 (for N = 2 16^m the
+// radix-2 pass and its radix-16 neighbour run as one radix-32 pass with two
+// threads per butterfly, saving an exchange in each direction); shared memory only
 // carries the data between passes, as float2 values padded by one slot
 // every 16 (conflict-free for the strides used). The
 // forward transform takes the raw row straight from global memory (zero
@@ -163,7 +165,26 @@ struct Fft {
     static constexpr int PASSES = L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4;
     static constexpr int T = N / 16 > 32 ? N / 16 : 32;
     static constexpr int SLOTS = pad(N - 1) + 1;       // float2 slots of the padded row
+    // N = 2 16^m, m >= 2: the radix-2 pass and the radix-16 pass next to it
+    // run as one radix-32 pass, two threads per butterfly (one shared-memory
+    // exchange fewer in each direction)
+    static constexpr bool MERGE = R0 == 2 && L >= 9;
 };
+
+// exp(S 2 pi i s / 32) for s = 0 .. 15 (compile-time s)
+template <int S>
+__device__ __forceinline__ float2 w32(int s)
+{
+    constexpr float C[16] = {1.0f, 0.980785280f, 0.923879533f, 0.831469612f, 0.707106781f,
+                             0.555570233f, 0.382683432f, 0.195090322f, 0.0f, -0.195090322f,
+                             -0.382683432f, -0.555570233f, -0.707106781f, -0.831469612f,
+                             -0.923879533f, -0.980785280f};
+    constexpr float SN[16] = {0.0f, 0.195090322f, 0.382683432f, 0.555570233f, 0.707106781f,
+                              0.831469612f, 0.923879533f, 0.980785280f, 1.0f, 0.980785280f,
+                              0.923879533f, 0.831469612f, 0.707106781f, 0.555570233f,
+                              0.382683432f, 0.195090322f};
+    return make_float2(C[s], S * SN[s]);
+}
 
 // Shared row: complex values as float2, one spare slot after every 16 (a
 // warp's 8-byte accesses are served 16 lanes at a time; with this padding
@@ -237,29 +258,57 @@ __device__ __forceinline__ void forward_to_registers(const float2* __restrict__ 
     using F = Fft<L>;
     constexpr int R0 = F::R0, B0 = EPT / R0, NB0 = F::N / R0;
     const int tid = threadIdx.x;
+    if constexpr (F::MERGE) {
+        // radix-32 Stockham pass of span 1 from global memory: butterfly j
+        // takes x[j + t N/32], t < 32; thread half h = 0 keeps the even outputs
+        // (a_s = x_s + x_(s+16)), h = 1 the odd ones
+        // (b_s = (x_s - x_(s+16)) W32^-s), each followed by a 16-point DFT, so
+        // thread h holds X32[2k + h] in v[k]
+        constexpr int Q32 = F::N / 32;
+        const int j = tid >> 1, h = tid & 1;
 #pragma unroll
-    for (int b = 0; b < B0; ++b) {
-        const int j = tid + b * F::T;
-#pragma unroll
-        for (int t = 0; t < R0; ++t) {
-            const int i = j + t * NB0;
-            v[b * R0 + t] = (j < NB0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
+        for (int s2 = 0; s2 < 16; ++s2) {
+            const int i0 = j + s2 * Q32, i1 = j + (s2 + 16) * Q32;
+            const float2 a = i0 < len ? __ldg(src + i0) : make_float2(0.f, 0.f);
+            const float2 b = i1 < len ? __ldg(src + i1) : make_float2(0.f, 0.f);
+            v[s2] = h == 0 ? cadd(a, b) : cmul(csub(a, b), w32<-1>(s2));
         }
-        dft<R0, -1>(v + b * R0);
-    }
-    if constexpr (F::PASSES > 1) {
+        dft<16, -1>(v);
+        const int pb = pad(j * 32);
 #pragma unroll
-        for (int b = 0; b < B0; ++b) {
-            const int j = tid + b * F::T;
-            if (j < NB0)
-                pass_store<R0, 1>(r, v + b * R0, j);
-        }
+        for (int k = 0; k < 16; ++k)
+            r.st(pb + 2 * k + h + ((2 * k + h) >> 4), v[k]);
         __syncthreads();
-        Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid, tw);
-        constexpr int NSL = F::N / 16;                 // span of the last pass
+        Middle<L, -1, 2, F::PASSES - 1, 32>::run(r, v, tid, tw);
+        constexpr int NSL = F::N / 16;
         if (tid < (F::N / 16))
             pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
         __syncthreads();
+    } else {
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+#pragma unroll
+            for (int t = 0; t < R0; ++t) {
+                const int i = j + t * NB0;
+                v[b * R0 + t] = (j < NB0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
+            }
+            dft<R0, -1>(v + b * R0);
+        }
+        if constexpr (F::PASSES > 1) {
+#pragma unroll
+            for (int b = 0; b < B0; ++b) {
+                const int j = tid + b * F::T;
+                if (j < NB0)
+                    pass_store<R0, 1>(r, v + b * R0, j);
+            }
+            __syncthreads();
+            Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid, tw);
+            constexpr int NSL = F::N / 16;             // span of the last pass
+            if (tid < (F::N / 16))
+                pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
+            __syncthreads();
+        }
     }
 }
 
@@ -334,21 +383,57 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
             pass_store<16, 1>(r, v, tid);
         }
         __syncthreads();
-        Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid, tw);
-        // last pass: radix R0, span N / R0; outputs go to j + t N/R0
-        constexpr int B0 = EPT / R0, NB0 = N / R0;
+        if constexpr (F::MERGE) {
+            Middle<L, 1, 1, F::PASSES - 2, 16>::run(r, v, tid, tw);
+            // last pass: radix 32, span N / 32, two threads per butterfly j:
+            // inputs x[j + t N/32] times exp(+2 pi i j t / N), then as in the
+            // forward merged pass; outputs go to j + t N/32
+            constexpr int Q32 = N / 32, NSH = N / 2;
+            const int j = tid >> 1, h = tid & 1;
+            // powers of w = exp(+2 pi i j / N): the table region of span N/2
+            // holds exp(-2 pi i t k / N) for rows t = 1, 4, 8, 12
+            const float2* tr = tw + 4 * (NSH - 1) + j;
+            const float2 w1 = conj_if(__ldg(tr), true), w4 = conj_if(__ldg(tr + NSH), true);
+            const float2 w8 = conj_if(__ldg(tr + 2 * NSH), true);
+            const float2 w12 = conj_if(__ldg(tr + 3 * NSH), true);
+            const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1), w16 = cmul(w8, w8);
+            const int pb = pad(j);
 #pragma unroll
-        for (int b = 0; b < B0; ++b) {
-            const int j = tid + b * F::T;
-            if (j >= NB0)
-                continue;
-            float2* w = v + b * R0;
-            pass_load<R0, 1, N, NB0>(r, w, j, tw);
+            for (int s2 = 0; s2 < 16; ++s2) {
+                const float2 lo4 = (s2 & 3) == 0 ? make_float2(1.f, 0.f)
+                                 : (s2 & 3) == 1 ? w1 : (s2 & 3) == 2 ? w2 : w3;
+                const float2 hi4 = (s2 >> 2) == 0 ? make_float2(1.f, 0.f)
+                                 : (s2 >> 2) == 1 ? w4 : (s2 >> 2) == 2 ? w8 : w12;
+                const float2 ws = (s2 == 0) ? make_float2(1.f, 0.f)
+                                : ((s2 & 3) == 0 ? hi4 : ((s2 >> 2) == 0 ? lo4 : cmul(hi4, lo4)));
+                const float2 a = cmul(r.ld(pb + pad(s2 * Q32)), ws);
+                const float2 b = cmul(r.ld(pb + pad((s2 + 16) * Q32)), cmul(w16, ws));
+                v[s2] = h == 0 ? cadd(a, b) : cmul(csub(a, b), w32<1>(s2));
+            }
+            dft<16, 1>(v);
 #pragma unroll
-            for (int t = 0; t < R0; ++t) {
-                const int i = j + t * NB0;
+            for (int k = 0; k < 16; ++k) {
+                const int i = j + (2 * k + h) * Q32;
                 if (i < ns_in)
-                    out[row0 + i] = w[t];
+                    out[row0 + i] = v[k];
+            }
+        } else {
+            Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid, tw);
+            // last pass: radix R0, span N / R0; outputs go to j + t N/R0
+            constexpr int B0 = EPT / R0, NB0 = N / R0;
+#pragma unroll
+            for (int b = 0; b < B0; ++b) {
+                const int j = tid + b * F::T;
+                if (j >= NB0)
+                    continue;
+                float2* w = v + b * R0;
+                pass_load<R0, 1, N, NB0>(r, w, j, tw);
+#pragma unroll
+                for (int t = 0; t < R0; ++t) {
+                    const int i = j + t * NB0;
+                    if (i < ns_in)
+                        out[row0 + i] = w[t];
+                }
             }
         }
     }
