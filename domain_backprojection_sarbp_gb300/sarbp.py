@@ -193,10 +193,10 @@ class Plan:
         return image
 
     def backproject_streamed(self, image, echoes, antenna_pos, chunk_pulses=1024, params=None,
-                             accumulate=False, stream=None):
-        """Host arrays, pulses in chunks of ``chunk_pulses`` whose copies overlap the compute
-        (linear interpolation); returns when the image is on the host."""
-        p = _params(params if params is not None else self.params, accumulate)
+                             accumulate=False, stream=None, interp="linear"):
+        """Host arrays, pulses in chunks of ``chunk_pulses`` whose copies overlap the compute;
+        returns when the image is on the host."""
+        p = _params(params if params is not None else self.params, accumulate, interp)
         img, ech, pos = _host_args(p, image, echoes, antenna_pos)
         stream_h = ctypes.c_void_p(None) if stream is None else _stream_handle(stream)
         st = self._lib.sarbp_backproject_streamed(self._h, img, ech, pos, ctypes.byref(p),

@@ -160,6 +160,7 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
  *
  * image, echoes, antenna_pos: HOST pointers as for sarbp_backproject_host.
  * chunk_pulses: pulses per chunk, >= 1 (values above na mean one chunk).
+ * params->flags: as for sarbp_backproject (any interpolation).
  *
  * For chunk c (pulses c*chunk_pulses ...) the call finds on the host the band
  * of range bins those pulses can reach from the image, copies that band into
