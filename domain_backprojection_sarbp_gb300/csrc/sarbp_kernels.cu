@@ -956,28 +956,31 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
     const float g = inv_r * inv_r;                // 1 / R^2
     const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
 
-    const float2 two_vx = make_float2(2.0f * vx.hi, 2.0f * vx.hi);
+    // s = q_x (2 v_x + q_x) + dz (2 v_z + dz) with q_x = i dx, i.e.
+    // i (2 v_x dx + i dx^2) + dz (2 v_z + dz); the series times hb is the
+    // polynomial a1 s + a2 s^2 + a3 s^3 + a4 s^4 with a_n = hb g^(n-1) c_n
+    const float ax = 2.0f * vx.hi * k.dx_f, bx = k.dx_f * k.dx_f;
+    const float2 ax2 = make_float2(ax, ax), bx2 = make_float2(bx, bx);
     const float2 two_vz = make_float2(2.0f * vz.hi, 2.0f * vz.hi);
     const float2 hrw = make_float2(-hr.hrow, -hr.hrow);
-    const float2 g2 = make_float2(g, g), hb2 = make_float2(hb, hb);
-    const float2 c3 = make_float2(-5.0f / 64.0f, -5.0f / 64.0f);
-    const float2 c2 = make_float2(0.125f, 0.125f), c1 = make_float2(-0.25f, -0.25f);
+    const float a1 = hb, a2 = -0.25f * hb * g, a3 = 0.125f * hb * g * g,
+                a4 = -0.078125f * hb * g * g * g;
+    const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
+    const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4, a4);
     const float2 one = make_float2(1.0f, 1.0f), neg1 = make_float2(-1.0f, -1.0f);
     const float2 f0 = make_float2(frac, frac);
     const float2 mm = make_float2(MAGIC, MAGIC), nmm = make_float2(-MAGIC, -MAGIC);
     const float2 cc = make_float2(k.c_phase, k.c_phase);
-    const float2 dx2 = make_float2(k.dx_f, k.dx_f);
     float2 id = make_float2(k.i0, k.i0 + NP);
     const int wmax = k.W - 1;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 qx = __fmul2_rn(id, dx2);
+        const float2 sx = __fmul2_rn(id, __ffma2_rn(id, bx2, ax2));
         id = __fadd2_rn(id, one);
         const float2 dz = __fadd2_rn(s_h2[q], hrw);
-        const float2 s = __ffma2_rn(dz, __fadd2_rn(dz, two_vz), __fmul2_rn(qx, __fadd2_rn(qx, two_vx)));
-        const float2 t = __fmul2_rn(s, g2);
-        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(t, c3, c2), t, c1), t, one);
-        const float2 ub = __ffma2_rn(__fmul2_rn(s, hb2), poly, f0);
+        const float2 s = __ffma2_rn(dz, __fadd2_rn(dz, two_vz), sx);
+        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12);
+        const float2 ub = __ffma2_rn(s, poly, f0);
         const float2 tt = __fadd2_rd(ub, mm);
         const float2 f = __ffma2_rn(__fadd2_rn(tt, nmm), neg1, ub);
         const float2 x = __fmul2_rn(f, cc);
