@@ -47,7 +47,7 @@ HBM_GBS = 6796.9            # measured copy bandwidth of the GB300s (MEA
 L2_FLUSH_BYTES = 256 << 20
 # dram read+write bytes of one bp_kernel launch, from ncu (None until captured
 # for the current kernel)
-MAIN_KERNEL_TRAFFIC = 10_690_048   # ncu dram read + write, one bp_kernel<0> launch, page-sized scene
+MAIN_KERNEL_TRAFFIC = 10_684_416   # ncu dram read + write, one bp_kernel<0> launch, page-sized scene
 
 
 # ------------------------------------------------------------------ ranks
