@@ -10,14 +10,18 @@ Definition used here (reading of the page's steps):
 with raw taken as zero beyond its last sample, i.e. the linear
 cross-correlation, computed as ifft(fft(raw, N) * conj(fft(ref, N)) * W)[:ns]
 with N the smallest power of two >= ns + L - 1 (no circular wrap). W = 1, or
-the Hamming weighting 0.54 + 0.46 cos(2 pi f / b) over the centred band
-|f| <= b/2 (f = signed frequency in cycles per sample, b = band fraction) and
-0 outside it. numpy's FFT is a library step of that definition.
+a weighting over the centred band |f| <= b/2 (f = signed frequency in cycles
+per sample, b = band fraction) and 0 outside it: Hamming
+0.54 + 0.46 cos(2 pi f / b), or Taylor (nbar = 4, 35 dB sidelobes)
+1 + 2 sum_m F_m cos(2 pi m f / b) with Taylor's coefficients F_m. numpy's FFT
+is a library step of that definition.
 
 Pinned by: the direct correlation sum on small sizes (brute force), the
 closed-form peak a * sum |ref|^2 at an integer delay, shift equivariance,
 linearity, and the sidelobe / mainlobe figures the page quotes (about -13 dB
-peak sidelobe without a window; Hamming widens the mainlobe 1.3-1.5x)
+peak sidelobe without a window; Hamming widens the mainlobe 1.3-1.5x), and for
+the Taylor weighting its design sidelobe level, its unit mean over the band
+and a mainlobe between those of no window and Hamming
 (tests/test_range_compression_oracle.py).
 """
 
@@ -33,13 +37,44 @@ def fft_size(ns: int, nref: int) -> int:
     return n
 
 
+TAYLOR_NBAR = 4          # terms kept (Taylor's n-bar)
+TAYLOR_SLL_DB = 35.0     # design sidelobe level below the peak
+
+
+def taylor_coefficients(nbar: int = TAYLOR_NBAR, sll_db: float = TAYLOR_SLL_DB) -> np.ndarray:
+    """F_1 .. F_(nbar-1) of Taylor's weighting w(x) = 1 + 2 sum F_m cos(2 pi m x).
+
+    With A = acosh(10^(sll/20)) / pi and the stretch sigma^2 = nbar^2 / (A^2 + (nbar - 1/2)^2),
+    F_m = (-1)^(m+1) prod_i (1 - m^2 / (sigma^2 (A^2 + (i - 1/2)^2)))
+          / (2 prod_(i != m) (1 - m^2 / i^2)),  i, m = 1 .. nbar - 1.
+    """
+    a = np.arccosh(10.0 ** (sll_db / 20.0)) / np.pi
+    sigma2 = nbar ** 2 / (a ** 2 + (nbar - 0.5) ** 2)
+    out = np.zeros(nbar - 1)
+    for m in range(1, nbar):
+        num = 1.0
+        den = 1.0
+        for i in range(1, nbar):
+            num *= 1.0 - m ** 2 / (sigma2 * (a ** 2 + (i - 0.5) ** 2))
+            if i != m:
+                den *= 1.0 - m ** 2 / i ** 2
+        out[m - 1] = (-1.0) ** (m + 1) * num / (2.0 * den)
+    return out
+
+
 def window_weights(n: int, window: str = "none", band_fraction: float = 1.0) -> np.ndarray:
     f = np.fft.fftfreq(n)                      # signed cycles per sample
     if window == "none":
         return np.ones(n)
+    inside = np.abs(f) <= band_fraction / 2.0
+    x = f / band_fraction
     if window == "hamming":
-        inside = np.abs(f) <= band_fraction / 2.0
-        return np.where(inside, 0.54 + 0.46 * np.cos(2.0 * np.pi * f / band_fraction), 0.0)
+        return np.where(inside, 0.54 + 0.46 * np.cos(2.0 * np.pi * x), 0.0)
+    if window == "taylor":
+        w = np.ones(n)
+        for m, fm in enumerate(taylor_coefficients(), start=1):
+            w += 2.0 * fm * np.cos(2.0 * np.pi * m * x)
+        return np.where(inside, w, 0.0)
     raise ValueError(window)
 
 

@@ -95,6 +95,35 @@ def test_sidelobes_and_mainlobe_match_the_page():
     assert abs(w_rect / 8 / (0.886 * cell) - 1) < 0.05
 
 
+def test_taylor_window_meets_its_design():
+    # SARBP-GPU §3.1 names Taylor beside Hamming. Taylor's weighting with
+    # nbar = 4 and a 35 dB design: the compressed chirp's peak sidelobe sits near
+    # -35 dB, the mainlobe widens less than with Hamming, and the weighting's
+    # mean over the band is its constant term, 1.
+    tay, d = _profile("taylor")
+    rect, _ = _profile("none")
+    ham, _ = _profile("hamming")
+    psl_t, w_t = _mainlobe_and_sidelobe(tay, d)
+    _, w_r = _mainlobe_and_sidelobe(rect, d)
+    _, w_h = _mainlobe_and_sidelobe(ham, d)
+    assert -37.5 < psl_t < -32.5, psl_t
+    assert w_r < w_t < w_h, (w_r, w_t, w_h)
+    x = (np.arange(100000) + 0.5) / 100000 - 0.5
+    fm = rc.taylor_coefficients()
+    w = 1 + 2 * sum(f * np.cos(2 * np.pi * (m + 1) * x) for m, f in enumerate(fm))
+    assert abs(w.mean() - 1.0) < 1e-9
+    assert np.allclose(w, w[::-1])
+
+
+def test_taylor_pin_rejects_a_sign_slip(monkeypatch):
+    # a plausible slip, (-1)^m for (-1)^(m+1), breaks the sidelobe design
+    good = rc.taylor_coefficients()
+    monkeypatch.setattr(rc, "taylor_coefficients", lambda *a, **k: -good)
+    tay, d = _profile("taylor")
+    psl, _ = _mainlobe_and_sidelobe(tay, d)
+    assert not (-37.5 < psl < -32.5), psl
+
+
 def test_raw_generator_compresses_to_target_range():
     pos = np.array([[0.0, -7000.0, 5000.0]])
     tgt = np.array([[0.0, 0.0, 0.0]])
