@@ -37,7 +37,7 @@ def fft_size(ns: int, nref: int) -> int:
     return n
 
 
-TAYLOR_NBAR = 4          # terms kept (Taylor's n-bar)
+TAYLOR_NBAR = 5          # terms kept (Taylor's n-bar; 35 dB needs nbar >= 2 A^2 + 1/2 = 5)
 TAYLOR_SLL_DB = 35.0     # design sidelobe level below the peak
 
 
