@@ -29,6 +29,7 @@ EXPORTS = (
 
 SARBP_WINDOW_NONE = 0
 SARBP_WINDOW_HAMMING = 1
+SARBP_WINDOW_TAYLOR = 2
 
 
 class Params(ctypes.Structure):

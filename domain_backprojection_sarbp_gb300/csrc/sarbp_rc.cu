@@ -316,6 +316,7 @@ template <int L>
 __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __restrict__ ref, int nref,
                                                               const float2* __restrict__ tw,
                                                               unsigned window, float band,
+                                                              float4 taylor,
                                                               float2* __restrict__ h)
 {
     using F = Fft<L>;
@@ -335,9 +336,16 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __re
         for (int t = 0; t < RL; ++t) {
             const int m = j + t * NBL;                  // natural frequency index
             float w = 1.0f;
-            if (window == SARBP_WINDOW_HAMMING) {
+            if (window != SARBP_WINDOW_NONE) {
                 const float f = (float)(m < F::N / 2 ? m : m - F::N) / (float)F::N;
-                w = fabsf(f) <= 0.5f * band ? 0.54f + 0.46f * cospif(2.0f * f / band) : 0.0f;
+                const float x = f / band;
+                if (!(fabsf(f) <= 0.5f * band))
+                    w = 0.0f;
+                else if (window == SARBP_WINDOW_HAMMING)
+                    w = 0.54f + 0.46f * cospif(2.0f * x);
+                else   // Taylor: 1 + 2 sum F_m cos(2 pi m x)
+                    w = 1.0f + 2.0f * (taylor.x * cospif(2.0f * x) + taylor.y * cospif(4.0f * x) +
+                                       taylor.z * cospif(6.0f * x) + taylor.w * cospif(8.0f * x));
             }
             const float2 x = v[b * RL + t];
             h[m] = make_float2(x.x * w * inv_n, -x.y * w * inv_n);
@@ -451,11 +459,12 @@ cudaError_t set_smem_l()
 
 template <int L>
 cudaError_t launch_l(bool filter, int na, const float2* in, int len, const float2* tw,
-                     const float2* h_in, unsigned window, float band, float2* out, cudaStream_t s)
+                     const float2* h_in, unsigned window, float band, float4 taylor, float2* out,
+                     cudaStream_t s)
 {
     const size_t bytes = (size_t)Fft<L>::SLOTS * sizeof(float2);
     if (filter)
-        rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, tw, window, band, out);
+        rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, tw, window, band, taylor, out);
     else
         rc_kernel<L><<<na, Fft<L>::T, bytes, s>>>(in, len, tw, h_in, out);
     return cudaGetLastError();
@@ -484,25 +493,50 @@ cudaError_t set_smem(int log2n)
 }
 
 cudaError_t launch(int log2n, bool filter, int na, const float2* in, int len, const float2* tw,
-                   const float2* h_in, unsigned window, float band, float2* out, cudaStream_t s)
+                   const float2* h_in, unsigned window, float band, float4 taylor, float2* out,
+                   cudaStream_t s)
 {
     switch (log2n) {
-    case 1: return launch_l<1>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 2: return launch_l<2>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 3: return launch_l<3>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 4: return launch_l<4>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 5: return launch_l<5>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 6: return launch_l<6>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 7: return launch_l<7>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 8: return launch_l<8>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 9: return launch_l<9>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 10: return launch_l<10>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 11: return launch_l<11>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 12: return launch_l<12>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 13: return launch_l<13>(filter, na, in, len, tw, h_in, window, band, out, s);
-    case 14: return launch_l<14>(filter, na, in, len, tw, h_in, window, band, out, s);
+    case 1: return launch_l<1>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 2: return launch_l<2>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 3: return launch_l<3>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 4: return launch_l<4>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 5: return launch_l<5>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 6: return launch_l<6>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 7: return launch_l<7>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 8: return launch_l<8>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 9: return launch_l<9>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 10: return launch_l<10>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 11: return launch_l<11>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 12: return launch_l<12>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 13: return launch_l<13>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 14: return launch_l<14>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
     }
     return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+namespace {
+
+// Taylor's weighting coefficients F_1 .. F_4 (nbar = 5, 35 dB), in float64.
+float4 taylor_coefficients()
+{
+    constexpr int NBAR = 5;
+    const double pi = 3.14159265358979323846;
+    const double a = std::acosh(std::pow(10.0, 35.0 / 20.0)) / pi;
+    const double sigma2 = (double)(NBAR * NBAR) / (a * a + (NBAR - 0.5) * (NBAR - 0.5));
+    double f[NBAR - 1];
+    for (int m = 1; m < NBAR; ++m) {
+        double num = 1.0, den = 1.0;
+        for (int i = 1; i < NBAR; ++i) {
+            num *= 1.0 - (double)(m * m) / (sigma2 * (a * a + (i - 0.5) * (i - 0.5)));
+            if (i != m)
+                den *= 1.0 - (double)(m * m) / (double)(i * i);
+        }
+        f[m - 1] = ((m % 2) ? 1.0 : -1.0) * num / (2.0 * den);
+    }
+    return make_float4((float)f[0], (float)f[1], (float)f[2], (float)f[3]);
 }
 
 }  // namespace
@@ -526,9 +560,10 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     if (!p || p->na < 0 || p->ns < 1 || p->nref < 1 || !ref ||
         (reinterpret_cast<uintptr_t>(ref) & 7u))
         return SARBP_ERR_INVALID_ARG;
-    if (p->window != SARBP_WINDOW_NONE && p->window != SARBP_WINDOW_HAMMING)
+    if (p->window != SARBP_WINDOW_NONE && p->window != SARBP_WINDOW_HAMMING &&
+        p->window != SARBP_WINDOW_TAYLOR)
         return SARBP_ERR_INVALID_ARG;
-    if (p->window == SARBP_WINDOW_HAMMING && !(p->band_fraction > 0.0 && p->band_fraction <= 1.0))
+    if (p->window != SARBP_WINDOW_NONE && !(p->band_fraction > 0.0 && p->band_fraction <= 1.0))
         return SARBP_ERR_INVALID_ARG;
     int log2n = 0;
     while ((1ll << log2n) < (long long)p->ns + p->nref - 1)
@@ -582,7 +617,7 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (e == cudaSuccess)
         e = launch(log2n, true, 1, static_cast<const float2*>(ref), p->nref, plan->tw, nullptr,
-                   p->window, (float)p->band_fraction, plan->h, s);
+                   p->window, (float)p->band_fraction, taylor_coefficients(), plan->h, s);
     if (e != cudaSuccess) {
         cudaFree(plan->tw);
         cudaFree(plan->h);
@@ -607,7 +642,8 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
     if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
         return SARBP_ERR_INVALID_ARG;
     return launch(plan->log2n, false, p.na, static_cast<const float2*>(raw), p.ns, plan->tw, plan->h,
-                  p.window, 0.0f, static_cast<float2*>(out), static_cast<cudaStream_t>(stream)) ==
+                  p.window, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f), static_cast<float2*>(out),
+                  static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? SARBP_OK
                : SARBP_ERR_CUDA;

@@ -250,7 +250,8 @@ class RangeCompressor:
         import torch
         self._lib = _native.lib()
         ref = _check_device_tensor(reference, "reference", torch.complex64, (reference.shape[0],))
-        win = {"none": _native.SARBP_WINDOW_NONE, "hamming": _native.SARBP_WINDOW_HAMMING}[window]
+        win = {"none": _native.SARBP_WINDOW_NONE, "hamming": _native.SARBP_WINDOW_HAMMING,
+               "taylor": _native.SARBP_WINDOW_TAYLOR}[window]
         self.params = _native.RcParams(int(na), int(ns), int(reference.shape[0]), win,
                                        float(band_fraction))
         handle = ctypes.c_void_p()

@@ -286,21 +286,27 @@ sarbp_status sarbp_kernel_times(sarbp_plan_t plan, double* main_ms, int32_t* lau
  *   rc[n][k] = sum_{l=0}^{nref-1} raw[n][k + l] * conj(ref[l])   (raw = 0 beyond ns)
  *
  * computed through FFTs of size N, the smallest power of two >= ns + nref - 1
- * (no circular wrap), N <= 16384. With SARBP_WINDOW_HAMMING the filter
- * spectrum is weighted by 0.54 + 0.46 cos(2 pi f / b) for |f| <= b/2 and 0
- * outside (f = signed frequency in cycles per sample, b = band_fraction, the
- * chirp bandwidth over the sampling rate); SARBP_WINDOW_NONE is the plain
- * matched filter.
+ * (no circular wrap), N <= 16384. With a window the filter spectrum is
+ * weighted over |f| <= b/2 and zeroed outside (f = signed frequency in cycles
+ * per sample, b = band_fraction, the chirp bandwidth over the sampling rate):
+ * SARBP_WINDOW_HAMMING by 0.54 + 0.46 cos(2 pi f / b); SARBP_WINDOW_TAYLOR by
+ * Taylor's weighting 1 + 2 sum_{m=1}^{4} F_m cos(2 pi m f / b) with nbar = 5
+ * and a 35 dB design sidelobe level (A = acosh(10^(35/20)) / pi,
+ * sigma^2 = 25 / (A^2 + 4.5^2),
+ * F_m = (-1)^(m+1) prod_i (1 - m^2 / (sigma^2 (A^2 + (i - 1/2)^2)))
+ *       / (2 prod_{i != m} (1 - m^2 / i^2)), i = 1 .. 4).
+ * SARBP_WINDOW_NONE is the plain matched filter.
  */
 #define SARBP_WINDOW_NONE 0u
 #define SARBP_WINDOW_HAMMING 1u
+#define SARBP_WINDOW_TAYLOR 2u
 
 typedef struct sarbp_rc_params {
     int32_t na;            /* pulses                                               */
     int32_t ns;            /* samples per pulse, input and output                  */
     int32_t nref;          /* samples of the reference (transmitted) pulse         */
-    uint32_t window;       /* SARBP_WINDOW_NONE or SARBP_WINDOW_HAMMING            */
-    double band_fraction;  /* b in (0, 1] for the Hamming window                   */
+    uint32_t window;       /* SARBP_WINDOW_NONE, _HAMMING or _TAYLOR              */
+    double band_fraction;  /* b in (0, 1] for the Hamming and Taylor windows      */
 } sarbp_rc_params;
 
 typedef struct sarbp_rc_plan_s* sarbp_rc_plan_t;

@@ -53,15 +53,16 @@ def test_random_rows(ns, nref):
     assert m["rel_l2"] < 1e-5 and m["max_err"] < 1e-5, m
 
 
-def test_chirp_hamming_page_size():
+@pytest.mark.parametrize("window", ["hamming", "taylor"])
+def test_chirp_windowed_page_size(window):
     sc = scenes.make_scene(scenes.shrink(scenes.CONFIGS[2], na=64, nx=64, ny=64, n_targets=1))
     ref = chirp.chirp()
     band = chirp.BANDWIDTH / (chirp.C_LIGHT / (2 * chirp.DR))
     tgt = np.array([[0.0, 0.0, 0.0]])
     raw = chirp.raw_echoes(sc.antenna_pos, tgt, np.array([1.0]), sc.params["r0"], 4096)
     raw += 0.1 * (np.random.default_rng(3).standard_normal(raw.shape) + 0j)
-    got = gpu_compress(raw, ref, "hamming", band)
-    want = rco.range_compress(raw.astype(np.complex64), ref.astype(np.complex64), "hamming", band)
+    got = gpu_compress(raw, ref, window, band)
+    want = rco.range_compress(raw.astype(np.complex64), ref.astype(np.complex64), window, band)
     m = parity.compare(got, want)
     assert m["rel_l2"] < 1e-5 and m["max_err"] < 1e-5, m
 
