@@ -43,7 +43,23 @@ MUFU_PER_SM_CLK = 16          # sine/cosine lanes per SM per clock
 MUFU_PER_UPDATE = 2           # sin and cos of the phase; the range needs no sqrt here
 PAGE_SFU_PER_UPDATE = 3       # the page's loop: sqrt, sin, cos
 SM_MAX_MHZ_FALLBACK = 2070.0
-HBM_GBS = 6796.9            # measured copy bandwidth of the GB300s (MEASURED_PEAKS.json)
+HBM_GBS_FALLBACK = 6796.9   # measured copy bandwidth of these GB300s, used when no peaks file is present
+
+
+def measured_hbm_gbs() -> tuple[float, str]:
+    """HBM copy bandwidth from the measured-peaks file beside this script, else the constant."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        if v > 0:
+            return v, "measured"
+    except (OSError, ValueError, KeyError, TypeError):
+        pass
+    return HBM_GBS_FALLBACK, "fallback"
+
+
+HBM_GBS, HBM_BASIS = measured_hbm_gbs()
 L2_FLUSH_BYTES = 256 << 20
 # dram read+write bytes of one bp_kernel launch, from ncu (None until captured
 # for the current kernel)
@@ -395,7 +411,8 @@ def run_ours(args, scene, rank, world, local, dist):
                          "unit": "TFLOP/s", "frac": rc_tflops / fp32_peak,
                          "flops_per_launch": rc_flops,
                          "peak_basis": "SMs x 128 FP32 lanes x 2 (FMA) x 2070 MHz",
-                         "hbm_frac": rc_gbs / HBM_GBS, "algorithmic_bytes": rc_bytes},
+                         "hbm_frac": rc_gbs / HBM_GBS, "hbm_peak_gbs": HBM_GBS,
+                         "hbm_peak_basis": HBM_BASIS, "algorithmic_bytes": rc_bytes},
         }
         del raw, rc_out
     plan.close()
