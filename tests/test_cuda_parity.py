@@ -94,6 +94,17 @@ def test_config_full_size_sampled(index):
     print(sc.cfg.name, m)
 
 
+@pytest.mark.slow
+def test_page_scene_every_pixel():
+    """The benchmark's scene compared at all 1,048,576 pixels (4.3e9 updates of
+    the oracle, a few seconds on the host's cores), not only a sample."""
+    sc = scenes.make_scene(scenes.CONFIGS[2])
+    img = gpu_image(sc.params, sc.echoes, sc.antenna_pos)
+    ref = oracle.backproject(sc.params, sc.echoes, sc.antenna_pos)
+    print(sc.cfg.name, "all pixels", parity.assert_parity(img, ref, "page scene, every pixel"))
+    assert not parity.argmax_mismatches(img, ref, sc.targets)
+
+
 # ---------------------------------------------------------------- edge cases
 def _small_scene(nx, ny, na=40, nr=512, spacing=0.5, step=0.5, seed=5, noise=0.05):
     cfg = scenes.shrink(scenes.CONFIGS[0], nx=nx, ny=ny, na=na, nr=nr, spacing=spacing,
