@@ -507,7 +507,8 @@ sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out)
     out->full_window = plan->full_window;
     out->kernels_per_call = 0;
     if (plan->tiles > 0 && plan->p.na > 0 && plan->p.nr >= 2)
-        out->kernels_per_call = any_split_tile(make_const(plan, &plan->p)) ? 3 : 2;
+        out->kernels_per_call = (any_split_tile(make_const(plan, &plan->p)) ? 3 : 2) +
+                                ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0);
     else if (plan->tiles > 0)
         out->kernels_per_call = 0;   // a memset at most
     out->scratch_bytes = plan->scratch_bytes;

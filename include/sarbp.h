@@ -260,7 +260,8 @@ typedef struct sarbp_plan_info {
     int32_t ctas_per_sm, sms;     /* occupancy used to size the grid                   */
     int32_t window;               /* W: table entries per pulse                        */
     int32_t full_window;          /* 1 if every table row spans the whole range axis   */
-    int32_t kernels_per_call;     /* kernel launches one sarbp_backproject enqueues    */
+    int32_t kernels_per_call;     /* kernel launches one sarbp_backproject enqueues
+                                     with the plan's own params (flags included)      */
     size_t scratch_bytes;         /* device memory held by the plan                    */
 } sarbp_plan_info;
 
