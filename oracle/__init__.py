@@ -16,7 +16,8 @@ stencil window rule, linearity, pulse-order invariance and focusing
 (tests/test_oracle_sinc_pins.py), with its own planted mistakes.
 ``backproject_heights`` - pinned by reduction to ``backproject`` (zero and
 constant heights), a hand-derived value on a raised pixel, and focusing of
-targets on a rough surface (tests/test_oracle_heights_pins.py).
+targets on a rough surface (tests/test_oracle_heights_pins.py); its sinc and
+nearest forms by the same reductions to the pinned planar variants.
 ``backproject_volume`` - a stack of ``backproject`` planes at z0 + iz dz; pinned by
 three-dimensional focusing of targets seen from a multi-pass aperture
 (tests/test_oracle_volume_pins.py).
@@ -83,8 +84,11 @@ def load_library(path: str) -> ctypes.CDLL:
             ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
         ]
-    fn = getattr(lib, "oracle_backproject_heights", None)
-    if fn is not None:
+    for name in ("oracle_backproject_heights", "oracle_backproject_heights_sinc8",
+                 "oracle_backproject_heights_nearest"):
+        fn = getattr(lib, name, None)
+        if fn is None:
+            continue
         fn.restype = ctypes.c_int
         fn.argtypes = [
             ctypes.POINTER(OracleGeometry), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -158,10 +162,13 @@ def backproject_volume(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray
 
 def backproject_heights(params: dict, echoes: np.ndarray, antenna_pos: np.ndarray,
                         heights: np.ndarray, pixels: np.ndarray | None = None, threads: int = 0,
-                        library: ctypes.CDLL | None = None):
-    """FP64 linear-interpolation image over pixels raised to z0 + heights[iy, ix]
-    (``heights`` float32 [ny, nx])."""
+                        library: ctypes.CDLL | None = None, interp: str = "linear"):
+    """FP64 image over pixels raised to z0 + heights[iy, ix] (``heights`` float32
+    [ny, nx]); ``interp`` as for :func:`backproject`."""
     library = library or lib()
+    fn = {"linear": library.oracle_backproject_heights,
+          "sinc8": library.oracle_backproject_heights_sinc8,
+          "nearest": library.oracle_backproject_heights_nearest}[interp]
     nx, ny, na, nr = (int(params[k]) for k in ("nx", "ny", "na", "nr"))
     echoes = np.ascontiguousarray(echoes, dtype=np.complex64).reshape(na, nr)
     pos = np.ascontiguousarray(antenna_pos, dtype=np.float64).reshape(na, 3)
@@ -171,7 +178,7 @@ def backproject_heights(params: dict, echoes: np.ndarray, antenna_pos: np.ndarra
            else np.ascontiguousarray(pixels, dtype=np.int64).reshape(-1))
     out = np.zeros((pix.size, 2), dtype=np.float64)
     g = geometry(params)
-    used = library.oracle_backproject_heights(
+    used = fn(
         ctypes.byref(g), echoes.ctypes.data if echoes.size else None,
         pos.ctypes.data if pos.size else None, hts.ctypes.data,
         pix.ctypes.data if pix.size else None, pix.size, out.ctypes.data if out.size else None,

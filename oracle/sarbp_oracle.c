@@ -161,13 +161,37 @@ static void backproject_pixel_nearest(const oracle_geometry* g, const float* ech
 
 /* One pixel of a non-planar grid: the linear-interpolation steps above with
    the pixel raised to z0 + heights[pixel]. */
+/* The geometry with the image plane moved to the height of one pixel. */
+static oracle_geometry raise_to_pixel(const oracle_geometry* g, const float* heights, int64_t pixel)
+{
+    oracle_geometry raised = *g;
+    raised.z0 = g->z0 + (double)heights[pixel];
+    return raised;
+}
+
 static void backproject_pixel_heights(const oracle_geometry* g, const float* echo,
                                       const double* antenna_pos, const float* heights,
                                       int64_t pixel, double* out)
 {
-    oracle_geometry raised = *g;
-    raised.z0 = g->z0 + (double)heights[pixel];
+    const oracle_geometry raised = raise_to_pixel(g, heights, pixel);
     backproject_pixel(&raised, echo, antenna_pos, NULL, pixel, out);
+}
+
+/* The same raised pixel with the windowed-sinc or nearest-sample interpolation. */
+static void backproject_pixel_heights_sinc8(const oracle_geometry* g, const float* echo,
+                                            const double* antenna_pos, const float* heights,
+                                            int64_t pixel, double* out)
+{
+    const oracle_geometry raised = raise_to_pixel(g, heights, pixel);
+    backproject_pixel_sinc8(&raised, echo, antenna_pos, NULL, pixel, out);
+}
+
+static void backproject_pixel_heights_nearest(const oracle_geometry* g, const float* echo,
+                                              const double* antenna_pos, const float* heights,
+                                              int64_t pixel, double* out)
+{
+    const oracle_geometry raised = raise_to_pixel(g, heights, pixel);
+    backproject_pixel_nearest(&raised, echo, antenna_pos, NULL, pixel, out);
 }
 
 typedef struct {
@@ -281,4 +305,26 @@ int oracle_backproject_heights(const oracle_geometry* g, const float* echo,
         return -1;
     return run_pixels(g, echo, antenna_pos, heights, pixels, npix, out, nthreads,
                       backproject_pixel_heights);
+}
+
+int oracle_backproject_heights_sinc8(const oracle_geometry* g, const float* echo,
+                                     const double* antenna_pos, const float* heights,
+                                     const int64_t* pixels, int64_t npix, double* out,
+                                     int nthreads)
+{
+    if (g && g->nx > 0 && g->ny > 0 && !heights)
+        return -1;
+    return run_pixels(g, echo, antenna_pos, heights, pixels, npix, out, nthreads,
+                      backproject_pixel_heights_sinc8);
+}
+
+int oracle_backproject_heights_nearest(const oracle_geometry* g, const float* echo,
+                                       const double* antenna_pos, const float* heights,
+                                       const int64_t* pixels, int64_t npix, double* out,
+                                       int nthreads)
+{
+    if (g && g->nx > 0 && g->ny > 0 && !heights)
+        return -1;
+    return run_pixels(g, echo, antenna_pos, heights, pixels, npix, out, nthreads,
+                      backproject_pixel_heights_nearest);
 }

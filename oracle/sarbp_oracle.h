@@ -76,6 +76,16 @@ int oracle_backproject_heights(const oracle_geometry* g, const float* echo,
                                const double* antenna_pos, const float* heights,
                                const int64_t* pixels, int64_t npix, double* out, int nthreads);
 
+/* The height map with the windowed-sinc or nearest-sample interpolation. */
+int oracle_backproject_heights_sinc8(const oracle_geometry* g, const float* echo,
+                                     const double* antenna_pos, const float* heights,
+                                     const int64_t* pixels, int64_t npix, double* out,
+                                     int nthreads);
+int oracle_backproject_heights_nearest(const oracle_geometry* g, const float* echo,
+                                       const double* antenna_pos, const float* heights,
+                                       const int64_t* pixels, int64_t npix, double* out,
+                                       int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

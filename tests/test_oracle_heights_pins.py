@@ -91,6 +91,28 @@ def test_height_pin(pin):
     assert ok, detail
 
 
+@pytest.mark.parametrize("interp", ["sinc8", "nearest"])
+def test_interpolation_variants_reduce_to_the_planar_ones(interp):
+    """Zero heights give the planar variant bit for bit; a constant height gives
+    the planar variant on the raised plane; a mixed map gives each pixel the
+    planar value of its own height."""
+    params, echo, pos, _, _ = _scene()
+    ny, nx = params["ny"], params["nx"]
+    zero = np.zeros((ny, nx), dtype=np.float32)
+    assert np.array_equal(oracle.backproject_heights(params, echo, pos, zero, interp=interp),
+                          oracle.backproject(params, echo, pos, interp=interp))
+    const = np.full((ny, nx), 7.25, dtype=np.float32)
+    assert np.array_equal(oracle.backproject_heights(params, echo, pos, const, interp=interp),
+                          oracle.backproject(dict(params, z0=params["z0"] + 7.25), echo, pos,
+                                             interp=interp))
+    mixed = np.where((np.arange(ny)[:, None] + np.arange(nx)[None, :]) % 2 == 0, 0.0, 3.5)
+    mixed = mixed.astype(np.float32)
+    got = oracle.backproject_heights(params, echo, pos, mixed, interp=interp)
+    raised = oracle.backproject(dict(params, z0=params["z0"] + 3.5), echo, pos, interp=interp)
+    flat = oracle.backproject(params, echo, pos, interp=interp)
+    assert np.array_equal(got, np.where(mixed == 0, flat, raised))
+
+
 SRC = os.path.join(os.path.dirname(oracle.__file__), "sarbp_oracle.c")
 HDR = os.path.join(os.path.dirname(oracle.__file__), "sarbp_oracle.h")
 MUTATIONS = {
