@@ -480,8 +480,8 @@ sarbp_status sarbp_plan_heights(sarbp_plan_t* out, const sarbp_params* p, double
     if (!out)
         return SARBP_ERR_INVALID_ARG;
     *out = nullptr;
-    if (!p || (p->flags & (SARBP_SINC8 | SARBP_NEAREST)))
-        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
+    if (!p)
+        return SARBP_ERR_INVALID_ARG;
     if (!(isfin(h_min) && isfin(h_max) && h_min <= h_max))
         return SARBP_ERR_INVALID_ARG;
     return plan_create(out, p, 1, h_min, h_max);
@@ -638,8 +638,6 @@ sarbp_status sarbp_backproject_heights(sarbp_plan_t plan, void* image, const voi
     st = check_geometry(params);
     if (st != SARBP_OK)
         return st;
-    if (params->flags & (SARBP_SINC8 | SARBP_NEAREST))
-        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
     const sarbp_params& q = plan->p;
     if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
         params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || !plan->heights_mode)

@@ -54,7 +54,10 @@ namespace {
 constexpr float MAGIC = 12582912.0f;   // 1.5 * 2^23: adding it leaves floor/round(x) in the mantissa
 constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 
-enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3 };
+enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3,
+                    INTERP_HEIGHTS_SINC8 = 4, INTERP_HEIGHTS_NEAREST = 5 };
+// pixels on a height map, with the linear, windowed-sinc or nearest interpolation
+__host__ __device__ constexpr bool on_heights(int interp) { return interp >= INTERP_HEIGHTS; }
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr int HROW2 = TILE_X / 2 + 1;      // float2 pairs per row of a tile's heights (padded)
 
@@ -291,7 +294,7 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
                                                   const float4* row, float jf, float jf2,
                                                   float jf3, float jf4)
 {
-    if (INTERP == INTERP_HEIGHTS) {
+    if (on_heights(INTERP)) {
         PulseState st;
         st.mode = __float_as_int(rec.d.w) == REC_SKIP ? MODE_SKIP : MODE_EXACT;
         return st;
@@ -927,9 +930,11 @@ __device__ __forceinline__ F2 f2_sqrt(F2 a)
 }
 
 // Returns false (and leaves the sums untouched) when the series does not apply.
+template <int INTERP>
 __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Record& rec,
                                                      const float4* row, const HRow& hr,
                                                      const float2* s_h2,
+                                                     const float2* __restrict__ psi,
                                                      float2 (&accre)[NP], float2 (&accim)[NP])
 {
     // reference vector: tile centre -> row centre -> row height
@@ -981,6 +986,18 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
         const float2 s = __ffma2_rn(dz, __fadd2_rn(dz, two_vz), sx);
         const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12);
         const float2 ub = __ffma2_rn(s, poly, f0);
+        if (INTERP != INTERP_HEIGHTS) {
+            // windowed sinc or nearest sample at this range, bounds checked
+            const int bin0 = __float_as_int(rec.d.y);
+            if (INTERP == INTERP_HEIGHTS_SINC8) {
+                sinc_pixel<true>(k, ub.x, kbase, bin0, row, psi, accre[q].x, accim[q].x);
+                sinc_pixel<true>(k, ub.y, kbase, bin0, row, psi, accre[q].y, accim[q].y);
+            } else {
+                nearest_pixel<true>(k, ub.x, kbase, bin0, row, psi, accre[q].x, accim[q].x);
+                nearest_pixel<true>(k, ub.y, kbase, bin0, row, psi, accre[q].y, accim[q].y);
+            }
+            continue;
+        }
         const float2 tt = __fadd2_rd(ub, mm);
         const float2 f = __ffma2_rn(__fadd2_rn(tt, nmm), neg1, ub);
         const float2 x = __fmul2_rn(f, cc);
@@ -1004,11 +1021,13 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
 
 // The fallback: float64 range to the row's reference point, then
 // R - R_row = s / (R_row + R) in float32, bounds on every table index.
+template <int INTERP>
 __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Record& rec,
                                                     const float4* row, const double* __restrict__ a,
                                                     double xc, double yrow, const HRow& hr,
-                                                    const float2* s_h2, float2 (&accre)[NP],
-                                                    float2 (&accim)[NP])
+                                                    const float2* s_h2,
+                                                    const float2* __restrict__ psi,
+                                                    float2 (&accre)[NP], float2 (&accim)[NP])
 {
     const double vx = xc - a[0], vy = yrow - a[1], vz = hr.zrow - a[2];
     const double r2 = vx * vx + vy * vy + vz * vz;
@@ -1032,6 +1051,15 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
         const float den = rf + rp;
         const float dr_m = den > 0.0f ? s / den : 0.0f;
         const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
+        if (INTERP != INTERP_HEIGHTS) {
+            float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
+            float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
+            if (INTERP == INTERP_HEIGHTS_SINC8)
+                sinc_pixel<true>(k, ub, kbase, __float_as_int(rec.d.y), row, psi, re, im);
+            else
+                nearest_pixel<true>(k, ub, kbase, __float_as_int(rec.d.y), row, psi, re, im);
+            continue;
+        }
         if (!(ub > -1.0e6f && ub < 1.0e6f))
             continue;
         const float kf = floorf(ub);
@@ -1058,9 +1086,10 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    if (INTERP == INTERP_HEIGHTS) {
-        if (st.mode == MODE_EXACT && !heights_series_pulse(k, rec, row, hr, s_h2, accre, accim))
-            heights_exact_pulse(k, rec, row, a, xc, yrow, hr, s_h2, accre, accim);
+    if (on_heights(INTERP)) {
+        if (st.mode == MODE_EXACT &&
+            !heights_series_pulse<INTERP>(k, rec, row, hr, s_h2, psi, accre, accim))
+            heights_exact_pulse<INTERP>(k, rec, row, a, xc, yrow, hr, s_h2, psi, accre, accim);
         return;
     }
     if (INTERP == INTERP_NEAREST) {
@@ -1132,7 +1161,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
 
         const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
         HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0};
-        if (INTERP == INTERP_HEIGHTS) {
+        if (on_heights(INTERP)) {
             // the thread's own row of the tile, heights clamped to the plan's
             // bounds; pixels outside the image repeat the last row or column
             // (their results are never stored)
@@ -1355,15 +1384,28 @@ constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW2 * sizeof(float2);
 
 cudaError_t prepare_heights_kernel()
 {
-    return cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)HEIGHTS_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)HEIGHTS_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS_SINC8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)HEIGHTS_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS_NEAREST>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)HEIGHTS_SMEM);
+    return e;
 }
 
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
                                const int* klo, float2* image, float4* partial,
                                const float2* psi, const float* heights, cudaStream_t s)
 {
-    if (k.heights_mode)
+    if (k.heights_mode && (k.flags & FLAG_SINC8))
+        bp_kernel<INTERP_HEIGHTS_SINC8><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(
+            k, pos, table, klo, image, partial, psi, heights);
+    else if (k.heights_mode && (k.flags & FLAG_NEAREST))
+        bp_kernel<INTERP_HEIGHTS_NEAREST><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(
+            k, pos, table, klo, image, partial, psi, heights);
+    else if (k.heights_mode)
         bp_kernel<INTERP_HEIGHTS><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(k, pos, table, klo, image,
                                                                        partial, psi, heights);
     else if (k.flags & FLAG_SINC8)

@@ -164,13 +164,14 @@ class Plan:
         return volume
 
     def backproject_heights(self, image, echoes, antenna_pos, heights, params=None,
-                            accumulate=False, stream=None):
-        """Linear-interpolation backprojection of pixels raised to z0 + heights[iy, ix].
+                            accumulate=False, stream=None, interp="linear"):
+        """Backprojection of pixels raised to z0 + heights[iy, ix].
 
-        heights float32 [ny, nx] on the device, clamped to the plan's height range.
+        heights float32 [ny, nx] on the device, clamped to the plan's height range;
+        ``interp``: "linear", "sinc8" or "nearest".
         """
         import torch
-        p = _params(params if params is not None else self.params, accumulate)
+        p = _params(params if params is not None else self.params, accumulate, interp)
         img = _check_device_tensor(image, "image", torch.complex64, (p.ny, p.nx))
         ech = _check_device_tensor(echoes, "echoes", torch.complex64, (p.na, p.nr))
         pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))

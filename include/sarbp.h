@@ -206,13 +206,12 @@ sarbp_status sarbp_backproject_volume(sarbp_plan_t plan, void* volume, const voi
  * have to take terrain elevation into account; the page gives no formula, so
  * this is the plain reading): pixel (ix, iy) sits at
  *   (x0 + ix*dx, y0 + iy*dy, z0 + heights[iy*nx + ix])
- * and the sum is otherwise that of sarbp_backproject with linear interpolation.
+ * and the sum is otherwise that of sarbp_backproject.
  *
  * sarbp_plan_heights - as sarbp_plan, for heights within [h_min, h_max]
  * (metres, added to z0). The table rows cover the slab z0 + [h_min, h_max]
  * over the image, so W grows with h_max - h_min. SARBP_ERR_INVALID_ARG as for
- * sarbp_plan, and also for SARBP_SINC8 / SARBP_NEAREST in p->flags and for
- * non-finite bounds or h_min > h_max.
+ * sarbp_plan, and also for non-finite bounds or h_min > h_max.
  */
 sarbp_status sarbp_plan_heights(sarbp_plan_t* out, const sarbp_params* p, double h_min,
                                 double h_max);
@@ -224,8 +223,8 @@ sarbp_status sarbp_plan_heights(sarbp_plan_t* out, const sarbp_params* p, double
  *          read during the work on `stream`. Each value is clamped to the
  *          plan's [h_min, h_max] (a NaN height is taken as h_min).
  * image, echoes, antenna_pos, params, stream: as for sarbp_backproject
- * (SARBP_ACCUMULATE allowed; SARBP_SINC8 / SARBP_NEAREST rejected with
- * SARBP_ERR_INVALID_ARG). The plan must come from sarbp_plan_heights, and
+ * (SARBP_ACCUMULATE, SARBP_SINC8 and SARBP_NEAREST included). The plan must
+ * come from sarbp_plan_heights, and
  * plans from sarbp_plan_heights are refused by sarbp_backproject and
  * sarbp_backproject_host (SARBP_ERR_PLAN_MISMATCH either way).
  *
