@@ -11,6 +11,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <limits>
 #include <new>
@@ -332,7 +333,35 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
 
 }  // namespace
 
+namespace sarbp {
+
+namespace {
+std::atomic<int> g_fail_countdown{0};
+}
+
+cudaError_t device_alloc(void** ptr, size_t bytes)
+{
+    int c = g_fail_countdown.load();
+    while (c > 0) {
+        if (g_fail_countdown.compare_exchange_weak(c, c - 1)) {
+            if (c == 1) {
+                *ptr = nullptr;
+                return cudaErrorMemoryAllocation;   // the injected failure
+            }
+            break;
+        }
+    }
+    return cudaMalloc(ptr, bytes);
+}
+
+}  // namespace sarbp
+
 extern "C" {
+
+void sarbp_debug_fail_alloc(int32_t countdown)
+{
+    sarbp::g_fail_countdown.store(countdown > 0 ? countdown : 0);
+}
 
 const char* sarbp_status_string(sarbp_status status)
 {
@@ -445,7 +474,7 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
                           reinterpret_cast<void**>(&plan->partial),
                           reinterpret_cast<void**>(&plan->psi)};
         for (int i = 0; i < 4; ++i) {
-            e = cudaMalloc(ptrs[i], sizes[i]);
+            e = device_alloc(ptrs[i], sizes[i]);
             if (e != cudaSuccess) {
                 st = cuda_fail(plan, e, "cudaMalloc");
                 free_plan(plan);
@@ -705,11 +734,11 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (img_bytes && !plan->d_image)
-        e = cudaMalloc(&plan->d_image, img_bytes);
+        e = device_alloc(&plan->d_image, img_bytes);
     if (e == cudaSuccess && params->na > 0 && !plan->d_pos)
-        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
+        e = device_alloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
     if (e == cudaSuccess && band_hi >= band_lo && !plan->d_echo)
-        e = cudaMalloc(&plan->d_echo, (size_t)params->na * params->nr * 8);
+        e = device_alloc(&plan->d_echo, (size_t)params->na * params->nr * 8);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMalloc (host staging)");
 
@@ -787,14 +816,14 @@ sarbp_status sarbp_backproject_streamed(sarbp_plan_t plan, void* image, const vo
     const int chunk = std::max(1, std::min(chunk_pulses, std::max(params->na, 1)));
     const size_t stage_need = (size_t)chunk * (size_t)params->nr * 8;
     if (img_bytes && !plan->d_image)
-        e = cudaMalloc(&plan->d_image, img_bytes);
+        e = device_alloc(&plan->d_image, img_bytes);
     if (e == cudaSuccess && params->na > 0 && !plan->d_pos)
-        e = cudaMalloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
+        e = device_alloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
     if (e == cudaSuccess && stage_need > plan->stage_bytes) {
         for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
             cudaFree(plan->d_stage[b]);
             plan->d_stage[b] = nullptr;
-            e = cudaMalloc(&plan->d_stage[b], stage_need);
+            e = device_alloc(&plan->d_stage[b], stage_need);
         }
         plan->stage_bytes = e == cudaSuccess ? stage_need : 0;
     }

@@ -78,6 +78,11 @@ cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);
 
+// Every device allocation of the library goes through here, so that tests can
+// make one of them fail on the host (sarbp_debug_fail_alloc) without touching
+// the GPU.
+cudaError_t device_alloc(void** ptr, size_t bytes);
+
 // Device address of the fixed scratch array used by sarbp_backproject_noalloc
 // (looked up once per device, with that device current).
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(16) << 20;

@@ -596,9 +596,9 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     // computed in float64 and rounded once
     const size_t tw_entries = 4 * (size_t)plan->n;
     if (e == cudaSuccess)
-        e = cudaMalloc(&plan->tw, tw_entries * sizeof(float2));
+        e = sarbp::device_alloc(reinterpret_cast<void**>(&plan->tw), tw_entries * sizeof(float2));
     if (e == cudaSuccess)
-        e = cudaMalloc(&plan->h, (size_t)plan->n * sizeof(float2));
+        e = sarbp::device_alloc(reinterpret_cast<void**>(&plan->h), (size_t)plan->n * sizeof(float2));
     if (e == cudaSuccess) {
         std::vector<float2> tw(tw_entries, make_float2(0.f, 0.f));
         const double pi = 3.14159265358979323846;

@@ -244,6 +244,16 @@ sarbp_status sarbp_host_transfer_bytes(sarbp_plan_t plan, uint64_t* h2d, uint64_
    must make sure no work that uses the plan is still running. */
 sarbp_status sarbp_destroy(sarbp_plan_t plan);
 
+/*
+ * Testing aid (host-side failure injection): the countdown-th device
+ * allocation the library makes from now on (plans, host-call staging,
+ * range-compression plans) fails as if cudaMalloc had returned
+ * cudaErrorMemoryAllocation, without touching the GPU; 0 disables. The call
+ * that meets the failure returns SARBP_ERR_OOM and frees what it had
+ * allocated. Process-wide, not meant for production use.
+ */
+void sarbp_debug_fail_alloc(int32_t countdown);
+
 /* Static, never-NULL description of a status code. */
 const char* sarbp_status_string(sarbp_status status);
 
