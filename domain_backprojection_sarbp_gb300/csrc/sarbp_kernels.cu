@@ -59,6 +59,7 @@ enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INT
 // pixels on a height map, with the linear, windowed-sinc or nearest interpolation
 __host__ __device__ constexpr bool on_heights(int interp) { return interp >= INTERP_HEIGHTS; }
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
+constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
 constexpr int HROW2 = TILE_X / 2 + 1;      // float2 pairs per row of a tile's heights (padded)
 
 struct __align__(16) Record {
@@ -333,11 +334,17 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     if (INTERP == INTERP_SINC8 && kind == REC_FAST) {
         // windowed sinc: when the thread's pixels span at most a quarter bin and
         // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
-        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN)
-        const int kabs0 = idx0 - bin0;
-        if (hi_u - lo_u <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1) {
+        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN). The
+        // interval is widened to at least 1/32 bin so that the monomial
+        // coefficients in u - mid stay bounded.
+        const float mid = 0.5f * (lo_u + hi_u);
+        const float lo_e = fminf(lo_u, mid - SINC_HALF_MIN), hi_e = fmaxf(hi_u, mid + SINC_HALF_MIN);
+        const float tke = __fadd_rd(lo_e, MAGIC);
+        const float k0e = tke - MAGIC;
+        const int kabs0 = kb + (__float_as_int(tke) - MAGIC_BITS) - bin0;
+        if (hi_e - lo_e <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1) {
             st.mode = MODE_POLY;
-            st.t0 = make_float4(lo_u, hi_u, k0, __int_as_float(kabs0));
+            st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
         }
     }
     if (st.mode != MODE_POLY)
@@ -513,6 +520,84 @@ __device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec,
 // ---------------------------------------------------------------------------
 // One pixel at row position ub (relative to row index kb). CHECK_ROW adds
 // bounds on the table row for the exact path.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// sin(pi y) / pi for y in [0, 1], accurate relative to its value near both
+// ends: y folds to z = min(y, 1 - y) (1 - y is exact for y >= 1/2) and
+// sin(pi z) / pi = z sum_n (-1)^n (pi z)^(2n) / (2n + 1)! is summed to n = 5;
+// the first dropped term is 6e-8 of the value at z = 1/2.
+__device__ __forceinline__ float sinpi_over_pi(float y)
+{
+    const float z = fminf(y, 1.0f - y);
+    const float s = z * z;
+    float t = fmaf(s, -2.34608104e-3f, 2.61478478e-2f);   // -pi^10 / 11!, pi^8 / 9!
+    t = fmaf(s, t, -0.190751824f);                          // -pi^6 / 7!
+    t = fmaf(s, t, 0.811742425f);                           // pi^4 / 5!
+    t = fmaf(s, t, -1.64493407f);                           // -pi^2 / 3!
+    t = fmaf(s, t, 1.0f);
+    return z * t;
+}
+
+// 8-tap windowed sinc at u = k + f (f in [0, 1)):
+//   G = sum_{d=-3..4} e_{k+d} h(f - d),  h(t) = sin(pi t) / (pi t) (1 + cos(pi t / 4)) / 2,
+// with p at entry k - 3 of a row of sample pairs (e_m, e_{m+1}); no phase.
+// Since sin(pi (f - d)) = (-1)^d sin(pi f), G = sin(pi f) / pi times
+// sum_d (-1)^d w_d e_{k+d} / (f - d). The reciprocals pair up:
+// (f - d)(f - 1 + d) = g - d (d - 1) with g = f (f - 1), so
+// 1 / (f - d) = (f - 1 + d) / (g - d (d - 1)) and four reciprocals serve the
+// eight taps. f is held in [1e-7, 1 - 1e-7] so that no f - d is 0 (the
+// fraction can round to exactly 1 for tiny negative u); the weights are
+// continuous in f, so the clamp changes them by less than 1e-6.
+__device__ __forceinline__ float2 sinc_sum(float f, const float4* p)
+{
+    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
+    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
+    const float fm1 = fc - 1.0f;
+    const float g = fc * fm1;
+    const float r0 = rcp_approx(g);              // 1 / (f (f - 1))
+    const float r1 = rcp_approx(g - 2.0f);       // 1 / ((f + 1)(f - 2))
+    const float r2 = rcp_approx(g - 6.0f);       // 1 / ((f + 2)(f - 3))
+    const float r3 = rcp_approx(g - 12.0f);      // 1 / ((f + 3)(f - 4))
+    // (-1)^d / (f - d), taps d = -3 .. 4
+    const float a0 = (4.0f - fc) * r3;
+    const float a1 = (fc - 3.0f) * r2;
+    const float a2 = (2.0f - fc) * r1;
+    const float a3 = fm1 * r0;
+    const float a4 = -fc * r0;
+    const float a5 = (fc + 1.0f) * r1;
+    const float a6 = -(fc + 2.0f) * r2;
+    const float a7 = (fc + 3.0f) * r3;
+    // (1 + cos(pi (f - d) / 4)) / 2 from cos and sin of pi f / 4 and of pi d / 4
+    float s4, c4;
+    __sincosf(0.785398163f * fc, &s4, &c4);
+    constexpr float H = 0.353553391f;                            // sqrt(2) / 4
+    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));           // d = -3
+    const float w1 = fmaf(-s4, 0.5f, 0.5f);                      // d = -2
+    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));            // d = -1
+    const float w3 = fmaf(c4, 0.5f, 0.5f);                       // d = 0
+    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));             // d = 1
+    const float w5 = fmaf(s4, 0.5f, 0.5f);                       // d = 2
+    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));            // d = 3
+    const float w7 = fmaf(c4, -0.5f, 0.5f);                      // d = 4
+    const float h0 = a0 * w0, h1 = a1 * w1, h2 = a2 * w2, h3 = a3 * w3;
+    const float h4 = a4 * w4, h5 = a5 * w5, h6 = a6 * w6, h7 = a7 * w7;
+    float sre = h0 * s0.x, sim = h0 * s0.y;
+    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
+    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
+    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
+    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
+    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
+    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
+    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
+    const float sf = sinpi_over_pi(fc);
+    return make_float2(sre * sf, sim * sf);
+}
+
 template <bool CHECK_ROW>
 __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, int bin0,
                                            const float4* row, const float2* __restrict__ psi,
@@ -528,59 +613,14 @@ __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, i
         return;                                 // stencil reaches outside the recorded range
     if (CHECK_ROW && (kr < 3 || kr + 3 > k.W - 1))
         return;
-    const float4* p = row + (kr - 3);
-    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
     const float2 ps = __ldg(psi + kabs);
-
-    // f + d for d = 3 .. -4. f in [1e-7, 1 - 1e-7] keeps every f + d off 0 (the
-    // fraction can round to exactly 1 for tiny negative u); the weights are
-    // continuous in f, so the clamp changes them by less than 1e-6.
-    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
-    const float x0 = fc + 3.0f, x1 = fc + 2.0f, x2 = fc + 1.0f, x3 = fc;
-    const float x4 = fc - 1.0f, x5 = fc - 2.0f, x6 = fc - 3.0f, x7 = fc - 4.0f;
-    const float a1 = x0 * x1, a2 = a1 * x2, a3 = a2 * x3, a4 = a3 * x4, a5 = a4 * x5,
-                a6 = a5 * x6, a7 = a6 * x7;
-    float r = __fdividef(1.0f, a7);
-    const float i7 = r * a6; r *= x7;
-    const float i6 = r * a5; r *= x6;
-    const float i5 = r * a4; r *= x5;
-    const float i4 = r * a3; r *= x4;
-    const float i3 = r * a2; r *= x3;
-    const float i2 = r * a1; r *= x2;
-    const float i1 = r * x0;
-    const float i0 = r * x1;
-    // sin(pi f) / pi with relative accuracy: the centre weight divides it by f
-    const float sf = sinpif(fc) * 0.318309886f;
-    float s4, c4;
-    __sincosf(0.785398163f * fc, &s4, &c4);                     // pi f / 4
-    // (1 + cos(pi (f + d) / 4)) / 2 with cos(pi d/4), sin(pi d/4) for d = 3 .. -4
-    constexpr float H = 0.353553391f;                            // sqrt(2) / 4
-    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));           // d = 3
-    const float w1 = fmaf(-s4, 0.5f, 0.5f);                      // d = 2
-    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));            // d = 1
-    const float w3 = fmaf(c4, 0.5f, 0.5f);                       // d = 0
-    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));             // d = -1
-    const float w5 = fmaf(s4, 0.5f, 0.5f);                       // d = -2
-    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));            // d = -3
-    const float w7 = fmaf(c4, -0.5f, 0.5f);                      // d = -4
-    // (-1)^d: d = 3, 1, -1, -3 are odd
-    const float h0 = -sf * i0 * w0, h1 = sf * i1 * w1, h2 = -sf * i2 * w2, h3 = sf * i3 * w3;
-    const float h4 = -sf * i4 * w4, h5 = sf * i5 * w5, h6 = -sf * i6 * w6, h7 = sf * i7 * w7;
-
-    float sre = h0 * s0.x, sim = h0 * s0.y;
-    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
-    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
-    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
-    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
-    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
-    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
-    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
+    const float2 gsum = sinc_sum(f, row + (kr - 3));
     float sn, cs;
     __sincosf(f * k.c_phase, &sn, &cs);
     const float zr = ps.x * cs - ps.y * sn;
     const float zi = ps.x * sn + ps.y * cs;
-    re = fmaf(sre, zr, fmaf(-sim, zi, re));
-    im = fmaf(sre, zi, fmaf(sim, zr, im));
+    re = fmaf(gsum.x, zr, fmaf(-gsum.y, zi, re));
+    im = fmaf(gsum.x, zi, fmaf(gsum.y, zr, im));
 }
 
 // Windowed-sinc interpolant G(u) = sum_m e_m h(u - m) at one position ub
@@ -591,52 +631,15 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
     const float tt = __fadd_rd(ub, MAGIC);
     const float f = ub - (tt - MAGIC);
     const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
-    const float4* p = row + (kr - 3);
-    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
-    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
-    const float x0 = fc + 3.0f, x1 = fc + 2.0f, x2 = fc + 1.0f, x3 = fc;
-    const float x4 = fc - 1.0f, x5 = fc - 2.0f, x6 = fc - 3.0f, x7 = fc - 4.0f;
-    const float a1 = x0 * x1, a2 = a1 * x2, a3 = a2 * x3, a4 = a3 * x4, a5 = a4 * x5,
-                a6 = a5 * x6, a7 = a6 * x7;
-    float r = __fdividef(1.0f, a7);
-    const float i7 = r * a6; r *= x7;
-    const float i6 = r * a5; r *= x6;
-    const float i5 = r * a4; r *= x5;
-    const float i4 = r * a3; r *= x4;
-    const float i3 = r * a2; r *= x3;
-    const float i2 = r * a1; r *= x2;
-    const float i1 = r * x0;
-    const float i0 = r * x1;
-    const float sf = sinpif(fc) * 0.318309886f;
-    float s4, c4;
-    __sincosf(0.785398163f * fc, &s4, &c4);
-    constexpr float H = 0.353553391f;
-    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));
-    const float w1 = fmaf(-s4, 0.5f, 0.5f);
-    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));
-    const float w3 = fmaf(c4, 0.5f, 0.5f);
-    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));
-    const float w5 = fmaf(s4, 0.5f, 0.5f);
-    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));
-    const float w7 = fmaf(c4, -0.5f, 0.5f);
-    const float h0 = -sf * i0 * w0, h1 = sf * i1 * w1, h2 = -sf * i2 * w2, h3 = sf * i3 * w3;
-    const float h4 = -sf * i4 * w4, h5 = sf * i5 * w5, h6 = -sf * i6 * w6, h7 = sf * i7 * w7;
-    float sre = h0 * s0.x, sim = h0 * s0.y;
-    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
-    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
-    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
-    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
-    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
-    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
-    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
-    return make_float2(sre, sim);
+    return sinc_sum(f, row + (kr - 3));
 }
 
 // All of the thread's pixels within SINC_SPAN bins, every stencil inside the
 // recorded range. G(u) is smooth (a sum of eight windowed sincs), so over the
-// interval [lo_u, hi_u] it is interpolated at the five Chebyshev nodes
-// mid + half cos((2i+1) pi / 10) by a degree-4 polynomial in
-// t = (u - mid) / half. The interpolation error is at most
+// interval [lo_u, hi_u] (widened to a half-width of at least SINC_HALF_MIN) it
+// is interpolated at the five Chebyshev nodes mid + half cos((2i+1) pi / 10)
+// by a degree-4 polynomial in t = (u - mid) / half, evaluated per pixel as a
+// polynomial in s = u - mid. The interpolation error is at most
 // max|G^(5)| (half)^5 / (2^4 5!) <= pi^5 |e| 8 (1/8)^5 / 1920 ~ 4e-5 |e| for
 // half <= 1/8. The echo phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0))
 // is applied per pixel; psi_k0 is folded into the coefficients.
@@ -666,29 +669,36 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
                        fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
     p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
                        fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
+    // coefficients in s = u - mid (t = s / half), psi_k0 folded in
     const float2 ps = __ldg(psi + kabs0);
+    const float ih = rcp_approx(half);            // half >= SINC_HALF_MIN
     float2 pr[5], pi[5];
+    float sc = 1.0f;
 #pragma unroll
     for (int n = 0; n < 5; ++n) {
-        const float re = p[n].x * ps.x - p[n].y * ps.y;
-        const float im = p[n].x * ps.y + p[n].y * ps.x;
+        const float psr = ps.x * sc, psi_ = ps.y * sc;
+        const float re = p[n].x * psr - p[n].y * psi_;
+        const float im = p[n].x * psi_ + p[n].y * psr;
         pr[n] = make_float2(re, re);
         pi[n] = make_float2(im, im);
+        sc *= ih;
     }
-    const float ih = half > 1.0e-7f ? 1.0f / half : 0.0f;
-    const float2 ih2 = make_float2(ih, ih), nm2 = make_float2(-mid * ih, -mid * ih);
+    // echo phase c (u - k0) = c s + c (mid - k0)
     const float c = k.c_phase;
-    const float2 c2 = make_float2(c, c), nk0c = make_float2(-k0 * c, -k0 * c);
+    const float2 c2 = make_float2(c, c);
+    const float cm = c * (mid - k0);
+    const float2 cm2 = make_float2(cm, cm);
+    const float s0 = st.q0.x - mid;
+    const float2 q0s = make_float2(s0, s0);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 u = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        const float2 sv = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), q0s);
         id = __fadd2_rn(id, one);
-        const float2 t = __ffma2_rn(u, ih2, nm2);
-        const float2 gr = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pr[4], t, pr[3]), t, pr[2]), t, pr[1]), t, pr[0]);
-        const float2 gi = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pi[4], t, pi[3]), t, pi[2]), t, pi[1]), t, pi[0]);
-        const float2 x = __ffma2_rn(u, c2, nk0c);
+        const float2 gr = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pr[4], sv, pr[3]), sv, pr[2]), sv, pr[1]), sv, pr[0]);
+        const float2 gi = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pi[4], sv, pi[3]), sv, pi[2]), sv, pi[1]), sv, pi[0]);
+        const float2 x = __ffma2_rn(sv, c2, cm2);
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
         __sincosf(x.y, &sb, &cb);
