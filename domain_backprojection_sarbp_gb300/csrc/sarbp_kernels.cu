@@ -60,7 +60,7 @@ enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INT
 __host__ __device__ constexpr bool on_heights(int interp) { return interp >= INTERP_HEIGHTS; }
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
-constexpr int HROW2 = TILE_X / 2 + 1;      // float2 pairs per row of a tile's heights (padded)
+constexpr int HROW4 = TILE_X / 2 + 1;      // float4 per row of a tile's height terms (padded)
 
 struct __align__(16) Record {
     float4 a;  // c00 (fraction of the tile-centre bin), c01 hi, c01 lo, c02
@@ -887,6 +887,8 @@ struct HRow {
     float qm;      // largest |q| over the row's pixels
     float jy;      // row offset from the tile centre, in pixels
     double zrow;   // z0 + hrow
+    float dz_lo, dz_hi;   // range of h - hrow over the row's pixels
+    float p_lo, p_hi;     // range of (i dx)^2 + (h - hrow)^2
 };
 
 struct F2 {
@@ -940,44 +942,17 @@ __device__ __forceinline__ F2 f2_sqrt(F2 a)
 }
 
 // Returns false (and leaves the sums untouched) when the series does not apply.
-template <int INTERP>
-__device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Record& rec,
-                                                     const float4* row, const HRow& hr,
-                                                     const float2* s_h2,
-                                                     const float2* __restrict__ psi,
-                                                     float2 (&accre)[NP], float2 (&accim)[NP])
+// One pulse of the range series over the thread's pixels (see
+// heights_series_pulse); DEG4 keeps the s^4 term.
+template <int INTERP, bool DEG4>
+__device__ __forceinline__ void heights_series_loop(const BpConst& k, const float4* row,
+                                                    const float4* s_hp,
+                                                    const float2* __restrict__ psi, int kbase,
+                                                    int bin0, float frac, float ax, float two_vz, float hb,
+                                                    float g, float2 (&accre)[NP],
+                                                    float2 (&accim)[NP])
 {
-    // reference vector: tile centre -> row centre -> row height
-    const F2 vx = {rec.a.x, rec.a.y};
-    const F2 yo = f2_add(two_prod(hr.jy, k.dy_f), two_prod(hr.jy, k.dy_lo));
-    const F2 vy = f2_add({rec.a.z, rec.a.w}, yo);
-    const F2 vz = f2_add({rec.b.x, rec.b.y}, {hr.hrow, 0.0f});
-    const F2 r2 = f2_add(f2_add(f2_sqr(vx), f2_sqr(vy)), f2_sqr(vz));
-    const F2 r = f2_sqrt(r2);
-    const F2 u = f2_mul(f2_add(r, {-k.r0_hi, -k.r0_lo}), {k.idr_hi, k.idr_lo});
-    if (!(fabsf(u.hi) < 1.0e7f))
-        return true;                              // far outside any window: nothing to add
-    float ku = floorf(u.hi);
-    float frac = __fadd_rn(__fsub_rn(u.hi, ku), u.lo);
-    const float kf = floorf(frac);                // -1, 0 or 1 after the lo part
-    ku += kf;
-    frac -= kf;
-    const float R = r.hi;
-    const float t_bound = hr.qm * (2.0f * R + hr.qm) / (R * R);
-    if (!(t_bound <= 0.01f))
-        return false;
-    const int kbase = (int)ku + __float_as_int(rec.d.y);
-    const float inv_r = __fdiv_rn(1.0f, R);
-    const float g = inv_r * inv_r;                // 1 / R^2
-    const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
-
-    // s = q_x (2 v_x + q_x) + dz (2 v_z + dz) with q_x = i dx, i.e.
-    // i (2 v_x dx + i dx^2) + dz (2 v_z + dz); the series times hb is the
-    // polynomial a1 s + a2 s^2 + a3 s^3 + a4 s^4 with a_n = hb g^(n-1) c_n
-    const float ax = 2.0f * vx.hi * k.dx_f, bx = k.dx_f * k.dx_f;
-    const float2 ax2 = make_float2(ax, ax), bx2 = make_float2(bx, bx);
-    const float2 two_vz = make_float2(2.0f * vz.hi, 2.0f * vz.hi);
-    const float2 hrw = make_float2(-hr.hrow, -hr.hrow);
+    const float2 ax2 = make_float2(ax, ax), tvz2 = make_float2(two_vz, two_vz);
     const float a1 = hb, a2 = -0.25f * hb * g, a3 = 0.125f * hb * g * g,
                 a4 = -0.078125f * hb * g * g * g;
     const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
@@ -990,15 +965,15 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
     const int wmax = k.W - 1;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 sx = __fmul2_rn(id, __ffma2_rn(id, bx2, ax2));
+        const float4 hp = s_hp[q];
+        const float2 s = __ffma2_rn(id, ax2, __ffma2_rn(make_float2(hp.x, hp.y), tvz2,
+                                                        make_float2(hp.z, hp.w)));
         id = __fadd2_rn(id, one);
-        const float2 dz = __fadd2_rn(s_h2[q], hrw);
-        const float2 s = __ffma2_rn(dz, __fadd2_rn(dz, two_vz), sx);
-        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12);
+        const float2 poly = DEG4 ? __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12)
+                                 : __ffma2_rn(__ffma2_rn(a32, s, a22), s, a12);
         const float2 ub = __ffma2_rn(s, poly, f0);
         if (INTERP != INTERP_HEIGHTS) {
             // windowed sinc or nearest sample at this range, bounds checked
-            const int bin0 = __float_as_int(rec.d.y);
             if (INTERP == INTERP_HEIGHTS_SINC8) {
                 sinc_pixel<true>(k, ub.x, kbase, bin0, row, psi, accre[q].x, accim[q].x);
                 sinc_pixel<true>(k, ub.y, kbase, bin0, row, psi, accre[q].y, accim[q].y);
@@ -1026,6 +1001,130 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
         accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, c, accim[q]));
         accre[q] = __ffma2_rn(__fmul2_rn(wi, sn), neg1, accre[q]);
     }
+}
+
+// Linear interpolation when every pixel of the row lies in bins k0 and k0 + 1:
+// the two-entry form of hinge_pulse with x = c (u - k0) from the range series
+// (u - k0 = frac - k0 + s poly(s), folded so that x comes out of one FFMA).
+template <bool DEG4>
+__device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float4* s_hp, float4 t0,
+                                                   float4 t1, float x0, float ax, float two_vz,
+                                                   float hb, float g, float2 (&accre)[NP],
+                                                   float2 (&accim)[NP])
+{
+    const float c = k.c_phase;
+    const float2 ax2 = make_float2(ax, ax), tvz2 = make_float2(two_vz, two_vz);
+    const float a1 = c * hb, a2 = -0.25f * a1 * g, a3 = 0.125f * a1 * g * g,
+                a4 = -0.078125f * a1 * g * g * g;
+    const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
+    const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4, a4);
+    const float2 x02 = make_float2(x0, x0);
+    const float gre = 0.5f * (k.rot_re * t1.z - k.rot_im * t1.w - t0.z);
+    const float gim = 0.5f * (k.rot_re * t1.w + k.rot_im * t1.z - t0.w);
+    const float a_re = fmaf(-c, gre, t0.x), a_im = fmaf(-c, gim, t0.y);
+    const float d_re = t0.z + gre, d_im = t0.w + gim;
+    const float2 are = make_float2(a_re, a_re), aim = make_float2(a_im, a_im);
+    const float2 dre = make_float2(d_re, d_re), dim = make_float2(d_im, d_im);
+    const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
+    const float2 negc = make_float2(-c, -c);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float4 hp = s_hp[q];
+        const float2 s = __ffma2_rn(id, ax2, __ffma2_rn(make_float2(hp.x, hp.y), tvz2,
+                                                        make_float2(hp.z, hp.w)));
+        id = __fadd2_rn(id, one);
+        const float2 poly = DEG4 ? __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12)
+                                 : __ffma2_rn(__ffma2_rn(a32, s, a22), s, a12);
+        const float2 x = __ffma2_rn(s, poly, x02);
+        const float2 y = __fadd2_rn(x, negc);
+        const float2 ay = make_float2(fabsf(y.x), fabsf(y.y));
+        const float2 wr = __ffma2_rn(ay, g_re, __ffma2_rn(x, dre, are));
+        const float2 wi = __ffma2_rn(ay, g_im, __ffma2_rn(x, dim, aim));
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, cs, accre[q]);
+        accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, cs, accim[q]));
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), sn, accre[q]);
+    }
+}
+
+template <int INTERP>
+__device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Record& rec,
+                                                     const float4* row, const HRow& hr,
+                                                     const float4* s_hp,
+                                                     const float2* __restrict__ psi,
+                                                     float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    // reference vector: tile centre -> row centre -> row height
+    const F2 vx = {rec.a.x, rec.a.y};
+    const F2 yo = f2_add(two_prod(hr.jy, k.dy_f), two_prod(hr.jy, k.dy_lo));
+    const F2 vy = f2_add({rec.a.z, rec.a.w}, yo);
+    const F2 vz = f2_add({rec.b.x, rec.b.y}, {hr.hrow, 0.0f});
+    const F2 r2 = f2_add(f2_add(f2_sqr(vx), f2_sqr(vy)), f2_sqr(vz));
+    const F2 r = f2_sqrt(r2);
+    const F2 u = f2_mul(f2_add(r, {-k.r0_hi, -k.r0_lo}), {k.idr_hi, k.idr_lo});
+    if (!(fabsf(u.hi) < 1.0e7f))
+        return true;                              // far outside any window: nothing to add
+    float ku = floorf(u.hi);
+    float frac = __fadd_rn(__fsub_rn(u.hi, ku), u.lo);
+    const float kf = floorf(frac);                // -1, 0 or 1 after the lo part
+    ku += kf;
+    frac -= kf;
+    const float R = r.hi;
+    const float t_bound = hr.qm * (2.0f * R + hr.qm) / (R * R);
+    if (!(t_bound <= 0.01f))
+        return false;
+    const int bin0 = __float_as_int(rec.d.y);
+    const int kbase = (int)ku + bin0;
+    const float inv_r = __fdiv_rn(1.0f, R);
+    const float g = inv_r * inv_r;                // 1 / R^2
+    const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
+
+    // s = q_x (2 v_x + q_x) + dz (2 v_z + dz) with q_x = i dx, i.e.
+    // i (2 v_x dx) + dz (2 v_z) + P with the pulse-independent P = (i dx)^2 + dz^2
+    // held per pixel beside dz; the series times hb is the polynomial
+    // a1 s + a2 s^2 + a3 s^3 + a4 s^4 with a_n = hb g^(n-1) c_n. Its s^4 term
+    // adds at most (4 pi R / lambda) (5/128) t^4 radians of phase; pulses where
+    // that is below 1e-5 rad leave it out.
+    const float ax = 2.0f * vx.hi * k.dx_f;
+    const float tb2 = t_bound * t_bound;
+    const bool deg4 = k.c_phase * R * k.inv_dr_f * 0.0390625f * tb2 * tb2 > 1.0e-5f;
+    if (INTERP == INTERP_HEIGHTS) {
+        // bounds of s over the row from the row's ranges of dz and P; u grows
+        // with s (s poly(s) is increasing for |s| / R^2 <= 0.01)
+        const float tvz = 2.0f * vz.hi;
+        const float sx = -k.i0 * fabsf(ax);
+        const float s_lo = -sx + fminf(tvz * hr.dz_lo, tvz * hr.dz_hi) + hr.p_lo;
+        const float s_hi = sx + fmaxf(tvz * hr.dz_lo, tvz * hr.dz_hi) + hr.p_hi;
+        const float a2 = -0.25f * hb * g, a3 = 0.125f * hb * g * g;
+        const float lo_u = fmaf(s_lo, fmaf(fmaf(a3, s_lo, a2), s_lo, hb), frac) - 1.0e-5f;
+        const float hi_u = fmaf(s_hi, fmaf(fmaf(a3, s_hi, a2), s_hi, hb), frac) + 1.0e-5f;
+        const float k0 = floorf(lo_u);
+        const int idx0 = kbase + (int)k0;
+        // both bins recorded (0 <= k <= nr - 2) and inside the row
+        if (hi_u - k0 < 2.0f && idx0 >= bin0 && idx0 + 1 <= bin0 + k.nr - 2 && idx0 >= 0 &&
+            idx0 + 1 <= k.W - 1) {
+            const float4 t0 = __ldg(row + idx0);
+            const float4 t1 = __ldg(row + idx0 + 1);
+            const float x0 = k.c_phase * (frac - k0);
+            if (deg4)
+                heights_hinge_loop<true>(k, s_hp, t0, t1, x0, ax, tvz, hb, g, accre, accim);
+            else
+                heights_hinge_loop<false>(k, s_hp, t0, t1, x0, ax, tvz, hb, g, accre, accim);
+            return true;
+        }
+    }
+    if (deg4)
+        heights_series_loop<INTERP, true>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vz.hi, hb, g,
+                                          accre, accim);
+    else
+        heights_series_loop<INTERP, false>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vz.hi, hb, g,
+                                           accre, accim);
     return true;
 }
 
@@ -1035,7 +1134,7 @@ template <int INTERP>
 __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Record& rec,
                                                     const float4* row, const double* __restrict__ a,
                                                     double xc, double yrow, const HRow& hr,
-                                                    const float2* s_h2,
+                                                    const float4* s_hp,
                                                     const float2* __restrict__ psi,
                                                     float2 (&accre)[NP], float2 (&accim)[NP])
 {
@@ -1054,8 +1153,7 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
 #pragma unroll
     for (int m = 0; m < TILE_X; ++m) {
         const float qx = ((float)m - 0.5f * (TILE_X - 1)) * k.dx_f;
-        const float hm = (m < NP) ? s_h2[m % NP].x : s_h2[m % NP].y;
-        const float dz = hm - hr.hrow;
+        const float dz = (m < NP) ? s_hp[m % NP].x : s_hp[m % NP].y;   // h - hrow
         const float s = fmaf(qx, two_vx + qx, dz * (two_vz + dz));
         const float rp = sqrtf(fmaxf(r2f + s, 0.0f));
         const float den = rf + rp;
@@ -1092,14 +1190,14 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, const HRow& hr, const float2* s_h2,
+                                            double yrow, const HRow& hr, const float4* s_hp,
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
     if (on_heights(INTERP)) {
         if (st.mode == MODE_EXACT &&
-            !heights_series_pulse<INTERP>(k, rec, row, hr, s_h2, psi, accre, accim))
-            heights_exact_pulse<INTERP>(k, rec, row, a, xc, yrow, hr, s_h2, psi, accre, accim);
+            !heights_series_pulse<INTERP>(k, rec, row, hr, s_hp, psi, accre, accim))
+            heights_exact_pulse<INTERP>(k, rec, row, a, xc, yrow, hr, s_hp, psi, accre, accim);
         return;
     }
     if (INTERP == INTERP_NEAREST) {
@@ -1146,7 +1244,9 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                                                         const float* __restrict__ heights)
 {
     __shared__ Record s_rec[CHUNK];
-    extern __shared__ float2 s_heights[];           // heights mode: TILE_Y x HROW2 pairs (h[q], h[q + 16])
+    // heights mode: per row, HROW4 float4 (dz[q], dz[q + 16], P[q], P[q + 16]) with
+    // dz = h - hrow and P = (i dx)^2 + dz^2 for the pixels at offsets i of q and q + 16
+    extern __shared__ float4 s_hp[];
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
     const float jf = (float)jr - 0.5f * (TILE_Y - 1);
@@ -1170,27 +1270,38 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
 
         const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
-        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0};
+        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0, 0.0f, 0.0f, 0.0f, 0.0f};
         if (on_heights(INTERP)) {
             // the thread's own row of the tile, heights clamped to the plan's
             // bounds; pixels outside the image repeat the last row or column
             // (their results are never stored)
             const int rowi_h = min(row0 + jr, k.ny - 1);
             const float* hsrc = heights + (size_t)rowi_h * k.nx;
+            float4* hp = s_hp + jr * HROW4;
             float sum = 0.0f;
 #pragma unroll 4
             for (int q = 0; q < NP; ++q) {
                 const float a = fminf(fmaxf(hsrc[min(col0 + q, k.nx - 1)], k.h_lo_f), k.h_hi_f);
                 const float b = fminf(fmaxf(hsrc[min(col0 + q + NP, k.nx - 1)], k.h_lo_f), k.h_hi_f);
-                s_heights[jr * HROW2 + q] = make_float2(a, b);
+                hp[q] = make_float4(a, b, 0.0f, 0.0f);
                 sum += a + b;
             }
             hr.hrow = sum * (1.0f / TILE_X);
             float dzm = 0.0f;
+            hr.dz_lo = hr.p_lo = 3.0e38f;
+            hr.dz_hi = hr.p_hi = -3.0e38f;
 #pragma unroll 4
             for (int q = 0; q < NP; ++q) {
-                const float2 h2 = s_heights[jr * HROW2 + q];
-                dzm = fmaxf(dzm, fmaxf(fabsf(h2.x - hr.hrow), fabsf(h2.y - hr.hrow)));
+                const float4 h2 = hp[q];
+                const float dza = h2.x - hr.hrow, dzb = h2.y - hr.hrow;
+                const float qa = (k.i0 + (float)q) * k.dx_f, qb = (k.i0 + (float)(q + NP)) * k.dx_f;
+                const float pa = fmaf(qa, qa, dza * dza), pb = fmaf(qb, qb, dzb * dzb);
+                hp[q] = make_float4(dza, dzb, pa, pb);
+                dzm = fmaxf(dzm, fmaxf(fabsf(dza), fabsf(dzb)));
+                hr.dz_lo = fminf(hr.dz_lo, fminf(dza, dzb));
+                hr.dz_hi = fmaxf(hr.dz_hi, fmaxf(dza, dzb));
+                hr.p_lo = fminf(hr.p_lo, fminf(pa, pb));
+                hr.p_hi = fmaxf(hr.p_hi, fmaxf(pa, pb));
             }
             const float hx = 0.5f * (TILE_X - 1) * k.dx_f;
             hr.qm = 1.0001f * sqrtf(hx * hx + dzm * dzm);
@@ -1220,14 +1331,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
-                                  s_heights + jr * HROW2, psi, accre, accim);
+                                  s_hp + jr * HROW4, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
-                                  s_heights + jr * HROW2, psi, accre, accim);
+                                  s_hp + jr * HROW4, psi, accre, accim);
             }
         }
 
@@ -1390,7 +1501,7 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
     return cudaGetLastError();
 }
 
-constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW2 * sizeof(float2);
+constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW4 * sizeof(float4);
 
 cudaError_t prepare_heights_kernel()
 {
