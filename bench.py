@@ -445,8 +445,8 @@ def run_ours(args, scene, rank, world, local, dist):
         },
         "e2e": {"value": aggregate_value(updates, e2e_steps, world, e2e_max), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
-                "api": "sarbp_backproject_host (pinned host buffers; copies the band of range "
-                       "bins the image reaches)"},
+                "api": "sarbp_backproject_host (pinned, device-mapped host buffers: the kernels read "
+                       "the band of range bins the image reaches and write the image in place)"},
         "gpu_launches": args.steps * info["kernels_per_call"],
         "clocks": clocks,
         "plan": info,

@@ -138,6 +138,7 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     k.ny = p->ny;
     k.na = p->na;
     k.nr = p->nr;
+    k.echo_stride = p->nr;
     k.W = plan->W;
     k.tiles_x = plan->tiles_x;
     k.tiles = plan->tiles;
@@ -234,17 +235,34 @@ bool any_split_tile(const BpConst& k)
 
 namespace {
 
+// The device address of a pinned host buffer mapped into the device's
+// address space, or null for any other buffer (pageable memory, device
+// memory, a null pointer).
+void* mapped_host(const void* p)
+{
+    if (!p)
+        return nullptr;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // The band of range bins that pulses n0 .. n1-1 can reach from the image,
 // found in float64 on the host from the antenna positions: for every pulse
 // the nearest and farthest point of the image rectangle, plus margins (six
 // bins below, seven above). Pulses with a non-finite position contribute
 // nothing and are left out. Returns false when no pulse reaches the axis.
+// The square root and the floor are monotone, so the band follows from the
+// smallest and largest squared distances with two square roots in all.
 bool host_band(const sarbp_params* params, const double* antenna_pos, int n0, int n1,
                long long* lo, long long* hi)
 {
-    long long band_lo = params->nr, band_hi = -1;
     const double xa = params->x0, xb = params->x0 + (params->nx - 1) * params->dx;
     const double ya = params->y0, yb = params->y0 + (params->ny - 1) * params->dy;
+    double d2min = HUGE_VAL, d2max = -1.0;
     for (int n = n0; n < n1 && params->nr >= 2; ++n) {
         const double ax = antenna_pos[3 * (size_t)n], ay = antenna_pos[3 * (size_t)n + 1],
                      az = antenna_pos[3 * (size_t)n + 2];
@@ -255,12 +273,15 @@ bool host_band(const sarbp_params* params, const double* antenna_pos, int n0, in
         const double ny_ = std::min(std::max(ay, ya), yb) - ay;
         const double fx = std::max(std::fabs(xa - ax), std::fabs(xb - ax));
         const double fy = std::max(std::fabs(ya - ay), std::fabs(yb - ay));
-        const double rmin = std::sqrt(nx_ * nx_ + ny_ * ny_ + dz * dz);
-        const double rmax = std::sqrt(fx * fx + fy * fy + dz * dz);
-        const double ulo = std::floor((rmin - params->r0) / params->dr) - 6.0;
-        const double uhi = std::floor((rmax - params->r0) / params->dr) + 7.0;
-        band_lo = std::min<long long>(band_lo, (long long)std::max(ulo, 0.0));
-        band_hi = std::max<long long>(band_hi, (long long)std::min(uhi, (double)params->nr - 1.0));
+        d2min = std::min(d2min, nx_ * nx_ + ny_ * ny_ + dz * dz);
+        d2max = std::max(d2max, fx * fx + fy * fy + dz * dz);
+    }
+    long long band_lo = params->nr, band_hi = -1;
+    if (d2max >= 0.0) {
+        const double ulo = std::floor((std::sqrt(d2min) - params->r0) / params->dr) - 6.0;
+        const double uhi = std::floor((std::sqrt(d2max) - params->r0) / params->dr) + 7.0;
+        band_lo = (long long)std::min(std::max(ulo, 0.0), (double)params->nr);
+        band_hi = (long long)std::max(std::min(uhi, (double)params->nr - 1.0), -1.0);
     }
     *lo = band_lo;
     *hi = band_hi;
@@ -272,7 +293,8 @@ bool host_band(const sarbp_params* params, const double* antenna_pos, int n0, in
 // shifted r0), which the plan's table rows always cover.
 sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
-                                    cudaStream_t s, const float* heights = nullptr)
+                                    cudaStream_t s, const float* heights = nullptr,
+                                    long long echo_stride = 0)
 {
     cudaError_t e = cudaSuccess;
     const long long pixels = (long long)params->nx * params->ny;
@@ -288,7 +310,9 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         return SARBP_OK;
     }
 
-    const BpConst k = make_const(plan, params);
+    BpConst k = make_const(plan, params);
+    if (echo_stride > 0)
+        k.echo_stride = echo_stride;
     float4* table = plan->table_alloc + TABLE_PAD;
     e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
     if (e != cudaSuccess)
@@ -728,29 +752,43 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
     if (pixels == 0)
         return SARBP_OK;
 
-    // Only the band of range bins the image can reach is copied.
+    // Only the band of range bins the image can reach crosses to the device.
     long long band_lo = 0, band_hi = -1;
     host_band(params, antenna_pos, 0, params->na, &band_lo, &band_hi);
+    const bool runs = band_hi - band_lo >= 1 && params->na > 0;   // the kernels will run
+
+    // Pinned host buffers the device can address are read and written in
+    // place by the kernels (the echo band through a row stride); other
+    // buffers go through device staging copies.
+    const void* const echo_map = runs ? mapped_host(echoes) : nullptr;
+    void* const img_map = runs ? mapped_host(image) : nullptr;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (img_bytes && !plan->d_image)
+    if (img_bytes && !img_map && !plan->d_image)
         e = device_alloc(&plan->d_image, img_bytes);
     if (e == cudaSuccess && params->na > 0 && !plan->d_pos)
         e = device_alloc(reinterpret_cast<void**>(&plan->d_pos), (size_t)params->na * 3 * sizeof(double));
-    if (e == cudaSuccess && band_hi >= band_lo && !plan->d_echo)
+    if (e == cudaSuccess && band_hi >= band_lo && !echo_map && !plan->d_echo)
         e = device_alloc(&plan->d_echo, (size_t)params->na * params->nr * 8);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMalloc (host staging)");
 
     sarbp_params band = *params;
+    const void* echo_src = plan->d_echo;
+    long long echo_stride = 0;
     if (band_hi >= band_lo) {
         const size_t width = (size_t)(band_hi - band_lo + 1);
         band.nr = (int32_t)width;
         band.r0 = params->r0 + (double)band_lo * params->dr;
-        e = cudaMemcpy2DAsync(plan->d_echo, width * 8,
-                              static_cast<const char*>(echoes) + (size_t)band_lo * 8,
-                              (size_t)params->nr * 8, width * 8, (size_t)params->na,
-                              cudaMemcpyHostToDevice, s);
+        if (echo_map) {
+            echo_src = static_cast<const char*>(echo_map) + (size_t)band_lo * 8;
+            echo_stride = params->nr;
+        } else {
+            e = cudaMemcpy2DAsync(plan->d_echo, width * 8,
+                                  static_cast<const char*>(echoes) + (size_t)band_lo * 8,
+                                  (size_t)params->nr * 8, width * 8, (size_t)params->na,
+                                  cudaMemcpyHostToDevice, s);
+        }
         plan->last_h2d += width * 8 * (size_t)params->na;
     } else {
         band.nr = 0;                         // no pulse reaches the range axis
@@ -761,15 +799,18 @@ sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* 
         plan->last_h2d += (size_t)params->na * 3 * sizeof(double);
     }
     if (e == cudaSuccess && (params->flags & SARBP_ACCUMULATE)) {
-        e = cudaMemcpyAsync(plan->d_image, image, img_bytes, cudaMemcpyHostToDevice, s);
+        if (!img_map)
+            e = cudaMemcpyAsync(plan->d_image, image, img_bytes, cudaMemcpyHostToDevice, s);
         plan->last_h2d += img_bytes;
     }
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "cudaMemcpyAsync (to device)");
-    st = enqueue_backprojection(plan, plan->d_image, plan->d_echo, plan->d_pos, &band, s);
+    st = enqueue_backprojection(plan, img_map ? img_map : plan->d_image, echo_src, plan->d_pos,
+                                &band, s, nullptr, echo_stride);
     if (st != SARBP_OK)
         return st;
-    e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
+    if (!img_map)
+        e = cudaMemcpyAsync(image, plan->d_image, img_bytes, cudaMemcpyDeviceToHost, s);
     plan->last_d2h = img_bytes;
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(s);

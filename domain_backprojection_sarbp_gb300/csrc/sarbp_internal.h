@@ -44,6 +44,7 @@ struct BpConst {
     int ctas;                    // persistent CTAs of the main kernel
     unsigned flags;
     long long units;             // tiles * na (tile-pulse work units)
+    long long echo_stride;       // complex samples from one pulse's echo row to the next
 
     double x0, y0, z0, dx, dy, r0, dr, inv_dr;
     double rect_x0, rect_x1, rect_y0, rect_y1;  // tile-padded image rectangle

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
     __syncthreads();
     const int lo = s_lo;
     float4* row = table + (size_t)n * k.W;
-    const float2* erow = echo + (size_t)n * k.nr;
+    const float2* erow = echo + (size_t)n * (size_t)k.echo_stride;
     for (int w = threadIdx.x; w < k.W; w += blockDim.x) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         const long long kk = (long long)lo + w;

@@ -69,6 +69,8 @@ def _host_ptr(a, name, shape, np_dtype):
             raise ValueError(f"{name} must be a contiguous CPU tensor")
         if tuple(a.shape) != shape:
             raise ValueError(f"{name} must have shape {shape}")
+        if str(a.dtype) != "torch." + np.dtype(np_dtype).name:
+            raise ValueError(f"{name} must have dtype {np.dtype(np_dtype).name}")
         return ctypes.c_void_p(a.data_ptr() if a.numel() else None)
     if not (isinstance(a, np.ndarray) and a.dtype == np_dtype and a.flags.c_contiguous
             and a.shape == shape):

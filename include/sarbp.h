@@ -136,17 +136,22 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
 /*
  * sarbp_backproject_host - the same operation on HOST buffers.
  *
- * image, echoes, antenna_pos are host pointers with the layouts above (pinned
- * memory gives the fastest copies; pageable memory works). From the antenna
- * positions the call finds, in float64 on the host, the band of range bins
- * that any pixel can reach (nearest and farthest point of the image for every
- * pulse, plus six bins of margin each side) and copies only that band of every
- * pulse, then backprojects it on `stream` against the same range axis, copies
- * the image back and waits for the stream: when it returns SARBP_OK the image
- * is on the host. The result equals sarbp_backproject's to float32 rounding.
- * Device buffers are owned by the plan (allocated on first use, kept until
- * sarbp_destroy). With SARBP_ACCUMULATE the host image is copied in first and
- * added into.
+ * image, echoes, antenna_pos are host pointers with the layouts above. From
+ * the antenna positions the call finds, in float64 on the host, the band of
+ * range bins that any pixel can reach (nearest and farthest point of the image
+ * for every pulse, plus six bins of margin each side); only that band of every
+ * pulse crosses to the device. It backprojects the band on `stream` against
+ * the same range axis and waits for the stream: when it returns SARBP_OK the
+ * image is on the host. The result equals sarbp_backproject's to float32
+ * rounding.
+ *
+ * Transport: an echo or image buffer that is pinned and mapped into the
+ * device's address space (cudaHostAlloc, cudaHostRegister, or any pinned
+ * allocation on a unified-addressing system) is read or written in place by
+ * the kernels, without a staging copy; any other buffer (pageable memory) is
+ * staged through device buffers owned by the plan (allocated on first use,
+ * kept until sarbp_destroy). Both give the same image bit for bit. With
+ * SARBP_ACCUMULATE the host image is read and added into.
  */
 sarbp_status sarbp_backproject_host(sarbp_plan_t plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
