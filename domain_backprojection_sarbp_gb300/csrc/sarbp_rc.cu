@@ -39,8 +39,12 @@ namespace {
 constexpr int RC_MAX_LOG2 = 14;            // N <= 16384: 135 KB of shared memory per row
 constexpr int EPT = 16;                    // complex values a thread holds
 
-__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
-__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+// complex sums as one packed f32x2 operation (a - b = b * -1 + a, rounded once)
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b)
+{
+    return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
 __device__ __forceinline__ float2 cmul(float2 a, float2 b)
 {
     return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
@@ -54,14 +58,21 @@ __device__ __forceinline__ float2 mul_si(float2 a)
 }
 
 // In-register DFTs, natural order in and out: X[k] = sum_m x[m] exp(S 2 pi i m k / R).
+// b and d take s1 +- S i (b - d) in scalar form, where the lane swap of the
+// factor i costs nothing.
 template <int S>
 __device__ __forceinline__ void dft4(float2& a, float2& b, float2& c, float2& d)
 {
-    const float2 s0 = cadd(a, c), s1 = csub(a, c), s2 = cadd(b, d), s3 = mul_si<S>(csub(b, d));
+    const float2 s0 = cadd(a, c), s1 = csub(a, c), s2 = cadd(b, d), dd = csub(b, d);
     a = cadd(s0, s2);
     c = csub(s0, s2);
-    b = cadd(s1, s3);
-    d = csub(s1, s3);
+    if (S < 0) {
+        b = make_float2(s1.x + dd.y, s1.y - dd.x);
+        d = make_float2(s1.x - dd.y, s1.y + dd.x);
+    } else {
+        b = make_float2(s1.x - dd.y, s1.y + dd.x);
+        d = make_float2(s1.x + dd.y, s1.y - dd.x);
+    }
 }
 
 template <int R, int S>
