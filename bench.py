@@ -181,6 +181,44 @@ def oracle_rate(scene, seconds: float = 8.0, threads: int = 0, seed: int = 0):
                        f"({updates:.3e} updates) of the same scene, {secs:.2f} s wall")
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as the OS reports it."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
+def cpu_baseline(scene, seconds: float):
+    """The oracle on all host cores (the reported baseline) and on one thread,
+    with the full-image times both rates extrapolate to, beside the page's own
+    single-thread figure for this scene size."""
+    allc = oracle_rate(scene, seconds=seconds)
+    one = oracle_rate(scene, seconds=max(1.0, seconds / 4), threads=1, seed=1)
+    updates = scene.params["na"] * scene.params["nx"] * scene.params["ny"]
+    allc.update(
+        cpu_model=cpu_model(), hardware_threads=os.cpu_count(),
+        one_thread={"value": one["value"], "unit": UNIT, "sample": one["sample"]},
+        extrapolated_full_image_s={"all_cores": updates / (allc["value"] * 1e9),
+                                   "one_thread": updates / (one["value"] * 1e9)},
+        page_figure={"one_thread_cpu_s": 56.0, "scene": "Na=4096 pulses, 1024x1024 image",
+                     "cpu": "not stated on the page"})
+    return allc
+
+
 def run_reference(args, scene):
     """The oracle as it stands, timed on the host cores, one bounded sample per step."""
     import oracle
@@ -453,7 +491,7 @@ def run_ours(args, scene, rank, world, local, dist):
         "variants": variants,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = oracle_rate(scene, seconds=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(scene, args.cpu_seconds)
     return out
 
 

@@ -79,3 +79,15 @@ def test_reference_arm_json(capsys):
 def test_warmup_below_three_is_refused():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_cpu_baseline_reports_one_thread_and_extrapolation():
+    from synth import scenes
+    sc = scenes.make_scene(scenes.CONFIGS[0])
+    cb = bench.cpu_baseline(sc, 0.2)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["one_thread"]["value"] > 0 and cb["one_thread"]["unit"] == "Gupd/s"
+    ex = cb["extrapolated_full_image_s"]
+    updates = sc.params["na"] * sc.params["nx"] * sc.params["ny"]
+    assert abs(ex["one_thread"] * cb["one_thread"]["value"] * 1e9 - updates) <= 1e-6 * updates
+    assert cb["cpu_model"] and cb["page_figure"]["one_thread_cpu_s"] == 56.0
