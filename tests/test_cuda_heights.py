@@ -72,10 +72,11 @@ def test_terrain_several_tiles(relief):
     assert not parity.argmax_mismatches(got, ref, sc.targets)
 
 
-def two_bin_fraction(params, pos, h, pulses):
-    """Share of (thread row of 32 pixels, pulse) pairs whose pixels all fall in
-    two adjacent range bins (u spans less than 0.9 bin): the rows the linear
-    path serves from two table entries; the others take one gather per pixel."""
+def two_bin_fraction(params, pos, h, pulses, span=0.9):
+    """Share of (thread row of 32 pixels, pulse) pairs whose range index u
+    spans less than ``span`` bins: below 0.9 the pixels fall in two adjacent
+    bins, the rows the linear path serves from two table entries; the others
+    take one gather per pixel."""
     p = params
     ny, nx = h.shape
     xs = p["x0"] + np.arange(nx) * p["dx"]
@@ -89,19 +90,20 @@ def two_bin_fraction(params, pos, h, pulses):
         u = np.sqrt((px - pos[n, 0]) ** 2 + (py - pos[n, 1]) ** 2 + (pz - pos[n, 2]) ** 2)
         u = ((u - p["r0"]) / p["dr"])[:, :full].reshape(ny, -1, 32)
         spans.append((u.max(axis=2) - u.min(axis=2)).ravel())
-    return float((np.concatenate(spans) < 0.9).mean())
+    return float((np.concatenate(spans) < span).mean())
 
 
-@pytest.mark.parametrize("relief", [40.0, 80.0])
+@pytest.mark.parametrize("relief", [40.0, 80.0, 240.0])
 def test_terrain_two_entry_and_gathered_rows(relief):
-    """Terrain where about 60 % (40 m) and 40 % (80 m) of the (row, pulse)
-    pairs lie in two range bins (two-entry form) and the rest in more (a
-    gather per pixel); both against the oracle in full."""
+    """Terrain where about 60 % (40 m), 40 % (80 m) and 7 % (240 m) of the
+    (row, pulse) pairs lie in two range bins (two-entry form) and the rest in
+    more (a gather per pixel); all against the oracle in full."""
     cfg = scenes.shrink(scenes.CONFIGS[1], na=384, nx=96, ny=700, n_targets=6)
     sc, h = terrain_scene(cfg, relief, mean=5.0)
-    share = two_bin_fraction(sc.params, sc.antenna_pos, h, range(0, cfg.na, 48))
-    print("two-bin share", share)
-    assert 0.1 < share < 0.95, share
+    share2 = two_bin_fraction(sc.params, sc.antenna_pos, h, range(0, cfg.na, 48))
+    share3 = two_bin_fraction(sc.params, sc.antenna_pos, h, range(0, cfg.na, 48), span=1.9)
+    print("two-bin share", share2, "three-bin share", share3)
+    assert 0.05 < share2 < share3 < 0.99, (share2, share3)
     got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (float(h.min()), float(h.max())))
     ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
     print(parity.assert_parity(got, ref, f"gentle terrain relief {relief}"))
