@@ -33,6 +33,13 @@
  * Threading. A plan may be used from one host thread and one stream at a
  * time. Different plans are independent.
  *
+ * CUDA graphs. The device-buffer calls (sarbp_backproject,
+ * sarbp_backproject_heights, sarbp_backproject_volume, sarbp_range_compress)
+ * only enqueue kernels and memsets on `stream`: they allocate nothing and do
+ * not synchronise, so they may be captured into a CUDA graph once the plan
+ * exists; each replay does the same work on the buffers given at capture.
+ * The host-buffer calls synchronise and cannot be captured.
+ *
  * Errors. No call throws or aborts. Every call returns a status; argument
  * checks happen before any GPU work is queued, and a call that returns an
  * error other than SARBP_ERR_CUDA has queued nothing. Errors raised by the
