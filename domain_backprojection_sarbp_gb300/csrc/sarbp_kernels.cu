@@ -280,10 +280,10 @@ enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXAC
                        MODE_PAIR = 5 };
 
 struct PulseState {
-    float2 q0, q1, q2;            // hinge: c (e0 - k0), c e1, c e2; otherwise e0, e1, e2 (both halves)
-    float4 t0;                    // hinge: table entry k0; sinc polynomial: lo_u, hi_u, k0, bin k0;
+    float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
+    float4 t0;                    // hinge: table entry k0 + 1; sinc polynomial: lo_u, hi_u, k0, bin k0;
                                   // nearest pair: table entry (e_kn, e_kn+1)
-    float2 t1d;                   // hinge: D part of entry k0 + 1; nearest pair: kn, bin kn
+    float2 t1d;                   // hinge: D part of entry k0; nearest pair: kn, bin kn
     unsigned long long base;      // gather: row pointer + (kb - magic bias) entries, in bytes
     int kb;                       // row index the polynomial u is relative to
     int bin0;                     // row index of absolute bin 0
@@ -364,11 +364,10 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         }
     }
     if (hinge) {
-        st.t0 = __ldg(row + idx0);
-        const float4 t1 = __ldg(row + idx0 + 1);
-        st.t1d = make_float2(t1.z, t1.w);
+        st.t0 = __ldg(row + idx0 + 1);
+        st.t1d = __ldg(reinterpret_cast<const float2*>(row + idx0) + 1);
         const float c = k.c_phase;
-        const float v0 = c * (e0 - k0), w1 = c * e1, w2 = c * e2;
+        const float v0 = c * ((e0 - k0) - 1.0f), w1 = c * e1, w2 = c * e2;
         st.q0 = make_float2(v0, v0);
         st.q1 = make_float2(w1, w1);
         st.q2 = make_float2(w2, w2);
@@ -384,37 +383,35 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     return st;
 }
 
-// All pixels in bins k0, k0 + 1. With v = u - k0 in [0, 2), x = c v and
-// h = max(x - c, 0), the interpolated, phase-compensated sample is
-//   exp(j x) [A + x D + h G],  A = t0.A,  D = t0.D,  G = exp(-j c) t1.D - t0.D
-// (the linear interpolant over the two bins written as one line plus a hinge).
-// With max(y, 0) = (y + |y|) / 2 this is A' + x D' + |x - c| G' where
-// A' = A - c G / 2, D' = D + G / 2, G' = G / 2.
+// All pixels in bins k0, k0 + 1. With y = c (u - k0 - 1) in [-c, c), a pixel in
+// bin k0 + 1 contributes exp(j y) (A1 + y D1) (entry k0 + 1 = (A1, D1)), one in
+// bin k0 contributes exp(j y) (A1 + y B), B = exp(j c) D0 (D0 from entry k0;
+// the two lines meet at y = 0 since psi_k0+1 = psi_k0 exp(j c)). So the
+// interpolated, phase-compensated sample is
+//   exp(j y) [A1 + y (D1 + B) / 2 + |y| (D1 - B) / 2].
 __device__ __forceinline__ void hinge_pulse(const BpConst& k, const PulseState& st,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const float c = k.c_phase;
-    const float gre = 0.5f * (k.rot_re * st.t1d.x - k.rot_im * st.t1d.y - st.t0.z);
-    const float gim = 0.5f * (k.rot_re * st.t1d.y + k.rot_im * st.t1d.x - st.t0.w);
-    const float a_re = fmaf(-c, gre, st.t0.x), a_im = fmaf(-c, gim, st.t0.y);
-    const float d_re = st.t0.z + gre, d_im = st.t0.w + gim;
-    const float2 are = make_float2(a_re, a_re), aim = make_float2(a_im, a_im);
+    // B = conj(r) D0 with r = exp(-j c)
+    const float bre = k.rot_re * st.t1d.x + k.rot_im * st.t1d.y;
+    const float bim = k.rot_re * st.t1d.y - k.rot_im * st.t1d.x;
+    const float d_re = 0.5f * (st.t0.z + bre), d_im = 0.5f * (st.t0.w + bim);
+    const float g_re = 0.5f * (st.t0.z - bre), g_im = 0.5f * (st.t0.w - bim);
+    const float2 are = make_float2(st.t0.x, st.t0.x), aim = make_float2(st.t0.y, st.t0.y);
     const float2 dre = make_float2(d_re, d_re), dim = make_float2(d_im, d_im);
-    const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
-    const float2 negc = make_float2(-c, -c);
+    const float2 gre = make_float2(g_re, g_re), gim = make_float2(g_im, g_im);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);    // pixel offsets of pair 0 (runtime: no constant pairs)
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 x = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        const float2 y = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
         id = __fadd2_rn(id, one);
-        const float2 y = __fadd2_rn(x, negc);
         const float2 ay = make_float2(fabsf(y.x), fabsf(y.y));
-        const float2 wr = __ffma2_rn(ay, g_re, __ffma2_rn(x, dre, are));
-        const float2 wi = __ffma2_rn(ay, g_im, __ffma2_rn(x, dim, aim));
+        const float2 wr = __ffma2_rn(ay, gre, __ffma2_rn(y, dre, are));
+        const float2 wi = __ffma2_rn(ay, gim, __ffma2_rn(y, dim, aim));
         float sa, ca, sb, cb;
-        __sincosf(x.x, &sa, &ca);
-        __sincosf(x.y, &sb, &cb);
+        __sincosf(y.x, &sa, &ca);
+        __sincosf(y.y, &sb, &cb);
         const float2 cs = make_float2(ca, cb);
         const float2 sn = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, cs, accre[q]);
@@ -1004,11 +1001,12 @@ __device__ __forceinline__ void heights_series_loop(const BpConst& k, const floa
 }
 
 // Linear interpolation when every pixel of the row lies in bins k0 and k0 + 1:
-// the two-entry form of hinge_pulse with x = c (u - k0) from the range series
-// (u - k0 = frac - k0 + s poly(s), folded so that x comes out of one FFMA).
+// the two-entry form of hinge_pulse with y = c (u - k0 - 1) from the range
+// series (u - k0 - 1 = frac - k0 - 1 + s poly(s), folded so that y comes out
+// of one FFMA). t0, t1: table entries k0, k0 + 1; y0 = c (frac - k0 - 1).
 template <bool DEG4>
 __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float4* s_hp, float4 t0,
-                                                   float4 t1, float x0, float ax, float two_vz,
+                                                   float4 t1, float y0, float ax, float two_vz,
                                                    float hb, float g, float2 (&accre)[NP],
                                                    float2 (&accim)[NP])
 {
@@ -1018,15 +1016,14 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
                 a4 = -0.078125f * a1 * g * g * g;
     const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
     const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4, a4);
-    const float2 x02 = make_float2(x0, x0);
-    const float gre = 0.5f * (k.rot_re * t1.z - k.rot_im * t1.w - t0.z);
-    const float gim = 0.5f * (k.rot_re * t1.w + k.rot_im * t1.z - t0.w);
-    const float a_re = fmaf(-c, gre, t0.x), a_im = fmaf(-c, gim, t0.y);
-    const float d_re = t0.z + gre, d_im = t0.w + gim;
-    const float2 are = make_float2(a_re, a_re), aim = make_float2(a_im, a_im);
+    const float2 y02 = make_float2(y0, y0);
+    const float bre = k.rot_re * t0.z + k.rot_im * t0.w;     // B = exp(j c) D0
+    const float bim = k.rot_re * t0.w - k.rot_im * t0.z;
+    const float d_re = 0.5f * (t1.z + bre), d_im = 0.5f * (t1.w + bim);
+    const float gre = 0.5f * (t1.z - bre), gim = 0.5f * (t1.w - bim);
+    const float2 are = make_float2(t1.x, t1.x), aim = make_float2(t1.y, t1.y);
     const float2 dre = make_float2(d_re, d_re), dim = make_float2(d_im, d_im);
     const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
-    const float2 negc = make_float2(-c, -c);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
@@ -1037,14 +1034,13 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
         id = __fadd2_rn(id, one);
         const float2 poly = DEG4 ? __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12)
                                  : __ffma2_rn(__ffma2_rn(a32, s, a22), s, a12);
-        const float2 x = __ffma2_rn(s, poly, x02);
-        const float2 y = __fadd2_rn(x, negc);
+        const float2 y = __ffma2_rn(s, poly, y02);
         const float2 ay = make_float2(fabsf(y.x), fabsf(y.y));
-        const float2 wr = __ffma2_rn(ay, g_re, __ffma2_rn(x, dre, are));
-        const float2 wi = __ffma2_rn(ay, g_im, __ffma2_rn(x, dim, aim));
+        const float2 wr = __ffma2_rn(ay, g_re, __ffma2_rn(y, dre, are));
+        const float2 wi = __ffma2_rn(ay, g_im, __ffma2_rn(y, dim, aim));
         float sa, ca, sb, cb;
-        __sincosf(x.x, &sa, &ca);
-        __sincosf(x.y, &sb, &cb);
+        __sincosf(y.x, &sa, &ca);
+        __sincosf(y.y, &sb, &cb);
         const float2 cs = make_float2(ca, cb);
         const float2 sn = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, cs, accre[q]);
@@ -1111,11 +1107,11 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
             idx0 + 1 <= k.W - 1) {
             const float4 t0 = __ldg(row + idx0);
             const float4 t1 = __ldg(row + idx0 + 1);
-            const float x0 = k.c_phase * (frac - k0);
+            const float y0 = k.c_phase * ((frac - k0) - 1.0f);
             if (deg4)
-                heights_hinge_loop<true>(k, s_hp, t0, t1, x0, ax, tvz, hb, g, accre, accim);
+                heights_hinge_loop<true>(k, s_hp, t0, t1, y0, ax, tvz, hb, g, accre, accim);
             else
-                heights_hinge_loop<false>(k, s_hp, t0, t1, x0, ax, tvz, hb, g, accre, accim);
+                heights_hinge_loop<false>(k, s_hp, t0, t1, y0, ax, tvz, hb, g, accre, accim);
             return true;
         }
     }
