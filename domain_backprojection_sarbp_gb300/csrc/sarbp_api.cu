@@ -170,6 +170,9 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     const double turns = alpha - std::floor(alpha);      // exp(-j c) = exp(-j 2 pi frac(alpha))
     k.rot_re = (float)std::cos(2.0 * PI * turns);
     k.rot_im = (float)-std::sin(2.0 * PI * turns);
+    const double half_turns = 0.5 * alpha - std::floor(0.5 * alpha);   // exp(+j c / 2)
+    k.hrot_re = (float)std::cos(2.0 * PI * half_turns);
+    k.hrot_im = (float)std::sin(2.0 * PI * half_turns);
     k.i0 = -0.5f * (float)(TILE_X - 1);
     k.dx_f = (float)p->dx;
     k.dy_f = (float)p->dy;

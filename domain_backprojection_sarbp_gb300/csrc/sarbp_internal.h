@@ -65,6 +65,7 @@ struct BpConst {
     float r0_hi, r0_lo;          // r0 as a float pair (hi + lo)
     float idr_hi, idr_lo;        // 1 / dr as a float pair
     float rot_re, rot_im;        // exp(-j c_phase): phase step from one bin to the next
+    float hrot_re, hrot_im;      // exp(+j c_phase / 2): phase across half a bin
     float i0;                    // column offset of a thread's first pixel from the tile centre
 };
 

@@ -350,11 +350,12 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     if (st.mode != MODE_POLY)
         st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
+    float kn = 0.0f;
     if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
         // nearest sample: when every pixel rounds to bin kn or kn + 1, one table
         // entry (e_kn, e_kn+1) serves the thread; psi_kn must exist
         const float tkn = __fadd_rd(lo_u + 0.5f, MAGIC);
-        const float kn = tkn - MAGIC;
+        kn = tkn - MAGIC;
         const int idxn = kb + (__float_as_int(tkn) - MAGIC_BITS);
         const int kabsn = idxn - bin0;
         if (hi_u + 0.5f - kn < 2.0f && kabsn >= 0 && kabsn <= k.nr - 1) {
@@ -368,6 +369,13 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         st.t1d = __ldg(reinterpret_cast<const float2*>(row + idx0) + 1);
         const float c = k.c_phase;
         const float v0 = c * ((e0 - k0) - 1.0f), w1 = c * e1, w2 = c * e2;
+        st.q0 = make_float2(v0, v0);
+        st.q1 = make_float2(w1, w1);
+        st.q2 = make_float2(w2, w2);
+    } else if (INTERP == INTERP_NEAREST && st.mode == MODE_PAIR) {
+        // phase from the bin boundary kn + 1/2: x = c (u - kn - 1/2)
+        const float c = k.c_phase;
+        const float v0 = c * ((e0 - kn) - 0.5f), w1 = c * e1, w2 = c * e2;
         st.q0 = make_float2(v0, v0);
         st.q1 = make_float2(w1, w1);
         st.q2 = make_float2(w2, w2);
@@ -789,25 +797,23 @@ __device__ __forceinline__ void nearest_pair_pulse(const BpConst& k, const Pulse
                                                    const float2* __restrict__ psi,
                                                    float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const float kn = st.t1d.x;
-    const float2 ps = __ldg(psi + __float_as_int(st.t1d.y));
+    // With x = c (u - kn - 1/2) (the state's polynomial), a pixel takes e_kn + 1
+    // when x >= 0 (u + 1/2 >= kn + 1), else e_kn, and its echo phase is
+    // psi_kn exp(j c (u - kn)) = psi_kn exp(j c / 2) exp(j x).
+    const float2 p0 = __ldg(psi + __float_as_int(st.t1d.y));
+    const float2 ps = make_float2(p0.x * k.hrot_re - p0.y * k.hrot_im, p0.x * k.hrot_im + p0.y * k.hrot_re);
     const float4 e = st.t0;
     const float w0r = e.x * ps.x - e.y * ps.y, w0i = e.x * ps.y + e.y * ps.x;
     const float w1r = e.z * ps.x - e.w * ps.y, w1i = e.z * ps.y + e.w * ps.x;
-    const float up = kn + 1.0f;
-    const float c = k.c_phase;
-    const float2 c2 = make_float2(c, c), nknc = make_float2(-kn * c, -kn * c);
-    const float2 one = make_float2(1.0f, 1.0f), hf = make_float2(0.5f, 0.5f);
+    const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        const float2 u = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
+        const float2 x = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
         id = __fadd2_rn(id, one);
-        const float2 v = __fadd2_rn(u, hf);
-        const bool ba = v.x >= up, bb = v.y >= up;
+        const bool ba = x.x >= 0.0f, bb = x.y >= 0.0f;
         const float2 wr = make_float2(ba ? w1r : w0r, bb ? w1r : w0r);
         const float2 wi = make_float2(ba ? w1i : w0i, bb ? w1i : w0i);
-        const float2 x = __ffma2_rn(u, c2, nknc);
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
         __sincosf(x.y, &sb, &cb);
