@@ -60,6 +60,7 @@ enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INT
 __host__ __device__ constexpr bool on_heights(int interp) { return interp >= INTERP_HEIGHTS; }
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
+constexpr float SINC_SPAN3 = 0.11f;         // widest spread for the cubic on four nodes
 constexpr int HROW4 = TILE_X / 2 + 1;      // float4 per row of a tile's height terms (padded)
 
 struct __align__(16) Record {
@@ -277,7 +278,7 @@ constexpr int NP = TILE_X / 2;
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
-                       MODE_PAIR = 5 };
+                       MODE_PAIR = 5, MODE_POLY3 = 6 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
@@ -343,11 +344,11 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         const float k0e = tke - MAGIC;
         const int kabs0 = kb + (__float_as_int(tke) - MAGIC_BITS) - bin0;
         if (hi_e - lo_e <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1) {
-            st.mode = MODE_POLY;
+            st.mode = hi_e - lo_e <= SINC_SPAN3 ? MODE_POLY3 : MODE_POLY;
             st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
         }
     }
-    if (st.mode != MODE_POLY)
+    if (st.mode != MODE_POLY && st.mode != MODE_POLY3)
         st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
     float kn = 0.0f;
@@ -639,48 +640,22 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
     return sinc_sum(f, row + (kr - 3));
 }
 
-// All of the thread's pixels within SINC_SPAN bins, every stencil inside the
-// recorded range. G(u) is smooth (a sum of eight windowed sincs), so over the
-// interval [lo_u, hi_u] (widened to a half-width of at least SINC_HALF_MIN) it
-// is interpolated at the five Chebyshev nodes mid + half cos((2i+1) pi / 10)
-// by a degree-4 polynomial in t = (u - mid) / half, evaluated per pixel as a
-// polynomial in s = u - mid. The interpolation error is at most
-// max|G^(5)| (half)^5 / (2^4 5!) <= pi^5 |e| 8 (1/8)^5 / 1920 ~ 4e-5 |e| for
-// half <= 1/8. The echo phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0))
-// is applied per pixel; psi_k0 is folded into the coefficients.
-__device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseState& st,
-                                                const float4* row, const float2* __restrict__ psi,
+// The per-pixel part of the polynomial mode: coefficients p[0 .. ND-1] of the
+// interpolant in t = (u - mid) / half, evaluated per pixel in s = u - mid
+// with the echo phase psi_k0 exp(j c (u - k0)).
+template <int ND>
+__device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
+                                                const float2* __restrict__ psi, const float2 (&p)[5],
+                                                float mid, float half, float k0, int kabs0,
                                                 float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const float lo_u = st.t0.x, hi_u = st.t0.y, k0 = st.t0.z;
-    const int kabs0 = __float_as_int(st.t0.w);
-    const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
-    constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
-    const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
-    const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
-    const float2 g2 = sinc_value(mid, st.kb, row);
-    const float2 g3 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
-    const float2 g4 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
-    // monomial coefficients of the interpolant (inverse Vandermonde of the nodes)
-    const float2 s04 = make_float2(g0.x + g4.x, g0.y + g4.y), d04 = make_float2(g0.x - g4.x, g0.y - g4.y);
-    const float2 s13 = make_float2(g1.x + g3.x, g1.y + g3.y), d13 = make_float2(g1.x - g3.x, g1.y - g3.y);
-    float2 p[5];
-    p[0] = g2;
-    p[1] = make_float2(fmaf(1.376381920f, d13.x, -0.324919696f * d04.x),
-                       fmaf(1.376381920f, d13.y, -0.324919696f * d04.y));
-    p[2] = make_float2(fmaf(-0.341640786f, s04.x, fmaf(2.341640786f, s13.x, -4.0f * g2.x)),
-                       fmaf(-0.341640786f, s04.y, fmaf(2.341640786f, s13.y, -4.0f * g2.y)));
-    p[3] = make_float2(fmaf(0.940456404f, d04.x, -1.521690426f * d13.x),
-                       fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
-    p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
-                       fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
     // coefficients in s = u - mid (t = s / half), psi_k0 folded in
     const float2 ps = __ldg(psi + kabs0);
     const float ih = rcp_approx(half);            // half >= SINC_HALF_MIN
     float2 pr[5], pi[5];
     float sc = 1.0f;
 #pragma unroll
-    for (int n = 0; n < 5; ++n) {
+    for (int n = 0; n < ND; ++n) {
         const float psr = ps.x * sc, psi_ = ps.y * sc;
         const float re = p[n].x * psr - p[n].y * psi_;
         const float im = p[n].x * psi_ + p[n].y * psr;
@@ -701,8 +676,12 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
     for (int q = 0; q < NP; ++q) {
         const float2 sv = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), q0s);
         id = __fadd2_rn(id, one);
-        const float2 gr = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pr[4], sv, pr[3]), sv, pr[2]), sv, pr[1]), sv, pr[0]);
-        const float2 gi = __ffma2_rn(__ffma2_rn(__ffma2_rn(__ffma2_rn(pi[4], sv, pi[3]), sv, pi[2]), sv, pi[1]), sv, pi[0]);
+        float2 gr = pr[ND - 1], gi = pi[ND - 1];
+#pragma unroll
+        for (int n = ND - 2; n >= 0; --n) {
+            gr = __ffma2_rn(gr, sv, pr[n]);
+            gi = __ffma2_rn(gi, sv, pi[n]);
+        }
         const float2 x = __ffma2_rn(sv, c2, cm2);
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
@@ -713,6 +692,68 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
         accim[q] = __ffma2_rn(gr, sn, __ffma2_rn(gi, cs, accim[q]));
         accre[q] = __ffma2_rn(make_float2(-gi.x, -gi.y), sn, accre[q]);
     }
+}
+
+// All of the thread's pixels within SINC_SPAN bins, every stencil inside the
+// recorded range. G(u) is smooth (a sum of eight windowed sincs), so over the
+// interval [lo_u, hi_u] (widened to a half-width of at least SINC_HALF_MIN) it
+// is interpolated at the five Chebyshev nodes mid + half cos((2i+1) pi / 10)
+// by a degree-4 polynomial in t = (u - mid) / half, evaluated per pixel as a
+// polynomial in s = u - mid. The interpolation error is at most
+// max|G^(5)| (half)^5 / (2^4 5!) <= pi^5 |e| 8 (1/8)^5 / 1920 ~ 4e-5 |e| for
+// half <= 1/8. Spans of at most SINC_SPAN3 take the cubic on the four nodes
+// mid + half cos((2i+1) pi / 8) instead (NN = 4): error at most
+// max|G^(4)| half^4 / (2^3 4!) <= pi^4 |e| 8 (0.055)^4 / 192 ~ 3.7e-5 |e|, one
+// node evaluation and two packed FMAs per pixel pair fewer. The echo phase
+// exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0)) is applied per pixel;
+// psi_k0 is folded into the coefficients.
+template <int NN>
+__device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseState& st,
+                                                const float4* row, const float2* __restrict__ psi,
+                                                float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float lo_u = st.t0.x, hi_u = st.t0.y, k0 = st.t0.z;
+    const int kabs0 = __float_as_int(st.t0.w);
+    const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
+    // monomial coefficients of the interpolant (inverse Vandermonde of the nodes)
+    float2 p[5];
+    if (NN == 4) {
+        constexpr float C1 = 0.923879533f, C2 = 0.382683432f;   // cos(pi/8), cos(3 pi/8)
+        const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
+        const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
+        const float2 g2 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
+        const float2 g3 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
+        const float2 s03 = make_float2(g0.x + g3.x, g0.y + g3.y), d03 = make_float2(g0.x - g3.x, g0.y - g3.y);
+        const float2 s12 = make_float2(g1.x + g2.x, g1.y + g2.y), d12 = make_float2(g1.x - g2.x, g1.y - g2.y);
+        p[0] = make_float2(fmaf(-0.103553391f, s03.x, 0.603553391f * s12.x),
+                           fmaf(-0.103553391f, s03.y, 0.603553391f * s12.y));
+        p[1] = make_float2(fmaf(-0.112085382f, d03.x, 1.577161015f * d12.x),
+                           fmaf(-0.112085382f, d03.y, 1.577161015f * d12.y));
+        p[2] = make_float2(0.707106781f * (s03.x - s12.x), 0.707106781f * (s03.y - s12.y));
+        p[3] = make_float2(fmaf(0.765366865f, d03.x, -1.847759065f * d12.x),
+                           fmaf(0.765366865f, d03.y, -1.847759065f * d12.y));
+        p[4] = make_float2(0.0f, 0.0f);
+        sinc_poly_apply<4>(k, st, psi, p, mid, half, k0, kabs0, accre, accim);
+        return;
+    }
+    constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
+    const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
+    const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
+    const float2 g2 = sinc_value(mid, st.kb, row);
+    const float2 g3 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
+    const float2 g4 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
+    const float2 s04 = make_float2(g0.x + g4.x, g0.y + g4.y), d04 = make_float2(g0.x - g4.x, g0.y - g4.y);
+    const float2 s13 = make_float2(g1.x + g3.x, g1.y + g3.y), d13 = make_float2(g1.x - g3.x, g1.y - g3.y);
+    p[0] = g2;
+    p[1] = make_float2(fmaf(1.376381920f, d13.x, -0.324919696f * d04.x),
+                       fmaf(1.376381920f, d13.y, -0.324919696f * d04.y));
+    p[2] = make_float2(fmaf(-0.341640786f, s04.x, fmaf(2.341640786f, s13.x, -4.0f * g2.x)),
+                       fmaf(-0.341640786f, s04.y, fmaf(2.341640786f, s13.y, -4.0f * g2.y)));
+    p[3] = make_float2(fmaf(0.940456404f, d04.x, -1.521690426f * d13.x),
+                       fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
+    p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
+                       fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
+    sinc_poly_apply<5>(k, st, psi, p, mid, half, k0, kabs0, accre, accim);
 }
 
 __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& st, const float4* row,
@@ -1212,8 +1253,10 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
         return;
     }
     if (INTERP == INTERP_SINC8) {
-        if (st.mode == MODE_POLY)
-            sinc_poly_pulse(k, st, row, psi, accre, accim);
+        if (st.mode == MODE_POLY3)
+            sinc_poly_pulse<4>(k, st, row, psi, accre, accim);
+        else if (st.mode == MODE_POLY)
+            sinc_poly_pulse<5>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
