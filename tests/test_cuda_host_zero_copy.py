@@ -57,6 +57,18 @@ def test_pinned_equals_pageable(scene, which):
     assert np.array_equal(got, ref), which
 
 
+@pytest.mark.parametrize("interp", ["sinc8", "nearest"])
+def test_pinned_equals_pageable_other_interpolations(scene, interp):
+    p = scene.params
+    shape = (p["ny"], p["nx"])
+    with Plan(p) as plan:
+        ref = np.zeros(shape, np.complex64)
+        plan.backproject_host(ref, scene.echoes, scene.antenna_pos, interp=interp)
+        got = pinned(np.zeros(shape, np.complex64))
+        plan.backproject_host(got, pinned(scene.echoes), pinned(scene.antenna_pos), interp=interp)
+    assert np.array_equal(got.numpy(), ref), interp
+
+
 def test_pinned_accumulate(scene):
     p = scene.params
     rng = np.random.default_rng(4)
