@@ -285,7 +285,6 @@ struct PulseState {
     float4 t0;                    // hinge: table entry k0 + 1; sinc polynomial: lo_u, hi_u, k0, bin k0;
                                   // nearest pair: table entry (e_kn, e_kn+1)
     float2 t1d;                   // hinge: D part of entry k0; nearest pair: kn, bin kn
-    unsigned long long base;      // gather: row pointer + (kb - magic bias) entries, in bytes
     int kb;                       // row index the polynomial u is relative to
     int bin0;                     // row index of absolute bin 0
     int mode;
@@ -327,8 +326,8 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const int bin0 = __float_as_int(rd.y);               // row index of absolute bin 0
     // both bins must hold recorded samples: the identity behind the hinge
     // form does not hold across the zero entries outside 0 <= k <= nr - 2
-    const bool hinge = INTERP == INTERP_LINEAR && kind == REC_FAST && hi_u - k0 < 2.0f && idx0 >= bin0 &&
-                       idx0 + 1 <= bin0 + k.nr - 2;
+    const bool hinge = INTERP == INTERP_LINEAR && kind == REC_FAST && hi_u - k0 < 2.0f &&
+                       (unsigned)(idx0 - bin0) <= (unsigned)(k.nr - 3);
     PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
@@ -385,8 +384,6 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         st.q1 = make_float2(e1, e1);
         st.q2 = make_float2(e2, e2);
     }
-    st.base = reinterpret_cast<unsigned long long>(row) +
-              (unsigned long long)(long long)(kb - MAGIC_BITS) * 16ull;
     st.kb = kb;
     st.bin0 = bin0;
     return st;
@@ -436,9 +433,13 @@ __device__ __forceinline__ float4 gather(unsigned long long base, float biased_i
 }
 
 // General case: one gather per pixel.
-__device__ __forceinline__ void gather_pulse(const BpConst& k, const PulseState& st,
+__device__ __forceinline__ void gather_pulse(const BpConst& k, const PulseState& st, const float4* row,
                                              float2 (&accre)[NP], float2 (&accim)[NP])
 {
+    // row pointer + (kb - magic bias) entries, in bytes: adding the biased
+    // float bits of floor(u) + MAGIC gives the entry of bin kb + floor(u)
+    const unsigned long long base = reinterpret_cast<unsigned long long>(row) +
+                                    (unsigned long long)(long long)(st.kb - MAGIC_BITS) * 16ull;
     const float2 mm = make_float2(MAGIC, MAGIC);
     const float2 nmm = make_float2(-MAGIC, -MAGIC);
     const float2 neg1 = make_float2(-1.0f, -1.0f);
@@ -453,8 +454,8 @@ __device__ __forceinline__ void gather_pulse(const BpConst& k, const PulseState&
         const float2 fl = __fadd2_rn(tt, nmm);      // floor(u), exact
         const float2 f = __ffma2_rn(fl, neg1, u);   // u - floor(u), exact
         const float2 x = __fmul2_rn(f, cc);         // phase inside the bin, radians
-        const float4 va = gather(st.base, tt.x);
-        const float4 vb = gather(st.base, tt.y);
+        const float4 va = gather(base, tt.x);
+        const float4 vb = gather(base, tt.y);
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
         __sincosf(x.y, &sb, &cb);
@@ -1266,7 +1267,7 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
     if (st.mode == MODE_HINGE)
         hinge_pulse(k, st, accre, accim);
     else if (st.mode == MODE_GATHER)
-        gather_pulse(k, st, accre, accim);
+        gather_pulse(k, st, row, accre, accim);
     else if (st.mode == MODE_EXACT)
         exact_pulse(k, rec, row, a, xc, yrow, accre, accim);
 }
