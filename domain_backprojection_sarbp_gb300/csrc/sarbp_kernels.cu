@@ -292,8 +292,7 @@ struct PulseState {
 
 template <int INTERP>
 __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record& rec,
-                                                  const float4* row, float jf, float jf2,
-                                                  float jf3, float jf4)
+                                                  const float4* row, float jf)
 {
     if (on_heights(INTERP)) {
         PulseState st;
@@ -306,12 +305,13 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     const float hi = ra.y * jf;
     float lo = fmaf(ra.y, jf, -hi);
     lo = fmaf(ra.z, jf, lo);
-    const float small = fmaf(rb.y, jf4, fmaf(rb.x, jf3, fmaf(ra.w, jf2, ra.x + lo)));
+    // polynomials in the row offset jf by Horner's rule (only jf stays live)
+    const float small = fmaf(jf * jf, fmaf(jf, fmaf(jf, rb.y, rb.x), ra.w), ra.x + lo);
     const float t = hi + MAGIC;
     const float hir = t - MAGIC;
     const float e0 = (hi - hir) + small;
-    const float e1 = fmaf(rc.y, jf3, fmaf(rc.x, jf2, fmaf(rb.w, jf, rb.z)));
-    const float e2 = fmaf(rd.x, jf2, fmaf(rc.w, jf, rc.z));
+    const float e1 = fmaf(jf, fmaf(jf, fmaf(jf, rc.y, rc.x), rb.w), rb.z);
+    const float e2 = fmaf(jf, fmaf(jf, rd.x, rc.w), rc.z);
     const int kb = __float_as_int(rd.z) + (__float_as_int(t) - MAGIC_BITS);
     const int kind = __float_as_int(rd.w);
 
@@ -1296,9 +1296,6 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
     const float jf = (float)jr - 0.5f * (TILE_Y - 1);
-    const float jf2 = jf * jf;
-    const float jf3 = jf2 * jf;
-    const float jf4 = jf2 * jf2;
     const long long b = blockIdx.x;
     const long long u0 = cta_start(k, b);
     const long long u1 = cta_start(k, b + 1);
@@ -1369,19 +1366,19 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const float4* rows = table + (size_t)c0 * k.W;
             // Two pulse states in ping-pong: the state of pulse p + 1 is built
             // while pulse p is applied, with no copy between them.
-            PulseState sa = pulse_setup<INTERP>(k, s_rec[0], rows, jf, jf2, jf3, jf4);
+            PulseState sa = pulse_setup<INTERP>(k, s_rec[0], rows, jf);
 #pragma unroll 1
             for (int p = 0; p < cnt; p += 2) {
                 const int p1 = min(p + 1, cnt - 1);
                 const PulseState sb =
-                    pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf, jf2, jf3, jf4);
+                    pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
                                   s_hp + jr * HROW4, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
-                sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf, jf2, jf3, jf4);
+                sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
                                   s_hp + jr * HROW4, psi, accre, accim);
