@@ -132,6 +132,11 @@ sarbp_status sarbp_plan(sarbp_plan_t* out, const sarbp_params* p);
  *
  * The inputs must stay valid and unmodified until the work on `stream` has
  * finished. A pulse whose antenna position is not finite contributes nothing.
+ * Echo samples should be finite: a non-finite sample makes non-finite every
+ * pixel whose interpolation uses it, and may also reach the other pixels of
+ * the same 32-pixel row segment that take their samples from the adjacent
+ * bin in that pulse (the two-bin form combines both bins). Samples no pixel
+ * can reach are never used.
  * Two calls with identical inputs give bitwise identical images (the pulse
  * sum has a fixed order). Null pointers are accepted only where the matching
  * array is empty.

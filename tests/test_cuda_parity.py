@@ -31,7 +31,8 @@ def _built():
     __graft_entry__.build()
 
 
-def gpu_image(params, echoes, pos, plan=None, accumulate=False, init=None, stream=None):
+def gpu_image(params, echoes, pos, plan=None, accumulate=False, init=None, stream=None,
+              interp="linear"):
     p = dict(params)
     e = torch.from_numpy(np.ascontiguousarray(echoes, dtype=np.complex64)).to(DEV)
     a = torch.from_numpy(np.ascontiguousarray(pos, dtype=np.float64)).to(DEV)
@@ -41,7 +42,7 @@ def gpu_image(params, echoes, pos, plan=None, accumulate=False, init=None, strea
     own = plan is None
     plan = plan or Plan(p)
     try:
-        plan.backproject(img, e, a, params=p, accumulate=accumulate, stream=stream)
+        plan.backproject(img, e, a, params=p, accumulate=accumulate, stream=stream, interp=interp)
         torch.cuda.synchronize()
     finally:
         if own:
@@ -210,6 +211,33 @@ def test_nan_guard_bands_untouched():
     got = img.cpu().numpy()
     assert np.all(np.isfinite(got))
     parity.assert_parity(got, oracle.backproject(sc.params, sc.echoes, sc.antenna_pos), "guards")
+
+
+@pytest.mark.parametrize("interp", ["linear", "sinc8", "nearest"])
+def test_unreachable_nonfinite_samples_are_ignored(interp):
+    """Samples more than 8 bins outside the ranges a pulse can reach from the
+    image (nearest and farthest point of the image rectangle) are set to NaN
+    and infinity: the image must be the clean one bit for bit."""
+    sc = scenes.make_scene(scenes.CONFIGS[1])
+    p = sc.params
+    xa, xb = p["x0"], p["x0"] + (p["nx"] - 1) * p["dx"]
+    ya, yb = p["y0"], p["y0"] + (p["ny"] - 1) * p["dy"]
+    dirty = sc.echoes.copy()
+    k = np.arange(p["nr"])
+    for n, (ax, ay, az) in enumerate(sc.antenna_pos):
+        dz = p["z0"] - az
+        rmin = np.sqrt((np.clip(ax, xa, xb) - ax) ** 2 + (np.clip(ay, ya, yb) - ay) ** 2 + dz * dz)
+        rmax = np.sqrt(max(abs(xa - ax), abs(xb - ax)) ** 2 + max(abs(ya - ay), abs(yb - ay)) ** 2
+                       + dz * dz)
+        lo = np.floor((rmin - p["r0"]) / p["dr"]) - 8
+        hi = np.floor((rmax - p["r0"]) / p["dr"]) + 9
+        out = (k < lo) | (k > hi)
+        dirty[n, out & (k % 2 == 0)] = complex(np.nan, np.nan)
+        dirty[n, out & (k % 2 == 1)] = complex(np.inf, -np.inf)
+    assert np.isnan(dirty).sum() > dirty.size // 4
+    clean = gpu_image(p, sc.echoes, sc.antenna_pos, interp=interp)
+    got = gpu_image(p, dirty, sc.antenna_pos, interp=interp)
+    assert np.array_equal(got, clean), interp
 
 
 def test_range_window_edges_full_window():
