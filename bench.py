@@ -167,10 +167,17 @@ def oracle_rate(scene, seconds: float = 8.0, threads: int = 0, seed: int = 0):
     import oracle
     rng = np.random.default_rng(seed)
     npx = scene.params["nx"] * scene.params["ny"]
-    probe = rng.choice(npx, size=64, replace=False)
-    _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, probe,
-                                       threads=threads, return_info=True)
-    per_pixel = max(secs, 1e-6) / probe.size
+    # two calibration runs: the first (64 pixels) is dominated by thread start-up
+    # and overestimates the cost per pixel; the second takes about a tenth of
+    # the requested time
+    per_pixel = None
+    size = 64
+    for _ in range(2):
+        probe = rng.choice(npx, size=min(npx, size), replace=False)
+        _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, probe,
+                                           threads=threads, return_info=True)
+        per_pixel = max(secs, 1e-6) / probe.size
+        size = int(max(64, 0.1 * seconds / per_pixel))
     count = int(min(npx, max(256, seconds / per_pixel)))
     pix = rng.choice(npx, size=count, replace=False)
     _, secs, used = oracle.backproject(scene.params, scene.echoes, scene.antenna_pos, pix,
