@@ -36,11 +36,17 @@
 //    directly; the pieces of a shared tile go to partial buffers that
 //    reduce_kernel sums in CTA order, so the result is deterministic.
 //
-// 4. Variants of the same kernel (template INTERP): the 8-tap windowed sinc
-//    (a degree-4 polynomial per thread and pulse when the thread's pixels span
-//    at most a quarter bin), the nearest sample (one table entry per thread
-//    and pulse when its pixels round to two bins), and pixels on a height map
-//    (a float-pair row reference and a range series per pixel).
+// 4. Linear interpolation, two-entry form: when a thread's 32 pixels fall in
+//    two range bins, the interpolated, phase-compensated samples are one line
+//    plus a hinge in y = c (u - k0 - 1) (hinge_pulse): two table entries per
+//    thread and pulse, no per-pixel gather; other threads gather per pixel.
+//
+// 5. Variants of the same kernel (template INTERP): the 8-tap windowed sinc
+//    (a degree-4 or, on narrower spans, degree-3 polynomial per thread and
+//    pulse when the thread's pixels span at most a quarter bin), the nearest
+//    sample (one table entry per thread and pulse when its pixels round to
+//    two bins), and pixels on a height map (a float-pair row reference and a
+//    range series per pixel, with the two-entry form for rows in two bins).
 #include "sarbp_internal.h"
 
 #include <cmath>
