@@ -221,8 +221,11 @@ def cpu_baseline(scene, seconds: float):
         one_thread={"value": one["value"], "unit": UNIT, "sample": one["sample"]},
         extrapolated_full_image_s={"all_cores": updates / (allc["value"] * 1e9),
                                    "one_thread": updates / (one["value"] * 1e9)},
-        page_figure={"one_thread_cpu_s": 56.0, "scene": "Na=4096 pulses, 1024x1024 image",
-                     "cpu": "not stated on the page"})
+        page_figure={"one_thread_cpu_s": 56.0, "gpu_s_per_frame": 0.8,
+                     "scene": "Na=4096 pulses, 1024x1024 image",
+                     "hardware": "RTX 3080 GPU; CPU not stated",
+                     "speedup_over_one_thread": "more than 70x",
+                     "serial_cpu_vs_gpu": "about 50 min against under 1 min (scene not stated)"})
     return allc
 
 
