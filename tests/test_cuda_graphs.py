@@ -133,3 +133,25 @@ def test_volume_and_height_map_graphs(scene):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(vol, vol0) and torch.equal(img, img0)
+
+
+def test_two_plans_on_two_streams_at_once(scene):
+    """Plans are independent: two plans enqueued on two streams at the same
+    time (linear and sinc, different images) give the images each computes
+    alone, bit for bit."""
+    p = scene.params
+    echoes, pos = _dev(scene.echoes), _dev(scene.antenna_pos)
+    with Plan(p) as pa, Plan(p) as pb:
+        solo = []
+        for plan, interp in ((pa, "linear"), (pb, "sinc8")):
+            img = torch.zeros((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+            plan.backproject(img, echoes, pos, interp=interp)
+            torch.cuda.synchronize()
+            solo.append(img)
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        both = [torch.zeros_like(solo[0]), torch.zeros_like(solo[1])]
+        for _ in range(3):
+            pa.backproject(both[0], echoes, pos, interp="linear", stream=sa)
+            pb.backproject(both[1], echoes, pos, interp="sinc8", stream=sb)
+        torch.cuda.synchronize()
+        assert torch.equal(both[0], solo[0]) and torch.equal(both[1], solo[1])
