@@ -31,7 +31,8 @@ struct sarbp_plan_s {
     double h_min = 0.0, h_max = 0.0; // its height bounds
     float4* table_alloc = nullptr;   // (na * W + 2 * TABLE_PAD) entries
     int* klo = nullptr;              // na
-    float2* psi = nullptr;           // nr: per-bin phasors (windowed-sinc interpolation)
+    float2* psi = nullptr;           // nr + 1: per-bin phasors (windowed-sinc interpolation),
+                                     // then one word: the wide-sinc flag of the last call
     float4* partial = nullptr;       // 2 * max_ctas * TILE_PIX / 2
     int max_ctas = 0;
     size_t scratch_bytes = 0;
@@ -317,7 +318,14 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
     if (echo_stride > 0)
         k.echo_stride = echo_stride;
     float4* table = plan->table_alloc + TABLE_PAD;
-    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo, s);
+    int* sinc_wide = reinterpret_cast<int*>(plan->psi + params->nr + 1);
+    if (k.flags & SARBP_SINC8) {
+        e = cudaMemsetAsync(sinc_wide, 0, sizeof(int), s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "cudaMemsetAsync");
+    }
+    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo,
+                     sinc_wide, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "table kernel launch");
     if (k.flags & (SARBP_SINC8 | SARBP_NEAREST)) {
@@ -344,7 +352,7 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         cudaEventRecord(ev->first, s);
     }
     e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
-                           plan->partial, plan->psi, heights, s);
+                           plan->partial, plan->psi, heights, sinc_wide, s);
     if (ev)
         cudaEventRecord(ev->second, s);
     if (e != cudaSuccess)
@@ -459,9 +467,9 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
         free_plan(plan);
         return SARBP_ERR_UNSUPPORTED_DEVICE;
     }
-    e = backproject_occupancy(&plan->ctas_per_sm);
-    if (e == cudaSuccess && heights_mode)
-        e = prepare_heights_kernel();
+    e = prepare_kernels();
+    if (e == cudaSuccess)
+        e = backproject_occupancy(&plan->ctas_per_sm);
     if (e != cudaSuccess || plan->ctas_per_sm < 1) {
         st = cuda_fail(plan, e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "occupancy");
         free_plan(plan);
@@ -495,7 +503,7 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
         const size_t table_entries = (size_t)p->na * plan->W + 2 * TABLE_PAD;
         const size_t sizes[4] = {table_entries * sizeof(float4), (size_t)p->na * sizeof(int),
                                  (size_t)plan->max_ctas * TILE_PIX * sizeof(float4),
-                                 ((size_t)p->nr + 1) * sizeof(float2)};
+                                 ((size_t)p->nr + 2) * sizeof(float2)};
         void** ptrs[4] = {reinterpret_cast<void**>(&plan->table_alloc),
                           reinterpret_cast<void**>(&plan->klo),
                           reinterpret_cast<void**>(&plan->partial),
@@ -563,8 +571,11 @@ sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out)
     out->full_window = plan->full_window;
     out->kernels_per_call = 0;
     if (plan->tiles > 0 && plan->p.na > 0 && plan->p.nr >= 2)
+        // table + main (+ reduce); the phasor kernel for sinc and nearest; sinc on a
+        // plane also enqueues its wide-geometry kernel (one of the two exits at once)
         out->kernels_per_call = (any_split_tile(make_const(plan, &plan->p)) ? 3 : 2) +
-                                ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0);
+                                ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0) +
+                                ((plan->p.flags & SARBP_SINC8) && !plan->heights_mode ? 1 : 0);
     else if (plan->tiles > 0)
         out->kernels_per_call = 0;   // a memset at most
     out->scratch_bytes = plan->scratch_bytes;
@@ -1065,10 +1076,11 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
         k.ctas = geo.tiles;                     // one whole tile per CTA: direct writes only
         k.units = (long long)geo.tiles * cn;
         e = launch_table(k, ech + (size_t)c0 * params->nr, antenna_pos + 3 * (size_t)c0, table,
-                         klo, s);
+                         klo, nullptr, s);
         if (e == cudaSuccess)
             e = launch_backproject(k, antenna_pos + 3 * (size_t)c0, table, klo,
-                                   static_cast<float2*>(image), nullptr, nullptr, nullptr, s);
+                                   static_cast<float2*>(image), nullptr, nullptr, nullptr, nullptr,
+                                   s);
         if (e != cudaSuccess)
             return SARBP_ERR_CUDA;
     }

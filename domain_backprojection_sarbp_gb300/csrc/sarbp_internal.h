@@ -69,13 +69,17 @@ struct BpConst {
     float i0;                    // column offset of a thread's first pixel from the tile centre
 };
 
+// sinc_wide (sinc only, else null): set to 1 when a thread's pixels can span more
+// range bins than the narrow sinc kernel's polynomial modes cover
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos,
-                         float4* table, int* klo, cudaStream_t s);
+                         float4* table, int* klo, int* sinc_wide, cudaStream_t s);
 cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s);
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
                                const int* klo, float2* image, float4* partial,
-                               const float2* psi, const float* heights, cudaStream_t s);
-cudaError_t prepare_heights_kernel();
+                               const float2* psi, const float* heights, const int* sinc_wide,
+                               cudaStream_t s);
+// Dynamic shared-memory limits of the kernels that use more than the default.
+cudaError_t prepare_kernels();
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);

@@ -63,7 +63,18 @@ constexpr int MAGIC_BITS = 0x4B400000; // bit pattern of MAGIC
 enum Interp : int { INTERP_LINEAR = 0, INTERP_SINC8 = 1, INTERP_NEAREST = 2, INTERP_HEIGHTS = 3,
                     INTERP_HEIGHTS_SINC8 = 4, INTERP_HEIGHTS_NEAREST = 5 };
 // pixels on a height map, with the linear, windowed-sinc or nearest interpolation
-__host__ __device__ constexpr bool on_heights(int interp) { return interp >= INTERP_HEIGHTS; }
+__host__ __device__ constexpr bool on_heights(int interp)
+{
+    return interp >= INTERP_HEIGHTS && interp <= INTERP_HEIGHTS_NEAREST;
+}
+// the windowed sinc on the plane: INTERP_SINC8 for geometries where every
+// thread's pixels span at most SINC_SPAN bins, INTERP_SINC8_WIDE (with the
+// two-half polynomial mode, and more registers in use) for the others
+constexpr int INTERP_SINC8_WIDE = 6;
+__host__ __device__ constexpr bool is_sinc(int interp)
+{
+    return interp == INTERP_SINC8 || interp == INTERP_SINC8_WIDE;
+}
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
 constexpr float SINC_SPAN3 = 0.11f;         // widest spread for the cubic on four nodes
@@ -87,7 +98,8 @@ template <bool SINC>
 __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __restrict__ echo,
                                                     const double* __restrict__ pos,
                                                     float4* __restrict__ table,
-                                                    int* __restrict__ klo)
+                                                    int* __restrict__ klo,
+                                                    int* __restrict__ sinc_wide)
 {
     const int n = blockIdx.x;
     __shared__ int s_lo;
@@ -111,6 +123,14 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
             double u = (rmin - (k.heights_mode ? k.qmax3 : k.qmax) - k.r0) * k.inv_dr;
             u = fmin(fmax(u, -1.0e9), 1.0e9);
             lo = (int)floor(u) - MARGIN;
+            if (SINC && sinc_wide) {
+                // a thread's 32 pixels span about 31 dx |g_x| / dr bins, |g_x| at
+                // most the largest x distance over the nearest range; above
+                // SINC_SPAN (with a margin for the curvature) the wide kernel runs
+                const double gx = fmax(fabs(k.rect_x0 - ax), fabs(k.rect_x1 - ax)) / fmax(rmin, 1.0);
+                if ((TILE_X - 1) * k.dx * gx * k.inv_dr + 0.01 > (double)SINC_SPAN)
+                    atomicOr(sinc_wide, 1);
+            }
         }
         s_lo = lo;
         klo[n] = lo;
@@ -284,7 +304,7 @@ constexpr int NP = TILE_X / 2;
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
-                       MODE_PAIR = 5, MODE_POLY3 = 6 };
+                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
@@ -295,6 +315,34 @@ struct PulseState {
     int bin0;                     // row index of absolute bin 0
     int mode;
 };
+
+// Bounds of u = e0 + e1 i + e2 i^2 over the 16 pixel offsets i in m +- 7.5
+// (m = -8: the left half of a thread's pixels, lanes .x; m = 8: the right half,
+// lanes .y).
+__device__ __forceinline__ void half_bounds(float e0, float e1, float e2, float m, float& lo,
+                                            float& hi)
+{
+    const float um = fmaf(m, fmaf(m, e2, e1), e0);
+    const float sl = fabsf(fmaf(2.0f * e2, m, e1));
+    lo = um - 7.5f * sl - 56.25f * fmaxf(-e2, 0.0f);
+    hi = um + 7.5f * sl + 56.25f * fmaxf(e2, 0.0f);
+}
+
+// The interval of a polynomial: [lo, hi] widened to a half-width of at least
+// SINC_HALF_MIN, its first bin k0 (row units) and k0's absolute bin; true when
+// it spans at most SINC_SPAN bins and the stencils of bins k0 and k0 + 1 lie
+// inside the recorded range.
+__device__ __forceinline__ bool poly_interval(const BpConst& k, int kb, int bin0, float lo, float hi,
+                                              float& lo_e, float& hi_e, float& k0, int& kabs0)
+{
+    const float mid = 0.5f * (lo + hi);
+    lo_e = fminf(lo, mid - SINC_HALF_MIN);
+    hi_e = fmaxf(hi, mid + SINC_HALF_MIN);
+    const float tke = __fadd_rd(lo_e, MAGIC);
+    k0 = tke - MAGIC;
+    kabs0 = kb + (__float_as_int(tke) - MAGIC_BITS) - bin0;
+    return hi_e - lo_e <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1;
+}
 
 template <int INTERP>
 __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record& rec,
@@ -337,24 +385,29 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     PulseState st;
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
-    if (INTERP == INTERP_SINC8 && kind == REC_FAST) {
+    if (is_sinc(INTERP) && kind == REC_FAST) {
         // windowed sinc: when the thread's pixels span at most a quarter bin and
         // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
-        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN). The
-        // interval is widened to at least 1/32 bin so that the monomial
-        // coefficients in u - mid stay bounded.
-        const float mid = 0.5f * (lo_u + hi_u);
-        const float lo_e = fminf(lo_u, mid - SINC_HALF_MIN), hi_e = fmaxf(hi_u, mid + SINC_HALF_MIN);
-        const float tke = __fadd_rd(lo_e, MAGIC);
-        const float k0e = tke - MAGIC;
-        const int kabs0 = kb + (__float_as_int(tke) - MAGIC_BITS) - bin0;
-        if (hi_e - lo_e <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1) {
+        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN); when each
+        // half of its pixels does, one polynomial per half (MODE_POLY2H)
+        float lo_e, hi_e, k0e;
+        int kabs0;
+        if (poly_interval(k, kb, bin0, lo_u, hi_u, lo_e, hi_e, k0e, kabs0)) {
             st.mode = hi_e - lo_e <= SINC_SPAN3 ? MODE_POLY3 : MODE_POLY;
             st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
+        } else if (INTERP == INTERP_SINC8_WIDE) {
+            float lo, hi, lh, hh, kh;
+            int ka;
+            half_bounds(e0, e1, e2, -8.0f, lo, hi);
+            bool ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka);
+            half_bounds(e0, e1, e2, 8.0f, lo, hi);
+            ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
+            if (ok)
+                st.mode = MODE_POLY2H;
         }
     }
     if (st.mode != MODE_POLY && st.mode != MODE_POLY3)
-        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
+        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);   // MODE_POLY2H recomputes its intervals
     st.t1d = make_float2(0.f, 0.f);
     float kn = 0.0f;
     if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
@@ -647,36 +700,91 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
     return sinc_sum(f, row + (kr - 3));
 }
 
-// The per-pixel part of the polynomial mode: coefficients p[0 .. ND-1] of the
-// interpolant in t = (u - mid) / half, evaluated per pixel in s = u - mid
-// with the echo phase psi_k0 exp(j c (u - k0)).
-template <int ND>
-__device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
-                                                const float2* __restrict__ psi, const float2 (&p)[5],
-                                                float mid, float half, float k0, int kabs0,
-                                                float2 (&accre)[NP], float2 (&accim)[NP])
+// Monomial coefficients p[n] (complex, in t = (u - mid) / half) of the
+// interpolant of G on [mid - half, mid + half] at NN Chebyshev nodes
+// (NN = 5: degree 4; NN = 4: degree 3), by the inverse Vandermonde matrix.
+template <int NN>
+__device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const float4* row,
+                                            float2 (&p)[5])
 {
-    // coefficients in s = u - mid (t = s / half), psi_k0 folded in
-    const float2 ps = __ldg(psi + kabs0);
+    if (NN == 4) {
+        constexpr float C1 = 0.923879533f, C2 = 0.382683432f;   // cos(pi/8), cos(3 pi/8)
+        const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
+        const float2 g1 = sinc_value(fmaf(half, C2, mid), kb, row);
+        const float2 g2 = sinc_value(fmaf(half, -C2, mid), kb, row);
+        const float2 g3 = sinc_value(fmaf(half, -C1, mid), kb, row);
+        const float2 s03 = make_float2(g0.x + g3.x, g0.y + g3.y), d03 = make_float2(g0.x - g3.x, g0.y - g3.y);
+        const float2 s12 = make_float2(g1.x + g2.x, g1.y + g2.y), d12 = make_float2(g1.x - g2.x, g1.y - g2.y);
+        p[0] = make_float2(fmaf(-0.103553391f, s03.x, 0.603553391f * s12.x),
+                           fmaf(-0.103553391f, s03.y, 0.603553391f * s12.y));
+        p[1] = make_float2(fmaf(-0.112085382f, d03.x, 1.577161015f * d12.x),
+                           fmaf(-0.112085382f, d03.y, 1.577161015f * d12.y));
+        p[2] = make_float2(0.707106781f * (s03.x - s12.x), 0.707106781f * (s03.y - s12.y));
+        p[3] = make_float2(fmaf(0.765366865f, d03.x, -1.847759065f * d12.x),
+                           fmaf(0.765366865f, d03.y, -1.847759065f * d12.y));
+        p[4] = make_float2(0.0f, 0.0f);
+        return;
+    }
+    constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
+    const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
+    const float2 g1 = sinc_value(fmaf(half, C2, mid), kb, row);
+    const float2 g2 = sinc_value(mid, kb, row);
+    const float2 g3 = sinc_value(fmaf(half, -C2, mid), kb, row);
+    const float2 g4 = sinc_value(fmaf(half, -C1, mid), kb, row);
+    const float2 s04 = make_float2(g0.x + g4.x, g0.y + g4.y), d04 = make_float2(g0.x - g4.x, g0.y - g4.y);
+    const float2 s13 = make_float2(g1.x + g3.x, g1.y + g3.y), d13 = make_float2(g1.x - g3.x, g1.y - g3.y);
+    p[0] = g2;
+    p[1] = make_float2(fmaf(1.376381920f, d13.x, -0.324919696f * d04.x),
+                       fmaf(1.376381920f, d13.y, -0.324919696f * d04.y));
+    p[2] = make_float2(fmaf(-0.341640786f, s04.x, fmaf(2.341640786f, s13.x, -4.0f * g2.x)),
+                       fmaf(-0.341640786f, s04.y, fmaf(2.341640786f, s13.y, -4.0f * g2.y)));
+    p[3] = make_float2(fmaf(0.940456404f, d04.x, -1.521690426f * d13.x),
+                       fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
+    p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
+                       fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
+}
+
+// The coefficients in s = u - mid with psi_k0 folded in, p[n] psi_k0 / half^n,
+// written into lane LANE (0: .x, 1: .y, 2: both) of the pairs pr (real parts)
+// and pi (imaginary parts).
+template <int ND, int LANE>
+__device__ __forceinline__ void poly_fold(const float2 (&p)[5], float2 ps, float half,
+                                          float2 (&pr)[5], float2 (&pi)[5])
+{
     const float ih = rcp_approx(half);            // half >= SINC_HALF_MIN
-    float2 pr[5], pi[5];
     float sc = 1.0f;
 #pragma unroll
     for (int n = 0; n < ND; ++n) {
         const float psr = ps.x * sc, psi_ = ps.y * sc;
         const float re = p[n].x * psr - p[n].y * psi_;
         const float im = p[n].x * psi_ + p[n].y * psr;
-        pr[n] = make_float2(re, re);
-        pi[n] = make_float2(im, im);
+        if (LANE != 1) {
+            pr[n].x = re;
+            pi[n].x = im;
+        }
+        if (LANE != 0) {
+            pr[n].y = re;
+            pi[n].y = im;
+        }
         sc *= ih;
     }
-    // echo phase c (u - k0) = c s + c (mid - k0)
+}
+
+// The per-pixel part of the polynomial modes: lane .x of every pixel pair
+// (the left 16 pixels) evaluates the .x coefficients about midL, lane .y (the
+// right 16) the .y coefficients about midR, each with the echo
+// phase psi_k0 exp(j c (u - k0)) of its own k0 (folded into the coefficients
+// and cm = c (mid - k0)).
+template <int ND>
+__device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
+                                                const float2 (&pr)[5], const float2 (&pi)[5],
+                                                float midL, float midR, float cmL, float cmR,
+                                                float2 (&accre)[NP], float2 (&accim)[NP])
+{
     const float c = k.c_phase;
     const float2 c2 = make_float2(c, c);
-    const float cm = c * (mid - k0);
-    const float2 cm2 = make_float2(cm, cm);
-    const float s0 = st.q0.x - mid;
-    const float2 q0s = make_float2(s0, s0);
+    const float2 cm2 = make_float2(cmL, cmR);
+    const float2 q0s = make_float2(st.q0.x - midL, st.q0.x - midR);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
@@ -722,47 +830,14 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
     const float lo_u = st.t0.x, hi_u = st.t0.y, k0 = st.t0.z;
     const int kabs0 = __float_as_int(st.t0.w);
     const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
-    // monomial coefficients of the interpolant (inverse Vandermonde of the nodes)
-    float2 p[5];
-    if (NN == 4) {
-        constexpr float C1 = 0.923879533f, C2 = 0.382683432f;   // cos(pi/8), cos(3 pi/8)
-        const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
-        const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
-        const float2 g2 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
-        const float2 g3 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
-        const float2 s03 = make_float2(g0.x + g3.x, g0.y + g3.y), d03 = make_float2(g0.x - g3.x, g0.y - g3.y);
-        const float2 s12 = make_float2(g1.x + g2.x, g1.y + g2.y), d12 = make_float2(g1.x - g2.x, g1.y - g2.y);
-        p[0] = make_float2(fmaf(-0.103553391f, s03.x, 0.603553391f * s12.x),
-                           fmaf(-0.103553391f, s03.y, 0.603553391f * s12.y));
-        p[1] = make_float2(fmaf(-0.112085382f, d03.x, 1.577161015f * d12.x),
-                           fmaf(-0.112085382f, d03.y, 1.577161015f * d12.y));
-        p[2] = make_float2(0.707106781f * (s03.x - s12.x), 0.707106781f * (s03.y - s12.y));
-        p[3] = make_float2(fmaf(0.765366865f, d03.x, -1.847759065f * d12.x),
-                           fmaf(0.765366865f, d03.y, -1.847759065f * d12.y));
-        p[4] = make_float2(0.0f, 0.0f);
-        sinc_poly_apply<4>(k, st, psi, p, mid, half, k0, kabs0, accre, accim);
-        return;
-    }
-    constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
-    const float2 g0 = sinc_value(fmaf(half, C1, mid), st.kb, row);
-    const float2 g1 = sinc_value(fmaf(half, C2, mid), st.kb, row);
-    const float2 g2 = sinc_value(mid, st.kb, row);
-    const float2 g3 = sinc_value(fmaf(half, -C2, mid), st.kb, row);
-    const float2 g4 = sinc_value(fmaf(half, -C1, mid), st.kb, row);
-    const float2 s04 = make_float2(g0.x + g4.x, g0.y + g4.y), d04 = make_float2(g0.x - g4.x, g0.y - g4.y);
-    const float2 s13 = make_float2(g1.x + g3.x, g1.y + g3.y), d13 = make_float2(g1.x - g3.x, g1.y - g3.y);
-    p[0] = g2;
-    p[1] = make_float2(fmaf(1.376381920f, d13.x, -0.324919696f * d04.x),
-                       fmaf(1.376381920f, d13.y, -0.324919696f * d04.y));
-    p[2] = make_float2(fmaf(-0.341640786f, s04.x, fmaf(2.341640786f, s13.x, -4.0f * g2.x)),
-                       fmaf(-0.341640786f, s04.y, fmaf(2.341640786f, s13.y, -4.0f * g2.y)));
-    p[3] = make_float2(fmaf(0.940456404f, d04.x, -1.521690426f * d13.x),
-                       fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
-    p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
-                       fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
-    sinc_poly_apply<5>(k, st, psi, p, mid, half, k0, kabs0, accre, accim);
+    float2 p[5], pr[5], pi[5];
+    poly_coeffs<NN>(mid, half, st.kb, row, p);
+    poly_fold<NN, 2>(p, __ldg(psi + kabs0), half, pr, pi);
+    const float cm = k.c_phase * (mid - k0);
+    sinc_poly_apply<NN>(k, st, pr, pi, mid, mid, cm, cm, accre, accim);
 }
 
+// Any span: the 8 taps evaluated per pixel.
 __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& st, const float4* row,
                                            const float2* __restrict__ psi,
                                            float2 (&accre)[NP], float2 (&accim)[NP])
@@ -777,6 +852,52 @@ __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& s
         sinc_pixel<false>(k, ub, st.kb, st.bin0, row, psi, re, im);
     }
 }
+
+// Spans up to about twice SINC_SPAN (INTERP_SINC8_WIDE): the left and right
+// 16 pixels (lanes .x and .y of every pair) each get their own degree-4
+// interpolant over their own interval (the same error bound), at no extra cost
+// per pixel. The halves' intervals were checked by pulse_setup.
+__device__ __forceinline__ void sinc_poly_halves_pulse(const BpConst& k, const PulseState& st,
+                                                       const float4* row,
+                                                       const float2* __restrict__ psi,
+                                                       float4* stash,
+                                                       float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
+    float midL = 0.0f, cmL = 0.0f, midR = 0.0f, cmR = 0.0f;
+    // one half per pass (one copy of the node code); each half's coefficients
+    // go to this thread's own shared-memory slots (stride THREADS)
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        float lo, hi, lo_e, hi_e, k0;
+        int ka;
+        half_bounds(e0, e1, e2, h ? 8.0f : -8.0f, lo, hi);
+        poly_interval(k, st.kb, st.bin0, lo, hi, lo_e, hi_e, k0, ka);
+        const float mid = 0.5f * (lo_e + hi_e), half = 0.5f * (hi_e - lo_e);
+        float2 p[5], cr[5], ci[5];
+        poly_coeffs<5>(mid, half, st.kb, row, p);
+        poly_fold<5, 0>(p, __ldg(psi + ka), half, cr, ci);
+        float4* slot = stash + 3 * h * THREADS;
+        slot[0] = make_float4(cr[0].x, ci[0].x, cr[1].x, ci[1].x);
+        slot[THREADS] = make_float4(cr[2].x, ci[2].x, cr[3].x, ci[3].x);
+        slot[2 * THREADS] = make_float4(cr[4].x, ci[4].x, 0.0f, 0.0f);
+        if (h == 0) {
+            midL = mid;
+            cmL = k.c_phase * (mid - k0);
+        } else {
+            midR = mid;
+            cmR = k.c_phase * (mid - k0);
+        }
+    }
+    const float4 l0 = stash[0], l1 = stash[THREADS], l2 = stash[2 * THREADS];
+    const float4 r0 = stash[3 * THREADS], r1 = stash[4 * THREADS], r2 = stash[5 * THREADS];
+    const float2 pr[5] = {make_float2(l0.x, r0.x), make_float2(l0.z, r0.z), make_float2(l1.x, r1.x),
+                          make_float2(l1.z, r1.z), make_float2(l2.x, r2.x)};
+    const float2 pi[5] = {make_float2(l0.y, r0.y), make_float2(l0.w, r0.w), make_float2(l1.y, r1.y),
+                          make_float2(l1.w, r1.w), make_float2(l2.y, r2.y)};
+    sinc_poly_apply<5>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
+}
+
 
 __device__ __forceinline__ void sinc_exact_pulse(const BpConst& k, const Record& rec, const float4* row,
                                                  const double* __restrict__ a, double xc,
@@ -1240,7 +1361,7 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, const HRow& hr, const float4* s_hp,
+                                            double yrow, const HRow& hr, const float4* s_hp, float4* stash,
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
@@ -1259,11 +1380,13 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
             nearest_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
         return;
     }
-    if (INTERP == INTERP_SINC8) {
+    if (is_sinc(INTERP)) {
         if (st.mode == MODE_POLY3)
             sinc_poly_pulse<4>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_POLY)
             sinc_poly_pulse<5>(k, st, row, psi, accre, accim);
+        else if (INTERP == INTERP_SINC8_WIDE && st.mode == MODE_POLY2H)
+            sinc_poly_halves_pulse(k, st, row, psi, stash, accre, accim);
         else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
@@ -1293,11 +1416,17 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                                                         float2* __restrict__ image,
                                                         float4* __restrict__ partial,
                                                         const float2* __restrict__ psi,
-                                                        const float* __restrict__ heights)
+                                                        const float* __restrict__ heights,
+                                                        const int* __restrict__ sinc_wide)
 {
+    // the two sinc kernels are both launched; the flag the table kernel set
+    // says which one does the work
+    if (is_sinc(INTERP) && ((*sinc_wide != 0) != (INTERP == INTERP_SINC8_WIDE)))
+        return;
     __shared__ Record s_rec[CHUNK];
     // heights mode: per row, HROW4 float4 (dz[q], dz[q + 16], P[q], P[q + 16]) with
     // dz = h - hrow and P = (i dx)^2 + dz^2 for the pixels at offsets i of q and q + 16
+    // wide sinc: six float4 per thread hold the two halves' coefficients
     extern __shared__ float4 s_hp[];
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
@@ -1380,14 +1509,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
-                                  s_hp + jr * HROW4, psi, accre, accim);
+                                  s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
-                                  s_hp + jr * HROW4, psi, accre, accim);
+                                  s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
             }
         }
 
@@ -1535,12 +1664,13 @@ cudaError_t noalloc_scratch(void** ptr)
 }
 
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
-                         int* klo, cudaStream_t s)
+                         int* klo, int* sinc_wide, cudaStream_t s)
 {
     if (k.flags & (FLAG_SINC8 | FLAG_NEAREST))
-        table_kernel<true><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+        table_kernel<true><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo,
+                                                (k.flags & FLAG_SINC8) ? sinc_wide : nullptr);
     else
-        table_kernel<false><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo);
+        table_kernel<false><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo, nullptr);
     return cudaGetLastError();
 }
 
@@ -1551,10 +1681,14 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
 }
 
 constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW4 * sizeof(float4);
+constexpr size_t SINC_SMEM = (size_t)6 * THREADS * sizeof(float4);
 
-cudaError_t prepare_heights_kernel()
+cudaError_t prepare_kernels()
 {
-    cudaError_t e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>,
+    cudaError_t e = cudaFuncSetAttribute(bp_kernel<INTERP_SINC8_WIDE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SINC_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)HEIGHTS_SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS_SINC8>,
@@ -1567,26 +1701,32 @@ cudaError_t prepare_heights_kernel()
 
 cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4* table,
                                const int* klo, float2* image, float4* partial,
-                               const float2* psi, const float* heights, cudaStream_t s)
+                               const float2* psi, const float* heights, const int* sinc_wide,
+                               cudaStream_t s)
 {
     if (k.heights_mode && (k.flags & FLAG_SINC8))
         bp_kernel<INTERP_HEIGHTS_SINC8><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(
-            k, pos, table, klo, image, partial, psi, heights);
+            k, pos, table, klo, image, partial, psi, heights, nullptr);
     else if (k.heights_mode && (k.flags & FLAG_NEAREST))
         bp_kernel<INTERP_HEIGHTS_NEAREST><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(
-            k, pos, table, klo, image, partial, psi, heights);
+            k, pos, table, klo, image, partial, psi, heights, nullptr);
     else if (k.heights_mode)
         bp_kernel<INTERP_HEIGHTS><<<k.ctas, THREADS, HEIGHTS_SMEM, s>>>(k, pos, table, klo, image,
-                                                                       partial, psi, heights);
+                                                                       partial, psi, heights, nullptr);
     else if (k.flags & FLAG_SINC8)
+    {
         bp_kernel<INTERP_SINC8><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi,
-                                                           nullptr);
+                                                           nullptr, sinc_wide);
+        bp_kernel<INTERP_SINC8_WIDE><<<k.ctas, THREADS, SINC_SMEM, s>>>(k, pos, table, klo, image,
+                                                                        partial, psi, nullptr,
+                                                                        sinc_wide);
+    }
     else if (k.flags & FLAG_NEAREST)
         bp_kernel<INTERP_NEAREST><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial,
-                                                             psi, nullptr);
+                                                             psi, nullptr, nullptr);
     else
         bp_kernel<INTERP_LINEAR><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial,
-                                                            psi, nullptr);
+                                                            psi, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -1603,6 +1743,12 @@ cudaError_t backproject_occupancy(int* ctas_per_sm)
                                                                   THREADS, 0);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, bp_kernel<INTERP_SINC8>, THREADS, 0);
+    if (e == cudaSuccess) {
+        int w = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w, bp_kernel<INTERP_SINC8_WIDE>, THREADS,
+                                                          SINC_SMEM);
+        b = std::min(b, w);
+    }
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, bp_kernel<INTERP_NEAREST>, THREADS, 0);
     *ctas_per_sm = std::min(a, std::min(b, c));

@@ -65,6 +65,17 @@ def test_sinc_page_scene_full_size():
     print(_check(sc, sinc_image(sc.params, sc.echoes, sc.antenna_pos)))
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("index", [4, 5])
+def test_sinc_wide_scenes_sampled(index):
+    """The 2048^2 and 4096^2 scenes: a thread's 32 pixels span up to about a
+    range bin per pulse at the image's far x edges, so these run the
+    wide-geometry sinc kernel (two polynomials per thread and pulse, one per
+    16-pixel half, where the halves are narrow enough)."""
+    sc = scenes.make_scene(scenes.CONFIGS[index - 1])
+    print(_check(sc, sinc_image(sc.params, sc.echoes, sc.antenna_pos)))
+
+
 def _small(nx, ny, na=40, nr=512, noise=0.05):
     cfg = scenes.shrink(scenes.CONFIGS[0], nx=nx, ny=ny, na=na, nr=nr, spacing=0.5,
                         pulse_step=0.5, n_targets=0, noise_sigma=noise)
