@@ -304,7 +304,7 @@ constexpr int NP = TILE_X / 2;
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
-                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7 };
+                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7, MODE_POLY4Q = 8 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
@@ -316,16 +316,19 @@ struct PulseState {
     int mode;
 };
 
-// Bounds of u = e0 + e1 i + e2 i^2 over the 16 pixel offsets i in m +- 7.5
-// (m = -8: the left half of a thread's pixels, lanes .x; m = 8: the right half,
-// lanes .y).
-__device__ __forceinline__ void half_bounds(float e0, float e1, float e2, float m, float& lo,
-                                            float& hi)
+// Bounds of u = e0 + e1 i + e2 i^2 over part h of nparts equal runs of a
+// thread's pixels (offsets i from the thread's centre, -15.5 ... 15.5): the
+// run's centre m and half-width r.
+__device__ __forceinline__ void part_bounds(float e0, float e1, float e2, int h, int nparts,
+                                            float& lo, float& hi)
 {
+    const float len = (float)(TILE_X / nparts);
+    const float m = fmaf((float)h + 0.5f, len, -0.5f * TILE_X);
+    const float r = 0.5f * (len - 1.0f);
     const float um = fmaf(m, fmaf(m, e2, e1), e0);
     const float sl = fabsf(fmaf(2.0f * e2, m, e1));
-    lo = um - 7.5f * sl - 56.25f * fmaxf(-e2, 0.0f);
-    hi = um + 7.5f * sl + 56.25f * fmaxf(e2, 0.0f);
+    lo = um - r * sl - r * r * fmaxf(-e2, 0.0f);
+    hi = um + r * sl + r * r * fmaxf(e2, 0.0f);
 }
 
 // The interval of a polynomial: [lo, hi] widened to a half-width of at least
@@ -389,7 +392,7 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         // windowed sinc: when the thread's pixels span at most a quarter bin and
         // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
         // interpolated echo is a degree-4 polynomial in u (SINC_SPAN); when each
-        // half of its pixels does, one polynomial per half (MODE_POLY2H)
+        // half (quarter) of its pixels does, one polynomial per half (quarter)
         float lo_e, hi_e, k0e;
         int kabs0;
         if (poly_interval(k, kb, bin0, lo_u, hi_u, lo_e, hi_e, k0e, kabs0)) {
@@ -398,16 +401,28 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         } else if (INTERP == INTERP_SINC8_WIDE) {
             float lo, hi, lh, hh, kh;
             int ka;
-            half_bounds(e0, e1, e2, -8.0f, lo, hi);
-            bool ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka);
-            half_bounds(e0, e1, e2, 8.0f, lo, hi);
-            ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
-            if (ok)
+            bool ok = true;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                part_bounds(e0, e1, e2, h, 2, lo, hi);
+                ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
+            }
+            if (ok) {
                 st.mode = MODE_POLY2H;
+            } else {
+                ok = true;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    part_bounds(e0, e1, e2, h, 4, lo, hi);
+                    ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
+                }
+                if (ok)
+                    st.mode = MODE_POLY4Q;
+            }
         }
     }
     if (st.mode != MODE_POLY && st.mode != MODE_POLY3)
-        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);   // MODE_POLY2H recomputes its intervals
+        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);   // the part modes recompute their intervals
     st.t1d = make_float2(0.f, 0.f);
     float kn = 0.0f;
     if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
@@ -775,7 +790,7 @@ __device__ __forceinline__ void poly_fold(const float2 (&p)[5], float2 ps, float
 // right 16) the .y coefficients about midR, each with the echo
 // phase psi_k0 exp(j c (u - k0)) of its own k0 (folded into the coefficients
 // and cm = c (mid - k0)).
-template <int ND>
+template <int ND, int Q0 = 0, int NQ = NP>
 __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
                                                 const float2 (&pr)[5], const float2 (&pi)[5],
                                                 float midL, float midR, float cmL, float cmR,
@@ -786,9 +801,9 @@ __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseSta
     const float2 cm2 = make_float2(cmL, cmR);
     const float2 q0s = make_float2(st.q0.x - midL, st.q0.x - midR);
     const float2 one = make_float2(1.0f, 1.0f);
-    float2 id = make_float2(k.i0, k.i0 + NP);
+    float2 id = make_float2(k.i0 + Q0, k.i0 + (NP + Q0));
 #pragma unroll
-    for (int q = 0; q < NP; ++q) {
+    for (int q = Q0; q < Q0 + NQ; ++q) {
         const float2 sv = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), q0s);
         id = __fadd2_rn(id, one);
         float2 gr = pr[ND - 1], gi = pi[ND - 1];
@@ -853,25 +868,52 @@ __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& s
     }
 }
 
-// Spans up to about twice SINC_SPAN (INTERP_SINC8_WIDE): the left and right
-// 16 pixels (lanes .x and .y of every pair) each get their own degree-4
-// interpolant over their own interval (the same error bound), at no extra cost
-// per pixel. The halves' intervals were checked by pulse_setup.
-__device__ __forceinline__ void sinc_poly_halves_pulse(const BpConst& k, const PulseState& st,
-                                                       const float4* row,
-                                                       const float2* __restrict__ psi,
-                                                       float4* stash,
-                                                       float2 (&accre)[NP], float2 (&accim)[NP])
+// Spans up to about twice (four times) SINC_SPAN, INTERP_SINC8_WIDE only: each
+// half (quarter) of the thread's pixels gets its own degree-4 interpolant over
+// its own interval (the same error bound), at no extra cost per pixel. Pixel m
+// sits in lane .x of pair m (m < 16) or lane .y of pair m - 16, so the halves
+// are the two lanes of all 16 pairs, and the quarters are lanes .x / .y of pairs
+// 0-7 (quarters 0 and 2), then of pairs 8-15 (quarters 1 and 3). The parts'
+// intervals were checked by pulse_setup.
+__device__ __forceinline__ void load_part_pair(const float4* stash, int a, int b,
+                                               float2 (&pr)[5], float2 (&pi)[5], float& mid_a,
+                                               float& cm_a, float& mid_b, float& cm_b)
+{
+    const float4* sa = stash + 3 * a * THREADS;
+    const float4* sb = stash + 3 * b * THREADS;
+    const float4 l0 = sa[0], l1 = sa[THREADS], l2 = sa[2 * THREADS];
+    const float4 r0 = sb[0], r1 = sb[THREADS], r2 = sb[2 * THREADS];
+    pr[0] = make_float2(l0.x, r0.x);
+    pi[0] = make_float2(l0.y, r0.y);
+    pr[1] = make_float2(l0.z, r0.z);
+    pi[1] = make_float2(l0.w, r0.w);
+    pr[2] = make_float2(l1.x, r1.x);
+    pi[2] = make_float2(l1.y, r1.y);
+    pr[3] = make_float2(l1.z, r1.z);
+    pi[3] = make_float2(l1.w, r1.w);
+    pr[4] = make_float2(l2.x, r2.x);
+    pi[4] = make_float2(l2.y, r2.y);
+    mid_a = l2.z;
+    cm_a = l2.w;
+    mid_b = r2.z;
+    cm_b = r2.w;
+}
+
+__device__ __forceinline__ void sinc_poly_parts_pulse(const BpConst& k, const PulseState& st,
+                                                      const float4* row,
+                                                      const float2* __restrict__ psi,
+                                                      float4* stash, int nparts,
+                                                      float2 (&accre)[NP], float2 (&accim)[NP])
 {
     const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
-    float midL = 0.0f, cmL = 0.0f, midR = 0.0f, cmR = 0.0f;
-    // one half per pass (one copy of the node code); each half's coefficients
-    // go to this thread's own shared-memory slots (stride THREADS)
+    // one part per pass (one copy of the node code); each part's coefficients,
+    // centre and phase offset go to this thread's own shared-memory slots
+    // (stride THREADS)
 #pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < nparts; ++h) {
         float lo, hi, lo_e, hi_e, k0;
         int ka;
-        half_bounds(e0, e1, e2, h ? 8.0f : -8.0f, lo, hi);
+        part_bounds(e0, e1, e2, h, nparts, lo, hi);
         poly_interval(k, st.kb, st.bin0, lo, hi, lo_e, hi_e, k0, ka);
         const float mid = 0.5f * (lo_e + hi_e), half = 0.5f * (hi_e - lo_e);
         float2 p[5], cr[5], ci[5];
@@ -880,22 +922,19 @@ __device__ __forceinline__ void sinc_poly_halves_pulse(const BpConst& k, const P
         float4* slot = stash + 3 * h * THREADS;
         slot[0] = make_float4(cr[0].x, ci[0].x, cr[1].x, ci[1].x);
         slot[THREADS] = make_float4(cr[2].x, ci[2].x, cr[3].x, ci[3].x);
-        slot[2 * THREADS] = make_float4(cr[4].x, ci[4].x, 0.0f, 0.0f);
-        if (h == 0) {
-            midL = mid;
-            cmL = k.c_phase * (mid - k0);
-        } else {
-            midR = mid;
-            cmR = k.c_phase * (mid - k0);
-        }
+        slot[2 * THREADS] = make_float4(cr[4].x, ci[4].x, mid, k.c_phase * (mid - k0));
     }
-    const float4 l0 = stash[0], l1 = stash[THREADS], l2 = stash[2 * THREADS];
-    const float4 r0 = stash[3 * THREADS], r1 = stash[4 * THREADS], r2 = stash[5 * THREADS];
-    const float2 pr[5] = {make_float2(l0.x, r0.x), make_float2(l0.z, r0.z), make_float2(l1.x, r1.x),
-                          make_float2(l1.z, r1.z), make_float2(l2.x, r2.x)};
-    const float2 pi[5] = {make_float2(l0.y, r0.y), make_float2(l0.w, r0.w), make_float2(l1.y, r1.y),
-                          make_float2(l1.w, r1.w), make_float2(l2.y, r2.y)};
-    sinc_poly_apply<5>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
+    float2 pr[5], pi[5];
+    float midL, cmL, midR, cmR;
+    if (nparts == 2) {
+        load_part_pair(stash, 0, 1, pr, pi, midL, cmL, midR, cmR);
+        sinc_poly_apply<5>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
+    } else {
+        load_part_pair(stash, 0, 2, pr, pi, midL, cmL, midR, cmR);
+        sinc_poly_apply<5, 0, NP / 2>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
+        load_part_pair(stash, 1, 3, pr, pi, midL, cmL, midR, cmR);
+        sinc_poly_apply<5, NP / 2, NP / 2>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
+    }
 }
 
 
@@ -1385,8 +1424,9 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
             sinc_poly_pulse<4>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_POLY)
             sinc_poly_pulse<5>(k, st, row, psi, accre, accim);
-        else if (INTERP == INTERP_SINC8_WIDE && st.mode == MODE_POLY2H)
-            sinc_poly_halves_pulse(k, st, row, psi, stash, accre, accim);
+        else if (INTERP == INTERP_SINC8_WIDE && (st.mode == MODE_POLY2H || st.mode == MODE_POLY4Q))
+            sinc_poly_parts_pulse(k, st, row, psi, stash, st.mode == MODE_POLY4Q ? 4 : 2, accre,
+                                  accim);
         else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
@@ -1681,7 +1721,8 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
 }
 
 constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW4 * sizeof(float4);
-constexpr size_t SINC_SMEM = (size_t)6 * THREADS * sizeof(float4);
+// wide sinc: three float4 per part (at most four parts) per thread
+constexpr size_t SINC_SMEM = (size_t)12 * THREADS * sizeof(float4);
 
 cudaError_t prepare_kernels()
 {
