@@ -30,6 +30,9 @@ struct sarbp_plan_s {
     int heights_mode = 0;            // plan made by sarbp_plan_heights
     double h_min = 0.0, h_max = 0.0; // its height bounds
     float4* table_alloc = nullptr;   // (na * W + 2 * TABLE_PAD) entries
+    float4* sinc_alloc = nullptr;    // (4 na W + 8 TABLE_PAD) entries: windowed-sinc
+                                     // coefficient rows, made by the plan when its flags
+                                     // carry SARBP_SINC8, else by the first sinc call
     int* klo = nullptr;              // na
     float2* psi = nullptr;           // nr + 1: per-bin phasors (windowed-sinc interpolation),
                                      // then one word: the wide-sinc flag of the last call
@@ -146,6 +149,7 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     k.full_window = plan->full_window;
     k.ctas = ctas_for(plan);
     k.flags = p->flags;
+    k.tw = (p->flags & SARBP_SINC8) ? 4 * plan->W : plan->W;
     k.units = (long long)plan->tiles * p->na;
     k.x0 = p->x0;
     k.y0 = p->y0;
@@ -198,6 +202,7 @@ void free_plan(sarbp_plan_s* plan)
     if (!plan)
         return;
     cudaFree(plan->table_alloc);
+    cudaFree(plan->sinc_alloc);
     cudaFree(plan->klo);
     cudaFree(plan->psi);
     cudaFree(plan->partial);
@@ -292,6 +297,26 @@ bool host_band(const sarbp_params* params, const double* antenna_pos, int n0, in
     return band_hi >= band_lo;
 }
 
+// The windowed-sinc coefficient rows: four float4 per table bin, zero pads of
+// 4 TABLE_PAD entries at both ends.
+cudaError_t ensure_sinc_table(sarbp_plan_s* plan)
+{
+    if (plan->sinc_alloc)
+        return cudaSuccess;
+    const size_t bytes = ((size_t)plan->p.na * 4 * plan->W + 8 * TABLE_PAD) * sizeof(float4);
+    cudaError_t e = device_alloc(reinterpret_cast<void**>(&plan->sinc_alloc), bytes);
+    if (e == cudaSuccess) {
+        e = cudaMemset(plan->sinc_alloc, 0, bytes);
+        if (e != cudaSuccess) {
+            cudaFree(plan->sinc_alloc);
+            plan->sinc_alloc = nullptr;
+        }
+    }
+    if (e == cudaSuccess)
+        plan->scratch_bytes += bytes;
+    return e;
+}
+
 // Queue the three kernels of one backprojection. Arguments are already
 // checked; params may describe a band of the plan's range axis (fewer bins,
 // shifted r0), which the plan's table rows always cover.
@@ -320,6 +345,10 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
     float4* table = plan->table_alloc + TABLE_PAD;
     int* sinc_wide = reinterpret_cast<int*>(plan->psi + params->nr + 1);
     if (k.flags & SARBP_SINC8) {
+        e = ensure_sinc_table(plan);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "cudaMalloc (sinc coefficient table)");
+        table = plan->sinc_alloc + 4 * TABLE_PAD;
         e = cudaMemsetAsync(sinc_wide, 0, sizeof(int), s);
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "cudaMemsetAsync");
@@ -519,6 +548,8 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
         }
         // the pads stay zero so that no read near the table's ends sees garbage
         e = cudaMemset(plan->table_alloc, 0, table_entries * sizeof(float4));
+        if (e == cudaSuccess && (p->flags & SARBP_SINC8))
+            e = ensure_sinc_table(plan);
         if (e != cudaSuccess) {
             st = cuda_fail(plan, e, "cudaMemset");
             free_plan(plan);

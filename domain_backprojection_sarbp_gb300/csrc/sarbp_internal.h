@@ -38,7 +38,8 @@ constexpr unsigned FLAG_NEAREST = 4u;
 // Launch constants, computed on the host in float64 for every call.
 struct BpConst {
     int nx, ny, na, nr;
-    int W;                       // table entries per pulse (row pitch, float4 units)
+    int W;                       // table bins per pulse
+    int tw;                      // row pitch in float4: W, or 4 W for the sinc coefficient rows
     int tiles_x, tiles;
     int full_window;             // every row spans bins [-MARGIN-4, nr+...)
     int ctas;                    // persistent CTAs of the main kernel

@@ -75,6 +75,13 @@ __host__ __device__ constexpr bool is_sinc(int interp)
 {
     return interp == INTERP_SINC8 || interp == INTERP_SINC8_WIDE;
 }
+// float4 from one pulse's table row to the next: the sinc kinds read the
+// coefficient rows (four entries per bin)
+template <int INTERP>
+__device__ __forceinline__ int row_pitch(const BpConst& k)
+{
+    return (is_sinc(INTERP) || INTERP == INTERP_HEIGHTS_SINC8) ? k.tw : k.W;
+}
 constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
 constexpr float SINC_SPAN3 = 0.11f;         // widest spread for the cubic on four nodes
@@ -87,20 +94,78 @@ struct __align__(16) Record {
     float4 d;  // c22, row index of bin 0 (int bits), kbase (int bits), kind (int bits)
 };
 
+// Monomial coefficients of the windowed-sinc tap weights on one bin: with
+// u = k + 1/2 + s (s in [-1/2, 1/2]) the tap on sample k + d (d = -3 .. 4) has
+// weight h(1/2 + s - d), h(t) = sinc(t) (1 + cos(pi t / 4)) / 2, and
+// c[d + 3][n] are the coefficients of s^n of its degree-7 interpolant at the
+// eight Chebyshev nodes s_i = cos((2i + 1) pi / 16) / 2. Measured on a fine
+// grid in float64, each interpolant is within 7.7e-7 of its weight and the
+// eight errors sum to 5.2e-6, so |G - sum_n P_n s^n| <= 5.2e-6 max|e_m|.
+struct SincTaps {
+    float c[8][8];
+};
+
+SincTaps fit_sinc_taps()
+{
+    constexpr double pi = 3.14159265358979323846;
+    SincTaps t{};
+    for (int d = -3; d <= 4; ++d) {
+        // Vandermonde system V c = h at the nodes, Gaussian elimination with
+        // partial pivoting in float64
+        double a[8][9];
+        for (int i = 0; i < 8; ++i) {
+            const double sn = 0.5 * std::cos((2 * i + 1) * pi / 16.0);
+            const double x = 0.5 + sn - d;            // never 0: the nodes are inside the bin
+            const double h = std::sin(pi * x) / (pi * x) * 0.5 * (1.0 + std::cos(pi * x / 4.0));
+            double pw = 1.0;
+            for (int n = 0; n < 8; ++n) {
+                a[i][n] = pw;
+                pw *= sn;
+            }
+            a[i][8] = h;
+        }
+        for (int c = 0; c < 8; ++c) {
+            int piv = c;
+            for (int r = c + 1; r < 8; ++r)
+                if (std::fabs(a[r][c]) > std::fabs(a[piv][c]))
+                    piv = r;
+            for (int n = 0; n < 9; ++n)
+                std::swap(a[c][n], a[piv][n]);
+            for (int r = 0; r < 8; ++r) {
+                if (r == c)
+                    continue;
+                const double f = a[r][c] / a[c][c];
+                for (int n = c; n < 9; ++n)
+                    a[r][n] -= f * a[c][n];
+            }
+        }
+        for (int n = 0; n < 8; ++n)
+            t.c[d + 3][n] = (float)(a[n][8] / a[n][n]);
+    }
+    return t;
+}
+
 // ---------------------------------------------------------------------------
 // Echo table: one block per pulse.
 // ---------------------------------------------------------------------------
-// Linear interpolation: entries (A_k, D_k / c) as above. Windowed-sinc and
-// nearest-neighbour interpolation: entries are plain sample pairs
-// (e_k, e_{k+1}), zero where a sample lies outside 0 .. nr - 1, and the phase
-// comes from psi_k (psi_kernel).
-template <bool SINC>
+// Linear interpolation (TABLE_LINEAR): entries (A_k, D_k / c) as above.
+// Nearest neighbour (TABLE_PAIRS): plain sample pairs (e_k, e_{k+1}), zero
+// where a sample lies outside 0 .. nr - 1. Windowed sinc (TABLE_SINC): four
+// entries per bin k, the complex coefficients P_0 .. P_7 of the interpolant on
+// that bin, G(k + 1/2 + s) = sum_n P_n s^n for s in [-1/2, 1/2], with
+// P_n = sum_d taps.c[d + 3][n] e_{k+d}; zero unless the whole stencil
+// k - 3 .. k + 4 lies in 0 .. nr - 1. The phase of the last two kinds comes
+// from psi_k (psi_kernel). Rows are k.tw float4 apart.
+enum TableKind : int { TABLE_LINEAR = 0, TABLE_PAIRS = 1, TABLE_SINC = 2 };
+
+template <int KIND>
 __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __restrict__ echo,
                                                     const double* __restrict__ pos,
                                                     float4* __restrict__ table,
                                                     int* __restrict__ klo,
-                                                    int* __restrict__ sinc_wide)
+                                                    int* __restrict__ sinc_wide, SincTaps taps)
 {
+    constexpr bool SINC = KIND == TABLE_SINC;
     const int n = blockIdx.x;
     __shared__ int s_lo;
     if (threadIdx.x == 0) {
@@ -137,12 +202,34 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
     }
     __syncthreads();
     const int lo = s_lo;
-    float4* row = table + (size_t)n * k.W;
+    float4* row = table + (size_t)n * k.tw;
     const float2* erow = echo + (size_t)n * (size_t)k.echo_stride;
     for (int w = threadIdx.x; w < k.W; w += blockDim.x) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         const long long kk = (long long)lo + w;
         if (SINC) {
+            float2 pc[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                pc[m] = make_float2(0.f, 0.f);
+            if (lo != KLO_INVALID && kk >= 3 && kk <= (long long)k.nr - 5) {
+#pragma unroll
+                for (int d = 0; d < 8; ++d) {
+                    const float2 e = erow[kk - 3 + d];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        pc[m].x = fmaf(taps.c[d][m], e.x, pc[m].x);
+                        pc[m].y = fmaf(taps.c[d][m], e.y, pc[m].y);
+                    }
+                }
+            }
+            float4* out = row + 4 * (size_t)w;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                out[m] = make_float4(pc[2 * m].x, pc[2 * m].y, pc[2 * m + 1].x, pc[2 * m + 1].y);
+            continue;
+        }
+        if (KIND == TABLE_PAIRS) {
             if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 1) {
                 const float2 e0 = erow[kk];
                 v.x = e0.x;
@@ -592,15 +679,13 @@ __device__ __forceinline__ void exact_pulse(const BpConst& k, const Record& rec,
 // ---------------------------------------------------------------------------
 // Windowed-sinc interpolation (8 taps, k-3 .. k+4).
 //
-// The echo at range u = k + f is psi(u) sum_m e_m h(u - m) with
-// psi(u) = psi_k exp(j c f). For tap m = k - 3 + t the argument is
-// f + d, d = 3 - t, and
-//   h(f + d) = (-1)^d sin(pi f) / (pi (f + d)) * (1 + cos(pi (f + d) / 4)) / 2,
-// so one sine, one sine/cosine pair (angle addition for the window) and one
-// reciprocal (batch inversion of the eight f + d) serve all eight weights.
+// The echo at range u = k + f is psi(u) G(u), G(u) = sum_m e_m h(u - m),
+// psi(u) = psi_k exp(j c f). On each bin G is a fixed combination of the
+// bin's eight samples with weights h(f - d), d = -3 .. 4; the table kernel
+// stores it as a degree-7 polynomial in s = f - 1/2 (each weight interpolated
+// at eight Chebyshev nodes of the bin, fit_sinc_taps), so a value of G costs
+// four loads and seven packed FMAs.
 // ---------------------------------------------------------------------------
-// One pixel at row position ub (relative to row index kb). CHECK_ROW adds
-// bounds on the table row for the exact path.
 __device__ __forceinline__ float rcp_approx(float x)
 {
     float r;
@@ -608,77 +693,22 @@ __device__ __forceinline__ float rcp_approx(float x)
     return r;
 }
 
-// sin(pi y) / pi for y in [0, 1], accurate relative to its value near both
-// ends: y folds to z = min(y, 1 - y) (1 - y is exact for y >= 1/2) and
-// sin(pi z) / pi = z sum_n (-1)^n (pi z)^(2n) / (2n + 1)! is summed to n = 5;
-// the first dropped term is 6e-8 of the value at z = 1/2.
-__device__ __forceinline__ float sinpi_over_pi(float y)
+// G at s = f - 1/2 from the four coefficient entries of its bin.
+__device__ __forceinline__ float2 bin_poly(const float4* c, float s)
 {
-    const float z = fminf(y, 1.0f - y);
-    const float s = z * z;
-    float t = fmaf(s, -2.34608104e-3f, 2.61478478e-2f);   // -pi^10 / 11!, pi^8 / 9!
-    t = fmaf(s, t, -0.190751824f);                          // -pi^6 / 7!
-    t = fmaf(s, t, 0.811742425f);                           // pi^4 / 5!
-    t = fmaf(s, t, -1.64493407f);                           // -pi^2 / 3!
-    t = fmaf(s, t, 1.0f);
-    return z * t;
+    const float4 c0 = __ldg(c), c1 = __ldg(c + 1), c2 = __ldg(c + 2), c3 = __ldg(c + 3);
+    const float2 sv = make_float2(s, s);
+    float2 g = __ffma2_rn(make_float2(c3.z, c3.w), sv, make_float2(c3.x, c3.y));
+    g = __ffma2_rn(g, sv, make_float2(c2.z, c2.w));
+    g = __ffma2_rn(g, sv, make_float2(c2.x, c2.y));
+    g = __ffma2_rn(g, sv, make_float2(c1.z, c1.w));
+    g = __ffma2_rn(g, sv, make_float2(c1.x, c1.y));
+    g = __ffma2_rn(g, sv, make_float2(c0.z, c0.w));
+    return __ffma2_rn(g, sv, make_float2(c0.x, c0.y));
 }
 
-// 8-tap windowed sinc at u = k + f (f in [0, 1)):
-//   G = sum_{d=-3..4} e_{k+d} h(f - d),  h(t) = sin(pi t) / (pi t) (1 + cos(pi t / 4)) / 2,
-// with p at entry k - 3 of a row of sample pairs (e_m, e_{m+1}); no phase.
-// Since sin(pi (f - d)) = (-1)^d sin(pi f), G = sin(pi f) / pi times
-// sum_d (-1)^d w_d e_{k+d} / (f - d). The reciprocals pair up:
-// (f - d)(f - 1 + d) = g - d (d - 1) with g = f (f - 1), so
-// 1 / (f - d) = (f - 1 + d) / (g - d (d - 1)) and four reciprocals serve the
-// eight taps. f is held in [1e-7, 1 - 1e-7] so that no f - d is 0 (the
-// fraction can round to exactly 1 for tiny negative u); the weights are
-// continuous in f, so the clamp changes them by less than 1e-6.
-__device__ __forceinline__ float2 sinc_sum(float f, const float4* p)
-{
-    const float4 s0 = __ldg(p), s1 = __ldg(p + 2), s2 = __ldg(p + 4), s3 = __ldg(p + 6);
-    const float fc = fminf(fmaxf(f, 1.0e-7f), 0.99999988f);
-    const float fm1 = fc - 1.0f;
-    const float g = fc * fm1;
-    const float r0 = rcp_approx(g);              // 1 / (f (f - 1))
-    const float r1 = rcp_approx(g - 2.0f);       // 1 / ((f + 1)(f - 2))
-    const float r2 = rcp_approx(g - 6.0f);       // 1 / ((f + 2)(f - 3))
-    const float r3 = rcp_approx(g - 12.0f);      // 1 / ((f + 3)(f - 4))
-    // (-1)^d / (f - d), taps d = -3 .. 4
-    const float a0 = (4.0f - fc) * r3;
-    const float a1 = (fc - 3.0f) * r2;
-    const float a2 = (2.0f - fc) * r1;
-    const float a3 = fm1 * r0;
-    const float a4 = -fc * r0;
-    const float a5 = (fc + 1.0f) * r1;
-    const float a6 = -(fc + 2.0f) * r2;
-    const float a7 = (fc + 3.0f) * r3;
-    // (1 + cos(pi (f - d) / 4)) / 2 from cos and sin of pi f / 4 and of pi d / 4
-    float s4, c4;
-    __sincosf(0.785398163f * fc, &s4, &c4);
-    constexpr float H = 0.353553391f;                            // sqrt(2) / 4
-    const float w0 = fmaf(c4, -H, fmaf(-s4, H, 0.5f));           // d = -3
-    const float w1 = fmaf(-s4, 0.5f, 0.5f);                      // d = -2
-    const float w2 = fmaf(c4, H, fmaf(-s4, H, 0.5f));            // d = -1
-    const float w3 = fmaf(c4, 0.5f, 0.5f);                       // d = 0
-    const float w4 = fmaf(c4, H, fmaf(s4, H, 0.5f));             // d = 1
-    const float w5 = fmaf(s4, 0.5f, 0.5f);                       // d = 2
-    const float w6 = fmaf(c4, -H, fmaf(s4, H, 0.5f));            // d = 3
-    const float w7 = fmaf(c4, -0.5f, 0.5f);                      // d = 4
-    const float h0 = a0 * w0, h1 = a1 * w1, h2 = a2 * w2, h3 = a3 * w3;
-    const float h4 = a4 * w4, h5 = a5 * w5, h6 = a6 * w6, h7 = a7 * w7;
-    float sre = h0 * s0.x, sim = h0 * s0.y;
-    sre = fmaf(h1, s0.z, sre); sim = fmaf(h1, s0.w, sim);
-    sre = fmaf(h2, s1.x, sre); sim = fmaf(h2, s1.y, sim);
-    sre = fmaf(h3, s1.z, sre); sim = fmaf(h3, s1.w, sim);
-    sre = fmaf(h4, s2.x, sre); sim = fmaf(h4, s2.y, sim);
-    sre = fmaf(h5, s2.z, sre); sim = fmaf(h5, s2.w, sim);
-    sre = fmaf(h6, s3.x, sre); sim = fmaf(h6, s3.y, sim);
-    sre = fmaf(h7, s3.z, sre); sim = fmaf(h7, s3.w, sim);
-    const float sf = sinpi_over_pi(fc);
-    return make_float2(sre * sf, sim * sf);
-}
-
+// One pixel at row position ub (relative to row index kb). CHECK_ROW adds
+// bounds on the table row for the exact path.
 template <bool CHECK_ROW>
 __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, int bin0,
                                            const float4* row, const float2* __restrict__ psi,
@@ -692,10 +722,10 @@ __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, i
     const int kabs = kr - bin0;
     if (kabs < 3 || kabs > k.nr - 5)
         return;                                 // stencil reaches outside the recorded range
-    if (CHECK_ROW && (kr < 3 || kr + 3 > k.W - 1))
+    if (CHECK_ROW && (kr < 0 || kr > k.W - 1))
         return;
     const float2 ps = __ldg(psi + kabs);
-    const float2 gsum = sinc_sum(f, row + (kr - 3));
+    const float2 gsum = bin_poly(row + 4 * kr, f - 0.5f);
     float sn, cs;
     __sincosf(f * k.c_phase, &sn, &cs);
     const float zr = ps.x * cs - ps.y * sn;
@@ -705,14 +735,13 @@ __device__ __forceinline__ void sinc_pixel(const BpConst& k, float ub, int kb, i
 }
 
 // Windowed-sinc interpolant G(u) = sum_m e_m h(u - m) at one position ub
-// (row units, relative to kb), no phase. The whole stencil must lie inside
-// the row and the recorded range.
+// (row units, relative to kb), no phase. Its bin must lie inside the row.
 __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row)
 {
     const float tt = __fadd_rd(ub, MAGIC);
-    const float f = ub - (tt - MAGIC);
+    const float s = (ub - (tt - MAGIC)) - 0.5f;
     const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
-    return sinc_sum(f, row + (kr - 3));
+    return bin_poly(row + 4 * kr, s);
 }
 
 // Monomial coefficients p[n] (complex, in t = (u - mid) / half) of the
@@ -1538,7 +1567,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             if (tid < cnt)
                 make_record(k, pos, klo, c0 + tid, xc, yc, s_rec[tid]);
             __syncthreads();
-            const float4* rows = table + (size_t)c0 * k.W;
+            const int tw = row_pitch<INTERP>(k);
+            const float4* rows = table + (size_t)c0 * tw;
             // Two pulse states in ping-pong: the state of pulse p + 1 is built
             // while pulse p is applied, with no copy between them.
             PulseState sa = pulse_setup<INTERP>(k, s_rec[0], rows, jf);
@@ -1546,15 +1576,15 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             for (int p = 0; p < cnt; p += 2) {
                 const int p1 = min(p + 1, cnt - 1);
                 const PulseState sb =
-                    pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * k.W, jf);
-                apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * k.W,
+                    pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * tw, jf);
+                apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * tw,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
                                   s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
-                sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * k.W, jf);
-                apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * k.W,
+                sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * tw, jf);
+                apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * tw,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
                                   s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
             }
@@ -1706,11 +1736,13 @@ cudaError_t noalloc_scratch(void** ptr)
 cudaError_t launch_table(const BpConst& k, const float2* echo, const double* pos, float4* table,
                          int* klo, int* sinc_wide, cudaStream_t s)
 {
-    if (k.flags & (FLAG_SINC8 | FLAG_NEAREST))
-        table_kernel<true><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo,
-                                                (k.flags & FLAG_SINC8) ? sinc_wide : nullptr);
+    static const SincTaps taps = fit_sinc_taps();
+    if (k.flags & FLAG_SINC8)
+        table_kernel<TABLE_SINC><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo, sinc_wide, taps);
+    else if (k.flags & FLAG_NEAREST)
+        table_kernel<TABLE_PAIRS><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo, nullptr, taps);
     else
-        table_kernel<false><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo, nullptr);
+        table_kernel<TABLE_LINEAR><<<k.na, 256, 0, s>>>(k, echo, pos, table, klo, nullptr, taps);
     return cudaGetLastError();
 }
 

@@ -87,18 +87,21 @@ def _host_args(p, image, echoes, antenna_pos):
 class Plan:
     """A libsarbp plan: fixed sizes, device scratch, repeated backprojections."""
 
-    def __init__(self, params, height_range=None):
+    def __init__(self, params, height_range=None, interp="linear"):
         """``height_range`` = (h_min, h_max) makes a height-map plan (sarbp_plan_heights),
-        used with :meth:`backproject_heights` only."""
+        used with :meth:`backproject_heights` only. ``interp="sinc8"`` allocates the
+        windowed-sinc coefficient rows with the plan (otherwise the first sinc call
+        does); each call still chooses its own interpolation."""
         self._lib = _native.lib()
         self.params = _params(params)
+        made = _params(params, interp=interp)
         self.height_range = None if height_range is None else tuple(map(float, height_range))
         handle = ctypes.c_void_p()
         if self.height_range is None:
-            st = self._lib.sarbp_plan(ctypes.byref(handle), ctypes.byref(self.params))
+            st = self._lib.sarbp_plan(ctypes.byref(handle), ctypes.byref(made))
             where = "sarbp_plan"
         else:
-            st = self._lib.sarbp_plan_heights(ctypes.byref(handle), ctypes.byref(self.params),
+            st = self._lib.sarbp_plan_heights(ctypes.byref(handle), ctypes.byref(made),
                                               *self.height_range)
             where = "sarbp_plan_heights"
         if st != _native.SARBP_OK:

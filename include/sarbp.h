@@ -38,6 +38,9 @@
  * only enqueue kernels and memsets on `stream`: they allocate nothing and do
  * not synchronise, so they may be captured into a CUDA graph once the plan
  * exists; each replay does the same work on the buffers given at capture.
+ * One exception: on a plan made without SARBP_SINC8 in its flags, the first
+ * SARBP_SINC8 call allocates the plan's windowed-sinc coefficient rows (see
+ * sarbp_plan), so that call must not be the first one captured.
  * The host-buffer calls synchronise and cannot be captured.
  *
  * Errors. No call throws or aborts. Every call returns a status; argument
@@ -110,7 +113,11 @@ typedef struct sarbp_plan_s* sarbp_plan_t;
  * with that device current. Scratch owned by the plan: the pre-multiplied
  * echo table (na x W x 16 bytes, W <= nr + 24, where W covers the image's
  * range extent), one int per pulse, one complex64 per range bin, and the
- * partial-sum buffers of the work split (about 40 MB). Returns SARBP_ERR_INVALID_ARG for negative sizes,
+ * partial-sum buffers of the work split (about 40 MB). With SARBP_SINC8 in
+ * p->flags also the windowed-sinc coefficient rows (na x W x 64 bytes: the
+ * degree-7 polynomial of the interpolant on each bin); without it the first
+ * SARBP_SINC8 call allocates them. Each call passes its own flags; p->flags
+ * only decides this allocation and what sarbp_plan_describe counts. Returns SARBP_ERR_INVALID_ARG for negative sizes,
  * non-finite or non-positive dx, dy, dr, wavelength, unknown flags, or image
  * sizes above 2^30 pixels; SARBP_ERR_UNSUPPORTED_DEVICE off compute
  * capability 10.3; SARBP_ERR_OOM if an allocation fails.

@@ -155,3 +155,24 @@ def test_two_plans_on_two_streams_at_once(scene):
             pb.backproject(both[1], echoes, pos, interp="sinc8", stream=sb)
         torch.cuda.synchronize()
         assert torch.equal(both[0], solo[0]) and torch.equal(both[1], solo[1])
+
+
+def test_sinc_plan_captures_its_first_call(scene):
+    """A plan made for sinc holds its coefficient rows from the start, so its
+    very first sinc call can be captured; the replay equals an eager call on a
+    plan that allocated them on first use."""
+    p = scene.params
+    echoes, pos = _dev(scene.echoes), _dev(scene.antenna_pos)
+    with Plan(p) as lazy:
+        eager = torch.zeros((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+        lazy.backproject(eager, echoes, pos, interp="sinc8")
+        torch.cuda.synchronize()
+    with Plan(p, interp="sinc8") as plan:
+        img = torch.zeros_like(eager)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.backproject(img, echoes, pos, interp="sinc8",
+                             stream=torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(img, eager)
