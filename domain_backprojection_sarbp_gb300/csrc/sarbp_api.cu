@@ -548,12 +548,18 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
         }
         // the pads stay zero so that no read near the table's ends sees garbage
         e = cudaMemset(plan->table_alloc, 0, table_entries * sizeof(float4));
-        if (e == cudaSuccess && (p->flags & SARBP_SINC8))
-            e = ensure_sinc_table(plan);
         if (e != cudaSuccess) {
             st = cuda_fail(plan, e, "cudaMemset");
             free_plan(plan);
             return st;
+        }
+        if (p->flags & SARBP_SINC8) {
+            e = ensure_sinc_table(plan);
+            if (e != cudaSuccess) {
+                st = cuda_fail(plan, e, "cudaMalloc (sinc coefficient table)");
+                free_plan(plan);
+                return st;
+            }
         }
     }
     *out = plan;

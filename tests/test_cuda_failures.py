@@ -126,3 +126,42 @@ def test_range_compression_plan_fails_cleanly(which):
     from oracle import range_compression as rco
     want = rco.range_compress(raw.cpu().numpy(), ref.cpu().numpy())
     assert parity.compare(out.cpu().numpy(), want)["rel_l2"] < 1e-5
+
+
+def test_sinc_plan_creation_fails_cleanly(scene):
+    """A plan made for sinc allocates its coefficient rows fifth; when that
+    fails the plan is not made and its other scratch is freed."""
+    lib = _native.lib()
+    prm = _native.Params.from_dict(scene.params)
+    prm.flags |= _native.SARBP_SINC8
+    h = ctypes.c_void_p()
+    Plan(scene.params).close()
+    before = _free_bytes()
+    lib.sarbp_debug_fail_alloc(5)
+    assert lib.sarbp_plan(ctypes.byref(h), ctypes.byref(prm)) == _native.SARBP_ERR_OOM
+    assert not h.value
+    assert abs(_free_bytes() - before) <= 8 << 20
+
+
+def test_first_sinc_call_allocation_fails_then_recovers(scene):
+    """On a plan made without sinc, the first sinc call allocates the
+    coefficient rows; when that fails the call returns SARBP_ERR_OOM having
+    queued nothing (the image is untouched), and the next call works."""
+    lib = _native.lib()
+    p = scene.params
+    e = torch.from_numpy(scene.echoes).to(DEV)
+    a = torch.from_numpy(scene.antenna_pos).to(DEV)
+    with Plan(p) as plan:
+        img = torch.full((p["ny"], p["nx"]), complex(3.0, 4.0), dtype=torch.complex64, device=DEV)
+        lib.sarbp_debug_fail_alloc(1)
+        with pytest.raises(SarbpError) as ex:
+            plan.backproject(img, e, a, interp="sinc8")
+        assert ex.value.status == _native.SARBP_ERR_OOM
+        assert "sinc" in lib.sarbp_last_error(plan.handle).decode()
+        torch.cuda.synchronize()
+        assert bool(torch.all(img == complex(3.0, 4.0)))
+        lib.sarbp_debug_fail_alloc(0)
+        plan.backproject(img, e, a, interp="sinc8")
+        torch.cuda.synchronize()
+    ref = oracle.backproject(p, scene.echoes, scene.antenna_pos, interp="sinc8")
+    parity.assert_parity(img.cpu().numpy(), ref, "sinc call after a failed coefficient-row allocation")
