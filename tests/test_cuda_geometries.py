@@ -149,3 +149,31 @@ def test_nearest(name):
     m = parity.compare(got, ref)
     print(name, m)
     assert m["rel_l2"] <= parity.REL_L2 and m["max_err"] <= parity.MAX_ERR, m
+
+
+@pytest.mark.parametrize("name", ["squint_25deg", "low_pass"])
+def test_sinc8_wide_geometry_at_range_axis_edges(name):
+    """A geometry where a thread's 32 pixels span more than a quarter bin (the
+    sinc kernel with half and quarter polynomials), with the recorded range
+    axis cut so that it starts and ends inside the image: stencils that reach
+    past either end contribute nothing, per pixel and per part."""
+    pos, fc, dr, spacing, centre = CASES[name]
+    params, echo, pos = _scene(pos, fc, dr, spacing, centre=centre, seed=4)
+    xs = params["x0"] + np.array([0.0, params["nx"] - 1]) * params["dx"]
+    rmin = np.min(np.linalg.norm(pos, axis=1)) - np.hypot(params["nx"] * spacing, params["ny"] * spacing)
+    spread = 31 * params["dx"] * np.max(np.abs(xs[None, :] - pos[:, :1])) / (rmin * dr)
+    assert spread > 0.25, spread
+    # keep the middle half of the bins the middle pulse sees the image in: its
+    # ranges then run past both ends of the cut axis
+    gx, gy = np.meshgrid(params["x0"] + np.arange(params["nx"]) * params["dx"],
+                         params["y0"] + np.arange(params["ny"]) * params["dy"])
+    a = pos[len(pos) // 2]
+    u = (np.sqrt((gx - a[0]) ** 2 + (gy - a[1]) ** 2 + a[2] ** 2) - params["r0"]) / dr
+    off = int(u.min() + 0.25 * (u.max() - u.min()))
+    keep = int(0.5 * (u.max() - u.min()))
+    assert u.min() - off < 0 and u.max() - off > keep
+    cut = dict(params, nr=keep, r0=params["r0"] + off * dr)
+    e = np.ascontiguousarray(echo[:, off:off + keep])
+    got = _gpu(cut, e, pos, "sinc8")
+    ref = oracle.backproject(cut, e, pos, interp="sinc8")
+    print(name, parity.assert_parity(got, ref, name + " cut range axis"))
