@@ -1050,15 +1050,20 @@ __device__ __forceinline__ void nearest_pair_pulse(const BpConst& k, const Pulse
     const float4 e = st.t0;
     const float w0r = e.x * ps.x - e.y * ps.y, w0i = e.x * ps.y + e.y * ps.x;
     const float w1r = e.z * ps.x - e.w * ps.y, w1i = e.z * ps.y + e.w * ps.x;
+    // the sample as w0 + h (w1 - w0) with h = 1 or 0: one set and one packed
+    // FMA per lane pair instead of compares and selects (w0 + (w1 - w0) is w1
+    // to one rounding)
+    const float2 w0r2 = make_float2(w0r, w0r), w0i2 = make_float2(w0i, w0i);
+    const float2 dwr2 = make_float2(w1r - w0r, w1r - w0r), dwi2 = make_float2(w1i - w0i, w1i - w0i);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
         const float2 x = __ffma2_rn(id, __ffma2_rn(id, st.q2, st.q1), st.q0);
         id = __fadd2_rn(id, one);
-        const bool ba = x.x >= 0.0f, bb = x.y >= 0.0f;
-        const float2 wr = make_float2(ba ? w1r : w0r, bb ? w1r : w0r);
-        const float2 wi = make_float2(ba ? w1i : w0i, bb ? w1i : w0i);
+        const float2 h = make_float2(x.x >= 0.0f ? 1.0f : 0.0f, x.y >= 0.0f ? 1.0f : 0.0f);
+        const float2 wr = __ffma2_rn(h, dwr2, w0r2);
+        const float2 wi = __ffma2_rn(h, dwi2, w0i2);
         float sa, ca, sb, cb;
         __sincosf(x.x, &sa, &ca);
         __sincosf(x.y, &sb, &cb);
