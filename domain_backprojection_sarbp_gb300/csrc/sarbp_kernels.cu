@@ -1695,6 +1695,28 @@ __global__ void __launch_bounds__(REDUCE_THREADS) reduce_kernel(BpConst k, const
         const int f = f0 + r * REDUCE_THREADS;
         if (f >= TILE_PIX / 2)
             continue;
+        {
+            // both pixels of the float4 (adjacent in one image row) in one 16-byte
+            // store where the row allows it: whole sectors, which matters when the
+            // image is mapped host memory
+            const int rowi = row0 + (2 * f) / TILE_X;
+            const int col = col0 + (2 * f) % TILE_X;
+            float4* dst4 = (rowi < k.ny && col + 1 < k.nx)
+                               ? reinterpret_cast<float4*>(image + (size_t)rowi * k.nx + col)
+                               : nullptr;
+            if (dst4 && (reinterpret_cast<uintptr_t>(dst4) & 15) == 0) {
+                float4 v = sum[r];
+                if (acc) {
+                    const float4 o = *dst4;
+                    v.x += o.x;
+                    v.y += o.y;
+                    v.z += o.z;
+                    v.w += o.w;
+                }
+                *dst4 = v;
+                continue;
+            }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int p = 2 * f + h;
