@@ -634,7 +634,7 @@ __device__ __forceinline__ void gather_pulse(const BpConst& k, const PulseState&
         const float2 s = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, c, accre[q]);
         accim[q] = __ffma2_rn(wr, s, __ffma2_rn(wi, c, accim[q]));
-        accre[q] = __ffma2_rn(__fmul2_rn(wi, s), neg1, accre[q]);
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), s, accre[q]);
     }
 }
 
@@ -1252,7 +1252,7 @@ __device__ __forceinline__ void heights_series_loop(const BpConst& k, const floa
         const float2 sn = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, c, accre[q]);
         accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, c, accim[q]));
-        accre[q] = __ffma2_rn(__fmul2_rn(wi, sn), neg1, accre[q]);
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), sn, accre[q]);
     }
 }
 
