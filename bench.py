@@ -63,7 +63,7 @@ HBM_GBS, HBM_BASIS = measured_hbm_gbs()
 L2_FLUSH_BYTES = 256 << 20
 # dram read+write bytes of one bp_kernel launch, from ncu (None until captured
 # for the current kernel)
-MAIN_KERNEL_TRAFFIC = 10_711_296   # ncu dram read + write, one bp_kernel<0> launch, page-sized scene
+MAIN_KERNEL_TRAFFIC = 14_007_552   # ncu dram read + write, one bp_kernel<0> launch, page-sized scene
 
 
 # ------------------------------------------------------------------ ranks
