@@ -35,7 +35,9 @@ struct sarbp_plan_s {
                                      // carry SARBP_SINC8, else by the first sinc call
     int* klo = nullptr;              // na
     float2* psi = nullptr;           // nr + 1: per-bin phasors (windowed-sinc interpolation),
-                                     // then one word: the wide-sinc flag of the last call
+                                     // then one word: the wide-sinc flag of the last call,
+                                     // then the sinc work split: SPLIT_CELLS + 1 words of
+                                     // cost scratch and max_ctas + 1 CTA start units
     float4* partial = nullptr;       // 2 * max_ctas * TILE_PIX / 2
     int max_ctas = 0;
     size_t scratch_bytes = 0;
@@ -380,13 +382,22 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         ev = &plan->events[plan->events_used++];
         cudaEventRecord(ev->first, s);
     }
+    if ((k.flags & SARBP_SINC8) && !plan->heights_mode) {
+        // the sinc kernels' cost varies across tiles: split the work by estimated cost
+        auto* cum = reinterpret_cast<unsigned long long*>(plan->psi + plan->p.nr + 2);
+        auto* starts = reinterpret_cast<long long*>(cum + SPLIT_CELLS + 1);
+        e = launch_split(k, antenna_pos, sinc_wide, cum, starts, s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "work-split kernel launch");
+        k.starts = starts;
+    }
     e = launch_backproject(k, antenna_pos, table, plan->klo, static_cast<float2*>(image),
                            plan->partial, plan->psi, heights, sinc_wide, s);
     if (ev)
         cudaEventRecord(ev->second, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "backprojection kernel launch");
-    if (any_split_tile(k)) {
+    if (k.starts || any_split_tile(k)) {
         e = launch_reduce(k, plan->partial, static_cast<float2*>(image), s);
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "reduce kernel launch");
@@ -532,7 +543,8 @@ sarbp_status plan_create(sarbp_plan_t* out, const sarbp_params* p, int heights_m
         const size_t table_entries = (size_t)p->na * plan->W + 2 * TABLE_PAD;
         const size_t sizes[4] = {table_entries * sizeof(float4), (size_t)p->na * sizeof(int),
                                  (size_t)plan->max_ctas * TILE_PIX * sizeof(float4),
-                                 ((size_t)p->nr + 2) * sizeof(float2)};
+                                 ((size_t)p->nr + 2 + (size_t)SPLIT_CELLS + 1 +
+                                  (size_t)plan->max_ctas + 1) * sizeof(float2)};
         void** ptrs[4] = {reinterpret_cast<void**>(&plan->table_alloc),
                           reinterpret_cast<void**>(&plan->klo),
                           reinterpret_cast<void**>(&plan->partial),
@@ -609,10 +621,13 @@ sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out)
     out->kernels_per_call = 0;
     if (plan->tiles > 0 && plan->p.na > 0 && plan->p.nr >= 2)
         // table + main (+ reduce); the phasor kernel for sinc and nearest; sinc on a
-        // plane also enqueues its wide-geometry kernel (one of the two exits at once)
-        out->kernels_per_call = (any_split_tile(make_const(plan, &plan->p)) ? 3 : 2) +
-                                ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0) +
-                                ((plan->p.flags & SARBP_SINC8) && !plan->heights_mode ? 1 : 0);
+        // plane also enqueues the work split, its wide-geometry kernel (one of the two
+        // exits at once) and always the reduce
+        out->kernels_per_call =
+            ((plan->p.flags & SARBP_SINC8) && !plan->heights_mode)
+                ? 6
+                : (any_split_tile(make_const(plan, &plan->p)) ? 3 : 2) +
+                      ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0);
     else if (plan->tiles > 0)
         out->kernels_per_call = 0;   // a memset at most
     out->scratch_bytes = plan->scratch_bytes;

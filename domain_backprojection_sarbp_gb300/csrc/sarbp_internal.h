@@ -46,6 +46,8 @@ struct BpConst {
     unsigned flags;
     long long units;             // tiles * na (tile-pulse work units)
     long long echo_stride;       // complex samples from one pulse's echo row to the next
+    const long long* starts;     // first unit of each CTA (ctas + 1 entries, device), or
+                                 // null: CTA b starts at b * units / ctas
 
     double x0, y0, z0, dx, dy, r0, dr, inv_dr;
     double rect_x0, rect_x1, rect_y0, rect_y1;  // tile-padded image rectangle
@@ -81,6 +83,12 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
                                cudaStream_t s);
 // Dynamic shared-memory limits of the kernels that use more than the default.
 cudaError_t prepare_kernels();
+// Cost-weighted CTA boundaries for the windowed-sinc kernels on a plane (after
+// the table kernel on the same stream, which sets sinc_wide): cum holds
+// SPLIT_CELLS + 1 words of scratch, starts receives ctas + 1 unit offsets.
+constexpr int SPLIT_CELLS = 65536;         // (tile, pulse segment) cells of the cost estimate
+cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
+                         unsigned long long* cum, long long* starts, cudaStream_t s);
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);

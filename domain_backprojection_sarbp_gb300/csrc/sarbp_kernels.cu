@@ -1485,7 +1485,7 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
 
 __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
 {
-    return b * k.units / k.ctas;
+    return k.starts ? k.starts[b] : b * k.units / k.ctas;
 }
 
 // ---------------------------------------------------------------------------
@@ -1645,7 +1645,18 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ long long cta_of_unit(const BpConst& k, long long u)
 {
-    return ((u + 1) * k.ctas - 1) / k.units;   // largest b with cta_start(b) <= u
+    // largest b < ctas with cta_start(b) <= u
+    if (!k.starts)
+        return ((u + 1) * k.ctas - 1) / k.units;
+    long long lo = 0, hi = k.ctas - 1;
+    while (lo < hi) {
+        const long long mid = (lo + hi + 1) / 2;
+        if (k.starts[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
 }
 
 constexpr int REDUCE_THREADS = 256;
@@ -1835,6 +1846,130 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
     else
         bp_kernel<INTERP_LINEAR><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial,
                                                             psi, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Cost-weighted work split for the windowed-sinc kernels on a plane. What a
+// (tile, pulse) unit costs depends on how far a thread's 32 pixels spread in
+// range (cubic or quartic polynomial, halves, quarters or per-pixel taps), and
+// that spread grows with the tile's x distance from the antenna, so equal unit
+// counts leave the CTAs holding the image's far edges working after the others
+// have finished. split_kernel estimates each tile's cost from SPLIT_SAMPLES
+// evenly spaced pulses, in integer units (the sums are exact and the split is
+// the same on every run), and places the CTA boundaries at equal shares of the
+// total; within a tile the pulses count as equally costly.
+// ---------------------------------------------------------------------------
+constexpr int SPLIT_THREADS = 1024;
+constexpr int SPLIT_SAMPLES = 64;
+
+// Relative cost of one (thread, pulse) by the spread of its pixels' range, in
+// bins, from the modes' instruction counts per thread and pulse.
+__device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
+{
+    if (span <= SINC_SPAN3)
+        return 100;
+    if (span <= SINC_SPAN)
+        return 113;
+    if (wide && span <= 2.0f * SINC_SPAN)
+        return 160;
+    if (wide && span <= 4.0f * SINC_SPAN)
+        return 220;
+    return 330;
+}
+
+// One block. The units are cut into cells: tile t, pulse segment i of NS
+// (NS = min(SPLIT_SAMPLES, SPLIT_CELLS / tiles), at least 1), so that the cost
+// can follow the antenna along the track; a cell's cost is the unit cost at
+// its middle pulse times its pulse count. cum: SPLIT_CELLS + 1 words of
+// scratch; starts: ctas + 1 unit offsets.
+__global__ void __launch_bounds__(SPLIT_THREADS) split_kernel(BpConst k, const double* __restrict__ pos,
+                                                              const int* __restrict__ sinc_wide,
+                                                              unsigned long long* __restrict__ cum,
+                                                              long long* __restrict__ starts)
+{
+    __shared__ unsigned long long s_part[SPLIT_THREADS];
+    const bool wide = *sinc_wide != 0;
+    const int T = k.tiles;
+    const int NS = max(1, min(SPLIT_SAMPLES, SPLIT_CELLS / max(T, 1)));
+    const int C = T * NS;
+    const int per = (C + SPLIT_THREADS - 1) / SPLIT_THREADS;
+    const int c0 = min((int)threadIdx.x * per, C), c1 = min(c0 + per, C);
+    const float span_scale = (float)((TILE_X - 1) * k.dx * k.inv_dr);
+    // per-cell costs (held in cum[c + 1] until the scan), and this thread's sum
+    unsigned long long sum = 0;
+    for (int c = c0; c < c1; ++c) {
+        const int t = c / NS, i = c % NS;
+        const long long n_lo = (long long)i * k.na / NS, n_hi = (long long)(i + 1) * k.na / NS;
+        unsigned long long w = 0;
+        if (n_hi > n_lo) {
+            const long long n = (n_lo + n_hi) / 2;
+            const float xc = (float)(k.x0 + ((double)((t % k.tiles_x) * TILE_X) + 0.5 * (TILE_X - 1)) * k.dx);
+            const float yc = (float)(k.y0 + ((double)((t / k.tiles_x) * TILE_Y) + 0.5 * (TILE_Y - 1)) * k.dy);
+            const float ax = (float)pos[3 * n], ay = (float)pos[3 * n + 1], az = (float)pos[3 * n + 2];
+            if (isfinite(ax) && isfinite(ay) && isfinite(az)) {
+                const float vx = xc - ax, vy = yc - ay, vz = (float)k.z0 - az;
+                const float r = sqrtf(fmaf(vx, vx, fmaf(vy, vy, vz * vz)));
+                w = (unsigned long long)sinc_unit_cost(span_scale * fabsf(vx) / fmaxf(r, 1.0f), wide) *
+                    (unsigned long long)(n_hi - n_lo);
+            }
+        }
+        cum[c + 1] = w;
+        sum += w;
+    }
+    // inclusive scan of the per-thread sums
+    s_part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < SPLIT_THREADS; off <<= 1) {
+        const unsigned long long v = threadIdx.x >= off ? s_part[threadIdx.x - off] : 0ull;
+        __syncthreads();
+        s_part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    unsigned long long run = threadIdx.x ? s_part[threadIdx.x - 1] : 0ull;
+    if (threadIdx.x == 0)
+        cum[0] = 0;
+    for (int c = c0; c < c1; ++c) {
+        run += cum[c + 1];
+        cum[c + 1] = run;                          // cost of cells 0 .. c
+    }
+    __syncthreads();
+    const unsigned long long total = s_part[SPLIT_THREADS - 1];
+    // CTA b starts where the cumulative cost reaches b / ctas of the total
+    const unsigned long long ctas = (unsigned long long)k.ctas;
+    for (int b = threadIdx.x; b <= k.ctas; b += SPLIT_THREADS) {
+        long long u;
+        if (b == k.ctas) {
+            u = k.units;
+        } else if (total == 0) {
+            u = (long long)b * k.units / k.ctas;
+        } else {
+            const unsigned long long target =
+                (total / ctas) * (unsigned long long)b + (total % ctas) * (unsigned long long)b / ctas;
+            int lo = 0, hi = C - 1;                // largest c < C with cum[c] <= target
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) / 2;
+                if (cum[mid] <= target)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const int t = lo / NS, i = lo % NS;
+            const long long n_lo = (long long)i * k.na / NS, n_hi = (long long)(i + 1) * k.na / NS;
+            const unsigned long long w = cum[lo + 1] - cum[lo];
+            const unsigned long long unit = n_hi > n_lo ? w / (unsigned long long)(n_hi - n_lo) : 0ull;
+            const long long into =
+                unit ? (long long)min((target - cum[lo]) / unit, (unsigned long long)(n_hi - n_lo)) : 0;
+            u = (long long)t * k.na + n_lo + into;
+        }
+        starts[b] = u;
+    }
+}
+
+cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
+                         unsigned long long* cum, long long* starts, cudaStream_t s)
+{
+    split_kernel<<<1, SPLIT_THREADS, 0, s>>>(k, pos, sinc_wide, cum, starts);
     return cudaGetLastError();
 }
 
