@@ -187,11 +187,14 @@ def test_accumulate_pulse_batches():
     parity.assert_parity(both, ref, "two batches")
 
 
-def test_bitwise_deterministic():
+@pytest.mark.parametrize("interp", ["linear", "sinc8"])
+def test_bitwise_deterministic(interp):
+    """Same inputs, same bits: the pulse sum has a fixed order, and the sinc
+    call's cost-weighted work split is computed in integers."""
     sc = scenes.make_scene(scenes.shrink(scenes.CONFIGS[1], na=300, nx=300, ny=260, nr=2048))
     with Plan(sc.params) as plan:
-        a = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
-        b = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan)
+        a = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan, interp=interp)
+        b = gpu_image(sc.params, sc.echoes, sc.antenna_pos, plan=plan, interp=interp)
     assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
 
 
@@ -256,15 +259,27 @@ def test_range_window_edges_full_window():
     parity.assert_parity(img, ref, "window edges")
 
 
-def test_non_finite_antenna_position_skips_pulse():
+@pytest.mark.parametrize("interp", ["linear", "sinc8"])
+def test_non_finite_antenna_position_skips_pulse(interp):
+    """Pulses with a non-finite antenna position contribute nothing (for sinc
+    they also carry no weight in the work split)."""
     sc = _small_scene(40, 130, na=30)
     pos = sc.antenna_pos.copy()
     pos[7, 1] = np.nan
     pos[19, 2] = np.inf
-    img = gpu_image(sc.params, sc.echoes, pos)
-    ref = oracle.backproject(sc.params, sc.echoes, pos)
+    img = gpu_image(sc.params, sc.echoes, pos, interp=interp)
+    ref = oracle.backproject(sc.params, sc.echoes, pos, interp=interp)
     assert np.all(np.isfinite(img))
-    parity.assert_parity(img, ref, "non-finite antenna")
+    parity.assert_parity(img, ref, "non-finite antenna " + interp)
+
+
+def test_sinc_all_antenna_positions_non_finite():
+    """No finite pulse at all: the sinc work split has zero total cost and
+    falls back to the equal split; the image is zero."""
+    sc = _small_scene(40, 130, na=30)
+    pos = np.full_like(sc.antenna_pos, np.nan)
+    img = gpu_image(sc.params, sc.echoes, pos, interp="sinc8")
+    assert np.array_equal(img, np.zeros_like(img))
 
 
 def test_near_field_exact_path():
