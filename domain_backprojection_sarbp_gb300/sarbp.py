@@ -63,13 +63,19 @@ def _check_device_tensor(t, name, dtype, shape):
     return ctypes.c_void_p(t.data_ptr() if t.numel() else None)
 
 
+# torch's name for each numpy dtype the host calls take (np.dtype(...).name
+# costs microseconds per call)
+_TORCH_DTYPE_NAME = {np.complex64: "torch.complex64", np.float64: "torch.float64",
+                     np.float32: "torch.float32"}
+
+
 def _host_ptr(a, name, shape, np_dtype):
     if hasattr(a, "is_cuda"):
         if a.is_cuda or not a.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")
         if tuple(a.shape) != shape:
             raise ValueError(f"{name} must have shape {shape}")
-        if str(a.dtype) != "torch." + np.dtype(np_dtype).name:
+        if str(a.dtype) != _TORCH_DTYPE_NAME[np_dtype]:
             raise ValueError(f"{name} must have dtype {np.dtype(np_dtype).name}")
         return ctypes.c_void_p(a.data_ptr() if a.numel() else None)
     if not (isinstance(a, np.ndarray) and a.dtype == np_dtype and a.flags.c_contiguous
