@@ -43,7 +43,7 @@
 //
 // 5. Variants of the same kernel (template INTERP): the 8-tap windowed sinc
 //    (a degree-4 or, on narrower spans, degree-3 polynomial per thread and
-//    pulse when the thread's pixels span at most a quarter bin), the nearest
+//    pulse when the thread's pixels span at most 0.34 bin), the nearest
 //    sample (one table entry per thread and pulse when its pixels round to
 //    two bins), and pixels on a height map (a float-pair row reference and a
 //    range series per pixel, with the two-entry form for rows in two bins).
@@ -82,9 +82,9 @@ __device__ __forceinline__ int row_pitch(const BpConst& k)
 {
     return (is_sinc(INTERP) || INTERP == INTERP_HEIGHTS_SINC8) ? k.tw : k.W;
 }
-constexpr float SINC_SPAN = 0.25f;          // widest spread of u (bins) for the sinc polynomial
+constexpr float SINC_SPAN = 0.34f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
-constexpr float SINC_SPAN3 = 0.11f;         // widest spread for the cubic on four nodes
+constexpr float SINC_SPAN3 = 0.17f;         // widest spread for the cubic on four nodes
 constexpr int HROW4 = TILE_X / 2 + 1;      // float4 per row of a tile's height terms (padded)
 
 struct __align__(16) Record {
@@ -476,10 +476,10 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
     if (is_sinc(INTERP) && kind == REC_FAST) {
-        // windowed sinc: when the thread's pixels span at most a quarter bin and
+        // windowed sinc: when the thread's pixels span at most SINC_SPAN bins and
         // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
-        // interpolated echo is a degree-4 polynomial in u (SINC_SPAN); when each
-        // half (quarter) of its pixels does, one polynomial per half (quarter)
+        // interpolated echo is a degree-4 polynomial in u; when each half
+        // (quarter) of its pixels does, one polynomial per half (quarter)
         float lo_e, hi_e, k0e;
         int kabs0;
         if (poly_interval(k, kb, bin0, lo_u, hi_u, lo_e, hi_e, k0e, kabs0)) {
@@ -862,18 +862,23 @@ __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseSta
 }
 
 // All of the thread's pixels within SINC_SPAN bins, every stencil inside the
-// recorded range. G(u) is smooth (a sum of eight windowed sincs), so over the
-// interval [lo_u, hi_u] (widened to a half-width of at least SINC_HALF_MIN) it
-// is interpolated at the five Chebyshev nodes mid + half cos((2i+1) pi / 10)
-// by a degree-4 polynomial in t = (u - mid) / half, evaluated per pixel as a
-// polynomial in s = u - mid. The interpolation error is at most
-// max|G^(5)| (half)^5 / (2^4 5!) <= pi^5 |e| 8 (1/8)^5 / 1920 ~ 4e-5 |e| for
-// half <= 1/8. Spans of at most SINC_SPAN3 take the cubic on the four nodes
-// mid + half cos((2i+1) pi / 8) instead (NN = 4): error at most
-// max|G^(4)| half^4 / (2^3 4!) <= pi^4 |e| 8 (0.055)^4 / 192 ~ 3.7e-5 |e|, one
-// node evaluation and two packed FMAs per pixel pair fewer. The echo phase
-// exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0)) is applied per pixel;
-// psi_k0 is folded into the coefficients.
+// recorded range. Within a bin G(u) is smooth (a sum of eight windowed sincs);
+// where a tap enters or leaves the stencil (a bin boundary) the Hann taper
+// makes G twice continuously differentiable. Over the interval [lo_u, hi_u]
+// (widened to a half-width of at least SINC_HALF_MIN) G is interpolated at the
+// five Chebyshev nodes mid + half cos((2i+1) pi / 10) by a degree-4 polynomial
+// in t = (u - mid) / half, evaluated per pixel as a polynomial in s = u - mid.
+// Inside one bin the error is at most max|G^(5)| half^5 / (2^4 5!), and
+// |G^(n)| <= max|e| max_f sum_d |h^(n)(f - d)|, which is 312 max|e| for n = 5
+// and 98 max|e| for n = 4 with this window (against 8 pi^n for a bare bound);
+// so half <= 0.17 gives at most 2.3e-5 max|e|. Spans of at most SINC_SPAN3
+// take the cubic on the four nodes mid + half cos((2i+1) pi / 8) instead
+// (NN = 4): error at most 98 max|e| half^4 / (2^3 4!) <= 2.7e-5 max|e| for
+// half <= 0.085, one node evaluation and two packed FMAs per pixel pair fewer.
+// Intervals across a bin boundary, where the bound does not apply, measure no
+// worse on random samples (at most 3.3e-5 max|e| at these spans). The echo
+// phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0)) is applied per
+// pixel; psi_k0 is folded into the coefficients.
 template <int NN>
 __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseState& st,
                                                 const float4* row, const float2* __restrict__ psi,

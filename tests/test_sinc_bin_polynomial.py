@@ -1,4 +1,4 @@
-"""The error figure behind the windowed-sinc kernel's per-bin polynomials.
+"""The error figures behind the windowed-sinc kernel's polynomials.
 
 The CUDA table stores, for each range bin, the interpolant G on that bin as a
 degree-7 polynomial: each of the eight tap weights h(1/2 + s - d), d = -3..4,
@@ -36,3 +36,65 @@ def test_degree_seven_error_bound():
 
 def test_degree_six_would_not_meet_the_budget():
     assert _summed_error(6) > 4e-5
+
+
+def _tap_derivative_sum(n):
+    """max over f of sum_d |h^(n)(f - d)|, d = -3..4: bounds |G^(n)| / max|e|."""
+    # the symbolic derivative cancels badly near t = 0 in float64: 30 digits
+    sympy = __import__("pytest").importorskip("sympy")
+    import mpmath
+    mpmath.mp.dps = 30
+    t = sympy.symbols("t", real=True)
+    h = sympy.sin(sympy.pi * t) / (sympy.pi * t) * (1 + sympy.cos(sympy.pi * t / 4)) / 2
+    d = sympy.lambdify(t, sympy.diff(h, t, n), "mpmath")
+    f = np.linspace(0.0005, 0.9995, 300)
+    return float(max(sum(abs(d(mpmath.mpf(float(x)) - k)) for k in range(-3, 5)) for x in f))
+
+
+def test_thread_polynomial_bounds_at_the_kernel_spans():
+    """The thread-level interpolants the kernel uses: degree 4 on spans up to
+    0.34 bin and degree 3 up to 0.17 bin. With the window's own derivative
+    sums (98 for n = 4, 312 for n = 5) the Chebyshev bounds stay under the
+    4e-5 budget; the bare 8 pi^n bound would not allow these spans."""
+    s4, s5 = _tap_derivative_sum(4), _tap_derivative_sum(5)
+    assert 95 < s4 < 101 and 305 < s5 < 318, (s4, s5)
+    quartic = s5 * 0.17 ** 5 / (2 ** 4 * 120)
+    cubic = s4 * 0.085 ** 4 / (2 ** 3 * 24)
+    assert quartic < 2.5e-5 and cubic < 2.8e-5, (quartic, cubic)
+    assert 8 * np.pi ** 5 * 0.17 ** 5 / (2 ** 4 * 120) > 4e-5
+
+
+def _window_g(u, e):
+    k = np.floor(u).astype(int)
+    out = np.zeros(u.shape, complex)
+    for d in range(-3, 5):
+        t = u - (k + d)
+        out += e[k + d] * _h(t)
+    return out
+
+
+def test_thread_polynomial_across_a_bin_boundary():
+    """Where the interval crosses a bin boundary G is only C^2 (a tap enters
+    the stencil, another leaves), so the derivative bound does not apply;
+    measured on random samples (|e| <= 1) the interpolants stay under 4e-5."""
+    rng = np.random.default_rng(7)
+    worst = {}
+    for nn, span in ((4, 0.17), (5, 0.34)):
+        i = np.arange(nn)
+        x = np.cos((2 * i + 1) * np.pi / (2 * nn))
+        w = 0.0
+        for _ in range(400):
+            e = np.exp(2j * np.pi * rng.random(64)) * rng.random(64) ** 0.2
+            base = 20 + rng.integers(0, 20)
+            mid = base + (rng.random() - 0.5) * span          # straddles bin `base`
+            nodes = mid + 0.5 * span * x
+            g = _window_g(nodes, e)
+            v = np.vander(x, nn, increasing=True)
+            cr, ci = np.linalg.solve(v, g.real), np.linalg.solve(v, g.imag)
+            uu = np.linspace(mid - 0.5 * span, mid + 0.5 * span, 101)
+            tt = (uu - mid) / (0.5 * span)
+            p = (np.polynomial.polynomial.polyval(tt, cr)
+                 + 1j * np.polynomial.polynomial.polyval(tt, ci))
+            w = max(w, np.abs(p - _window_g(uu, e)).max())
+        worst[nn] = w
+    assert worst[4] < 4e-5 and worst[5] < 4e-5, worst
