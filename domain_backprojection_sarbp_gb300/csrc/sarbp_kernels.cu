@@ -85,6 +85,7 @@ __device__ __forceinline__ int row_pitch(const BpConst& k)
 constexpr float SINC_SPAN = 0.34f;          // widest spread of u (bins) for the sinc polynomial
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
 constexpr float SINC_SPAN3 = 0.17f;         // widest spread for the cubic on four nodes
+constexpr float SINC_SPAN2 = 0.05f;         // widest spread for the quadratic on three nodes
 constexpr int HROW4 = TILE_X / 2 + 1;      // float4 per row of a tile's height terms (padded)
 
 struct __align__(16) Record {
@@ -391,7 +392,8 @@ constexpr int NP = TILE_X / 2;
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
-                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7, MODE_POLY4Q = 8 };
+                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7, MODE_POLY4Q = 8,
+                       MODE_POLY2 = 9 };
 
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
@@ -483,7 +485,8 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
         float lo_e, hi_e, k0e;
         int kabs0;
         if (poly_interval(k, kb, bin0, lo_u, hi_u, lo_e, hi_e, k0e, kabs0)) {
-            st.mode = hi_e - lo_e <= SINC_SPAN3 ? MODE_POLY3 : MODE_POLY;
+            const float sp = hi_e - lo_e;
+            st.mode = sp <= SINC_SPAN2 ? MODE_POLY2 : (sp <= SINC_SPAN3 ? MODE_POLY3 : MODE_POLY);
             st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
             if (INTERP == INTERP_SINC8_WIDE) {
                 // the nodes lie in bins k0 and k0 + 1: start fetching their
@@ -516,7 +519,7 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
             }
         }
     }
-    if (st.mode != MODE_POLY && st.mode != MODE_POLY3)
+    if (st.mode != MODE_POLY && st.mode != MODE_POLY3 && st.mode != MODE_POLY2)
         st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);   // the part modes recompute their intervals
     st.t1d = make_float2(0.f, 0.f);
     float kn = 0.0f;
@@ -754,11 +757,24 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
 
 // Monomial coefficients p[n] (complex, in t = (u - mid) / half) of the
 // interpolant of G on [mid - half, mid + half] at NN Chebyshev nodes
-// (NN = 5: degree 4; NN = 4: degree 3), by the inverse Vandermonde matrix.
+// (NN = 5: degree 4; NN = 4: degree 3; NN = 3: degree 2), by the inverse
+// Vandermonde matrix.
 template <int NN>
 __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const float4* row,
                                             float2 (&p)[5])
 {
+    if (NN == 3) {
+        constexpr float C1 = 0.866025404f;                       // cos(pi/6)
+        const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
+        const float2 g1 = sinc_value(mid, kb, row);
+        const float2 g2 = sinc_value(fmaf(half, -C1, mid), kb, row);
+        p[0] = g1;
+        p[1] = make_float2(0.577350269f * (g0.x - g2.x), 0.577350269f * (g0.y - g2.y));
+        p[2] = make_float2(0.666666667f * (g0.x + g2.x - 2.0f * g1.x),
+                           0.666666667f * (g0.y + g2.y - 2.0f * g1.y));
+        p[3] = p[4] = make_float2(0.0f, 0.0f);
+        return;
+    }
     if (NN == 4) {
         constexpr float C1 = 0.923879533f, C2 = 0.382683432f;   // cos(pi/8), cos(3 pi/8)
         const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
@@ -874,7 +890,11 @@ __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseSta
 // so half <= 0.17 gives at most 2.3e-5 max|e|. Spans of at most SINC_SPAN3
 // take the cubic on the four nodes mid + half cos((2i+1) pi / 8) instead
 // (NN = 4): error at most 98 max|e| half^4 / (2^3 4!) <= 2.7e-5 max|e| for
-// half <= 0.085, one node evaluation and two packed FMAs per pixel pair fewer.
+// half <= 0.085, one node evaluation and two packed FMAs per pixel pair fewer;
+// spans of at most SINC_SPAN2 the quadratic on mid, mid +- half cos(pi / 6)
+// (NN = 3): at most 31 max|e| half^3 / (2^2 3!) <= 2.0e-5 max|e| for
+// half <= 0.025 (the third derivative is bounded on both sides of a bin
+// boundary, so this bound also holds across one).
 // Intervals across a bin boundary, where the bound does not apply, measure no
 // worse on random samples (at most 3.3e-5 max|e| at these spans). The echo
 // phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0)) is applied per
@@ -1467,7 +1487,9 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
         return;
     }
     if (is_sinc(INTERP)) {
-        if (st.mode == MODE_POLY3)
+        if (st.mode == MODE_POLY2)
+            sinc_poly_pulse<3>(k, st, row, psi, accre, accim);
+        else if (st.mode == MODE_POLY3)
             sinc_poly_pulse<4>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_POLY)
             sinc_poly_pulse<5>(k, st, row, psi, accre, accim);
@@ -1872,6 +1894,8 @@ constexpr int SPLIT_SAMPLES = 64;
 // bins, from the modes' instruction counts per thread and pulse.
 __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
 {
+    if (span <= SINC_SPAN2)
+        return 89;
     if (span <= SINC_SPAN3)
         return 100;
     if (span <= SINC_SPAN)

@@ -53,14 +53,16 @@ def _tap_derivative_sum(n):
 
 def test_thread_polynomial_bounds_at_the_kernel_spans():
     """The thread-level interpolants the kernel uses: degree 4 on spans up to
-    0.34 bin and degree 3 up to 0.17 bin. With the window's own derivative
-    sums (98 for n = 4, 312 for n = 5) the Chebyshev bounds stay under the
-    4e-5 budget; the bare 8 pi^n bound would not allow these spans."""
-    s4, s5 = _tap_derivative_sum(4), _tap_derivative_sum(5)
-    assert 95 < s4 < 101 and 305 < s5 < 318, (s4, s5)
+    0.34 bin, degree 3 up to 0.17 bin and degree 2 up to 0.05 bin. With the
+    window's own derivative sums (31 for n = 3, 98 for n = 4, 312 for n = 5)
+    the Chebyshev bounds stay under the 4e-5 budget; the bare 8 pi^n bound
+    would not allow these spans."""
+    s3, s4, s5 = _tap_derivative_sum(3), _tap_derivative_sum(4), _tap_derivative_sum(5)
+    assert 30 < s3 < 32.5 and 95 < s4 < 101 and 305 < s5 < 318, (s3, s4, s5)
     quartic = s5 * 0.17 ** 5 / (2 ** 4 * 120)
     cubic = s4 * 0.085 ** 4 / (2 ** 3 * 24)
-    assert quartic < 2.5e-5 and cubic < 2.8e-5, (quartic, cubic)
+    quadratic = s3 * 0.025 ** 3 / (2 ** 2 * 6)       # spans up to 0.05 bin
+    assert quartic < 2.5e-5 and cubic < 2.8e-5 and quadratic < 2.1e-5, (quartic, cubic, quadratic)
     assert 8 * np.pi ** 5 * 0.17 ** 5 / (2 ** 4 * 120) > 4e-5
 
 
