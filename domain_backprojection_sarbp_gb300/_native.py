@@ -24,7 +24,7 @@ EXPORTS = (
     "sarbp_set_timing", "sarbp_kernel_times", "sarbp_backproject_noalloc",
     "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
     "sarbp_plan_heights", "sarbp_backproject_heights", "sarbp_backproject_streamed",
-    "sarbp_backproject_volume", "sarbp_debug_fail_alloc",
+    "sarbp_backproject_volume", "sarbp_debug_fail_alloc", "sarbp_debug_sinc_taps",
 )
 
 SARBP_WINDOW_NONE = 0
@@ -98,6 +98,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_rc_destroy.restype = st
     lib.sarbp_debug_fail_alloc.argtypes = [ctypes.c_int32]
     lib.sarbp_debug_fail_alloc.restype = None
+    lib.sarbp_debug_sinc_taps.argtypes = [ctypes.POINTER(ctypes.c_float)]
+    lib.sarbp_debug_sinc_taps.restype = ctypes.c_int32
     lib.sarbp_destroy.argtypes = [vp]
     lib.sarbp_destroy.restype = st
     lib.sarbp_status_string.argtypes = [st]

@@ -438,6 +438,14 @@ void sarbp_debug_fail_alloc(int32_t countdown)
     sarbp::g_fail_countdown.store(countdown > 0 ? countdown : 0);
 }
 
+sarbp_status sarbp_debug_sinc_taps(float* out)
+{
+    if (!out)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp::sinc_taps_host(out);
+    return SARBP_OK;
+}
+
 const char* sarbp_status_string(sarbp_status status)
 {
     switch (status) {

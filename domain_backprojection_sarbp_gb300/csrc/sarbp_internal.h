@@ -89,6 +89,8 @@ cudaError_t prepare_kernels();
 constexpr int SPLIT_CELLS = 65536;         // (tile, pulse segment) cells of the cost estimate
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s);
+// The 8 x 8 windowed-sinc tap polynomial coefficients (row d + 3, column n).
+void sinc_taps_host(float* out);
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,
                           cudaStream_t s);
 cudaError_t backproject_occupancy(int* ctas_per_sm);

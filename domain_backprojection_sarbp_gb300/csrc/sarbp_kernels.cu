@@ -1995,6 +1995,14 @@ __global__ void __launch_bounds__(SPLIT_THREADS) split_kernel(BpConst k, const d
     }
 }
 
+void sinc_taps_host(float* out)
+{
+    static const SincTaps taps = fit_sinc_taps();
+    for (int d = 0; d < 8; ++d)
+        for (int n = 0; n < 8; ++n)
+            out[8 * d + n] = taps.c[d][n];
+}
+
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s)
 {

@@ -278,6 +278,18 @@ sarbp_status sarbp_destroy(sarbp_plan_t plan);
  */
 void sarbp_debug_fail_alloc(int32_t countdown);
 
+/*
+ * Testing aid (host only, needs no GPU): the 64 coefficients of the
+ * windowed-sinc tap polynomials the library's sinc table is built from.
+ * out[8 * (d + 3) + n], d = -3 .. 4, n = 0 .. 7, is the coefficient of s^n in
+ * the degree-7 interpolant (eight Chebyshev nodes of the bin) of the weight
+ * h(1/2 + s - d), h(t) = sinc(t) (1 + cos(pi t / 4)) / 2, on s in [-1/2, 1/2]
+ * (the interpolant of the 8-tap windowed sinc on bin k at u = k + 1/2 + s is
+ * sum_n s^n sum_d out[8 (d + 3) + n] e_{k+d}). out: host pointer to 64 floats.
+ * Returns SARBP_ERR_INVALID_ARG for a NULL pointer.
+ */
+sarbp_status sarbp_debug_sinc_taps(float* out);
+
 /* Static, never-NULL description of a status code. */
 const char* sarbp_status_string(sarbp_status status);
 

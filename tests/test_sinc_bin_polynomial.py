@@ -100,3 +100,28 @@ def test_thread_polynomial_across_a_bin_boundary():
             w = max(w, np.abs(p - _window_g(uu, e)).max())
         worst[nn] = w
     assert worst[4] < 4e-5 and worst[5] < 4e-5, worst
+
+
+def test_library_tap_polynomials():
+    """The coefficients the CUDA library builds its sinc table from
+    (sarbp_debug_sinc_taps, host code, no GPU needed) reproduce each tap weight
+    h(1/2 + s - d) on a fine grid: the eight errors sum to under 5.5e-6 (the
+    figure the kernel's comments and the design state), and they match a
+    float64 fit at the same nodes to float32 rounding."""
+    import ctypes
+    from domain_backprojection_sarbp_gb300 import _native
+    lib = _native.lib()
+    out = (ctypes.c_float * 64)()
+    assert lib.sarbp_debug_sinc_taps(out) == _native.SARBP_OK
+    assert lib.sarbp_debug_sinc_taps(None) == _native.SARBP_ERR_INVALID_ARG
+    c = np.frombuffer(out, dtype=np.float32).reshape(8, 8).astype(np.float64)
+    s = np.linspace(-0.5, 0.5, 20001)
+    total = 0.0
+    i = np.arange(8)
+    nodes = 0.5 * np.cos((2 * i + 1) * np.pi / 16)
+    for row, d in enumerate(range(-3, 5)):
+        fit = np.polynomial.polynomial.polyval(s, c[row])
+        total += np.max(np.abs(fit - _h(0.5 + s - d)))
+        ref = np.linalg.solve(np.vander(nodes, increasing=True), _h(0.5 + nodes - d))
+        assert np.allclose(c[row], ref, rtol=1e-6, atol=1e-6), (d, c[row], ref)
+    assert total < 5.5e-6, total
