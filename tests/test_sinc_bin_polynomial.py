@@ -109,7 +109,8 @@ def test_library_tap_polynomials():
     figure the kernel's comments and the design state), and they match a
     float64 fit at the same nodes to float32 rounding."""
     import ctypes
-    from domain_backprojection_sarbp_gb300 import _native
+    from domain_backprojection_sarbp_gb300 import _native, build
+    build.build()                      # the library builds and loads without a GPU
     lib = _native.lib()
     out = (ctypes.c_float * 64)()
     assert lib.sarbp_debug_sinc_taps(out) == _native.SARBP_OK
