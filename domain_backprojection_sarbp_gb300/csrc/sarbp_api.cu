@@ -1132,6 +1132,13 @@ sarbp_status sarbp_backproject_noalloc(void* image, const void* echoes,
         if (c0 > 0)
             pc.flags |= SARBP_ACCUMULATE;
         geo.p = pc;
+        // a short last chunk: the zero pad the kernels may read past the last
+        // row goes straight after row cn - 1, as in a plan's table (rows cn ..
+        // chunk - 1 still hold the previous chunk's entries)
+        if (cn < chunk &&
+            cudaMemsetAsync(table + (size_t)cn * geo.W, 0, TABLE_PAD * sizeof(float4), s) !=
+                cudaSuccess)
+            return SARBP_ERR_CUDA;
         BpConst k = make_const(&geo, &pc);
         k.ctas = geo.tiles;                     // one whole tile per CTA: direct writes only
         k.units = (long long)geo.tiles * cn;

@@ -101,7 +101,7 @@ cudaError_t backproject_occupancy(int* ctas_per_sm);
 cudaError_t device_alloc(void** ptr, size_t bytes);
 
 // Device address of the fixed scratch array used by sarbp_backproject_noalloc
-// (looked up once per device, with that device current).
+// in the context current on the calling thread (looked up on every call).
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(16) << 20;
 cudaError_t noalloc_scratch(void** ptr);
 

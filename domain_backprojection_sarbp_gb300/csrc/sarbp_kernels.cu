@@ -52,7 +52,6 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
-#include <mutex>
 
 namespace sarbp {
 namespace {
@@ -1783,25 +1782,14 @@ static __device__ __align__(256) unsigned char noalloc_scratch_array[NOALLOC_SCR
 cudaError_t noalloc_scratch(void** ptr)
 {
     // The symbol's name is only a host-side stand-in; kernels need the device
-    // address, looked up once per device and cached.
-    constexpr int MAX_CACHED_DEVICES = 64;
-    static std::mutex mu;
-    static void* cached[MAX_CACHED_DEVICES] = {};
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < MAX_CACHED_DEVICES && cached[dev]) {
-        *ptr = cached[dev];
-        return cudaSuccess;
-    }
+    // address. It is looked up on every call, in the context current on the
+    // calling thread: the array lives in each context that loads this module,
+    // and a reset device or another context gives it a new address. The
+    // lookup allocates nothing; the first one in a context loads the array.
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, noalloc_scratch_array);
+    const cudaError_t e = cudaGetSymbolAddress(&p, noalloc_scratch_array);
     if (e != cudaSuccess)
         return e;
-    if (dev >= 0 && dev < MAX_CACHED_DEVICES)
-        cached[dev] = p;
     *ptr = p;
     return cudaSuccess;
 }

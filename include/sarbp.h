@@ -391,10 +391,14 @@ sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan);
  * (about (image range extent / dr) x 16 bytes) does not fit are rejected with
  * SARBP_ERR_SCRATCH_TOO_SMALL before any work is queued.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. The call allocates nothing: no cudaMalloc, no cudaFree, no
- * allocating library routine.
+ * Every call looks up the array's device address in the CUDA context current
+ * on the calling thread (cudaGetSymbolAddress, which allocates nothing). The
+ * array exists once per context that loads the library: after a
+ * cudaDeviceReset, or in another context on the same device, it has a new
+ * address and new, uninitialised contents, and the next call uses that one.
+ * The first call in a context loads the array; make that first call before
+ * any stream capture. The call allocates nothing: no cudaMalloc, no cudaFree,
+ * no allocating library routine.
  *
  * All calls share the one array and it keeps the last call's contents; the
  * parts that must start at zero are cleared by each call. Calls whose work

@@ -12,7 +12,7 @@ cross-correlation, computed as ifft(fft(raw, N) * conj(fft(ref, N)) * W)[:ns]
 with N the smallest power of two >= ns + L - 1 (no circular wrap). W = 1, or
 a weighting over the centred band |f| <= b/2 (f = signed frequency in cycles
 per sample, b = band fraction) and 0 outside it: Hamming
-0.54 + 0.46 cos(2 pi f / b), or Taylor (nbar = 4, 35 dB sidelobes)
+0.54 + 0.46 cos(2 pi f / b), or Taylor (nbar = 5, 35 dB sidelobes)
 1 + 2 sum_m F_m cos(2 pi m f / b) with Taylor's coefficients F_m. numpy's FFT
 is a library step of that definition.
 

@@ -3,10 +3,15 @@
 sarbp_backproject_noalloc serves callers that cannot allocate device memory
 (a plug-in handed only buffers, a framework whose pool owns the GPU, a
 real-time loop that forbids cudaMalloc once running). It keeps its scratch in
-a fixed device array shared by all calls, so it is called twice in a row here:
-the second call must not see anything the first one left behind. It groups
-the pulse sum by chunks, so it is compared with sarbp_backproject within the
-parity tolerance, not bitwise. This file is named to run last.
+a fixed device array shared by all calls, so the calls here follow one
+another with different sizes: the page-sized scene (two chunks of pulses, the
+second one short, 368 table entries per pulse), then the tiny scene (one
+chunk, a narrower row), then the page-sized scene again. Each result must
+match the plan-based entry point, so nothing one call leaves in the array
+may leak into the next. It groups the pulse sum by chunks, so it is compared
+with sarbp_backproject within the parity tolerance, not bitwise. A call is
+also made with the library's next device allocation armed to fail: it must
+succeed and leave that failure unused. This file is named to run last.
 """
 
 import ctypes
@@ -46,34 +51,65 @@ def _with_plan(sc, e, a):
     return img.cpu().numpy()
 
 
+def _call(img, sc, e, a, flags=0):
+    p = _native.Params.from_dict(sc.params, flags=flags)
+    stream = torch.cuda.current_stream().cuda_stream
+    return _native.lib().sarbp_backproject_noalloc(
+        ctypes.c_void_p(img.data_ptr()), ctypes.c_void_p(e.data_ptr()),
+        ctypes.c_void_p(a.data_ptr()), ctypes.byref(p), ctypes.c_void_p(stream))
+
+
 def _no_alloc(sc, e, a, flags=0, init=None):
     img = torch.full((sc.params["ny"], sc.params["nx"]), complex(5.0, 5.0),
                      dtype=torch.complex64, device=DEV)
     if init is not None:
         img.copy_(torch.from_numpy(init))
-    p = _native.Params.from_dict(sc.params, flags=flags)
-    stream = torch.cuda.current_stream().cuda_stream
-    st = _native.lib().sarbp_backproject_noalloc(
-        ctypes.c_void_p(img.data_ptr()), ctypes.c_void_p(e.data_ptr()),
-        ctypes.c_void_p(a.data_ptr()), ctypes.byref(p), ctypes.c_void_p(stream))
+    st = _call(img, sc, e, a, flags)
     assert st == _native.SARBP_OK, _native.lib().sarbp_status_string(st)
     torch.cuda.synchronize()
     return img.cpu().numpy()
 
 
-def test_matches_plan_entry_point_twice_in_a_row():
+def test_matches_plan_entry_point_across_sizes():
     small = scenes.make_scene(scenes.CONFIGS[0])
     # the page-sized scene needs two chunks of pulses in the 16 MiB scratch
     page = scenes.make_scene(scenes.CONFIGS[2])
+    refs, dev = {}, {}
     for sc in (small, page):
-        e, a = _device(sc)
-        ref = _with_plan(sc, e, a)
-        first = _no_alloc(sc, e, a)
-        second = _no_alloc(sc, e, a)
-        parity.assert_parity(first, ref, f"{sc.cfg.name} first call")
-        parity.assert_parity(second, ref, f"{sc.cfg.name} second call")
-        assert np.array_equal(first.view(np.uint64), second.view(np.uint64))
-        del e, a
+        dev[sc.cfg.name] = _device(sc)
+        refs[sc.cfg.name] = _with_plan(sc, *dev[sc.cfg.name])
+    out = []
+    for sc in (page, small, page):
+        got = _no_alloc(sc, *dev[sc.cfg.name])
+        parity.assert_parity(got, refs[sc.cfg.name], f"{sc.cfg.name} call {len(out) + 1}")
+        out.append(got)
+    # the same inputs give the same image, whatever ran in between
+    assert np.array_equal(out[0].view(np.uint64), out[2].view(np.uint64))
+
+
+def test_allocates_nothing():
+    sc = scenes.make_scene(scenes.CONFIGS[1])
+    e, a = _device(sc)
+    ref = _with_plan(sc, e, a)
+    _no_alloc(sc, e, a)                            # the array is loaded in this context
+    lib = _native.lib()
+    img = torch.full((sc.params["ny"], sc.params["nx"]), complex(5.0, 5.0),
+                     dtype=torch.complex64, device=DEV)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    lib.sarbp_debug_fail_alloc(1)                  # the next device allocation would fail
+    try:
+        assert _call(img, sc, e, a) == _native.SARBP_OK
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free_before
+        # the armed failure is still there: the next plan meets it
+        h = ctypes.c_void_p()
+        prm = _native.Params.from_dict(sc.params)
+        assert lib.sarbp_plan(ctypes.byref(h), ctypes.byref(prm)) == _native.SARBP_ERR_OOM
+        assert not h.value
+    finally:
+        lib.sarbp_debug_fail_alloc(0)
+    parity.assert_parity(img.cpu().numpy(), ref, "no-alloc call with allocations armed to fail")
 
 
 def test_accumulate_and_rejection():
