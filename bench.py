@@ -17,6 +17,7 @@ The reported value is all ranks' updates divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -61,9 +62,32 @@ def measured_hbm_gbs() -> tuple[float, str]:
 
 HBM_GBS, HBM_BASIS = measured_hbm_gbs()
 L2_FLUSH_BYTES = 256 << 20
-# dram read+write bytes of one bp_kernel launch, from ncu (None until captured
-# for the current kernel)
-MAIN_KERNEL_TRAFFIC = 14_007_552   # ncu dram read + write, one bp_kernel<0> launch, page-sized scene
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one bp_kernel<0> launch on
+# the page-sized scene (profiles/bp_kernel_page_spotlight.md), and the SHA-256
+# of the kernel sources that capture ran: the bench reports the figure only
+# while the sources are unchanged, and null (no counters for this kernel) after
+MAIN_KERNEL_TRAFFIC = 14_007_552
+MAIN_KERNEL_TRAFFIC_SOURCES = ("domain_backprojection_sarbp_gb300/csrc/sarbp_kernels.cu",
+                               "domain_backprojection_sarbp_gb300/csrc/sarbp_internal.h")
+MAIN_KERNEL_TRAFFIC_SHA256 = "f9d8e6d3f64ea6e4c3f8842c12ddde66919cadd3ad8a67cf4e64fcd7ee6079a2"
+
+
+def kernel_sources_sha256(paths=None) -> str:
+    """SHA-256 over the kernel sources, in order."""
+    h = hashlib.sha256()
+    for rel in paths or MAIN_KERNEL_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def main_kernel_traffic():
+    """The captured traffic while the kernel sources match the capture, else None."""
+    try:
+        same = kernel_sources_sha256() == MAIN_KERNEL_TRAFFIC_SHA256
+    except OSError:
+        same = False
+    return MAIN_KERNEL_TRAFFIC if same else None
 
 
 # ------------------------------------------------------------------ ranks
@@ -485,7 +509,7 @@ def run_ours(args, scene, rank, world, local, dist):
         "config": config_block(scene, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)"),
         "roofline": {
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
-            "frac": (achieved / peak) if achieved else None, "traffic": MAIN_KERNEL_TRAFFIC,
+            "frac": (achieved / peak) if achieved else None, "traffic": main_kernel_traffic(),
             "kernel": "bp_kernel",
             "peak_basis": f"{sms} SMs x {clock_mhz:.0f} MHz x {MUFU_PER_SM_CLK} MUFU/clk / "
                           f"{MUFU_PER_UPDATE} MUFU per update",

@@ -91,3 +91,16 @@ def test_cpu_baseline_reports_one_thread_and_extrapolation():
     updates = sc.params["na"] * sc.params["nx"] * sc.params["ny"]
     assert abs(ex["one_thread"] * cb["one_thread"]["value"] * 1e9 - updates) <= 1e-6 * updates
     assert cb["cpu_model"] and cb["page_figure"]["one_thread_cpu_s"] == 56.0
+
+
+def test_traffic_is_reported_only_for_the_captured_kernel(monkeypatch):
+    """The ncu traffic figure belongs to one revision of the kernel sources:
+    the same sources report it, any other revision reports null."""
+    now = bench.kernel_sources_sha256()
+    monkeypatch.setattr(bench, "MAIN_KERNEL_TRAFFIC_SHA256", now)
+    assert bench.main_kernel_traffic() == bench.MAIN_KERNEL_TRAFFIC
+    monkeypatch.setattr(bench, "MAIN_KERNEL_TRAFFIC_SHA256", "0" * 64)
+    assert bench.main_kernel_traffic() is None
+    monkeypatch.setattr(bench, "MAIN_KERNEL_TRAFFIC_SOURCES", ("no/such/file.cu",))
+    monkeypatch.setattr(bench, "MAIN_KERNEL_TRAFFIC_SHA256", now)
+    assert bench.main_kernel_traffic() is None

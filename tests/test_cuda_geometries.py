@@ -79,6 +79,15 @@ CASES = {
     "off_broadside": (_track_line(256, 0.1), 9.6e9, 0.8333, 0.25, (2500.0, 1500.0)),
 }
 
+# slant ranges at and beyond the ~10 km the float32 phase must hold at
+# (SARBP-GPU §2.2, range-computation precision): X band at 12.8 km (8000 m
+# altitude, 10 km ground offset) and Ka band (lambda = 8.6 mm, 4.5 rad of phase
+# per millimetre of range) at 10 km (6000 m, 8 km)
+LONG_RANGE = {
+    "x_band_12800m": (_track_line(512, 0.1, y=-10000.0, z=8000.0), 9.6e9, 0.8333, 0.15, (0.0, 0.0)),
+    "ka_band_10km": (_track_line(512, 0.02, y=-8000.0, z=6000.0), 35e9, 0.15, 0.05, (0.0, 0.0)),
+}
+
 
 def test_anisotropic_pixels_and_raised_plane():
     """dx != dy, an image plane 120 m above the origin and a descending track."""
@@ -178,3 +187,18 @@ def test_sinc8_wide_geometry_at_range_axis_edges(name):
     got = _gpu(cut, e, pos, "sinc8")
     ref = oracle.backproject(cut, e, pos, interp="sinc8")
     print(name, parity.assert_parity(got, ref, name + " cut range axis"))
+
+
+@pytest.mark.parametrize("interp", ["linear", "sinc8", "nearest"])
+@pytest.mark.parametrize("name", sorted(LONG_RANGE))
+def test_long_slant_range(name, interp):
+    """Every pixel against the oracle at 10-13 km slant range."""
+    pos, fc, dr, spacing, centre = LONG_RANGE[name]
+    params, echo, pos = _scene(pos, fc, dr, spacing, centre=centre, seed=5)
+    rng_c = float(np.linalg.norm(pos[len(pos) // 2]))
+    assert rng_c >= (12_000.0 if fc < 20e9 else 9_900.0), rng_c
+    got = _gpu(params, echo, pos, interp)
+    ref = oracle.backproject(params, echo, pos, interp=interp)
+    m = parity.compare(got, ref)
+    print(name, interp, f"slant range {rng_c:.0f} m", m)
+    assert m["finite"] and m["rel_l2"] <= parity.REL_L2 and m["max_err"] <= parity.MAX_ERR, m
