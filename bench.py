@@ -41,6 +41,15 @@ WORKLOAD = ("page-sized airborne spotlight: Na=4096 pulses, Nr=4096 complex64 bi
 # 1024 x 1024 image (4096 * 1024 * 1024 updates, §1.2) -> 5.37 Gupd/s.
 PAGE_GUPD = 4096 * 1024 * 1024 / 0.8 / 1e9
 MUFU_PER_SM_CLK = 16          # sine/cosine lanes per SM per clock
+FMA_PER_SM_CLK = 128          # FP32 lanes per SM per clock
+# FP32-pipe operations per update of the page's loop for each interpolation
+# (SARBP-GPU §2.2 and the §3.3 pseudo-code): p - a (3), |p - a|^2 (3), the
+# range index (1) and its fraction or rounding (1), the interpolation (linear:
+# 2 complex lerps = 4; 8-tap sinc: 8 real weights on complex samples = 16;
+# nearest: none) and the phase multiply-accumulate (4). The height map adds
+# no operation: the pixel's z enters p - a like x and y.
+FMA_OPS_PER_UPDATE = {"linear": 16, "sinc8": 28, "nearest": 12, "heights": 16}
+LARGE_SCENES = ("large_scene", "nonideal_track")
 MUFU_PER_UPDATE = 2           # sin and cos of the phase; the range needs no sqrt here
 PAGE_SFU_PER_UPDATE = 3       # the page's loop: sqrt, sin, cos
 SM_MAX_MHZ_FALLBACK = 2070.0
@@ -292,6 +301,64 @@ def config_block(scene, l2):
 
 
 # ------------------------------------------------------------------ GPU leg
+def time_calls(call, steps, flush, stream):
+    """Summed CUDA-event milliseconds of ``steps`` calls, L2 flushed before each."""
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for i in range(steps):
+        flush.fill_(float(i))
+        start.record(stream)
+        call()
+        end.record(stream)
+        end.synchronize()
+        total += start.elapsed_time(end)
+    return total
+
+
+def large_scene_lines(name, steps, flush, stream, dev, roofs):
+    """Per-call rates of the linear and windowed-sinc backprojection of one of
+    the large scenes (device-resident inputs, L2 flushed before each call)."""
+    import torch
+
+    from domain_backprojection_sarbp_gb300 import Plan
+    from synth import scenes
+
+    cfg = scenes.config_by_name(name)
+    t0 = time.perf_counter()
+    sc = scenes.make_scene(cfg)
+    gen_s = time.perf_counter() - t0
+    p = sc.params
+    updates = p["na"] * p["nx"] * p["ny"]
+    echoes = torch.from_numpy(sc.echoes).to(dev)
+    pos = torch.from_numpy(sc.antenna_pos).to(dev)
+    del sc
+    image = torch.empty((p["ny"], p["nx"]), dtype=torch.complex64, device=dev)
+    out = {"workload": f"{name}: Na={p['na']} pulses, Nr={p['nr']} complex64 bins, "
+                       f"{p['nx']}x{p['ny']} image at {p['dx']} m",
+           "updates_per_call": updates, "scene_generation_s": gen_s}
+    with Plan(p, interp="sinc8") as plan:
+        plan.set_timing(True)
+        for interp in ("linear", "sinc8"):
+            def call():
+                plan.backproject(image, echoes, pos, interp=interp)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(dev)
+            plan.kernel_times()
+            ms = time_calls(call, steps, flush, stream)
+            main_ms, launches = plan.kernel_times()
+            main = updates / (main_ms / max(launches, 1) / 1e3) / 1e9
+            out[interp] = {"steps": steps, "value": updates * steps / (ms / 1e3) / 1e9,
+                           "unit": UNIT, "ms_per_step": ms / steps, "main_kernel_gupd": main,
+                           "mufu_roof_frac": main / roofs["mufu"],
+                           "fma_roof_frac": main / roofs["fma"][interp]}
+    del echoes, pos, image
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, scene, rank, world, local, dist):
     import torch
 
@@ -495,12 +562,22 @@ def run_ours(args, scene, rank, world, local, dist):
         clock_mhz = clocks["sm_max_mhz"]
     peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / MUFU_PER_UPDATE / 1e9
     page_peak = sms * clock_mhz * 1e6 * MUFU_PER_SM_CLK / PAGE_SFU_PER_UPDATE / 1e9
+    fma_peaks = {k: sms * clock_mhz * 1e6 * FMA_PER_SM_CLK / v / 1e9
+                 for k, v in FMA_OPS_PER_UPDATE.items()}
     achieved = updates / (main_ms / max(launches, 1) / 1e3) / 1e9 if launches else None
     # every interpolation variant issues one sine and one cosine per update on its
-    # common path, so it shares the main kernel's MUFU roof
-    for var in variants.values():
+    # common path, so it shares the main kernel's MUFU roof; the FP32-pipe roof
+    # counts the page loop's own FP32 operations of that variant
+    for key, var in variants.items():
         if "main_kernel_gupd" in var:
             var["mufu_roof_frac"] = var["main_kernel_gupd"] / peak
+            if key in fma_peaks:
+                var["fma_roof_frac"] = var["main_kernel_gupd"] / fma_peaks[key]
+    if not args.no_variants and not args.no_large:
+        roofs = {"mufu": peak, "fma": fma_peaks}
+        for name in LARGE_SCENES:
+            variants[name] = large_scene_lines(name, max(3, min(args.steps, 5)), flush, stream,
+                                               dev, roofs)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
@@ -514,6 +591,10 @@ def run_ours(args, scene, rank, world, local, dist):
             "peak_basis": f"{sms} SMs x {clock_mhz:.0f} MHz x {MUFU_PER_SM_CLK} MUFU/clk / "
                           f"{MUFU_PER_UPDATE} MUFU per update",
             "frac_of_page_loop_roof": (achieved / page_peak) if achieved else None,
+            "fma_roof_frac": (achieved / fma_peaks["linear"]) if achieved else None,
+            "fma_peak_basis": f"{sms} SMs x {clock_mhz:.0f} MHz x {FMA_PER_SM_CLK} FP32 lanes/clk / "
+                              "the page loop's FP32 operations per update "
+                              f"({FMA_OPS_PER_UPDATE})",
         },
         "e2e": {"value": aggregate_value(updates, e2e_steps, world, e2e_max), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
@@ -540,7 +621,9 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the windowed-sinc variant measurement")
+                    help="skip the interpolation-variant and large-scene measurements")
+    ap.add_argument("--no-large", action="store_true",
+                    help="skip the large-scene (16384 x 2048^2, 8192 x 4096^2) lines")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

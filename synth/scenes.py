@@ -24,6 +24,8 @@ This module is input generation only: it never backprojects.
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -242,13 +244,28 @@ def make_scene(cfg: SceneConfig, noise: bool = True, seed: int | None = None,
 
     echoes = np.empty((cfg.na, cfg.nr), dtype=np.complex64)
     scale = cfg.noise_sigma / np.sqrt(2.0)
-    for n0 in range(0, cfg.na, NOISE_CHUNK):
-        n1 = min(cfg.na, n0 + NOISE_CHUNK)
-        block = simulate_echoes(pos[n0:n1], txyz, amps, r0, DR, cfg.nr)
-        if noise and cfg.noise_sigma > 0:
-            g = rng.standard_normal((n1 - n0, cfg.nr, 2))
-            block += scale * (g[..., 0] + 1j * g[..., 1])
-        echoes[n0:n1] = block.astype(np.complex64)
+    # the noiseless blocks do not touch the random stream, so they are made on
+    # worker threads while this thread draws the noise in block order
+    chunks = [(n0, min(cfg.na, n0 + NOISE_CHUNK)) for n0 in range(0, cfg.na, NOISE_CHUNK)]
+    workers = max(1, min(len(chunks), (os.cpu_count() or 1), 16))
+    with ThreadPoolExecutor(max_workers=workers) as pool:
+        def submit(i):
+            n0, n1 = chunks[i]
+            return pool.submit(simulate_echoes, pos[n0:n1], txyz, amps, r0, DR, cfg.nr)
+        ahead = 2 * workers                     # blocks in flight (bounds host memory)
+        blocks = [submit(i) for i in range(min(ahead, len(chunks)))]
+        for i, (n0, n1) in enumerate(chunks):
+            if i + ahead < len(chunks):
+                blocks.append(submit(i + ahead))
+            fut = blocks[i]
+            blocks[i] = None
+            g = None
+            if noise and cfg.noise_sigma > 0:
+                g = rng.standard_normal((n1 - n0, cfg.nr, 2))
+            block = fut.result()
+            if g is not None:
+                block += scale * (g[..., 0] + 1j * g[..., 1])
+            echoes[n0:n1] = block.astype(np.complex64)
     return Scene(cfg=cfg, params=params, echoes=echoes, antenna_pos=pos,
                  targets=targets, amps=amps, heights=heights)
 
