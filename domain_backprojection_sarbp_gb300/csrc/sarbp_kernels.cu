@@ -42,8 +42,9 @@
 //    thread and pulse, no per-pixel gather; other threads gather per pixel.
 //
 // 5. Variants of the same kernel (template INTERP): the 8-tap windowed sinc
-//    (a degree-4 or, on narrower spans, degree-3 polynomial per thread and
-//    pulse when the thread's pixels span at most 0.34 bin), the nearest
+//    (one polynomial per thread and pulse, of degree 2 to 4 by the spread of
+//    the thread's pixels up to 0.34 bin, and in a second instantiation for
+//    wide geometries degree 5 or 6 up to 0.8 bin), the nearest
 //    sample (one table entry per thread and pulse when its pixels round to
 //    two bins), and pixels on a height map (a float-pair row reference and a
 //    range series per pixel, with the two-entry form for rows in two bins).
@@ -68,7 +69,7 @@ __host__ __device__ constexpr bool on_heights(int interp)
 }
 // the windowed sinc on the plane: INTERP_SINC8 for geometries where every
 // thread's pixels span at most SINC_SPAN bins, INTERP_SINC8_WIDE (with the
-// two-half polynomial mode, and more registers in use) for the others
+// degree-5 and degree-6 polynomial modes, and more registers in use) for the others
 constexpr int INTERP_SINC8_WIDE = 6;
 __host__ __device__ constexpr bool is_sinc(int interp)
 {
@@ -85,6 +86,9 @@ constexpr float SINC_SPAN = 0.34f;          // widest spread of u (bins) for the
 constexpr float SINC_HALF_MIN = 1.0f / 64;  // narrowest half-width of its interval
 constexpr float SINC_SPAN3 = 0.17f;         // widest spread for the cubic on four nodes
 constexpr float SINC_SPAN2 = 0.05f;         // widest spread for the quadratic on three nodes
+constexpr float SINC_SPAN5 = 0.56f;         // widest spread for degree 5 on six nodes (wide kernel)
+constexpr float SINC_SPAN6 = 0.80f;         // widest spread for degree 6 on seven nodes (wide kernel)
+constexpr int SINC_MAXC = 7;                // coefficients of the highest-degree thread polynomial
 constexpr int HROW4 = TILE_X / 2 + 1;      // float4 per row of a tile's height terms (padded)
 
 struct __align__(16) Record {
@@ -391,11 +395,11 @@ constexpr int NP = TILE_X / 2;
 // What one pulse needs, built one pulse ahead of its use. Nothing here waits
 // on the table loads; their values are consumed by the next pulse step.
 enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXACT = 3, MODE_POLY = 4,
-                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY2H = 7, MODE_POLY4Q = 8,
+                       MODE_PAIR = 5, MODE_POLY3 = 6, MODE_POLY5 = 7, MODE_POLY6 = 8,
                        MODE_POLY2 = 9 };
 
 struct PulseState {
-    float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both halves)
+    float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both lanes)
     float4 t0;                    // hinge: table entry k0 + 1; sinc polynomial: lo_u, hi_u, k0, bin k0;
                                   // nearest pair: table entry (e_kn, e_kn+1)
     float2 t1d;                   // hinge: D part of entry k0; nearest pair: kn, bin kn
@@ -404,27 +408,13 @@ struct PulseState {
     int mode;
 };
 
-// Bounds of u = e0 + e1 i + e2 i^2 over part h of nparts equal runs of a
-// thread's pixels (offsets i from the thread's centre, -15.5 ... 15.5): the
-// run's centre m and half-width r.
-__device__ __forceinline__ void part_bounds(float e0, float e1, float e2, int h, int nparts,
-                                            float& lo, float& hi)
-{
-    const float len = (float)(TILE_X / nparts);
-    const float m = fmaf((float)h + 0.5f, len, -0.5f * TILE_X);
-    const float r = 0.5f * (len - 1.0f);
-    const float um = fmaf(m, fmaf(m, e2, e1), e0);
-    const float sl = fabsf(fmaf(2.0f * e2, m, e1));
-    lo = um - r * sl - r * r * fmaxf(-e2, 0.0f);
-    hi = um + r * sl + r * r * fmaxf(e2, 0.0f);
-}
-
 // The interval of a polynomial: [lo, hi] widened to a half-width of at least
 // SINC_HALF_MIN, its first bin k0 (row units) and k0's absolute bin; true when
-// it spans at most SINC_SPAN bins and the stencils of bins k0 and k0 + 1 lie
-// inside the recorded range.
+// it spans at most `span` bins (less than one: the interval then touches bins
+// k0 and k0 + 1 only) and the stencils of both bins lie inside the recorded range.
 __device__ __forceinline__ bool poly_interval(const BpConst& k, int kb, int bin0, float lo, float hi,
-                                              float& lo_e, float& hi_e, float& k0, int& kabs0)
+                                              float span, float& lo_e, float& hi_e, float& k0,
+                                              int& kabs0)
 {
     const float mid = 0.5f * (lo + hi);
     lo_e = fminf(lo, mid - SINC_HALF_MIN);
@@ -432,7 +422,7 @@ __device__ __forceinline__ bool poly_interval(const BpConst& k, int kb, int bin0
     const float tke = __fadd_rd(lo_e, MAGIC);
     k0 = tke - MAGIC;
     kabs0 = kb + (__float_as_int(tke) - MAGIC_BITS) - bin0;
-    return hi_e - lo_e <= SINC_SPAN && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1;
+    return hi_e - lo_e <= span && kabs0 >= 3 && kabs0 + 5 <= k.nr - 1;
 }
 
 template <int INTERP>
@@ -477,49 +467,31 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     st.mode = kind == REC_FAST ? (hinge ? MODE_HINGE : MODE_GATHER)
                                : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
     if (is_sinc(INTERP) && kind == REC_FAST) {
-        // windowed sinc: when the thread's pixels span at most SINC_SPAN bins and
-        // the stencils of bins k0 and k0 + 1 lie inside the recorded range, the
-        // interpolated echo is a degree-4 polynomial in u; when each half
-        // (quarter) of its pixels does, one polynomial per half (quarter)
+        // windowed sinc: when the thread's pixels span at most SINC_SPAN bins
+        // (SINC_SPAN6 in the wide kernel) and the stencils of bins k0 and k0 + 1
+        // lie inside the recorded range, the interpolated echo is one polynomial
+        // in u, of a degree chosen by the span
+        constexpr float widest = INTERP == INTERP_SINC8_WIDE ? SINC_SPAN6 : SINC_SPAN;
         float lo_e, hi_e, k0e;
         int kabs0;
-        if (poly_interval(k, kb, bin0, lo_u, hi_u, lo_e, hi_e, k0e, kabs0)) {
+        if (poly_interval(k, kb, bin0, lo_u, hi_u, widest, lo_e, hi_e, k0e, kabs0)) {
             const float sp = hi_e - lo_e;
             st.mode = sp <= SINC_SPAN2 ? MODE_POLY2 : (sp <= SINC_SPAN3 ? MODE_POLY3 : MODE_POLY);
+            if (INTERP == INTERP_SINC8_WIDE && sp > SINC_SPAN)
+                st.mode = sp <= SINC_SPAN5 ? MODE_POLY5 : MODE_POLY6;
             st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
             if (INTERP == INTERP_SINC8_WIDE) {
                 // the nodes lie in bins k0 and k0 + 1: start fetching their
-                // coefficient rows into L1 a pulse ahead of their use (1.7 %
-                // faster on the wide scenes, 1.5 % slower on narrow ones)
+                // coefficient rows into L1 a pulse ahead of their use
                 const float4* cb = row + 4 * (kabs0 + bin0);
                 asm volatile("prefetch.global.L1 [%0];" ::"l"(cb));
                 asm volatile("prefetch.global.L1 [%0];" ::"l"(cb + 4));
             }
-        } else if (INTERP == INTERP_SINC8_WIDE) {
-            float lo, hi, lh, hh, kh;
-            int ka;
-            bool ok = true;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                part_bounds(e0, e1, e2, h, 2, lo, hi);
-                ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
-            }
-            if (ok) {
-                st.mode = MODE_POLY2H;
-            } else {
-                ok = true;
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    part_bounds(e0, e1, e2, h, 4, lo, hi);
-                    ok = poly_interval(k, kb, bin0, lo, hi, lh, hh, kh, ka) && ok;
-                }
-                if (ok)
-                    st.mode = MODE_POLY4Q;
-            }
         }
     }
-    if (st.mode != MODE_POLY && st.mode != MODE_POLY3 && st.mode != MODE_POLY2)
-        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);   // the part modes recompute their intervals
+    if (st.mode != MODE_POLY && st.mode != MODE_POLY3 && st.mode != MODE_POLY2 &&
+        st.mode != MODE_POLY5 && st.mode != MODE_POLY6)
+        st.t0 = make_float4(0.f, 0.f, 0.f, 0.f);
     st.t1d = make_float2(0.f, 0.f);
     float kn = 0.0f;
     if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
@@ -754,14 +726,71 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
     return bin_poly(row + 4 * kr, s);
 }
 
+// Complex a x + b y, with real weights a, b.
+__device__ __forceinline__ float2 cmix(float a, float2 x, float b, float2 y)
+{
+    return make_float2(fmaf(a, x.x, b * y.x), fmaf(a, x.y, b * y.y));
+}
+__device__ __forceinline__ float2 cmix3(float a, float2 x, float b, float2 y, float c, float2 z)
+{
+    return make_float2(fmaf(a, x.x, fmaf(b, y.x, c * z.x)), fmaf(a, x.y, fmaf(b, y.y, c * z.y)));
+}
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+
 // Monomial coefficients p[n] (complex, in t = (u - mid) / half) of the
-// interpolant of G on [mid - half, mid + half] at NN Chebyshev nodes
-// (NN = 5: degree 4; NN = 4: degree 3; NN = 3: degree 2), by the inverse
-// Vandermonde matrix.
+// interpolant of G on [mid - half, mid + half] at the NN Chebyshev nodes
+// mid + half cos((2i + 1) pi / (2 NN)) (degree NN - 1, NN = 3 .. 7), by the
+// inverse Vandermonde matrix. The nodes are symmetric about mid, so the even
+// coefficients come from the sums g_i + g_(NN-1-i) and the odd ones from the
+// differences; for NN = 6 and 7 the weights are the inverses of those
+// halves' Vandermonde matrices, in float64 and rounded once.
 template <int NN>
 __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const float4* row,
-                                            float2 (&p)[5])
+                                            float2 (&p)[SINC_MAXC])
 {
+    if (NN == 6) {
+        constexpr float C1 = 0.965925826f, C2 = 0.707106781f, C3 = 0.258819045f;
+        const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
+        const float2 g5 = sinc_value(fmaf(half, -C1, mid), kb, row);
+        const float2 g1 = sinc_value(fmaf(half, C2, mid), kb, row);
+        const float2 g4 = sinc_value(fmaf(half, -C2, mid), kb, row);
+        const float2 g2 = sinc_value(fmaf(half, C3, mid), kb, row);
+        const float2 g3 = sinc_value(fmaf(half, -C3, mid), kb, row);
+        const float2 s0 = cadd(g0, g5), s1 = cadd(g1, g4), s2 = cadd(g2, g3);
+        const float2 d0 = csub(g0, g5), d1 = csub(g1, g4), d2 = csub(g2, g3);
+        p[0] = cmix3(0.0446581987f, s0, -0.166666667f, s1, 0.622008468f, s2);
+        p[2] = cmix3(-0.755983064f, s0, 2.66666667f, s1, -1.91068360f, s2);
+        p[4] = cmix3(1.33333333f, s0, -2.66666667f, s1, 1.33333333f, s2);
+        p[1] = cmix3(0.0462335694f, d0, -0.235702260f, d1, 2.40325617f, d2);
+        p[3] = cmix3(-0.782651259f, d0, 3.77123617f, d1, -7.38231455f, d2);
+        p[5] = cmix3(1.38036824f, d0, -3.77123617f, d1, 5.15160441f, d2);
+        p[6] = make_float2(0.0f, 0.0f);
+        return;
+    }
+    if (NN == 7) {
+        constexpr float C1 = 0.974927912f, C2 = 0.781831482f, C3 = 0.433883739f;
+        const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
+        const float2 g6 = sinc_value(fmaf(half, -C1, mid), kb, row);
+        const float2 g1 = sinc_value(fmaf(half, C2, mid), kb, row);
+        const float2 g5 = sinc_value(fmaf(half, -C2, mid), kb, row);
+        const float2 g2 = sinc_value(fmaf(half, C3, mid), kb, row);
+        const float2 g4 = sinc_value(fmaf(half, -C3, mid), kb, row);
+        const float2 g3 = sinc_value(mid, kb, row);
+        // even part: (s_i / 2 - g3) against [t^2 t^4 t^6]; odd: d_i / 2 against [t t^3 t^5]
+        const float2 s0 = make_float2(fmaf(0.5f, g0.x + g6.x, -g3.x), fmaf(0.5f, g0.y + g6.y, -g3.y));
+        const float2 s1 = make_float2(fmaf(0.5f, g1.x + g5.x, -g3.x), fmaf(0.5f, g1.y + g5.y, -g3.y));
+        const float2 s2 = make_float2(fmaf(0.5f, g2.x + g4.x, -g3.x), fmaf(0.5f, g2.y + g4.y, -g3.y));
+        const float2 d0 = csub(g0, g6), d1 = csub(g1, g5), d2 = csub(g2, g4);
+        p[0] = g3;
+        p[2] = cmix3(0.468226361f, s0, -2.04001350f, s1, 9.57178714f, s2);
+        p[4] = cmix3(-3.25319224f, s0, 12.9827197f, s1, -25.7295275f, s2);
+        p[6] = cmix3(4.06895422f, s0, -11.4009564f, s1, 16.4748593f, s2);
+        p[1] = cmix3(0.228243474f, d0, -0.797473389f, d1, 2.07652140f, d2);
+        p[3] = cmix3(-1.58581396f, d0, 5.07514951f, d1, -5.58181180f, d2);
+        p[5] = cmix3(1.98346852f, d0, -4.45681331f, d1, 3.57408678f, d2);
+        return;
+    }
     if (NN == 3) {
         constexpr float C1 = 0.866025404f;                       // cos(pi/6)
         const float2 g0 = sinc_value(fmaf(half, C1, mid), kb, row);
@@ -771,7 +800,7 @@ __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const
         p[1] = make_float2(0.577350269f * (g0.x - g2.x), 0.577350269f * (g0.y - g2.y));
         p[2] = make_float2(0.666666667f * (g0.x + g2.x - 2.0f * g1.x),
                            0.666666667f * (g0.y + g2.y - 2.0f * g1.y));
-        p[3] = p[4] = make_float2(0.0f, 0.0f);
+        p[3] = p[4] = p[5] = p[6] = make_float2(0.0f, 0.0f);
         return;
     }
     if (NN == 4) {
@@ -789,7 +818,7 @@ __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const
         p[2] = make_float2(0.707106781f * (s03.x - s12.x), 0.707106781f * (s03.y - s12.y));
         p[3] = make_float2(fmaf(0.765366865f, d03.x, -1.847759065f * d12.x),
                            fmaf(0.765366865f, d03.y, -1.847759065f * d12.y));
-        p[4] = make_float2(0.0f, 0.0f);
+        p[4] = p[5] = p[6] = make_float2(0.0f, 0.0f);
         return;
     }
     constexpr float C1 = 0.951056516f, C2 = 0.587785252f;   // cos(pi/10), cos(3 pi/10)
@@ -809,14 +838,15 @@ __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const
                        fmaf(0.940456404f, d04.y, -1.521690426f * d13.y));
     p[4] = make_float2(fmaf(0.988854382f, s04.x, fmaf(-2.588854382f, s13.x, 3.2f * g2.x)),
                        fmaf(0.988854382f, s04.y, fmaf(-2.588854382f, s13.y, 3.2f * g2.y)));
+    p[5] = p[6] = make_float2(0.0f, 0.0f);
 }
 
 // The coefficients in s = u - mid with psi_k0 folded in, p[n] psi_k0 / half^n,
 // written into lane LANE (0: .x, 1: .y, 2: both) of the pairs pr (real parts)
 // and pi (imaginary parts).
 template <int ND, int LANE>
-__device__ __forceinline__ void poly_fold(const float2 (&p)[5], float2 ps, float half,
-                                          float2 (&pr)[5], float2 (&pi)[5])
+__device__ __forceinline__ void poly_fold(const float2 (&p)[SINC_MAXC], float2 ps, float half,
+                                          float2 (&pr)[SINC_MAXC], float2 (&pi)[SINC_MAXC])
 {
     const float ih = rcp_approx(half);            // half >= SINC_HALF_MIN
     float sc = 1.0f;
@@ -844,7 +874,8 @@ __device__ __forceinline__ void poly_fold(const float2 (&p)[5], float2 ps, float
 // and cm = c (mid - k0)).
 template <int ND, int Q0 = 0, int NQ = NP>
 __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
-                                                const float2 (&pr)[5], const float2 (&pi)[5],
+                                                const float2 (&pr)[SINC_MAXC],
+                                                const float2 (&pi)[SINC_MAXC],
                                                 float midL, float midR, float cmL, float cmR,
                                                 float2 (&accre)[NP], float2 (&accim)[NP])
 {
@@ -906,7 +937,7 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
     const float lo_u = st.t0.x, hi_u = st.t0.y, k0 = st.t0.z;
     const int kabs0 = __float_as_int(st.t0.w);
     const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
-    float2 p[5], pr[5], pi[5];
+    float2 p[SINC_MAXC], pr[SINC_MAXC], pi[SINC_MAXC];
     poly_coeffs<NN>(mid, half, st.kb, row, p);
     poly_fold<NN, 2>(p, __ldg(psi + kabs0), half, pr, pi);
     const float cm = k.c_phase * (mid - k0);
@@ -928,76 +959,6 @@ __device__ __forceinline__ void sinc_pulse(const BpConst& k, const PulseState& s
         sinc_pixel<false>(k, ub, st.kb, st.bin0, row, psi, re, im);
     }
 }
-
-// Spans up to about twice (four times) SINC_SPAN, INTERP_SINC8_WIDE only: each
-// half (quarter) of the thread's pixels gets its own degree-4 interpolant over
-// its own interval (the same error bound), at no extra cost per pixel. Pixel m
-// sits in lane .x of pair m (m < 16) or lane .y of pair m - 16, so the halves
-// are the two lanes of all 16 pairs, and the quarters are lanes .x / .y of pairs
-// 0-7 (quarters 0 and 2), then of pairs 8-15 (quarters 1 and 3). The parts'
-// intervals were checked by pulse_setup.
-__device__ __forceinline__ void load_part_pair(const float4* stash, int a, int b,
-                                               float2 (&pr)[5], float2 (&pi)[5], float& mid_a,
-                                               float& cm_a, float& mid_b, float& cm_b)
-{
-    const float4* sa = stash + 3 * a * THREADS;
-    const float4* sb = stash + 3 * b * THREADS;
-    const float4 l0 = sa[0], l1 = sa[THREADS], l2 = sa[2 * THREADS];
-    const float4 r0 = sb[0], r1 = sb[THREADS], r2 = sb[2 * THREADS];
-    pr[0] = make_float2(l0.x, r0.x);
-    pi[0] = make_float2(l0.y, r0.y);
-    pr[1] = make_float2(l0.z, r0.z);
-    pi[1] = make_float2(l0.w, r0.w);
-    pr[2] = make_float2(l1.x, r1.x);
-    pi[2] = make_float2(l1.y, r1.y);
-    pr[3] = make_float2(l1.z, r1.z);
-    pi[3] = make_float2(l1.w, r1.w);
-    pr[4] = make_float2(l2.x, r2.x);
-    pi[4] = make_float2(l2.y, r2.y);
-    mid_a = l2.z;
-    cm_a = l2.w;
-    mid_b = r2.z;
-    cm_b = r2.w;
-}
-
-__device__ __forceinline__ void sinc_poly_parts_pulse(const BpConst& k, const PulseState& st,
-                                                      const float4* row,
-                                                      const float2* __restrict__ psi,
-                                                      float4* stash, int nparts,
-                                                      float2 (&accre)[NP], float2 (&accim)[NP])
-{
-    const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
-    // one part per pass (one copy of the node code); each part's coefficients,
-    // centre and phase offset go to this thread's own shared-memory slots
-    // (stride THREADS)
-#pragma unroll 1
-    for (int h = 0; h < nparts; ++h) {
-        float lo, hi, lo_e, hi_e, k0;
-        int ka;
-        part_bounds(e0, e1, e2, h, nparts, lo, hi);
-        poly_interval(k, st.kb, st.bin0, lo, hi, lo_e, hi_e, k0, ka);
-        const float mid = 0.5f * (lo_e + hi_e), half = 0.5f * (hi_e - lo_e);
-        float2 p[5], cr[5], ci[5];
-        poly_coeffs<5>(mid, half, st.kb, row, p);
-        poly_fold<5, 0>(p, __ldg(psi + ka), half, cr, ci);
-        float4* slot = stash + 3 * h * THREADS;
-        slot[0] = make_float4(cr[0].x, ci[0].x, cr[1].x, ci[1].x);
-        slot[THREADS] = make_float4(cr[2].x, ci[2].x, cr[3].x, ci[3].x);
-        slot[2 * THREADS] = make_float4(cr[4].x, ci[4].x, mid, k.c_phase * (mid - k0));
-    }
-    float2 pr[5], pi[5];
-    float midL, cmL, midR, cmR;
-    if (nparts == 2) {
-        load_part_pair(stash, 0, 1, pr, pi, midL, cmL, midR, cmR);
-        sinc_poly_apply<5>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
-    } else {
-        load_part_pair(stash, 0, 2, pr, pi, midL, cmL, midR, cmR);
-        sinc_poly_apply<5, 0, NP / 2>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
-        load_part_pair(stash, 1, 3, pr, pi, midL, cmL, midR, cmR);
-        sinc_poly_apply<5, NP / 2, NP / 2>(k, st, pr, pi, midL, midR, cmL, cmR, accre, accim);
-    }
-}
-
 
 __device__ __forceinline__ void sinc_exact_pulse(const BpConst& k, const Record& rec, const float4* row,
                                                  const double* __restrict__ a, double xc,
@@ -1466,7 +1427,7 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
                                             const float4* row, const double* a, double xc,
-                                            double yrow, const HRow& hr, const float4* s_hp, float4* stash,
+                                            double yrow, const HRow& hr, const float4* s_hp,
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
@@ -1492,9 +1453,10 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
             sinc_poly_pulse<4>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_POLY)
             sinc_poly_pulse<5>(k, st, row, psi, accre, accim);
-        else if (INTERP == INTERP_SINC8_WIDE && (st.mode == MODE_POLY2H || st.mode == MODE_POLY4Q))
-            sinc_poly_parts_pulse(k, st, row, psi, stash, st.mode == MODE_POLY4Q ? 4 : 2, accre,
-                                  accim);
+        else if (INTERP == INTERP_SINC8_WIDE && st.mode == MODE_POLY5)
+            sinc_poly_pulse<6>(k, st, row, psi, accre, accim);
+        else if (INTERP == INTERP_SINC8_WIDE && st.mode == MODE_POLY6)
+            sinc_poly_pulse<7>(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
@@ -1534,7 +1496,6 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
     __shared__ Record s_rec[CHUNK];
     // heights mode: per row, HROW4 float4 (dz[q], dz[q + 16], P[q], P[q + 16]) with
     // dz = h - hrow and P = (i dx)^2 + dz^2 for the pixels at offsets i of q and q + 16
-    // wide sinc: six float4 per thread hold the two halves' coefficients
     extern __shared__ float4 s_hp[];
     const int tid = threadIdx.x;
     const int jr = tid;                                   // warp w, lane l -> row 32 w + l
@@ -1618,14 +1579,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * tw, jf);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * tw,
                                   pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
-                                  s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
+                                  s_hp + jr * HROW4, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * tw, jf);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * tw,
                                   pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
-                                  s_hp + jr * HROW4, s_hp + tid, psi, accre, accim);
+                                  s_hp + jr * HROW4, psi, accre, accim);
             }
         }
 
@@ -1814,15 +1775,10 @@ cudaError_t launch_psi(const BpConst& k, float2* psi, cudaStream_t s)
 }
 
 constexpr size_t HEIGHTS_SMEM = (size_t)TILE_Y * HROW4 * sizeof(float4);
-// wide sinc: three float4 per part (at most four parts) per thread
-constexpr size_t SINC_SMEM = (size_t)12 * THREADS * sizeof(float4);
 
 cudaError_t prepare_kernels()
 {
-    cudaError_t e = cudaFuncSetAttribute(bp_kernel<INTERP_SINC8_WIDE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SINC_SMEM);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>,
+    cudaError_t e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)HEIGHTS_SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bp_kernel<INTERP_HEIGHTS_SINC8>,
@@ -1851,7 +1807,7 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
     {
         bp_kernel<INTERP_SINC8><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image, partial, psi,
                                                            nullptr, sinc_wide);
-        bp_kernel<INTERP_SINC8_WIDE><<<k.ctas, THREADS, SINC_SMEM, s>>>(k, pos, table, klo, image,
+        bp_kernel<INTERP_SINC8_WIDE><<<k.ctas, THREADS, 0, s>>>(k, pos, table, klo, image,
                                                                         partial, psi, nullptr,
                                                                         sinc_wide);
     }
@@ -1867,7 +1823,7 @@ cudaError_t launch_backproject(const BpConst& k, const double* pos, const float4
 // ---------------------------------------------------------------------------
 // Cost-weighted work split for the windowed-sinc kernels on a plane. What a
 // (tile, pulse) unit costs depends on how far a thread's 32 pixels spread in
-// range (cubic or quartic polynomial, halves, quarters or per-pixel taps), and
+// range (a polynomial of degree 2 to 6, or per-pixel taps), and
 // that spread grows with the tile's x distance from the antenna, so equal unit
 // counts leave the CTAs holding the image's far edges working after the others
 // have finished. split_kernel estimates each tile's cost from SPLIT_SAMPLES
@@ -1888,10 +1844,10 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
         return 100;
     if (span <= SINC_SPAN)
         return 113;
-    if (wide && span <= 2.0f * SINC_SPAN)
-        return 160;
-    if (wide && span <= 4.0f * SINC_SPAN)
-        return 220;
+    if (wide && span <= SINC_SPAN5)
+        return 125;
+    if (wide && span <= SINC_SPAN6)
+        return 138;
     return 330;
 }
 
@@ -2014,7 +1970,7 @@ cudaError_t backproject_occupancy(int* ctas_per_sm)
     if (e == cudaSuccess) {
         int w = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w, bp_kernel<INTERP_SINC8_WIDE>, THREADS,
-                                                          SINC_SMEM);
+                                                          0);
         b = std::min(b, w);
     }
     if (e == cudaSuccess)

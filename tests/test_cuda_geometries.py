@@ -163,8 +163,8 @@ def test_nearest(name):
 @pytest.mark.parametrize("name", ["squint_25deg", "low_pass"])
 def test_sinc8_wide_geometry_at_range_axis_edges(name):
     """A geometry where a thread's 32 pixels span more than 0.34 bin, the
-    widest single sinc polynomial (so the kernel with half and quarter
-    polynomials runs), with the recorded range
+    widest polynomial of the narrow sinc kernel (so the wide kernel, with its
+    degree-5 and degree-6 polynomials and per-pixel taps, runs), with the recorded range
     axis cut so that it starts and ends inside the image: stencils that reach
     past either end contribute nothing, per pixel and per part."""
     pos, fc, dr, spacing, centre = CASES[name]

@@ -70,8 +70,8 @@ def test_sinc_page_scene_full_size():
 def test_sinc_wide_scenes_sampled(index):
     """The 2048^2 and 4096^2 scenes: a thread's 32 pixels span up to about a
     range bin per pulse at the image's far x edges, so these run the
-    wide-geometry sinc kernel (one polynomial per 16-pixel half or per 8-pixel
-    quarter of a thread's pixels, whichever is narrow enough)."""
+    wide-geometry sinc kernel (one polynomial of degree 5 or 6 per thread and
+    pulse where its pixels span more than 0.34 bin)."""
     sc = scenes.make_scene(scenes.CONFIGS[index - 1])
     print(_check(sc, sinc_image(sc.params, sc.echoes, sc.antenna_pos)))
 

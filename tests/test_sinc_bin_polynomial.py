@@ -66,6 +66,18 @@ def test_thread_polynomial_bounds_at_the_kernel_spans():
     assert 8 * np.pi ** 5 * 0.17 ** 5 / (2 ** 4 * 120) > 4e-5
 
 
+def test_wide_kernel_polynomial_bounds():
+    """The wide-geometry kernel's higher degrees: degree 5 on six nodes up to
+    0.56 bin and degree 6 on seven nodes up to 0.80 bin. The window's
+    derivative sums (1007 for n = 6, 3199 for n = 7) keep the Chebyshev bounds
+    within one bin under 2.2e-5, the budget of the lower degrees."""
+    s6, s7 = _tap_derivative_sum(6), _tap_derivative_sum(7)
+    assert 990 < s6 < 1025 and 3140 < s7 < 3260, (s6, s7)
+    quintic = s6 * 0.28 ** 6 / (2 ** 5 * 720)
+    sextic = s7 * 0.40 ** 7 / (2 ** 6 * 5040)
+    assert quintic < 2.2e-5 and sextic < 1.7e-5, (quintic, sextic)
+
+
 def _window_g(u, e):
     k = np.floor(u).astype(int)
     out = np.zeros(u.shape, complex)
@@ -78,10 +90,11 @@ def _window_g(u, e):
 def test_thread_polynomial_across_a_bin_boundary():
     """Where the interval crosses a bin boundary G is only C^2 (a tap enters
     the stencil, another leaves), so the derivative bound does not apply;
-    measured on random samples (|e| <= 1) the interpolants stay under 4e-5."""
+    measured on random samples (|e| <= 1) the interpolants of every degree the
+    kernels use, at their widest spans, stay under 4e-5."""
     rng = np.random.default_rng(7)
     worst = {}
-    for nn, span in ((4, 0.17), (5, 0.34)):
+    for nn, span in ((4, 0.17), (5, 0.34), (6, 0.56), (7, 0.80)):
         i = np.arange(nn)
         x = np.cos((2 * i + 1) * np.pi / (2 * nn))
         w = 0.0
@@ -99,7 +112,7 @@ def test_thread_polynomial_across_a_bin_boundary():
                  + 1j * np.polynomial.polynomial.polyval(tt, ci))
             w = max(w, np.abs(p - _window_g(uu, e)).max())
         worst[nn] = w
-    assert worst[4] < 4e-5 and worst[5] < 4e-5, worst
+    assert all(w < 4e-5 for w in worst.values()), worst
 
 
 def test_library_tap_polynomials():
