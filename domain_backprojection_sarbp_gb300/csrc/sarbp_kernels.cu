@@ -480,13 +480,6 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
             if (INTERP == INTERP_SINC8_WIDE && sp > SINC_SPAN)
                 st.mode = sp <= SINC_SPAN5 ? MODE_POLY5 : MODE_POLY6;
             st.t0 = make_float4(lo_e, hi_e, k0e, __int_as_float(kabs0));
-            if (INTERP == INTERP_SINC8_WIDE) {
-                // the nodes lie in bins k0 and k0 + 1: start fetching their
-                // coefficient rows into L1 a pulse ahead of their use
-                const float4* cb = row + 4 * (kabs0 + bin0);
-                asm volatile("prefetch.global.L1 [%0];" ::"l"(cb));
-                asm volatile("prefetch.global.L1 [%0];" ::"l"(cb + 4));
-            }
         }
     }
     if (st.mode != MODE_POLY && st.mode != MODE_POLY3 && st.mode != MODE_POLY2 &&
@@ -841,37 +834,36 @@ __device__ __forceinline__ void poly_coeffs(float mid, float half, int kb, const
     p[5] = p[6] = make_float2(0.0f, 0.0f);
 }
 
-// The coefficients in s = u - mid with psi_k0 folded in, p[n] psi_k0 / half^n,
-// written into lane LANE (0: .x, 1: .y, 2: both) of the pairs pr (real parts)
-// and pi (imaginary parts).
-template <int ND, int LANE>
-__device__ __forceinline__ void poly_fold(const float2 (&p)[SINC_MAXC], float2 ps, float half,
-                                          float2 (&pr)[SINC_MAXC], float2 (&pi)[SINC_MAXC])
+// frac(2 r_k / lambda) of absolute bin k, in turns: the phase of psi_k from the
+// same 64-bit fixed-point accumulator the table kernel uses.
+__device__ __forceinline__ float bin_turns(const BpConst& k, int kabs)
+{
+    const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)(long long)kabs;
+    return (float)(ph >> 40) * 0x1p-24f;
+}
+
+// The coefficients in s = u - mid, p[n] / half^n, in both lanes of the pairs pr
+// (real parts) and pi (imaginary parts).
+template <int ND>
+__device__ __forceinline__ void poly_scale(const float2 (&p)[SINC_MAXC], float half,
+                                           float2 (&pr)[SINC_MAXC], float2 (&pi)[SINC_MAXC])
 {
     const float ih = rcp_approx(half);            // half >= SINC_HALF_MIN
     float sc = 1.0f;
 #pragma unroll
     for (int n = 0; n < ND; ++n) {
-        const float psr = ps.x * sc, psi_ = ps.y * sc;
-        const float re = p[n].x * psr - p[n].y * psi_;
-        const float im = p[n].x * psi_ + p[n].y * psr;
-        if (LANE != 1) {
-            pr[n].x = re;
-            pi[n].x = im;
-        }
-        if (LANE != 0) {
-            pr[n].y = re;
-            pi[n].y = im;
-        }
+        const float re = p[n].x * sc, im = p[n].y * sc;
+        pr[n] = make_float2(re, re);
+        pi[n] = make_float2(im, im);
         sc *= ih;
     }
 }
 
 // The per-pixel part of the polynomial modes: lane .x of every pixel pair
 // (the left 16 pixels) evaluates the .x coefficients about midL, lane .y (the
-// right 16) the .y coefficients about midR, each with the echo
-// phase psi_k0 exp(j c (u - k0)) of its own k0 (folded into the coefficients
-// and cm = c (mid - k0)).
+// right 16) the .y coefficients about midR, each with the echo phase
+// psi_k0 exp(j c (u - k0)) = exp(j (c (u - mid) + cm)) of its own k0, with
+// cm = c (mid - k0) + arg psi_k0.
 template <int ND, int Q0 = 0, int NQ = NP>
 __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseState& st,
                                                 const float2 (&pr)[SINC_MAXC],
@@ -928,7 +920,7 @@ __device__ __forceinline__ void sinc_poly_apply(const BpConst& k, const PulseSta
 // Intervals across a bin boundary, where the bound does not apply, measure no
 // worse on random samples (at most 3.3e-5 max|e| at these spans). The echo
 // phase exp(j 4 pi R / lambda) = psi_k0 exp(j c (u - k0)) is applied per
-// pixel; psi_k0 is folded into the coefficients.
+// pixel as one angle, c (u - k0) + 2 pi frac(2 r_k0 / lambda).
 template <int NN>
 __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseState& st,
                                                 const float4* row, const float2* __restrict__ psi,
@@ -939,8 +931,9 @@ __device__ __forceinline__ void sinc_poly_pulse(const BpConst& k, const PulseSta
     const float mid = 0.5f * (lo_u + hi_u), half = 0.5f * (hi_u - lo_u);
     float2 p[SINC_MAXC], pr[SINC_MAXC], pi[SINC_MAXC];
     poly_coeffs<NN>(mid, half, st.kb, row, p);
-    poly_fold<NN, 2>(p, __ldg(psi + kabs0), half, pr, pi);
-    const float cm = k.c_phase * (mid - k0);
+    poly_scale<NN>(p, half, pr, pi);
+    constexpr float TWO_PI = 6.283185307f;
+    const float cm = fmaf(TWO_PI, bin_turns(k, kabs0), k.c_phase * (mid - k0));
     sinc_poly_apply<NN>(k, st, pr, pi, mid, mid, cm, cm, accre, accim);
 }
 
@@ -1569,6 +1562,19 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             __syncthreads();
             const int tw = row_pitch<INTERP>(k);
             const float4* rows = table + (size_t)c0 * tw;
+            if (is_sinc(INTERP)) {
+                // the sinc modes load their table entries inside the pulse step
+                // (the polynomial's nodes), so nothing is gained by building the
+                // next pulse's state early, and one state leaves registers free
+#pragma unroll 1
+                for (int p = 0; p < cnt; ++p) {
+                    const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rows + (size_t)p * tw, jf);
+                    apply_pulse<INTERP>(k, st, s_rec[p], rows + (size_t)p * tw,
+                                        pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
+                                        s_hp + jr * HROW4, psi, accre, accim);
+                }
+                continue;
+            }
             // Two pulse states in ping-pong: the state of pulse p + 1 is built
             // while pulse p is applied, with no copy between them.
             PulseState sa = pulse_setup<INTERP>(k, s_rec[0], rows, jf);
