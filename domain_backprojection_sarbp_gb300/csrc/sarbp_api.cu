@@ -359,7 +359,7 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
                      sinc_wide, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "table kernel launch");
-    if (k.flags & (SARBP_SINC8 | SARBP_NEAREST)) {
+    if (k.flags & SARBP_SINC8) {
         e = launch_psi(k, plan->psi, s);
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "phasor kernel launch");
@@ -628,14 +628,14 @@ sarbp_status sarbp_plan_describe(sarbp_plan_t plan, sarbp_plan_info* out)
     out->full_window = plan->full_window;
     out->kernels_per_call = 0;
     if (plan->tiles > 0 && plan->p.na > 0 && plan->p.nr >= 2)
-        // table + main (+ reduce); the phasor kernel for sinc and nearest; sinc on a
+        // table + main (+ reduce); the phasor kernel for sinc; sinc on a
         // plane also enqueues the work split, its wide-geometry kernel (one of the two
         // exits at once) and always the reduce
         out->kernels_per_call =
             ((plan->p.flags & SARBP_SINC8) && !plan->heights_mode)
                 ? 6
                 : (any_split_tile(make_const(plan, &plan->p)) ? 3 : 2) +
-                      ((plan->p.flags & (SARBP_SINC8 | SARBP_NEAREST)) ? 1 : 0);
+                      ((plan->p.flags & SARBP_SINC8) ? 1 : 0);
     else if (plan->tiles > 0)
         out->kernels_per_call = 0;   // a memset at most
     out->scratch_bytes = plan->scratch_bytes;

@@ -153,13 +153,17 @@ SincTaps fit_sinc_taps()
 // Echo table: one block per pulse.
 // ---------------------------------------------------------------------------
 // Linear interpolation (TABLE_LINEAR): entries (A_k, D_k / c) as above.
-// Nearest neighbour (TABLE_PAIRS): plain sample pairs (e_k, e_{k+1}), zero
-// where a sample lies outside 0 .. nr - 1. Windowed sinc (TABLE_SINC): four
+// Nearest neighbour (TABLE_PAIRS): entries (N_k, M_k) with N_k = e_k psi_k h
+// and M_k = (e_{k+1} - e_k) psi_k h, h = exp(j c / 2), a sample taken as zero
+// where it lies outside 0 .. nr - 1: a pixel whose nearest sample is k has
+// the compensated echo N_k exp(j c (u - k - 1/2)), and the two samples of
+// bins k and k + 1 seen from the boundary between them are N_k and N_k + M_k
+// (psi_k+1 = psi_k exp(j c)). Windowed sinc (TABLE_SINC): four
 // entries per bin k, the complex coefficients P_0 .. P_7 of the interpolant on
 // that bin, G(k + 1/2 + s) = sum_n P_n s^n for s in [-1/2, 1/2], with
 // P_n = sum_d taps.c[d + 3][n] e_{k+d}; zero unless the whole stencil
 // k - 3 .. k + 4 lies in 0 .. nr - 1. The phase of the last two kinds comes
-// from psi_k (psi_kernel). Rows are k.tw float4 apart.
+// of the sinc kind comes from psi_k (psi_kernel). Rows are k.tw float4 apart.
 enum TableKind : int { TABLE_LINEAR = 0, TABLE_PAIRS = 1, TABLE_SINC = 2 };
 
 template <int KIND>
@@ -234,16 +238,23 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
             continue;
         }
         if (KIND == TABLE_PAIRS) {
-            if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 1) {
-                const float2 e0 = erow[kk];
-                v.x = e0.x;
-                v.y = e0.y;
-            }
-            if (lo != KLO_INVALID && kk + 1 >= 0 && kk + 1 <= (long long)k.nr - 1) {
-                const float2 e1 = erow[kk + 1];
-                v.z = e1.x;
-                v.w = e1.y;
-            }
+            float2 e0 = make_float2(0.f, 0.f), e1 = make_float2(0.f, 0.f);
+            if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 1)
+                e0 = erow[kk];
+            if (lo != KLO_INVALID && kk + 1 >= 0 && kk + 1 <= (long long)k.nr - 1)
+                e1 = erow[kk + 1];
+            // psi_k h = exp(j 2 pi (frac(2 r_k / lambda) + c / (4 pi)))
+            const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
+            const float turns = (float)(ph >> 40) * 0x1p-24f;
+            float sn, cs;
+            sincospif(2.0f * turns, &sn, &cs);
+            const float c = cs * k.hrot_re - sn * k.hrot_im;
+            const float s = cs * k.hrot_im + sn * k.hrot_re;
+            const float dre = e1.x - e0.x, dim = e1.y - e0.y;
+            v.x = e0.x * c - e0.y * s;
+            v.y = e0.x * s + e0.y * c;
+            v.z = dre * c - dim * s;
+            v.w = dre * s + dim * c;
         } else if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 2) {
             const float2 e0 = erow[kk];
             const float2 e1 = erow[kk + 1];
@@ -401,8 +412,8 @@ enum PulseMode : int { MODE_SKIP = 0, MODE_HINGE = 1, MODE_GATHER = 2, MODE_EXAC
 struct PulseState {
     float2 q0, q1, q2;            // hinge: c (e0 - k0 - 1), c e1, c e2; otherwise e0, e1, e2 (both lanes)
     float4 t0;                    // hinge: table entry k0 + 1; sinc polynomial: lo_u, hi_u, k0, bin k0;
-                                  // nearest pair: table entry (e_kn, e_kn+1)
-    float2 t1d;                   // hinge: D part of entry k0; nearest pair: kn, bin kn
+                                  // nearest pair: table entry (N_kn, M_kn)
+    float2 t1d;                   // hinge: D part of entry k0
     int kb;                       // row index the polynomial u is relative to
     int bin0;                     // row index of absolute bin 0
     int mode;
@@ -489,15 +500,14 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
     float kn = 0.0f;
     if (INTERP == INTERP_NEAREST && kind == REC_FAST) {
         // nearest sample: when every pixel rounds to bin kn or kn + 1, one table
-        // entry (e_kn, e_kn+1) serves the thread; psi_kn must exist
+        // entry (N_kn, M_kn) serves the thread (the fast path's pixels lie
+        // inside the row, so entry kn does too)
         const float tkn = __fadd_rd(lo_u + 0.5f, MAGIC);
         kn = tkn - MAGIC;
         const int idxn = kb + (__float_as_int(tkn) - MAGIC_BITS);
-        const int kabsn = idxn - bin0;
-        if (hi_u + 0.5f - kn < 2.0f && kabsn >= 0 && kabsn <= k.nr - 1) {
+        if (hi_u + 0.5f - kn < 2.0f) {
             st.mode = MODE_PAIR;
             st.t0 = __ldg(row + idxn);
-            st.t1d = make_float2(kn, __int_as_float(kabsn));
         }
     }
     if (hinge) {
@@ -988,51 +998,40 @@ __device__ __forceinline__ void sinc_exact_pulse(const BpConst& k, const Record&
 // psi(u) = psi_k exp(j c (u - k)), u - k in [-1/2, 1/2).
 // ---------------------------------------------------------------------------
 template <bool CHECK_ROW>
-__device__ __forceinline__ void nearest_pixel(const BpConst& k, float ub, int kb, int bin0,
-                                              const float4* row, const float2* __restrict__ psi,
-                                              float& re, float& im)
+__device__ __forceinline__ void nearest_pixel(const BpConst& k, float ub, int kb,
+                                              const float4* row, float& re, float& im)
 {
     if (CHECK_ROW && !(ub > -1.0e6f && ub < 1.0e6f))
         return;
     const float tt = __fadd_rd(ub + 0.5f, MAGIC);
     const float d = ub - (tt - MAGIC);                  // u - k in [-1/2, 1/2)
     const int kr = kb + (__float_as_int(tt) - MAGIC_BITS);
-    const int kabs = kr - bin0;
-    if (kabs < 0 || kabs > k.nr - 1)
-        return;                                         // nearest sample not recorded
     if (CHECK_ROW && (kr < 0 || kr > k.W - 1))
         return;
+    // N_k: zero where sample k was not recorded
     const float2 e = __ldg(reinterpret_cast<const float2*>(row) + 2 * (size_t)kr);
-    const float2 ps = __ldg(psi + kabs);
     float sn, cs;
-    __sincosf(d * k.c_phase, &sn, &cs);
-    const float zr = ps.x * cs - ps.y * sn;
-    const float zi = ps.x * sn + ps.y * cs;
-    re = fmaf(e.x, zr, fmaf(-e.y, zi, re));
-    im = fmaf(e.x, zi, fmaf(e.y, zr, im));
+    __sincosf(fmaf(d, k.c_phase, -0.5f * k.c_phase), &sn, &cs);
+    re = fmaf(e.x, cs, fmaf(-e.y, sn, re));
+    im = fmaf(e.x, sn, fmaf(e.y, cs, im));
 }
 
-// Every pixel rounds to bin kn or kn + 1: the two samples come from one
-// table entry, pre-multiplied by psi_kn, since the echo phase
-// psi_k exp(j c (u - k)) equals psi_kn exp(j c (u - kn)) for either k. Per
-// pixel: the choice of sample (u + 1/2 >= kn + 1), the phase, the sum.
+// Every pixel rounds to bin kn or kn + 1: one table entry (N_kn, M_kn) serves
+// all, since the echo phase psi_k exp(j c (u - k)) equals
+// psi_kn exp(j c (u - kn)) for either k. Per pixel: the choice of sample
+// (u + 1/2 >= kn + 1), the phase, the sum.
 __device__ __forceinline__ void nearest_pair_pulse(const BpConst& k, const PulseState& st,
-                                                   const float2* __restrict__ psi,
                                                    float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    // With x = c (u - kn - 1/2) (the state's polynomial), a pixel takes e_kn + 1
-    // when x >= 0 (u + 1/2 >= kn + 1), else e_kn, and its echo phase is
-    // psi_kn exp(j c (u - kn)) = psi_kn exp(j c / 2) exp(j x).
-    const float2 p0 = __ldg(psi + __float_as_int(st.t1d.y));
-    const float2 ps = make_float2(p0.x * k.hrot_re - p0.y * k.hrot_im, p0.x * k.hrot_im + p0.y * k.hrot_re);
+    // With x = c (u - kn - 1/2) (the state's polynomial), a pixel takes sample
+    // kn + 1 when x >= 0 (u + 1/2 >= kn + 1), else sample kn, and its echo is
+    // (N_kn + h M_kn) exp(j x) with h = 1 or 0: one set and one packed FMA per
+    // lane pair instead of compares and selects (N + M is the second sample to
+    // one rounding)
     const float4 e = st.t0;
-    const float w0r = e.x * ps.x - e.y * ps.y, w0i = e.x * ps.y + e.y * ps.x;
-    const float w1r = e.z * ps.x - e.w * ps.y, w1i = e.z * ps.y + e.w * ps.x;
-    // the sample as w0 + h (w1 - w0) with h = 1 or 0: one set and one packed
-    // FMA per lane pair instead of compares and selects (w0 + (w1 - w0) is w1
-    // to one rounding)
+    const float w0r = e.x, w0i = e.y, w1r = e.z, w1i = e.w;
     const float2 w0r2 = make_float2(w0r, w0r), w0i2 = make_float2(w0i, w0i);
-    const float2 dwr2 = make_float2(w1r - w0r, w1r - w0r), dwi2 = make_float2(w1i - w0i, w1i - w0i);
+    const float2 dwr2 = make_float2(w1r, w1r), dwi2 = make_float2(w1i, w1i);
     const float2 one = make_float2(1.0f, 1.0f);
     float2 id = make_float2(k.i0, k.i0 + NP);
 #pragma unroll
@@ -1054,7 +1053,6 @@ __device__ __forceinline__ void nearest_pair_pulse(const BpConst& k, const Pulse
 }
 
 __device__ __forceinline__ void nearest_pulse(const BpConst& k, const PulseState& st, const float4* row,
-                                              const float2* __restrict__ psi,
                                               float2 (&accre)[NP], float2 (&accim)[NP])
 {
     const float e0 = st.q0.x, e1 = st.q1.x, e2 = st.q2.x;
@@ -1064,14 +1062,13 @@ __device__ __forceinline__ void nearest_pulse(const BpConst& k, const PulseState
         const float ub = fmaf(i, fmaf(i, e2, e1), e0);
         float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
         float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
-        nearest_pixel<false>(k, ub, st.kb, st.bin0, row, psi, re, im);
+        nearest_pixel<false>(k, ub, st.kb, row, re, im);
     }
 }
 
 __device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Record& rec,
                                                     const float4* row, const double* __restrict__ a,
                                                     double xc, double yrow,
-                                                    const float2* __restrict__ psi,
                                                     float2 (&accre)[NP], float2 (&accim)[NP])
 {
     const double vx = xc - a[0], vy = yrow - a[1], vz = k.z0 - a[2];
@@ -1081,8 +1078,7 @@ __device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Reco
     if (!(fabs(u) < 1.0e9))
         return;
     const double ku = floor(u);
-    const int bin0 = __float_as_int(rec.d.y);
-    const int kbase = (int)ku + bin0;
+    const int kbase = (int)ku + __float_as_int(rec.d.y);
     const float frac0 = (float)(u - ku);
     const float two_vx = (float)(2.0 * vx), rf = (float)r, r2f = (float)r2;
 #pragma unroll
@@ -1095,7 +1091,7 @@ __device__ __forceinline__ void nearest_exact_pulse(const BpConst& k, const Reco
         const float ub = fmaf(dr_m, k.inv_dr_f, frac0);
         float& re = (m < NP) ? accre[m % NP].x : accre[m % NP].y;
         float& im = (m < NP) ? accim[m % NP].x : accim[m % NP].y;
-        nearest_pixel<true>(k, ub, kbase, bin0, row, psi, re, im);
+        nearest_pixel<true>(k, ub, kbase, row, re, im);
     }
 }
 
@@ -1209,8 +1205,8 @@ __device__ __forceinline__ void heights_series_loop(const BpConst& k, const floa
                 sinc_pixel<true>(k, ub.x, kbase, bin0, row, psi, accre[q].x, accim[q].x);
                 sinc_pixel<true>(k, ub.y, kbase, bin0, row, psi, accre[q].y, accim[q].y);
             } else {
-                nearest_pixel<true>(k, ub.x, kbase, bin0, row, psi, accre[q].x, accim[q].x);
-                nearest_pixel<true>(k, ub.y, kbase, bin0, row, psi, accre[q].y, accim[q].y);
+                nearest_pixel<true>(k, ub.x, kbase, row, accre[q].x, accim[q].x);
+                nearest_pixel<true>(k, ub.y, kbase, row, accre[q].y, accim[q].y);
             }
             continue;
         }
@@ -1395,7 +1391,7 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
             if (INTERP == INTERP_HEIGHTS_SINC8)
                 sinc_pixel<true>(k, ub, kbase, __float_as_int(rec.d.y), row, psi, re, im);
             else
-                nearest_pixel<true>(k, ub, kbase, __float_as_int(rec.d.y), row, psi, re, im);
+                nearest_pixel<true>(k, ub, kbase, row, re, im);
             continue;
         }
         if (!(ub > -1.0e6f && ub < 1.0e6f))
@@ -1417,26 +1413,37 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
     }
 }
 
+// x of a tile's centre column and y of an image row, float64 (recomputed where
+// needed rather than held in registers across the pulse loop)
+__device__ __forceinline__ double tile_xc(const BpConst& k, int col0)
+{
+    return k.x0 + ((double)col0 + 0.5 * (TILE_X - 1)) * k.dx;
+}
+__device__ __forceinline__ double row_y(const BpConst& k, int rowi)
+{
+    return k.y0 + (double)rowi * k.dy;
+}
+
 template <int INTERP>
 __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& st, const Record& rec,
-                                            const float4* row, const double* a, double xc,
-                                            double yrow, const HRow& hr, const float4* s_hp,
+                                            const float4* row, const double* a, int col0,
+                                            int rowi, const HRow& hr, const float4* s_hp,
                                             const float2* __restrict__ psi,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
     if (on_heights(INTERP)) {
         if (st.mode == MODE_EXACT &&
             !heights_series_pulse<INTERP>(k, rec, row, hr, s_hp, psi, accre, accim))
-            heights_exact_pulse<INTERP>(k, rec, row, a, xc, yrow, hr, s_hp, psi, accre, accim);
+            heights_exact_pulse<INTERP>(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), hr, s_hp, psi, accre, accim);
         return;
     }
     if (INTERP == INTERP_NEAREST) {
         if (st.mode == MODE_PAIR)
-            nearest_pair_pulse(k, st, psi, accre, accim);
+            nearest_pair_pulse(k, st, accre, accim);
         else if (st.mode == MODE_GATHER)
-            nearest_pulse(k, st, row, psi, accre, accim);
+            nearest_pulse(k, st, row, accre, accim);
         else if (st.mode == MODE_EXACT)
-            nearest_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
+            nearest_exact_pulse(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), accre, accim);
         return;
     }
     if (is_sinc(INTERP)) {
@@ -1453,7 +1460,7 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
         else if (st.mode == MODE_GATHER)
             sinc_pulse(k, st, row, psi, accre, accim);
         else if (st.mode == MODE_EXACT)
-            sinc_exact_pulse(k, rec, row, a, xc, yrow, psi, accre, accim);
+            sinc_exact_pulse(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), psi, accre, accim);
         return;
     }
     if (st.mode == MODE_HINGE)
@@ -1461,7 +1468,7 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
     else if (st.mode == MODE_GATHER)
         gather_pulse(k, st, row, accre, accim);
     else if (st.mode == MODE_EXACT)
-        exact_pulse(k, rec, row, a, xc, yrow, accre, accim);
+        exact_pulse(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), accre, accim);
 }
 
 __device__ __forceinline__ long long cta_start(const BpConst& k, long long b)
@@ -1506,10 +1513,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const int n1 = (int)(min(u1, (t + 1) * k.na) - t * k.na);
         const int col0 = (int)(t % k.tiles_x) * TILE_X;
         const int row0 = (int)(t / k.tiles_x) * TILE_Y;
-        const double xc = k.x0 + ((double)col0 + 0.5 * (TILE_X - 1)) * k.dx;
-        const double yc = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
-
-        const double yrow = k.y0 + (double)(row0 + jr) * k.dy;
+        const int rowi = row0 + jr;
         HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0, 0.0f, 0.0f, 0.0f, 0.0f};
         if (on_heights(INTERP)) {
             // the thread's own row of the tile, heights clamped to the plan's
@@ -1558,7 +1562,8 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const int cnt = min(CHUNK, n1 - c0);
             __syncthreads();
             if (tid < cnt)
-                make_record(k, pos, klo, c0 + tid, xc, yc, s_rec[tid]);
+                make_record(k, pos, klo, c0 + tid, tile_xc(k, col0),
+                            k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy, s_rec[tid]);
             __syncthreads();
             const int tw = row_pitch<INTERP>(k);
             const float4* rows = table + (size_t)c0 * tw;
@@ -1570,7 +1575,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 for (int p = 0; p < cnt; ++p) {
                     const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rows + (size_t)p * tw, jf);
                     apply_pulse<INTERP>(k, st, s_rec[p], rows + (size_t)p * tw,
-                                        pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
+                                        pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
                                         s_hp + jr * HROW4, psi, accre, accim);
                 }
                 continue;
@@ -1584,19 +1589,18 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 const PulseState sb =
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * tw, jf);
                 apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * tw,
-                                  pos + 3 * (size_t)(c0 + p), xc, yrow, hr,
+                                  pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
                                   s_hp + jr * HROW4, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
                 const int p2 = min(p + 2, cnt - 1);
                 sa = pulse_setup<INTERP>(k, s_rec[p2], rows + (size_t)p2 * tw, jf);
                 apply_pulse<INTERP>(k, sb, s_rec[p + 1], rows + (size_t)(p + 1) * tw,
-                                  pos + 3 * (size_t)(c0 + p + 1), xc, yrow, hr,
+                                  pos + 3 * (size_t)(c0 + p + 1), col0, rowi, hr,
                                   s_hp + jr * HROW4, psi, accre, accim);
             }
         }
 
-        const int rowi = row0 + jr;
         if (n0 == 0 && n1 == k.na) {
             if (rowi < k.ny) {
                 float2* dst = image + (size_t)rowi * k.nx;
