@@ -25,6 +25,7 @@ EXPORTS = (
     "sarbp_host_transfer_bytes", "sarbp_rc_plan", "sarbp_range_compress", "sarbp_rc_destroy",
     "sarbp_plan_heights", "sarbp_backproject_heights", "sarbp_backproject_streamed",
     "sarbp_backproject_volume", "sarbp_debug_fail_alloc", "sarbp_debug_sinc_taps",
+    "sarbp_backproject_raw",
 )
 
 SARBP_WINDOW_NONE = 0
@@ -96,6 +97,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sarbp_range_compress.restype = st
     lib.sarbp_rc_destroy.argtypes = [vp]
     lib.sarbp_rc_destroy.restype = st
+    lib.sarbp_backproject_raw.argtypes = [vp, vp, vp, vp, vp, P(Params), vp]
+    lib.sarbp_backproject_raw.restype = st
     lib.sarbp_debug_fail_alloc.argtypes = [ctypes.c_int32]
     lib.sarbp_debug_fail_alloc.restype = None
     lib.sarbp_debug_sinc_taps.argtypes = [ctypes.POINTER(ctypes.c_float)]

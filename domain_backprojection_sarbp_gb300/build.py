@@ -38,8 +38,8 @@ def sources() -> list[str]:
 
 
 def _inputs() -> list[str]:
-    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "sarbp.h"),
-                                                                os.path.abspath(__file__)]
+    return (sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+            + [os.path.join(INCLUDE, "sarbp.h"), os.path.abspath(__file__)])
 
 
 def is_stale() -> bool:

@@ -321,11 +321,14 @@ cudaError_t ensure_sinc_table(sarbp_plan_s* plan)
 
 // Queue the three kernels of one backprojection. Arguments are already
 // checked; params may describe a band of the plan's range axis (fewer bins,
-// shifted r0), which the plan's table rows always cover.
+// shifted r0), which the plan's table rows always cover. With a
+// range-compression plan rc, `echoes` is the raw frame and the table rows
+// come from the fused compression kernel (linear interpolation only).
 sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void* echoes,
                                     const double* antenna_pos, const sarbp_params* params,
                                     cudaStream_t s, const float* heights = nullptr,
-                                    long long echo_stride = 0)
+                                    long long echo_stride = 0,
+                                    const sarbp_rc_plan_s* rc = nullptr)
 {
     cudaError_t e = cudaSuccess;
     const long long pixels = (long long)params->nx * params->ny;
@@ -355,8 +358,12 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "cudaMemsetAsync");
     }
-    e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo,
-                     sinc_wide, s);
+    if (rc)
+        e = launch_rc_table(rc, k, static_cast<const float2*>(echoes), antenna_pos, table,
+                            plan->klo, s);
+    else
+        e = launch_table(k, static_cast<const float2*>(echoes), antenna_pos, table, plan->klo,
+                         sinc_wide, s);
     if (e != cudaSuccess)
         return cuda_fail(plan, e, "table kernel launch");
     if (k.flags & SARBP_SINC8) {
@@ -704,6 +711,47 @@ sarbp_status sarbp_backproject(sarbp_plan_t plan, void* image, const void* echoe
 
     return enqueue_backprojection(plan, image, echoes, antenna_pos, params,
                                   static_cast<cudaStream_t>(stream));
+}
+
+sarbp_status sarbp_backproject_raw(sarbp_plan_t plan, sarbp_rc_plan_t rc, void* image,
+                                   const void* raw, const double* antenna_pos,
+                                   const sarbp_params* params, void* stream)
+{
+    if (!plan || !rc || !params)
+        return SARBP_ERR_INVALID_ARG;
+    sarbp_status st = check_sizes(params);
+    if (st != SARBP_OK)
+        return st;
+    st = check_geometry(params);
+    if (st != SARBP_OK)
+        return st;
+    if (params->flags & (SARBP_SINC8 | SARBP_NEAREST))
+        return SARBP_ERR_INVALID_ARG;          // linear interpolation only
+    const sarbp_params& q = plan->p;
+    if (params->nx != q.nx || params->ny != q.ny || params->na != q.na || params->nr != q.nr ||
+        params->dx != q.dx || params->dy != q.dy || params->dr != q.dr || plan->heights_mode)
+        return SARBP_ERR_PLAN_MISMATCH;
+    int rc_na = 0, rc_ns = 0, rc_dev = -1;
+    rc_plan_shape(rc, &rc_na, &rc_ns, &rc_dev);
+    if (rc_na != params->na || rc_ns != params->nr || rc_dev != plan->device)
+        return SARBP_ERR_PLAN_MISMATCH;
+    const long long pixels = (long long)params->nx * params->ny;
+    if (pixels > 0 && (!image || !aligned8(image)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && (!antenna_pos || !aligned8(antenna_pos)))
+        return SARBP_ERR_INVALID_ARG;
+    if (params->na > 0 && params->nr > 0 && (!raw || !aligned8(raw)))
+        return SARBP_ERR_INVALID_ARG;
+    plan->last_error.clear();
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(plan, e, "cudaGetDevice");
+    if (dev != plan->device)
+        return SARBP_ERR_INVALID_ARG;
+    return enqueue_backprojection(plan, image, raw, antenna_pos, params,
+                                  static_cast<cudaStream_t>(stream), nullptr, 0, rc);
 }
 
 sarbp_status sarbp_backproject_volume(sarbp_plan_t plan, void* volume, const void* echoes,

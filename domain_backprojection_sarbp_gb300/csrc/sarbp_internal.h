@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct sarbp_rc_plan_s;
+
 namespace sarbp {
 
 // Work tile: one thread owns TILE_X consecutive pixels of one image row; the
@@ -89,6 +91,14 @@ cudaError_t prepare_kernels();
 constexpr int SPLIT_CELLS = 65536;         // (tile, pulse segment) cells of the cost estimate
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s);
+// Range compression fused with the linear echo table (sarbp_rc.cu): for every
+// pulse the compressed samples of the table row's window only, written as the
+// row's entries, with klo as launch_table sets it. k describes the
+// backprojection; the raw frame is [k.na][k.nr].
+cudaError_t launch_rc_table(const sarbp_rc_plan_s* rc, const BpConst& k, const float2* raw,
+                            const double* pos, float4* table, int* klo, cudaStream_t s);
+// Pulses, samples per pulse and device of a range-compression plan.
+bool rc_plan_shape(const sarbp_rc_plan_s* rc, int* na, int* ns, int* device);
 // The 8 x 8 windowed-sinc tap polynomial coefficients (row d + 3, column n).
 void sinc_taps_host(float* out);
 cudaError_t launch_reduce(const BpConst& k, const float4* partial, float2* image,

@@ -48,6 +48,7 @@
 //    sample (one table entry per thread and pulse when its pixels round to
 //    two bins), and pixels on a height map (a float-pair row reference and a
 //    range series per pixel, with the two-entry form for rows in two bins).
+#include "sarbp_device.cuh"
 #include "sarbp_internal.h"
 
 #include <cmath>
@@ -180,30 +181,15 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
         const double ax = pos[3 * (size_t)n + 0];
         const double ay = pos[3 * (size_t)n + 1];
         const double az = pos[3 * (size_t)n + 2];
-        int lo;
-        if (!(isfinite(ax) && isfinite(ay) && isfinite(az))) {
-            lo = KLO_INVALID;
-        } else if (k.full_window) {
-            lo = -(MARGIN + 4);
-        } else {
-            // nearest point of the tile-padded image box (a rectangle at z0, or
-            // the slab z0 + [h_min, h_max] for a height map) to the antenna
-            const double cx = fmin(fmax(ax, k.rect_x0), k.rect_x1);
-            const double cy = fmin(fmax(ay, k.rect_y0), k.rect_y1);
-            const double cz = k.heights_mode ? fmin(fmax(az, k.z_lo), k.z_hi) : k.z0;
-            const double ddx = cx - ax, ddy = cy - ay, ddz = cz - az;
-            const double rmin = sqrt(ddx * ddx + ddy * ddy + ddz * ddz);
-            double u = (rmin - (k.heights_mode ? k.qmax3 : k.qmax) - k.r0) * k.inv_dr;
-            u = fmin(fmax(u, -1.0e9), 1.0e9);
-            lo = (int)floor(u) - MARGIN;
-            if (SINC && sinc_wide) {
-                // a thread's 32 pixels span about 31 dx |g_x| / dr bins, |g_x| at
-                // most the largest x distance over the nearest range; above
-                // SINC_SPAN (with a margin for the curvature) the wide kernel runs
-                const double gx = fmax(fabs(k.rect_x0 - ax), fabs(k.rect_x1 - ax)) / fmax(rmin, 1.0);
-                if ((TILE_X - 1) * k.dx * gx * k.inv_dr + 0.01 > (double)SINC_SPAN)
-                    atomicOr(sinc_wide, 1);
-            }
+        double rmin;
+        const int lo = window_start(k, ax, ay, az, rmin);
+        if (SINC && sinc_wide && lo != KLO_INVALID && !k.full_window) {
+            // a thread's 32 pixels span about 31 dx |g_x| / dr bins, |g_x| at
+            // most the largest x distance over the nearest range; above
+            // SINC_SPAN (with a margin for the curvature) the wide kernel runs
+            const double gx = fmax(fabs(k.rect_x0 - ax), fabs(k.rect_x1 - ax)) / fmax(rmin, 1.0);
+            if ((TILE_X - 1) * k.dx * gx * k.inv_dr + 0.01 > (double)SINC_SPAN)
+                atomicOr(sinc_wide, 1);
         }
         s_lo = lo;
         klo[n] = lo;
@@ -243,33 +229,17 @@ __global__ void __launch_bounds__(256) table_kernel(BpConst k, const float2* __r
                 e0 = erow[kk];
             if (lo != KLO_INVALID && kk + 1 >= 0 && kk + 1 <= (long long)k.nr - 1)
                 e1 = erow[kk + 1];
-            // psi_k h = exp(j 2 pi (frac(2 r_k / lambda) + c / (4 pi)))
-            const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
-            const float turns = (float)(ph >> 40) * 0x1p-24f;
-            float sn, cs;
-            sincospif(2.0f * turns, &sn, &cs);
-            const float c = cs * k.hrot_re - sn * k.hrot_im;
-            const float s = cs * k.hrot_im + sn * k.hrot_re;
+            // psi_k h, h = exp(j c / 2)
+            const float2 ps = bin_phasor(k, kk);
+            const float c = ps.x * k.hrot_re - ps.y * k.hrot_im;
+            const float s = ps.x * k.hrot_im + ps.y * k.hrot_re;
             const float dre = e1.x - e0.x, dim = e1.y - e0.y;
             v.x = e0.x * c - e0.y * s;
             v.y = e0.x * s + e0.y * c;
             v.z = dre * c - dim * s;
             v.w = dre * s + dim * c;
         } else if (lo != KLO_INVALID && kk >= 0 && kk <= (long long)k.nr - 2) {
-            const float2 e0 = erow[kk];
-            const float2 e1 = erow[kk + 1];
-            // frac(2 r_k / lambda) in 64-bit fixed point, exact up to the
-            // rounding of the two constants
-            const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
-            const float turns = (float)(ph >> 40) * 0x1p-24f;
-            float s, c;
-            sincospif(2.0f * turns, &s, &c);
-            const float dre = e1.x - e0.x;
-            const float dim = e1.y - e0.y;
-            v.x = e0.x * c - e0.y * s;
-            v.y = e0.x * s + e0.y * c;
-            v.z = (dre * c - dim * s) * k.inv_c;
-            v.w = (dre * s + dim * c) * k.inv_c;
+            v = linear_entry(k, kk, erow[kk], erow[kk + 1]);
         }
         row[w] = v;
     }
@@ -281,11 +251,7 @@ __global__ void __launch_bounds__(256) psi_kernel(BpConst k, float2* __restrict_
     const long long kk = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (kk >= k.nr)
         return;
-    const unsigned long long ph = k.beta_fx + k.alpha_fx * (unsigned long long)kk;
-    const float turns = (float)(ph >> 40) * 0x1p-24f;
-    float s, c;
-    sincospif(2.0f * turns, &s, &c);
-    psi[kk] = make_float2(c, s);
+    psi[kk] = bin_phasor(k, kk);
 }
 
 // ---------------------------------------------------------------------------

@@ -27,6 +27,7 @@
 // straight to global memory. The filter spectrum H (conj FFT of the reference
 // times the window, divided by N) is built once by the plan, in natural order.
 #include "../../include/sarbp.h"
+#include "sarbp_device.cuh"
 #include "sarbp_internal.h"
 
 #include <cmath>
@@ -364,21 +365,43 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __re
     }
 }
 
-template <int L>
-__global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict__ raw, int ns_in,
-                                                       const float2* __restrict__ tw,
-                                                       const float2* __restrict__ h,
-                                                       float2* __restrict__ out)
+// Where the inverse transform's outputs go. GlobalOut writes sample i of the
+// row (i < ns) to global memory. BandOut writes the samples lo .. lo + nb - 1
+// of the compressed row into shared memory (band[i - lo]); it takes the
+// place of the transform's own row buffer, so the outputs are held in
+// registers until every thread has read its last inputs (SHARED).
+struct GlobalOut {
+    static constexpr bool SHARED = false;
+    float2* out;
+    int ns;
+    __device__ __forceinline__ void put(int i, float2 v) const
+    {
+        if (i < ns)
+            out[i] = v;
+    }
+};
+struct BandOut {
+    static constexpr bool SHARED = true;
+    float2* band;
+    int lo, nb, ns;
+    __device__ __forceinline__ void put(int i, float2 v) const
+    {
+        const int w = i - lo;
+        if (i < ns && (unsigned)w < (unsigned)nb)
+            band[w] = v;
+    }
+};
+
+// The filter product on the spectrum the forward transform left in registers,
+// then the inverse transform, its outputs handed to `out`.
+template <int L, class Out>
+__device__ __forceinline__ void filter_inverse(const Row& r, float2 (&v)[EPT],
+                                               const float2* __restrict__ tw,
+                                               const float2* __restrict__ h, const Out& out)
 {
     using F = Fft<L>;
     constexpr int N = F::N, R0 = F::R0;
-    extern __shared__ float2 smem[];
-    const Row r{smem};
     const int tid = threadIdx.x;
-    const size_t row0 = (size_t)blockIdx.x * ns_in;
-    float2 v[EPT];
-    forward_to_registers<L>(raw + row0, ns_in, tw, r, v);
-
     if constexpr (F::PASSES == 1) {
         // N = R0 <= 16: thread 0 holds the whole spectrum
         if (tid == 0) {
@@ -386,10 +409,13 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
             for (int t = 0; t < R0; ++t)
                 v[t] = cmul(v[t], __ldg(h + t));
             dft<R0, 1>(v);
+        }
+        if (Out::SHARED)
+            __syncthreads();
+        if (tid == 0) {
 #pragma unroll
             for (int t = 0; t < R0; ++t)
-                if (t < ns_in)
-                    out[row0 + t] = v[t];
+                out.put(t, v[t]);
         }
     } else {
         // filter, then the inverse's first pass (radix 16, span 1) on the held values
@@ -408,7 +434,7 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
             // inputs x[j + t N/32] times exp(+2 pi i j t / N), then as in the
             // forward merged pass; outputs go to j + t N/32
             constexpr int Q32 = N / 32, NSH = N / 2;
-            const int j = tid >> 1, h = tid & 1;
+            const int j = tid >> 1, hh = tid & 1;
             // powers of w = exp(+2 pi i j / N): the table region of span N/2
             // holds exp(-2 pi i t k / N) for rows t = 1, 4, 8, 12
             const float2* tr = tw + 4 * (NSH - 1) + j;
@@ -427,15 +453,14 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
                                 : ((s2 & 3) == 0 ? hi4 : ((s2 >> 2) == 0 ? lo4 : cmul(hi4, lo4)));
                 const float2 a = cmul(r.ld(pb + pad(s2 * Q32)), ws);
                 const float2 b = cmul(r.ld(pb + pad((s2 + 16) * Q32)), cmul(w16, ws));
-                v[s2] = h == 0 ? cadd(a, b) : cmul(csub(a, b), w32<1>(s2));
+                v[s2] = hh == 0 ? cadd(a, b) : cmul(csub(a, b), w32<1>(s2));
             }
             dft<16, 1>(v);
+            if (Out::SHARED)
+                __syncthreads();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int i = j + (2 * k + h) * Q32;
-                if (i < ns_in)
-                    out[row0 + i] = v[k];
-            }
+            for (int k = 0; k < 16; ++k)
+                out.put(j + (2 * k + hh) * Q32, v[k]);
         } else {
             Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid, tw);
             // last pass: radix R0, span N / R0; outputs go to j + t N/R0
@@ -443,20 +468,91 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
 #pragma unroll
             for (int b = 0; b < B0; ++b) {
                 const int j = tid + b * F::T;
+                if (j < NB0)
+                    pass_load<R0, 1, N, NB0>(r, v + b * R0, j, tw);
+            }
+            if (Out::SHARED)
+                __syncthreads();
+#pragma unroll
+            for (int b = 0; b < B0; ++b) {
+                const int j = tid + b * F::T;
                 if (j >= NB0)
                     continue;
-                float2* w = v + b * R0;
-                pass_load<R0, 1, N, NB0>(r, w, j, tw);
 #pragma unroll
-                for (int t = 0; t < R0; ++t) {
-                    const int i = j + t * NB0;
-                    if (i < ns_in)
-                        out[row0 + i] = w[t];
-                }
+                for (int t = 0; t < R0; ++t)
+                    out.put(j + t * NB0, v[b * R0 + t]);
             }
         }
     }
 }
+
+template <int L>
+__global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict__ raw, int ns_in,
+                                                       const float2* __restrict__ tw,
+                                                       const float2* __restrict__ h,
+                                                       float2* __restrict__ out)
+{
+    extern __shared__ float2 smem[];
+    const Row r{smem};
+    const size_t row0 = (size_t)blockIdx.x * ns_in;
+    float2 v[EPT];
+    forward_to_registers<L>(raw + row0, ns_in, tw, r, v);
+    filter_inverse<L>(r, v, tw, h, GlobalOut{out + row0, ns_in});
+}
+
+// Range compression fused with the linear echo table of a backprojection
+// plan: for pulse n the window start lo = klo[n] (as the table kernel finds
+// it), the compressed samples lo .. lo + W kept in shared memory, and the
+// W table entries (A_k, D_k / c) of that row written from them. The
+// compressed frame itself never reaches global memory.
+template <int L>
+__global__ void __launch_bounds__(Fft<L>::T) rc_table_kernel(sarbp::BpConst k,
+                                                             const float2* __restrict__ raw,
+                                                             const float2* __restrict__ tw,
+                                                             const float2* __restrict__ h,
+                                                             const double* __restrict__ pos,
+                                                             float4* __restrict__ table,
+                                                             int* __restrict__ klo)
+{
+    extern __shared__ float2 smem[];
+    __shared__ int s_lo;
+    const int n = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        double rmin;
+        const int lo = sarbp::window_start(k, pos[3 * (size_t)n], pos[3 * (size_t)n + 1],
+                                           pos[3 * (size_t)n + 2], rmin);
+        s_lo = lo;
+        klo[n] = lo;
+    }
+    __syncthreads();
+    const int lo = s_lo;
+    float4* row = table + (size_t)n * k.tw;
+    if (lo == sarbp::KLO_INVALID) {
+        // the pulse contributes nothing: a zero row
+        for (int w = tid; w < k.W; w += blockDim.x)
+            row[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const Row r{smem};
+    const size_t row0 = (size_t)n * k.nr;
+    float2 v[EPT];
+    forward_to_registers<L>(raw + row0, k.nr, tw, r, v);
+    filter_inverse<L>(r, v, tw, h, BandOut{smem, lo, k.W + 1, k.nr});
+    __syncthreads();
+    for (int w = tid; w < k.W; w += blockDim.x) {
+        float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long kk = (long long)lo + w;
+        if (kk >= 0 && kk <= (long long)k.nr - 2)
+            e = sarbp::linear_entry(k, kk, smem[w], smem[w + 1]);
+        row[w] = e;
+    }
+}
+
+// Shared memory of the fused table kernel: the transform's row, or the band
+// of W + 1 samples if that is longer (W <= ns + 19 <= N + 19)
+template <int L>
+constexpr int table_slots() { return Fft<L>::SLOTS > Fft<L>::N + 20 ? Fft<L>::SLOTS : Fft<L>::N + 20; }
 
 template <int L>
 cudaError_t set_smem_l()
@@ -465,7 +561,21 @@ cudaError_t set_smem_l()
     cudaError_t e = cudaFuncSetAttribute(rc_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(rc_filter_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(rc_table_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 table_slots<L>() * (int)sizeof(float2));
     return e;
+}
+
+template <int L>
+cudaError_t launch_table_l(const sarbp::BpConst& k, const float2* raw, const float2* tw,
+                           const float2* h, const double* pos, float4* table, int* klo,
+                           cudaStream_t s)
+{
+    const int slots = Fft<L>::SLOTS > k.W + 1 ? Fft<L>::SLOTS : k.W + 1;
+    rc_table_kernel<L><<<k.na, Fft<L>::T, (size_t)slots * sizeof(float2), s>>>(k, raw, tw, h, pos,
+                                                                                table, klo);
+    return cudaGetLastError();
 }
 
 template <int L>
@@ -499,6 +609,29 @@ cudaError_t set_smem(int log2n)
     case 12: return set_smem_l<12>();
     case 13: return set_smem_l<13>();
     case 14: return set_smem_l<14>();
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_table_any(int log2n, const sarbp::BpConst& k, const float2* raw,
+                             const float2* tw, const float2* h, const double* pos, float4* table,
+                             int* klo, cudaStream_t s)
+{
+    switch (log2n) {
+    case 1: return launch_table_l<1>(k, raw, tw, h, pos, table, klo, s);
+    case 2: return launch_table_l<2>(k, raw, tw, h, pos, table, klo, s);
+    case 3: return launch_table_l<3>(k, raw, tw, h, pos, table, klo, s);
+    case 4: return launch_table_l<4>(k, raw, tw, h, pos, table, klo, s);
+    case 5: return launch_table_l<5>(k, raw, tw, h, pos, table, klo, s);
+    case 6: return launch_table_l<6>(k, raw, tw, h, pos, table, klo, s);
+    case 7: return launch_table_l<7>(k, raw, tw, h, pos, table, klo, s);
+    case 8: return launch_table_l<8>(k, raw, tw, h, pos, table, klo, s);
+    case 9: return launch_table_l<9>(k, raw, tw, h, pos, table, klo, s);
+    case 10: return launch_table_l<10>(k, raw, tw, h, pos, table, klo, s);
+    case 11: return launch_table_l<11>(k, raw, tw, h, pos, table, klo, s);
+    case 12: return launch_table_l<12>(k, raw, tw, h, pos, table, klo, s);
+    case 13: return launch_table_l<13>(k, raw, tw, h, pos, table, klo, s);
+    case 14: return launch_table_l<14>(k, raw, tw, h, pos, table, klo, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -559,6 +692,26 @@ struct sarbp_rc_plan_s {
     float2* tw = nullptr;      // per-span twiddle rows, 4 N entries
     float2* h = nullptr;       // N filter coefficients / N, natural order
 };
+
+namespace sarbp {
+
+bool rc_plan_shape(const sarbp_rc_plan_s* rc, int* na, int* ns, int* device)
+{
+    if (!rc)
+        return false;
+    *na = rc->p.na;
+    *ns = rc->p.ns;
+    *device = rc->device;
+    return true;
+}
+
+cudaError_t launch_rc_table(const sarbp_rc_plan_s* rc, const BpConst& k, const float2* raw,
+                            const double* pos, float4* table, int* klo, cudaStream_t s)
+{
+    return launch_table_any(rc->log2n, k, raw, rc->tw, rc->h, pos, table, klo, s);
+}
+
+}  // namespace sarbp
 
 extern "C" {
 

@@ -157,6 +157,22 @@ class Plan:
             self._raise(st, "sarbp_backproject")
         return image
 
+    def backproject_raw(self, image, raw, antenna_pos, rc, params=None, accumulate=False,
+                        stream=None):
+        """Raw echoes to image (sarbp_backproject_raw): range compression with the
+        RangeCompressor ``rc`` fused with the echo table, then the linear
+        backprojection. raw complex64 [na, nr] on the device."""
+        import torch
+        p = _params(params if params is not None else self.params, accumulate)
+        img = _check_device_tensor(image, "image", torch.complex64, (p.ny, p.nx))
+        r = _check_device_tensor(raw, "raw", torch.complex64, (p.na, p.nr))
+        pos = _check_device_tensor(antenna_pos, "antenna_pos", torch.float64, (p.na, 3))
+        st = self._lib.sarbp_backproject_raw(self._h, rc.handle, img, r, pos, ctypes.byref(p),
+                                             _stream_handle(stream))
+        if st != _native.SARBP_OK:
+            self._raise(st, "sarbp_backproject_raw")
+        return image
+
     def backproject_volume(self, volume, echoes, antenna_pos, dz, params=None, accumulate=False,
                            stream=None, interp="linear"):
         """Voxel grid: volume complex64 [nz, ny, nx] on the device, plane iz at z0 + iz * dz."""
@@ -283,6 +299,10 @@ class RangeCompressor:
         if st != _native.SARBP_OK:
             raise SarbpError(st, "sarbp_range_compress")
         return out
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
 
     def close(self):
         if getattr(self, "_h", None):

@@ -34,7 +34,8 @@
  * time. Different plans are independent.
  *
  * CUDA graphs. The device-buffer calls (sarbp_backproject,
- * sarbp_backproject_heights, sarbp_backproject_volume, sarbp_range_compress)
+ * sarbp_backproject_heights, sarbp_backproject_volume, sarbp_range_compress,
+ * sarbp_backproject_raw)
  * only enqueue kernels and memsets on `stream`: they allocate nothing and do
  * not synchronise, so they may be captured into a CUDA graph once the plan
  * exists; each replay does the same work on the buffers given at capture.
@@ -369,6 +370,34 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
 
 /* Free the plan. NULL is accepted. */
 sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan);
+
+/*
+ * sarbp_backproject_raw - raw echoes to image in one call: range compression
+ * (SARBP-GPU §3.1, as sarbp_range_compress) feeding the backprojection
+ * (SARBP-GPU §2.2, §3.3, as sarbp_backproject with linear interpolation).
+ *
+ * raw          device pointer, complex64 [na][nr] raw (uncompressed) echoes,
+ *              caller-owned, 8-byte aligned; sample k of the compressed row
+ *              is the echo from range r0 + k dr, as for sarbp_backproject.
+ * rc           a range-compression plan with rc na == params->na and
+ *              ns == params->nr, made on the plan's device (else
+ *              SARBP_ERR_PLAN_MISMATCH).
+ * plan, image, antenna_pos, params, stream: as for sarbp_backproject;
+ *              params->flags may carry SARBP_ACCUMULATE only (SARBP_SINC8 or
+ *              SARBP_NEAREST: SARBP_ERR_INVALID_ARG); height-map plans are
+ *              refused (SARBP_ERR_PLAN_MISMATCH).
+ *
+ * Per pulse, one kernel compresses the raw row and keeps, in shared memory,
+ * only the compressed samples of the band of range bins the image can reach
+ * (the plan's table window), and writes the plan's echo-table entries from
+ * them: the compressed frame is never written to global memory. The image
+ * equals sarbp_range_compress followed by sarbp_backproject to float32
+ * rounding (the same arithmetic in both; only where the samples live
+ * differs). Enqueues on `stream` and returns; allocates nothing.
+ */
+sarbp_status sarbp_backproject_raw(sarbp_plan_t plan, sarbp_rc_plan_t rc, void* image,
+                                   const void* raw, const double* antenna_pos,
+                                   const sarbp_params* params, void* stream);
 
 /*
  * sarbp_backproject_noalloc - the same backprojection without any device

@@ -106,3 +106,73 @@ def test_raw_to_image_pipeline():
     want = oracle.backproject(p, rc_ref, sc.antenna_pos)
     parity.assert_parity(got, want, "raw -> image")
     assert not parity.argmax_mismatches(got, want, sc.targets)
+
+
+def _raw_scene(nr, na=64, nx=64, ny=64):
+    cfg = scenes.shrink(scenes.CONFIGS[0], na=na, nr=nr, nx=nx, ny=ny, n_targets=3,
+                        pulse_step=0.5)
+    sc = scenes.make_scene(cfg, noise=False)
+    p = sc.params
+    txyz = np.zeros((len(sc.targets), 3))
+    txyz[:, 0] = p["x0"] + sc.targets[:, 0] * p["dx"]
+    txyz[:, 1] = p["y0"] + sc.targets[:, 1] * p["dy"]
+    raw = chirp.raw_echoes(sc.antenna_pos, txyz, sc.amps, p["r0"], p["nr"])
+    g = np.random.default_rng(nr).standard_normal((na, nr, 2))
+    raw += 0.05 * (g[..., 0] + 1j * g[..., 1])
+    return sc, raw.astype(np.complex64)
+
+
+# FFT sizes 1024 (first pass of radix 4) and 8192 (merged radix-32 passes)
+@pytest.mark.parametrize("nr", [512, 4096])
+def test_raw_entry_point(nr):
+    """sarbp_backproject_raw (range compression fused with the echo table)
+    against the oracle's range compression followed by its backprojection,
+    and bit for bit against the two library calls it fuses. One pulse has a
+    non-finite antenna position and contributes nothing."""
+    sc, raw = _raw_scene(nr)
+    p = sc.params
+    pos_np = sc.antenna_pos.copy()
+    pos_np[7] = np.nan
+    ref = chirp.chirp().astype(np.complex64)
+    band = chirp.BANDWIDTH / (chirp.C_LIGHT / (2 * chirp.DR))
+    r = torch.from_numpy(raw).to(DEV)
+    pos = torch.from_numpy(pos_np).to(DEV)
+    f = torch.from_numpy(ref).to(DEV)
+    img = torch.full((p["ny"], p["nx"]), complex(3.0, 3.0), dtype=torch.complex64, device=DEV)
+    two = torch.full_like(img, complex(3.0, 3.0))
+    comp = torch.empty_like(r)
+    with RangeCompressor(f, p["na"], p["nr"], "hamming", band) as rc, Plan(p) as plan:
+        plan.backproject_raw(img, r, pos, rc)
+        rc(comp, r)
+        plan.backproject(two, comp, pos)
+        torch.cuda.synchronize()
+    got = img.cpu().numpy()
+    assert np.array_equal(got.view(np.uint64), two.cpu().numpy().view(np.uint64))
+
+    rc_ref = rco.range_compress(raw, ref, "hamming", band).astype(np.complex64)
+    want = oracle.backproject(p, rc_ref, pos_np)
+    print(parity.assert_parity(got, want, f"raw -> image, nr={nr}"))
+    assert not parity.argmax_mismatches(got, want, sc.targets)
+
+
+def test_raw_entry_point_accumulates_and_checks_plans():
+    sc, raw = _raw_scene(512, na=48)
+    p = sc.params
+    ref = torch.from_numpy(chirp.chirp().astype(np.complex64)).to(DEV)
+    r = torch.from_numpy(raw).to(DEV)
+    pos = torch.from_numpy(sc.antenna_pos).to(DEV)
+    img = torch.zeros((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+    with RangeCompressor(ref, p["na"], p["nr"]) as rc, Plan(p) as plan:
+        plan.backproject_raw(img, r, pos, rc)
+        once = img.clone()
+        plan.backproject_raw(img, r, pos, rc, accumulate=True)
+        torch.cuda.synchronize()
+        assert torch.allclose(img, 2 * once, rtol=1e-6, atol=1e-6 * once.abs().max().item())
+        with pytest.raises(SarbpError) as err:
+            plan.backproject_raw(img, r, pos, rc, params=dict(p, flags=_native.SARBP_SINC8))
+        assert err.value.status == _native.SARBP_ERR_INVALID_ARG
+    # a compression plan of another shape
+    with RangeCompressor(ref, p["na"], p["nr"] - 1) as rc_other, Plan(p) as plan:
+        with pytest.raises(SarbpError) as err:
+            plan.backproject_raw(img, r, pos, rc_other)
+        assert err.value.status == _native.SARBP_ERR_PLAN_MISMATCH
