@@ -33,12 +33,10 @@
 #include <cmath>
 #include <cstdint>
 #include <new>
-#include <vector>
 
 namespace {
 
 constexpr int RC_MAX_LOG2 = 14;            // N <= 16384: 135 KB of shared memory per row
-constexpr int EPT = 16;                    // complex values a thread holds
 
 // complex sums as one packed f32x2 operation (a - b = b * -1 + a, rounded once)
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
@@ -77,6 +75,63 @@ __device__ __forceinline__ void dft4(float2& a, float2& b, float2& c, float2& d)
 }
 
 template <int R, int S>
+__device__ __forceinline__ void dft(float2* v);
+
+// exp(S 2 pi i s / 32) for s = 0 .. 15 (compile-time s)
+template <int S>
+__device__ __forceinline__ float2 w32(int s)
+{
+    constexpr float C[16] = {1.0f, 0.980785280f, 0.923879533f, 0.831469612f, 0.707106781f,
+                             0.555570233f, 0.382683432f, 0.195090322f, 0.0f, -0.195090322f,
+                             -0.382683432f, -0.555570233f, -0.707106781f, -0.831469612f,
+                             -0.923879533f, -0.980785280f};
+    constexpr float SN[16] = {0.0f, 0.195090322f, 0.382683432f, 0.555570233f, 0.707106781f,
+                              0.831469612f, 0.923879533f, 0.980785280f, 1.0f, 0.980785280f,
+                              0.923879533f, 0.831469612f, 0.707106781f, 0.555570233f,
+                              0.382683432f, 0.195090322f};
+    return make_float2(C[s], S * SN[s]);
+}
+
+// 32 = 2 x 16: the DFTs of the even and the odd inputs, then X[k] = E[k] +
+// W32^k O[k] and X[k + 16] = E[k] - W32^k O[k] (W32^8 = S i costs nothing).
+template <int S>
+__device__ __forceinline__ void dft32(float2* v)
+{
+    float2 e[16], o[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        e[m] = v[2 * m];
+        o[m] = v[2 * m + 1];
+    }
+    dft<16, S>(e);
+    dft<16, S>(o);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float2 t = k == 0 ? o[k] : (k == 8 ? mul_si<S>(o[k]) : cmul(o[k], w32<S>(k)));
+        v[k] = cadd(e[k], t);
+        v[k + 16] = csub(e[k], t);
+    }
+}
+
+// 32-point DFT of inputs whose second half is zero: X[2k] = DFT16(x)[k] and
+// X[2k + 1] = DFT16(x W32^(S m))[k] (no radix-2 sums).
+template <int S>
+__device__ __forceinline__ void dft32_half(float2* v)
+{
+    float2 o[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        o[m] = m == 0 ? v[0] : (m == 8 ? mul_si<S>(v[8]) : cmul(v[m], w32<S>(m)));
+    dft<16, S>(v);
+    dft<16, S>(o);
+#pragma unroll
+    for (int k = 15; k >= 0; --k) {
+        v[2 * k] = v[k];
+        v[2 * k + 1] = o[k];
+    }
+}
+
+template <int R, int S>
 __device__ __forceinline__ void dft(float2* v)
 {
     constexpr float H = 0.707106781186547524f;     // cos(pi/4)
@@ -100,6 +155,8 @@ __device__ __forceinline__ void dft(float2* v)
         v[1] = cadd(e1, o1); v[5] = csub(e1, o1);
         v[2] = cadd(e2, o2); v[6] = csub(e2, o2);
         v[3] = cadd(e3, o3); v[7] = csub(e3, o3);
+    } else if (R == 32) {
+        dft32<S>(v);
     } else {
         // 16 = 4 x 4: m = 4 m1 + m2, k = k1 + 4 k2
         float2 y[16];
@@ -128,31 +185,67 @@ __device__ __forceinline__ void dft(float2* v)
     }
 }
 
-// v[t] *= w^t for t = 1 .. R-1, where w is the input twiddle of span NS at
-// position k. The table region of span NS (tw + 4 (NS - 1)) holds, for
-// t in {1, 4, 8, 12}, the four rows w^t over k = 0 .. NS-1 (forward sign;
-// conjugated for the inverse), so the 32 lanes of a warp read consecutive
-// entries. The other powers are products at most three roundings deep.
-template <int R, int S, int NS>
-__device__ __forceinline__ void twiddle_inputs(float2* v, int k, const float2* __restrict__ tw)
+// exp(S 2 pi i (t k mod M) / M), M = 2^m <= 16384, from the SFU (the sine and
+// cosine units sit idle in this kernel otherwise): the angle is reduced exactly,
+// in integer turns, to [-pi, pi), where the SFU's absolute error is about
+// 2^-21; that adds about 1e-6 of relative error to a transform, within the
+// 1e-5 the range-compression tests hold the library to.
+template <int S, int M>
+__device__ __forceinline__ float2 tw_sfu(int t, int k)
 {
-    const bool c = S > 0;
-    const float2* t = tw + 4 * (NS - 1) + k;
-    const float2 w1 = conj_if(__ldg(t), c);
+    float turns = (float)((t * k) & (M - 1)) * (1.0f / (float)M);
+    turns = turns >= 0.5f ? turns - 1.0f : turns;
+    float sn, cs;
+    __sincosf(6.28318530718f * turns, &sn, &cs);
+    return make_float2(cs, S * sn);
+}
+
+// v[t] *= w^t for t = 1 .. R-1, where w = exp(S 2 pi i k / (NS R)) is the input
+// twiddle of span NS at position k: w, w^4, w^8 and w^12 from the SFU, the
+// other powers as products at most three roundings deep.
+template <int R, int S, int NS>
+__device__ __forceinline__ void twiddle_inputs(float2* v, int k)
+{
+    if (R == 32) {
+        // span NS = N / 32: w = exp(-2 pi i k / N), the rows of the span-N/2
+        // region (stride NSH = N / 2); w^(16 + t) = w^16 w^t
+        constexpr int M = 32 * NS;
+        const float2 w1 = tw_sfu<S, M>(1, k), w4 = tw_sfu<S, M>(4, k);
+        const float2 w8 = tw_sfu<S, M>(8, k), w12 = tw_sfu<S, M>(12, k);
+        const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1), w16 = cmul(w8, w8);
+        v[16] = cmul(v[16], w16);
+        // each power formed where it is applied (few live registers)
+#pragma unroll
+        for (int a = 0; a < 16; a += 4) {
+            const float2 wa = a == 0 ? make_float2(1.f, 0.f) : (a == 4 ? w4 : (a == 8 ? w8 : w12));
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                if (a + b == 0)
+                    continue;
+                const float2 wb = b == 1 ? w1 : (b == 2 ? w2 : w3);
+                const float2 w = b == 0 ? wa : (a == 0 ? wb : cmul(wa, wb));
+                v[a + b] = cmul(v[a + b], w);
+                v[16 + a + b] = cmul(v[16 + a + b], cmul(w16, w));
+            }
+        }
+        return;
+    }
+    constexpr int M = NS * R;
+    const float2 w1 = tw_sfu<S, M>(1, k);
     v[1] = cmul(v[1], w1);
     if (R >= 4) {
         const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1);
         v[2] = cmul(v[2], w2);
         v[3] = cmul(v[3], w3);
         if (R >= 8) {
-            const float2 w4 = conj_if(__ldg(t + NS), c);
+            const float2 w4 = tw_sfu<S, M>(4, k);
             v[4] = cmul(v[4], w4);
             v[5] = cmul(v[5], cmul(w4, w1));
             v[6] = cmul(v[6], cmul(w4, w2));
             v[7] = cmul(v[7], cmul(w4, w3));
             if (R == 16) {
-                const float2 w8 = conj_if(__ldg(t + 2 * NS), c);
-                const float2 w12 = conj_if(__ldg(t + 3 * NS), c);
+                const float2 w8 = tw_sfu<S, M>(8, k);
+                const float2 w12 = tw_sfu<S, M>(12, k);
                 v[8] = cmul(v[8], w8);
                 v[9] = cmul(v[9], cmul(w8, w1));
                 v[10] = cmul(v[10], cmul(w8, w2));
@@ -168,35 +261,49 @@ __device__ __forceinline__ void twiddle_inputs(float2* v, int k, const float2* _
 
 __host__ __device__ constexpr int pad(int i) { return i + (i >> 4); }
 
-// Pass structure of an N = 2^L transform: a first pass of radix R0 (2, 4, 8
-// or 16, so that the rest are radix 16), PASSES passes in all, T threads.
+// Rows ahead of its own that a CTA asks L2 to fetch: about a wave of CTAs
+// later the CTA of that row finds it in L2 instead of waiting on HBM.
+constexpr int RC_PREFETCH_AHEAD = 512;
+
+// One bulk L2 prefetch of raw row n (ns complex samples), if it exists and
+// starts and ends on 16-byte boundaries (ns even).
+__device__ __forceinline__ void prefetch_row_l2(const float2* raw, int ns, int n, int rows)
+{
+    if (threadIdx.x == 0 && n < rows && (ns & 1) == 0 &&
+        (reinterpret_cast<uintptr_t>(raw) & 15) == 0) {
+        const float2* p = raw + (size_t)n * ns;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(ns * 8) : "memory");
+    }
+}
+
+// A raw sample: read once, so it is not kept in L1, where the filter and
+// twiddle rows that every pulse reads should stay.
+__device__ __forceinline__ float2 ld_stream(const float2* p)
+{
+    float2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
+// Pass structure of an N = 2^L transform: a first pass of radix R0 (2, 4, 8,
+// 16 or 32, so that the rest are radix 16), PASSES passes in all, T threads,
+// EPT complex values per thread. When log2 N = 1 mod 4 (N = 2 16^m) the first
+// pass is radix 32 on 32 values a thread holds, and every radix-16 pass gives
+// each thread two butterflies (BF = 2): no radix-2 pass and no exchange for it.
 template <int L>
 struct Fft {
     static constexpr int N = 1 << L;
-    static constexpr int R0 = L < 4 ? N : ((L % 4) ? (1 << (L % 4)) : 16);
-    static constexpr int PASSES = L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4;
-    static constexpr int T = N / 16 > 32 ? N / 16 : 32;
+    static constexpr bool R32 = L % 4 == 1 && L >= 5;
+    static constexpr int R0 = R32 ? 32 : (L < 4 ? N : ((L % 4) ? (1 << (L % 4)) : 16));
+    static constexpr int EPT = R32 ? 32 : 16;
+    static constexpr int BF = EPT / 16;                // radix-16 butterflies per thread
+    static constexpr int PASSES = R32 ? 1 + (L - 5) / 4 : (L < 4 ? 1 : 1 + (L - (L % 4 ? L % 4 : 4)) / 4);
+    static constexpr int T = N / EPT > 32 ? N / EPT : 32;
+    // resident CTAs per SM the fused table kernel's registers are sized for
+    // (three CTAs of 256 threads fit the registers and the shared rows of one SM)
+    static constexpr int TABLE_MINB = T <= 256 ? 3 : 1;
     static constexpr int SLOTS = pad(N - 1) + 1;       // float2 slots of the padded row
-    // N = 2 16^m, m >= 2: the radix-2 pass and the radix-16 pass next to it
-    // run as one radix-32 pass, two threads per butterfly (one shared-memory
-    // exchange fewer in each direction)
-    static constexpr bool MERGE = R0 == 2 && L >= 9;
 };
-
-// exp(S 2 pi i s / 32) for s = 0 .. 15 (compile-time s)
-template <int S>
-__device__ __forceinline__ float2 w32(int s)
-{
-    constexpr float C[16] = {1.0f, 0.980785280f, 0.923879533f, 0.831469612f, 0.707106781f,
-                             0.555570233f, 0.382683432f, 0.195090322f, 0.0f, -0.195090322f,
-                             -0.382683432f, -0.555570233f, -0.707106781f, -0.831469612f,
-                             -0.923879533f, -0.980785280f};
-    constexpr float SN[16] = {0.0f, 0.195090322f, 0.382683432f, 0.555570233f, 0.707106781f,
-                              0.831469612f, 0.923879533f, 0.980785280f, 1.0f, 0.980785280f,
-                              0.923879533f, 0.831469612f, 0.707106781f, 0.555570233f,
-                              0.382683432f, 0.195090322f};
-    return make_float2(C[s], S * SN[s]);
-}
 
 // Shared row: complex values as float2, one spare slot after every 16 (a
 // warp's 8-byte accesses are served 16 lanes at a time; with this padding
@@ -214,8 +321,7 @@ struct Row {
 // of span NS, the DFT. Outputs belong at pad(base) + pad(t NS), base =
 // (j / NS) NS R + j % NS.
 template <int R, int S, int N, int NS>
-__device__ __forceinline__ void pass_load(const Row& r, float2* v, int j,
-                                          const float2* __restrict__ tw)
+__device__ __forceinline__ void pass_load(const Row& r, float2* v, int j)
 {
     constexpr int STRIDE = N / R;
     const int pb = pad(j);
@@ -223,7 +329,7 @@ __device__ __forceinline__ void pass_load(const Row& r, float2* v, int j,
     for (int t = 0; t < R; ++t)
         v[t] = r.ld(pb + pad(t * STRIDE));
     if (NS > 1)
-        twiddle_inputs<R, S, NS>(v, j & (NS - 1), tw);
+        twiddle_inputs<R, S, NS>(v, j & (NS - 1));
     dft<R, S>(v);
 }
 
@@ -242,18 +348,25 @@ __device__ __forceinline__ void pass_store(const Row& r, const float2* v, int j)
 // time so that every span and offset is a constant.
 template <int L, int S, int P, int P1, int NS>
 struct Middle {
-    static __device__ __forceinline__ void run(const Row& r, float2* v, int tid,
-                                               const float2* __restrict__ tw)
+    static __device__ __forceinline__ void run(const Row& r, float2* v, int tid)
     {
         if constexpr (P < P1) {
-            const bool act = tid < (Fft<L>::N / 16);
-            if (act)
-                pass_load<16, S, Fft<L>::N, NS>(r, v, tid, tw);
+            using F = Fft<L>;
+#pragma unroll
+            for (int b = 0; b < F::BF; ++b) {
+                const int j = tid + b * F::T;
+                if (j < F::N / 16)
+                    pass_load<16, S, F::N, NS>(r, v + 16 * b, j);
+            }
             __syncthreads();
-            if (act)
-                pass_store<16, NS>(r, v, tid);
+#pragma unroll
+            for (int b = 0; b < F::BF; ++b) {
+                const int j = tid + b * F::T;
+                if (j < F::N / 16)
+                    pass_store<16, NS>(r, v + 16 * b, j);
+            }
             __syncthreads();
-            Middle<L, S, P + 1, P1, NS * 16>::run(r, v, tid, tw);
+            Middle<L, S, P + 1, P1, NS * 16>::run(r, v, tid);
         }
     }
 };
@@ -263,39 +376,22 @@ struct Middle {
 // in v[b RL + t], j = tid + b T, RL = 16 when PASSES > 1, else R0. Ends after
 // a barrier, so the shared row may be rewritten.
 template <int L>
-__device__ __forceinline__ void forward_to_registers(const float2* __restrict__ src, int len,
-                                                     const float2* __restrict__ tw, const Row& r,
-                                                     float2 (&v)[EPT])
+__device__ __forceinline__ void forward_to_registers(const float2* __restrict__ src, int len, const Row& r,
+                                                     float2 (&v)[Fft<L>::EPT])
 {
     using F = Fft<L>;
-    constexpr int R0 = F::R0, B0 = EPT / R0, NB0 = F::N / R0;
+    constexpr int R0 = F::R0, B0 = F::EPT / R0, NB0 = F::N / R0;
     const int tid = threadIdx.x;
-    if constexpr (F::MERGE) {
-        // radix-32 Stockham pass of span 1 from global memory: butterfly j
-        // takes x[j + t N/32], t < 32; thread half h = 0 keeps the even outputs
-        // (a_s = x_s + x_(s+16)), h = 1 the odd ones
-        // (b_s = (x_s - x_(s+16)) W32^-s), each followed by a 16-point DFT, so
-        // thread h holds X32[2k + h] in v[k]
-        constexpr int Q32 = F::N / 32;
-        const int j = tid >> 1, h = tid & 1;
+    if (F::R32 && len <= F::N / 2) {
+        // zero padding fills the second half of the row: the radix-32 pass
+        // reads and transforms 16 values (one butterfly per thread)
+        const int j = tid;
 #pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-            const int i0 = j + s2 * Q32, i1 = j + (s2 + 16) * Q32;
-            const float2 a = i0 < len ? __ldg(src + i0) : make_float2(0.f, 0.f);
-            const float2 b = i1 < len ? __ldg(src + i1) : make_float2(0.f, 0.f);
-            v[s2] = h == 0 ? cadd(a, b) : cmul(csub(a, b), w32<-1>(s2));
+        for (int t = 0; t < 16; ++t) {
+            const int i = j + t * NB0;
+            v[t] = (j < NB0 && i < len) ? ld_stream(src + i) : make_float2(0.f, 0.f);
         }
-        dft<16, -1>(v);
-        const int pb = pad(j * 32);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            r.st(pb + 2 * k + h + ((2 * k + h) >> 4), v[k]);
-        __syncthreads();
-        Middle<L, -1, 2, F::PASSES - 1, 32>::run(r, v, tid, tw);
-        constexpr int NSL = F::N / 16;
-        if (tid < (F::N / 16))
-            pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
-        __syncthreads();
+        dft32_half<-1>(v);
     } else {
 #pragma unroll
         for (int b = 0; b < B0; ++b) {
@@ -303,30 +399,33 @@ __device__ __forceinline__ void forward_to_registers(const float2* __restrict__ 
 #pragma unroll
             for (int t = 0; t < R0; ++t) {
                 const int i = j + t * NB0;
-                v[b * R0 + t] = (j < NB0 && i < len) ? __ldg(src + i) : make_float2(0.f, 0.f);
+                v[b * R0 + t] = (j < NB0 && i < len) ? ld_stream(src + i) : make_float2(0.f, 0.f);
             }
             dft<R0, -1>(v + b * R0);
         }
-        if constexpr (F::PASSES > 1) {
+    }
+    if constexpr (F::PASSES > 1) {
 #pragma unroll
-            for (int b = 0; b < B0; ++b) {
-                const int j = tid + b * F::T;
-                if (j < NB0)
-                    pass_store<R0, 1>(r, v + b * R0, j);
-            }
-            __syncthreads();
-            Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid, tw);
-            constexpr int NSL = F::N / 16;             // span of the last pass
-            if (tid < (F::N / 16))
-                pass_load<16, -1, F::N, NSL>(r, v, tid, tw);
-            __syncthreads();
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+            if (j < NB0)
+                pass_store<R0, 1>(r, v + b * R0, j);
         }
+        __syncthreads();
+        Middle<L, -1, 1, F::PASSES - 1, R0>::run(r, v, tid);
+        constexpr int NSL = F::N / 16;             // span of the last pass
+#pragma unroll
+        for (int b = 0; b < F::BF; ++b) {
+            const int j = tid + b * F::T;
+            if (j < F::N / 16)
+                pass_load<16, -1, F::N, NSL>(r, v + 16 * b, j);
+        }
+        __syncthreads();
     }
 }
 
 template <int L>
 __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __restrict__ ref, int nref,
-                                                              const float2* __restrict__ tw,
                                                               unsigned window, float band,
                                                               float4 taylor,
                                                               float2* __restrict__ h)
@@ -334,10 +433,10 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_filter_kernel(const float2* __re
     using F = Fft<L>;
     extern __shared__ float2 smem[];
     const Row r{smem};
-    float2 v[EPT];
-    forward_to_registers<L>(ref, nref, tw, r, v);
+    float2 v[F::EPT];
+    forward_to_registers<L>(ref, nref, r, v);
     constexpr int RL = F::PASSES > 1 ? 16 : F::R0;
-    constexpr int BL = EPT / RL, NBL = F::N / RL;
+    constexpr int BL = F::EPT / RL, NBL = F::N / RL;
     const float inv_n = 1.0f / (float)F::N;
 #pragma unroll
     for (int b = 0; b < BL; ++b) {
@@ -395,15 +494,14 @@ struct BandOut {
 // The filter product on the spectrum the forward transform left in registers,
 // then the inverse transform, its outputs handed to `out`.
 template <int L, class Out>
-__device__ __forceinline__ void filter_inverse(const Row& r, float2 (&v)[EPT],
-                                               const float2* __restrict__ tw,
+__device__ __forceinline__ void filter_inverse(const Row& r, float2 (&v)[Fft<L>::EPT],
                                                const float2* __restrict__ h, const Out& out)
 {
     using F = Fft<L>;
     constexpr int N = F::N, R0 = F::R0;
     const int tid = threadIdx.x;
     if constexpr (F::PASSES == 1) {
-        // N = R0 <= 16: thread 0 holds the whole spectrum
+        // N = R0 <= 32: thread 0 holds the whole spectrum
         if (tid == 0) {
 #pragma unroll
             for (int t = 0; t < R0; ++t)
@@ -420,84 +518,54 @@ __device__ __forceinline__ void filter_inverse(const Row& r, float2 (&v)[EPT],
     } else {
         // filter, then the inverse's first pass (radix 16, span 1) on the held values
         constexpr int Q = (F::N / 16);
-        if (tid < Q) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-                v[t] = cmul(v[t], __ldg(h + tid + t * Q));
-            dft<16, 1>(v);
-            pass_store<16, 1>(r, v, tid);
+        for (int b = 0; b < F::BF; ++b) {
+            const int j = tid + b * F::T;
+            if (j < Q) {
+                float2* w = v + 16 * b;
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    w[t] = cmul(w[t], __ldg(h + j + t * Q));
+                dft<16, 1>(w);
+                pass_store<16, 1>(r, w, j);
+            }
         }
         __syncthreads();
-        if constexpr (F::MERGE) {
-            Middle<L, 1, 1, F::PASSES - 2, 16>::run(r, v, tid, tw);
-            // last pass: radix 32, span N / 32, two threads per butterfly j:
-            // inputs x[j + t N/32] times exp(+2 pi i j t / N), then as in the
-            // forward merged pass; outputs go to j + t N/32
-            constexpr int Q32 = N / 32, NSH = N / 2;
-            const int j = tid >> 1, hh = tid & 1;
-            // powers of w = exp(+2 pi i j / N): the table region of span N/2
-            // holds exp(-2 pi i t k / N) for rows t = 1, 4, 8, 12
-            const float2* tr = tw + 4 * (NSH - 1) + j;
-            const float2 w1 = conj_if(__ldg(tr), true), w4 = conj_if(__ldg(tr + NSH), true);
-            const float2 w8 = conj_if(__ldg(tr + 2 * NSH), true);
-            const float2 w12 = conj_if(__ldg(tr + 3 * NSH), true);
-            const float2 w2 = cmul(w1, w1), w3 = cmul(w2, w1), w16 = cmul(w8, w8);
-            const int pb = pad(j);
+        Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid);
+        // last pass: radix R0, span N / R0; outputs go to j + t N/R0
+        constexpr int B0 = F::EPT / R0, NB0 = N / R0;
 #pragma unroll
-            for (int s2 = 0; s2 < 16; ++s2) {
-                const float2 lo4 = (s2 & 3) == 0 ? make_float2(1.f, 0.f)
-                                 : (s2 & 3) == 1 ? w1 : (s2 & 3) == 2 ? w2 : w3;
-                const float2 hi4 = (s2 >> 2) == 0 ? make_float2(1.f, 0.f)
-                                 : (s2 >> 2) == 1 ? w4 : (s2 >> 2) == 2 ? w8 : w12;
-                const float2 ws = (s2 == 0) ? make_float2(1.f, 0.f)
-                                : ((s2 & 3) == 0 ? hi4 : ((s2 >> 2) == 0 ? lo4 : cmul(hi4, lo4)));
-                const float2 a = cmul(r.ld(pb + pad(s2 * Q32)), ws);
-                const float2 b = cmul(r.ld(pb + pad((s2 + 16) * Q32)), cmul(w16, ws));
-                v[s2] = hh == 0 ? cadd(a, b) : cmul(csub(a, b), w32<1>(s2));
-            }
-            dft<16, 1>(v);
-            if (Out::SHARED)
-                __syncthreads();
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+            if (j < NB0)
+                pass_load<R0, 1, N, NB0>(r, v + b * R0, j);
+        }
+        if (Out::SHARED)
+            __syncthreads();
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                out.put(j + (2 * k + hh) * Q32, v[k]);
-        } else {
-            Middle<L, 1, 1, F::PASSES - 1, 16>::run(r, v, tid, tw);
-            // last pass: radix R0, span N / R0; outputs go to j + t N/R0
-            constexpr int B0 = EPT / R0, NB0 = N / R0;
+        for (int b = 0; b < B0; ++b) {
+            const int j = tid + b * F::T;
+            if (j >= NB0)
+                continue;
 #pragma unroll
-            for (int b = 0; b < B0; ++b) {
-                const int j = tid + b * F::T;
-                if (j < NB0)
-                    pass_load<R0, 1, N, NB0>(r, v + b * R0, j, tw);
-            }
-            if (Out::SHARED)
-                __syncthreads();
-#pragma unroll
-            for (int b = 0; b < B0; ++b) {
-                const int j = tid + b * F::T;
-                if (j >= NB0)
-                    continue;
-#pragma unroll
-                for (int t = 0; t < R0; ++t)
-                    out.put(j + t * NB0, v[b * R0 + t]);
-            }
+            for (int t = 0; t < R0; ++t)
+                out.put(j + t * NB0, v[b * R0 + t]);
         }
     }
 }
 
 template <int L>
-__global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict__ raw, int ns_in,
-                                                       const float2* __restrict__ tw,
+__global__ void __launch_bounds__(Fft<L>::T, Fft<L>::TABLE_MINB) rc_kernel(const float2* __restrict__ raw, int ns_in,
                                                        const float2* __restrict__ h,
                                                        float2* __restrict__ out)
 {
     extern __shared__ float2 smem[];
     const Row r{smem};
     const size_t row0 = (size_t)blockIdx.x * ns_in;
-    float2 v[EPT];
-    forward_to_registers<L>(raw + row0, ns_in, tw, r, v);
-    filter_inverse<L>(r, v, tw, h, GlobalOut{out + row0, ns_in});
+    prefetch_row_l2(raw, ns_in, blockIdx.x + RC_PREFETCH_AHEAD, gridDim.x);
+    float2 v[Fft<L>::EPT];
+    forward_to_registers<L>(raw + row0, ns_in, r, v);
+    filter_inverse<L>(r, v, h, GlobalOut{out + row0, ns_in});
 }
 
 // Range compression fused with the linear echo table of a backprojection
@@ -506,9 +574,8 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_kernel(const float2* __restrict_
 // W table entries (A_k, D_k / c) of that row written from them. The
 // compressed frame itself never reaches global memory.
 template <int L>
-__global__ void __launch_bounds__(Fft<L>::T) rc_table_kernel(sarbp::BpConst k,
+__global__ void __launch_bounds__(Fft<L>::T, Fft<L>::TABLE_MINB) rc_table_kernel(sarbp::BpConst k,
                                                              const float2* __restrict__ raw,
-                                                             const float2* __restrict__ tw,
                                                              const float2* __restrict__ h,
                                                              const double* __restrict__ pos,
                                                              float4* __restrict__ table,
@@ -536,9 +603,10 @@ __global__ void __launch_bounds__(Fft<L>::T) rc_table_kernel(sarbp::BpConst k,
     }
     const Row r{smem};
     const size_t row0 = (size_t)n * k.nr;
-    float2 v[EPT];
-    forward_to_registers<L>(raw + row0, k.nr, tw, r, v);
-    filter_inverse<L>(r, v, tw, h, BandOut{smem, lo, k.W + 1, k.nr});
+    prefetch_row_l2(raw, k.nr, n + RC_PREFETCH_AHEAD, k.na);
+    float2 v[Fft<L>::EPT];
+    forward_to_registers<L>(raw + row0, k.nr, r, v);
+    filter_inverse<L>(r, v, h, BandOut{smem, lo, k.W + 1, k.nr});
     __syncthreads();
     for (int w = tid; w < k.W; w += blockDim.x) {
         float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -568,26 +636,26 @@ cudaError_t set_smem_l()
 }
 
 template <int L>
-cudaError_t launch_table_l(const sarbp::BpConst& k, const float2* raw, const float2* tw,
+cudaError_t launch_table_l(const sarbp::BpConst& k, const float2* raw,
                            const float2* h, const double* pos, float4* table, int* klo,
                            cudaStream_t s)
 {
     const int slots = Fft<L>::SLOTS > k.W + 1 ? Fft<L>::SLOTS : k.W + 1;
-    rc_table_kernel<L><<<k.na, Fft<L>::T, (size_t)slots * sizeof(float2), s>>>(k, raw, tw, h, pos,
+    rc_table_kernel<L><<<k.na, Fft<L>::T, (size_t)slots * sizeof(float2), s>>>(k, raw, h, pos,
                                                                                 table, klo);
     return cudaGetLastError();
 }
 
 template <int L>
-cudaError_t launch_l(bool filter, int na, const float2* in, int len, const float2* tw,
+cudaError_t launch_l(bool filter, int na, const float2* in, int len,
                      const float2* h_in, unsigned window, float band, float4 taylor, float2* out,
                      cudaStream_t s)
 {
     const size_t bytes = (size_t)Fft<L>::SLOTS * sizeof(float2);
     if (filter)
-        rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, tw, window, band, taylor, out);
+        rc_filter_kernel<L><<<1, Fft<L>::T, bytes, s>>>(in, len, window, band, taylor, out);
     else
-        rc_kernel<L><<<na, Fft<L>::T, bytes, s>>>(in, len, tw, h_in, out);
+        rc_kernel<L><<<na, Fft<L>::T, bytes, s>>>(in, len, h_in, out);
     return cudaGetLastError();
 }
 
@@ -614,47 +682,47 @@ cudaError_t set_smem(int log2n)
 }
 
 cudaError_t launch_table_any(int log2n, const sarbp::BpConst& k, const float2* raw,
-                             const float2* tw, const float2* h, const double* pos, float4* table,
+                             const float2* h, const double* pos, float4* table,
                              int* klo, cudaStream_t s)
 {
     switch (log2n) {
-    case 1: return launch_table_l<1>(k, raw, tw, h, pos, table, klo, s);
-    case 2: return launch_table_l<2>(k, raw, tw, h, pos, table, klo, s);
-    case 3: return launch_table_l<3>(k, raw, tw, h, pos, table, klo, s);
-    case 4: return launch_table_l<4>(k, raw, tw, h, pos, table, klo, s);
-    case 5: return launch_table_l<5>(k, raw, tw, h, pos, table, klo, s);
-    case 6: return launch_table_l<6>(k, raw, tw, h, pos, table, klo, s);
-    case 7: return launch_table_l<7>(k, raw, tw, h, pos, table, klo, s);
-    case 8: return launch_table_l<8>(k, raw, tw, h, pos, table, klo, s);
-    case 9: return launch_table_l<9>(k, raw, tw, h, pos, table, klo, s);
-    case 10: return launch_table_l<10>(k, raw, tw, h, pos, table, klo, s);
-    case 11: return launch_table_l<11>(k, raw, tw, h, pos, table, klo, s);
-    case 12: return launch_table_l<12>(k, raw, tw, h, pos, table, klo, s);
-    case 13: return launch_table_l<13>(k, raw, tw, h, pos, table, klo, s);
-    case 14: return launch_table_l<14>(k, raw, tw, h, pos, table, klo, s);
+    case 1: return launch_table_l<1>(k, raw, h, pos, table, klo, s);
+    case 2: return launch_table_l<2>(k, raw, h, pos, table, klo, s);
+    case 3: return launch_table_l<3>(k, raw, h, pos, table, klo, s);
+    case 4: return launch_table_l<4>(k, raw, h, pos, table, klo, s);
+    case 5: return launch_table_l<5>(k, raw, h, pos, table, klo, s);
+    case 6: return launch_table_l<6>(k, raw, h, pos, table, klo, s);
+    case 7: return launch_table_l<7>(k, raw, h, pos, table, klo, s);
+    case 8: return launch_table_l<8>(k, raw, h, pos, table, klo, s);
+    case 9: return launch_table_l<9>(k, raw, h, pos, table, klo, s);
+    case 10: return launch_table_l<10>(k, raw, h, pos, table, klo, s);
+    case 11: return launch_table_l<11>(k, raw, h, pos, table, klo, s);
+    case 12: return launch_table_l<12>(k, raw, h, pos, table, klo, s);
+    case 13: return launch_table_l<13>(k, raw, h, pos, table, klo, s);
+    case 14: return launch_table_l<14>(k, raw, h, pos, table, klo, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch(int log2n, bool filter, int na, const float2* in, int len, const float2* tw,
+cudaError_t launch(int log2n, bool filter, int na, const float2* in, int len,
                    const float2* h_in, unsigned window, float band, float4 taylor, float2* out,
                    cudaStream_t s)
 {
     switch (log2n) {
-    case 1: return launch_l<1>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 2: return launch_l<2>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 3: return launch_l<3>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 4: return launch_l<4>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 5: return launch_l<5>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 6: return launch_l<6>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 7: return launch_l<7>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 8: return launch_l<8>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 9: return launch_l<9>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 10: return launch_l<10>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 11: return launch_l<11>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 12: return launch_l<12>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 13: return launch_l<13>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
-    case 14: return launch_l<14>(filter, na, in, len, tw, h_in, window, band, taylor, out, s);
+    case 1: return launch_l<1>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 2: return launch_l<2>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 3: return launch_l<3>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 4: return launch_l<4>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 5: return launch_l<5>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 6: return launch_l<6>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 7: return launch_l<7>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 8: return launch_l<8>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 9: return launch_l<9>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 10: return launch_l<10>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 11: return launch_l<11>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 12: return launch_l<12>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 13: return launch_l<13>(filter, na, in, len, h_in, window, band, taylor, out, s);
+    case 14: return launch_l<14>(filter, na, in, len, h_in, window, band, taylor, out, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -689,7 +757,6 @@ struct sarbp_rc_plan_s {
     sarbp_rc_params p{};
     int n = 0, log2n = 0;
     int device = -1;
-    float2* tw = nullptr;      // per-span twiddle rows, 4 N entries
     float2* h = nullptr;       // N filter coefficients / N, natural order
 };
 
@@ -708,7 +775,7 @@ bool rc_plan_shape(const sarbp_rc_plan_s* rc, int* na, int* ns, int* device)
 cudaError_t launch_rc_table(const sarbp_rc_plan_s* rc, const BpConst& k, const float2* raw,
                             const double* pos, float4* table, int* klo, cudaStream_t s)
 {
-    return launch_table_any(rc->log2n, k, raw, rc->tw, rc->h, pos, table, klo, s);
+    return launch_table_any(rc->log2n, k, raw, rc->h, pos, table, klo, s);
 }
 
 }  // namespace sarbp
@@ -755,35 +822,13 @@ sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const
     }
     if (e == cudaSuccess)
         e = set_smem(log2n);
-    // per-span twiddle rows: span ns (a power of two) at offset 4 (ns - 1),
-    // rows t = 1, 4, 8, 12 of exp(-2 pi i t k / (ns r)), r = min(16, N / ns),
-    // computed in float64 and rounded once
-    const size_t tw_entries = 4 * (size_t)plan->n;
-    if (e == cudaSuccess)
-        e = sarbp::device_alloc(reinterpret_cast<void**>(&plan->tw), tw_entries * sizeof(float2));
     if (e == cudaSuccess)
         e = sarbp::device_alloc(reinterpret_cast<void**>(&plan->h), (size_t)plan->n * sizeof(float2));
-    if (e == cudaSuccess) {
-        std::vector<float2> tw(tw_entries, make_float2(0.f, 0.f));
-        const double pi = 3.14159265358979323846;
-        const int powers[4] = {1, 4, 8, 12};
-        for (int ns = 1; ns < plan->n; ns *= 2) {
-            const int r = plan->n / ns < 16 ? plan->n / ns : 16;
-            for (int row = 0; row < 4; ++row)
-                for (int k = 0; k < ns; ++k) {
-                    const double a = -2.0 * pi * (double)powers[row] * (double)k / ((double)ns * r);
-                    tw[4 * (size_t)(ns - 1) + (size_t)row * ns + k] =
-                        make_float2((float)std::cos(a), (float)std::sin(a));
-                }
-        }
-        e = cudaMemcpy(plan->tw, tw.data(), tw.size() * sizeof(float2), cudaMemcpyHostToDevice);
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (e == cudaSuccess)
-        e = launch(log2n, true, 1, static_cast<const float2*>(ref), p->nref, plan->tw, nullptr,
+        e = launch(log2n, true, 1, static_cast<const float2*>(ref), p->nref, nullptr,
                    p->window, (float)p->band_fraction, taylor_coefficients(), plan->h, s);
     if (e != cudaSuccess) {
-        cudaFree(plan->tw);
         cudaFree(plan->h);
         delete plan;
         return e == cudaErrorMemoryAllocation ? SARBP_ERR_OOM : SARBP_ERR_CUDA;
@@ -805,7 +850,7 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device)
         return SARBP_ERR_INVALID_ARG;
-    return launch(plan->log2n, false, p.na, static_cast<const float2*>(raw), p.ns, plan->tw, plan->h,
+    return launch(plan->log2n, false, p.na, static_cast<const float2*>(raw), p.ns, plan->h,
                   p.window, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f), static_cast<float2*>(out),
                   static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
@@ -816,7 +861,6 @@ sarbp_status sarbp_range_compress(sarbp_rc_plan_t plan, void* out, const void* r
 sarbp_status sarbp_rc_destroy(sarbp_rc_plan_t plan)
 {
     if (plan) {
-        cudaFree(plan->tw);
         cudaFree(plan->h);
         delete plan;
     }
