@@ -191,6 +191,9 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     k.qmax3 = tile_qmax3(p->dx, p->dy, plan->h_max - plan->h_min);
     k.h_lo_f = (float)plan->h_min;
     k.h_hi_f = (float)plan->h_max;
+    const double h_mid = 0.5 * (plan->h_min + plan->h_max);
+    k.h_mid_f = (float)h_mid;
+    k.h_mid_lo = (float)(h_mid - (double)k.h_mid_f);
     k.dy_lo = (float)(p->dy - (double)k.dy_f);
     k.r0_hi = (float)p->r0;
     k.r0_lo = (float)(p->r0 - (double)k.r0_hi);

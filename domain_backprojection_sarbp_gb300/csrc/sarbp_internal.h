@@ -66,6 +66,7 @@ struct BpConst {
     double qmax3;                // tile reach including height offsets from the mid height
     double z_mid;                // z0 + mid height: records are built on this plane
     float h_lo_f, h_hi_f;        // height bounds; the kernel clamps heights into them
+    float h_mid_f, h_mid_lo;     // mid height (z_mid - z0) as a float pair (hi + lo)
     float dy_lo;                 // dy - dy_f
     float r0_hi, r0_lo;          // r0 as a float pair (hi + lo)
     float idr_hi, idr_lo;        // 1 / dr as a float pair

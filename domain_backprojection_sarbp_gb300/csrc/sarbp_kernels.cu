@@ -343,16 +343,26 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             rec.c = make_float4(c12, c13, c20, c21);
             rec.d = make_float4(c22, __int_as_float(-lo), __int_as_float((int)kb), 0.f);
             if (k.heights_mode) {
-                // height map: the antenna-to-tile-centre vector as float pairs,
-                // with its z part taken from z0 (each row adds its own height)
-                const double vz0 = k.z0 - az;
-                const float vxh = f32(vx), vyh = f32(vy), vzh = f32(vz0);
-                rec.a = make_float4(vxh, f32(vx - (double)vxh), vyh, f32(vy - (double)vyh));
-                rec.b = make_float4(vzh, f32(vz0 - (double)vzh), 0.f, 0.f);
-                rec.c = make_float4(0.f, 0.f, 0.f, 0.f);
-                rec.d.x = 0.f;
-                rec.d.z = 0.f;
-                kind = REC_EXACT;
+                // height map: a row's reference point is offset from the tile
+                // centre (at the mid height) by q = (0, Y, Z), Y = j dy, Z its
+                // height above the mid height. The record carries what its
+                // range expansion to fourth order in |q| / R needs (see
+                // heights_row_curvature): the tile-centre bin and fraction,
+                // the linear terms gy dy / dr and gz / dr as float pairs, gy,
+                // gz, 1 / R, and v_x, v_z and R for the per-pixel series. The
+                // order-5 remainder is at most |q|^5 / R^4 (|q| <= qmax3);
+                // where that exceeds the fast-path tolerance the row takes
+                // the float64 path.
+                const double gz = vz * ir;
+                const double bz = gz * k.inv_dr;
+                const float bzh = f32(bz);
+                const double q5 = pow(k.qmax3, 5.0) * ir * ir * ir * ir * k.inv_dr;
+                const bool hfast = r > 8.0 * k.qmax3 && q5 <= k.fast_tol_bins;
+                rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), bzh);
+                rec.b = make_float4(f32(bz - (double)bzh), gyf, f32(gz), irf);
+                rec.c = make_float4(f32(vx), f32(vz), f32(r), 0.f);
+                rec.d = make_float4(0.f, __int_as_float(-lo), __int_as_float((int)kb), 0.f);
+                kind = hfast ? REC_FAST : REC_EXACT;
             }
         }
     }
@@ -407,8 +417,10 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
                                                   const float4* row, float jf)
 {
     if (on_heights(INTERP)) {
+        // height map: the row's range expansion (MODE_GATHER) or the float64 path
         PulseState st;
-        st.mode = __float_as_int(rec.d.w) == REC_SKIP ? MODE_SKIP : MODE_EXACT;
+        const int kind = __float_as_int(rec.d.w);
+        st.mode = kind == REC_FAST ? MODE_GATHER : (kind == REC_EXACT ? MODE_EXACT : MODE_SKIP);
         return st;
     }
     // u(i) = E0 + i E1 + i^2 E2 for this thread's row j; the large c01 j term
@@ -696,10 +708,6 @@ __device__ __forceinline__ float2 sinc_value(float ub, int kb, const float4* row
 }
 
 // Complex a x + b y, with real weights a, b.
-__device__ __forceinline__ float2 cmix(float a, float2 x, float b, float2 y)
-{
-    return make_float2(fmaf(a, x.x, b * y.x), fmaf(a, x.y, b * y.y));
-}
 __device__ __forceinline__ float2 cmix3(float a, float2 x, float b, float2 y, float c, float2 z)
 {
     return make_float2(fmaf(a, x.x, fmaf(b, y.x, c * z.x)), fmaf(a, x.y, fmaf(b, y.y, c * z.y)));
@@ -1080,6 +1088,8 @@ struct HRow {
     float qm;      // largest |q| over the row's pixels
     float jy;      // row offset from the tile centre, in pixels
     double zrow;   // z0 + hrow
+    float zh, zl;  // Z = hrow - mid height as a float pair
+    float qq;      // Y^2 + Z^2, Y = jy dy: squared offset of the row's reference point
     float dz_lo, dz_hi;   // range of h - hrow over the row's pixels
     float p_lo, p_hi;     // range of (i dx)^2 + (h - hrow)^2
 };
@@ -1094,44 +1104,6 @@ __device__ __forceinline__ F2 two_sum(float a, float b)
     const float bb = __fsub_rn(s, a);
     const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
     return {s, e};
-}
-__device__ __forceinline__ F2 fast_two_sum(float a, float b)
-{
-    const float s = __fadd_rn(a, b);
-    return {s, __fsub_rn(b, __fsub_rn(s, a))};
-}
-__device__ __forceinline__ F2 two_prod(float a, float b)
-{
-    const float p = __fmul_rn(a, b);
-    return {p, fmaf(a, b, -p)};
-}
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b)
-{
-    F2 s = two_sum(a.hi, b.hi);
-    const F2 t = two_sum(a.lo, b.lo);
-    s.lo = __fadd_rn(s.lo, t.hi);
-    s = fast_two_sum(s.hi, s.lo);
-    s.lo = __fadd_rn(s.lo, t.lo);
-    return fast_two_sum(s.hi, s.lo);
-}
-__device__ __forceinline__ F2 f2_mul(F2 a, F2 b)
-{
-    F2 p = two_prod(a.hi, b.hi);
-    p.lo = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, p.lo));
-    return fast_two_sum(p.hi, p.lo);
-}
-__device__ __forceinline__ F2 f2_sqr(F2 a)
-{
-    F2 p = two_prod(a.hi, a.hi);
-    p.lo = fmaf(2.0f * a.hi, a.lo, p.lo);
-    return fast_two_sum(p.hi, p.lo);
-}
-__device__ __forceinline__ F2 f2_sqrt(F2 a)
-{
-    const float x = __fsqrt_rn(a.hi);
-    const F2 p = two_prod(x, x);
-    const float d = __fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo);
-    return fast_two_sum(x, __fmul_rn(d, __fdiv_rn(0.5f, x)));
 }
 
 // Returns false (and leaves the sums untouched) when the series does not apply.
@@ -1245,6 +1217,23 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
     }
 }
 
+// Range from the tile centre (at the mid height) to a row's reference point,
+// offset by q = (0, Y, Z), Y = jy dy: with g = v / R, L = g.q = gy Y + gz Z and
+// Q = |q|^2, |v + q| - R = L + (Q - L^2) / (2R) - L (Q - L^2) / (2R^2)
+//   + (-Q^2 / 8 + 3 L^2 Q / 4 - 5 L^4 / 8) / R^3 + O(|q|^5 / R^4).
+// This is the part beyond the linear term L, in metres (small enough for
+// float32; the linear term is taken in split precision by the caller).
+__device__ __forceinline__ float heights_row_curvature(const Record& rec, const HRow& hr, float dy)
+{
+    const float L = fmaf(rec.b.y, hr.jy * dy, rec.b.z * hr.zh);
+    const float ir = rec.b.w;
+    const float L2 = L * L;
+    const float P = hr.qq - L2;                            // |q|^2 - (g.q)^2 >= 0
+    const float o4 = fmaf(hr.qq, fmaf(-0.125f, hr.qq, 0.75f * L2), -0.625f * L2 * L2);
+    // ((o4 / R - L P / 2) / R + P / 2) / R
+    return fmaf(fmaf(o4, ir, -0.5f * L * P), ir, 0.5f * P) * ir;
+}
+
 template <int INTERP>
 __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Record& rec,
                                                      const float4* row, const HRow& hr,
@@ -1252,27 +1241,27 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
                                                      const float2* __restrict__ psi,
                                                      float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    // reference vector: tile centre -> row centre -> row height
-    const F2 vx = {rec.a.x, rec.a.y};
-    const F2 yo = f2_add(two_prod(hr.jy, k.dy_f), two_prod(hr.jy, k.dy_lo));
-    const F2 vy = f2_add({rec.a.z, rec.a.w}, yo);
-    const F2 vz = f2_add({rec.b.x, rec.b.y}, {hr.hrow, 0.0f});
-    const F2 r2 = f2_add(f2_add(f2_sqr(vx), f2_sqr(vy)), f2_sqr(vz));
-    const F2 r = f2_sqrt(r2);
-    const F2 u = f2_mul(f2_add(r, {-k.r0_hi, -k.r0_lo}), {k.idr_hi, k.idr_lo});
-    if (!(fabsf(u.hi) < 1.0e7f))
-        return true;                              // far outside any window: nothing to add
-    float ku = floorf(u.hi);
-    float frac = __fadd_rn(__fsub_rn(u.hi, ku), u.lo);
-    const float kf = floorf(frac);                // -1, 0 or 1 after the lo part
-    ku += kf;
+    // the row's reference point, by the range expansion about the tile centre
+    const float curv = heights_row_curvature(rec, hr, k.dy_f);
+    const float R = rec.c.z + fmaf(rec.b.y, hr.jy * k.dy_f, fmaf(rec.b.z, hr.zh, curv));
+    // u_row = kb + (c01 j + bz Z) + c00 + curv / dr, the linear terms as float
+    // pairs with their integer part kept apart
+    const float jf = hr.jy;
+    const float h1 = rec.a.y * jf;
+    const float l1 = fmaf(rec.a.z, jf, fmaf(rec.a.y, jf, -h1));
+    const float h2 = rec.a.w * hr.zh;
+    const float l2 = fmaf(rec.a.w, hr.zl, fmaf(rec.b.x, hr.zh, fmaf(rec.a.w, hr.zh, -h2)));
+    const F2 sl = two_sum(h1, h2);
+    const float tr = sl.hi + MAGIC;
+    const float ki = tr - MAGIC;
+    float frac = (((sl.hi - ki) + sl.lo) + (l1 + l2)) + fmaf(curv, k.inv_dr_f, rec.a.x);
+    const float kf = floorf(frac);
     frac -= kf;
-    const float R = r.hi;
     const float t_bound = hr.qm * (2.0f * R + hr.qm) / (R * R);
     if (!(t_bound <= 0.01f))
         return false;
     const int bin0 = __float_as_int(rec.d.y);
-    const int kbase = (int)ku + bin0;
+    const int kbase = __float_as_int(rec.d.z) + (__float_as_int(tr) - MAGIC_BITS) + (int)kf;
     const float inv_r = __fdiv_rn(1.0f, R);
     const float g = inv_r * inv_r;                // 1 / R^2
     const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
@@ -1283,13 +1272,14 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
     // a1 s + a2 s^2 + a3 s^3 + a4 s^4 with a_n = hb g^(n-1) c_n. Its s^4 term
     // adds at most (4 pi R / lambda) (5/128) t^4 radians of phase; pulses where
     // that is below 1e-5 rad leave it out.
-    const float ax = 2.0f * vx.hi * k.dx_f;
+    const float vzr = rec.c.y + hr.zh;              // v_z at the row's height
+    const float ax = 2.0f * rec.c.x * k.dx_f;
     const float tb2 = t_bound * t_bound;
     const bool deg4 = k.c_phase * R * k.inv_dr_f * 0.0390625f * tb2 * tb2 > 1.0e-5f;
     if (INTERP == INTERP_HEIGHTS) {
         // bounds of s over the row from the row's ranges of dz and P; u grows
         // with s (s poly(s) is increasing for |s| / R^2 <= 0.01)
-        const float tvz = 2.0f * vz.hi;
+        const float tvz = 2.0f * vzr;
         const float sx = -k.i0 * fabsf(ax);
         const float s_lo = -sx + fminf(tvz * hr.dz_lo, tvz * hr.dz_hi) + hr.p_lo;
         const float s_hi = sx + fmaxf(tvz * hr.dz_lo, tvz * hr.dz_hi) + hr.p_hi;
@@ -1312,10 +1302,10 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
         }
     }
     if (deg4)
-        heights_series_loop<INTERP, true>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vz.hi, hb, g,
+        heights_series_loop<INTERP, true>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vzr, hb, g,
                                           accre, accim);
     else
-        heights_series_loop<INTERP, false>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vz.hi, hb, g,
+        heights_series_loop<INTERP, false>(k, row, s_hp, psi, kbase, bin0, frac, ax, 2.0f * vzr, hb, g,
                                            accre, accim);
     return true;
 }
@@ -1398,9 +1388,11 @@ __device__ __forceinline__ void apply_pulse(const BpConst& k, const PulseState& 
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
     if (on_heights(INTERP)) {
-        if (st.mode == MODE_EXACT &&
-            !heights_series_pulse<INTERP>(k, rec, row, hr, s_hp, psi, accre, accim))
-            heights_exact_pulse<INTERP>(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), hr, s_hp, psi, accre, accim);
+        if (st.mode == MODE_EXACT ||
+            (st.mode == MODE_GATHER &&
+             !heights_series_pulse<INTERP>(k, rec, row, hr, s_hp, psi, accre, accim)))
+            heights_exact_pulse<INTERP>(k, rec, row, a, tile_xc(k, col0), row_y(k, rowi), hr, s_hp,
+                                        psi, accre, accim);
         return;
     }
     if (INTERP == INTERP_NEAREST) {
@@ -1480,7 +1472,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const int col0 = (int)(t % k.tiles_x) * TILE_X;
         const int row0 = (int)(t / k.tiles_x) * TILE_Y;
         const int rowi = row0 + jr;
-        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0, 0.0f, 0.0f, 0.0f, 0.0f};
+        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         if (on_heights(INTERP)) {
             // the thread's own row of the tile, heights clamped to the plan's
             // bounds; pixels outside the image repeat the last row or column
@@ -1516,6 +1508,11 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const float hx = 0.5f * (TILE_X - 1) * k.dx_f;
             hr.qm = 1.0001f * sqrtf(hx * hx + dzm * dzm);
             hr.zrow = k.z0 + (double)hr.hrow;
+            const F2 zp = two_sum(hr.hrow, -k.h_mid_f);
+            hr.zh = zp.hi;
+            hr.zl = zp.lo - k.h_mid_lo;
+            const float yy = hr.jy * k.dy_f;
+            hr.qq = fmaf(yy, yy, hr.zh * hr.zh);
         }
         float2 accre[NP], accim[NP];
 #pragma unroll
