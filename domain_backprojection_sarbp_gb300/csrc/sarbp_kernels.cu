@@ -1087,7 +1087,6 @@ struct HRow {
     float hrow;    // the row's reference height (mean of its pixels)
     float qm;      // largest |q| over the row's pixels
     float jy;      // row offset from the tile centre, in pixels
-    double zrow;   // z0 + hrow
     float zh, zl;  // Z = hrow - mid height as a float pair
     float qq;      // Y^2 + Z^2, Y = jy dy: squared offset of the row's reference point
     float dz_lo, dz_hi;   // range of h - hrow over the row's pixels
@@ -1146,6 +1145,9 @@ __device__ __forceinline__ void heights_series_loop(const BpConst& k, const floa
                 nearest_pixel<true>(k, ub.x, kbase, row, accre[q].x, accim[q].x);
                 nearest_pixel<true>(k, ub.y, kbase, row, accre[q].y, accim[q].y);
             }
+            // keep the next pair's table loads from being hoisted above this
+            // pair's arithmetic: bounds the registers held in flight
+            asm volatile("" ::: "memory");
             continue;
         }
         const float2 tt = __fadd2_rd(ub, mm);
@@ -1257,12 +1259,14 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
     float frac = (((sl.hi - ki) + sl.lo) + (l1 + l2)) + fmaf(curv, k.inv_dr_f, rec.a.x);
     const float kf = floorf(frac);
     frac -= kf;
-    const float t_bound = hr.qm * (2.0f * R + hr.qm) / (R * R);
+    // 1 / R to float precision: the SFU reciprocal and one Newton step
+    const float r0i = rcp_approx(R);
+    const float inv_r = fmaf(r0i, fmaf(-R, r0i, 1.0f), r0i);
+    const float t_bound = hr.qm * (2.0f * R + hr.qm) * (inv_r * inv_r);
     if (!(t_bound <= 0.01f))
         return false;
     const int bin0 = __float_as_int(rec.d.y);
     const int kbase = __float_as_int(rec.d.z) + (__float_as_int(tr) - MAGIC_BITS) + (int)kf;
-    const float inv_r = __fdiv_rn(1.0f, R);
     const float g = inv_r * inv_r;                // 1 / R^2
     const float hb = 0.5f * inv_r * k.inv_dr_f;   // bins per metre of s, first order
 
@@ -1320,7 +1324,7 @@ __device__ __forceinline__ void heights_exact_pulse(const BpConst& k, const Reco
                                                     const float2* __restrict__ psi,
                                                     float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    const double vx = xc - a[0], vy = yrow - a[1], vz = hr.zrow - a[2];
+    const double vx = xc - a[0], vy = yrow - a[1], vz = (k.z0 + (double)hr.hrow) - a[2];
     const double r2 = vx * vx + vy * vy + vz * vz;
     const double r = sqrt(r2);
     const double u = (r - k.r0) * k.inv_dr;
@@ -1472,7 +1476,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
         const int col0 = (int)(t % k.tiles_x) * TILE_X;
         const int row0 = (int)(t / k.tiles_x) * TILE_Y;
         const int rowi = row0 + jr;
-        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), k.z0, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        HRow hr{0.0f, 0.0f, (float)jr - 0.5f * (TILE_Y - 1), 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         if (on_heights(INTERP)) {
             // the thread's own row of the tile, heights clamped to the plan's
             // bounds; pixels outside the image repeat the last row or column
@@ -1507,7 +1511,6 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             }
             const float hx = 0.5f * (TILE_X - 1) * k.dx_f;
             hr.qm = 1.0001f * sqrtf(hx * hx + dzm * dzm);
-            hr.zrow = k.z0 + (double)hr.hrow;
             const F2 zp = two_sum(hr.hrow, -k.h_mid_f);
             hr.zh = zp.hi;
             hr.zl = zp.lo - k.h_mid_lo;
