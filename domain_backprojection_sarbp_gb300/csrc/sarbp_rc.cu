@@ -13,19 +13,25 @@
 // |f| <= b/2 (f in cycles per sample), zero outside it.
 //
 // One CTA per pulse. The transforms are self-sorting (Stockham) passes of
-// radix 16 held in registers (16 complex values per thread), plus one pass of
-// radix 2, 4 or 8 when log2 N is not a multiple of 4 (for N = 2 16^m the
-// radix-2 pass and its radix-16 neighbour run as one radix-32 pass with two
-// threads per butterfly, saving an exchange in each direction); shared memory only
-// carries the data between passes, as float2 values padded by one slot
-// every 16 (conflict-free for the strides used). The
-// forward transform takes the raw row straight from global memory (zero
-// beyond ns) and its last pass leaves each thread holding the spectrum at
-// indices j + t N/16, which are exactly the inputs of the inverse transform's
-// first pass: the filter multiply happens there in registers, with no trip
-// through shared memory. The inverse's last pass writes natural-order samples
-// straight to global memory. The filter spectrum H (conj FFT of the reference
-// times the window, divided by N) is built once by the plan, in natural order.
+// radix 16 held in registers, plus one pass of radix 2, 4, 8 or 32 when log2 N
+// is not a multiple of 4. For N = 2 16^m (N = 8192 for 4096-sample rows) a
+// thread holds 32 values: the radix-32 pass is one thread's own DFT (two
+// radix-16 DFTs and a radix-2 step; when the second half of the zero-padded
+// input is empty, just the two DFTs), and each thread takes two radix-16
+// butterflies per pass after it. Shared memory only carries the data between
+// passes, as float2 values padded by one slot every 16. The input twiddles of
+// a pass, exp(-2 pi i t k / (NS R)), come from the SFU (whose sine and cosine
+// units the transform leaves idle) for t = 1, 4, 8, 12 (and 16 for radix 32)
+// and as products for the other powers. The forward transform takes the raw
+// row straight from global memory (zero beyond ns, not kept in L1) and its
+// last pass leaves each thread holding the spectrum at indices j + t N/16,
+// which are exactly the inputs of the inverse transform's first pass: the
+// filter multiply happens there in registers, with no trip through shared
+// memory. The inverse's last pass writes natural-order samples straight to
+// global memory, or, fused with a backprojection plan's echo table, keeps
+// the band of samples the table row needs in shared memory. The filter
+// spectrum H (conj FFT of the reference times the window, divided by N) is
+// built once by the plan, in natural order.
 #include "../../include/sarbp.h"
 #include "sarbp_device.cuh"
 #include "sarbp_internal.h"

@@ -358,9 +358,10 @@ typedef struct sarbp_rc_params {
 
 typedef struct sarbp_rc_plan_s* sarbp_rc_plan_t;
 
-/* Build the filter spectrum from `ref` (device, complex64 [nref], read only
-   during this call's work on `stream`) and allocate twiddles (N x 16 bytes).
-   INVALID_ARG for bad sizes, N > 16384, an unknown window or b outside (0, 1]. */
+/* Build the filter spectrum (N x 8 bytes of device memory, the plan's only
+   allocation) from `ref` (device, complex64 [nref], read only during this
+   call's work on `stream`). INVALID_ARG for bad sizes, N > 16384, an unknown
+   window or b outside (0, 1]; SARBP_ERR_OOM if the allocation fails. */
 sarbp_status sarbp_rc_plan(sarbp_rc_plan_t* out, const sarbp_rc_params* p, const void* ref,
                            void* stream);
 
