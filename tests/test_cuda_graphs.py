@@ -1,7 +1,8 @@
 """The device entry points captured into CUDA graphs.
 
-Once a plan exists, sarbp_backproject and sarbp_range_compress only enqueue
-kernels on the caller's stream (no allocation, no synchronisation), so a
+Once a plan exists, sarbp_backproject, sarbp_range_compress and
+sarbp_backproject_raw only enqueue kernels on the caller's stream (no
+allocation, no synchronisation), so a
 stream capture records them into a graph whose replays must give the eager
 result bit for bit: the whole range-compression -> backprojection pipeline
 then runs as one graph launch.
@@ -98,6 +99,42 @@ def test_pipeline_graph(scene):
             s = torch.cuda.current_stream()
             rc(rc_out, raw_buf, stream=s)
             plan.backproject(img, rc_out, pos, stream=s)
+        for f, w in zip(frames, want):
+            raw_buf.copy_(f)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(img, w)
+    assert not torch.equal(want[0], want[1])
+
+
+def test_raw_entry_point_graph(scene):
+    """sarbp_backproject_raw (compression fused with the echo table) captured
+    into a graph: replays equal the eager call bit for bit, for two raw frames
+    copied into the captured input."""
+    p = scene.params
+    ref = _dev(chirp.chirp().astype(np.complex64))
+    tgt = np.array([[0.0, 0.0, 0.0], [12.0, -20.0, 0.0]])
+    frames = [_dev(chirp.raw_echoes(scene.antenna_pos, tgt, np.array([amp, 1.0]), p["r0"],
+                                    p["nr"]).astype(np.complex64)) for amp in (1.0, 0.5)]
+    pos = _dev(scene.antenna_pos)
+    raw_buf = frames[0].clone()
+    img = torch.empty((p["ny"], p["nx"]), dtype=torch.complex64, device=DEV)
+    with RangeCompressor(ref, p["na"], p["nr"], "hamming", 0.8) as rc, Plan(p) as plan:
+        want = []
+        for f in frames:
+            im = torch.empty_like(img)
+            plan.backproject_raw(im, f, pos, rc)
+            torch.cuda.synchronize()
+            want.append(im)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            plan.backproject_raw(img, raw_buf, pos, rc, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.backproject_raw(img, raw_buf, pos, rc, stream=torch.cuda.current_stream())
         for f, w in zip(frames, want):
             raw_buf.copy_(f)
             g.replay()

@@ -122,8 +122,11 @@ def _raw_scene(nr, na=64, nx=64, ny=64):
     return sc, raw.astype(np.complex64)
 
 
-# FFT sizes 1024 (first pass of radix 4) and 8192 (merged radix-32 passes)
-@pytest.mark.parametrize("nr", [512, 4096])
+# FFT sizes 512 (radix-32 first pass, one pass of radix 16), 1024 (first pass of
+# radix 4) and 8192 (radix 32, 16, 16); up to 512 bins the table rows of this
+# 64 x 64 image (one 512-row tile) span the whole range axis, so the band kept
+# in shared memory is the whole row; at 4096 it is a window of it
+@pytest.mark.parametrize("nr", [128, 256, 512, 4096])
 def test_raw_entry_point(nr):
     """sarbp_backproject_raw (range compression fused with the echo table)
     against the oracle's range compression followed by its backprojection,
@@ -131,6 +134,9 @@ def test_raw_entry_point(nr):
     non-finite antenna position and contributes nothing."""
     sc, raw = _raw_scene(nr)
     p = sc.params
+    with Plan(p) as probe:
+        full = probe.describe()["full_window"]
+    assert full == (1 if nr <= 512 else 0), (nr, full)
     pos_np = sc.antenna_pos.copy()
     pos_np[7] = np.nan
     ref = chirp.chirp().astype(np.complex64)
@@ -175,4 +181,9 @@ def test_raw_entry_point_accumulates_and_checks_plans():
     with RangeCompressor(ref, p["na"], p["nr"] - 1) as rc_other, Plan(p) as plan:
         with pytest.raises(SarbpError) as err:
             plan.backproject_raw(img, r, pos, rc_other)
+        assert err.value.status == _native.SARBP_ERR_PLAN_MISMATCH
+    # a height-map plan
+    with RangeCompressor(ref, p["na"], p["nr"]) as rc, Plan(p, height_range=(0.0, 5.0)) as hplan:
+        with pytest.raises(SarbpError) as err:
+            hplan.backproject_raw(img, r, pos, rc)
         assert err.value.status == _native.SARBP_ERR_PLAN_MISMATCH
