@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(256) psi_kernel(BpConst k, float2* __restrict_
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float f32(double v) { return __double2float_rn(v); }
 
-__device__ void make_record(const BpConst& k, const double* __restrict__ pos,
+template <int INTERP>
+__device__ __forceinline__ void make_record(const BpConst& k, const double* __restrict__ pos,
                             const int* __restrict__ klo, int n, double xc, double yc,
                             Record& out)
 {
@@ -267,10 +268,15 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
     const double ay = pos[3 * (size_t)n + 1];
     const double az = pos[3 * (size_t)n + 2];
     const int lo = klo[n];
-    const double vx = xc - ax, vy = yc - ay, vz = (k.heights_mode ? k.z_mid : k.z0) - az;
+    // the height-map kernels (plans of sarbp_plan_heights only) build their
+    // records about the mid height, the planar ones on the image plane. The
+    // linear kernel keeps this a run-time test of the plan (always false
+    // there): compiled that way its register allocation has no spills.
+    const bool HM = on_heights(INTERP) || (INTERP == INTERP_LINEAR && k.heights_mode);
+    const double vx = xc - ax, vy = yc - ay, vz = (HM ? k.z_mid : k.z0) - az;
     const double r2 = vx * vx + vy * vy + vz * vz;
     const double r = sqrt(r2);
-    const double reach = k.heights_mode ? k.qmax3 : k.qmax;
+    const double reach = HM ? k.qmax3 : k.qmax;
     int kind = REC_SKIP;
     Record rec;
     rec.a = rec.b = rec.c = rec.d = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -342,7 +348,7 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
             rec.b = make_float4(c03, c04, c10, c11);
             rec.c = make_float4(c12, c13, c20, c21);
             rec.d = make_float4(c22, __int_as_float(-lo), __int_as_float((int)kb), 0.f);
-            if (k.heights_mode) {
+            if (HM) {
                 // height map: a row's reference point is offset from the tile
                 // centre (at the mid height) by q = (0, Y, Z), Y = j dy, Z its
                 // height above the mid height. The record carries what its
@@ -356,7 +362,8 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
                 const double gz = vz * ir;
                 const double bz = gz * k.inv_dr;
                 const float bzh = f32(bz);
-                const double q5 = pow(k.qmax3, 5.0) * ir * ir * ir * ir * k.inv_dr;
+                const double qr = k.qmax3 * ir;
+                const double q5 = qr * qr * qr * qr * k.qmax3 * k.inv_dr;   // |q|^5 / R^4, bins
                 const bool hfast = r > 8.0 * k.qmax3 && q5 <= k.fast_tol_bins;
                 rec.a = make_float4(f32(u - kt), c01h, f32(c01 - (double)c01h), bzh);
                 rec.b = make_float4(f32(bz - (double)bzh), gyf, f32(gz), irf);
@@ -368,6 +375,19 @@ __device__ void make_record(const BpConst& k, const double* __restrict__ pos,
     }
     rec.d.w = __int_as_float(kind);
     out = rec;
+}
+
+// The record builder as a call of its own (one thread per pulse, once per
+// chunk of 512 pulses) for the nearest and height-map kernels: their main
+// loops' register allocation then does not have to make room for its float64
+// work (fewer spilled bytes, and 1-2 % faster). The linear and sinc kernels
+// inline it (as a call it cost the linear kernel 5 %).
+template <int INTERP>
+__device__ __noinline__ void make_record_call(const BpConst& k, const double* __restrict__ pos,
+                                              const int* __restrict__ klo, int n, double xc,
+                                              double yc, Record& out)
+{
+    make_record<INTERP>(k, pos, klo, n, xc, yc, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -1528,8 +1548,14 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             const int cnt = min(CHUNK, n1 - c0);
             __syncthreads();
             if (tid < cnt)
-                make_record(k, pos, klo, c0 + tid, tile_xc(k, col0),
-                            k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy, s_rec[tid]);
+            {
+                const double xct = tile_xc(k, col0);
+                const double yct = k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy;
+                if (is_sinc(INTERP) || INTERP == INTERP_LINEAR)
+                    make_record<INTERP>(k, pos, klo, c0 + tid, xct, yct, s_rec[tid]);
+                else
+                    make_record_call<INTERP>(k, pos, klo, c0 + tid, xct, yct, s_rec[tid]);
+            }
             __syncthreads();
             const int tw = row_pitch<INTERP>(k);
             const float4* rows = table + (size_t)c0 * tw;

@@ -267,21 +267,6 @@ __device__ __forceinline__ void twiddle_inputs(float2* v, int k)
 
 __host__ __device__ constexpr int pad(int i) { return i + (i >> 4); }
 
-// Rows ahead of its own that a CTA asks L2 to fetch: about a wave of CTAs
-// later the CTA of that row finds it in L2 instead of waiting on HBM.
-constexpr int RC_PREFETCH_AHEAD = 512;
-
-// One bulk L2 prefetch of raw row n (ns complex samples), if it exists and
-// starts and ends on 16-byte boundaries (ns even).
-__device__ __forceinline__ void prefetch_row_l2(const float2* raw, int ns, int n, int rows)
-{
-    if (threadIdx.x == 0 && n < rows && (ns & 1) == 0 &&
-        (reinterpret_cast<uintptr_t>(raw) & 15) == 0) {
-        const float2* p = raw + (size_t)n * ns;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(ns * 8) : "memory");
-    }
-}
-
 // A raw sample: read once, so it is not kept in L1, where the filter and
 // twiddle rows that every pulse reads should stay.
 __device__ __forceinline__ float2 ld_stream(const float2* p)
@@ -568,7 +553,6 @@ __global__ void __launch_bounds__(Fft<L>::T, Fft<L>::TABLE_MINB) rc_kernel(const
     extern __shared__ float2 smem[];
     const Row r{smem};
     const size_t row0 = (size_t)blockIdx.x * ns_in;
-    prefetch_row_l2(raw, ns_in, blockIdx.x + RC_PREFETCH_AHEAD, gridDim.x);
     float2 v[Fft<L>::EPT];
     forward_to_registers<L>(raw + row0, ns_in, r, v);
     filter_inverse<L>(r, v, h, GlobalOut{out + row0, ns_in});
@@ -609,7 +593,6 @@ __global__ void __launch_bounds__(Fft<L>::T, Fft<L>::TABLE_MINB) rc_table_kernel
     }
     const Row r{smem};
     const size_t row0 = (size_t)n * k.nr;
-    prefetch_row_l2(raw, k.nr, n + RC_PREFETCH_AHEAD, k.na);
     float2 v[Fft<L>::EPT];
     forward_to_registers<L>(raw + row0, k.nr, r, v);
     filter_inverse<L>(r, v, h, BandOut{smem, lo, k.W + 1, k.nr});
