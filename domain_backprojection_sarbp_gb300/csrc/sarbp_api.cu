@@ -177,6 +177,8 @@ BpConst make_const(const sarbp_plan_s* plan, const sarbp_params* p)
     const double turns = alpha - std::floor(alpha);      // exp(-j c) = exp(-j 2 pi frac(alpha))
     k.rot_re = (float)std::cos(2.0 * PI * turns);
     k.rot_im = (float)-std::sin(2.0 * PI * turns);
+    k.hrt_re = 0.5f * k.rot_re;                            // halving a float is exact
+    k.hrt_im = 0.5f * k.rot_im;
     const double half_turns = 0.5 * alpha - std::floor(0.5 * alpha);   // exp(+j c / 2)
     k.hrot_re = (float)std::cos(2.0 * PI * half_turns);
     k.hrot_im = (float)std::sin(2.0 * PI * half_turns);
@@ -392,11 +394,24 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         ev = &plan->events[plan->events_used++];
         cudaEventRecord(ev->first, s);
     }
-    if ((k.flags & SARBP_SINC8) && !plan->heights_mode) {
+    // The cost-weighted split takes one cell per (tile, pulse segment), at
+    // most SPLIT_CELLS of them; with more tiles than that (only narrow images
+    // of over 33 million rows) every CTA covers many whole tiles, and the
+    // even split serves.
+    const bool costed = plan->tiles <= SPLIT_CELLS;
+    if (costed && (k.flags & SARBP_SINC8) && !plan->heights_mode) {
         // the sinc kernels' cost varies across tiles: split the work by estimated cost
         auto* cum = reinterpret_cast<unsigned long long*>(plan->psi + plan->p.nr + 2);
         auto* starts = reinterpret_cast<long long*>(cum + SPLIT_CELLS + 1);
         e = launch_split(k, antenna_pos, sinc_wide, cum, starts, s);
+        if (e != cudaSuccess)
+            return cuda_fail(plan, e, "work-split kernel launch");
+        k.starts = starts;
+    } else if (costed && heights && (k.flags & (SARBP_SINC8 | SARBP_NEAREST))) {
+        // so does the height-map sinc and nearest kernels', with the terrain
+        auto* cum = reinterpret_cast<unsigned long long*>(plan->psi + plan->p.nr + 2);
+        auto* starts = reinterpret_cast<long long*>(cum + SPLIT_CELLS + 1);
+        e = launch_heights_split(k, antenna_pos, heights, cum, starts, s);
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "work-split kernel launch");
         k.starts = starts;

@@ -71,6 +71,7 @@ struct BpConst {
     float r0_hi, r0_lo;          // r0 as a float pair (hi + lo)
     float idr_hi, idr_lo;        // 1 / dr as a float pair
     float rot_re, rot_im;        // exp(-j c_phase): phase step from one bin to the next
+    float hrt_re, hrt_im;        // rot_re / 2, rot_im / 2
     float hrot_re, hrot_im;      // exp(+j c_phase / 2): phase across half a bin
     float i0;                    // column offset of a thread's first pixel from the tile centre
 };
@@ -89,9 +90,15 @@ cudaError_t prepare_kernels();
 // Cost-weighted CTA boundaries for the windowed-sinc kernels on a plane (after
 // the table kernel on the same stream, which sets sinc_wide): cum holds
 // SPLIT_CELLS + 1 words of scratch, starts receives ctas + 1 unit offsets.
+// Only for k.tiles <= SPLIT_CELLS (one cell per tile at least).
 constexpr int SPLIT_CELLS = 65536;         // (tile, pulse segment) cells of the cost estimate
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s);
+// The same for the height-map sinc and nearest kernels (k.flags says which),
+// whose cost follows the terrain: per-tile costs from the rows' height
+// statistics, then the split.
+cudaError_t launch_heights_split(const BpConst& k, const double* pos, const float* heights,
+                                 unsigned long long* cum, long long* starts, cudaStream_t s);
 // Range compression fused with the linear echo table (sarbp_rc.cu): for every
 // pulse the compressed samples of the table row's window only, written as the
 // row's entries, with klo as launch_table sets it. k describes the

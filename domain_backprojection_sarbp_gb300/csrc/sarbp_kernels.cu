@@ -542,7 +542,8 @@ __device__ __forceinline__ PulseState pulse_setup(const BpConst& k, const Record
 __device__ __forceinline__ void hinge_pulse(const BpConst& k, const PulseState& st,
                                             float2 (&accre)[NP], float2 (&accim)[NP])
 {
-    // B = conj(r) D0 with r = exp(-j c)
+    // B = conj(r) D0 with r = exp(-j c) (the hinge FMA form of the height-map
+    // kernel schedules worse here)
     const float bre = k.rot_re * st.t1d.x + k.rot_im * st.t1d.y;
     const float bim = k.rot_re * st.t1d.y - k.rot_im * st.t1d.x;
     const float d_re = 0.5f * (st.t0.z + bre), d_im = 0.5f * (st.t0.w + bim);
@@ -1207,10 +1208,13 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
     const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
     const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4, a4);
     const float2 y02 = make_float2(y0, y0);
-    const float bre = k.rot_re * t0.z + k.rot_im * t0.w;     // B = exp(j c) D0
-    const float bim = k.rot_re * t0.w - k.rot_im * t0.z;
-    const float d_re = 0.5f * (t1.z + bre), d_im = 0.5f * (t1.w + bim);
-    const float gre = 0.5f * (t1.z - bre), gim = 0.5f * (t1.w - bim);
+    // B / 2 = exp(j c) D0 / 2 (half the rotation from the constants), then the
+    // line and hinge slopes (D1 +- B) / 2 in one FMA each: the same bits as
+    // halving the sums
+    const float bre = k.hrt_re * t0.z + k.hrt_im * t0.w;
+    const float bim = k.hrt_re * t0.w - k.hrt_im * t0.z;
+    const float d_re = fmaf(0.5f, t1.z, bre), d_im = fmaf(0.5f, t1.w, bim);
+    const float gre = fmaf(0.5f, t1.z, -bre), gim = fmaf(0.5f, t1.w, -bim);
     const float2 are = make_float2(t1.x, t1.x), aim = make_float2(t1.y, t1.y);
     const float2 dre = make_float2(d_re, d_re), dim = make_float2(d_im, d_im);
     const float2 g_re = make_float2(gre, gre), g_im = make_float2(gim, gim);
@@ -1231,6 +1235,100 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
         float sa, ca, sb, cb;
         __sincosf(y.x, &sa, &ca);
         __sincosf(y.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(wr, cs, accre[q]);
+        accim[q] = __ffma2_rn(wr, sn, __ffma2_rn(wi, cs, accim[q]));
+        accre[q] = __ffma2_rn(make_float2(-wi.x, -wi.y), sn, accre[q]);
+    }
+}
+
+// Windowed sinc on a height map when the row's pixels span at most SINC_SPAN
+// bins: G is interpolated over [lo, hi] (row units, relative to kb) at NN
+// Chebyshev nodes as in the planar polynomial modes (same degrees, spans and
+// error bounds), and each pixel evaluates it at s_v = u - mid from the range
+// series; the echo phase is psi_k0 exp(j c (u - k0)), one angle per pixel.
+// a4 is the series' s^4 coefficient, or 0 where that term is left out.
+template <int NN>
+__device__ __forceinline__ void heights_sinc_poly(const BpConst& k, const float4* s_hp,
+                                                  const float4* row, int kb, float lo, float hi,
+                                                  float k0, int kabs0, float frac, float ax,
+                                                  float two_vz, float hb, float g, float a4,
+                                                  float2 (&accre)[NP], float2 (&accim)[NP])
+{
+    const float mid = 0.5f * (lo + hi), half = 0.5f * (hi - lo);
+    float2 p[SINC_MAXC], pr[SINC_MAXC], pi[SINC_MAXC];
+    poly_coeffs<NN>(mid, half, kb, row, p);
+    poly_scale<NN>(p, half, pr, pi);
+    constexpr float TWO_PI = 6.283185307f;
+    const float cm = fmaf(TWO_PI, bin_turns(k, kabs0), k.c_phase * (mid - k0));
+    const float2 c2 = make_float2(k.c_phase, k.c_phase), cm2 = make_float2(cm, cm);
+    const float2 ax2 = make_float2(ax, ax), tvz2 = make_float2(two_vz, two_vz);
+    const float a2 = -0.25f * hb * g, a3 = 0.125f * hb * g * g;
+    const float2 a12 = make_float2(hb, hb), a22 = make_float2(a2, a2);
+    const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4, a4);
+    const float2 f0 = make_float2(frac - mid, frac - mid);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float4 hp = s_hp[q];
+        const float2 s = __ffma2_rn(id, ax2, __ffma2_rn(make_float2(hp.x, hp.y), tvz2,
+                                                        make_float2(hp.z, hp.w)));
+        id = __fadd2_rn(id, one);
+        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12);
+        const float2 sv = __ffma2_rn(s, poly, f0);
+        float2 gr = pr[NN - 1], gi = pi[NN - 1];
+#pragma unroll
+        for (int n = NN - 2; n >= 0; --n) {
+            gr = __ffma2_rn(gr, sv, pr[n]);
+            gi = __ffma2_rn(gi, sv, pi[n]);
+        }
+        const float2 x = __ffma2_rn(sv, c2, cm2);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
+        const float2 cs = make_float2(ca, cb);
+        const float2 sn = make_float2(sa, sb);
+        accre[q] = __ffma2_rn(gr, cs, accre[q]);
+        accim[q] = __ffma2_rn(gr, sn, __ffma2_rn(gi, cs, accim[q]));
+        accre[q] = __ffma2_rn(make_float2(-gi.x, -gi.y), sn, accre[q]);
+    }
+}
+
+// Nearest sample on a height map when every pixel of the row rounds to bin kn
+// or kn + 1: the two-sample form of nearest_pair_pulse with
+// x = c (u - kn - 1/2) from the range series (c folded into its
+// coefficients, y0 = c (frac - kn - 1/2)); e is table entry (N_kn, M_kn).
+__device__ __forceinline__ void heights_nearest_pair(const BpConst& k, const float4* s_hp, float4 e,
+                                                     float y0, float ax, float two_vz, float hb,
+                                                     float g, float a4, float2 (&accre)[NP],
+                                                     float2 (&accim)[NP])
+{
+    const float c = k.c_phase;
+    const float2 ax2 = make_float2(ax, ax), tvz2 = make_float2(two_vz, two_vz);
+    const float a1 = c * hb, a2 = -0.25f * a1 * g, a3 = 0.125f * a1 * g * g, a4c = c * a4;
+    const float2 a12 = make_float2(a1, a1), a22 = make_float2(a2, a2);
+    const float2 a32 = make_float2(a3, a3), a42 = make_float2(a4c, a4c);
+    const float2 y02 = make_float2(y0, y0);
+    const float2 w0r2 = make_float2(e.x, e.x), w0i2 = make_float2(e.y, e.y);
+    const float2 dwr2 = make_float2(e.z, e.z), dwi2 = make_float2(e.w, e.w);
+    const float2 one = make_float2(1.0f, 1.0f);
+    float2 id = make_float2(k.i0, k.i0 + NP);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const float4 hp = s_hp[q];
+        const float2 s = __ffma2_rn(id, ax2, __ffma2_rn(make_float2(hp.x, hp.y), tvz2,
+                                                        make_float2(hp.z, hp.w)));
+        id = __fadd2_rn(id, one);
+        const float2 poly = __ffma2_rn(__ffma2_rn(__ffma2_rn(a42, s, a32), s, a22), s, a12);
+        const float2 x = __ffma2_rn(s, poly, y02);
+        const float2 h = make_float2(x.x >= 0.0f ? 1.0f : 0.0f, x.y >= 0.0f ? 1.0f : 0.0f);
+        const float2 wr = __ffma2_rn(h, dwr2, w0r2);
+        const float2 wi = __ffma2_rn(h, dwi2, w0i2);
+        float sa, ca, sb, cb;
+        __sincosf(x.x, &sa, &ca);
+        __sincosf(x.y, &sb, &cb);
         const float2 cs = make_float2(ca, cb);
         const float2 sn = make_float2(sa, sb);
         accre[q] = __ffma2_rn(wr, cs, accre[q]);
@@ -1300,7 +1398,7 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
     const float ax = 2.0f * rec.c.x * k.dx_f;
     const float tb2 = t_bound * t_bound;
     const bool deg4 = k.c_phase * R * k.inv_dr_f * 0.0390625f * tb2 * tb2 > 1.0e-5f;
-    if (INTERP == INTERP_HEIGHTS) {
+    {
         // bounds of s over the row from the row's ranges of dz and P; u grows
         // with s (s poly(s) is increasing for |s| / R^2 <= 0.01)
         const float tvz = 2.0f * vzr;
@@ -1313,8 +1411,8 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
         const float k0 = floorf(lo_u);
         const int idx0 = kbase + (int)k0;
         // both bins recorded (0 <= k <= nr - 2) and inside the row
-        if (hi_u - k0 < 2.0f && idx0 >= bin0 && idx0 + 1 <= bin0 + k.nr - 2 && idx0 >= 0 &&
-            idx0 + 1 <= k.W - 1) {
+        if (INTERP == INTERP_HEIGHTS && hi_u - k0 < 2.0f && idx0 >= bin0 &&
+            idx0 + 1 <= bin0 + k.nr - 2 && idx0 >= 0 && idx0 + 1 <= k.W - 1) {
             const float4 t0 = __ldg(row + idx0);
             const float4 t1 = __ldg(row + idx0 + 1);
             const float y0 = k.c_phase * ((frac - k0) - 1.0f);
@@ -1323,6 +1421,54 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
             else
                 heights_hinge_loop<false>(k, s_hp, t0, t1, y0, ax, tvz, hb, g, accre, accim);
             return true;
+        }
+        if (INTERP == INTERP_HEIGHTS_SINC8) {
+            // the row within SINC_SPAN6 bins, the stencils of its two bins
+            // recorded and both bins inside the row: one polynomial in u, of
+            // degree 2 to 6 by the span (the planar kernels' degrees and
+            // spans). The warp's polynomial rows take the highest degree any
+            // of them needs (on a narrower interval a higher degree is as
+            // accurate), so that a warp runs one polynomial path, not one per
+            // degree.
+            float lo_e, hi_e, k0e;
+            int kabs0;
+            const bool poly = poly_interval(k, kbase, bin0, lo_u, hi_u, SINC_SPAN6, lo_e, hi_e, k0e, kabs0) &&
+                              kabs0 + bin0 >= 0 && kabs0 + bin0 + 1 <= k.W - 1;
+            const float sp = hi_e - lo_e;
+            const int nn = !poly ? 0 : (sp <= SINC_SPAN2 ? 3 : sp <= SINC_SPAN3 ? 4 : sp <= SINC_SPAN ? 5 :
+                                       sp <= SINC_SPAN5 ? 6 : 7);
+            const int wn = __reduce_max_sync(__activemask(), nn);
+            if (poly) {
+                const float a4 = deg4 ? -0.078125f * hb * g * g * g : 0.0f;
+                if (wn <= 3)
+                    heights_sinc_poly<3>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
+                                         hb, g, a4, accre, accim);
+                else if (wn == 4)
+                    heights_sinc_poly<4>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
+                                         hb, g, a4, accre, accim);
+                else if (wn == 5)
+                    heights_sinc_poly<5>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
+                                         hb, g, a4, accre, accim);
+                else if (wn == 6)
+                    heights_sinc_poly<6>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
+                                         hb, g, a4, accre, accim);
+                else
+                    heights_sinc_poly<7>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
+                                         hb, g, a4, accre, accim);
+                return true;
+            }
+        }
+        if (INTERP == INTERP_HEIGHTS_NEAREST) {
+            // every pixel rounds to bin kn or kn + 1, entry kn inside the row
+            const float kn = floorf(lo_u + 0.5f);
+            const int idxn = kbase + (int)kn;
+            if (hi_u + 0.5f - kn < 2.0f && idxn >= 0 && idxn <= k.W - 1) {
+                const float4 e = __ldg(row + idxn);
+                const float y0 = k.c_phase * ((frac - kn) - 0.5f);
+                const float a4 = deg4 ? -0.078125f * hb * g * g * g : 0.0f;
+                heights_nearest_pair(k, s_hp, e, y0, ax, tvz, hb, g, a4, accre, accim);
+                return true;
+            }
         }
     }
     if (deg4)
@@ -1487,12 +1633,18 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
     const long long u1 = cta_start(k, b + 1);
     if (u0 >= u1)
         return;
-    const long long t_first = u0 / k.na;
-    const long long t_last = (u1 - 1) / k.na;
+    // The CTA's tiles and the pulse bounds in its first and last tile, as
+    // 32-bit values (tile indices and pulse counts fit): fewer registers held
+    // through the pulse loop than the 64-bit unit bounds (the wide sinc kernel
+    // 2 % faster, fewer spilled bytes)
+    const int t_first = (int)(u0 / k.na);
+    const int t_last = (int)((u1 - 1) / k.na);
+    const int n0_first = (int)(u0 - (long long)t_first * k.na);
+    const int n1_last = (int)(u1 - (long long)t_last * k.na);
 
-    for (long long t = t_first; t <= t_last; ++t) {
-        const int n0 = (int)(max(u0, t * k.na) - t * k.na);
-        const int n1 = (int)(min(u1, (t + 1) * k.na) - t * k.na);
+    for (int t = t_first; t <= t_last; ++t) {
+        const int n0 = (t == t_first) ? n0_first : 0;
+        const int n1 = (t == t_last) ? n1_last : k.na;
         const int col0 = (int)(t % k.tiles_x) * TILE_X;
         const int row0 = (int)(t / k.tiles_x) * TILE_Y;
         const int rowi = row0 + jr;
@@ -1559,10 +1711,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
             __syncthreads();
             const int tw = row_pitch<INTERP>(k);
             const float4* rows = table + (size_t)c0 * tw;
-            if (is_sinc(INTERP)) {
+            if (is_sinc(INTERP) || INTERP == INTERP_NEAREST) {
                 // the sinc modes load their table entries inside the pulse step
                 // (the polynomial's nodes), so nothing is gained by building the
-                // next pulse's state early, and one state leaves registers free
+                // next pulse's state early, and one state leaves registers free;
+                // the nearest kernel too runs faster with one state (3 %, and 4
+                // bytes of spill instead of 12)
 #pragma unroll 1
                 for (int p = 0; p < cnt; ++p) {
                     const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rows + (size_t)p * tw, jf);
@@ -1853,6 +2007,121 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
     return 330;
 }
 
+// Relative cost of one (thread, pulse) of the height-map sinc and nearest
+// kernels by the spread of the thread's row in bins: the row forms (one
+// polynomial per row for sinc, by degree; one table entry per row for
+// nearest) against the per-pixel path and the float64 path, in SM cycles per
+// (row, pulse) times ten, fitted to per-CTA cycle counts on terrain. Sinc
+// costs per warp, since a warp runs each path its rows take once: the
+// highest polynomial degree among them (which the kernel uses for all of
+// them; 8.9, 10.7, 11.5, 13.0 and 16.2 for degrees 2 to 6), 33.5 more when a
+// row takes the per-pixel path, 49 when one takes the float64 path. Nearest:
+// one table entry 2.25 times faster than a gather per pixel, 38 on the
+// float64 path; a nearest row falls in two bins whenever it spreads over at
+// most one bin, and with probability 2 - span up to two bins. Called by all
+// 32 lanes of a warp together.
+template <int INTERP>
+__device__ __forceinline__ float heights_row_cost(float span, bool exact)
+{
+    if (INTERP == INTERP_HEIGHTS_SINC8) {
+        const float sp = fmaxf(span, 2.0f * SINC_HALF_MIN);
+        const int nn = exact ? 0 : (sp <= SINC_SPAN2 ? 1 : sp <= SINC_SPAN3 ? 2 : sp <= SINC_SPAN ? 3 :
+                                    sp <= SINC_SPAN5 ? 4 : sp <= SINC_SPAN6 ? 5 : 0);
+        const int wn = __reduce_max_sync(0xffffffffu, nn);
+        const bool any_pixel = __any_sync(0xffffffffu, !exact && nn == 0);
+        const bool any_exact = __any_sync(0xffffffffu, exact);
+        const float poly = wn == 0 ? 0.0f : wn == 1 ? 89.0f : wn == 2 ? 107.0f : wn == 3 ? 115.0f :
+                           wn == 4 ? 130.0f : 162.0f;
+        return poly + (any_pixel ? 335.0f : 0.0f) + (any_exact ? 490.0f : 0.0f);
+    }
+    if (exact)
+        return 380.0f;
+    const float p2 = fminf(fmaxf(2.0f - span, 0.0f), 1.0f);
+    return p2 * 100.0f + (1.0f - p2) * 225.0f;
+}
+
+// The cells of split_kernel for the height-map sinc and nearest kernels, whose
+// cost follows the terrain: one block per tile, one thread per row. Each row
+// takes the main kernel's statistics of its heights (the range of h - hrow
+// and of P = (i dx)^2 + (h - hrow)^2) and, at the middle pulse of each of the
+// NS pulse segments, the spread of its range in bins from the bound the main
+// kernel uses (s = i 2 v_x dx + dz 2 v_z + P over the row, times 1 / (2 R dr)),
+// or the float64 path where the record builder's or the row's test sends the
+// row there; cum[1 + t NS + i] receives the tile's summed row cost times the
+// segment's pulse count.
+constexpr int COST_SAMPLES = 16;           // pulse segments per block of heights_cost_kernel
+
+template <int INTERP>
+__global__ void __launch_bounds__(THREADS) heights_cost_kernel(BpConst k, const double* __restrict__ pos,
+                                                               const float* __restrict__ heights,
+                                                               unsigned long long* __restrict__ cum)
+{
+    __shared__ float s_sum[COST_SAMPLES][WARPS];
+    const int t = blockIdx.x;
+    const int NS = max(1, min(SPLIT_SAMPLES, SPLIT_CELLS / max(k.tiles, 1)));
+    const int i0 = blockIdx.y * COST_SAMPLES, i1 = min(NS, i0 + COST_SAMPLES);
+    const int col0 = (t % k.tiles_x) * TILE_X;
+    const int row0 = (t / k.tiles_x) * TILE_Y;
+    const int rowi = min(row0 + (int)threadIdx.x, k.ny - 1);
+    const float* hsrc = heights + (size_t)rowi * k.nx;
+    float sum = 0.0f, hmin = 3.0e38f, hmax = -3.0e38f;
+    for (int m = 0; m < TILE_X; ++m) {
+        const float h = fminf(fmaxf(hsrc[min(col0 + m, k.nx - 1)], k.h_lo_f), k.h_hi_f);
+        sum += h;
+        hmin = fminf(hmin, h);
+        hmax = fmaxf(hmax, h);
+    }
+    const float hrow = sum * (1.0f / TILE_X);
+    const float dzm = fmaxf(hmax - hrow, hrow - hmin);
+    const float hx = 0.5f * (TILE_X - 1) * k.dx_f;
+    const float dp = hx * hx + dzm * dzm;              // bound on the spread of P
+    const float qm = 1.0001f * sqrtf(hx * hx + dzm * dzm);
+    const float xc = (float)(k.x0 + ((double)col0 + 0.5 * (TILE_X - 1)) * k.dx);
+    const float yc = (float)(k.y0 + ((double)row0 + 0.5 * (TILE_Y - 1)) * k.dy);
+    const float yr = (float)(k.y0 + (double)(row0 + (int)threadIdx.x) * k.dy);
+    const float zr = (float)k.z0 + hrow;
+    const float q3 = (float)k.qmax3, zm = (float)k.z_mid;
+    for (int i = i0; i < i1; ++i) {
+        const long long n_lo = (long long)i * k.na / NS, n_hi = (long long)(i + 1) * k.na / NS;
+        float cost = 0.0f;
+        if (n_hi > n_lo) {
+            const long long n = (n_lo + n_hi) / 2;
+            const float ax = (float)pos[3 * n], ay = (float)pos[3 * n + 1], az = (float)pos[3 * n + 2];
+            if (isfinite(ax) && isfinite(ay) && isfinite(az)) {
+                // the record's test at the tile centre (mid height) ...
+                const float tx = xc - ax, ty = yc - ay, tz = zm - az;
+                const float rt = sqrtf(fmaf(tx, tx, fmaf(ty, ty, tz * tz)));
+                const float qr = q3 / rt;
+                const bool fast = rt > 8.0f * q3 && qr * qr * qr * qr * q3 * k.inv_dr_f <= (float)k.fast_tol_bins;
+                // ... and the row's
+                const float vx = xc - ax, vy = yr - ay, vz = zr - az;
+                const float r = sqrtf(fmaf(vx, vx, fmaf(vy, vy, vz * vz)));
+                const bool series = qm * (2.0f * r + qm) <= 0.01f * r * r;
+                const float ss = (TILE_X - 1) * fabsf(2.0f * vx * k.dx_f) +
+                                 fabsf(2.0f * vz) * (hmax - hmin) + dp;
+                cost = heights_row_cost<INTERP>(ss * 0.5f * k.inv_dr_f / fmaxf(r, 1.0f),
+                                                !(fast && series));
+            }
+        }
+        // the warp's sum over its rows
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            cost += __shfl_down_sync(0xffffffffu, cost, o);
+        if ((threadIdx.x & 31) == 0)
+            s_sum[i - i0][threadIdx.x >> 5] = cost;
+    }
+    __syncthreads();
+    // the block's sums, one sample per thread
+    const int i = i0 + (int)threadIdx.x;
+    if (i < i1) {
+        float tot = 0.0f;
+        for (int w = 0; w < WARPS; ++w)
+            tot += s_sum[threadIdx.x][w];
+        const long long n_lo = (long long)i * k.na / NS, n_hi = (long long)(i + 1) * k.na / NS;
+        cum[1 + (size_t)t * NS + i] = (unsigned long long)tot * (unsigned long long)(n_hi - n_lo);
+    }
+}
+
 // One block. The units are cut into cells: tile t, pulse segment i of NS
 // (NS = min(SPLIT_SAMPLES, SPLIT_CELLS / tiles), at least 1), so that the cost
 // can follow the antenna along the track; a cell's cost is the unit cost at
@@ -1860,11 +2129,12 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
 // scratch; starts: ctas + 1 unit offsets.
 __global__ void __launch_bounds__(SPLIT_THREADS) split_kernel(BpConst k, const double* __restrict__ pos,
                                                               const int* __restrict__ sinc_wide,
+                                                              bool costed,
                                                               unsigned long long* __restrict__ cum,
                                                               long long* __restrict__ starts)
 {
     __shared__ unsigned long long s_part[SPLIT_THREADS];
-    const bool wide = *sinc_wide != 0;
+    const bool wide = !costed && *sinc_wide != 0;
     const int T = k.tiles;
     const int NS = max(1, min(SPLIT_SAMPLES, SPLIT_CELLS / max(T, 1)));
     const int C = T * NS;
@@ -1877,7 +2147,9 @@ __global__ void __launch_bounds__(SPLIT_THREADS) split_kernel(BpConst k, const d
         const int t = c / NS, i = c % NS;
         const long long n_lo = (long long)i * k.na / NS, n_hi = (long long)(i + 1) * k.na / NS;
         unsigned long long w = 0;
-        if (n_hi > n_lo) {
+        if (costed) {
+            w = cum[c + 1];                        // written by heights_cost_kernel
+        } else if (n_hi > n_lo) {
             const long long n = (n_lo + n_hi) / 2;
             const float xc = (float)(k.x0 + ((double)((t % k.tiles_x) * TILE_X) + 0.5 * (TILE_X - 1)) * k.dx);
             const float yc = (float)(k.y0 + ((double)((t / k.tiles_x) * TILE_Y) + 0.5 * (TILE_Y - 1)) * k.dy);
@@ -1952,7 +2224,23 @@ void sinc_taps_host(float* out)
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s)
 {
-    split_kernel<<<1, SPLIT_THREADS, 0, s>>>(k, pos, sinc_wide, cum, starts);
+    split_kernel<<<1, SPLIT_THREADS, 0, s>>>(k, pos, sinc_wide, false, cum, starts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_heights_split(const BpConst& k, const double* pos, const float* heights,
+                                 unsigned long long* cum, long long* starts, cudaStream_t s)
+{
+    const int ns = std::max(1, std::min(SPLIT_SAMPLES, SPLIT_CELLS / std::max(k.tiles, 1)));
+    const dim3 grid((unsigned)k.tiles, (unsigned)((ns + COST_SAMPLES - 1) / COST_SAMPLES));
+    if (k.flags & FLAG_SINC8)
+        heights_cost_kernel<INTERP_HEIGHTS_SINC8><<<grid, THREADS, 0, s>>>(k, pos, heights, cum);
+    else
+        heights_cost_kernel<INTERP_HEIGHTS_NEAREST><<<grid, THREADS, 0, s>>>(k, pos, heights, cum);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    split_kernel<<<1, SPLIT_THREADS, 0, s>>>(k, pos, nullptr, true, cum, starts);
     return cudaGetLastError();
 }
 

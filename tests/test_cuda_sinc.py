@@ -98,6 +98,37 @@ def test_sinc_ragged_image():
                                                  interp="sinc8"), "sinc ragged")
 
 
+def test_more_tiles_than_split_cells():
+    """3 x 33,554,944 pixels at 0.1 mm: 65,537 tiles of 32 x 512, one more than
+    the cells of the cost-weighted work split, so the call takes the even
+    split (every CTA covers hundreds of whole tiles); sampled pixels and the
+    image's corners against the oracle."""
+    nx, ny = 3, 65537 * 512
+    na, nr = 8, 4096
+    spacing = 1.0e-4
+    rng = np.random.default_rng(65537)
+    pos = scenes.straight_track(na, 0.5)
+    geo = scenes.image_geometry(nx, ny, spacing)
+    near = np.array([0.0, geo["y0"], 0.0])
+    far = np.array([0.0, geo["y0"] + ny * spacing, 0.0])
+    rmin = float(np.min(np.linalg.norm(pos - near, axis=1))) - 20.0
+    p = dict(nx=nx, ny=ny, na=na, nr=nr, r0=rmin, dr=scenes.DR, wavelength=scenes.WAVELENGTH, **geo)
+    assert float(np.max(np.linalg.norm(pos - far, axis=1))) < rmin + (nr - 8) * scenes.DR
+    echo = (rng.standard_normal((na, nr)) + 1j * rng.standard_normal((na, nr))).astype(np.complex64)
+    img = torch.empty((ny, nx), dtype=torch.complex64, device=DEV)
+    with Plan(p, interp="sinc8") as plan:
+        assert plan.describe()["tiles"] == 65537
+        plan.backproject(img, torch.from_numpy(echo).to(DEV), torch.from_numpy(pos).to(DEV),
+                         interp="sinc8")
+        torch.cuda.synchronize()
+    pix = np.unique(np.concatenate([rng.choice(nx * ny, 3000, replace=False),
+                                    [0, nx - 1, nx * ny - nx, nx * ny - 1]])).astype(np.int64)
+    got = img.reshape(-1)[torch.from_numpy(pix).to(DEV)].cpu().numpy()
+    del img
+    ref = oracle.backproject(p, echo, pos, pix, interp="sinc8")
+    parity.assert_parity(got, ref, "65537 tiles, sinc8")
+
+
 def test_sinc_near_field_exact_path():
     na, nx, ny = 48, 64, 130
     pos = np.zeros((na, 3))
