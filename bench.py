@@ -48,7 +48,8 @@ FMA_PER_SM_CLK = 128          # FP32 lanes per SM per clock
 # 2 complex lerps = 4; 8-tap sinc: 8 real weights on complex samples = 16;
 # nearest: none) and the phase multiply-accumulate (4). The height map adds
 # no operation: the pixel's z enters p - a like x and y.
-FMA_OPS_PER_UPDATE = {"linear": 16, "sinc8": 28, "nearest": 12, "heights": 16}
+FMA_OPS_PER_UPDATE = {"linear": 16, "sinc8": 28, "nearest": 12, "heights": 16,
+                      "heights_sinc8": 28, "heights_nearest": 12}
 LARGE_SCENES = ("large_scene", "nonideal_track")
 MUFU_PER_UPDATE = 2           # sin and cos of the phase; the range needs no sqrt here
 PAGE_SFU_PER_UPDATE = 3       # the page's loop: sqrt, sin, cos
@@ -494,26 +495,29 @@ def run_ours(args, scene, rank, world, local, dist):
         heights = torch.from_numpy(hmap).to(dev)
         with Plan(p, height_range=(float(hmap.min()), float(hmap.max()))) as hplan:
             hplan.set_timing(True)
-            for _ in range(3):
-                hplan.backproject_heights(image, echoes, pos, heights)
-            torch.cuda.synchronize(dev)
-            hplan.kernel_times()
-            steps_v = max(3, min(args.steps, 20))
-            total = 0.0
-            for i in range(steps_v):
-                flush.fill_(float(i))
-                starts[0].record(stream)
-                hplan.backproject_heights(image, echoes, pos, heights)
-                ends[0].record(stream)
-                ends[0].synchronize()
-                total += starts[0].elapsed_time(ends[0])
-            main_ms_v, launches_v = hplan.kernel_times()
-        variants["heights"] = {
-            "interp": "linear, pixels on a 40 m terrain height map (sarbp_backproject_heights)",
-            "steps": steps_v, "value": updates * steps_v / (total / 1e3) / 1e9, "unit": UNIT,
-            "ms_per_step": total / steps_v,
-            "main_kernel_gupd": updates / (main_ms_v / max(launches_v, 1) / 1e3) / 1e9,
-        }
+            for hinterp, key in (("linear", "heights"), ("sinc8", "heights_sinc8"),
+                                 ("nearest", "heights_nearest")):
+                for _ in range(3):
+                    hplan.backproject_heights(image, echoes, pos, heights, interp=hinterp)
+                torch.cuda.synchronize(dev)
+                hplan.kernel_times()
+                steps_v = max(3, min(args.steps, 20 if hinterp != "sinc8" else 10))
+                total = 0.0
+                for i in range(steps_v):
+                    flush.fill_(float(i))
+                    starts[0].record(stream)
+                    hplan.backproject_heights(image, echoes, pos, heights, interp=hinterp)
+                    ends[0].record(stream)
+                    ends[0].synchronize()
+                    total += starts[0].elapsed_time(ends[0])
+                main_ms_v, launches_v = hplan.kernel_times()
+                variants[key] = {
+                    "interp": f"{hinterp}, pixels on a 40 m terrain height map "
+                              "(sarbp_backproject_heights)",
+                    "steps": steps_v, "value": updates * steps_v / (total / 1e3) / 1e9, "unit": UNIT,
+                    "ms_per_step": total / steps_v,
+                    "main_kernel_gupd": updates / (main_ms_v / max(launches_v, 1) / 1e3) / 1e9,
+                }
         # range compression of this scene's shape (SARBP-GPU §3.1): raw chirps -> echoes
         from domain_backprojection_sarbp_gb300 import RangeCompressor
         from synth import chirp as chirp_mod

@@ -407,8 +407,10 @@ sarbp_status enqueue_backprojection(sarbp_plan_s* plan, void* image, const void*
         if (e != cudaSuccess)
             return cuda_fail(plan, e, "work-split kernel launch");
         k.starts = starts;
-    } else if (costed && heights && (k.flags & (SARBP_SINC8 | SARBP_NEAREST))) {
-        // so does the height-map sinc and nearest kernels', with the terrain
+    } else if (costed && heights && (k.flags & SARBP_SINC8)) {
+        // so does the height-map sinc kernel's, with the terrain (the nearest
+        // kernel's rows cost the same on smooth terrain, where they all fall
+        // in two bins, and it keeps the equal split)
         auto* cum = reinterpret_cast<unsigned long long*>(plan->psi + plan->p.nr + 2);
         auto* starts = reinterpret_cast<long long*>(cum + SPLIT_CELLS + 1);
         e = launch_heights_split(k, antenna_pos, heights, cum, starts, s);

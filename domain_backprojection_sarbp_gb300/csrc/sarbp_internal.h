@@ -94,9 +94,8 @@ cudaError_t prepare_kernels();
 constexpr int SPLIT_CELLS = 65536;         // (tile, pulse segment) cells of the cost estimate
 cudaError_t launch_split(const BpConst& k, const double* pos, const int* sinc_wide,
                          unsigned long long* cum, long long* starts, cudaStream_t s);
-// The same for the height-map sinc and nearest kernels (k.flags says which),
-// whose cost follows the terrain: per-tile costs from the rows' height
-// statistics, then the split.
+// The same for the height-map sinc kernel, whose cost follows the terrain:
+// per-tile costs from the rows' height statistics, then the split.
 cudaError_t launch_heights_split(const BpConst& k, const double* pos, const float* heights,
                                  unsigned long long* cum, long long* starts, cudaStream_t s);
 // Range compression fused with the linear echo table (sarbp_rc.cu): for every

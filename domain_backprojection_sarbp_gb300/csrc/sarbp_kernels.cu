@@ -2007,51 +2007,38 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
     return 330;
 }
 
-// Relative cost of one (thread, pulse) of the height-map sinc and nearest
-// kernels by the spread of the thread's row in bins: the row forms (one
-// polynomial per row for sinc, by degree; one table entry per row for
-// nearest) against the per-pixel path and the float64 path, in SM cycles per
-// (row, pulse) times ten, fitted to per-CTA cycle counts on terrain. Sinc
-// costs per warp, since a warp runs each path its rows take once: the
-// highest polynomial degree among them (which the kernel uses for all of
-// them; 8.9, 10.7, 11.5, 13.0 and 16.2 for degrees 2 to 6), 33.5 more when a
-// row takes the per-pixel path, 49 when one takes the float64 path. Nearest:
-// one table entry 2.25 times faster than a gather per pixel, 38 on the
-// float64 path; a nearest row falls in two bins whenever it spreads over at
-// most one bin, and with probability 2 - span up to two bins. Called by all
-// 32 lanes of a warp together.
-template <int INTERP>
-__device__ __forceinline__ float heights_row_cost(float span, bool exact)
+// Relative cost of one (thread, pulse) of the height-map sinc kernel by the
+// spread of the thread's row in bins, in SM cycles per (row, pulse) times ten,
+// fitted to per-CTA cycle counts on terrain. The cost is the warp's, since a
+// warp runs each path its rows take once: the highest polynomial degree among
+// them (which the kernel uses for all of them; 8.9, 10.7, 11.5, 13.0 and 16.2
+// for degrees 2 to 6), 33.5 more when a row takes the per-pixel path, 49 when
+// one takes the float64 path. Called by all 32 lanes of a warp together.
+__device__ __forceinline__ float heights_sinc_row_cost(float span, bool exact)
 {
-    if (INTERP == INTERP_HEIGHTS_SINC8) {
-        const float sp = fmaxf(span, 2.0f * SINC_HALF_MIN);
-        const int nn = exact ? 0 : (sp <= SINC_SPAN2 ? 1 : sp <= SINC_SPAN3 ? 2 : sp <= SINC_SPAN ? 3 :
-                                    sp <= SINC_SPAN5 ? 4 : sp <= SINC_SPAN6 ? 5 : 0);
-        const int wn = __reduce_max_sync(0xffffffffu, nn);
-        const bool any_pixel = __any_sync(0xffffffffu, !exact && nn == 0);
-        const bool any_exact = __any_sync(0xffffffffu, exact);
-        const float poly = wn == 0 ? 0.0f : wn == 1 ? 89.0f : wn == 2 ? 107.0f : wn == 3 ? 115.0f :
-                           wn == 4 ? 130.0f : 162.0f;
-        return poly + (any_pixel ? 335.0f : 0.0f) + (any_exact ? 490.0f : 0.0f);
-    }
-    if (exact)
-        return 380.0f;
-    const float p2 = fminf(fmaxf(2.0f - span, 0.0f), 1.0f);
-    return p2 * 100.0f + (1.0f - p2) * 225.0f;
+    const float sp = fmaxf(span, 2.0f * SINC_HALF_MIN);
+    const int nn = exact ? 0 : (sp <= SINC_SPAN2 ? 1 : sp <= SINC_SPAN3 ? 2 : sp <= SINC_SPAN ? 3 :
+                                sp <= SINC_SPAN5 ? 4 : sp <= SINC_SPAN6 ? 5 : 0);
+    const int wn = __reduce_max_sync(0xffffffffu, nn);
+    const bool any_pixel = __any_sync(0xffffffffu, !exact && nn == 0);
+    const bool any_exact = __any_sync(0xffffffffu, exact);
+    const float poly = wn == 0 ? 0.0f : wn == 1 ? 89.0f : wn == 2 ? 107.0f : wn == 3 ? 115.0f :
+                       wn == 4 ? 130.0f : 162.0f;
+    return poly + (any_pixel ? 335.0f : 0.0f) + (any_exact ? 490.0f : 0.0f);
 }
 
-// The cells of split_kernel for the height-map sinc and nearest kernels, whose
-// cost follows the terrain: one block per tile, one thread per row. Each row
-// takes the main kernel's statistics of its heights (the range of h - hrow
-// and of P = (i dx)^2 + (h - hrow)^2) and, at the middle pulse of each of the
-// NS pulse segments, the spread of its range in bins from the bound the main
+// The cells of split_kernel for the height-map sinc kernel, whose cost follows
+// the terrain: one block per tile and up to COST_SAMPLES pulse segments, one
+// thread per row. Each row takes the main kernel's statistics of its heights
+// (the range of h - hrow and of P = (i dx)^2 + (h - hrow)^2) and, at the
+// middle pulse of each of the NS pulse segments, the spread of its range in
+// bins from the bound the main
 // kernel uses (s = i 2 v_x dx + dz 2 v_z + P over the row, times 1 / (2 R dr)),
 // or the float64 path where the record builder's or the row's test sends the
 // row there; cum[1 + t NS + i] receives the tile's summed row cost times the
 // segment's pulse count.
 constexpr int COST_SAMPLES = 16;           // pulse segments per block of heights_cost_kernel
 
-template <int INTERP>
 __global__ void __launch_bounds__(THREADS) heights_cost_kernel(BpConst k, const double* __restrict__ pos,
                                                                const float* __restrict__ heights,
                                                                unsigned long long* __restrict__ cum)
@@ -2099,8 +2086,8 @@ __global__ void __launch_bounds__(THREADS) heights_cost_kernel(BpConst k, const 
                 const bool series = qm * (2.0f * r + qm) <= 0.01f * r * r;
                 const float ss = (TILE_X - 1) * fabsf(2.0f * vx * k.dx_f) +
                                  fabsf(2.0f * vz) * (hmax - hmin) + dp;
-                cost = heights_row_cost<INTERP>(ss * 0.5f * k.inv_dr_f / fmaxf(r, 1.0f),
-                                                !(fast && series));
+                cost = heights_sinc_row_cost(ss * 0.5f * k.inv_dr_f / fmaxf(r, 1.0f),
+                                             !(fast && series));
             }
         }
         // the warp's sum over its rows
@@ -2233,10 +2220,7 @@ cudaError_t launch_heights_split(const BpConst& k, const double* pos, const floa
 {
     const int ns = std::max(1, std::min(SPLIT_SAMPLES, SPLIT_CELLS / std::max(k.tiles, 1)));
     const dim3 grid((unsigned)k.tiles, (unsigned)((ns + COST_SAMPLES - 1) / COST_SAMPLES));
-    if (k.flags & FLAG_SINC8)
-        heights_cost_kernel<INTERP_HEIGHTS_SINC8><<<grid, THREADS, 0, s>>>(k, pos, heights, cum);
-    else
-        heights_cost_kernel<INTERP_HEIGHTS_NEAREST><<<grid, THREADS, 0, s>>>(k, pos, heights, cum);
+    heights_cost_kernel<<<grid, THREADS, 0, s>>>(k, pos, heights, cum);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
