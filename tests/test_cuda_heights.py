@@ -36,7 +36,8 @@ def _dev(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=dtype)).to(DEV)
 
 
-def heights_image(params, echoes, pos, heights, h_range, init=None, accumulate=False, plan=None):
+def heights_image(params, echoes, pos, heights, h_range, init=None, accumulate=False, plan=None,
+                  interp="linear"):
     img = torch.full((params["ny"], params["nx"]), complex(7.0, -3.0), dtype=torch.complex64,
                      device=DEV)
     if init is not None:
@@ -45,7 +46,8 @@ def heights_image(params, echoes, pos, heights, h_range, init=None, accumulate=F
     plan = plan or Plan(params, height_range=h_range)
     try:
         plan.backproject_heights(img, _dev(echoes, np.complex64), _dev(pos, np.float64),
-                                 _dev(heights, np.float32), params=params, accumulate=accumulate)
+                                 _dev(heights, np.float32), params=params, accumulate=accumulate,
+                                 interp=interp)
         torch.cuda.synchronize()
     finally:
         if own:
@@ -239,7 +241,11 @@ def test_heights_are_clamped_to_the_plan_range():
     parity.assert_parity(a, ref, "clamped heights")
 
 
-def test_accumulate_and_determinism():
+@pytest.mark.parametrize("interp", ["linear", "sinc8", "nearest"])
+def test_accumulate_and_determinism(interp):
+    """Repeated calls give the same bits (for sinc with the terrain cost split,
+    which is computed in integers and so the same on every run), and
+    accumulation adds the image to what the buffer held."""
     cfg = scenes.shrink(scenes.CONFIGS[1], na=256, nx=70, ny=530, n_targets=3)
     sc, h = terrain_scene(cfg, 20.0)
     rng = np.random.default_rng(3)
@@ -247,10 +253,10 @@ def test_accumulate_and_determinism():
     init = init.astype(np.complex64)
     rng_h = (float(h.min()), float(h.max()))
     with Plan(sc.params, height_range=rng_h) as plan:
-        one = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan)
-        two = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan)
+        one = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan, interp=interp)
+        two = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, plan=plan, interp=interp)
         acc = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, None, init=init,
-                            accumulate=True, plan=plan)
+                            accumulate=True, plan=plan, interp=interp)
     assert np.array_equal(one, two)
     scale = np.abs(one).max()
     assert np.abs(acc - (init + one)).max() <= 1e-5 * scale
@@ -258,15 +264,20 @@ def test_accumulate_and_determinism():
 
 # ------------------------------------------- full size, sampled pixels
 @pytest.mark.slow
-def test_page_spotlight_on_terrain_sampled():
+@pytest.mark.parametrize("interp", ["linear", "sinc8"])
+def test_page_spotlight_on_terrain_sampled(interp):
     """4096 pulses onto 1024 x 1024 pixels on 40 m of relief, in the launch
-    configuration the planar benchmark uses; compared on sampled pixels."""
+    configuration the bench uses (for sinc: polynomial rows of degree 2 to 6,
+    per-pixel rows in the steep tiles, the terrain cost split); compared on
+    sampled pixels."""
     cfg = scenes.CONFIGS[2]
     sc, h = terrain_scene(cfg, 40.0)
-    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (float(h.min()), float(h.max())))
+    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (float(h.min()), float(h.max())),
+                        interp=interp)
     pix = scenes.compared_pixels(sc)
-    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h, pixels=pix)
-    print(parity.assert_parity(got.reshape(-1)[pix], ref, "page_spotlight on terrain"))
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h, pixels=pix,
+                                     interp=interp)
+    print(parity.assert_parity(got.reshape(-1)[pix], ref, f"page_spotlight on terrain, {interp}"))
     full = np.zeros(cfg.nx * cfg.ny, dtype=np.complex128)
     full[pix] = ref
     assert not parity.argmax_mismatches(got, full.reshape(cfg.ny, cfg.nx), sc.targets)
