@@ -1426,10 +1426,11 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
             // the row within SINC_SPAN6 bins, the stencils of its two bins
             // recorded and both bins inside the row: one polynomial in u, of
             // degree 2 to 6 by the span (the planar kernels' degrees and
-            // spans). The warp's polynomial rows take the highest degree any
-            // of them needs (on a narrower interval a higher degree is as
-            // accurate), so that a warp runs one polynomial path, not one per
-            // degree.
+            // spans). The warp takes one path: the polynomial when all its
+            // rows here can, at the highest degree any of them needs (on a
+            // narrower interval a higher degree is as accurate), else the
+            // per-pixel taps for all of them (a warp that ran both paths cost
+            // several times either).
             float lo_e, hi_e, k0e;
             int kabs0;
             const bool poly = poly_interval(k, kbase, bin0, lo_u, hi_u, SINC_SPAN6, lo_e, hi_e, k0e, kabs0) &&
@@ -1437,8 +1438,9 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
             const float sp = hi_e - lo_e;
             const int nn = !poly ? 0 : (sp <= SINC_SPAN2 ? 3 : sp <= SINC_SPAN3 ? 4 : sp <= SINC_SPAN ? 5 :
                                        sp <= SINC_SPAN5 ? 6 : 7);
-            const int wn = __reduce_max_sync(__activemask(), nn);
-            if (poly) {
+            const unsigned lanes = __activemask();
+            const int wn = __reduce_max_sync(lanes, nn);
+            if (__all_sync(lanes, poly)) {
                 const float a4 = deg4 ? -0.078125f * hb * g * g * g : 0.0f;
                 if (wn <= 3)
                     heights_sinc_poly<3>(k, s_hp, row, kbase, lo_e, hi_e, k0e, kabs0, frac, ax, tvz,
@@ -2009,11 +2011,14 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
 
 // Relative cost of one (thread, pulse) of the height-map sinc kernel by the
 // spread of the thread's row in bins, in SM cycles per (row, pulse) times ten,
-// fitted to per-CTA cycle counts on terrain. The cost is the warp's, since a
-// warp runs each path its rows take once: the highest polynomial degree among
-// them (which the kernel uses for all of them; 8.9, 10.7, 11.5, 13.0 and 16.2
-// for degrees 2 to 6), 33.5 more when a row takes the per-pixel path, 49 when
-// one takes the float64 path. Called by all 32 lanes of a warp together.
+// fitted to per-CTA cycle counts on terrain. The cost is the warp's, since the
+// warp takes one path for all its rows: the polynomial at the highest degree
+// among them (8.9, 10.6, 11.5, 13.2 and 14.8 for degrees 2 to 6) when every
+// row allows one, else the per-pixel taps: 24.7 when no row allows a
+// polynomial, 123 when some do (measured so; such warps, 1.3 % of them on a
+// 40 m terrain, sit where the terrain steepens across the tile), and 49 more
+// when a row takes the float64 path.
+// Called by all 32 lanes of a warp together.
 __device__ __forceinline__ float heights_sinc_row_cost(float span, bool exact)
 {
     const float sp = fmaxf(span, 2.0f * SINC_HALF_MIN);
@@ -2022,9 +2027,9 @@ __device__ __forceinline__ float heights_sinc_row_cost(float span, bool exact)
     const int wn = __reduce_max_sync(0xffffffffu, nn);
     const bool any_pixel = __any_sync(0xffffffffu, !exact && nn == 0);
     const bool any_exact = __any_sync(0xffffffffu, exact);
-    const float poly = wn == 0 ? 0.0f : wn == 1 ? 89.0f : wn == 2 ? 107.0f : wn == 3 ? 115.0f :
-                       wn == 4 ? 130.0f : 162.0f;
-    return poly + (any_pixel ? 335.0f : 0.0f) + (any_exact ? 490.0f : 0.0f);
+    const float poly = wn == 0 ? 0.0f : wn == 1 ? 89.0f : wn == 2 ? 106.0f : wn == 3 ? 115.0f :
+                       wn == 4 ? 132.0f : 148.0f;
+    return (any_pixel ? (wn > 0 ? 1230.0f : 247.0f) : poly) + (any_exact ? 490.0f : 0.0f);
 }
 
 // The cells of split_kernel for the height-map sinc kernel, whose cost follows
