@@ -1243,7 +1243,7 @@ __device__ __forceinline__ void heights_hinge_loop(const BpConst& k, const float
     }
 }
 
-// Windowed sinc on a height map when the row's pixels span at most SINC_SPAN
+// Windowed sinc on a height map when the row's pixels span at most SINC_SPAN6
 // bins: G is interpolated over [lo, hi] (row units, relative to kb) at NN
 // Chebyshev nodes as in the planar polynomial modes (same degrees, spans and
 // error bounds), and each pixel evaluates it at s_v = u - mid from the range
@@ -1429,8 +1429,8 @@ __device__ __forceinline__ bool heights_series_pulse(const BpConst& k, const Rec
             // spans). The warp takes one path: the polynomial when all its
             // rows here can, at the highest degree any of them needs (on a
             // narrower interval a higher degree is as accurate), else the
-            // per-pixel taps for all of them (a warp that ran both paths cost
-            // several times either).
+            // per-pixel taps for all of them, so that it never runs two paths
+            // one after the other.
             float lo_e, hi_e, k0e;
             int kabs0;
             const bool poly = poly_interval(k, kbase, bin0, lo_u, hi_u, SINC_SPAN6, lo_e, hi_e, k0e, kabs0) &&
@@ -2015,9 +2015,10 @@ __device__ __forceinline__ unsigned sinc_unit_cost(float span, bool wide)
 // warp takes one path for all its rows: the polynomial at the highest degree
 // among them (8.9, 10.6, 11.5, 13.2 and 14.8 for degrees 2 to 6) when every
 // row allows one, else the per-pixel taps: 24.7 when no row allows a
-// polynomial, 123 when some do (measured so; such warps, 1.3 % of them on a
-// 40 m terrain, sit where the terrain steepens across the tile), and 49 more
-// when a row takes the float64 path.
+// polynomial, 123 when some do, and 49 more when a row takes the float64
+// path. The last class is the fit's proxy for the tiles where the terrain
+// steepens (1.3 % of the warps on a 40 m terrain): timed per warp, their
+// per-pixel path costs what other warps' does.
 // Called by all 32 lanes of a warp together.
 __device__ __forceinline__ float heights_sinc_row_cost(float span, bool exact)
 {
@@ -2117,7 +2118,9 @@ __global__ void __launch_bounds__(THREADS) heights_cost_kernel(BpConst k, const 
 // One block. The units are cut into cells: tile t, pulse segment i of NS
 // (NS = min(SPLIT_SAMPLES, SPLIT_CELLS / tiles), at least 1), so that the cost
 // can follow the antenna along the track; a cell's cost is the unit cost at
-// its middle pulse times its pulse count. cum: SPLIT_CELLS + 1 words of
+// its middle pulse times its pulse count. With `costed` the cells' costs are
+// already in cum[1 ..] (heights_cost_kernel, whole numbers summed exactly in
+// float32) and only the scan and the cuts run. cum: SPLIT_CELLS + 1 words of
 // scratch; starts: ctas + 1 unit offsets.
 __global__ void __launch_bounds__(SPLIT_THREADS) split_kernel(BpConst k, const double* __restrict__ pos,
                                                               const int* __restrict__ sinc_wide,
