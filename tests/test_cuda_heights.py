@@ -112,6 +112,31 @@ def test_terrain_two_entry_and_gathered_rows(relief):
     assert not parity.argmax_mismatches(got, ref, sc.targets)
 
 
+def assert_nearest_parity(got, ref, p, e, pos, h, label):
+    """Nearest sample on a height map: where a pulse's range lies within KNIFE
+    bins of a half bin, the float32 and float64 paths may take different
+    samples and both are valid; such pixels are held to the sum of
+    |e_k - e_k+1| over those pulses, the rest to the usual tolerances."""
+    err = np.abs(got - ref).reshape(-1)
+    tol = parity.MAX_ERR * np.abs(ref).max()
+    explained = []
+    for pix in np.nonzero(err > tol)[0]:
+        ix, iy = pix % p["nx"], pix // p["nx"]
+        pt = np.array([p["x0"] + ix * p["dx"], p["y0"] + iy * p["dy"], p["z0"] + float(h[iy, ix])])
+        u = (np.linalg.norm(pos - pt[None, :], axis=1) - p["r0"]) / p["dr"]
+        kk = np.floor(u).astype(np.int64)
+        knife = (np.abs(u - kk - 0.5) < KNIFE) & (kk >= -1) & (kk <= p["nr"] - 1)
+        gap = sum(abs(complex(e[n, kk[n]] if kk[n] >= 0 else 0) -
+                      complex(e[n, kk[n] + 1] if kk[n] + 1 <= p["nr"] - 1 else 0))
+                  for n in np.nonzero(knife)[0])
+        assert err[pix] <= gap + tol, (int(pix), err[pix], gap)
+        explained.append(pix)
+    keep = np.setdiff1d(np.arange(err.size), np.array(explained, dtype=np.int64))
+    m = parity.compare(got.reshape(-1)[keep], ref.reshape(-1)[keep])
+    print(label, m, len(explained), "knife-edge pixels")
+    assert m["rel_l2"] <= parity.REL_L2 and m["max_err"] <= parity.MAX_ERR, m
+
+
 # the widest spread of u over a row that the sinc kernel serves with one
 # polynomial (degree 6 on seven nodes); below one bin, the two-sample nearest rows
 SINC_SPAN6 = 0.80
@@ -145,28 +170,7 @@ def test_terrain_with_other_interpolations(interp, relief):
         print(interp, parity.assert_parity(got, ref, f"terrain {relief} m, sinc8"))
         assert not parity.argmax_mismatches(got, ref, sc.targets)
         return
-    # nearest: where a pulse's range lies within KNIFE bins of a half bin, the
-    # float32 and float64 paths may take different samples and both are valid;
-    # such pixels are held to the sum of |e_k - e_k+1| over those pulses
-    p, e, pos = sc.params, sc.echoes, sc.antenna_pos
-    err = np.abs(got - ref).reshape(-1)
-    tol = parity.MAX_ERR * np.abs(ref).max()
-    explained = []
-    for pix in np.nonzero(err > tol)[0]:
-        ix, iy = pix % p["nx"], pix // p["nx"]
-        pt = np.array([p["x0"] + ix * p["dx"], p["y0"] + iy * p["dy"], p["z0"] + float(h[iy, ix])])
-        u = (np.linalg.norm(pos - pt[None, :], axis=1) - p["r0"]) / p["dr"]
-        kk = np.floor(u).astype(np.int64)
-        knife = (np.abs(u - kk - 0.5) < KNIFE) & (kk >= -1) & (kk <= p["nr"] - 1)
-        gap = sum(abs(complex(e[n, kk[n]] if kk[n] >= 0 else 0) -
-                      complex(e[n, kk[n] + 1] if kk[n] + 1 <= p["nr"] - 1 else 0))
-                  for n in np.nonzero(knife)[0])
-        assert err[pix] <= gap + tol, (int(pix), err[pix], gap)
-        explained.append(pix)
-    keep = np.setdiff1d(np.arange(err.size), np.array(explained, dtype=np.int64))
-    m = parity.compare(got.reshape(-1)[keep], ref.reshape(-1)[keep])
-    print(interp, m, len(explained), "knife-edge pixels")
-    assert m["rel_l2"] <= parity.REL_L2 and m["max_err"] <= parity.MAX_ERR, m
+    assert_nearest_parity(got, ref, sc.params, sc.echoes, sc.antenna_pos, h, interp)
 
 
 def test_focusing_pin_on_the_gpu():
@@ -189,21 +193,28 @@ def test_constant_height_is_the_raised_plane():
     parity.assert_parity(got, ref, "constant height")
 
 
-def test_wide_height_range():
+@pytest.mark.parametrize("interp", ["linear", "sinc8", "nearest"])
+def test_wide_height_range(interp):
     """A 500 m height range widens every table row; pixels at both extremes
-    still receive every pulse's echo."""
+    still receive every pulse's echo. (The tile reach this range gives sends
+    the records to the float64 path; for sinc the terrain cost split prices
+    them so.)"""
     cfg = scenes.shrink(scenes.CONFIGS[1], na=256, nx=96, ny=96, n_targets=4)
     base = scenes.terrain(cfg.nx, cfg.ny, cfg.spacing, cfg.seed + 5, relief=4.0, mean=0.0)
     h = base.copy()
     h[:48] += -100.0
     h[48:] += 400.0
     sc = scenes.make_scene(cfg, heights=h)
-    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (-110.0, 410.0))
-    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h)
-    print(parity.assert_parity(got, ref, "wide height range"))
+    got = heights_image(sc.params, sc.echoes, sc.antenna_pos, h, (-110.0, 410.0), interp=interp)
+    ref = oracle.backproject_heights(sc.params, sc.echoes, sc.antenna_pos, h, interp=interp)
+    if interp == "nearest":
+        assert_nearest_parity(got, ref, sc.params, sc.echoes, sc.antenna_pos, h, "wide height range")
+    else:
+        print(parity.assert_parity(got, ref, f"wide height range, {interp}"))
 
 
-def test_near_field_uses_the_exact_rows():
+@pytest.mark.parametrize("interp", ["linear", "sinc8", "nearest"])
+def test_near_field_uses_the_exact_rows(interp):
     """Antenna 40-60 m from the pixels: the range series does not apply
     (|t| > 0.01) and every row takes the float64 reference with an exact
     float32 difference per pixel."""
@@ -216,9 +227,12 @@ def test_near_field_uses_the_exact_rows():
     p = dict(nx=nx, ny=ny, na=na, nr=512, r0=10.0, dr=0.25, wavelength=scenes.WAVELENGTH, **geo)
     echo = (np.random.default_rng(8).standard_normal((na, 512)) * (1 + 1j)).astype(np.complex64)
     h = scenes.terrain(nx, ny, 0.1, 99, relief=3.0, mean=1.0)
-    got = heights_image(p, echo, pos, h, (float(h.min()), float(h.max())))
-    ref = oracle.backproject_heights(p, echo, pos, h)
-    print(parity.assert_parity(got, ref, "near field on terrain"))
+    got = heights_image(p, echo, pos, h, (float(h.min()), float(h.max())), interp=interp)
+    ref = oracle.backproject_heights(p, echo, pos, h, interp=interp)
+    if interp == "nearest":
+        assert_nearest_parity(got, ref, p, echo, pos, h, "near field on terrain")
+    else:
+        print(parity.assert_parity(got, ref, f"near field on terrain, {interp}"))
 
 
 def test_heights_are_clamped_to_the_plan_range():
