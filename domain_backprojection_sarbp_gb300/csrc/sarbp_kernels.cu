@@ -1751,12 +1751,27 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 // next pulse's state early, and one state leaves registers free;
                 // the nearest kernel too runs faster with one state (3 %, and 4
                 // bytes of spill instead of 12)
+                // (the wide kernel forms the row pointer from the table per
+                // pulse, and the nearest kernel unrolls this loop by two: their
+                // register allocations then spill nothing)
+                if constexpr (INTERP == INTERP_NEAREST) {
+#pragma unroll 2
+                    for (int p = 0; p < cnt; ++p) {
+                        const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rows + (size_t)p * tw, jf);
+                        apply_pulse<INTERP>(k, st, s_rec[p], rows + (size_t)p * tw,
+                                            pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
+                                            s_hp + jr * HROW4, psi, accre, accim);
+                    }
+                } else {
 #pragma unroll 1
-                for (int p = 0; p < cnt; ++p) {
-                    const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rows + (size_t)p * tw, jf);
-                    apply_pulse<INTERP>(k, st, s_rec[p], rows + (size_t)p * tw,
-                                        pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
-                                        s_hp + jr * HROW4, psi, accre, accim);
+                    for (int p = 0; p < cnt; ++p) {
+                        const float4* rowp = INTERP == INTERP_SINC8_WIDE ? table + (size_t)(c0 + p) * tw
+                                                                         : rows + (size_t)p * tw;
+                        const PulseState st = pulse_setup<INTERP>(k, s_rec[p], rowp, jf);
+                        apply_pulse<INTERP>(k, st, s_rec[p], rowp,
+                                            pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
+                                            s_hp + jr * HROW4, psi, accre, accim);
+                    }
                 }
                 continue;
             }
@@ -1768,8 +1783,12 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 const int p1 = min(p + 1, cnt - 1);
                 const PulseState sb =
                     pulse_setup<INTERP>(k, s_rec[p1], rows + (size_t)p1 * tw, jf);
-                apply_pulse<INTERP>(k, sa, s_rec[p], rows + (size_t)p * tw,
-                                  pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
+                // (the height-map nearest kernel forms this row pointer from the
+                // table per pulse: its register allocation then spills nothing)
+                apply_pulse<INTERP>(k, sa, s_rec[p],
+                                    INTERP == INTERP_HEIGHTS_NEAREST ? table + (size_t)(c0 + p) * tw
+                                                                     : rows + (size_t)p * tw,
+                                    pos + 3 * (size_t)(c0 + p), col0, rowi, hr,
                                   s_hp + jr * HROW4, psi, accre, accim);
                 if (p + 1 >= cnt)
                     break;
