@@ -1749,8 +1749,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS) bp_kernel(BpConst k, cons
                 // the sinc modes load their table entries inside the pulse step
                 // (the polynomial's nodes), so nothing is gained by building the
                 // next pulse's state early, and one state leaves registers free;
-                // the nearest kernel too runs faster with one state (3 %, and 4
-                // bytes of spill instead of 12)
+                // the nearest kernel too runs faster with one state (3 %)
                 // (the wide kernel forms the row pointer from the table per
                 // pulse, and the nearest kernel unrolls this loop by two: their
                 // register allocations then spill nothing)
@@ -2089,11 +2088,10 @@ __device__ __forceinline__ float heights_sinc_row_cost(float span, bool exact)
 // thread per row. Each row takes the main kernel's statistics of its heights
 // (the range of h - hrow and of P = (i dx)^2 + (h - hrow)^2) and, at the
 // middle pulse of each of the NS pulse segments, the spread of its range in
-// bins from the bound the main
-// kernel uses (s = i 2 v_x dx + dz 2 v_z + P over the row, times 1 / (2 R dr)),
-// or the float64 path where the record builder's or the row's test sends the
-// row there; cum[1 + t NS + i] receives the tile's summed row cost times the
-// segment's pulse count.
+// bins from the bound the main kernel uses (s = i 2 v_x dx + dz 2 v_z + P over
+// the row, times 1 / (2 R dr)), or the float64 path where the record builder's
+// or the row's test sends the row there; cum[1 + t NS + i] receives the
+// tile's summed row cost times the segment's pulse count.
 constexpr int COST_SAMPLES = 16;           // pulse segments per block of heights_cost_kernel
 
 __global__ void __launch_bounds__(THREADS) heights_cost_kernel(BpConst k, const double* __restrict__ pos,
