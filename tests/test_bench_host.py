@@ -65,6 +65,21 @@ def test_clock_summary_window():
     assert s.summary(30.0, 31.0)["window"].startswith("whole run")
 
 
+def test_clock_sampler_waits_for_its_first_sample():
+    import threading
+    import time
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc, s.samples = object(), []
+    threading.Timer(0.1, lambda: s.samples.append((0.0, 2070.0, 2070.0, []))).start()
+    t = time.time()
+    s.wait_first(timeout=5.0)
+    assert s.samples and time.time() - t < 2.0
+    s.samples = []
+    t = time.time()
+    s.wait_first(timeout=0.2)                  # none arrive: bounded
+    assert not s.samples and 0.15 < time.time() - t < 2.0
+
+
 def test_reference_arm_json(capsys):
     rc = bench.main(["--impl", "reference", "--config", "tiny_stripmap", "--steps", "2",
                      "--warmup", "3", "--ref-step-seconds", "0.05"])
